@@ -1,0 +1,405 @@
+"""Benchmark of the Gated DeltaNet hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload of the headline line: chunkwise prefill of 4 sequences x 8192
+tokens, 6 heads of dimension 256, bf16 q/k/v/out, fp32 alpha/beta/state,
+S0 ~ N(0, 0.02^2) (the 8K training length).  One step = one gdn_prefill call
+over that batch, inputs resident in HBM.  `value` is prefill throughput in
+Mtok/s per layer (a token = all 6 heads of one layer) over all ranks.
+The metric also names decode state GB/s: the same line carries, under
+"decode", 1000 consecutive gdn_decode_step calls over 256 sequences (fp32
+256x256 states per head updated in place) with their own roofline.
+
+Multi-GPU: replicas only (the path has no exchange step); each rank runs the
+same workload on its own GPU, timed between barriers, max time over ranks.
+
+--impl reference times the fp64 CPU oracle (the parity reference) on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill Mtok/s/layer and decode state GB/s; % of GB300 roofline"
+C = 64
+DK = DV = 256
+H = 6
+
+
+def prefill_flops(lengths, H=H, dk=DK, dv=DV):
+    """Counted chunked-form FLOPs at C = 64: per (chunk, head)
+    C^2 (6 dk + 4 dv) + 6 C dk dv + C^3 / 3 (full C x C products; elementwise
+    work not counted).  Partial chunks are counted as full chunks."""
+    f_chunk = C * C * (6 * dk + 4 * dv) + 6 * C * dk * dv + C ** 3 / 3
+    chunks = sum((L + C - 1) // C for L in lengths)
+    return f_chunk * chunks * H
+
+
+def prefill_bytes(lengths, io_bytes=2, H=H, s0=True, s_final=True):
+    """Algorithmic bytes: q, k, v in, out written (io dtype), alpha and beta
+    (fp32) per token-head, plus S0 read and S_final written per sequence."""
+    tok = sum(lengths)
+    per_tok = H * ((2 * DK + 2 * DV) * io_bytes + 8)
+    state = len(lengths) * H * DV * DK * 4
+    return tok * per_tok + state * (int(s0) + int(s_final))
+
+
+def decode_bytes(N, io_bytes=2):
+    """Per step: the fp32 state read and written once, q, k, v, out and
+    alpha, beta once."""
+    return N * H * (2 * DV * DK * 4 + (2 * DK + 2 * DV) * io_bytes + 8)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sus=d.get("bf16_tflops_sustained", d["bf16_tflops"]), src="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def source_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, or
+    None when the kernel's sources changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d:
+        return None
+    if source_sha(d["sources"]) != d["source_sha"]:
+        return None
+    return d["dram_bytes_per_launch"]
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.text = self.proc.communicate(timeout=5)[0]
+            except Exception:
+                self.proc.kill()
+                self.text = ""
+        else:
+            self.text = ""
+
+    def summary(self):
+        rows = [r.split(",") for r in self.text.strip().splitlines() if r.count(",") >= 8]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ ours
+def run_ours(args, rank, world, local_rank, dist):
+    import torch
+
+    import gdn_inputs
+    import hybrid_linear_attention_deltanet_gb300 as gdn
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    gdn.load()
+    stream = torch.cuda.current_stream(dev)
+    peaks = load_peaks()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    case = gdn_inputs.prefill_8k()
+    x = gdn_inputs.make_prefill(case, device=dev)
+    out = torch.empty_like(x["v"])
+    S_final = torch.empty_like(x["S0"])
+
+    def step():
+        gdn.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"], out=out,
+                    S_final=S_final)
+
+    for _ in range(args.warmup):
+        step()
+    assert gdn.device_status() == 0
+    torch.cuda.synchronize(dev)
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index)
+    barrier()
+    with sampler:
+        torch.cuda.synchronize(dev)
+        n0 = gdn.kernel_launches()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        n1 = gdn.kernel_launches()
+    barrier()
+    assert gdn.device_status() == 0
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(ms_local)
+    tokens = case.total_tokens
+    value = tokens * world / (ms * 1e-3) / 1e6
+    flops = prefill_flops(case.lengths)
+    achieved_tf = flops / (ms_local * 1e-3) / 1e12
+    path = gdn.prefill_path(case.io_dtype)
+
+    # ---- end to end: pinned host buffers, H2D of the inputs and D2H of the
+    # outputs inside the timed region, through the same public call
+    names = ("q", "k", "v", "alpha", "beta", "S0")
+    host = {n: x[n].cpu().pin_memory() for n in names}
+    dbuf = {n: torch.empty_like(x[n]) for n in names}
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_sf = torch.empty(S_final.shape, dtype=S_final.dtype).pin_memory()
+
+    def e2e_step():
+        for n in names:
+            dbuf[n].copy_(host[n], non_blocking=True)
+        gdn.prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["alpha"], dbuf["beta"], dbuf["S0"],
+                    out=out, S_final=S_final)
+        h_out.copy_(out, non_blocking=True)
+        h_sf.copy_(S_final, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(3, min(args.steps, 10))
+    barrier()
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = h_out.numel() * h_out.element_size() + h_sf.numel() * h_sf.element_size()
+
+    # ---- decode: 1000 consecutive steps over 256 sequences
+    dcase = gdn_inputs.decode_256x1000()
+    dsteps = dcase.steps
+    d = gdn_inputs.make_decode(dcase, device=dev)
+    S = d["S"].clone()
+    dout = torch.empty(d["v"].shape[1:], dtype=d["v"].dtype, device=dev)
+    for t in range(3):
+        gdn.decode_step(d["q"][t], d["k"][t], d["v"][t], d["alpha"][t], d["beta"][t], S, out=dout)
+    S.copy_(d["S"])
+    torch.cuda.synchronize(dev)
+    barrier()
+    dn0 = gdn.kernel_launches()
+    ev0.record(stream)
+    for t in range(dsteps):
+        gdn.decode_step(d["q"][t], d["k"][t], d["v"][t], d["alpha"][t], d["beta"][t], S, out=dout)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    dn1 = gdn.kernel_launches()
+    barrier()
+    assert gdn.device_status() == 0
+    d_ms_local = ev0.elapsed_time(ev1) / dsteps
+    d_ms = max_over_ranks(d_ms_local)
+    dbytes = decode_bytes(dcase.N)
+    d_gbs_local = dbytes / (d_ms_local * 1e-3) / 1e9
+
+    res = None
+    if rank == 0:
+        clocks = sampler.summary()
+        cpu = cpu_baseline(args)
+        res = {
+            "metric": METRIC,
+            "value": round(value, 4),
+            "unit": "Mtok/s/layer",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16" if path.startswith("tcgen05") else "f32",
+            "data": "synthetic",
+            "config": {
+                "workload": case.name,
+                "global_batch": 4 * world, "seq_len": 8192, "heads": H, "head_dim": DK,
+                "chunk": C, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                "prefill_path": path,
+                "l2": "inputs larger than L2 (q, k, v = 302 MB per step)",
+            },
+            "roofline": {
+                "bound": "tensor",
+                "achieved": round(achieved_tf, 3),
+                "peak": peaks["bf16"],
+                "unit": "TFLOP/s",
+                "frac": round(achieved_tf / peaks["bf16"], 5),
+                "traffic": ncu_traffic("prefill"),
+                "kernel": "whole gdn_prefill call (chunk prep + state pass)",
+                "counted_flops_per_launch": flops,
+                "peak_source": f"{peaks['src']} bf16 dense (burst)",
+                "hbm_gbs_achieved": round(prefill_bytes(case.lengths) / (ms_local * 1e-3) / 1e9, 2),
+            },
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(tokens * world / (e2e_ms * 1e-3) / 1e6, 4),
+                    "unit": "Mtok/s/layer", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": int(n1 - n0),
+            "clocks": clocks,
+            "decode": {
+                "workload": dcase.name,
+                "value": round(dbytes * world / (d_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "tokens_per_s": round(dcase.N * world / (d_ms * 1e-3), 1),
+                "ms_per_step": round(d_ms, 5), "steps": dsteps,
+                "gpu_launches": int(dn1 - dn0),
+                "roofline": {"bound": "hbm", "achieved": round(d_gbs_local, 2),
+                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": round(d_gbs_local / peaks["hbm_gbs"], 4),
+                             "traffic": ncu_traffic("decode"),
+                             "algorithmic_bytes_per_launch": dbytes,
+                             "peak_source": f"{peaks['src']} HBM copy"},
+            },
+        }
+    return res
+
+
+def cpu_baseline(args, sample_tokens=2048):
+    """The oracle, as it stands, on a bounded sample of the prefill workload:
+    the first `sample_tokens` tokens of all 4 x 6 (sequence, head) units."""
+    import gdn_inputs
+    import oracle
+    case = gdn_inputs.prefill_8k()
+    x = gdn_inputs.make_prefill(case, device="cpu")
+    sl = {n: x[n][:, :sample_tokens].contiguous() for n in ("q", "k", "v", "alpha", "beta")}
+    t = time.perf_counter()
+    _, _, used = oracle.prefill(sl["q"], sl["k"], sl["v"], sl["alpha"], sl["beta"], x["S0"])
+    dt = time.perf_counter() - t
+    tok = 4 * sample_tokens
+    return {"value": round(tok / dt / 1e6, 8), "unit": "Mtok/s/layer", "cores": int(used),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"first {sample_tokens} tokens of each of the 4 sequences x 6 heads "
+                      f"({tok} token-layers) of the prefill workload, fp64 token recurrence"}
+
+
+# ------------------------------------------------------------- reference
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    import gdn_inputs
+    import oracle
+    case = gdn_inputs.prefill_8k()
+    x = gdn_inputs.make_prefill(case, device="cpu")
+    sample_tokens = 512    # per (sequence, head) unit per step: a bounded sample
+    for w in range(args.warmup):
+        sl = {n: x[n][:, :64].contiguous() for n in ("q", "k", "v", "alpha", "beta")}
+        oracle.prefill(sl["q"], sl["k"], sl["v"], sl["alpha"], sl["beta"], x["S0"])
+    times, used = [], 1
+    for s in range(args.steps):
+        a = (s * sample_tokens) % 8192
+        sl = {n: x[n][:, a:a + sample_tokens].contiguous() for n in ("q", "k", "v", "alpha", "beta")}
+        t = time.perf_counter()
+        _, _, used = oracle.prefill(sl["q"], sl["k"], sl["v"], sl["alpha"], sl["beta"], x["S0"])
+        times.append(time.perf_counter() - t)
+    ms = 1e3 * sum(times) / len(times)
+    tok = 4 * sample_tokens
+    value = tok / (ms * 1e-3) / 1e6
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 8), "unit": "Mtok/s/layer",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": case.name, "global_batch": 4, "seq_len": 8192, "heads": H,
+                   "head_dim": DK, "parallelism": "host cores (OpenMP over sequence x head)"},
+        "cpu_baseline": {"value": round(value, 8), "unit": "Mtok/s/layer", "cores": int(used),
+                         "kind": "oracle",
+                         "sample": f"each step: {sample_tokens} consecutive tokens of all 4 x 6 "
+                                   f"(sequence, head) units of the prefill workload"},
+        "e2e": {"value": round(value, 8), "unit": "Mtok/s/layer", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+    else:
+        if world > 1:
+            import torch.distributed as dist_mod
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist_mod.init_process_group("gloo", rank=rank, world_size=world)
+            dist = dist_mod
+        res = run_ours(args, rank, world, local_rank, dist)
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,195 @@
+"""GB300-native Gated DeltaNet (gated delta rule) sequence mixer.
+
+Thin ctypes binding over the C ABI in ``include/gdn.h``: it checks tensor
+shapes, dtypes and devices, reads sizes off the tensors, and passes raw device
+pointers and the current CUDA stream.  Every step of the computation runs in
+the library's CUDA kernels; there is no CPU or PyTorch fallback, and calls
+raise when the compiled library is missing.
+
+    out, S_final = prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None)
+    out = decode_step(q, k, v, alpha, beta, S)          # S updated in place
+
+Recurrence (Appendix A.3, Eq. 16-19 of "Long-Context Aware Upcycling"):
+S_t = alpha_t S_{t-1}(I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+o_t = S_t q_t / sqrt(dk), with the state stored as [dv, dk].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_NAME = "libgdn_gb300.so"
+_lib = None
+
+GDN_F32, GDN_BF16 = 0, 1
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment",
+           4: "CUDA error", 5: "device timeout", 6: "malformed cu_seqlens"}
+
+
+class GDNError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed with status {code} ({_STATUS.get(code, 'unknown')})")
+        self.code = code
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, LIB_NAME)
+
+
+def load():
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{LIB_NAME} is not built; run __graft_entry__.build() "
+                           f"(or python -m hybrid_linear_attention_deltanet_gb300._build)")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.gdn_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32,
+                                vp]
+    lib.gdn_prefill.restype = ctypes.c_int
+    lib.gdn_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+    lib.gdn_decode_step.restype = ctypes.c_int
+    lib.gdn_get_device_status.argtypes = [vp]
+    lib.gdn_get_device_status.restype = ctypes.c_int
+    lib.gdn_version.restype = ctypes.c_char_p
+    lib.gdn_status_string.argtypes = [ctypes.c_int]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_kernel_launches.restype = ctypes.c_uint64
+    lib.gdn_prefill_path.argtypes = [ctypes.c_int32]
+    lib.gdn_prefill_path.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def version() -> str:
+    return load().gdn_version().decode()
+
+
+def kernel_launches() -> int:
+    """Cumulative count of the library's kernel launches in this process."""
+    return int(load().gdn_kernel_launches())
+
+
+def prefill_path(io_dtype=torch.bfloat16) -> str:
+    """Kernel path gdn_prefill takes for this I/O dtype."""
+    return load().gdn_prefill_path(_io_code(io_dtype)).decode()
+
+
+def _stream_handle(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _io_code(dtype):
+    if dtype == torch.bfloat16:
+        return GDN_BF16
+    if dtype == torch.float32:
+        return GDN_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {dtype}")
+
+
+def _check(t, name, dtype, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=None,
+            return_final: bool = True, stream=None):
+    """Chunkwise prefill (``gdn_prefill``).
+
+    Dense: q, k [B, T, H, dk]; v [B, T, H, dv]; alpha, beta [B, T, H] fp32.
+    Varlen: the same with B = 1 (or no batch axis) and ``cu_seqlens`` int32
+    [N + 1] on the device.  S0 / S_final: [N, H, dv, dk] fp32.
+    Returns (out, S_final); S_final is None when ``return_final`` is False.
+    """
+    lib = load()
+    dev = q.device
+    io = q.dtype
+    _io_code(io)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, io, dev)
+    _check(alpha, "alpha", torch.float32, dev)
+    _check(beta, "beta", torch.float32, dev)
+    if q.dim() not in (3, 4) or k.shape != q.shape:
+        raise ValueError("q and k must be [B, T, H, dk] (or [T, H, dk]) and equal in shape")
+    H, dk, dv = q.shape[-2], q.shape[-1], v.shape[-1]
+    if v.shape[:-1] != q.shape[:-1] or alpha.shape != q.shape[:-1] or beta.shape != q.shape[:-1]:
+        raise ValueError("v, alpha, beta must match q's leading [.., T, H] axes")
+    if cu_seqlens is None:
+        B, T = (q.shape[0], q.shape[1]) if q.dim() == 4 else (1, q.shape[0])
+        N, seqlen = B, T
+    else:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        if q.dim() == 4 and q.shape[0] != 1:
+            raise ValueError("varlen input must have batch axis 1")
+        N = cu_seqlens.numel() - 1
+        seqlen = q.shape[-3]
+    if S0 is not None:
+        _check(S0, "S0", torch.float32, dev)
+        if tuple(S0.shape) != (N, H, dv, dk):
+            raise ValueError(f"S0 must be [{N}, {H}, {dv}, {dk}]")
+    if out is None:
+        out = torch.empty_like(v)
+    else:
+        _check(out, "out", io, dev)
+    if S_final is None and return_final:
+        S_final = torch.empty((N, H, dv, dk), dtype=torch.float32, device=dev)
+    elif S_final is not None:
+        _check(S_final, "S_final", torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = lib.gdn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
+                             _ptr(cu_seqlens), _ptr(out), _ptr(S_final), N, seqlen, H, dk, dv,
+                             _io_code(io), _stream_handle(stream))
+    if rc != 0:
+        raise GDNError("gdn_prefill", rc)
+    return out, S_final
+
+
+def decode_step(q, k, v, alpha, beta, S, out=None, stream=None):
+    """One token per sequence (``gdn_decode_step``): q, k [N, H, dk];
+    v [N, H, dv]; alpha, beta [N, H]; S [N, H, dv, dk] fp32 updated in place.
+    Returns out [N, H, dv] in the dtype of v."""
+    lib = load()
+    dev = q.device
+    io = q.dtype
+    _io_code(io)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, io, dev)
+    _check(alpha, "alpha", torch.float32, dev)
+    _check(beta, "beta", torch.float32, dev)
+    _check(S, "S", torch.float32, dev)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if tuple(S.shape) != (N, H, dv, dk) or alpha.shape != (N, H) or beta.shape != (N, H):
+        raise ValueError("shape mismatch in decode_step arguments")
+    if out is None:
+        out = torch.empty_like(v)
+    else:
+        _check(out, "out", io, dev)
+    with torch.cuda.device(dev):
+        rc = lib.gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S),
+                                 _ptr(out), N, H, dk, dv, _io_code(io), _stream_handle(stream))
+    if rc != 0:
+        raise GDNError("gdn_decode_step", rc)
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device status word."""
+    return int(load().gdn_get_device_status(_stream_handle(stream)))

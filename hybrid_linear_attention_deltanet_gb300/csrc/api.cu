@@ -1,0 +1,229 @@
+// C ABI of the library: host-side argument checks, scratch management and
+// dispatch to the kernels.  Declarations and contracts: include/gdn.h.
+#include <atomic>
+#include <mutex>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+// Device status word (first device-side error code since the last read).
+__device__ unsigned g_status_word = 0;
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+unsigned* g_status_ptr[kMaxDevices] = {};
+std::mutex g_status_mu;
+
+// Address of this device's status word, looked up once per device with that
+// device current.
+unsigned* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = (unsigned*)p;
+  }
+  return g_status_ptr[dev];
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+Range span(const void* p, size_t bytes) { return {(uintptr_t)p, (uintptr_t)p + bytes}; }
+bool overlaps(Range a, Range b) {
+  return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
+// cu_seqlens -> exclusive prefix of per-sequence chunk counts, with the
+// monotonicity / end checks.  One CTA; N may be large, so it loops in tiles.
+__global__ void __launch_bounds__(1024)
+chunk_offsets_kernel(const int32_t* __restrict__ cu, int32_t N, int64_t T_total,
+                     int32_t* __restrict__ chunk_off, unsigned* status) {
+  __shared__ int bad;
+  __shared__ int64_t carry;
+  __shared__ int64_t warp_tot[32];
+  if (threadIdx.x == 0) {
+    bad = (cu[0] != 0 || (int64_t)cu[N] != T_total) ? 1 : 0;
+    carry = 0;
+  }
+  __syncthreads();
+  for (int n = threadIdx.x; n < N; n += blockDim.x)
+    if (cu[n + 1] < cu[n]) bad = 1;
+  __syncthreads();
+  if (bad) {
+    for (int n = threadIdx.x; n <= N; n += blockDim.x) chunk_off[n] = 0;
+    if (threadIdx.x == 0) flag_status(status, GDN_ERR_BAD_SEQLENS);
+    return;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int base = 0; base < N; base += blockDim.x) {
+    const int n = base + threadIdx.x;
+    int64_t c = n < N ? ((int64_t)cu[n + 1] - cu[n] + kC - 1) / kC : 0;
+    int64_t x = c;  // inclusive warp scan
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int64_t w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_tot[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int64_t before = carry + (warp ? warp_tot[warp - 1] : 0) + x - c;
+    if (n < N) chunk_off[n] = (int32_t)before;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = before + c;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) chunk_off[N] = (int32_t)carry;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_offsets(const int32_t* cu_seqlens, int32_t N, int64_t T_total,
+                                 int32_t* chunk_off, unsigned* status, cudaStream_t stream) {
+  chunk_offsets_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, T_total, chunk_off, status);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
+                const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
+                float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                int32_t dv, int32_t io_dtype, gdn_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (batch < 1 || seqlen < 0 || heads < 1) return GDN_ERR_INVALID_ARG;
+  const bool varlen = cu_seqlens != nullptr;
+  const int64_t T_total = varlen ? seqlen : (int64_t)batch * seqlen;
+  // token tensors may be empty (and then null) only when there are no tokens
+  if (T_total > 0 && (!q || !k || !v || !alpha || !beta || !out)) return GDN_ERR_INVALID_ARG;
+  if (io_dtype != GDN_F32 && io_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  if (dk != kDK || dv != kDV) return GDN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) ||
+      !aligned16(beta) || !aligned16(out) || !aligned16(S0) || !aligned16(S_final) ||
+      ((uintptr_t)cu_seqlens & 3u))
+    return GDN_ERR_ALIGNMENT;
+  if (varlen && T_total > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;   // int32 offsets
+  const size_t es = io_dtype == GDN_BF16 ? 2 : 4;
+  const size_t n_tok_h = (size_t)T_total * heads;
+  const size_t state_bytes = (size_t)batch * heads * dv * dk * sizeof(float);
+  const Range in[] = {span(q, n_tok_h * dk * es), span(k, n_tok_h * dk * es),
+                      span(v, n_tok_h * dv * es), span(alpha, n_tok_h * 4),
+                      span(beta, n_tok_h * 4),
+                      span(S0, S0 ? state_bytes : 0),
+                      span(cu_seqlens, varlen ? ((size_t)batch + 1) * 4 : 0)};
+  const Range r_out = span(out, n_tok_h * dv * es);
+  const Range r_sf = span(S_final, S_final ? state_bytes : 0);
+  for (const Range& r : in)
+    if (overlaps(r, r_out) || overlaps(r, r_sf)) return GDN_ERR_INVALID_ARG;
+  if (overlaps(r_out, r_sf)) return GDN_ERR_INVALID_ARG;
+
+  unsigned* status = status_ptr();
+  if (!status) return GDN_ERR_CUDA;
+
+  PrefillLaunch a{};
+  a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.S0 = S0;
+  a.out = out; a.S_final = S_final; a.H = heads; a.status = status;
+  a.map.cu_seqlens = cu_seqlens;
+  a.map.N = batch;
+  a.map.T = varlen ? T_total : seqlen;
+  a.map.chunks_per_seq = varlen ? 0 : (seqlen + kC - 1) / kC;
+  a.max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
+
+  const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
+  const size_t work_bytes = prefill_simt_scratch_bytes(a.max_chunks, heads);
+  void* scratch = nullptr;
+  if (off_bytes + work_bytes > 0 &&
+      cudaMallocAsync(&scratch, off_bytes + work_bytes, stream) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  a.scratch = (char*)scratch + off_bytes;
+  cudaError_t e = cudaSuccess;
+  if (varlen) {
+    a.map.chunk_off = (int32_t*)scratch;
+    e = launch_chunk_offsets(cu_seqlens, batch, T_total, (int32_t*)scratch, status, stream);
+  }
+  if (e == cudaSuccess) e = launch_prefill_simt(a, io_dtype, stream);
+  const cudaError_t ef = scratch ? cudaFreeAsync(scratch, stream) : cudaSuccess;
+  return (e == cudaSuccess && ef == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_decode_step(const void* q, const void* k, const void* v, const float* alpha,
+                    const float* beta, float* S_inout, void* out, int32_t batch,
+                    int32_t heads, int32_t dk, int32_t dv, int32_t io_dtype,
+                    gdn_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (!q || !k || !v || !alpha || !beta || !S_inout || !out) return GDN_ERR_INVALID_ARG;
+  if (batch < 1 || heads < 1) return GDN_ERR_INVALID_ARG;
+  if (io_dtype != GDN_F32 && io_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  if (dk != kDK || dv != kDV) return GDN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) ||
+      !aligned16(beta) || !aligned16(S_inout) || !aligned16(out))
+    return GDN_ERR_ALIGNMENT;
+  const size_t es = io_dtype == GDN_BF16 ? 2 : 4;
+  const size_t nh = (size_t)batch * heads;
+  const Range r_out = span(out, nh * dv * es);
+  const Range others[] = {span(q, nh * dk * es), span(k, nh * dk * es), span(v, nh * dv * es),
+                          span(alpha, nh * 4), span(beta, nh * 4),
+                          span(S_inout, nh * dv * dk * 4)};
+  for (const Range& r : others)
+    if (overlaps(r, r_out)) return GDN_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i)
+    if (overlaps(others[i], others[5])) return GDN_ERR_INVALID_ARG;
+  const cudaError_t e =
+      launch_decode_step(q, k, v, alpha, beta, S_inout, out, batch, heads, io_dtype, stream);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_get_device_status(gdn_stream_t stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof v) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess) return GDN_ERR_CUDA;
+  return (int)v;
+}
+
+uint64_t gdn_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* gdn_prefill_path(int32_t io_dtype) {
+  if (io_dtype == GDN_F32) return "simt-f32";
+  if (io_dtype == GDN_BF16) return "simt-f32";
+  return nullptr;
+}
+
+const char* gdn_version(void) { return "gdn-gb300 0.1.0 (sm_103a)"; }
+
+const char* gdn_status_string(int s) {
+  switch (s) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_INVALID_ARG: return "invalid argument";
+    case GDN_ERR_UNSUPPORTED: return "unsupported head geometry or dtype";
+    case GDN_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case GDN_ERR_CUDA: return "CUDA runtime error";
+    case GDN_ERR_TIMEOUT: return "device: bounded wait timed out";
+    case GDN_ERR_BAD_SEQLENS: return "device: malformed cu_seqlens";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

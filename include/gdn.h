@@ -1,0 +1,146 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) Gated DeltaNet library.
+ *
+ * The library computes the gated delta rule of "Long-Context Aware Upcycling:
+ * A New Frontier for Hybrid LLM Scaling", Appendix A.3, Eq. (16)-(19):
+ *
+ *     S_t = alpha_t * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = S_t q_t / sqrt(dk)                  (read out from the UPDATED state)
+ *
+ * per sequence and head, with alpha_t = e^{g_t} in (0, 1] (the decay itself,
+ * Eq. 16) and beta_t in [0, 1] (the write strength, Eq. 18).  The paper keeps
+ * its state as S^T (dk x dv); this library stores S as dv x dk, so row i of a
+ * state here is column i of the paper's state.  Eq. 17-18 expand to exactly
+ * the update above under that transpose.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers, owned by the caller, contiguous
+ *    (row-major) in the layouts given below, and 16-byte aligned; a
+ *    misaligned pointer returns GDN_ERR_ALIGNMENT before anything is launched.
+ *  - io_dtype selects the element type of q, k, v and out: GDN_F32 (float) or
+ *    GDN_BF16 (bfloat16 stored as uint16).  alpha, beta and every state are
+ *    always fp32; accumulation is always fp32.
+ *  - Supported head geometry: dk = dv = 256 (6 heads of 256 in the pages'
+ *    GDN layers; any heads >= 1 is accepted).  Others: GDN_ERR_UNSUPPORTED.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and never synchronise the host.  Host-side argument
+ *    errors are returned before any launch; a failed launch or allocation
+ *    returns GDN_ERR_CUDA.  Problems only the device can see (a malformed
+ *    cu_seqlens, a bounded wait that ran out) set a device status word, read
+ *    back with gdn_get_device_status().
+ *  - Preconditions, documented but not checked on the hot path:
+ *    0 < alpha <= 1 (the pages' g_t in (-inf, 0); decay is handled in log
+ *    space, so alpha = 0 is not supported) and 0 <= beta <= 1.
+ *  - The CUDA device used is the one current on the calling thread.
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* same object as cudaStream_t; spelled out so that this header needs no CUDA header */
+typedef struct CUstream_st* gdn_stream_t;
+
+enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 };
+
+enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, overlapping out/state */
+  GDN_ERR_UNSUPPORTED = 2,   /* dk/dv/io_dtype outside what the kernels implement */
+  GDN_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned */
+  GDN_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  GDN_ERR_TIMEOUT = 5,       /* device: a bounded wait inside a kernel gave up */
+  GDN_ERR_BAD_SEQLENS = 6    /* device: cu_seqlens not 0 = cu[0] <= ... <= cu[N] = T_total */
+};
+
+/*
+ * gdn_prefill -- chunkwise-parallel prefill of whole sequences.
+ *
+ * Computes the recurrence above for every token of every sequence and head,
+ * starting each sequence from its own initial state, and returns every
+ * output o_t and (optionally) each sequence's final state.  The pages'
+ * training kernel splits the sequence into chunks of C = 64 tokens, batches
+ * the delta corrections inside a chunk through the WY representation, and
+ * carries the state across chunks sequentially (Appendix A.3, last
+ * paragraph); this library uses the same chunk size and decomposition, with
+ * chunks restarting at every sequence start.
+ *
+ * Dense batch (cu_seqlens == NULL): batch = B sequences of seqlen = T tokens.
+ *   q, k   [B, T, H, dk]     v, out [B, T, H, dv]     alpha, beta [B, T, H]
+ * Packed varlen batch (cu_seqlens != NULL, the pages' continuous batching,
+ * Section 3.4): batch = N sequences packed along one token axis of length
+ * seqlen = T_total; cu_seqlens is a DEVICE int32 array of N+1 offsets with
+ * cu[0] = 0, non-decreasing, cu[N] = T_total (zero-length sequences are
+ * allowed).  Tensors are [1, T_total, H, .] (or equivalently [T_total, H, .]).
+ *
+ *   S0       [N, H, dv, dk] fp32 initial states, or NULL for zero states.
+ *   S_final  [N, H, dv, dk] fp32 final states, or NULL to skip writing them.
+ *            A zero-length sequence gets S_final = S0.
+ *   out      same dtype as v; every token row is written exactly once.
+ * Neither out nor S_final may overlap any input (GDN_ERR_INVALID_ARG when the
+ * byte ranges intersect).  Results do not depend on how sequences are packed:
+ * a sequence gives bit-identical out and S_final alone or inside any batch.
+ *
+ * Scratch: intermediate per-chunk factors are kept in device memory obtained
+ * with stream-ordered cudaMallocAsync / cudaFreeAsync on `stream`; nothing
+ * persists after the call except the device status word.
+ */
+int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
+                const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
+                float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                int32_t dv, int32_t io_dtype, gdn_stream_t stream);
+
+/*
+ * gdn_decode_step -- one generated token for each of `batch` independent
+ * sequences against their cached states (the fixed-size recurrent state the
+ * pages' serving stack keeps per linear-attention layer, Section 4.4).
+ *
+ *   q, k      [N, H, dk]       v, out [N, H, dv]       alpha, beta [N, H]
+ *   S_inout   [N, H, dv, dk] fp32 states, read and overwritten in place with
+ *             S_t (each state makes one round trip through HBM).
+ * out must not overlap any input or the state (GDN_ERR_INVALID_ARG).
+ */
+int gdn_decode_step(const void* q, const void* k, const void* v, const float* alpha,
+                    const float* beta, float* S_inout, void* out, int32_t batch,
+                    int32_t heads, int32_t dk, int32_t dv, int32_t io_dtype,
+                    gdn_stream_t stream);
+
+/*
+ * gdn_get_device_status -- synchronises `stream`, then returns and clears the
+ * device status word of the current device (GDN_OK when no kernel flagged a
+ * problem since the last call; GDN_ERR_CUDA if the synchronisation failed).
+ */
+int gdn_get_device_status(gdn_stream_t stream);
+
+/*
+ * gdn_kernel_launches -- cumulative number of kernels this library has
+ * launched in this process (all devices, all streams).  Host-side counter,
+ * incremented at each launch; for benchmarks that report how many of the
+ * library's kernels ran inside a timed region.
+ */
+uint64_t gdn_kernel_launches(void);
+
+/*
+ * gdn_prefill_path -- name of the kernel path gdn_prefill takes for an
+ * io_dtype ("simt-f32": CUDA-core fp32 FFMA; "tcgen05-bf16": tensor-core
+ * MMAs with bf16 operands and fp32 accumulation).  NULL for an unknown dtype.
+ */
+const char* gdn_prefill_path(int32_t io_dtype);
+
+/* Library version string (static storage). */
+const char* gdn_version(void);
+
+/* Human-readable text for a gdn_status value (static storage). */
+const char* gdn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

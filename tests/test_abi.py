@@ -1,0 +1,86 @@
+"""The C-ABI library loads, exports every entry point include/gdn.h declares,
+and rejects malformed host arguments before touching the GPU.  CPU only: no
+call here reaches a CUDA runtime function."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import hybrid_linear_attention_deltanet_gb300 as gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(gdn_\w+)\s*\(", text,
+                                 flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(gdn.lib_path()):
+        from hybrid_linear_attention_deltanet_gb300 import _build
+        _build.build()
+    return gdn.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for fn in ("gdn_prefill", "gdn_decode_step", "gdn_get_device_status", "gdn_version",
+               "gdn_status_string"):
+        assert fn in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for fn in declared_functions():
+        assert hasattr(lib, fn), fn
+
+
+def test_version_and_status_strings(lib):
+    assert b"sm_103a" in lib.gdn_version()
+    assert lib.gdn_status_string(0) == b"ok"
+    assert lib.gdn_status_string(3).startswith(b"pointer")
+
+
+P = ctypes.c_void_p
+A16 = P(0x10000)          # aligned fake device addresses: validation fails before any use
+A16b = P(0x20000)
+MIS = P(0x10004)
+
+
+def _prefill(lib, q=A16, k=A16, v=A16, alpha=A16, beta=A16, S0=None, cu=None, out=A16b,
+             S_final=None, batch=1, T=64, H=6, dk=256, dv=256, io=1):
+    return lib.gdn_prefill(q, k, v, alpha, beta, S0, cu, out, S_final, batch, T, H, dk, dv, io,
+                           None)
+
+
+def test_prefill_rejects_bad_host_arguments(lib):
+    assert _prefill(lib, q=None) == 1
+    assert _prefill(lib, out=None) == 1
+    assert _prefill(lib, batch=0) == 1
+    assert _prefill(lib, H=0) == 1
+    assert _prefill(lib, T=-1) == 1
+    assert _prefill(lib, dk=128) == 2
+    assert _prefill(lib, dv=512) == 2
+    assert _prefill(lib, io=7) == 2
+    assert _prefill(lib, q=MIS) == 3
+    assert _prefill(lib, S_final=MIS) == 3
+    assert _prefill(lib, cu=P(0x30002)) == 3
+    # out overlapping an input range
+    assert _prefill(lib, q=P(0x100000), k=P(0x200000), v=P(0x300000), alpha=P(0x400000),
+                    beta=P(0x500000), out=P(0x100000 + 4096)) == 1
+
+
+def test_decode_rejects_bad_host_arguments(lib):
+    f = lambda **kw: lib.gdn_decode_step(kw.get("q", A16), A16, A16, A16, A16,
+                                         kw.get("S", P(0x800000)), kw.get("out", P(0x900000)),
+                                         kw.get("N", 4), 6, kw.get("dk", 256), 256, 1, None)
+    assert f(S=None) == 1
+    assert f(N=0) == 1
+    assert f(dk=64) == 2
+    assert f(q=MIS) == 3
+    assert f(out=P(0x800000 + 1024)) == 1      # out inside the state
