@@ -4,6 +4,7 @@
 #include <mutex>
 
 #include "gdn_internal.cuh"
+#include "../../include/gdn_testing.h"
 
 namespace gdn {
 
@@ -19,6 +20,8 @@ constexpr int kMaxDevices = 64;
 unsigned* g_status_ptr[kMaxDevices] = {};
 std::mutex g_status_mu;
 
+}  // namespace
+
 // Address of this device's status word, looked up once per device with that
 // device current.
 unsigned* status_ptr() {
@@ -32,6 +35,8 @@ unsigned* status_ptr() {
   }
   return g_status_ptr[dev];
 }
+
+namespace {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -152,7 +157,9 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
   a.max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
 
   const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
-  const size_t work_bytes = prefill_simt_scratch_bytes(a.max_chunks, heads);
+  const bool tc = io_dtype == GDN_BF16;
+  const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads)
+                               : prefill_simt_scratch_bytes(a.max_chunks, heads);
   void* scratch = nullptr;
   if (off_bytes + work_bytes > 0 &&
       cudaMallocAsync(&scratch, off_bytes + work_bytes, stream) != cudaSuccess)
@@ -163,7 +170,7 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
     a.map.chunk_off = (int32_t*)scratch;
     e = launch_chunk_offsets(cu_seqlens, batch, T_total, (int32_t*)scratch, status, stream);
   }
-  if (e == cudaSuccess) e = launch_prefill_simt(a, io_dtype, stream);
+  if (e == cudaSuccess) e = tc ? launch_prefill_tc(a, stream) : launch_prefill_simt(a, io_dtype, stream);
   const cudaError_t ef = scratch ? cudaFreeAsync(scratch, stream) : cudaSuccess;
   return (e == cudaSuccess && ef == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -195,6 +202,42 @@ int gdn_decode_step(const void* q, const void* k, const void* v, const float* al
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+int gdn_testing_prefill_prep(const void* q, const void* k, const void* v, const float* alpha,
+                             const float* beta, const int32_t* cu_seqlens, int32_t batch,
+                             int64_t seqlen, int32_t heads, void* images, size_t image_bytes,
+                             gdn_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (!q || !k || !v || !alpha || !beta || !images || batch < 1 || seqlen < 1 || heads < 1)
+    return GDN_ERR_INVALID_ARG;
+  const bool varlen = cu_seqlens != nullptr;
+  const int64_t T_total = varlen ? seqlen : (int64_t)batch * seqlen;
+  PrefillLaunch a{};
+  a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.H = heads;
+  a.status = status_ptr();
+  if (!a.status) return GDN_ERR_CUDA;
+  a.map.cu_seqlens = cu_seqlens;
+  a.map.N = batch;
+  a.map.T = varlen ? T_total : seqlen;
+  a.map.chunks_per_seq = varlen ? 0 : (seqlen + kC - 1) / kC;
+  a.max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
+  if (image_bytes < (size_t)a.max_chunks * heads * prefill_tc_image_stride())
+    return GDN_ERR_INVALID_ARG;
+  void* offs = nullptr;
+  if (varlen) {
+    if (cudaMallocAsync(&offs, ((size_t)batch + 1) * 4, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    a.map.chunk_off = (int32_t*)offs;
+    if (launch_chunk_offsets(cu_seqlens, batch, T_total, (int32_t*)offs, a.status, stream) !=
+        cudaSuccess)
+      return GDN_ERR_CUDA;
+  }
+  a.scratch = images;
+  cudaError_t e = launch_prefill_tc(a, stream, /*prep_only=*/true);
+  if (offs) cudaFreeAsync(offs, stream);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+size_t gdn_testing_prefill_image_stride(void) { return prefill_tc_image_stride(); }
+
 int gdn_get_device_status(gdn_stream_t stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
   unsigned v = 0, zero = 0;
@@ -207,7 +250,7 @@ uint64_t gdn_kernel_launches(void) { return g_launches.load(std::memory_order_re
 
 const char* gdn_prefill_path(int32_t io_dtype) {
   if (io_dtype == GDN_F32) return "simt-f32";
-  if (io_dtype == GDN_BF16) return "simt-f32";
+  if (io_dtype == GDN_BF16) return "tcgen05-bf16";
   return nullptr;
 }
 

@@ -89,6 +89,9 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // host-side count of kernel launches (gdn_kernel_launches)
 void count_launches(int n);
 
+// device address of the current device's status word (nullptr on failure)
+unsigned* status_ptr();
+
 // ---------------------------------------------------------------------------
 // launchers (one translation unit each)
 struct PrefillLaunch {
@@ -108,6 +111,11 @@ cudaError_t launch_chunk_offsets(const int32_t* cu_seqlens, int32_t N, int64_t T
 // CUDA-core (fp32 FFMA) chunkwise path: used for fp32 I/O.
 size_t prefill_simt_scratch_bytes(int64_t max_chunks, int32_t H);
 cudaError_t launch_prefill_simt(const PrefillLaunch& a, int io_dtype, cudaStream_t stream);
+
+// Tensor-core (tcgen05) chunkwise path: used for bf16 I/O.
+size_t prefill_tc_scratch_bytes(int64_t max_chunks, int32_t H);
+cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool prep_only = false);
+size_t prefill_tc_image_stride();
 
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, const float* alpha,
                                const float* beta, float* S, void* out, int32_t N, int32_t H,
