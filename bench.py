@@ -141,6 +141,38 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+class Replicas:
+    """Rank bookkeeping for replica runs: a barrier around timed regions, the
+    max of a time over ranks, and the sum of work over ranks.  `dist` is
+    torch.distributed (gloo) or None for a single process."""
+
+    def __init__(self, dist, world):
+        self.dist, self.world = dist, world
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        return self._reduce(x, "MAX")
+
+    def sum(self, x: float) -> float:
+        return self._reduce(x, "SUM")
+
+    def _reduce(self, x, op):
+        if self.dist is None:
+            return float(x)
+        import torch
+        t = torch.tensor([float(x)], dtype=torch.float64)
+        self.dist.all_reduce(t, op=getattr(self.dist.ReduceOp, op))
+        return float(t.item())
+
+
+def throughput(units_all_ranks: float, ms_max: float) -> float:
+    """Whole-job rate: the units every rank processed over the slowest rank's time."""
+    return units_all_ranks / (ms_max * 1e-3)
+
+
 # ------------------------------------------------------------------ ours
 def run_ours(args, rank, world, local_rank, dist):
     import torch
@@ -154,16 +186,8 @@ def run_ours(args, rank, world, local_rank, dist):
     stream = torch.cuda.current_stream(dev)
     peaks = load_peaks()
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    rep = Replicas(dist, world)
+    barrier, max_over_ranks = rep.barrier, rep.max
 
     case = gdn_inputs.prefill_8k()
     x = gdn_inputs.make_prefill(case, device=dev)
@@ -196,7 +220,7 @@ def run_ours(args, rank, world, local_rank, dist):
     ms_local = ev0.elapsed_time(ev1) / args.steps
     ms = max_over_ranks(ms_local)
     tokens = case.total_tokens
-    value = tokens * world / (ms * 1e-3) / 1e6
+    value = throughput(rep.sum(tokens), ms) / 1e6
     flops = prefill_flops(case.lengths)
     achieved_tf = flops / (ms_local * 1e-3) / 1e12
     path = gdn.prefill_path(case.io_dtype)
@@ -294,15 +318,15 @@ def run_ours(args, rank, world, local_rank, dist):
                 "hbm_gbs_achieved": round(prefill_bytes(case.lengths) / (ms_local * 1e-3) / 1e9, 2),
             },
             "cpu_baseline": cpu,
-            "e2e": {"value": round(tokens * world / (e2e_ms * 1e-3) / 1e6, 4),
+            "e2e": {"value": round(throughput(tokens * world, e2e_ms) / 1e6, 4),
                     "unit": "Mtok/s/layer", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": int(n1 - n0),
             "clocks": clocks,
             "decode": {
                 "workload": dcase.name,
-                "value": round(dbytes * world / (d_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "tokens_per_s": round(dcase.N * world / (d_ms * 1e-3), 1),
+                "value": round(throughput(dbytes * world, d_ms) / 1e9, 2), "unit": "GB/s",
+                "tokens_per_s": round(throughput(dcase.N * world, d_ms), 1),
                 "ms_per_step": round(d_ms, 5), "steps": dsteps,
                 "gpu_launches": int(dn1 - dn0),
                 "roofline": {"bound": "hbm", "achieved": round(d_gbs_local, 2),
@@ -332,6 +356,31 @@ def cpu_baseline(args, sample_tokens=2048):
             "kind": "oracle", "seconds": round(dt, 3),
             "sample": f"first {sample_tokens} tokens of each of the 4 sequences x 6 heads "
                       f"({tok} token-layers) of the prefill workload, fp64 token recurrence"}
+
+
+def run_profile(args):
+    """Only the library's kernels of one family, for a profiler: W warm-up
+    then K steps of the 8K prefill workload, or of the 256-sequence decode."""
+    import torch
+
+    import gdn_inputs
+    import hybrid_linear_attention_deltanet_gb300 as gdn
+    dev = torch.device("cuda", 0)
+    gdn.load()
+    if args.profile == "prefill":
+        x = gdn_inputs.make_prefill(gdn_inputs.prefill_8k(), device=dev)
+        out, sf = torch.empty_like(x["v"]), torch.empty_like(x["S0"])
+        for _ in range(args.warmup + args.steps):
+            gdn.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"], out=out,
+                        S_final=sf)
+    else:
+        case = gdn_inputs.decode_256x1000()
+        d = gdn_inputs.make_decode(case, device=dev, steps=args.warmup + args.steps)
+        S = d["S"]
+        for t in range(args.warmup + args.steps):
+            gdn.decode_step(d["q"][t], d["k"][t], d["v"][t], d["alpha"][t], d["beta"][t], S)
+    torch.cuda.synchronize(dev)
+    assert gdn.device_status() == 0
 
 
 # ------------------------------------------------------------- reference
@@ -378,6 +427,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+                    help="run only W + K steps of one kernel family (for ncu captures); "
+                         "prints no benchmark line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -385,6 +437,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     dist = None
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         res = run_reference(args, rank)
     else:
