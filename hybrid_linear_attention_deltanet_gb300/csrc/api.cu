@@ -39,6 +39,7 @@ unsigned* status_ptr() {
 namespace {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
 
 struct Range {
   uintptr_t lo, hi;  // [lo, hi)
@@ -125,9 +126,8 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
   if (T_total > 0 && (!q || !k || !v || !alpha || !beta || !out)) return GDN_ERR_INVALID_ARG;
   if (io_dtype != GDN_F32 && io_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
   if (dk != kDK || dv != kDV) return GDN_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) ||
-      !aligned16(beta) || !aligned16(out) || !aligned16(S0) || !aligned16(S_final) ||
-      ((uintptr_t)cu_seqlens & 3u))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(alpha) || !aligned4(beta) ||
+      !aligned16(out) || !aligned16(S0) || !aligned16(S_final) || !aligned4(cu_seqlens))
     return GDN_ERR_ALIGNMENT;
   if (varlen && T_total > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;   // int32 offsets
   const size_t es = io_dtype == GDN_BF16 ? 2 : 4;
@@ -184,8 +184,8 @@ int gdn_decode_step(const void* q, const void* k, const void* v, const float* al
   if (batch < 1 || heads < 1) return GDN_ERR_INVALID_ARG;
   if (io_dtype != GDN_F32 && io_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
   if (dk != kDK || dv != kDV) return GDN_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) ||
-      !aligned16(beta) || !aligned16(S_inout) || !aligned16(out))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(alpha) || !aligned4(beta) ||
+      !aligned16(S_inout) || !aligned16(out))
     return GDN_ERR_ALIGNMENT;
   const size_t es = io_dtype == GDN_BF16 ? 2 : 4;
   const size_t nh = (size_t)batch * heads;
@@ -261,7 +261,7 @@ const char* gdn_status_string(int s) {
     case GDN_OK: return "ok";
     case GDN_ERR_INVALID_ARG: return "invalid argument";
     case GDN_ERR_UNSUPPORTED: return "unsupported head geometry or dtype";
-    case GDN_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case GDN_ERR_ALIGNMENT: return "pointer not aligned (16 B for tensors, 4 B for alpha/beta/cu_seqlens)";
     case GDN_ERR_CUDA: return "CUDA runtime error";
     case GDN_ERR_TIMEOUT: return "device: bounded wait timed out";
     case GDN_ERR_BAD_SEQLENS: return "device: malformed cu_seqlens";

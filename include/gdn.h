@@ -16,8 +16,11 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All tensor pointers are DEVICE pointers, owned by the caller, contiguous
- *    (row-major) in the layouts given below, and 16-byte aligned; a
- *    misaligned pointer returns GDN_ERR_ALIGNMENT before anything is launched.
+ *    (row-major) in the layouts given below.  q, k, v, out and the fp32
+ *    states must be 16-byte aligned (they are moved with 16-byte vector and
+ *    TMA copies); alpha, beta and cu_seqlens need only their natural 4-byte
+ *    alignment.  A misaligned pointer returns GDN_ERR_ALIGNMENT before
+ *    anything is launched.
  *  - io_dtype selects the element type of q, k, v and out: GDN_F32 (float) or
  *    GDN_BF16 (bfloat16 stored as uint16).  alpha, beta and every state are
  *    always fp32; accumulation is always fp32.
@@ -53,7 +56,7 @@ enum gdn_status {
   GDN_OK = 0,
   GDN_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, overlapping out/state */
   GDN_ERR_UNSUPPORTED = 2,   /* dk/dv/io_dtype outside what the kernels implement */
-  GDN_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned */
+  GDN_ERR_ALIGNMENT = 3,     /* a pointer is not aligned as the conventions require */
   GDN_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
   GDN_ERR_TIMEOUT = 5,       /* device: a bounded wait inside a kernel gave up */
   GDN_ERR_BAD_SEQLENS = 6    /* device: cu_seqlens not 0 = cu[0] <= ... <= cu[N] = T_total */

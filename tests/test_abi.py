@@ -70,6 +70,8 @@ def test_prefill_rejects_bad_host_arguments(lib):
     assert _prefill(lib, q=MIS) == 3
     assert _prefill(lib, S_final=MIS) == 3
     assert _prefill(lib, cu=P(0x30002)) == 3
+    assert _prefill(lib, alpha=P(0x40001)) == 3
+    assert _prefill(lib, alpha=P(0x40004), beta=P(0x50004), out=P(0x900000)) != 3  # 4 B is enough
     # out overlapping an input range
     assert _prefill(lib, q=P(0x100000), k=P(0x200000), v=P(0x300000), alpha=P(0x400000),
                     beta=P(0x500000), out=P(0x100000 + 4096)) == 1
