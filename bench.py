@@ -138,7 +138,9 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm),
+                "window": "nvidia-smi every 100 ms from before the timed prefill steps (GPU kept "
+                          "busy by untimed steps) through the e2e and decode timing"}
 
 
 class Replicas:
@@ -205,16 +207,23 @@ def run_ours(args, rank, world, local_rank, dist):
 
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev.index)
+    sampler.__enter__()
+    # nvidia-smi needs a moment to start sampling: keep the GPU busy with
+    # untimed prefill steps meanwhile, so the sampled window holds the timed
+    # steps (and the e2e and decode timing after them) under load
+    t_spin = time.perf_counter() + 0.6
+    while time.perf_counter() < t_spin:
+        step()
+        torch.cuda.synchronize(dev)
     barrier()
-    with sampler:
-        torch.cuda.synchronize(dev)
-        n0 = gdn.kernel_launches()
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        n1 = gdn.kernel_launches()
+    torch.cuda.synchronize(dev)
+    n0 = gdn.kernel_launches()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    n1 = gdn.kernel_launches()
     barrier()
     assert gdn.device_status() == 0
     ms_local = ev0.elapsed_time(ev1) / args.steps
@@ -276,6 +285,7 @@ def run_ours(args, rank, world, local_rank, dist):
     dn1 = gdn.kernel_launches()
     barrier()
     assert gdn.device_status() == 0
+    sampler.__exit__(None, None, None)
     d_ms_local = ev0.elapsed_time(ev1) / dsteps
     d_ms = max_over_ranks(d_ms_local)
     dbytes = decode_bytes(dcase.N)

@@ -8,20 +8,22 @@
 // alpha), gamma = exp(G), Gam_rj = exp(G_r - G_j), d_r = gamma_L / gamma_r:
 //   A  = strict_lower(beta_r Gam_rj k_r.k_j),   T = (I + A)^{-1}
 //   W  = T diag(beta gamma) K,  U~ = T diag(beta) V,  P^ = lower(Gam Q K^T)/sqrt(dk)
-//   Q^ = diag(gamma) Q / sqrt(dk)
-//   U  = U~ - W S^T,  O = Q^ S^T + P^ U,  S' = gamma_L S + U^T diag(d) K
+//   Q^ = diag(gamma) Q / sqrt(dk),   K^ = diag(d) K
+//   U  = U~ - W S^T,  O = Q^ S^T + P^ U,  S' = gamma_L S + U^T K^
 //
-// Kernel 1, tc_prep (one CTA per (chunk, head), fully parallel):
-//   [K;Q] K^T on tcgen05 (M=128, N=64, K=256) -> A and P^ in fp32;
-//   T by a blocked (16 x 16) fp32 forward substitution on the CUDA cores;
-//   W^T = K^T T_w^T and U~^T = V^T T_u^T on tcgen05 (M=128 x 2 halves);
-//   writes W, Q^, P^, U~^T and G to scratch as ready-to-load swizzled
-//   operand images (the state pass copies them with 1-D TMA bulk copies).
+// Kernel 1, tc_prep (one CTA per (chunk, head), fully parallel, two CTAs per SM):
+//   TMA tensor copies of the K, Q, V tiles; [K;Q] K^T on tcgen05 (M=128, N=64,
+//   K=256) -> A and P^; T by a two-level recursive block inverse in fp32 on
+//   the CUDA cores; W^T = K^T T_w^T and U~^T = V^T T_u^T on tcgen05; writes
+//   W, Q^, K^, P^, U~^T and G to scratch as ready-to-load swizzled operand
+//   images (the state pass copies them with 1-D TMA bulk copies).
 // Kernel 2, tc_state (one CTA per (sequence, head, 128-row half of S)):
-//   rows of S are independent, so each CTA owns 128 rows (the MMA M) and
-//   walks the sequence's chunks: D_U = S W^T, D_O = S Q^^T (M=128, N=64,
-//   K=256); U = U~ - D_U -> bf16; D_S = U^T (d K) (N=256, K=64) and
-//   D_O += U^T P^^T; S = gamma_L S + D_S in fp32 registers; O -> out.
+//   rows of S are independent, so each CTA owns 128 rows (the MMA M).  The
+//   bf16 copy of its S rows lives in TMEM as the A operand; the fp32 master
+//   copy lives in registers.  Per chunk: D_U = S W^T, D_O = S Q^^T (M=128,
+//   N=64, K=256, A from TMEM); U = U~ - D_U -> bf16; D_S = U^T K^ (N=256,
+//   K=64) and D_O += U^T P^^T; S = gamma_L S + D_S; O -> out.  W and Q^ are
+//   double-buffered (fetched two chunks ahead), the rest one chunk ahead.
 //
 // Shared-memory operand images use the 128-byte swizzle: rows of 64 bf16,
 // 16-byte chunk index XOR (row % 8), 8-row groups 1024 bytes apart.
@@ -43,10 +45,11 @@ using namespace sm100;
 // ---- scratch image per (chunk, head)
 constexpr size_t kImgW = 0;           // W   : MN-major B image, 256 K-rows (c) x 64 (r)
 constexpr size_t kImgQ = 32768;       // Q^  : K-major B image, 4 K-blocks x (64 rows x 128 B)
-constexpr size_t kImgP = 65536;       // P^  : K-major B image, 64 rows x 64
-constexpr size_t kImgU = 73728;       // U~^T: 256 rows (i) x 64 (r), 128-byte swizzled rows
-constexpr size_t kImgG = 106496;      // G   : 64 fp32
-constexpr size_t kImgStride = 107520;
+constexpr size_t kImgK = 65536;       // K^  : MN-major B image, 4 column blocks x (64 rows x 128 B)
+constexpr size_t kImgP = 98304;       // P^  : K-major B image, 64 rows x 64
+constexpr size_t kImgU = 106496;      // U~^T: 256 rows (i) x 64 (r), 128-byte swizzled rows
+constexpr size_t kImgG = 139264;      // G   : 64 fp32
+constexpr size_t kImgStride = 140288;
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
@@ -54,6 +57,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ uint4 scale8(uint4 v, float s) {
+  v.x = pack_bf16(bf16_lo(v.x) * s, bf16_hi(v.x) * s);
+  v.y = pack_bf16(bf16_lo(v.y) * s, bf16_hi(v.y) * s);
+  v.z = pack_bf16(bf16_lo(v.z) * s, bf16_hi(v.z) * s);
+  v.w = pack_bf16(bf16_lo(v.w) * s, bf16_hi(v.w) * s);
+  return v;
+}
 
 // byte offset of 16-byte chunk `ch` (0..7) of row `row` in a 128-byte-swizzled image
 __device__ __forceinline__ uint32_t sw_chunk(uint32_t row, uint32_t ch) {
@@ -61,21 +71,23 @@ __device__ __forceinline__ uint32_t sw_chunk(uint32_t row, uint32_t ch) {
 }
 
 // ============================================================ prep kernel
-constexpr int kPrepThreads = 128;
+constexpr int kPrepThreads = 256;
 // shared memory layout (offsets from the 1024-aligned base)
-constexpr uint32_t kP_KQ = 0;          // 64 KB: K-block b at b*16K: rows 0-63 K, 64-127 Q
-constexpr uint32_t kP_V = 65536;       // 32 KB: column block b at b*8K (64 rows x 128 B)
-constexpr uint32_t kP_TW = 98304;      // 8 KB : T diag(beta gamma), K-major 64 x 64
-constexpr uint32_t kP_TU = 106496;     // 8 KB : T diag(beta)
-constexpr uint32_t kP_A = 114688;      // fp32 [64][65]
-constexpr uint32_t kP_T = kP_A + 64 * 65 * 4;
-constexpr uint32_t kP_X = kP_T + 64 * 65 * 4;   // fp32 [3][256] block temporaries
-constexpr uint32_t kP_G = kP_X + 3 * 256 * 4;   // fp32 [64]
-constexpr uint32_t kP_B = kP_G + 256;           // fp32 [64]
+constexpr uint32_t kP_KQ = 0;          // 64 KB: K-block b at b*16K: rows 0-63 K, 64-127 Q;
+                                       //        V replaces Q once Q is consumed
+constexpr uint32_t kP_A = 65536;       // fp32 [64][65]; afterwards T_w (8 KB) and T_u (8 KB)
+constexpr uint32_t kP_TW = 65536;
+constexpr uint32_t kP_TU = 73728;
+constexpr uint32_t kP_T = kP_A + 64 * 65 * 4;      // fp32 [64][65]
+constexpr uint32_t kP_Y1 = kP_T + 64 * 65 * 4;     // fp32 [2][16][16]
+constexpr uint32_t kP_Y2 = kP_Y1 + 2 * 256 * 4;    // fp32 [32][33]
+constexpr uint32_t kP_G = kP_Y2 + 32 * 33 * 4;     // fp32 [64]
+constexpr uint32_t kP_B = kP_G + 256;              // fp32 [64]
 constexpr uint32_t kP_END = kP_B + 256;
 constexpr uint32_t kPrepSmem = kP_END + 1024;
+constexpr int kLd = 65;                            // row stride of the fp32 64 x 64 tiles
 
-__global__ void __launch_bounds__(kPrepThreads, 1)
+__global__ void __launch_bounds__(kPrepThreads, 2)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ alpha,
                const float* __restrict__ beta, SeqMap map, int32_t H,
@@ -84,7 +96,8 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   uint8_t* sm = align_smem_1024(smem_raw);
   float* sA = (float*)(sm + kP_A);
   float* sT = (float*)(sm + kP_T);
-  float* sX = (float*)(sm + kP_X);
+  float* sY1 = (float*)(sm + kP_Y1);
+  float* sY2 = (float*)(sm + kP_Y2);
   float* sG = (float*)(sm + kP_G);
   float* sB = (float*)(sm + kP_B);
   __shared__ uint64_t bar_kq, bar_v, bar_a, bar_bc;
@@ -97,6 +110,8 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   int64_t t0;
   if (!map.locate(ci, n, t0, L)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, hv = warp >> 2;
+  const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
   uint8_t* img = scratch + (size_t)(ci * H + h) * kImgStride;
 
   if (tid == 0) {
@@ -106,28 +121,31 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     mbar_init(&bar_bc, 1);
     fence_barrier_init();
     s_abort = 0;
-  }
-  if (warp == 0) tmem_alloc(&tmem_base, 256);
-  if (tid < kC) {
-    const bool ok = tid < L;
-    sG[tid] = ok ? logf(alpha[(t0 + tid) * H + h]) : 0.f;
-    sB[tid] = ok ? beta[(t0 + tid) * H + h] : 0.f;
-  }
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_base;
-  if (tid == 0) {
     mbar_arrive_expect_tx(&bar_kq, 65536);
     for (int b = 0; b < 4; ++b) {
       tma_load_3d(sm + kP_KQ + b * 16384, &tm_k, b * 64, h, (int32_t)t0, &bar_kq);
       tma_load_3d(sm + kP_KQ + b * 16384 + 8192, &tm_q, b * 64, h, (int32_t)t0, &bar_kq);
     }
-    mbar_arrive_expect_tx(&bar_v, 32768);
-    for (int b = 0; b < 4; ++b)
-      tma_load_3d(sm + kP_V + b * 8192, &tm_v, b * 64, h, (int32_t)t0, &bar_v);
-    float acc = 0.f;   // decay prefix G_r = sum_{s <= r} log alpha_s
-    for (int r = 0; r < kC; ++r) { acc += sG[r]; sG[r] = acc; }
   }
+  if (warp == 0) tmem_alloc(&tmem_base, 256);
+  // decay prefix G_r = sum_{s <= r} log alpha_s (pad rows: log alpha = 0, beta = 0)
+  float g_scan = 0.f;
+  if (tid < kC) {
+    const bool ok = tid < L;
+    g_scan = ok ? logf(alpha[(t0 + tid) * H + h]) : 0.f;
+    sB[tid] = ok ? beta[(t0 + tid) * H + h] : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, g_scan, o);
+      if (lane >= o) g_scan += y;
+    }
+    if (tid < 32) sG[tid] = g_scan;
+  }
+  for (int e = tid; e < 64 * kLd; e += kPrepThreads) sT[e] = 0.f;
+  __syncthreads();
+  if (tid >= 32 && tid < kC) sG[tid] = g_scan + sG[31];
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
   __syncthreads();
 
   // ---- [K; Q] K^T  ->  TMEM columns [0, 64): lanes 0-63 K K^T, 64-127 Q K^T
@@ -139,11 +157,27 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const uint32_t idesc = idesc_bf16(128, 64, 0, 0);
       const uint32_t base = smem_u32(sm + kP_KQ);
       for (int s = 0; s < 16; ++s) {
-        const uint32_t off = (s >> 2) * 16384u + (s & 3) * 32u;
-        const uint64_t d = smem_desc(base + off, 16, 1024, kSwizzle128B);
+        const uint64_t d = smem_desc(base + (s >> 2) * 16384u + (s & 3) * 32u, 16, 1024,
+                                     kSwizzle128B);
         mma_bf16(tmem, d, d, idesc, s > 0);
       }
       mma_commit(&bar_a);
+    }
+  }
+  {
+    // Q^ = gamma_r Q / sqrt(dk) and K^ = (gamma_L / gamma_r) K, copied out of
+    // the loaded tiles row by row (same swizzled positions)
+    const float GL = sG[L - 1];
+    if (!mbar_wait(&bar_kq, 0)) { s_abort = 1; }
+    for (int e = tid; e < 4 * 64 * 8; e += kPrepThreads) {
+      const int b = e >> 9, r = (e >> 3) & 63, p = e & 7;
+      const float gq = r < L ? kScale * __expf(sG[r]) : 0.f;
+      const float dk = r < L ? __expf(GL - sG[r]) : 0.f;
+      const uint8_t* src = sm + kP_KQ + b * 16384 + r * 128 + p * 16;
+      *reinterpret_cast<uint4*>(img + kImgQ + b * 8192 + r * 128 + p * 16) =
+          scale8(*reinterpret_cast<const uint4*>(src + 8192), gq);
+      *reinterpret_cast<uint4*>(img + kImgK + b * 8192 + r * 128 + p * 16) =
+          scale8(*reinterpret_cast<const uint4*>(src), dk);
     }
   }
   __syncthreads();
@@ -153,53 +187,48 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (s_abort) goto teardown;
   tc_fence_after();
   {
-    uint32_t g0[32], g1[32];
-    tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), g0);
-    tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32, g1);
+    uint32_t g[32];
+    tmem_ld32(tmem + lane_off + 32 * hv, g);
     tmem_ld_wait();
-    const int row = tid;
-    if (row < kC) {   // A = strict_lower(beta_r Gam_rj k_r.k_j)
+    const int row = 32 * quarter + lane;
+    if (row < kC) {   // A = strict_lower(beta_r Gam_rj k_r.k_j), columns 32hv .. 32hv+31
       const float Gr = sG[row], br = sB[row];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const float kk = __uint_as_float(j < 32 ? g0[j] : g1[j - 32]);
-        sA[row * 65 + j] = j < row ? br * __expf(Gr - sG[j]) * kk : 0.f;
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * hv + jj;
+        sA[row * kLd + j] = j < row ? br * __expf(Gr - sG[j]) * __uint_as_float(g[jj]) : 0.f;
       }
-    } else {          // P^ = lower(Gam_rj q_r.k_j) / sqrt(dk), bf16 K-major image
+    } else {          // P^ = lower(Gam_rj q_r.k_j) / sqrt(dk), chunks 4hv .. 4hv+3 of row r
       const int r = row - kC;
       const float Gr = sG[r];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
+      for (int cq = 0; cq < 4; ++cq) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
-          const float q0 = __uint_as_float(j0 < 32 ? g0[j0] : g1[j0 - 32]);
-          const float q1 = __uint_as_float(j1 < 32 ? g0[j1] : g1[j1 - 32]);
-          const float p0 = (j0 <= r && r < L) ? kScale * __expf(Gr - sG[j0]) * q0 : 0.f;
-          const float p1 = (j1 <= r && r < L) ? kScale * __expf(Gr - sG[j1]) * q1 : 0.f;
+          const int j0 = 32 * hv + 8 * cq + 2 * e, j1 = j0 + 1;
+          const float p0 = (j0 <= r && r < L) ? kScale * __expf(Gr - sG[j0]) * __uint_as_float(g[8 * cq + 2 * e]) : 0.f;
+          const float p1 = (j1 <= r && r < L) ? kScale * __expf(Gr - sG[j1]) * __uint_as_float(g[8 * cq + 2 * e + 1]) : 0.f;
           w[e] = pack_bf16(p0, p1);
         }
-        *reinterpret_cast<uint4*>(img + kImgP + sw_chunk(r, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(img + kImgP + sw_chunk(r, 4 * hv + cq)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-    // Q^ = gamma_r Q / sqrt(dk): same swizzled rows as the Q half of the [K; Q] image
-    for (int e = tid; e < 4 * 64 * 8; e += kPrepThreads) {
-      const int b = e >> 9, r = (e >> 3) & 63, p = e & 7;
-      const float sc = r < L ? kScale * __expf(sG[r]) : 0.f;
-      uint4 v = *reinterpret_cast<const uint4*>(sm + kP_KQ + b * 16384 + 8192 + r * 128 + p * 16);
-      v.x = pack_bf16(bf16_lo(v.x) * sc, bf16_hi(v.x) * sc);
-      v.y = pack_bf16(bf16_lo(v.y) * sc, bf16_hi(v.y) * sc);
-      v.z = pack_bf16(bf16_lo(v.z) * sc, bf16_hi(v.z) * sc);
-      v.w = pack_bf16(bf16_lo(v.w) * sc, bf16_hi(v.w) * sc);
-      *reinterpret_cast<uint4*>(img + kImgQ + b * 8192 + r * 128 + p * 16) = v;
-    }
   }
+  // the Q slots are free (MMA done, Q^ copied out): bring V there
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar_v, 32768);
+    for (int b = 0; b < 4; ++b)
+      tma_load_3d(sm + kP_KQ + b * 16384 + 8192, &tm_v, b * 64, h, (int32_t)t0, &bar_v);
+  }
 
-  // ---- T = (I + A)^{-1}, blocked 4 x 4 over 16 x 16 blocks, fp32
-  if (tid < 64) {   // diagonal blocks: thread -> (block b, column c)
+  // ---- T = (I + A)^{-1}: 16 x 16 diagonal inverses, then two levels of
+  //      [[T1, 0], [X, T2]] with X = -T2 A21 T1
+  if (tid < 64) {
     const int b = tid >> 4, c = tid & 15, o = 16 * b;
     float x[16];
 #pragma unroll
@@ -208,46 +237,72 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     for (int r = 1; r < 16; ++r) {
       float acc = 0.f;
 #pragma unroll
-      for (int j = 0; j < r; ++j) acc = fmaf(sA[(o + r) * 65 + o + j], x[j], acc);
+      for (int j = 0; j < r; ++j) acc = fmaf(sA[(o + r) * kLd + o + j], x[j], acc);
       if (r > c) x[r] = -acc;
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) sT[(o + r) * 65 + o + c] = x[r];
+    for (int r = 0; r < 16; ++r) sT[(o + r) * kLd + o + c] = x[r];
   }
   __syncthreads();
-  for (int bi = 1; bi < 4; ++bi) {
-    // X_bj = sum_{k=j}^{bi-1} A_{bi,k} T_{k,j}   for j < bi
-    for (int e = tid; e < bi * 256; e += kPrepThreads) {
-      const int bj = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-      float acc = 0.f;
-      for (int m = 16 * bj; m < 16 * bi; ++m)
-        acc = fmaf(sA[(16 * bi + rr) * 65 + m], sT[m * 65 + 16 * bj + cc], acc);
-      sX[e] = acc;
-    }
-    __syncthreads();
-    // T_{bi,j} = -T_{bi,bi} X_bj
-    for (int e = tid; e < bi * 256; e += kPrepThreads) {
-      const int bj = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-      float acc = 0.f;
+  {  // level 1, blocks p = 0, 1: Y = A[16(2p+1):, 16(2p):] T_{2p};  T_off = -T_{2p+1} Y
+    const int p = tid >> 7, c = tid & 15, r0 = (tid >> 4) & 7;
+    const int ro = 16 * (2 * p + 1), co = 16 * (2 * p);
+    float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-      for (int m = 0; m < 16; ++m)
-        acc = fmaf(sT[(16 * bi + rr) * 65 + 16 * bi + m], sX[bj * 256 + m * 16 + cc], acc);
-      sT[(16 * bi + rr) * 65 + 16 * bj + cc] = -acc;
+    for (int k = 0; k < 16; ++k) {
+      const float t = sT[(co + k) * kLd + co + c];
+      y0 = fmaf(sA[(ro + r0) * kLd + co + k], t, y0);
+      y1 = fmaf(sA[(ro + r0 + 8) * kLd + co + k], t, y1);
     }
+    sY1[p * 256 + r0 * 16 + c] = y0;
+    sY1[p * 256 + (r0 + 8) * 16 + c] = y1;
     __syncthreads();
+    float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float y = sY1[p * 256 + k * 16 + c];
+      z0 = fmaf(sT[(ro + r0) * kLd + ro + k], y, z0);
+      z1 = fmaf(sT[(ro + r0 + 8) * kLd + ro + k], y, z1);
+    }
+    sT[(ro + r0) * kLd + co + c] = -z0;
+    sT[(ro + r0 + 8) * kLd + co + c] = -z1;
   }
-  // T_w = T diag(beta gamma), T_u = T diag(beta): K-major bf16 images (row r, col j)
-  {
-    const int r = tid >> 1, jh = tid & 1;
+  __syncthreads();
+  {  // level 2: Y = A[32:, :32] T[:32, :32];  T[32:, :32] = -T[32:, 32:] Y
+    const int c = tid & 31, r0 = tid >> 5;
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float t = sT[k * kLd + c];
 #pragma unroll
-    for (int cq = 0; cq < 4; ++cq) {
-      const int ch = jh * 4 + cq;
+      for (int m = 0; m < 4; ++m) y[m] = fmaf(sA[(32 + r0 + 8 * m) * kLd + k], t, y[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) sY2[(r0 + 8 * m) * 33 + c] = y[m];
+    __syncthreads();
+    float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float yy = sY2[k * 33 + c];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) z[m] = fmaf(sT[(32 + r0 + 8 * m) * kLd + 32 + k], yy, z[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) sT[(32 + r0 + 8 * m) * kLd + c] = -z[m];
+  }
+  __syncthreads();
+  // T_w = T diag(beta gamma), T_u = T diag(beta): K-major bf16 images over the dead A tile
+  {
+    const int r = tid >> 2, c2 = tid & 3;
+#pragma unroll
+    for (int cq = 0; cq < 2; ++cq) {
+      const int ch = 2 * c2 + cq;
       uint32_t ww[4], uu[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
-        const float t0v = j0 <= r ? sT[r * 65 + j0] : 0.f;
-        const float t1v = j1 <= r ? sT[r * 65 + j1] : 0.f;
+        const float t0v = j0 <= r ? sT[r * kLd + j0] : 0.f;
+        const float t1v = j1 <= r ? sT[r * kLd + j1] : 0.f;
         const float b0 = sB[j0], b1 = sB[j1];
         ww[e] = pack_bf16(t0v * b0 * __expf(sG[j0]), t1v * b1 * __expf(sG[j1]));
         uu[e] = pack_bf16(t0v * b0, t1v * b1);
@@ -266,7 +321,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     } else {
       tc_fence_after();
       const uint32_t idesc = idesc_bf16(128, 64, 1, 0);
-      const uint32_t kq = smem_u32(sm + kP_KQ), v = smem_u32(sm + kP_V);
+      const uint32_t kq = smem_u32(sm + kP_KQ);
       const uint32_t tw = smem_u32(sm + kP_TW), tu = smem_u32(sm + kP_TU);
       for (int hh = 0; hh < 2; ++hh) {
         for (int s = 0; s < 4; ++s)
@@ -274,7 +329,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                    smem_desc(tw + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
         for (int s = 0; s < 4; ++s)
           mma_bf16(tmem + 128 + hh * 64,
-                   smem_desc(v + hh * 16384 + s * 2048, 8192, 1024, kSwizzle128B),
+                   smem_desc(kq + 8192 + hh * 32768 + s * 2048, 16384, 1024, kSwizzle128B),
                    smem_desc(tu + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
       }
       mma_commit(&bar_bc);
@@ -286,26 +341,22 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   __syncthreads();
   if (s_abort) goto teardown;
   tc_fence_after();
+#pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
-    const uint32_t c = 128 * hh + 32 * warp + lane;   // d_k row of W^T / d_v row of U~^T
-    for (int part = 0; part < 2; ++part) {        // 0: W, 1: U~^T
-      uint32_t g0[32], g1[32];
-      const uint32_t col = part * 128 + hh * 64;
-      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + col, g0);
-      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + col + 32, g1);
+    const uint32_t c = 128 * hh + 32 * quarter + lane;   // d_k row of W^T / d_v row of U~^T
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {               // 0: W, 1: U~^T
+      uint32_t g[32];
+      tmem_ld32(tmem + lane_off + part * 128 + hh * 64 + 32 * hv, g);
       tmem_ld_wait();
       uint8_t* dst = img + (part == 0 ? kImgW : kImgU);
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j0 = ch * 8 + 2 * e;
-          const float a0 = __uint_as_float(j0 < 32 ? g0[j0] : g1[j0 - 32]);
-          const float a1 = __uint_as_float(j0 + 1 < 32 ? g0[j0 + 1] : g1[j0 + 1 - 32]);
-          w[e] = pack_bf16(a0, a1);
-        }
-        *reinterpret_cast<uint4*>(dst + sw_chunk(c, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int cq = 0; cq < 4; ++cq) {
+        const uint32_t w0 = pack_bf16(__uint_as_float(g[8 * cq]), __uint_as_float(g[8 * cq + 1]));
+        const uint32_t w1 = pack_bf16(__uint_as_float(g[8 * cq + 2]), __uint_as_float(g[8 * cq + 3]));
+        const uint32_t w2 = pack_bf16(__uint_as_float(g[8 * cq + 4]), __uint_as_float(g[8 * cq + 5]));
+        const uint32_t w3 = pack_bf16(__uint_as_float(g[8 * cq + 6]), __uint_as_float(g[8 * cq + 7]));
+        *reinterpret_cast<uint4*>(dst + sw_chunk(c, 4 * hv + cq)) = make_uint4(w0, w1, w2, w3);
       }
     }
   }
@@ -324,30 +375,28 @@ teardown:
 
 // =========================================================== state kernel
 constexpr int kStateThreads = 256;
-constexpr uint32_t kS_S = 0;          // 64 KB: S bf16, K-major A image, 128 rows x 256
-constexpr uint32_t kS_W = 65536;      // 32 KB
-constexpr uint32_t kS_Q = 98304;      // 32 KB
-constexpr uint32_t kS_K = 131072;     // 32 KB: K, MN-major B image (4 column blocks of 8 KB)
-constexpr uint32_t kS_P = 163840;     // 8 KB
+constexpr uint32_t kS_WQ = 0;         // 2 x 64 KB: [W (32 KB) | Q^ (32 KB)] per buffer
+constexpr uint32_t kS_K = 131072;     // 32 KB: K^, MN-major B image (4 column blocks of 8 KB)
+constexpr uint32_t kS_P = 163840;     // 8 KB : P^
 constexpr uint32_t kS_AU = 172032;    // 16 KB: U^T bf16, K-major A image, 128 rows x 64
 constexpr uint32_t kS_UT = 188416;    // 16 KB: U~^T rows of this half
 constexpr uint32_t kS_O = 204800;     // 16 KB: output staging [64][128] bf16
-constexpr uint32_t kS_END = 221184;
+constexpr uint32_t kS_G = 221184;     // 256 B: G of the chunk
+constexpr uint32_t kS_END = 221440;
 constexpr uint32_t kStateSmem = kS_END + 1024;
-// TMEM columns
-constexpr uint32_t kT_U = 0, kT_O = 64, kT_S = 256;
+// TMEM columns: D_U, D_O (fp32), the bf16 A operand copy of S (2 per column), D_S (fp32)
+constexpr uint32_t kT_U = 0, kT_O = 64, kT_SA = 128, kT_S = 256;
 
 __global__ void __launch_bounds__(kStateThreads, 1)
-tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restrict__ S0,
-                __nv_bfloat16* __restrict__ out, float* __restrict__ S_final, SeqMap map,
-                int32_t H, const uint8_t* __restrict__ scratch, unsigned* status) {
+tc_state_kernel(const float* __restrict__ S0, __nv_bfloat16* __restrict__ out,
+                float* __restrict__ S_final, SeqMap map, int32_t H,
+                const uint8_t* __restrict__ scratch, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align_smem_1024(smem_raw);
-  __shared__ uint64_t bar_wq, bar_k, bar_u, bar_m1, bar_m2;
+  const float* sG = reinterpret_cast<const float*>(sm + kS_G);
+  __shared__ uint64_t bar_wq[2], bar_k, bar_u, bar_m1, bar_m1b, bar_m2, bar_mo;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
-  __shared__ float s_d[64];
-  __shared__ float s_gC;
 
   const int n = blockIdx.x, h = blockIdx.y, half = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -358,17 +407,20 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
   const int64_t s_begin = map.seq_begin(n), s_end = map.seq_end(n);
 
   if (tid == 0) {
-    mbar_init(&bar_wq, 1);
+    mbar_init(&bar_wq[0], 1);
+    mbar_init(&bar_wq[1], 1);
     mbar_init(&bar_k, 1);
     mbar_init(&bar_u, 1);
     mbar_init(&bar_m1, 1);
+    mbar_init(&bar_m1b, 1);
     mbar_init(&bar_m2, 1);
+    mbar_init(&bar_mo, 1);
     fence_barrier_init();
     s_abort = 0;
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
 
-  // master state rows (fp32, registers): this thread's 128 columns of row iloc
+  // master state: this thread's 128 columns of row iloc (fp32, registers)
   float S[128];
   const size_t srow = (((size_t)n * H + h) * kDV + 128 * half + iloc) * kDK + 128 * colhalf;
   if (S0) {
@@ -382,104 +434,86 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
 #pragma unroll
     for (int j = 0; j < 128; ++j) S[j] = 0.f;
   }
-  auto write_S_image = [&]() {
-#pragma unroll
-    for (int q8 = 0; q8 < 16; ++q8) {   // 16 chunks of 8 columns
-      const int kb = 2 * colhalf + (q8 >> 3), ch = q8 & 7;
-      uint4 v = make_uint4(pack_bf16(S[8 * q8], S[8 * q8 + 1]), pack_bf16(S[8 * q8 + 2], S[8 * q8 + 3]),
-                           pack_bf16(S[8 * q8 + 4], S[8 * q8 + 5]), pack_bf16(S[8 * q8 + 6], S[8 * q8 + 7]));
-      *reinterpret_cast<uint4*>(sm + kS_S + kb * 16384 + sw_chunk(iloc, ch)) = v;
-    }
-  };
-  write_S_image();
-  fence_proxy_async_smem();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
+  // bf16 copy of S into TMEM: two packed columns hold four state columns
+  auto store_S_operand = [&]() {
+#pragma unroll
+    for (int hq = 0; hq < 2; ++hq) {
+      uint32_t r[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = pack_bf16(S[64 * hq + 2 * j], S[64 * hq + 2 * j + 1]);
+      tmem_st32(tmem + lane_off + kT_SA + 64 * colhalf + 32 * hq, r);
+    }
+    tmem_st_wait();
+  };
+  store_S_operand();
 
-  auto issue_wqu = [&](int64_t ci) {
-    const uint8_t* src = scratch + (size_t)(ci * H + h) * kImgStride;
-    mbar_arrive_expect_tx(&bar_wq, 65536);
-    tma_load_1d(sm + kS_W, src + kImgW, 32768, &bar_wq);
-    tma_load_1d(sm + kS_Q, src + kImgQ, 32768, &bar_wq);
-    mbar_arrive_expect_tx(&bar_u, 16384);
-    tma_load_1d(sm + kS_UT, src + kImgU + half * 16384, 16384, &bar_u);
+  auto img_of = [&](int64_t ci) { return scratch + (size_t)(ci * H + h) * kImgStride; };
+  auto issue_wq = [&](int64_t ci, int buf) {
+    const uint8_t* src = img_of(ci);
+    mbar_arrive_expect_tx(&bar_wq[buf], 65536);
+    tma_load_1d(sm + kS_WQ + buf * 65536, src + kImgW, 32768, &bar_wq[buf]);
+    tma_load_1d(sm + kS_WQ + buf * 65536 + 32768, src + kImgQ, 32768, &bar_wq[buf]);
   };
   auto issue_kp = [&](int64_t ci) {
-    const uint8_t* src = scratch + (size_t)(ci * H + h) * kImgStride;
-    const int32_t t0 = (int32_t)(s_begin + (ci - cb) * kC);
+    const uint8_t* src = img_of(ci);
     mbar_arrive_expect_tx(&bar_k, 32768 + 8192);
-    for (int b = 0; b < 4; ++b) tma_load_3d(sm + kS_K + b * 8192, &tm_k, b * 64, h, t0, &bar_k);
+    tma_load_1d(sm + kS_K, src + kImgK, 32768, &bar_k);
     tma_load_1d(sm + kS_P, src + kImgP, 8192, &bar_k);
   };
+  auto issue_u = [&](int64_t ci) {
+    const uint8_t* src = img_of(ci);
+    mbar_arrive_expect_tx(&bar_u, 16384 + 256);
+    tma_load_1d(sm + kS_UT, src + kImgU + half * 16384, 16384, &bar_u);
+    tma_load_1d(sm + kS_G, src + kImgG, 256, &bar_u);
+  };
   // outstanding-load bookkeeping (thread 0), for a clean exit after a timeout
-  int pend_wq = 0, pend_k = 0, pend_u = 0;
+  uint32_t pend = 0;   // bit 0/1: wq buffers, bit 2: k, bit 3: u
   if (tid == 0 && cb < ce) {
-    issue_wqu(cb);
+    issue_wq(cb, 0);
+    if (cb + 1 < ce) issue_wq(cb + 1, 1);
     issue_kp(cb);
-    pend_wq = pend_k = pend_u = 1;
+    issue_u(cb);
+    pend = 0xF;
   }
+  tc_fence_before();
+  __syncthreads();
 
   for (int64_t ci = cb; ci < ce; ++ci) {
-    const uint32_t par = (uint32_t)((ci - cb) & 1);
-    const int64_t t0 = s_begin + (ci - cb) * kC;
+    const int64_t it = ci - cb;
+    const uint32_t par = (uint32_t)(it & 1);
+    const int wb = (int)(it & 1);
+    const uint32_t wpar = (uint32_t)((it >> 1) & 1);
+    const int64_t t0 = s_begin + it * kC;
     const int L = (int)min((int64_t)kC, s_end - t0);
-    const float* Gg = reinterpret_cast<const float*>(scratch + (size_t)(ci * H + h) * kImgStride + kImgG);
 
-    // 1. D_U = S W^T, D_O = S Q^^T
+    // 1. D_U = S W^T (commit m1), D_O = S Q^^T (commit m1b); A = S from TMEM
     if (tid == 0) {
-      if (!mbar_wait(&bar_wq, par)) {
+      if (!mbar_wait(&bar_wq[wb], wpar)) {
         s_abort = 1;
       } else {
-        pend_wq = 0;
+        pend &= ~(1u << wb);
         tc_fence_after();
         const uint32_t idW = idesc_bf16(128, 64, 0, 1), idQ = idesc_bf16(128, 64, 0, 0);
-        const uint32_t sS = smem_u32(sm + kS_S), sW = smem_u32(sm + kS_W), sQ = smem_u32(sm + kS_Q);
-        for (int s = 0; s < 16; ++s) {
-          const uint64_t a = smem_desc(sS + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024, kSwizzle128B);
-          mma_bf16(tmem + kT_U, a, smem_desc(sW + s * 2048, 32768, 1024, kSwizzle128B), idW, s > 0);
-          mma_bf16(tmem + kT_O, a,
-                   smem_desc(sQ + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024, kSwizzle128B), idQ,
-                   s > 0);
-        }
+        const uint32_t sW = smem_u32(sm + kS_WQ + wb * 65536), sQ = sW + 32768;
+        for (int s = 0; s < 16; ++s)
+          mma_bf16_ts(tmem + kT_U, tmem + kT_SA + 8 * s,
+                      smem_desc(sW + s * 2048, 32768, 1024, kSwizzle128B), idW, s > 0);
         mma_commit(&bar_m1);
+        for (int s = 0; s < 16; ++s)
+          mma_bf16_ts(tmem + kT_O, tmem + kT_SA + 8 * s,
+                      smem_desc(sQ + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024, kSwizzle128B),
+                      idQ, s > 0);
+        mma_commit(&bar_m1b);
       }
     }
-    // 2. decay factors for this chunk
-    if (tid < kC) {
-      const float GL = Gg[L - 1];
-      s_d[tid] = tid < L ? __expf(GL - Gg[tid]) : 0.f;
-      if (tid == 0) s_gC = __expf(GL);
-    }
-    __syncthreads();
-    if (s_abort) break;
-    // K <- diag(d) K in place (rows r: 8 lanes cover one 128-byte row)
-    if (!mbar_wait(&bar_k, par)) { flag_status(status, GDN_ERR_TIMEOUT); s_abort = 1; }
-    if (tid == 0) pend_k = 0;
-    {
-      const int p = tid & 7, r0 = tid >> 3;
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int r = r0 + 32 * rr;
-        const float d = s_d[r];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          uint4* ptr = reinterpret_cast<uint4*>(sm + kS_K + b * 8192 + r * 128 + p * 16);
-          uint4 v = *ptr;
-          v.x = pack_bf16(bf16_lo(v.x) * d, bf16_hi(v.x) * d);
-          v.y = pack_bf16(bf16_lo(v.y) * d, bf16_hi(v.y) * d);
-          v.z = pack_bf16(bf16_lo(v.z) * d, bf16_hi(v.z) * d);
-          v.w = pack_bf16(bf16_lo(v.w) * d, bf16_hi(v.w) * d);
-          *ptr = v;
-        }
-      }
-    }
-    // 3. U = U~ - D_U  ->  bf16 K-major A image (row iloc, columns r)
+    // 2. U = U~ - D_U  ->  bf16 K-major A image (row iloc, columns r)
     if (!mbar_wait(&bar_m1, par) || !mbar_wait(&bar_u, par)) {
       flag_status(status, GDN_ERR_TIMEOUT);
       s_abort = 1;
     } else {
-      if (tid == 0) pend_u = 0;
       tc_fence_after();
       uint32_t g[32];
       tmem_ld32(tmem + lane_off + kT_U + 32 * colhalf, g);
@@ -491,43 +525,55 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
         const uint32_t uw[4] = {ut.x, ut.y, ut.z, ut.w};
         uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float u0 = bf16_lo(uw[e]) - __uint_as_float(g[8 * cq + 2 * e]);
-          const float u1 = bf16_hi(uw[e]) - __uint_as_float(g[8 * cq + 2 * e + 1]);
-          w[e] = pack_bf16(u0, u1);
-        }
+        for (int e = 0; e < 4; ++e)
+          w[e] = pack_bf16(bf16_lo(uw[e]) - __uint_as_float(g[8 * cq + 2 * e]),
+                           bf16_hi(uw[e]) - __uint_as_float(g[8 * cq + 2 * e + 1]));
         *reinterpret_cast<uint4*>(sm + kS_AU + sw_chunk(iloc, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
+    const float gC = __expf(sG[L - 1]);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     if (s_abort) break;
+    if (tid == 0) pend &= ~8u;
 
-    // 4. D_S = U^T (d K) ; D_O += U^T P^^T ; prefetch the next chunk's W, Q^, U~^T
+    // 3. D_S = U^T K^ (commit m2) ; D_O += U^T P^^T (commit mo); prefetches
     if (tid == 0) {
-      tc_fence_after();
-      const uint32_t id2 = idesc_bf16(128, 256, 0, 1), idO = idesc_bf16(128, 64, 0, 0);
-      const uint32_t sAU = smem_u32(sm + kS_AU), sK = smem_u32(sm + kS_K), sP = smem_u32(sm + kS_P);
-      for (int s = 0; s < 4; ++s) {
-        const uint64_t a = smem_desc(sAU + s * 32, 16, 1024, kSwizzle128B);
-        mma_bf16(tmem + kT_S, a, smem_desc(sK + s * 2048, 8192, 1024, kSwizzle128B), id2, s > 0);
-        mma_bf16(tmem + kT_O, a, smem_desc(sP + s * 32, 16, 1024, kSwizzle128B), idO, 1);
-      }
-      mma_commit(&bar_m2);
-      if (ci + 1 < ce) {
-        issue_wqu(ci + 1);
-        pend_wq = pend_u = 1;
+      if (!mbar_wait(&bar_k, par)) {
+        s_abort = 1;
+      } else {
+        pend &= ~4u;
+        tc_fence_after();
+        const uint32_t id2 = idesc_bf16(128, 256, 0, 1), idO = idesc_bf16(128, 64, 0, 0);
+        const uint32_t sAU = smem_u32(sm + kS_AU), sK = smem_u32(sm + kS_K), sP = smem_u32(sm + kS_P);
+        for (int s = 0; s < 4; ++s)
+          mma_bf16(tmem + kT_S, smem_desc(sAU + s * 32, 16, 1024, kSwizzle128B),
+                   smem_desc(sK + s * 2048, 8192, 1024, kSwizzle128B), id2, s > 0);
+        mma_commit(&bar_m2);
+        for (int s = 0; s < 4; ++s)
+          mma_bf16(tmem + kT_O, smem_desc(sAU + s * 32, 16, 1024, kSwizzle128B),
+                   smem_desc(sP + s * 32, 16, 1024, kSwizzle128B), idO, 1);
+        mma_commit(&bar_mo);
+        if (ci + 1 < ce) { issue_u(ci + 1); pend |= 8u; }
+        // this W / Q^ buffer is free once both MMA-1 halves are done
+        if (ci + 2 < ce) {
+          if (!mbar_wait(&bar_m1b, par)) {
+            s_abort = 1;
+          } else {
+            issue_wq(ci + 2, wb);
+            pend |= 1u << wb;
+          }
+        }
       }
     }
 
-    // 5. S = gamma_L S + D_S (fp32) -> bf16 image; O -> staging
+    // 4. S = gamma_L S + D_S (fp32) -> bf16 operand copy in TMEM; O -> staging
     if (!mbar_wait(&bar_m2, par)) {
       flag_status(status, GDN_ERR_TIMEOUT);
       s_abort = 1;
     } else {
       tc_fence_after();
-      const float gC = s_gC;
 #pragma unroll
       for (int g4 = 0; g4 < 4; ++g4) {
         uint32_t g[32];
@@ -536,24 +582,29 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
 #pragma unroll
         for (int j = 0; j < 32; ++j) S[32 * g4 + j] = fmaf(gC, S[32 * g4 + j], __uint_as_float(g[j]));
       }
-      write_S_image();
-      uint32_t g[32];
-      tmem_ld32(tmem + lane_off + kT_O + 32 * colhalf, g);
-      tmem_ld_wait();
-      __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(sm + kS_O);
+      store_S_operand();
+      if (!mbar_wait(&bar_mo, par)) {
+        flag_status(status, GDN_ERR_TIMEOUT);
+        s_abort = 1;
+      } else {
+        tc_fence_after();
+        uint32_t g[32];
+        tmem_ld32(tmem + lane_off + kT_O + 32 * colhalf, g);
+        tmem_ld_wait();
+        __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(sm + kS_O);
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        so[(32 * colhalf + j) * 128 + iloc] = __float2bfloat16_rn(__uint_as_float(g[j]));
+        for (int j = 0; j < 32; ++j)
+          so[(32 * colhalf + j) * 128 + iloc] = __float2bfloat16_rn(__uint_as_float(g[j]));
+      }
     }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     if (s_abort) break;
 
-    // 6. prefetch the next chunk's K and P^; write this chunk's rows of out
+    // 5. prefetch the next chunk's K^ and P^; write this chunk's rows of out
     if (tid == 0 && ci + 1 < ce) {
       issue_kp(ci + 1);
-      pend_k = 1;
+      pend |= 4u;
     }
     {
       const int r = tid >> 2, seg = tid & 3;
@@ -573,9 +624,11 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
   }
   if (tid == 0 && s_abort) {   // let copies still in flight land before the CTA exits
     flag_status(status, GDN_ERR_TIMEOUT);
-    if (pend_wq) mbar_wait(&bar_wq, 0, 100000000ull), mbar_wait(&bar_wq, 1, 100000000ull);
-    if (pend_k) mbar_wait(&bar_k, 0, 100000000ull), mbar_wait(&bar_k, 1, 100000000ull);
-    if (pend_u) mbar_wait(&bar_u, 0, 100000000ull), mbar_wait(&bar_u, 1, 100000000ull);
+    const uint64_t lim = 100000000ull;
+    for (int b = 0; b < 2; ++b)
+      if (pend & (1u << b)) { mbar_wait(&bar_wq[b], 0, lim); mbar_wait(&bar_wq[b], 1, lim); }
+    if (pend & 4u) { mbar_wait(&bar_k, 0, lim); mbar_wait(&bar_k, 1, lim); }
+    if (pend & 8u) { mbar_wait(&bar_u, 0, lim); mbar_wait(&bar_u, 1, lim); }
   }
   tc_fence_before();
   __syncthreads();
@@ -646,8 +699,7 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
   }
   if (prep_only) return cudaSuccess;
   tc_state_kernel<<<dim3((unsigned)a.map.N, (unsigned)a.H, 2), kStateThreads, kStateSmem,
-                    stream>>>(tk, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr,
-                              a.status);
+                    stream>>>(a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr, a.status);
   count_launches(1);
   return cudaGetLastError();
 }

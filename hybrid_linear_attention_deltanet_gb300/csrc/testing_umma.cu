@@ -52,28 +52,43 @@ __global__ void __launch_bounds__(128) umma_gemm_kernel(UmmaArgs a,
     mbar_init(&bar_tma, 1);
     fence_barrier_init();
   }
-  if (warp == 0) tmem_alloc(&tmem_base, a.N < 32 ? 32 : a.N);
+  if (warp == 0) tmem_alloc(&tmem_base, 512);
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
+  const uint32_t a_tmem = tmem + 256;   // A operand columns when staged in TMEM (mode 2)
 
   // stage B (and A unless TMA) by threads
   for (int e = tid; e < a.N * a.K; e += blockDim.x) {
     const int n = e / a.K, k = e % a.K;
     *(__nv_bfloat16*)(imgB + image_offset(a.b_mn, a.N, a.K, n, k)) = a.B[e];
   }
-  if (!a.a_via_tma) {
+  if (a.a_via_tma == 2) {   // row m -> TMEM lane m, K pairs packed per column
+    for (int c0 = 0; c0 < a.K / 2; c0 += 32) {
+      uint32_t r[32];
+      const __nv_bfloat16* row = a.A + (size_t)tid * a.K + 2 * c0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t lo = __bfloat16_as_ushort(row[2 * j]);
+        const uint32_t hi = __bfloat16_as_ushort(row[2 * j + 1]);
+        r[j] = lo | (hi << 16);
+      }
+      tmem_st32(a_tmem + ((uint32_t)(warp * 32) << 16) + c0, r);
+    }
+    tmem_st_wait();
+  } else if (!a.a_via_tma) {
     for (int e = tid; e < 128 * a.K; e += blockDim.x) {
       const int m = e / a.K, k = e % a.K;
       *(__nv_bfloat16*)(imgA + image_offset(a.a_mn, 128, a.K, m, k)) = a.A[e];
     }
   }
   fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
 
   bool ok = true;
   if (tid == 0) {
-    if (a.a_via_tma) {
+    if (a.a_via_tma == 1) {
       mbar_arrive_expect_tx(&bar_tma, 128 * a.K * 2);
       for (int b = 0; b < a.K / 64; ++b) tma_load_2d(imgA + b * 128 * 128, &tmA, b * 64, 0, &bar_tma);
       ok = mbar_wait(&bar_tma, 0);
@@ -85,8 +100,12 @@ __global__ void __launch_bounds__(128) umma_gemm_kernel(UmmaArgs a,
       for (int s = 0; s < a.K / 16; ++s) {
         const uint32_t oa = a.a_mn ? s * 2048u : (s / 4) * (128u * 128u) + (s % 4) * 32u;
         const uint32_t ob = a.b_mn ? s * 2048u : (s / 4) * (uint32_t)(a.N * 128) + (s % 4) * 32u;
-        mma_bf16(tmem, smem_desc(sa + oa, a.a_lbo, a.a_sbo, kSwizzle128B),
-                 smem_desc(sb + ob, a.b_lbo, a.b_sbo, kSwizzle128B), idesc, s > 0);
+        if (a.a_via_tma == 2)
+          mma_bf16_ts(tmem, a_tmem + 8 * s, smem_desc(sb + ob, a.b_lbo, a.b_sbo, kSwizzle128B),
+                      idesc, s > 0);
+        else
+          mma_bf16(tmem, smem_desc(sa + oa, a.a_lbo, a.a_sbo, kSwizzle128B),
+                   smem_desc(sb + ob, a.b_lbo, a.b_sbo, kSwizzle128B), idesc, s > 0);
       }
       mma_commit(&bar_mma);
     }
@@ -110,7 +129,7 @@ __global__ void __launch_bounds__(128) umma_gemm_kernel(UmmaArgs a,
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, a.N < 32 ? 32 : a.N);
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // furthest byte (exclusive) an MMA of this operand can read from its start
@@ -133,7 +152,7 @@ extern "C" int gdn_testing_umma_gemm(const void* A, const void* B, float* D, int
   if (!A || !B || !D) return GDN_ERR_INVALID_ARG;
   if (N < 16 || N > 256 || N % 16 || K < 64 || K > 256 || K % 64) return GDN_ERR_UNSUPPORTED;
   if ((N & (N - 1)) && N != 192) return GDN_ERR_UNSUPPORTED;   // TMEM allocation size
-  if (a_via_tma && a_mn) return GDN_ERR_UNSUPPORTED;
+  if (a_via_tma < 0 || a_via_tma > 2 || (a_via_tma && a_mn)) return GDN_ERR_UNSUPPORTED;
   const uint32_t a_bytes = 128u * K * 2, b_bytes = (uint32_t)N * K * 2;
   const uint32_t b_off = (a_bytes + 1023u) / 1024u * 1024u;
   // every descriptor must stay inside the shared-memory allocation
@@ -143,7 +162,7 @@ extern "C" int gdn_testing_umma_gemm(const void* A, const void* B, float* D, int
     return GDN_ERR_INVALID_ARG;
   CUtensorMap tm;
   memset(&tm, 0, sizeof tm);
-  if (a_via_tma) {
+  if (a_via_tma == 1) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,

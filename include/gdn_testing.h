@@ -29,7 +29,10 @@ extern "C" {
  *                 R*128 bytes apart (R = 128 for A, N for B).
  *   *_lbo/*_sbo : leading / stride byte offsets written into the matrix
  *                 descriptors (so a test can check the convention).
- *   a_via_tma   : load A (K-major only) with a 2-D TMA tensor copy.
+ *   a_via_tma   : 0: threads stage A in shared memory; 1: a 2-D TMA tensor
+ *                 copy loads A (K-major only); 2: A is stored into TMEM
+ *                 (row m in lane m, two K elements per 32-bit column, the
+ *                 lower half holding the even one) and the MMA reads it there.
  * 16 <= N <= 256 (N a multiple of 16 and a power of two, or 192);
  * K in {64, 128, 192, 256}.  Returns GDN_ERR_INVALID_ARG when a descriptor
  * could reach outside the kernel's shared-memory allocation.
@@ -50,9 +53,10 @@ int gdn_testing_umma_gemm(const void* A, const void* B, float* D, int32_t N, int
  *   +0       W      (64 x 256): 256 rows of 128 B; row c = W[0..63][c]
  *   +32768   Q^     (64 x 256): 4 blocks of 64 rows x 128 B; block b, row r
  *                               = Q^[r][64b .. 64b+63]  (Q^ = gamma Q / sqrt(dk))
- *   +65536   P^     (64 x 64) : 64 rows of 128 B (lower(Gam Q K^T) / sqrt(dk))
- *   +73728   U~^T  (256 x 64) : row i = U~[0..63][i]
- *   +106496  G      (64 fp32) : cumulative log decay within the chunk
+ *   +65536   K^     (64 x 256): same block layout; K^ = diag(gamma_L / gamma) K
+ *   +98304   P^     (64 x 64) : 64 rows of 128 B (lower(Gam Q K^T) / sqrt(dk))
+ *   +106496  U~^T  (256 x 64) : row i = U~[0..63][i]
+ *   +139264  G      (64 fp32) : cumulative log decay within the chunk
  * Every 128-byte row r stores its 16-byte chunk j at position j XOR (r % 8).
  * Other arguments as for gdn_prefill with io_dtype = GDN_BF16.
  */

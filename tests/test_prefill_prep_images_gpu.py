@@ -34,14 +34,19 @@ def _rows(buf, nrows):
     return (logical.reshape(nrows, 64).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def _blocks(img, off):
+    return np.concatenate([_rows(img[off + b * 8192:off + (b + 1) * 8192], 64)
+                           for b in range(4)], axis=1)    # [64][256]
+
+
 def _decode(img):
     W = _rows(img[0:32768], 256).T                        # [64 r][256 c]
-    Q = np.concatenate([_rows(img[32768 + b * 8192:32768 + (b + 1) * 8192], 64)
-                        for b in range(4)], axis=1)       # [64][256]
-    P = _rows(img[65536:65536 + 8192], 64)                # [64][64]
-    Ut = _rows(img[73728:73728 + 32768], 256).T           # [64 r][256 i]
-    G = img[106496:106496 + 256].view(np.float32).astype(np.float64)
-    return W, Q, P, Ut, G
+    Q = _blocks(img, 32768)
+    K = _blocks(img, 65536)
+    P = _rows(img[98304:98304 + 8192], 64)                # [64][64]
+    Ut = _rows(img[106496:106496 + 32768], 256).T         # [64 r][256 i]
+    G = img[139264:139264 + 256].view(np.float32).astype(np.float64)
+    return W, Q, K, P, Ut, G
 
 
 def _model_chunk(q, k, v, a, b):
@@ -55,7 +60,8 @@ def _model_chunk(q, k, v, a, b):
     Ut = T @ (b[:, None] * v)
     P = np.tril(Gam * (q @ k.T)) / 16.0
     Qh = g[:, None] * q / 16.0
-    return W, Qh, P, Ut, G
+    Kh = np.exp(G[-1] - G)[:, None] * k
+    return W, Qh, Kh, P, Ut, G
 
 
 def rel(x, y):
@@ -93,16 +99,20 @@ def test_prep_images_match_chunk_algebra(gdn_lib, lens, varlen):
             L = min(C, Ln - c0)
             for h in range(H):
                 img = img_all[(ci * H + h) * stride:(ci * H + h + 1) * stride]
-                W, Q, P, Ut, G = _decode(img)
+                W, Q, K, P, Ut, G = _decode(img)
                 sl = slice(t0, t0 + L)
-                Wm, Qm, Pm, Um, Gm = _model_chunk(q[sl, h], k[sl, h], v[sl, h], al[sl, h], be[sl, h])
-                errs = dict(W=rel(W[:L], Wm), Q=rel(Q[:L], Qm), P=rel(P[:L, :L], Pm),
-                            U=rel(Ut[:L], Um), G=float(np.abs(G[:L] - Gm).max()))
+                Wm, Qm, Km, Pm, Um, Gm = _model_chunk(q[sl, h], k[sl, h], v[sl, h], al[sl, h],
+                                                      be[sl, h])
+                errs = dict(W=rel(W[:L], Wm), Q=rel(Q[:L], Qm), K=rel(K[:L], Km),
+                            P=rel(P[:L, :L], Pm), U=rel(Ut[:L], Um),
+                            G=float(np.abs(G[:L] - Gm).max()))
                 for key, val in errs.items():
                     worst[key] = max(worst.get(key, 0.0), val)
                 # rows past the chunk's end must not write anything
                 assert np.all(W[L:] == 0) and np.all(Ut[L:] == 0) and np.all(Q[L:] == 0)
+                assert np.all(K[L:] == 0) and np.all(P[L:] == 0)
             ci += 1
     print("worst relative errors:", worst)
-    assert worst["W"] < 2e-2 and worst["U"] < 2e-2 and worst["P"] < 2e-2 and worst["Q"] < 1e-2
+    assert worst["W"] < 2e-2 and worst["U"] < 2e-2 and worst["P"] < 2e-2
+    assert worst["Q"] < 1e-2 and worst["K"] < 1e-2
     assert worst["G"] < 1e-4

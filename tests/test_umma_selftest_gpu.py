@@ -71,3 +71,17 @@ def test_umma_tma_staged_operand(gdn_lib, N, K):
     rc, D = _run(f, A, B, 0, 1, _desc(0, 128, K), _desc(1, N, K), tma=1)
     assert rc == 0 and gdn_lib.device_status() == 0
     assert float((D - ref).abs().max() / ref.abs().max()) < 1e-5
+
+
+@pytest.mark.parametrize("N,K", [(64, 256), (256, 64), (128, 128)])
+@pytest.mark.parametrize("b_mn", [0, 1])
+def test_umma_a_operand_in_tmem(gdn_lib, N, K, b_mn):
+    """A operand read from tensor memory (row per lane, K pairs per column)."""
+    f = _fn(gdn_lib.load())
+    g = torch.Generator(device="cuda").manual_seed(3 + N + K + b_mn)
+    A = torch.randn(128, K, device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, device="cuda", generator=g).to(torch.bfloat16)
+    ref = A.float() @ B.float().T
+    rc, D = _run(f, A, B, 0, b_mn, _desc(0, 128, K), _desc(b_mn, N, K), tma=2)
+    assert rc == 0 and gdn_lib.device_status() == 0
+    assert float((D - ref).abs().max() / ref.abs().max()) < 1e-5
