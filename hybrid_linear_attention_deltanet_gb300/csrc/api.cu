@@ -265,6 +265,7 @@ const char* gdn_status_string(int s) {
     case GDN_ERR_CUDA: return "CUDA runtime error";
     case GDN_ERR_TIMEOUT: return "device: bounded wait timed out";
     case GDN_ERR_BAD_SEQLENS: return "device: malformed cu_seqlens";
+    case GDN_ERR_SCRATCH_LIMIT: return "problem needs more than the 64 MiB static no-allocation scratch";
     default: return "unknown status";
   }
 }

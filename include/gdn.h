@@ -59,7 +59,9 @@ enum gdn_status {
   GDN_ERR_ALIGNMENT = 3,     /* a pointer is not aligned as the conventions require */
   GDN_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
   GDN_ERR_TIMEOUT = 5,       /* device: a bounded wait inside a kernel gave up */
-  GDN_ERR_BAD_SEQLENS = 6    /* device: cu_seqlens not 0 = cu[0] <= ... <= cu[N] = T_total */
+  GDN_ERR_BAD_SEQLENS = 6,   /* device: cu_seqlens not 0 = cu[0] <= ... <= cu[N] = T_total */
+  GDN_ERR_SCRATCH_LIMIT = 7  /* gdn_prefill_noalloc: the problem needs more scratch than its
+                                static buffer holds */
 };
 
 /*
@@ -98,6 +100,39 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
                 const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
                 float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
                 int32_t dv, int32_t io_dtype, gdn_stream_t stream);
+
+/*
+ * gdn_prefill_noalloc -- gdn_prefill for callers that cannot allocate.
+ *
+ * The pages have no counterpart: this is a deployment variant of the same
+ * computation.  gdn_prefill takes its scratch with cudaMallocAsync on the
+ * caller's stream.  Callers that must not allocate device memory while they
+ * run -- serving loops that fix their memory footprint at start-up so that
+ * no request can fail on an allocation or fragment the pool, processes whose
+ * device memory belongs to another allocator that forbids raw CUDA
+ * allocations, runtimes with a static memory budget -- call this instead.
+ * It takes the same arguments, runs the same kernels and returns the same
+ * results, and calls no allocator: its scratch is one static device array of
+ * 64 MiB (enough for about 5000 tokens of a 6-head bf16 layer, or about 4800
+ * with fp32 I/O), which every GPU that loads the library holds until the
+ * process exits.
+ *
+ *  - A problem whose scratch would exceed 64 MiB is rejected with
+ *    GDN_ERR_SCRATCH_LIMIT before anything is launched.
+ *  - The first call on a device looks up that device's copy of the array
+ *    (with the device current); make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the one array and leaves its contents
+ *    behind.  No part of it has to start at zero: every byte a call reads is
+ *    written earlier in the same call.  Calls whose executions overlap on the
+ *    GPU (different streams, no ordering between them) race on the array and
+ *    give undefined results; order them on one stream or with events.
+ */
+int gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float* alpha,
+                        const float* beta, const float* S0, const int32_t* cu_seqlens,
+                        void* out, float* S_final, int32_t batch, int64_t seqlen,
+                        int32_t heads, int32_t dk, int32_t dv, int32_t io_dtype,
+                        gdn_stream_t stream);
 
 /*
  * gdn_decode_step -- one generated token for each of `batch` independent
