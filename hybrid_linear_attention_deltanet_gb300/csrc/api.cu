@@ -158,7 +158,9 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
 
   const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
   const bool tc = io_dtype == GDN_BF16;
-  const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads)
+  a.allow_waves = true;
+  const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads) +
+                                     prefill_tc_wave_state_bytes(a)
                                : prefill_simt_scratch_bytes(a.max_chunks, heads);
   void* scratch = nullptr;
   if (off_bytes + work_bytes > 0 &&
@@ -237,6 +239,11 @@ int gdn_testing_prefill_prep(const void* q, const void* k, const void* v, const 
 }
 
 size_t gdn_testing_prefill_image_stride(void) { return prefill_tc_image_stride(); }
+
+void gdn_testing_set_trace(uint64_t* device_buf, int32_t max_chunks) {
+  g_trace = device_buf;
+  g_trace_chunks = device_buf ? (max_chunks < 256 ? max_chunks : 256) : 0;
+}
 
 int gdn_get_device_status(gdn_stream_t stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;

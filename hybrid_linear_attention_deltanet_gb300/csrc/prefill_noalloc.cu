@@ -17,9 +17,9 @@
 namespace gdn {
 namespace {
 
-// 64 MiB: room for 478 (chunk, head) units of 64 tokens on the bf16
-// tensor-core path (about 5000 tokens of a 6-head layer) and about 450 on the
-// fp32 path.
+// 64 MiB: room for 624 (chunk, head) units of 64 tokens on the bf16
+// tensor-core path (about 6600 tokens of a 6-head layer) and about 450 on the
+// fp32 path (about 4800 tokens).
 constexpr size_t kNoAllocScratchBytes = 64ull << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -8,22 +8,24 @@
 // alpha), gamma = exp(G), Gam_rj = exp(G_r - G_j), d_r = gamma_L / gamma_r:
 //   A  = strict_lower(beta_r Gam_rj k_r.k_j),   T = (I + A)^{-1}
 //   W  = T diag(beta gamma) K,  U~ = T diag(beta) V,  P^ = lower(Gam Q K^T)/sqrt(dk)
-//   Q^ = diag(gamma) Q / sqrt(dk),   K^ = diag(d) K
-//   U  = U~ - W S^T,  O = Q^ S^T + P^ U,  S' = gamma_L S + U^T K^
+//   Q^ = diag(gamma) Q / sqrt(dk)
+//   U  = U~ - W S^T,  O = Q^ S^T + P^ U,  S' = gamma_L S + (diag(d) U)^T K
 //
 // Kernel 1, tc_prep (one CTA per (chunk, head), fully parallel, two CTAs per SM):
 //   TMA tensor copies of the K, Q, V tiles; [K;Q] K^T on tcgen05 (M=128, N=64,
 //   K=256) -> A and P^; T by a two-level recursive block inverse in fp32 on
 //   the CUDA cores; W^T = K^T T_w^T and U~^T = V^T T_u^T on tcgen05; writes
-//   W, Q^, K^, P^, U~^T and G to scratch as ready-to-load swizzled operand
-//   images (the state pass copies them with 1-D TMA bulk copies).
+//   W, Q^, P^, U~^T and G to scratch as ready-to-load swizzled operand images
+//   (the state pass copies them with 1-D TMA bulk copies).
 // Kernel 2, tc_state (one CTA per (sequence, head, 128-row half of S)):
 //   rows of S are independent, so each CTA owns 128 rows (the MMA M).  The
-//   bf16 copy of its S rows lives in TMEM as the A operand; the fp32 master
+//   bf16 copy of its S rows lives in TMEM as an A operand; the fp32 master
 //   copy lives in registers.  Per chunk: D_U = S W^T, D_O = S Q^^T (M=128,
-//   N=64, K=256, A from TMEM); U = U~ - D_U -> bf16; D_S = U^T K^ (N=256,
-//   K=64) and D_O += U^T P^^T; S = gamma_L S + D_S; O -> out.  W and Q^ are
-//   double-buffered (fetched two chunks ahead), the rest one chunk ahead.
+//   N=64, K=256, A from TMEM); U = U~ - D_U and d*U -> bf16, stored back into
+//   TMEM as A operands; D_S = (dU)^T K (N=256, K=64, K straight from the
+//   input by a TMA tensor copy) and D_O += U^T P^^T; S = gamma_L S + D_S;
+//   O -> out.  W, Q^, K and P^ are double-buffered (two chunks ahead), the
+//   images of the chunk after are pre-warmed in L2.
 //
 // Shared-memory operand images use the 128-byte swizzle: rows of 64 bf16,
 // 16-byte chunk index XOR (row % 8), 8-row groups 1024 bytes apart.
@@ -33,6 +35,7 @@
 #include <cuda.h>
 
 #include <cstring>
+#include <mutex>
 
 #include "gdn_internal.cuh"
 #include "sm100_ptx.cuh"
@@ -44,12 +47,21 @@ using namespace sm100;
 
 // ---- scratch image per (chunk, head)
 constexpr size_t kImgW = 0;           // W   : MN-major B image, 256 K-rows (c) x 64 (r)
-constexpr size_t kImgQ = 32768;       // Q^  : K-major B image, 4 K-blocks x (64 rows x 128 B)
-constexpr size_t kImgK = 65536;       // K^  : MN-major B image, 4 column blocks x (64 rows x 128 B)
-constexpr size_t kImgP = 98304;       // P^  : K-major B image, 64 rows x 64
-constexpr size_t kImgU = 106496;      // U~^T: 256 rows (i) x 64 (r), 128-byte swizzled rows
-constexpr size_t kImgG = 139264;      // G   : 64 fp32
-constexpr size_t kImgStride = 140288;
+constexpr size_t kImgQ = 32768;       // Q^  : MN-major B image, 256 K-rows (c) x 64 (r), right
+                                      //       after W so that [W | Q^] is one N = 128 operand
+constexpr size_t kImgP = 65536;       // P^  : K-major B image, 64 rows x 64
+// per 128-row half h of S: U~^T rows [128h, 128h+128) (128-byte swizzled,
+// 16 KB) followed by the chunk's decay block (512 B: d_r = gamma_L / gamma_r
+// for r < L else 0, then G_r), so that one bulk copy brings both
+constexpr size_t kImgU0 = 73728;
+constexpr size_t kImgHalf = 16896;    // 16384 + 512
+constexpr size_t kImgDecay = 16384;   // offset of the decay block inside a half
+constexpr size_t kImgStride = 107520; // kImgU0 + 2 * kImgHalf, rounded to 1 KB
+
+// chunk-position waves (see launch_prefill_tc)
+constexpr int kMaxWaves = 8;
+constexpr int64_t kWaveMinChunks = 32;      // chunk positions per wave, at least
+constexpr int64_t kWaveMaxStateCtas = 120;  // leave SMs free for the overlapping prep
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
@@ -83,15 +95,19 @@ constexpr uint32_t kP_Y1 = kP_T + 64 * 65 * 4;     // fp32 [2][16][16]
 constexpr uint32_t kP_Y2 = kP_Y1 + 2 * 256 * 4;    // fp32 [32][33]
 constexpr uint32_t kP_G = kP_Y2 + 32 * 33 * 4;     // fp32 [64]
 constexpr uint32_t kP_B = kP_G + 256;              // fp32 [64]
-constexpr uint32_t kP_END = kP_B + 256;
+constexpr uint32_t kP_GAM = kP_B + 256;            // fp32 [64]: gamma_r = exp(G_r)
+constexpr uint32_t kP_END = kP_GAM + 256;
 constexpr uint32_t kPrepSmem = kP_END + 1024;
 constexpr int kLd = 65;                            // row stride of the fp32 64 x 64 tiles
+constexpr int kPrepTraceOffset = 4096;             // uint64 slots before the prep timeline
+constexpr int kWaveTraceOffset = 3072;             // per-wave launch timeline (global timer)
 
 __global__ void __launch_bounds__(kPrepThreads, 2)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ alpha,
                const float* __restrict__ beta, SeqMap map, int32_t H,
-               uint8_t* __restrict__ scratch, unsigned* status) {
+               uint8_t* __restrict__ scratch, unsigned* status, uint64_t* __restrict__ trace,
+               int32_t win_p0, int32_t win_np, uint64_t* __restrict__ wave_trace, int32_t wave) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align_smem_1024(smem_raw);
   float* sA = (float*)(sm + kP_A);
@@ -100,11 +116,16 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   float* sY2 = (float*)(sm + kP_Y2);
   float* sG = (float*)(sm + kP_G);
   float* sB = (float*)(sm + kP_B);
+  float* sGam = (float*)(sm + kP_GAM);
   __shared__ uint64_t bar_kq, bar_v, bar_a, bar_bc;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
 
-  const int64_t ci = blockIdx.x;
+  // win_np > 0 (dense batches): this launch covers chunk positions
+  // [win_p0, win_p0 + win_np) of every sequence; otherwise every chunk
+  const int64_t ci = win_np > 0 ? (int64_t)(blockIdx.x / win_np) * map.chunks_per_seq + win_p0 +
+                                      blockIdx.x % win_np
+                                : (int64_t)blockIdx.x;
   const int h = blockIdx.y;
   int n, L;
   int64_t t0;
@@ -113,6 +134,15 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int quarter = warp & 3, hv = warp >> 2;
   const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
   uint8_t* img = scratch + (size_t)(ci * H + h) * kImgStride;
+  // optional phase timeline (test hook): thread 0 of CTA (0, 0) stamps its
+  // SM cycle counter at 10 points
+  const bool tracing = trace && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0;
+  auto stamp = [&](int k) {
+    if (tracing) trace[k] = clock64();
+  };
+  stamp(0);
+  if (wave_trace && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+    wave_trace[100 + 2 * wave] = globaltimer_ns();
 
   if (tid == 0) {
     mbar_init(&bar_kq, 1);
@@ -144,9 +174,11 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   for (int e = tid; e < 64 * kLd; e += kPrepThreads) sT[e] = 0.f;
   __syncthreads();
   if (tid >= 32 && tid < kC) sG[tid] = g_scan + sG[31];
+  if (tid < kC) sGam[tid] = __expf(tid < 32 ? g_scan : g_scan + sG[31]);
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   __syncthreads();
+  stamp(1);
 
   // ---- [K; Q] K^T  ->  TMEM columns [0, 64): lanes 0-63 K K^T, 64-127 Q K^T
   if (tid == 0) {
@@ -165,26 +197,38 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
   }
   {
-    // Q^ = gamma_r Q / sqrt(dk) and K^ = (gamma_L / gamma_r) K, copied out of
-    // the loaded tiles row by row (same swizzled positions)
-    const float GL = sG[L - 1];
+    // Q^ = gamma_r Q / sqrt(dk), transposed into an MN-major image (row c =
+    // Q^[0..63][c]) so that it sits beside W as one N = 128 operand
     if (!mbar_wait(&bar_kq, 0)) { s_abort = 1; }
-    for (int e = tid; e < 4 * 64 * 8; e += kPrepThreads) {
-      const int b = e >> 9, r = (e >> 3) & 63, p = e & 7;
-      const float gq = r < L ? kScale * __expf(sG[r]) : 0.f;
-      const float dk = r < L ? __expf(GL - sG[r]) : 0.f;
-      const uint8_t* src = sm + kP_KQ + b * 16384 + r * 128 + p * 16;
-      *reinterpret_cast<uint4*>(img + kImgQ + b * 8192 + r * 128 + p * 16) =
-          scale8(*reinterpret_cast<const uint4*>(src + 8192), gq);
-      *reinterpret_cast<uint4*>(img + kImgK + b * 8192 + r * 128 + p * 16) =
-          scale8(*reinterpret_cast<const uint4*>(src), dk);
+    {
+      const int c = tid;   // d_k column, 0..255
+      const uint8_t* qb = sm + kP_KQ + (c >> 6) * 16384 + 8192;
+      const uint32_t cc = c & 63;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r0 = 8 * ch + 2 * e, r1 = r0 + 1;
+          const float q0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+              qb + r0 * 128 + ((((cc >> 3) ^ (r0 & 7)) << 4) | ((cc & 7) << 1))));
+          const float q1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+              qb + r1 * 128 + ((((cc >> 3) ^ (r1 & 7)) << 4) | ((cc & 7) << 1))));
+          const float g0 = r0 < L ? kScale * sGam[r0] : 0.f;
+          const float g1 = r1 < L ? kScale * sGam[r1] : 0.f;
+          w[e] = pack_bf16(q0 * g0, q1 * g1);
+        }
+        *reinterpret_cast<uint4*>(img + kImgQ + sw_chunk(c, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
   }
+  stamp(2);
   __syncthreads();
   if (s_abort) goto teardown;
   if (!mbar_wait(&bar_a, 0)) { flag_status(status, GDN_ERR_TIMEOUT); s_abort = 1; }
   __syncthreads();
   if (s_abort) goto teardown;
+  stamp(3);
   tc_fence_after();
   {
     uint32_t g[32];
@@ -226,6 +270,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tma_load_3d(sm + kP_KQ + b * 16384 + 8192, &tm_v, b * 64, h, (int32_t)t0, &bar_v);
   }
 
+  stamp(4);
   // ---- T = (I + A)^{-1}: 16 x 16 diagonal inverses, then two levels of
   //      [[T1, 0], [X, T2]] with X = -T2 A21 T1
   if (tid < 64) {
@@ -291,6 +336,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     for (int m = 0; m < 4; ++m) sT[(32 + r0 + 8 * m) * kLd + c] = -z[m];
   }
   __syncthreads();
+  stamp(5);
   // T_w = T diag(beta gamma), T_u = T diag(beta): K-major bf16 images over the dead A tile
   {
     const int r = tid >> 2, c2 = tid & 3;
@@ -304,7 +350,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const float t0v = j0 <= r ? sT[r * kLd + j0] : 0.f;
         const float t1v = j1 <= r ? sT[r * kLd + j1] : 0.f;
         const float b0 = sB[j0], b1 = sB[j1];
-        ww[e] = pack_bf16(t0v * b0 * __expf(sG[j0]), t1v * b1 * __expf(sG[j1]));
+        ww[e] = pack_bf16(t0v * b0 * sGam[j0], t1v * b1 * sGam[j1]);
         uu[e] = pack_bf16(t0v * b0, t1v * b1);
       }
       *reinterpret_cast<uint4*>(sm + kP_TW + sw_chunk(r, ch)) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
@@ -314,6 +360,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   fence_proxy_async_smem();
   __syncthreads();
 
+  stamp(6);
   // ---- W^T = K^T T_w^T and U~^T = V^T T_u^T, two 128-row halves each
   if (tid == 0) {
     if (!mbar_wait(&bar_v, 0)) {
@@ -340,6 +387,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (!mbar_wait(&bar_bc, 0)) { flag_status(status, GDN_ERR_TIMEOUT); s_abort = 1; }
   __syncthreads();
   if (s_abort) goto teardown;
+  stamp(7);
   tc_fence_after();
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
@@ -349,7 +397,8 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       uint32_t g[32];
       tmem_ld32(tmem + lane_off + part * 128 + hh * 64 + 32 * hv, g);
       tmem_ld_wait();
-      uint8_t* dst = img + (part == 0 ? kImgW : kImgU);
+      // W rows c; U~^T rows c live in the half image of their 128-row half
+      uint8_t* dst = part == 0 ? img + kImgW : img + kImgU0 + hh * kImgHalf - hh * 128 * 128;
 #pragma unroll
       for (int cq = 0; cq < 4; ++cq) {
         const uint32_t w0 = pack_bf16(__uint_as_float(g[8 * cq]), __uint_as_float(g[8 * cq + 1]));
@@ -360,7 +409,15 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
     }
   }
-  if (tid < kC) reinterpret_cast<float*>(img + kImgG)[tid] = sG[tid];
+  if (tid < kC) {
+    const float d = tid < L ? __expf(sG[L - 1] - sG[tid]) : 0.f;
+    for (int hh = 0; hh < 2; ++hh) {
+      float* blk = reinterpret_cast<float*>(img + kImgU0 + hh * kImgHalf + kImgDecay);
+      blk[tid] = d;
+      blk[64 + tid] = sG[tid];
+    }
+  }
+  stamp(8);
 
 teardown:
   if (s_abort && tid == 0) {
@@ -371,30 +428,39 @@ teardown:
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
+  if (wave_trace && tid == 0) {   // the last CTA of the launch to finish stamps the end
+    const unsigned long long done =
+        atomicAdd(reinterpret_cast<unsigned long long*>(wave_trace + 200 + wave), 1ull);
+    if (done + 1 == (unsigned long long)gridDim.x * gridDim.y) wave_trace[101 + 2 * wave] = globaltimer_ns();
+  }
 }
 
 // =========================================================== state kernel
 constexpr int kStateThreads = 256;
 constexpr uint32_t kS_WQ = 0;         // 2 x 64 KB: [W (32 KB) | Q^ (32 KB)] per buffer
-constexpr uint32_t kS_K = 131072;     // 32 KB: K^, MN-major B image (4 column blocks of 8 KB)
-constexpr uint32_t kS_P = 163840;     // 8 KB : P^
-constexpr uint32_t kS_AU = 172032;    // 16 KB: U^T bf16, K-major A image, 128 rows x 64
-constexpr uint32_t kS_UT = 188416;    // 16 KB: U~^T rows of this half
-constexpr uint32_t kS_O = 204800;     // 16 KB: output staging [64][128] bf16
-constexpr uint32_t kS_G = 221184;     // 256 B: G of the chunk
-constexpr uint32_t kS_END = 221440;
+constexpr uint32_t kS_KP = 131072;    // 2 x 40 KB: [K (32 KB, MN-major) | P^ (8 KB)] per buffer
+constexpr uint32_t kS_UT = 212992;    // 16.5 KB: U~^T rows of this half + decay block
+constexpr uint32_t kS_END = 229888;
 constexpr uint32_t kStateSmem = kS_END + 1024;
-// TMEM columns: D_U, D_O (fp32), the bf16 A operand copy of S (2 per column), D_S (fp32)
+// TMEM columns: D_U (fp32), D_O (fp32), the bf16 A-operand copy of S (2 per
+// column), D_S (fp32).  After the U epilogue the D_U columns hold bf16 A
+// operands: each half [32h, 32h+32) of D_U is overwritten only by the warps
+// that read it, with U for rows r in [32h, 32h+32) in its first 16 columns
+// and d*U for the same rows in its last 16.
 constexpr uint32_t kT_U = 0, kT_O = 64, kT_SA = 128, kT_S = 256;
+__device__ __forceinline__ uint32_t col_U(int s) { return 32u * (s >> 1) + 8u * (s & 1); }
+__device__ __forceinline__ uint32_t col_dU(int s) { return col_U(s) + 16u; }
 
 __global__ void __launch_bounds__(kStateThreads, 1)
-tc_state_kernel(const float* __restrict__ S0, __nv_bfloat16* __restrict__ out,
-                float* __restrict__ S_final, SeqMap map, int32_t H,
-                const uint8_t* __restrict__ scratch, unsigned* status) {
+tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restrict__ S0,
+                __nv_bfloat16* __restrict__ out, float* __restrict__ S_final, SeqMap map,
+                int32_t H, const uint8_t* __restrict__ scratch, unsigned* status,
+                uint64_t* __restrict__ trace, int32_t trace_chunks, int32_t win_p0,
+                int32_t win_np, uint64_t* __restrict__ wave_trace, int32_t wave) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align_smem_1024(smem_raw);
-  const float* sG = reinterpret_cast<const float*>(sm + kS_G);
-  __shared__ uint64_t bar_wq[2], bar_k, bar_u, bar_m1, bar_m1b, bar_m2, bar_mo;
+  const float* sD = reinterpret_cast<const float*>(sm + kS_UT + kImgDecay);   // d_r, then G_r
+  __shared__ uint64_t bar_wq[2], bar_kp[2], bar_u, bar_m1, bar_m1b, bar_m2, bar_mo;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
 
@@ -403,13 +469,28 @@ tc_state_kernel(const float* __restrict__ S0, __nv_bfloat16* __restrict__ out,
   const int quarter = warp & 3, colhalf = warp >> 2;
   const uint32_t iloc = 32 * quarter + lane;            // TMEM lane = local row of S
   const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-  const int64_t cb = map.chunk_begin(n), ce = map.chunk_end(n);
-  const int64_t s_begin = map.seq_begin(n), s_end = map.seq_end(n);
+  // chunks of this launch: positions [win_p0, win_p0 + win_np) of the
+  // sequence (all of them when win_np <= 0); S0 holds the state at the
+  // window's start and S_final receives the state at its end
+  const int64_t c_first = map.chunk_begin(n), c_last = map.chunk_end(n);
+  const int64_t cb = win_np > 0 ? min(c_first + win_p0, c_last) : c_first;
+  const int64_t ce = win_np > 0 ? min(cb + win_np, c_last) : c_last;
+  const int64_t s_begin = map.seq_begin(n) + (cb - c_first) * kC, s_end = map.seq_end(n);
+  // optional phase timeline (test hook): thread 0 of the first CTA stamps
+  // its SM cycle counter at 12 points of each of its first trace_chunks chunks
+  const bool tracing = trace && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
+                       blockIdx.z == 0 && win_p0 == 0;
+  auto stamp = [&](int64_t it, int k) {
+    if (tracing && it < trace_chunks) trace[it * 12 + k] = clock64();
+  };
 
+  const bool wave_stamp = wave_trace && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+  if (wave_stamp) wave_trace[2 * wave] = globaltimer_ns();
   if (tid == 0) {
-    mbar_init(&bar_wq[0], 1);
-    mbar_init(&bar_wq[1], 1);
-    mbar_init(&bar_k, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_wq[b], 1);
+      mbar_init(&bar_kp[b], 1);
+    }
     mbar_init(&bar_u, 1);
     mbar_init(&bar_m1, 1);
     mbar_init(&bar_m1b, 1);
@@ -417,6 +498,7 @@ tc_state_kernel(const float* __restrict__ S0, __nv_bfloat16* __restrict__ out,
     mbar_init(&bar_mo, 1);
     fence_barrier_init();
     s_abort = 0;
+    prefetch_tensormap(&tm_k);
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
 
@@ -437,7 +519,7 @@ tc_state_kernel(const float* __restrict__ S0, __nv_bfloat16* __restrict__ out,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  // bf16 copy of S into TMEM: two packed columns hold four state columns
+  // bf16 copy of S into TMEM: one packed column holds two state columns
   auto store_S_operand = [&]() {
 #pragma unroll
     for (int hq = 0; hq < 2; ++hq) {
@@ -451,65 +533,90 @@ tc_state_kernel(const float* __restrict__ S0, __nv_bfloat16* __restrict__ out,
   store_S_operand();
 
   auto img_of = [&](int64_t ci) { return scratch + (size_t)(ci * H + h) * kImgStride; };
-  auto issue_wq = [&](int64_t ci, int buf) {
-    const uint8_t* src = img_of(ci);
+  auto t0_of = [&](int64_t ci) { return (int32_t)(s_begin + (ci - cb) * kC); };
+  auto issue_wq = [&](int64_t ci, int buf) {   // W and Q^ are adjacent in the image
     mbar_arrive_expect_tx(&bar_wq[buf], 65536);
-    tma_load_1d(sm + kS_WQ + buf * 65536, src + kImgW, 32768, &bar_wq[buf]);
-    tma_load_1d(sm + kS_WQ + buf * 65536 + 32768, src + kImgQ, 32768, &bar_wq[buf]);
+    tma_load_1d(sm + kS_WQ + buf * 65536, img_of(ci) + kImgW, 65536, &bar_wq[buf]);
   };
-  auto issue_kp = [&](int64_t ci) {
-    const uint8_t* src = img_of(ci);
-    mbar_arrive_expect_tx(&bar_k, 32768 + 8192);
-    tma_load_1d(sm + kS_K, src + kImgK, 32768, &bar_k);
-    tma_load_1d(sm + kS_P, src + kImgP, 8192, &bar_k);
+  auto issue_kp = [&](int64_t ci, int buf) {
+    uint8_t* dst = sm + kS_KP + buf * 40960;
+    mbar_arrive_expect_tx(&bar_kp[buf], 40960);
+    tma_load_4d(dst, &tm_k, 0, t0_of(ci), 0, h, &bar_kp[buf]);
+    tma_load_1d(dst + 32768, img_of(ci) + kImgP, 8192, &bar_kp[buf]);
   };
-  auto issue_u = [&](int64_t ci) {
-    const uint8_t* src = img_of(ci);
-    mbar_arrive_expect_tx(&bar_u, 16384 + 256);
-    tma_load_1d(sm + kS_UT, src + kImgU + half * 16384, 16384, &bar_u);
-    tma_load_1d(sm + kS_G, src + kImgG, 256, &bar_u);
+  auto issue_u = [&](int64_t ci) {    // this half's U~^T rows and the decay block
+    mbar_arrive_expect_tx(&bar_u, (uint32_t)kImgHalf);
+    tma_load_1d(sm + kS_UT, img_of(ci) + kImgU0 + half * kImgHalf, (uint32_t)kImgHalf, &bar_u);
   };
-  // outstanding-load bookkeeping (thread 0), for a clean exit after a timeout
-  uint32_t pend = 0;   // bit 0/1: wq buffers, bit 2: k, bit 3: u
-  if (tid == 0 && cb < ce) {
-    issue_wq(cb, 0);
-    if (cb + 1 < ce) issue_wq(cb + 1, 1);
-    issue_kp(cb);
-    issue_u(cb);
-    pend = 0xF;
+  auto warm_l2 = [&](int64_t ci) {    // the whole image of a later chunk
+    prefetch_l2(img_of(ci), (uint32_t)kImgStride);
+  };
+  // Loads are issued by single threads of warps 1 and 2 (thread 0 issues the
+  // MMAs), so the kinds of issue overlap.  Each counts the phases it started
+  // on its load barriers, for a clean exit after a timeout.
+  constexpr int kLoaderA = 32;   // K / P^ and U~^T
+  constexpr int kLoaderB = 64;   // W / Q^ and the L2 warm-up
+  uint32_t n_wq[2] = {0, 0}, n_kp[2] = {0, 0}, n_u = 0;
+  if (tid == kLoaderA && cb < ce) {
+    issue_kp(cb, 0); ++n_kp[0];
+    issue_u(cb); ++n_u;
+  }
+  if (tid == kLoaderB && cb < ce) {
+    issue_wq(cb, 0); ++n_wq[0];
+    if (cb + 1 < ce) { issue_wq(cb + 1, 1); ++n_wq[1]; }
+    if (cb + 1 < ce) warm_l2(cb + 1);
+    if (cb + 2 < ce) warm_l2(cb + 2);
   }
   tc_fence_before();
   __syncthreads();
+  int prev_L = 0;
+  int64_t prev_t0 = 0;
+  // rows of out for the previous chunk, staged in its (consumed) K / P^ buffer
+  // (warps 1-7 only: warp 0 is busy issuing MMA-1 at that point)
+  auto copy_out_prev = [&](int prev_buf) {
+    for (int w = tid - 32; w < 256; w += kStateThreads - 32) {
+      if (w < 0) break;
+      const int r = w >> 2, seg = w & 3;
+      if (r < prev_L) {
+        const uint4* src = reinterpret_cast<const uint4*>(sm + kS_KP + prev_buf * 40960 + r * 256 + seg * 64);
+        uint4* dst = reinterpret_cast<uint4*>(out + ((prev_t0 + r) * H + h) * kDV + 128 * half + 32 * seg);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = src[q];
+      }
+    }
+  };
 
   for (int64_t ci = cb; ci < ce; ++ci) {
     const int64_t it = ci - cb;
     const uint32_t par = (uint32_t)(it & 1);
-    const int wb = (int)(it & 1);
-    const uint32_t wpar = (uint32_t)((it >> 1) & 1);
+    const int buf = (int)(it & 1);
+    const uint32_t bpar = (uint32_t)((it >> 1) & 1);
     const int64_t t0 = s_begin + it * kC;
     const int L = (int)min((int64_t)kC, s_end - t0);
 
-    // 1. D_U = S W^T (commit m1), D_O = S Q^^T (commit m1b); A = S from TMEM
+    // 1. [D_U | D_O] = S [W | Q^]^T (commit m1 and m1b); A = S from TMEM
+    stamp(it, 0);
     if (tid == 0) {
-      if (!mbar_wait(&bar_wq[wb], wpar)) {
+      if (!mbar_wait(&bar_wq[buf], bpar)) {
         s_abort = 1;
       } else {
-        pend &= ~(1u << wb);
         tc_fence_after();
-        const uint32_t idW = idesc_bf16(128, 64, 0, 1), idQ = idesc_bf16(128, 64, 0, 0);
-        const uint32_t sW = smem_u32(sm + kS_WQ + wb * 65536), sQ = sW + 32768;
+        // [D_U | D_O] = S [W | Q^]^T : one N = 128 operand (MN-major, the two
+        // 64-element MN blocks 32 KB apart)
+        const uint32_t id1 = idesc_bf16(128, 128, 0, 1);
+        const uint32_t sW = smem_u32(sm + kS_WQ + buf * 65536);
         for (int s = 0; s < 16; ++s)
           mma_bf16_ts(tmem + kT_U, tmem + kT_SA + 8 * s,
-                      smem_desc(sW + s * 2048, 32768, 1024, kSwizzle128B), idW, s > 0);
+                      smem_desc(sW + s * 2048, 32768, 1024, kSwizzle128B), id1, s > 0);
         mma_commit(&bar_m1);
-        for (int s = 0; s < 16; ++s)
-          mma_bf16_ts(tmem + kT_O, tmem + kT_SA + 8 * s,
-                      smem_desc(sQ + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024, kSwizzle128B),
-                      idQ, s > 0);
         mma_commit(&bar_m1b);
       }
     }
-    // 2. U = U~ - D_U  ->  bf16 K-major A image (row iloc, columns r)
+    stamp(it, 1);
+    // the previous chunk's output rows go out while MMA-1 runs
+    if (it > 0) copy_out_prev(buf ^ 1);
+    // 2. U = U~ - D_U (columns r = 32 colhalf ..), and d_r U: bf16 A operands in TMEM
+    float gC = 0.f;
     if (!mbar_wait(&bar_m1, par) || !mbar_wait(&bar_u, par)) {
       flag_status(status, GDN_ERR_TIMEOUT);
       s_abort = 1;
@@ -518,121 +625,151 @@ tc_state_kernel(const float* __restrict__ S0, __nv_bfloat16* __restrict__ out,
       uint32_t g[32];
       tmem_ld32(tmem + lane_off + kT_U + 32 * colhalf, g);
       tmem_ld_wait();
+      stamp(it, 8);
+      gC = __expf(sD[64 + L - 1]);
+      uint32_t ua[16], ud[16];
 #pragma unroll
       for (int cq = 0; cq < 4; ++cq) {
-        const int ch = 4 * colhalf + cq;
-        const uint4 ut = *reinterpret_cast<const uint4*>(sm + kS_UT + sw_chunk(iloc, ch));
+        const uint4 ut = *reinterpret_cast<const uint4*>(sm + kS_UT + sw_chunk(iloc, 4 * colhalf + cq));
         const uint32_t uw[4] = {ut.x, ut.y, ut.z, ut.w};
-        uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          w[e] = pack_bf16(bf16_lo(uw[e]) - __uint_as_float(g[8 * cq + 2 * e]),
-                           bf16_hi(uw[e]) - __uint_as_float(g[8 * cq + 2 * e + 1]));
-        *reinterpret_cast<uint4*>(sm + kS_AU + sw_chunk(iloc, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int e = 0; e < 4; ++e) {
+          const int j = 8 * cq + 2 * e, r = 32 * colhalf + j;
+          const float u0 = bf16_lo(uw[e]) - __uint_as_float(g[j]);
+          const float u1 = bf16_hi(uw[e]) - __uint_as_float(g[j + 1]);
+          const float d0 = sD[r], d1 = sD[r + 1];
+          ua[4 * cq + e] = pack_bf16(u0, u1);
+          ud[4 * cq + e] = pack_bf16(u0 * d0, u1 * d1);
+        }
       }
+      tmem_st16(tmem + lane_off + kT_U + 32 * colhalf, ua);
+      tmem_st16(tmem + lane_off + kT_U + 32 * colhalf + 16, ud);
+      tmem_st_wait();
     }
-    const float gC = __expf(sG[L - 1]);
-    fence_proxy_async_smem();
+    stamp(it, 2);
     tc_fence_before();
     __syncthreads();
     if (s_abort) break;
-    if (tid == 0) pend &= ~8u;
+    stamp(it, 3);
 
-    // 3. D_S = U^T K^ (commit m2) ; D_O += U^T P^^T (commit mo); prefetches
+    // 3. D_S = (dU)^T K (commit m2) ; D_O += U^T P^^T (commit mo)
     if (tid == 0) {
-      if (!mbar_wait(&bar_k, par)) {
+      if (!mbar_wait(&bar_kp[buf], bpar)) {
         s_abort = 1;
       } else {
-        pend &= ~4u;
         tc_fence_after();
         const uint32_t id2 = idesc_bf16(128, 256, 0, 1), idO = idesc_bf16(128, 64, 0, 0);
-        const uint32_t sAU = smem_u32(sm + kS_AU), sK = smem_u32(sm + kS_K), sP = smem_u32(sm + kS_P);
+        const uint32_t sK = smem_u32(sm + kS_KP + buf * 40960), sP = sK + 32768;
         for (int s = 0; s < 4; ++s)
-          mma_bf16(tmem + kT_S, smem_desc(sAU + s * 32, 16, 1024, kSwizzle128B),
-                   smem_desc(sK + s * 2048, 8192, 1024, kSwizzle128B), id2, s > 0);
+          mma_bf16_ts(tmem + kT_S, tmem + kT_U + col_dU(s),
+                      smem_desc(sK + s * 2048, 8192, 1024, kSwizzle128B), id2, s > 0);
         mma_commit(&bar_m2);
         for (int s = 0; s < 4; ++s)
-          mma_bf16(tmem + kT_O, smem_desc(sAU + s * 32, 16, 1024, kSwizzle128B),
-                   smem_desc(sP + s * 32, 16, 1024, kSwizzle128B), idO, 1);
+          mma_bf16_ts(tmem + kT_O, tmem + kT_U + col_U(s),
+                      smem_desc(sP + s * 32, 16, 1024, kSwizzle128B), idO, 1);
         mma_commit(&bar_mo);
-        if (ci + 1 < ce) { issue_u(ci + 1); pend |= 8u; }
-        // this W / Q^ buffer is free once both MMA-1 halves are done
-        if (ci + 2 < ce) {
-          if (!mbar_wait(&bar_m1b, par)) {
-            s_abort = 1;
-          } else {
-            issue_wq(ci + 2, wb);
-            pend |= 1u << wb;
-          }
+      }
+    }
+    // ... meanwhile the loader fetches ahead: K / P^ of the next chunk into
+    // the other buffer (the previous chunk's staging was copied out above),
+    // U~^T of the next chunk (E1 is done with the buffer), the W / Q^ buffer
+    // of this chunk for chunk + 2 (once MMA-1 finished reading it), and warms
+    // L2 with a later chunk's image
+    if (tid == kLoaderA && ci + 1 < ce) {
+      issue_kp(ci + 1, buf ^ 1); ++n_kp[buf ^ 1];
+      issue_u(ci + 1); ++n_u;
+    }
+    if (tid == kLoaderB) {
+      if (ci + 3 < ce) warm_l2(ci + 3);
+      if (ci + 2 < ce) {
+        if (!mbar_wait(&bar_m1b, par)) {
+          s_abort = 1;
+        } else {
+          issue_wq(ci + 2, buf); ++n_wq[buf];
         }
       }
     }
 
-    // 4. S = gamma_L S + D_S (fp32) -> bf16 operand copy in TMEM; O -> staging
+    // 4. S = gamma_L S + D_S (fp32) -> bf16 operand copy in TMEM; O -> out
+    stamp(it, 4);
     if (!mbar_wait(&bar_m2, par)) {
       flag_status(status, GDN_ERR_TIMEOUT);
       s_abort = 1;
     } else {
+      stamp(it, 5);
       tc_fence_after();
+      // MMA-1 has finished reading the bf16 state operand (it precedes
+      // MMA-2), so each folded group can replace its columns right away
+      if (!mbar_wait(&bar_m1b, par)) s_abort = 1;
 #pragma unroll
       for (int g4 = 0; g4 < 4; ++g4) {
         uint32_t g[32];
         tmem_ld32(tmem + lane_off + kT_S + 128 * colhalf + 32 * g4, g);
         tmem_ld_wait();
+        uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) S[32 * g4 + j] = fmaf(gC, S[32 * g4 + j], __uint_as_float(g[j]));
+        for (int j = 0; j < 32; j += 2) {
+          const float s0 = fmaf(gC, S[32 * g4 + j], __uint_as_float(g[j]));
+          const float s1 = fmaf(gC, S[32 * g4 + j + 1], __uint_as_float(g[j + 1]));
+          S[32 * g4 + j] = s0;
+          S[32 * g4 + j + 1] = s1;
+          pk[j >> 1] = pack_bf16(s0, s1);
+        }
+        tmem_st16(tmem + lane_off + kT_SA + 64 * colhalf + 16 * g4, pk);
       }
-      store_S_operand();
+      tmem_st_wait();
+      stamp(it, 9);
       if (!mbar_wait(&bar_mo, par)) {
         flag_status(status, GDN_ERR_TIMEOUT);
         s_abort = 1;
       } else {
+        stamp(it, 10);
         tc_fence_after();
         uint32_t g[32];
         tmem_ld32(tmem + lane_off + kT_O + 32 * colhalf, g);
         tmem_ld_wait();
-        __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(sm + kS_O);
+        stamp(it, 11);
+        // O^T (row iloc, columns r) -> staging [r][128] bf16 in this chunk's
+        // K / P^ buffer, which MMA-2 and MMA-O no longer read
+        __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(sm + kS_KP + buf * 40960);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          so[(32 * colhalf + j) * 128 + iloc] = __float2bfloat16_rn(__uint_as_float(g[j]));
+        for (int j = 0; j < 32; j += 2) {
+          const __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(g[j]), __uint_as_float(g[j + 1]));
+          so[(32 * colhalf + j) * 128 + iloc] = pr.x;
+          so[(32 * colhalf + j + 1) * 128 + iloc] = pr.y;
+        }
       }
     }
+    stamp(it, 6);
     tc_fence_before();
     __syncthreads();
     if (s_abort) break;
+    stamp(it, 7);
 
-    // 5. prefetch the next chunk's K^ and P^; write this chunk's rows of out
-    if (tid == 0 && ci + 1 < ce) {
-      issue_kp(ci + 1);
-      pend |= 4u;
-    }
-    {
-      const int r = tid >> 2, seg = tid & 3;
-      if (r < L) {
-        const uint4* src = reinterpret_cast<const uint4*>(sm + kS_O + r * 256 + seg * 64);
-        uint4* dst = reinterpret_cast<uint4*>(out + ((t0 + r) * H + h) * kDV + 128 * half + 32 * seg);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = src[q];
-      }
-    }
+    prev_L = L;
+    prev_t0 = t0;
   }
+  // the last chunk's output rows
+  if (!s_abort && ce > cb) copy_out_prev((int)((ce - cb - 1) & 1));
 
   if (!s_abort && S_final) {
     float4* p = reinterpret_cast<float4*>(S_final + srow);
 #pragma unroll
     for (int j = 0; j < 32; ++j) p[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
   }
-  if (tid == 0 && s_abort) {   // let copies still in flight land before the CTA exits
+  if ((tid == kLoaderA || tid == kLoaderB) && s_abort) {   // let copies in flight land
     flag_status(status, GDN_ERR_TIMEOUT);
     const uint64_t lim = 100000000ull;
-    for (int b = 0; b < 2; ++b)
-      if (pend & (1u << b)) { mbar_wait(&bar_wq[b], 0, lim); mbar_wait(&bar_wq[b], 1, lim); }
-    if (pend & 4u) { mbar_wait(&bar_k, 0, lim); mbar_wait(&bar_k, 1, lim); }
-    if (pend & 8u) { mbar_wait(&bar_u, 0, lim); mbar_wait(&bar_u, 1, lim); }
+    for (int b = 0; b < 2; ++b) {
+      if (n_wq[b]) mbar_wait(&bar_wq[b], (n_wq[b] - 1) & 1, lim);
+      if (n_kp[b]) mbar_wait(&bar_kp[b], (n_kp[b] - 1) & 1, lim);
+    }
+    if (n_u) mbar_wait(&bar_u, (n_u - 1) & 1, lim);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
+  if (wave_stamp) wave_trace[2 * wave + 1] = globaltimer_ns();
 }
 
 // ------------------------------------------------------------- host side
@@ -668,7 +805,29 @@ bool make_token_map(CUtensorMap* m, const void* base, int64_t T_total, int32_t H
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same tensor viewed as (64 features, token, 4 feature blocks, head) so
+// that one box of 64 x 64 x 4 x 1 lands the four 64-column blocks of a
+// chunk's 64 tokens one after another: the MN-major image the state pass
+// feeds to its MMA, in a single TMA copy.
+bool make_token_map_blocked(CUtensorMap* m, const void* base, int64_t T_total, int32_t H) {
+  EncodeFn enc = encoder();
+  if (!enc) return false;
+  memset(m, 0, sizeof *m);
+  cuuint64_t dims[4] = {64, (cuuint64_t)(T_total > 0 ? T_total : 1), 4, (cuuint64_t)H};
+  cuuint64_t strides[3] = {(cuuint64_t)H * kDK * 2, 128, (cuuint64_t)kDK * 2};
+  cuuint32_t box[4] = {64, 64, 4, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
+
+// phase-timeline buffer for the state pass and, at kPrepTraceOffset, for the
+// first CTA of the per-chunk kernel (test hook; null when off)
+uint64_t* g_trace = nullptr;
+int32_t g_trace_chunks = 0;
 
 size_t prefill_tc_scratch_bytes(int64_t max_chunks, int32_t H) {
   return (size_t)max_chunks * H * kImgStride;
@@ -676,12 +835,63 @@ size_t prefill_tc_scratch_bytes(int64_t max_chunks, int32_t H) {
 
 size_t prefill_tc_image_stride() { return kImgStride; }
 
+namespace {
+
+// Per-device helper streams and events for overlapping the parallel prep of
+// one chunk-position wave with the sequential state pass of the previous one.
+// The state pass runs on the highest-priority stream, so its CTAs take SMs
+// as soon as they free up instead of queueing behind the next prep wave.
+struct WaveStreams {
+  cudaStream_t prep = nullptr, state = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t prep_done[kMaxWaves] = {};
+  bool ok = false;
+};
+
+WaveStreams* wave_streams() {
+  static WaveStreams ws[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  WaveStreams& w = ws[dev];
+  if (!w.ok) {
+    int lo = 0, hi = 0;
+    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return nullptr;
+    if (cudaStreamCreateWithPriority(&w.prep, cudaStreamNonBlocking, lo) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&w.state, cudaStreamNonBlocking, hi) != cudaSuccess ||
+        cudaEventCreateWithFlags(&w.start, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&w.done, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+    for (int i = 0; i < kMaxWaves; ++i)
+      if (cudaEventCreateWithFlags(&w.prep_done[i], cudaEventDisableTiming) != cudaSuccess)
+        return nullptr;
+    w.ok = true;
+  }
+  return &w;
+}
+
+// Number of chunk-position waves: dense batches only, whose state pass
+// leaves most SMs free, and long enough for every wave to have work to hide.
+int wave_count(const PrefillLaunch& a) {
+  if (!a.allow_waves || a.map.cu_seqlens || a.map.chunks_per_seq < 2 * kWaveMinChunks) return 1;
+  if ((int64_t)a.map.N * a.H * 2 > kWaveMaxStateCtas) return 1;
+  const int64_t w = a.map.chunks_per_seq / kWaveMinChunks;
+  return (int)(w < kMaxWaves ? w : kMaxWaves);
+}
+
+}  // namespace
+
+size_t prefill_tc_wave_state_bytes(const PrefillLaunch& a) {
+  return wave_count(a) > 1 ? (size_t)a.map.N * a.H * kDV * kDK * sizeof(float) : 0;
+}
+
 cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool prep_only) {
   static_assert(kDK == 256 && kDV == 256, "image layouts assume 256 x 256 heads");
   const int64_t T_total = a.map.cu_seqlens ? a.map.T : (int64_t)a.map.N * a.map.T;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tkb;
   if (!make_token_map(&tq, a.q, T_total, a.H) || !make_token_map(&tk, a.k, T_total, a.H) ||
-      !make_token_map(&tv, a.v, T_total, a.H))
+      !make_token_map(&tv, a.v, T_total, a.H) || !make_token_map_blocked(&tkb, a.k, T_total, a.H))
     return cudaErrorInvalidValue;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -691,17 +901,58 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
                                 (int)kStateSmem)) != cudaSuccess)
     return e;
   uint8_t* scr = (uint8_t*)a.scratch;
-  if (a.max_chunks > 0) {
-    tc_prep_kernel<<<dim3((unsigned)a.max_chunks, (unsigned)a.H), kPrepThreads, kPrepSmem,
-                     stream>>>(tq, tk, tv, a.alpha, a.beta, a.map, a.H, scr, a.status);
+  uint64_t* prep_trace = g_trace ? g_trace + kPrepTraceOffset : nullptr;
+  uint64_t* wave_trace = g_trace ? g_trace + kWaveTraceOffset : nullptr;
+  const int waves = prep_only ? 1 : wave_count(a);
+  if (waves == 1) {
+    if (a.max_chunks > 0) {
+      tc_prep_kernel<<<dim3((unsigned)a.max_chunks, (unsigned)a.H), kPrepThreads, kPrepSmem,
+                       stream>>>(tq, tk, tv, a.alpha, a.beta, a.map, a.H, scr, a.status,
+                                 prep_trace, 0, 0, wave_trace, 0);
+      count_launches(1);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (prep_only) return cudaSuccess;
+    tc_state_kernel<<<dim3((unsigned)a.map.N, (unsigned)a.H, 2), kStateThreads, kStateSmem,
+                      stream>>>(tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr,
+                                a.status, g_trace, g_trace_chunks, 0, 0, wave_trace, 0);
+    count_launches(1);
+    return cudaGetLastError();
+  }
+  // Waves: the prep of every wave is queued on a low-priority helper stream
+  // and overlaps the state pass of the earlier waves on a high-priority one
+  // (state wave w waits only for prep wave w); the state carries between
+  // waves in scratch, and the caller's stream waits for the last state wave.
+  WaveStreams* ws = wave_streams();
+  if (!ws) return cudaErrorUnknown;
+  float* carry = (float*)(scr + prefill_tc_scratch_bytes(a.max_chunks, a.H));
+  const int64_t cps = a.map.chunks_per_seq;
+  if ((e = cudaEventRecord(ws->start, stream)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(ws->prep, ws->start, 0)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(ws->state, ws->start, 0)) != cudaSuccess) return e;
+  for (int w = 0; w < waves; ++w) {
+    const int32_t p0 = (int32_t)(cps * w / waves), np = (int32_t)(cps * (w + 1) / waves) - p0;
+    tc_prep_kernel<<<dim3((unsigned)(a.map.N * np), (unsigned)a.H), kPrepThreads, kPrepSmem,
+                     ws->prep>>>(tq, tk, tv, a.alpha, a.beta, a.map, a.H, scr, a.status,
+                                 w == 0 ? prep_trace : nullptr, p0, np, wave_trace, w);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(ws->prep_done[w], ws->prep)) != cudaSuccess) return e;
+  }
+  for (int w = 0; w < waves; ++w) {
+    const int32_t p0 = (int32_t)(cps * w / waves), np = (int32_t)(cps * (w + 1) / waves) - p0;
+    if ((e = cudaStreamWaitEvent(ws->state, ws->prep_done[w], 0)) != cudaSuccess) return e;
+    const float* s_in = w == 0 ? a.S0 : carry;
+    float* s_out = w == waves - 1 ? a.S_final : carry;
+    tc_state_kernel<<<dim3((unsigned)a.map.N, (unsigned)a.H, 2), kStateThreads, kStateSmem,
+                      ws->state>>>(tkb, s_in, (__nv_bfloat16*)a.out, s_out, a.map, a.H, scr,
+                                   a.status, g_trace, g_trace_chunks, p0, np, wave_trace, w);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (prep_only) return cudaSuccess;
-  tc_state_kernel<<<dim3((unsigned)a.map.N, (unsigned)a.H, 2), kStateThreads, kStateSmem,
-                    stream>>>(a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr, a.status);
-  count_launches(1);
-  return cudaGetLastError();
+  if ((e = cudaEventRecord(ws->done, ws->state)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(stream, ws->done, 0)) != cudaSuccess) return e;
+  return cudaSuccess;
 }
 
 }  // namespace gdn

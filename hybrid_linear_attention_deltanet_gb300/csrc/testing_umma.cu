@@ -132,6 +132,55 @@ __global__ void __launch_bounds__(128) umma_gemm_kernel(UmmaArgs a,
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// Issue `reps` back-to-back chains of K/16 MMAs (M=128, N, bf16) from one
+// thread and count SM cycles from the first issue to the commit's arrival.
+// Operand contents are whatever the shared memory / TMEM holds: only time.
+__global__ void __launch_bounds__(128) umma_timing_kernel(int N, int K, int a_tmem_mode,
+                                                           int b_mn, int reps,
+                                                           unsigned long long* cycles,
+                                                           unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_smem_1024(smem_raw);
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, 512);
+  for (int e = tid; e < 48 * 1024; e += blockDim.x) reinterpret_cast<uint32_t*>(smem)[e] = 0x3c003c00u;
+  fence_proxy_async_smem();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  if (tid == 0) {
+    const uint32_t idesc = idesc_bf16(128, N, 0, b_mn);
+    const uint32_t sa = smem_u32(smem), sb = smem_u32(smem + 65536);
+    const unsigned long long t0 = clock64();
+    for (int r = 0; r < reps; ++r) {
+      for (int s = 0; s < K / 16; ++s) {
+        const uint64_t bd = b_mn ? smem_desc(sb + s * 2048, N * 128 > 8192 ? 8192 : 8192, 1024, kSwizzle128B)
+                                 : smem_desc(sb + (s / 4) * (N * 128) + (s % 4) * 32, 16, 1024, kSwizzle128B);
+        if (a_tmem_mode)
+          mma_bf16_ts(tmem, tmem + 256 + 8 * (s % 16), bd, idesc, (r | s) != 0);
+        else
+          mma_bf16(tmem, smem_desc(sa + (s / 4) * 16384 + (s % 4) * 32, 16, 1024, kSwizzle128B), bd,
+                   idesc, (r | s) != 0);
+      }
+    }
+    const unsigned long long t1 = clock64();
+    mma_commit(&bar);
+    if (!mbar_wait(&bar, 0)) flag_status(status, GDN_ERR_TIMEOUT);
+    const unsigned long long t2 = clock64();
+    cycles[0] = t1 - t0;   // issue
+    cycles[1] = t2 - t0;   // issue + completion
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
 // furthest byte (exclusive) an MMA of this operand can read from its start
 uint32_t reach(int mn_major, int R, int K, uint32_t lbo, uint32_t sbo) {
   if (!mn_major) {   // per instruction: R/8 groups at SBO, last step at K-block K/64-1
@@ -144,6 +193,24 @@ uint32_t reach(int mn_major, int R, int K, uint32_t lbo, uint32_t sbo) {
 }  // namespace gdn
 
 using namespace gdn;
+
+extern "C" int gdn_testing_umma_timing(int32_t N, int32_t K, int32_t a_from_tmem, int32_t b_mn,
+                                       int32_t reps, unsigned long long* cycles,
+                                       gdn_stream_t stream) {
+  // operands stay inside 64 KB (A) + 128 KB (B) of the allocation
+  if (!cycles || N < 16 || N > 256 || N % 16 || K < 16 || K > 256 || K % 64 || reps < 1 ||
+      reps > 4096)
+    return GDN_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(umma_timing_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes + 1024) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  unsigned* st = status_ptr();
+  if (!st) return GDN_ERR_CUDA;
+  umma_timing_kernel<<<1, 128, kSmemBytes + 1024, (cudaStream_t)stream>>>(N, K, a_from_tmem, b_mn,
+                                                                          reps, cycles, st);
+  count_launches(1);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
 
 extern "C" int gdn_testing_umma_gemm(const void* A, const void* B, float* D, int32_t N,
                                      int32_t K, int32_t a_mn, int32_t b_mn, uint32_t a_lbo,

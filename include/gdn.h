@@ -113,7 +113,7 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
  * allocations, runtimes with a static memory budget -- call this instead.
  * It takes the same arguments, runs the same kernels and returns the same
  * results, and calls no allocator: its scratch is one static device array of
- * 64 MiB (enough for about 5000 tokens of a 6-head bf16 layer, or about 4800
+ * 64 MiB (enough for about 6600 tokens of a 6-head bf16 layer, or about 4800
  * with fp32 I/O), which every GPU that loads the library holds until the
  * process exits.
  *

@@ -43,6 +43,16 @@ int gdn_testing_umma_gemm(const void* A, const void* B, float* D, int32_t N, int
                           gdn_stream_t stream);
 
 /*
+ * gdn_testing_umma_timing -- cycles of `reps` back-to-back chains of K/16
+ * tcgen05.mma (M=128, N, bf16, fp32 accumulate) issued by one thread: A from
+ * shared memory (K-major) or TMEM, B K-major or MN-major.  cycles (device,
+ * 2 x uint64): [0] SM cycles spent issuing, [1] issue plus completion.
+ * Operand values are arbitrary: this measures time only.
+ */
+int gdn_testing_umma_timing(int32_t N, int32_t K, int32_t a_from_tmem, int32_t b_mn,
+                            int32_t reps, unsigned long long* cycles, gdn_stream_t stream);
+
+/*
  * gdn_testing_prefill_prep -- run only the first (per-chunk, fully parallel)
  * kernel of the bf16 tensor-core prefill and leave its per-(chunk, head)
  * operand images in `images` (device, image_bytes >= max_chunks * heads *
@@ -51,12 +61,13 @@ int gdn_testing_umma_gemm(const void* A, const void* B, float* D, int32_t N, int
  * ci (global index over all sequences), head h lives at byte offset
  * (ci * heads + h) * stride and holds, for the chunked WY form:
  *   +0       W      (64 x 256): 256 rows of 128 B; row c = W[0..63][c]
- *   +32768   Q^     (64 x 256): 4 blocks of 64 rows x 128 B; block b, row r
- *                               = Q^[r][64b .. 64b+63]  (Q^ = gamma Q / sqrt(dk))
- *   +65536   K^     (64 x 256): same block layout; K^ = diag(gamma_L / gamma) K
- *   +98304   P^     (64 x 64) : 64 rows of 128 B (lower(Gam Q K^T) / sqrt(dk))
- *   +106496  U~^T  (256 x 64) : row i = U~[0..63][i]
- *   +139264  G      (64 fp32) : cumulative log decay within the chunk
+ *   +32768   Q^     (64 x 256): 256 rows of 128 B; row c = Q^[0..63][c]
+ *                               (Q^ = gamma Q / sqrt(dk))
+ *   +65536   P^     (64 x 64) : 64 rows of 128 B (lower(Gam Q K^T) / sqrt(dk))
+ *   +73728   U~^T rows 0-127   : row i = U~[0..63][i]
+ *   +90112   decay block       : fp32 d[64] (d_r = gamma_L / gamma_r for r < L,
+ *                               else 0), then fp32 G[64] (cumulative log decay)
+ *   +90624   U~^T rows 128-255, then a copy of the decay block at +107008
  * Every 128-byte row r stores its 16-byte chunk j at position j XOR (r % 8).
  * Other arguments as for gdn_prefill with io_dtype = GDN_BF16.
  */
@@ -67,6 +78,29 @@ int gdn_testing_prefill_prep(const void* q, const void* k, const void* v, const 
 
 /* Byte stride between consecutive (chunk, head) images of gdn_testing_prefill_prep. */
 size_t gdn_testing_prefill_image_stride(void);
+
+/*
+ * gdn_testing_set_trace -- phase timeline of the bf16 state pass.  While set,
+ * every later gdn_prefill with bf16 I/O makes thread 0 of its first state-pass
+ * CTA (sequence 0, head 0, first row half) write its SM cycle counter
+ * (clock64) at 12 points of each of its first max_chunks (at most 256)
+ * chunks into device_buf (uint64 [max_chunks][12]): loop top, MMA-1 issued, U epilogue done, after
+ * the following barrier, MMA-2 issued, MMA-2 complete, state epilogue done,
+ * after the closing barrier, then (8) U accumulator loaded, (9) state
+ * accumulator folded into the master state, (10) bf16 state operand stored,
+ * (11) output accumulator loaded.  Thread 0 of the per-chunk kernel's first
+ * CTA (chunk 0, head 0) stamps 9 points of its life at device_buf[4096 +
+ * 0..8] (start, prologue done, before the Gram MMA wait, Gram done, A and P^
+ * written, T solved, T_w / T_u ready, W / U~ MMAs done, images written).
+ * At device_buf[3072 ..] the launches of one call leave a timeline on the GPU
+ * global timer (ns): [2w], [2w+1] = start and end of state-pass wave w (its
+ * first CTA); [100+2w] = start of per-chunk wave w (first CTA) and [101+2w]
+ * its end (last CTA to finish, found with the counter at [200+w], which must
+ * start at zero).  So device_buf must hold at least 4105 entries, zeroed.
+ * Pass NULL to switch it off.
+ * Not thread-safe; for profiling only.
+ */
+void gdn_testing_set_trace(uint64_t* device_buf, int32_t max_chunks);
 
 #ifdef __cplusplus
 }

@@ -205,3 +205,30 @@ def test_decode_equals_single_token_prefill(gdn_lib):
     o_d = gdn_lib.decode_step(args["q"], args["k"], args["v"], args["alpha"], args["beta"], S)
     assert rel(o_d.cpu().numpy(), o_p[:, 0].cpu().numpy()) <= 1e-5
     assert rel(S.cpu().numpy(), s_p.cpu().numpy()) <= 1e-5
+
+
+def test_prefill_chunk_waves_against_oracle(gdn_lib):
+    """65 chunks per sequence: the tensor-core prefill splits the sequence
+    into chunk-position waves (uneven split), carrying the state between
+    them; the result still matches the oracle."""
+    check_case(gdn_lib, PrefillCase("waves", [4160], H=2, io_dtype=torch.bfloat16, seed=61))
+
+
+def test_prefill_chunk_waves_are_bitwise_neutral(gdn_lib):
+    """The state carried between waves is the fp32 master state itself, so a
+    run split into waves equals the single-wave run bit for bit (the
+    no-allocation entry point always runs one wave)."""
+    import ctypes
+    case = PrefillCase("waves bitwise", [4160], H=2, io_dtype=torch.bfloat16, seed=62)
+    x = to_dev(gdn_inputs.make_prefill(case, device="cpu"))
+    out, Sf = run_gpu(gdn_lib, x)
+    f = gdn_lib.load().gdn_prefill_noalloc
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    f.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, vp]
+    out1 = torch.empty_like(out)
+    Sf1 = torch.empty_like(Sf)
+    rc = f(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), x["alpha"].data_ptr(),
+           x["beta"].data_ptr(), x["S0"].data_ptr(), None, out1.data_ptr(), Sf1.data_ptr(), 1,
+           4160, 2, 256, 256, 1, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0 and gdn_lib.device_status() == 0
+    assert torch.equal(out, out1) and torch.equal(Sf, Sf1)

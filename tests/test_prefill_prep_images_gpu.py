@@ -1,5 +1,6 @@
 """The tensor-core prefill's per-chunk kernel, checked on its own: decode the
-128-byte-swizzled operand images it leaves behind (W, Q^, P^, U~^T, G) and
+128-byte-swizzled operand images it leaves behind (W, Q^, P^, U~^T and the
+decay factors) and
 compare them with the fp64 chunk algebra computed from the same bf16 inputs.
 A layout or descriptor mistake shows up here as a wrong matrix, before the
 state pass mixes everything together."""
@@ -41,12 +42,15 @@ def _blocks(img, off):
 
 def _decode(img):
     W = _rows(img[0:32768], 256).T                        # [64 r][256 c]
-    Q = _blocks(img, 32768)
-    K = _blocks(img, 65536)
-    P = _rows(img[98304:98304 + 8192], 64)                # [64][64]
-    Ut = _rows(img[106496:106496 + 32768], 256).T         # [64 r][256 i]
-    G = img[139264:139264 + 256].view(np.float32).astype(np.float64)
-    return W, Q, K, P, Ut, G
+    Q = _rows(img[32768:65536], 256).T                    # [64 r][256 c]
+    P = _rows(img[65536:65536 + 8192], 64)                # [64][64]
+    half = 16896                                          # U~^T rows of one half + decay block
+    Ut = np.concatenate([_rows(img[73728 + h * half:73728 + h * half + 16384], 128)
+                         for h in range(2)]).T            # [64 r][256 i]
+    blocks = [img[73728 + h * half + 16384:73728 + (h + 1) * half].view(np.float32) for h in range(2)]
+    assert np.array_equal(blocks[0], blocks[1])
+    d, G = blocks[0][:64].astype(np.float64), blocks[0][64:].astype(np.float64)
+    return W, Q, P, Ut, G, d
 
 
 def _model_chunk(q, k, v, a, b):
@@ -60,8 +64,7 @@ def _model_chunk(q, k, v, a, b):
     Ut = T @ (b[:, None] * v)
     P = np.tril(Gam * (q @ k.T)) / 16.0
     Qh = g[:, None] * q / 16.0
-    Kh = np.exp(G[-1] - G)[:, None] * k
-    return W, Qh, Kh, P, Ut, G
+    return W, Qh, P, Ut, G
 
 
 def rel(x, y):
@@ -99,20 +102,22 @@ def test_prep_images_match_chunk_algebra(gdn_lib, lens, varlen):
             L = min(C, Ln - c0)
             for h in range(H):
                 img = img_all[(ci * H + h) * stride:(ci * H + h + 1) * stride]
-                W, Q, K, P, Ut, G = _decode(img)
+                W, Q, P, Ut, G, d = _decode(img)
                 sl = slice(t0, t0 + L)
-                Wm, Qm, Km, Pm, Um, Gm = _model_chunk(q[sl, h], k[sl, h], v[sl, h], al[sl, h],
-                                                      be[sl, h])
-                errs = dict(W=rel(W[:L], Wm), Q=rel(Q[:L], Qm), K=rel(K[:L], Km),
-                            P=rel(P[:L, :L], Pm), U=rel(Ut[:L], Um),
-                            G=float(np.abs(G[:L] - Gm).max()))
+                Wm, Qm, Pm, Um, Gm = _model_chunk(q[sl, h], k[sl, h], v[sl, h], al[sl, h],
+                                                  be[sl, h])
+                dm = np.exp(Gm[-1] - Gm)
+                errs = dict(W=rel(W[:L], Wm), Q=rel(Q[:L], Qm), P=rel(P[:L, :L], Pm),
+                            U=rel(Ut[:L], Um), G=float(np.abs(G[:L] - Gm).max()),
+                            d=float(np.abs(d[:L] - dm).max()))
+                assert np.all(d[L:] == 0)
                 for key, val in errs.items():
                     worst[key] = max(worst.get(key, 0.0), val)
                 # rows past the chunk's end must not write anything
                 assert np.all(W[L:] == 0) and np.all(Ut[L:] == 0) and np.all(Q[L:] == 0)
-                assert np.all(K[L:] == 0) and np.all(P[L:] == 0)
+                assert np.all(P[L:] == 0)
             ci += 1
     print("worst relative errors:", worst)
     assert worst["W"] < 2e-2 and worst["U"] < 2e-2 and worst["P"] < 2e-2
-    assert worst["Q"] < 1e-2 and worst["K"] < 1e-2
-    assert worst["G"] < 1e-4
+    assert worst["Q"] < 1e-2
+    assert worst["G"] < 1e-4 and worst["d"] < 1e-4
