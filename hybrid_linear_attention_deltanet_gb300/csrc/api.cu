@@ -158,9 +158,8 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
 
   const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
   const bool tc = io_dtype == GDN_BF16;
-  a.allow_waves = true;
-  const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads) +
-                                     prefill_tc_wave_state_bytes(a)
+  a.allow_overlap = true;
+  const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads)
                                : prefill_simt_scratch_bytes(a.max_chunks, heads);
   void* scratch = nullptr;
   if (off_bytes + work_bytes > 0 &&
@@ -239,6 +238,8 @@ int gdn_testing_prefill_prep(const void* q, const void* k, const void* v, const 
 }
 
 size_t gdn_testing_prefill_image_stride(void) { return prefill_tc_image_stride(); }
+
+int32_t gdn_testing_last_prefill_form(void) { return g_last_tc_form; }
 
 void gdn_testing_set_trace(uint64_t* device_buf, int32_t max_chunks) {
   g_trace = device_buf;

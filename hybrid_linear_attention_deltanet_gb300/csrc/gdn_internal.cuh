@@ -103,7 +103,7 @@ struct PrefillLaunch {
   int64_t max_chunks;   // grid bound for per-chunk kernels
   unsigned* status;
   void* scratch;        // device scratch of the size the path's *_scratch_bytes asks for
-  bool allow_waves;     // tensor-core path may overlap prep and state pass on a helper stream
+  bool allow_overlap;   // tensor-core path may run prep and state pass in one cooperative launch
 };
 
 cudaError_t launch_chunk_offsets(const int32_t* cu_seqlens, int32_t N, int64_t T_total,
@@ -117,11 +117,11 @@ cudaError_t launch_prefill_simt(const PrefillLaunch& a, int io_dtype, cudaStream
 size_t prefill_tc_scratch_bytes(int64_t max_chunks, int32_t H);
 cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool prep_only = false);
 size_t prefill_tc_image_stride();
-// extra scratch (after the images) for the state carried between waves
-size_t prefill_tc_wave_state_bytes(const PrefillLaunch& a);
 // phase-timeline buffer of the tensor-core state pass (test hook)
 extern uint64_t* g_trace;
 extern int32_t g_trace_chunks;
+// launch form of the last tensor-core prefill on this process: 1 fused, 0 split
+extern int32_t g_last_tc_form;
 
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, const float* alpha,
                                const float* beta, float* S, void* out, int32_t N, int32_t H,

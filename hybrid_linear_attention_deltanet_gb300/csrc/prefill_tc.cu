@@ -11,21 +11,31 @@
 //   Q^ = diag(gamma) Q / sqrt(dk)
 //   U  = U~ - W S^T,  O = Q^ S^T + P^ U,  S' = gamma_L S + (diag(d) U)^T K
 //
-// Kernel 1, tc_prep (one CTA per (chunk, head), fully parallel, two CTAs per SM):
+// Prep (fully parallel over (chunk, head) items):
 //   TMA tensor copies of the K, Q, V tiles; [K;Q] K^T on tcgen05 (M=128, N=64,
 //   K=256) -> A and P^; T by a two-level recursive block inverse in fp32 on
-//   the CUDA cores; W^T = K^T T_w^T and U~^T = V^T T_u^T on tcgen05; writes
-//   W, Q^, P^, U~^T and G to scratch as ready-to-load swizzled operand images
-//   (the state pass copies them with 1-D TMA bulk copies).
-// Kernel 2, tc_state (one CTA per (sequence, head, 128-row half of S)):
-//   rows of S are independent, so each CTA owns 128 rows (the MMA M).  The
+//   the CUDA cores; W^T = K^T T_w^T and U~^T = V^T T_u^T on tcgen05.  W, Q^,
+//   U~^T and the decay factors are laid out in shared memory as ready-to-load
+//   swizzled operand images and written to scratch by TMA bulk stores.
+// State pass (one unit per (sequence, head, 128-row half of S)):
+//   rows of S are independent, so each unit owns 128 rows (the MMA M).  The
 //   bf16 copy of its S rows lives in TMEM as an A operand; the fp32 master
-//   copy lives in registers.  Per chunk: D_U = S W^T, D_O = S Q^^T (M=128,
-//   N=64, K=256, A from TMEM); U = U~ - D_U and d*U -> bf16, stored back into
-//   TMEM as A operands; D_S = (dU)^T K (N=256, K=64, K straight from the
+//   copy lives in registers.  Per chunk: [D_U | D_O] = S [W | Q^]^T (M=128,
+//   N=128, K=256, A from TMEM); U = U~ - D_U and d*U -> bf16, stored back
+//   into TMEM as A operands; D_S = (dU)^T K (N=256, K=64, K straight from the
 //   input by a TMA tensor copy) and D_O += U^T P^^T; S = gamma_L S + D_S;
-//   O -> out.  W, Q^, K and P^ are double-buffered (two chunks ahead), the
-//   images of the chunk after are pre-warmed in L2.
+//   O -> out.  W, Q^, K and P^ are double-buffered (two chunks ahead).
+//
+// Two launch forms:
+//   fused  one cooperative launch, one CTA per SM.  The first CTAs run the
+//          state units; the others are prep workers that take items in
+//          chunk-position order and publish each finished image with a
+//          release flag, which a state unit acquires before it copies that
+//          chunk's images.  The sequential pass starts after the first
+//          chunk position instead of after the whole prep.  Used when the
+//          state units leave enough SMs over for the workers.
+//   split  a persistent prep kernel over all items (two CTAs per SM), then
+//          the state kernel (one CTA per unit).
 //
 // Shared-memory operand images use the 128-byte swizzle: rows of 64 bf16,
 // 16-byte chunk index XOR (row % 8), 8-row groups 1024 bytes apart.
@@ -58,155 +68,268 @@ constexpr size_t kImgHalf = 16896;    // 16384 + 512
 constexpr size_t kImgDecay = 16384;   // offset of the decay block inside a half
 constexpr size_t kImgStride = 107520; // kImgU0 + 2 * kImgHalf, rounded to 1 KB
 
-// chunk-position waves (see launch_prefill_tc)
-constexpr int kMaxWaves = 8;
-constexpr int64_t kWaveMinChunks = 32;      // chunk positions per wave, at least
-constexpr int64_t kWaveMaxStateCtas = 120;  // leave SMs free for the overlapping prep
-
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&t);
 }
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-__device__ __forceinline__ uint4 scale8(uint4 v, float s) {
-  v.x = pack_bf16(bf16_lo(v.x) * s, bf16_hi(v.x) * s);
-  v.y = pack_bf16(bf16_lo(v.y) * s, bf16_hi(v.y) * s);
-  v.z = pack_bf16(bf16_lo(v.z) * s, bf16_hi(v.z) * s);
-  v.w = pack_bf16(bf16_lo(v.w) * s, bf16_hi(v.w) * s);
-  return v;
-}
 
 // byte offset of 16-byte chunk `ch` (0..7) of row `row` in a 128-byte-swizzled image
 __device__ __forceinline__ uint32_t sw_chunk(uint32_t row, uint32_t ch) {
   return row * 128u + ((ch ^ (row & 7u)) << 4);
 }
 
-// ============================================================ prep kernel
-constexpr int kPrepThreads = 256;
-// shared memory layout (offsets from the 1024-aligned base)
-constexpr uint32_t kP_KQ = 0;          // 64 KB: K-block b at b*16K: rows 0-63 K, 64-127 Q;
-                                       //        V replaces Q once Q is consumed
-constexpr uint32_t kP_A = 65536;       // fp32 [64][65]; afterwards T_w (8 KB) and T_u (8 KB)
-constexpr uint32_t kP_TW = 65536;
-constexpr uint32_t kP_TU = 73728;
-constexpr uint32_t kP_T = kP_A + 64 * 65 * 4;      // fp32 [64][65]
-constexpr uint32_t kP_Y1 = kP_T + 64 * 65 * 4;     // fp32 [2][16][16]
-constexpr uint32_t kP_Y2 = kP_Y1 + 2 * 256 * 4;    // fp32 [32][33]
-constexpr uint32_t kP_G = kP_Y2 + 32 * 33 * 4;     // fp32 [64]
-constexpr uint32_t kP_B = kP_G + 256;              // fp32 [64]
-constexpr uint32_t kP_GAM = kP_B + 256;            // fp32 [64]: gamma_r = exp(G_r)
-constexpr uint32_t kP_END = kP_GAM + 256;
-constexpr uint32_t kPrepSmem = kP_END + 1024;
-constexpr int kLd = 65;                            // row stride of the fp32 64 x 64 tiles
-constexpr int kPrepTraceOffset = 4096;             // uint64 slots before the prep timeline
-constexpr int kWaveTraceOffset = 3072;             // per-wave launch timeline (global timer)
+// Bounded spin on a ready flag (fused form): false after one second.
+constexpr uint64_t kReadyWaitNs = 1000000000ull;
+__device__ __forceinline__ bool ready_wait(const uint32_t* f) {
+  if (!ld_acquire_gpu(f)) {
+    const uint64_t t_start = globaltimer_ns();
+    while (!ld_acquire_gpu(f)) {
+      if (globaltimer_ns() - t_start > kReadyWaitNs) return false;
+      __nanosleep(64);
+    }
+  }
+  fence_proxy_async_global();
+  return true;
+}
+__device__ __forceinline__ bool ready_now(const uint32_t* f) {
+  if (!ld_acquire_gpu(f)) return false;
+  fence_proxy_async_global();
+  return true;
+}
 
-__global__ void __launch_bounds__(kPrepThreads, 2)
-tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ alpha,
-               const float* __restrict__ beta, SeqMap map, int32_t H,
-               uint8_t* __restrict__ scratch, unsigned* status, uint64_t* __restrict__ trace,
-               int32_t win_p0, int32_t win_np, uint64_t* __restrict__ wave_trace, int32_t wave) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align_smem_1024(smem_raw);
-  float* sA = (float*)(sm + kP_A);
-  float* sT = (float*)(sm + kP_T);
-  float* sY1 = (float*)(sm + kP_Y1);
-  float* sY2 = (float*)(sm + kP_Y2);
-  float* sG = (float*)(sm + kP_G);
-  float* sB = (float*)(sm + kP_B);
-  float* sGam = (float*)(sm + kP_GAM);
-  __shared__ uint64_t bar_kq, bar_v, bar_a, bar_bc;
+// ============================================================ prep
+constexpr int kPrepThreads = 256;
+constexpr int kLd = 65;                  // row stride of the fp32 64 x 64 tiles
+constexpr int kPrepTraceOffset = 4096;   // uint64 slots before the prep timeline
+// global-timer timeline of one call (test hook): per state unit u < 128 its
+// start, first chunk top and end; per prep worker w < 200 its start and end;
+// the start of each of the first 240 items of worker 0
+constexpr int kUnitTimes = 3072, kMaxTracedUnits = 128;
+constexpr int kWorkerTimes = kUnitTimes + 3 * kMaxTracedUnits, kMaxTracedWorkers = 200;
+constexpr int kItemTimes = kWorkerTimes + 2 * kMaxTracedWorkers, kMaxTracedItems = 240;
+static_assert(kItemTimes + kMaxTracedItems <= kPrepTraceOffset, "trace layout");
+constexpr int kPrepIO = 64;              // thread that issues the prep's bulk copies
+
+// Shared-memory layout of the prep (offsets from the 1024-aligned base).
+// kBufs K/Q buffers of 64 KB; K-block b at b*16K holds rows 0-63 of K, then
+// rows 64-127 of Q.  Within a buffer's life the Q slots hold Q, then the Q^
+// rows on their way out, then V; after the W / U~ MMAs the K slots hold the
+// W rows and the V slots the U~^T rows on their way out.
+template <int kBufs>
+struct PrepSmem {
+  static constexpr uint32_t KQ = 0;
+  static constexpr uint32_t A = 65536u * kBufs;      // fp32 [64][65]; then T_w, T_u
+  static constexpr uint32_t TW = A;                  //   (bf16 K-major 64 x 64, 8 KB each)
+  static constexpr uint32_t TU = A + 8192;
+  static constexpr uint32_t T = A + 64 * kLd * 4;    // fp32 [64][65]
+  static constexpr uint32_t Y1 = T + 64 * kLd * 4;   // fp32 [2][16][16]; decay block at the end
+  static constexpr uint32_t Y2 = Y1 + 2 * 256 * 4;   // fp32 [32][33]
+  static constexpr uint32_t G = Y2 + 32 * 33 * 4;    // fp32 [64]
+  static constexpr uint32_t B = G + 256;             // fp32 [64]
+  static constexpr uint32_t GAM = B + 256;           // fp32 [64]: gamma_r = exp(G_r)
+  static constexpr uint32_t END = GAM + 256;
+  static constexpr uint32_t BYTES = END + 1024;      // + alignment slack
+};
+
+struct PrepItem {
+  int64_t ci = 0, t0 = 0;   // global chunk index, first token
+  int h = 0, L = 0;         // head, valid rows
+};
+
+// Item j of the prep.  kOrdered: chunk positions in order (position p of
+// every sequence and head before position p + 1), so that the next chunk of
+// every state unit is among the first finished; otherwise global chunk order
+// with the head fastest.  False for positions past a sequence's end.
+template <bool kOrdered>
+__device__ __forceinline__ bool prep_item(const SeqMap& map, int32_t H, int64_t j, PrepItem& it) {
+  if (!kOrdered) {
+    int n;
+    it.ci = j / H;
+    it.h = (int)(j % H);
+    return map.locate(it.ci, n, it.t0, it.L);
+  }
+  const int64_t nh = (int64_t)map.N * H;
+  const int64_t p = j / nh;
+  const int rem = (int)(j - p * nh);
+  const int n = rem / H;
+  it.h = rem - n * H;
+  const int64_t cb = map.chunk_begin(n);
+  if (cb + p >= map.chunk_end(n)) return false;
+  it.ci = cb + p;
+  it.t0 = map.seq_begin(n) + p * kC;
+  const int64_t left = map.seq_end(n) - it.t0;
+  it.L = left < kC ? (int)left : kC;
+  return true;
+}
+
+// The prep over items worker, worker + n_workers, ... < n_items.
+// kFused: two K/Q buffers (the next item's tiles load during this one),
+// items in chunk-position order, and a ready flag per finished item.
+template <bool kFused>
+__device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
+                                          const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                          const float* __restrict__ alpha,
+                                          const float* __restrict__ beta, const SeqMap& map,
+                                          int32_t H, uint8_t* __restrict__ scratch,
+                                          uint32_t* ready, unsigned* status,
+                                          uint64_t* __restrict__ trace,
+                                          uint64_t* __restrict__ timeline, int64_t n_items,
+                                          int64_t worker, int64_t n_workers) {
+  constexpr int kBufs = kFused ? 2 : 1;
+  using Lay = PrepSmem<kBufs>;
+  float* sA = (float*)(sm + Lay::A);
+  float* sT = (float*)(sm + Lay::T);
+  float* sY1 = (float*)(sm + Lay::Y1);
+  float* sY2 = (float*)(sm + Lay::Y2);
+  float* sG = (float*)(sm + Lay::G);
+  float* sB = (float*)(sm + Lay::B);
+  float* sGam = (float*)(sm + Lay::GAM);
+  float* sDecay = (float*)(sm + Lay::Y1);   // d[64], G[64] staged for the bulk store
+  __shared__ uint64_t bar_kq[kBufs], bar_v, bar_a, bar_bc;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
 
-  // win_np > 0 (dense batches): this launch covers chunk positions
-  // [win_p0, win_p0 + win_np) of every sequence; otherwise every chunk
-  const int64_t ci = win_np > 0 ? (int64_t)(blockIdx.x / win_np) * map.chunks_per_seq + win_p0 +
-                                      blockIdx.x % win_np
-                                : (int64_t)blockIdx.x;
-  const int h = blockIdx.y;
-  int n, L;
-  int64_t t0;
-  if (!map.locate(ci, n, t0, L)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, hv = warp >> 2;
   const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-  uint8_t* img = scratch + (size_t)(ci * H + h) * kImgStride;
-  // optional phase timeline (test hook): thread 0 of CTA (0, 0) stamps its
-  // SM cycle counter at 10 points
-  const bool tracing = trace && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0;
+  // optional phase timeline (test hook): thread 0 of worker 0 stamps its SM
+  // cycle counter at 9 points of its first item
+  bool tracing = trace && tid == 0 && worker == 0;
   auto stamp = [&](int k) {
     if (tracing) trace[k] = clock64();
   };
-  stamp(0);
-  if (wave_trace && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0)
-    wave_trace[100 + 2 * wave] = globaltimer_ns();
+  const bool timed = timeline && tid == 0 && worker < kMaxTracedWorkers;
+  if (timed) timeline[kWorkerTimes + 2 * worker] = globaltimer_ns();
+  int n_done = 0;
 
   if (tid == 0) {
-    mbar_init(&bar_kq, 1);
+    for (int b = 0; b < kBufs; ++b) mbar_init(&bar_kq[b], 1);
     mbar_init(&bar_v, 1);
     mbar_init(&bar_a, 1);
     mbar_init(&bar_bc, 1);
     fence_barrier_init();
     s_abort = 0;
-    mbar_arrive_expect_tx(&bar_kq, 65536);
-    for (int b = 0; b < 4; ++b) {
-      tma_load_3d(sm + kP_KQ + b * 16384, &tm_k, b * 64, h, (int32_t)t0, &bar_kq);
-      tma_load_3d(sm + kP_KQ + b * 16384 + 8192, &tm_q, b * 64, h, (int32_t)t0, &bar_kq);
-    }
   }
   if (warp == 0) tmem_alloc(&tmem_base, 256);
-  // decay prefix G_r = sum_{s <= r} log alpha_s (pad rows: log alpha = 0, beta = 0)
-  float g_scan = 0.f;
-  if (tid < kC) {
-    const bool ok = tid < L;
-    g_scan = ok ? logf(alpha[(t0 + tid) * H + h]) : 0.f;
-    sB[tid] = ok ? beta[(t0 + tid) * H + h] : 0.f;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, g_scan, o);
-      if (lane >= o) g_scan += y;
-    }
-    if (tid < 32) sG[tid] = g_scan;
-  }
-  for (int e = tid; e < 64 * kLd; e += kPrepThreads) sT[e] = 0.f;
+  tc_fence_before();
   __syncthreads();
-  if (tid >= 32 && tid < kC) sG[tid] = g_scan + sG[31];
-  if (tid < kC) sGam[tid] = __expf(tid < 32 ? g_scan : g_scan + sG[31]);
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  __syncthreads();
-  stamp(1);
 
-  // ---- [K; Q] K^T  ->  TMEM columns [0, 64): lanes 0-63 K K^T, 64-127 Q K^T
-  if (tid == 0) {
-    if (!mbar_wait(&bar_kq, 0)) {
-      s_abort = 1;
-    } else {
-      tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, 64, 0, 0);
-      const uint32_t base = smem_u32(sm + kP_KQ);
-      for (int s = 0; s < 16; ++s) {
-        const uint64_t d = smem_desc(base + (s >> 2) * 16384u + (s & 3) * 32u, 16, 1024,
-                                     kSwizzle128B);
-        mma_bf16(tmem, d, d, idesc, s > 0);
-      }
-      mma_commit(&bar_a);
+  auto next_valid = [&](int64_t j, PrepItem& it) -> int64_t {
+    for (; j < n_items; j += n_workers)
+      if (prep_item<kFused>(map, H, j, it)) return j;
+    return n_items;
+  };
+  // copies issued by kPrepIO, counted per barrier for a clean exit after a timeout
+  uint32_t n_kq[kBufs] = {}, n_v = 0;
+  auto issue_kq = [&](const PrepItem& it, int b) {
+    uint8_t* dst = sm + Lay::KQ + b * 65536;
+    mbar_arrive_expect_tx(&bar_kq[b], 65536);
+    for (int kb = 0; kb < 4; ++kb) {
+      tma_load_3d(dst + kb * 16384, tm_k, kb * 64, it.h, (int32_t)it.t0, &bar_kq[b]);
+      tma_load_3d(dst + kb * 16384 + 8192, tm_q, kb * 64, it.h, (int32_t)it.t0, &bar_kq[b]);
+    }
+    ++n_kq[b];
+  };
+  auto img_of = [&](const PrepItem& it) {
+    return scratch + (size_t)(it.ci * H + it.h) * kImgStride;
+  };
+  // (kPrepIO) the item's bulk stores have landed: raise its ready flag.  The
+  // P^ rows, written by other threads with plain stores, were fenced by
+  // their writers before the barriers that precede this.
+  auto publish = [&](const PrepItem& it) {
+    bulk_wait_all();
+    fence_proxy_async_global();
+    st_release_gpu(ready + it.ci * H + it.h, 1u);
+  };
+
+  PrepItem cur, nxt, prev;
+  bool have_prev = false;
+  int64_t j = next_valid(worker, cur);
+  uint32_t kq_ph[kBufs] = {};   // parity of each K/Q buffer's next phase
+  uint32_t ph = 0;              // parity of bar_v / bar_a / bar_bc for this item
+  int buf = 0;
+  float a_cur = 1.f, b_cur = 0.f;   // this item's gates (threads < C)
+  if (kFused && j < n_items) {
+    if (tid == kPrepIO) issue_kq(cur, 0);
+    if (tid < kC && tid < cur.L) {
+      a_cur = alpha[(cur.t0 + tid) * H + cur.h];
+      b_cur = beta[(cur.t0 + tid) * H + cur.h];
     }
   }
-  {
-    // Q^ = gamma_r Q / sqrt(dk), transposed into an MN-major image (row c =
-    // Q^[0..63][c]) so that it sits beside W as one N = 128 operand
-    if (!mbar_wait(&bar_kq, 0)) { s_abort = 1; }
+
+  while (j < n_items) {
+    const int64_t jn = next_valid(j + n_workers, nxt);
+    const int L = cur.L;
+    uint8_t* const img = img_of(cur);
+    uint8_t* const kq = sm + Lay::KQ + buf * 65536;
+    stamp(0);
+    if (timed && worker == 0 && n_done < kMaxTracedItems) timeline[kItemTimes + n_done] = globaltimer_ns();
+    ++n_done;
+    float a_nx = 1.f, b_nx = 0.f;
+    if (!kFused) {
+      // one buffer: the previous item's stores must have read it
+      if (tid == kPrepIO) {
+        bulk_wait_read_all();
+        issue_kq(cur, 0);
+      }
+      if (tid < kC && tid < L) {
+        a_cur = alpha[(cur.t0 + tid) * H + cur.h];
+        b_cur = beta[(cur.t0 + tid) * H + cur.h];
+      }
+    } else if (jn < n_items && tid < kC && tid < nxt.L) {   // gates of the next item
+      a_nx = alpha[(nxt.t0 + tid) * H + nxt.h];
+      b_nx = beta[(nxt.t0 + tid) * H + nxt.h];
+    }
+    // decay prefix G_r = sum_{s <= r} log alpha_s (pad rows: log alpha = 0, beta = 0)
+    float g_scan = 0.f;
+    if (tid < kC) {
+      const bool ok = tid < L;
+      g_scan = ok ? logf(a_cur) : 0.f;
+      sB[tid] = ok ? b_cur : 0.f;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, g_scan, o);
+        if (lane >= o) g_scan += y;
+      }
+      if (tid < 32) sG[tid] = g_scan;
+    }
+    for (int e = tid; e < 64 * kLd; e += kPrepThreads) sT[e] = 0.f;
+    __syncthreads();
+    if (tid >= 32 && tid < kC) sG[tid] = g_scan + sG[31];
+    if (tid < kC) sGam[tid] = __expf(tid < 32 ? g_scan : g_scan + sG[31]);
+    __syncthreads();
+    stamp(1);
+
+    // ---- [K; Q] K^T  ->  TMEM columns [0, 64): lanes 0-63 K K^T, 64-127 Q K^T
+    if (tid == 0) {
+      if (!mbar_wait(&bar_kq[buf], kq_ph[buf])) {
+        s_abort = 1;
+      } else {
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16(128, 64, 0, 0);
+        const uint32_t base = smem_u32(kq);
+        for (int s = 0; s < 16; ++s) {
+          const uint64_t d = smem_desc(base + (s >> 2) * 16384u + (s & 3) * 32u, 16, 1024,
+                                       kSwizzle128B);
+          mma_bf16(tmem, d, d, idesc, s > 0);
+        }
+        mma_commit(&bar_a);
+      }
+    }
+    // Q^ = gamma_r Q / sqrt(dk) in registers, row c of its MN-major image
+    // (Q^[0..63][c]), so that it sits beside W as one N = 128 operand
+    uint32_t qv[8][4];
+    if (!mbar_wait(&bar_kq[buf], kq_ph[buf])) s_abort = 1;
     {
       const int c = tid;   // d_k column, 0..255
-      const uint8_t* qb = sm + kP_KQ + (c >> 6) * 16384 + 8192;
+      const uint8_t* qb = kq + (c >> 6) * 16384 + 8192;
       const uint32_t cc = c & 63;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
-        uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int r0 = 8 * ch + 2 * e, r1 = r0 + 1;
@@ -216,226 +339,263 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
               qb + r1 * 128 + ((((cc >> 3) ^ (r1 & 7)) << 4) | ((cc & 7) << 1))));
           const float g0 = r0 < L ? kScale * sGam[r0] : 0.f;
           const float g1 = r1 < L ? kScale * sGam[r1] : 0.f;
-          w[e] = pack_bf16(q0 * g0, q1 * g1);
+          qv[ch][e] = pack_bf16(q0 * g0, q1 * g1);
         }
-        *reinterpret_cast<uint4*>(img + kImgQ + sw_chunk(c, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-  }
-  stamp(2);
-  __syncthreads();
-  if (s_abort) goto teardown;
-  if (!mbar_wait(&bar_a, 0)) { flag_status(status, GDN_ERR_TIMEOUT); s_abort = 1; }
-  __syncthreads();
-  if (s_abort) goto teardown;
-  stamp(3);
-  tc_fence_after();
-  {
-    uint32_t g[32];
-    tmem_ld32(tmem + lane_off + 32 * hv, g);
-    tmem_ld_wait();
-    const int row = 32 * quarter + lane;
-    if (row < kC) {   // A = strict_lower(beta_r Gam_rj k_r.k_j), columns 32hv .. 32hv+31
-      const float Gr = sG[row], br = sB[row];
+    kq_ph[buf] ^= 1u;
+    stamp(2);
+    // two buffers: the other one is free once the previous item's stores
+    // have read it; publish that item and start the next item's tiles there
+    if (kFused && tid == kPrepIO) {
+      if (have_prev) publish(prev);
+      if (jn < n_items) issue_kq(nxt, buf ^ 1);
+    }
+    __syncthreads();
+    if (s_abort) goto teardown;
+    if (!mbar_wait(&bar_a, ph)) { flag_status(status, GDN_ERR_TIMEOUT); s_abort = 1; }
+    __syncthreads();
+    if (s_abort) goto teardown;
+    stamp(3);
+    tc_fence_after();
+    {  // Q^ rows over Q (the Gram MMA has finished reading it)
+      const int c = tid;
+      uint8_t* qs = kq + (c >> 6) * 16384 + 8192;
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = 32 * hv + jj;
-        sA[row * kLd + j] = j < row ? br * __expf(Gr - sG[j]) * __uint_as_float(g[jj]) : 0.f;
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(qs + sw_chunk(c & 63, ch)) =
+            make_uint4(qv[ch][0], qv[ch][1], qv[ch][2], qv[ch][3]);
+    }
+    {
+      uint32_t g[32];
+      tmem_ld32(tmem + lane_off + 32 * hv, g);
+      tmem_ld_wait();
+      const int row = 32 * quarter + lane;
+      if (row < kC) {   // A = strict_lower(beta_r Gam_rj k_r.k_j), columns 32hv .. 32hv+31
+        const float Gr = sG[row], br = sB[row];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int jc = 32 * hv + jj;
+          sA[row * kLd + jc] = jc < row ? br * __expf(Gr - sG[jc]) * __uint_as_float(g[jj]) : 0.f;
+        }
+      } else {          // P^ = lower(Gam_rj q_r.k_j) / sqrt(dk), chunks 4hv .. 4hv+3 of row r
+        const int r = row - kC;
+        const float Gr = sG[r];
+#pragma unroll
+        for (int cq = 0; cq < 4; ++cq) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j0 = 32 * hv + 8 * cq + 2 * e, j1 = j0 + 1;
+            const float p0 = (j0 <= r && r < L) ? kScale * __expf(Gr - sG[j0]) * __uint_as_float(g[8 * cq + 2 * e]) : 0.f;
+            const float p1 = (j1 <= r && r < L) ? kScale * __expf(Gr - sG[j1]) * __uint_as_float(g[8 * cq + 2 * e + 1]) : 0.f;
+            w[e] = pack_bf16(p0, p1);
+          }
+          *reinterpret_cast<uint4*>(img + kImgP + sw_chunk(r, 4 * hv + cq)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (kFused) __threadfence();   // P^ is visible before the item's ready flag
       }
-    } else {          // P^ = lower(Gam_rj q_r.k_j) / sqrt(dk), chunks 4hv .. 4hv+3 of row r
-      const int r = row - kC;
-      const float Gr = sG[r];
+    }
+    // Q^ out of the Q slots, then V into them
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == kPrepIO) {
+      for (int b = 0; b < 4; ++b) tma_store_1d(img + kImgQ + b * 8192, kq + b * 16384 + 8192, 8192);
+      bulk_commit();
+      bulk_wait_read_all();
+      mbar_arrive_expect_tx(&bar_v, 32768);
+      for (int b = 0; b < 4; ++b)
+        tma_load_3d(kq + b * 16384 + 8192, tm_v, b * 64, cur.h, (int32_t)cur.t0, &bar_v);
+      ++n_v;
+    }
+
+    stamp(4);
+    // ---- T = (I + A)^{-1}: 16 x 16 diagonal inverses, then two levels of
+    //      [[T1, 0], [X, T2]] with X = -T2 A21 T1
+    if (tid < 64) {
+      const int b = tid >> 4, c = tid & 15, o = 16 * b;
+      float x[16];
 #pragma unroll
-      for (int cq = 0; cq < 4; ++cq) {
-        uint32_t w[4];
+      for (int r = 0; r < 16; ++r) x[r] = r == c ? 1.f : 0.f;
+#pragma unroll
+      for (int r = 1; r < 16; ++r) {
+        float acc = 0.f;
+#pragma unroll
+        for (int jc = 0; jc < r; ++jc) acc = fmaf(sA[(o + r) * kLd + o + jc], x[jc], acc);
+        if (r > c) x[r] = -acc;
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) sT[(o + r) * kLd + o + c] = x[r];
+    }
+    __syncthreads();
+    {  // level 1, blocks p = 0, 1: Y = A[16(2p+1):, 16(2p):] T_{2p};  T_off = -T_{2p+1} Y
+      const int p = tid >> 7, c = tid & 15, r0 = (tid >> 4) & 7;
+      const int ro = 16 * (2 * p + 1), co = 16 * (2 * p);
+      float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float t = sT[(co + k) * kLd + co + c];
+        y0 = fmaf(sA[(ro + r0) * kLd + co + k], t, y0);
+        y1 = fmaf(sA[(ro + r0 + 8) * kLd + co + k], t, y1);
+      }
+      sY1[p * 256 + r0 * 16 + c] = y0;
+      sY1[p * 256 + (r0 + 8) * 16 + c] = y1;
+      __syncthreads();
+      float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float y = sY1[p * 256 + k * 16 + c];
+        z0 = fmaf(sT[(ro + r0) * kLd + ro + k], y, z0);
+        z1 = fmaf(sT[(ro + r0 + 8) * kLd + ro + k], y, z1);
+      }
+      sT[(ro + r0) * kLd + co + c] = -z0;
+      sT[(ro + r0 + 8) * kLd + co + c] = -z1;
+    }
+    __syncthreads();
+    {  // level 2: Y = A[32:, :32] T[:32, :32];  T[32:, :32] = -T[32:, 32:] Y
+      const int c = tid & 31, r0 = tid >> 5;
+      float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+      for (int k = 0; k < 32; ++k) {
+        const float t = sT[k * kLd + c];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) y[m] = fmaf(sA[(32 + r0 + 8 * m) * kLd + k], t, y[m]);
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) sY2[(r0 + 8 * m) * 33 + c] = y[m];
+      __syncthreads();
+      float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+      for (int k = 0; k < 32; ++k) {
+        const float yy = sY2[k * 33 + c];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) z[m] = fmaf(sT[(32 + r0 + 8 * m) * kLd + 32 + k], yy, z[m]);
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) sT[(32 + r0 + 8 * m) * kLd + c] = -z[m];
+    }
+    __syncthreads();
+    stamp(5);
+    // T_w = T diag(beta gamma), T_u = T diag(beta): K-major bf16 images over the dead A tile
+    {
+      const int r = tid >> 2, c2 = tid & 3;
+#pragma unroll
+      for (int cq = 0; cq < 2; ++cq) {
+        const int ch = 2 * c2 + cq;
+        uint32_t ww[4], uu[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int j0 = 32 * hv + 8 * cq + 2 * e, j1 = j0 + 1;
-          const float p0 = (j0 <= r && r < L) ? kScale * __expf(Gr - sG[j0]) * __uint_as_float(g[8 * cq + 2 * e]) : 0.f;
-          const float p1 = (j1 <= r && r < L) ? kScale * __expf(Gr - sG[j1]) * __uint_as_float(g[8 * cq + 2 * e + 1]) : 0.f;
-          w[e] = pack_bf16(p0, p1);
+          const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
+          const float t0v = j0 <= r ? sT[r * kLd + j0] : 0.f;
+          const float t1v = j1 <= r ? sT[r * kLd + j1] : 0.f;
+          const float b0 = sB[j0], b1 = sB[j1];
+          ww[e] = pack_bf16(t0v * b0 * sGam[j0], t1v * b1 * sGam[j1]);
+          uu[e] = pack_bf16(t0v * b0, t1v * b1);
         }
-        *reinterpret_cast<uint4*>(img + kImgP + sw_chunk(r, 4 * hv + cq)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(sm + Lay::TW + sw_chunk(r, ch)) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+        *reinterpret_cast<uint4*>(sm + Lay::TU + sw_chunk(r, ch)) = make_uint4(uu[0], uu[1], uu[2], uu[3]);
       }
     }
-  }
-  // the Q slots are free (MMA done, Q^ copied out): bring V there
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&bar_v, 32768);
-    for (int b = 0; b < 4; ++b)
-      tma_load_3d(sm + kP_KQ + b * 16384 + 8192, &tm_v, b * 64, h, (int32_t)t0, &bar_v);
-  }
-
-  stamp(4);
-  // ---- T = (I + A)^{-1}: 16 x 16 diagonal inverses, then two levels of
-  //      [[T1, 0], [X, T2]] with X = -T2 A21 T1
-  if (tid < 64) {
-    const int b = tid >> 4, c = tid & 15, o = 16 * b;
-    float x[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) x[r] = r == c ? 1.f : 0.f;
-#pragma unroll
-    for (int r = 1; r < 16; ++r) {
-      float acc = 0.f;
-#pragma unroll
-      for (int j = 0; j < r; ++j) acc = fmaf(sA[(o + r) * kLd + o + j], x[j], acc);
-      if (r > c) x[r] = -acc;
-    }
-#pragma unroll
-    for (int r = 0; r < 16; ++r) sT[(o + r) * kLd + o + c] = x[r];
-  }
-  __syncthreads();
-  {  // level 1, blocks p = 0, 1: Y = A[16(2p+1):, 16(2p):] T_{2p};  T_off = -T_{2p+1} Y
-    const int p = tid >> 7, c = tid & 15, r0 = (tid >> 4) & 7;
-    const int ro = 16 * (2 * p + 1), co = 16 * (2 * p);
-    float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float t = sT[(co + k) * kLd + co + c];
-      y0 = fmaf(sA[(ro + r0) * kLd + co + k], t, y0);
-      y1 = fmaf(sA[(ro + r0 + 8) * kLd + co + k], t, y1);
-    }
-    sY1[p * 256 + r0 * 16 + c] = y0;
-    sY1[p * 256 + (r0 + 8) * 16 + c] = y1;
+    fence_proxy_async_smem();
     __syncthreads();
-    float z0 = 0.f, z1 = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float y = sY1[p * 256 + k * 16 + c];
-      z0 = fmaf(sT[(ro + r0) * kLd + ro + k], y, z0);
-      z1 = fmaf(sT[(ro + r0 + 8) * kLd + ro + k], y, z1);
-    }
-    sT[(ro + r0) * kLd + co + c] = -z0;
-    sT[(ro + r0 + 8) * kLd + co + c] = -z1;
-  }
-  __syncthreads();
-  {  // level 2: Y = A[32:, :32] T[:32, :32];  T[32:, :32] = -T[32:, 32:] Y
-    const int c = tid & 31, r0 = tid >> 5;
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float t = sT[k * kLd + c];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) y[m] = fmaf(sA[(32 + r0 + 8 * m) * kLd + k], t, y[m]);
-    }
-#pragma unroll
-    for (int m = 0; m < 4; ++m) sY2[(r0 + 8 * m) * 33 + c] = y[m];
-    __syncthreads();
-    float z[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float yy = sY2[k * 33 + c];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) z[m] = fmaf(sT[(32 + r0 + 8 * m) * kLd + 32 + k], yy, z[m]);
-    }
-#pragma unroll
-    for (int m = 0; m < 4; ++m) sT[(32 + r0 + 8 * m) * kLd + c] = -z[m];
-  }
-  __syncthreads();
-  stamp(5);
-  // T_w = T diag(beta gamma), T_u = T diag(beta): K-major bf16 images over the dead A tile
-  {
-    const int r = tid >> 2, c2 = tid & 3;
-#pragma unroll
-    for (int cq = 0; cq < 2; ++cq) {
-      const int ch = 2 * c2 + cq;
-      uint32_t ww[4], uu[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
-        const float t0v = j0 <= r ? sT[r * kLd + j0] : 0.f;
-        const float t1v = j1 <= r ? sT[r * kLd + j1] : 0.f;
-        const float b0 = sB[j0], b1 = sB[j1];
-        ww[e] = pack_bf16(t0v * b0 * sGam[j0], t1v * b1 * sGam[j1]);
-        uu[e] = pack_bf16(t0v * b0, t1v * b1);
-      }
-      *reinterpret_cast<uint4*>(sm + kP_TW + sw_chunk(r, ch)) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
-      *reinterpret_cast<uint4*>(sm + kP_TU + sw_chunk(r, ch)) = make_uint4(uu[0], uu[1], uu[2], uu[3]);
-    }
-  }
-  fence_proxy_async_smem();
-  __syncthreads();
 
-  stamp(6);
-  // ---- W^T = K^T T_w^T and U~^T = V^T T_u^T, two 128-row halves each
-  if (tid == 0) {
-    if (!mbar_wait(&bar_v, 0)) {
-      s_abort = 1;
-    } else {
-      tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, 64, 1, 0);
-      const uint32_t kq = smem_u32(sm + kP_KQ);
-      const uint32_t tw = smem_u32(sm + kP_TW), tu = smem_u32(sm + kP_TU);
-      for (int hh = 0; hh < 2; ++hh) {
-        for (int s = 0; s < 4; ++s)
-          mma_bf16(tmem + hh * 64, smem_desc(kq + hh * 32768 + s * 2048, 16384, 1024, kSwizzle128B),
-                   smem_desc(tw + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
-        for (int s = 0; s < 4; ++s)
-          mma_bf16(tmem + 128 + hh * 64,
-                   smem_desc(kq + 8192 + hh * 32768 + s * 2048, 16384, 1024, kSwizzle128B),
-                   smem_desc(tu + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
-      }
-      mma_commit(&bar_bc);
-    }
-  }
-  __syncthreads();
-  if (s_abort) goto teardown;
-  if (!mbar_wait(&bar_bc, 0)) { flag_status(status, GDN_ERR_TIMEOUT); s_abort = 1; }
-  __syncthreads();
-  if (s_abort) goto teardown;
-  stamp(7);
-  tc_fence_after();
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const uint32_t c = 128 * hh + 32 * quarter + lane;   // d_k row of W^T / d_v row of U~^T
-#pragma unroll
-    for (int part = 0; part < 2; ++part) {               // 0: W, 1: U~^T
-      uint32_t g[32];
-      tmem_ld32(tmem + lane_off + part * 128 + hh * 64 + 32 * hv, g);
-      tmem_ld_wait();
-      // W rows c; U~^T rows c live in the half image of their 128-row half
-      uint8_t* dst = part == 0 ? img + kImgW : img + kImgU0 + hh * kImgHalf - hh * 128 * 128;
-#pragma unroll
-      for (int cq = 0; cq < 4; ++cq) {
-        const uint32_t w0 = pack_bf16(__uint_as_float(g[8 * cq]), __uint_as_float(g[8 * cq + 1]));
-        const uint32_t w1 = pack_bf16(__uint_as_float(g[8 * cq + 2]), __uint_as_float(g[8 * cq + 3]));
-        const uint32_t w2 = pack_bf16(__uint_as_float(g[8 * cq + 4]), __uint_as_float(g[8 * cq + 5]));
-        const uint32_t w3 = pack_bf16(__uint_as_float(g[8 * cq + 6]), __uint_as_float(g[8 * cq + 7]));
-        *reinterpret_cast<uint4*>(dst + sw_chunk(c, 4 * hv + cq)) = make_uint4(w0, w1, w2, w3);
+    stamp(6);
+    // ---- W^T = K^T T_w^T and U~^T = V^T T_u^T, two 128-row halves each
+    if (tid == 0) {
+      if (!mbar_wait(&bar_v, ph)) {
+        s_abort = 1;
+      } else {
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16(128, 64, 1, 0);
+        const uint32_t kqa = smem_u32(kq);
+        const uint32_t tw = smem_u32(sm + Lay::TW), tu = smem_u32(sm + Lay::TU);
+        for (int hh = 0; hh < 2; ++hh) {
+          for (int s = 0; s < 4; ++s)
+            mma_bf16(tmem + hh * 64, smem_desc(kqa + hh * 32768 + s * 2048, 16384, 1024, kSwizzle128B),
+                     smem_desc(tw + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
+          for (int s = 0; s < 4; ++s)
+            mma_bf16(tmem + 128 + hh * 64,
+                     smem_desc(kqa + 8192 + hh * 32768 + s * 2048, 16384, 1024, kSwizzle128B),
+                     smem_desc(tu + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
+        }
+        mma_commit(&bar_bc);
       }
     }
-  }
-  if (tid < kC) {
-    const float d = tid < L ? __expf(sG[L - 1] - sG[tid]) : 0.f;
+    __syncthreads();
+    if (s_abort) goto teardown;
+    if (!mbar_wait(&bar_bc, ph)) { flag_status(status, GDN_ERR_TIMEOUT); s_abort = 1; }
+    __syncthreads();
+    if (s_abort) goto teardown;
+    stamp(7);
+    tc_fence_after();
+    // W rows c over the K slots, U~^T rows over the V slots (both consumed)
+#pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      float* blk = reinterpret_cast<float*>(img + kImgU0 + hh * kImgHalf + kImgDecay);
-      blk[tid] = d;
-      blk[64 + tid] = sG[tid];
+      const uint32_t c = 128 * hh + 32 * quarter + lane;   // d_k row of W^T / d_v row of U~^T
+      uint8_t* rowblk = kq + (c >> 6) * 16384;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {               // 0: W, 1: U~^T
+        uint32_t g[32];
+        tmem_ld32(tmem + lane_off + part * 128 + hh * 64 + 32 * hv, g);
+        tmem_ld_wait();
+        uint8_t* dst = rowblk + part * 8192;
+#pragma unroll
+        for (int cq = 0; cq < 4; ++cq) {
+          const uint32_t w0 = pack_bf16(__uint_as_float(g[8 * cq]), __uint_as_float(g[8 * cq + 1]));
+          const uint32_t w1 = pack_bf16(__uint_as_float(g[8 * cq + 2]), __uint_as_float(g[8 * cq + 3]));
+          const uint32_t w2 = pack_bf16(__uint_as_float(g[8 * cq + 4]), __uint_as_float(g[8 * cq + 5]));
+          const uint32_t w3 = pack_bf16(__uint_as_float(g[8 * cq + 6]), __uint_as_float(g[8 * cq + 7]));
+          *reinterpret_cast<uint4*>(dst + sw_chunk(c & 63, 4 * hv + cq)) = make_uint4(w0, w1, w2, w3);
+        }
+      }
     }
+    if (tid < kC) {
+      sDecay[tid] = tid < L ? __expf(sG[L - 1] - sG[tid]) : 0.f;
+      sDecay[64 + tid] = sG[tid];
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == kPrepIO) {
+      for (int b = 0; b < 4; ++b) {
+        tma_store_1d(img + kImgW + b * 8192, kq + b * 16384, 8192);
+        tma_store_1d(img + kImgU0 + (b >> 1) * kImgHalf + (b & 1) * 8192, kq + b * 16384 + 8192, 8192);
+      }
+      for (int hh = 0; hh < 2; ++hh) tma_store_1d(img + kImgU0 + hh * kImgHalf + kImgDecay, sDecay, 512);
+      bulk_commit();
+    }
+    stamp(8);
+    tracing = false;
+    prev = cur;
+    have_prev = true;
+    cur = nxt;
+    j = jn;
+    a_cur = a_nx;
+    b_cur = b_nx;
+    if (kFused) buf ^= 1;
+    ph ^= 1u;
   }
-  stamp(8);
 
 teardown:
-  if (s_abort && tid == 0) {
-    flag_status(status, GDN_ERR_TIMEOUT);
-    mbar_wait(&bar_kq, 0, 100000000ull);   // let copies still in flight land
-    mbar_wait(&bar_v, 0, 100000000ull);
+  if (tid == kPrepIO) {
+    if (kFused && have_prev && !s_abort) publish(prev);
+    bulk_wait_all();   // the stores read shared memory: finish before the CTA exits
+    if (s_abort) {     // let copies still in flight land
+      flag_status(status, GDN_ERR_TIMEOUT);
+      for (int b = 0; b < kBufs; ++b)
+        if (n_kq[b]) mbar_wait(&bar_kq[b], (n_kq[b] - 1) & 1, 100000000ull);
+      if (n_v) mbar_wait(&bar_v, (n_v - 1) & 1, 100000000ull);
+    }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
-  if (wave_trace && tid == 0) {   // the last CTA of the launch to finish stamps the end
-    const unsigned long long done =
-        atomicAdd(reinterpret_cast<unsigned long long*>(wave_trace + 200 + wave), 1ull);
-    if (done + 1 == (unsigned long long)gridDim.x * gridDim.y) wave_trace[101 + 2 * wave] = globaltimer_ns();
-  }
+  if (timed) timeline[kWorkerTimes + 2 * worker + 1] = globaltimer_ns();
 }
 
-// =========================================================== state kernel
+// =========================================================== state pass
 constexpr int kStateThreads = 256;
 constexpr uint32_t kS_WQ = 0;         // 2 x 64 KB: [W (32 KB) | Q^ (32 KB)] per buffer
 constexpr uint32_t kS_KP = 131072;    // 2 x 40 KB: [K (32 KB, MN-major) | P^ (8 KB)] per buffer
@@ -451,41 +611,38 @@ constexpr uint32_t kT_U = 0, kT_O = 64, kT_SA = 128, kT_S = 256;
 __device__ __forceinline__ uint32_t col_U(int s) { return 32u * (s >> 1) + 8u * (s & 1); }
 __device__ __forceinline__ uint32_t col_dU(int s) { return col_U(s) + 16u; }
 
-__global__ void __launch_bounds__(kStateThreads, 1)
-tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restrict__ S0,
-                __nv_bfloat16* __restrict__ out, float* __restrict__ S_final, SeqMap map,
-                int32_t H, const uint8_t* __restrict__ scratch, unsigned* status,
-                uint64_t* __restrict__ trace, int32_t trace_chunks, int32_t win_p0,
-                int32_t win_np, uint64_t* __restrict__ wave_trace, int32_t wave) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align_smem_1024(smem_raw);
+// One state unit: sequence n, head h, rows [128 half, 128 half + 128) of S.
+// kFused: the images of each chunk are acquired through its ready flag.
+template <bool kFused>
+__device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
+                                           const float* __restrict__ S0,
+                                           __nv_bfloat16* __restrict__ out,
+                                           float* __restrict__ S_final, const SeqMap& map,
+                                           int32_t H, const uint8_t* __restrict__ scratch,
+                                           const uint32_t* ready, unsigned* status,
+                                           uint64_t* __restrict__ trace, int32_t trace_chunks,
+                                           int n, int h, int half) {
+  const int unit = (n * H + h) * 2 + half;
+  const bool timed = trace && threadIdx.x == 0 && unit < kMaxTracedUnits;
+  if (timed) trace[kUnitTimes + 3 * unit] = globaltimer_ns();
   const float* sD = reinterpret_cast<const float*>(sm + kS_UT + kImgDecay);   // d_r, then G_r
   __shared__ uint64_t bar_wq[2], bar_kp[2], bar_u, bar_m1, bar_m1b, bar_m2, bar_mo;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
 
-  const int n = blockIdx.x, h = blockIdx.y, half = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, colhalf = warp >> 2;
   const uint32_t iloc = 32 * quarter + lane;            // TMEM lane = local row of S
   const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-  // chunks of this launch: positions [win_p0, win_p0 + win_np) of the
-  // sequence (all of them when win_np <= 0); S0 holds the state at the
-  // window's start and S_final receives the state at its end
-  const int64_t c_first = map.chunk_begin(n), c_last = map.chunk_end(n);
-  const int64_t cb = win_np > 0 ? min(c_first + win_p0, c_last) : c_first;
-  const int64_t ce = win_np > 0 ? min(cb + win_np, c_last) : c_last;
-  const int64_t s_begin = map.seq_begin(n) + (cb - c_first) * kC, s_end = map.seq_end(n);
-  // optional phase timeline (test hook): thread 0 of the first CTA stamps
+  const int64_t cb = map.chunk_begin(n), ce = map.chunk_end(n);
+  const int64_t s_begin = map.seq_begin(n), s_end = map.seq_end(n);
+  // optional phase timeline (test hook): thread 0 of unit (0, 0, 0) stamps
   // its SM cycle counter at 12 points of each of its first trace_chunks chunks
-  const bool tracing = trace && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
-                       blockIdx.z == 0 && win_p0 == 0;
+  const bool tracing = trace && tid == 0 && n == 0 && h == 0 && half == 0;
   auto stamp = [&](int64_t it, int k) {
     if (tracing && it < trace_chunks) trace[it * 12 + k] = clock64();
   };
 
-  const bool wave_stamp = wave_trace && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
-  if (wave_stamp) wave_trace[2 * wave] = globaltimer_ns();
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar_wq[b], 1);
@@ -498,7 +655,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
     mbar_init(&bar_mo, 1);
     fence_barrier_init();
     s_abort = 0;
-    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(tm_k);
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
 
@@ -516,6 +673,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
 #pragma unroll
     for (int j = 0; j < 128; ++j) S[j] = 0.f;
   }
+  tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
@@ -534,6 +692,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
 
   auto img_of = [&](int64_t ci) { return scratch + (size_t)(ci * H + h) * kImgStride; };
   auto t0_of = [&](int64_t ci) { return (int32_t)(s_begin + (ci - cb) * kC); };
+  auto flag_of = [&](int64_t ci) { return ready + ci * H + h; };
   auto issue_wq = [&](int64_t ci, int buf) {   // W and Q^ are adjacent in the image
     mbar_arrive_expect_tx(&bar_wq[buf], 65536);
     tma_load_1d(sm + kS_WQ + buf * 65536, img_of(ci) + kImgW, 65536, &bar_wq[buf]);
@@ -541,7 +700,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
   auto issue_kp = [&](int64_t ci, int buf) {
     uint8_t* dst = sm + kS_KP + buf * 40960;
     mbar_arrive_expect_tx(&bar_kp[buf], 40960);
-    tma_load_4d(dst, &tm_k, 0, t0_of(ci), 0, h, &bar_kp[buf]);
+    tma_load_4d(dst, tm_k, 0, t0_of(ci), 0, h, &bar_kp[buf]);
     tma_load_1d(dst + 32768, img_of(ci) + kImgP, 8192, &bar_kp[buf]);
   };
   auto issue_u = [&](int64_t ci) {    // this half's U~^T rows and the decay block
@@ -554,18 +713,44 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
   // Loads are issued by single threads of warps 1 and 2 (thread 0 issues the
   // MMAs), so the kinds of issue overlap.  Each counts the phases it started
   // on its load barriers, for a clean exit after a timeout.
-  constexpr int kLoaderA = 32;   // K / P^ and U~^T
-  constexpr int kLoaderB = 64;   // W / Q^ and the L2 warm-up
+  constexpr int kLoaderA = 32;   // K / P^ and U~^T, one chunk ahead
+  constexpr int kLoaderB = 64;   // W / Q^, two chunks ahead, and the L2 warm-up
   uint32_t n_wq[2] = {0, 0}, n_kp[2] = {0, 0}, n_u = 0;
-  if (tid == kLoaderA && cb < ce) {
-    issue_kp(cb, 0); ++n_kp[0];
-    issue_u(cb); ++n_u;
+  int64_t wq_next = cb;          // (kLoaderB) first chunk whose W / Q^ is not issued yet
+  auto load_kp_u = [&](int64_t ci, int buf) -> bool {   // (kLoaderA)
+    if (kFused && !ready_wait(flag_of(ci))) return false;
+    issue_kp(ci, buf); ++n_kp[buf];
+    issue_u(ci); ++n_u;
+    return true;
+  };
+  // (kLoaderB) W / Q^ of every chunk up to `must` (waiting for its flag) and
+  // of the chunk after it if that is already published; the buffer of chunk
+  // c is free once MMA-1 of chunk c - 2 has finished (m1_done).
+  auto load_wq = [&](int64_t must, bool m1_done) -> bool {
+    while (wq_next < ce && wq_next <= must + 1) {
+      if (wq_next == must + 1) {
+        if (!m1_done) break;
+        if (kFused && !ready_now(flag_of(wq_next))) break;
+      } else if (kFused && !ready_wait(flag_of(wq_next))) {
+        return false;
+      }
+      const int b = (int)((wq_next - cb) & 1);
+      issue_wq(wq_next, b); ++n_wq[b];
+      ++wq_next;
+    }
+    return true;
+  };
+  if (tid == kLoaderA && cb < ce && !load_kp_u(cb, 0)) {
+    flag_status(status, GDN_ERR_TIMEOUT);
+    s_abort = 1;
   }
   if (tid == kLoaderB && cb < ce) {
-    issue_wq(cb, 0); ++n_wq[0];
-    if (cb + 1 < ce) { issue_wq(cb + 1, 1); ++n_wq[1]; }
-    if (cb + 1 < ce) warm_l2(cb + 1);
-    if (cb + 2 < ce) warm_l2(cb + 2);
+    if (!load_wq(cb, true)) {
+      flag_status(status, GDN_ERR_TIMEOUT);
+      s_abort = 1;
+    }
+    if (!kFused && cb + 1 < ce) warm_l2(cb + 1);
+    if (!kFused && cb + 2 < ce) warm_l2(cb + 2);
   }
   tc_fence_before();
   __syncthreads();
@@ -586,7 +771,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
     }
   };
 
-  for (int64_t ci = cb; ci < ce; ++ci) {
+  for (int64_t ci = cb; ci < ce && !s_abort; ++ci) {
     const int64_t it = ci - cb;
     const uint32_t par = (uint32_t)(it & 1);
     const int buf = (int)(it & 1);
@@ -596,6 +781,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
 
     // 1. [D_U | D_O] = S [W | Q^]^T (commit m1 and m1b); A = S from TMEM
     stamp(it, 0);
+    if (timed && it == 0) trace[kUnitTimes + 3 * unit + 1] = globaltimer_ns();
     if (tid == 0) {
       if (!mbar_wait(&bar_wq[buf], bpar)) {
         s_abort = 1;
@@ -670,22 +856,23 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
         mma_commit(&bar_mo);
       }
     }
-    // ... meanwhile the loader fetches ahead: K / P^ of the next chunk into
-    // the other buffer (the previous chunk's staging was copied out above),
-    // U~^T of the next chunk (E1 is done with the buffer), the W / Q^ buffer
-    // of this chunk for chunk + 2 (once MMA-1 finished reading it), and warms
-    // L2 with a later chunk's image
-    if (tid == kLoaderA && ci + 1 < ce) {
-      issue_kp(ci + 1, buf ^ 1); ++n_kp[buf ^ 1];
-      issue_u(ci + 1); ++n_u;
+    // ... meanwhile the loaders fetch ahead: K / P^ and U~^T of the next
+    // chunk (the previous chunk's staging was copied out above and E1 is done
+    // with the U~^T buffer), W / Q^ of the next chunk if not yet in flight
+    // and of the chunk after it once MMA-1 finished reading this buffer, and
+    // (split form) L2 warm-up of a later chunk's image
+    if (tid == kLoaderA && ci + 1 < ce && !load_kp_u(ci + 1, buf ^ 1)) {
+      flag_status(status, GDN_ERR_TIMEOUT);
+      s_abort = 1;
     }
     if (tid == kLoaderB) {
-      if (ci + 3 < ce) warm_l2(ci + 3);
-      if (ci + 2 < ce) {
-        if (!mbar_wait(&bar_m1b, par)) {
+      if (!kFused && ci + 3 < ce) warm_l2(ci + 3);
+      if (ci + 1 < ce) {
+        const bool m1_done = ci + 2 < ce ? mbar_wait(&bar_m1b, par) : true;
+        if (!m1_done) s_abort = 1;
+        if (!load_wq(ci + 1, m1_done)) {
+          flag_status(status, GDN_ERR_TIMEOUT);
           s_abort = 1;
-        } else {
-          issue_wq(ci + 2, buf); ++n_wq[buf];
         }
       }
     }
@@ -769,8 +956,72 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
-  if (wave_stamp) wave_trace[2 * wave + 1] = globaltimer_ns();
+  if (timed) trace[kUnitTimes + 3 * unit + 2] = globaltimer_ns();
 }
+
+// ================================================================ kernels
+// split form, kernel 1: items j = blockIdx.x + k * gridDim.x < n_items,
+// (chunk j / H, head j % H); two CTAs per SM
+__global__ void __launch_bounds__(kPrepThreads, 2)
+tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ alpha,
+               const float* __restrict__ beta, SeqMap map, int32_t H,
+               uint8_t* __restrict__ scratch, unsigned* status, uint64_t* __restrict__ trace,
+               int64_t n_items) {
+  extern __shared__ uint8_t smem_raw[];
+  prep_role<false>(align_smem_1024(smem_raw), &tm_q, &tm_k, &tm_v, alpha, beta, map, H, scratch,
+                   nullptr, status, trace ? trace + kPrepTraceOffset : nullptr, trace, n_items,
+                   blockIdx.x, gridDim.x);
+}
+
+// split form, kernel 2: one CTA per unit (blockIdx = sequence, head, half)
+__global__ void __launch_bounds__(kStateThreads, 1)
+tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restrict__ S0,
+                __nv_bfloat16* __restrict__ out, float* __restrict__ S_final, SeqMap map,
+                int32_t H, const uint8_t* __restrict__ scratch, unsigned* status,
+                uint64_t* __restrict__ trace, int32_t trace_chunks) {
+  extern __shared__ uint8_t smem_raw[];
+  state_role<false>(align_smem_1024(smem_raw), &tm_k, S0, out, S_final, map, H, scratch, nullptr,
+                    status, trace, trace_chunks, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+// fused form: cooperative, one CTA per SM; CTAs [0, n_state) are the state
+// units (unit u = (sequence u / 2H, head (u / 2) % H, half u % 2)), the rest
+// prep workers over all chunk positions in order
+__global__ void __launch_bounds__(kStateThreads, 1)
+tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kb,
+                const float* __restrict__ alpha, const float* __restrict__ beta,
+                const float* __restrict__ S0, __nv_bfloat16* __restrict__ out,
+                float* __restrict__ S_final, SeqMap map, int32_t H, uint8_t* __restrict__ scratch,
+                uint32_t* ready, unsigned* status, uint64_t* __restrict__ trace,
+                int32_t trace_chunks, int32_t n_state) {
+  static_assert(kPrepThreads == kStateThreads, "one block shape for both roles");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align_smem_1024(smem_raw);
+  if ((int32_t)blockIdx.x < n_state) {
+    const int u = blockIdx.x;
+    state_role<true>(sm, &tm_kb, S0, out, S_final, map, H, scratch, ready, status, trace,
+                     trace_chunks, u / (2 * H), (u >> 1) % H, u & 1);
+  } else {
+    int64_t positions = map.chunks_per_seq;
+    if (map.cu_seqlens) {
+      positions = 0;
+      for (int n = 0; n < map.N; ++n) {
+        const int64_t c = map.chunk_end(n) - map.chunk_begin(n);
+        positions = c > positions ? c : positions;
+      }
+    }
+    prep_role<true>(sm, &tm_q, &tm_k, &tm_v, alpha, beta, map, H, scratch, ready, status,
+                    trace ? trace + kPrepTraceOffset : nullptr, trace, positions * map.N * H,
+                    blockIdx.x - n_state, gridDim.x - n_state);
+  }
+}
+
+constexpr uint32_t kPrepSmemSplit = PrepSmem<1>::BYTES;
+constexpr uint32_t kFusedSmem = kStateSmem > PrepSmem<2>::BYTES ? kStateSmem : PrepSmem<2>::BYTES;
+// the fused form runs only if this many SMs are left for prep workers
+constexpr int kMinPrepWorkers = 32;
 
 // ------------------------------------------------------------- host side
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -822,69 +1073,56 @@ bool make_token_map_blocked(CUtensorMap* m, const void* base, int64_t T_total, i
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-// phase-timeline buffer for the state pass and, at kPrepTraceOffset, for the
-// first CTA of the per-chunk kernel (test hook; null when off)
-uint64_t* g_trace = nullptr;
-int32_t g_trace_chunks = 0;
-
-size_t prefill_tc_scratch_bytes(int64_t max_chunks, int32_t H) {
-  return (size_t)max_chunks * H * kImgStride;
-}
-
-size_t prefill_tc_image_stride() { return kImgStride; }
-
-namespace {
-
-// Per-device helper streams and events for overlapping the parallel prep of
-// one chunk-position wave with the sequential state pass of the previous one.
-// The state pass runs on the highest-priority stream, so its CTAs take SMs
-// as soon as they free up instead of queueing behind the next prep wave.
-struct WaveStreams {
-  cudaStream_t prep = nullptr, state = nullptr;
-  cudaEvent_t start = nullptr, done = nullptr;
-  cudaEvent_t prep_done[kMaxWaves] = {};
-  bool ok = false;
+// Per-device launch facts, looked up once: SM count, and whether the fused
+// form can be launched (cooperative launches supported and one fused CTA
+// fits on an SM).
+struct DeviceFacts {
+  int sms = 0;
+  bool fused_ok = false;
+  bool ready = false;
 };
 
-WaveStreams* wave_streams() {
-  static WaveStreams ws[64];
+DeviceFacts* device_facts() {
+  static DeviceFacts facts[64];
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  WaveStreams& w = ws[dev];
-  if (!w.ok) {
-    int lo = 0, hi = 0;
-    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return nullptr;
-    if (cudaStreamCreateWithPriority(&w.prep, cudaStreamNonBlocking, lo) != cudaSuccess ||
-        cudaStreamCreateWithPriority(&w.state, cudaStreamNonBlocking, hi) != cudaSuccess ||
-        cudaEventCreateWithFlags(&w.start, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&w.done, cudaEventDisableTiming) != cudaSuccess)
+  DeviceFacts& f = facts[dev];
+  if (!f.ready) {
+    int coop = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kPrepSmemSplit) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kStateSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kFusedSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_fused_kernel, kStateThreads,
+                                                      kFusedSmem) != cudaSuccess)
       return nullptr;
-    for (int i = 0; i < kMaxWaves; ++i)
-      if (cudaEventCreateWithFlags(&w.prep_done[i], cudaEventDisableTiming) != cudaSuccess)
-        return nullptr;
-    w.ok = true;
+    f.fused_ok = coop != 0 && per_sm >= 1;
+    f.ready = true;
   }
-  return &w;
-}
-
-// Number of chunk-position waves: dense batches only, whose state pass
-// leaves most SMs free, and long enough for every wave to have work to hide.
-int wave_count(const PrefillLaunch& a) {
-  if (!a.allow_waves || a.map.cu_seqlens || a.map.chunks_per_seq < 2 * kWaveMinChunks) return 1;
-  if ((int64_t)a.map.N * a.H * 2 > kWaveMaxStateCtas) return 1;
-  const int64_t w = a.map.chunks_per_seq / kWaveMinChunks;
-  return (int)(w < kMaxWaves ? w : kMaxWaves);
+  return &f;
 }
 
 }  // namespace
 
-size_t prefill_tc_wave_state_bytes(const PrefillLaunch& a) {
-  return wave_count(a) > 1 ? (size_t)a.map.N * a.H * kDV * kDK * sizeof(float) : 0;
+// phase-timeline buffer for the state pass and, at kPrepTraceOffset, for the
+// first prep worker (test hook; null when off)
+uint64_t* g_trace = nullptr;
+int32_t g_trace_chunks = 0;
+int32_t g_last_tc_form = -1;
+
+// operand images, then one ready flag per (chunk, head) for the fused form
+size_t prefill_tc_scratch_bytes(int64_t max_chunks, int32_t H) {
+  const size_t items = (size_t)max_chunks * H;
+  return items * kImgStride + align_up(items * sizeof(uint32_t), 256);
 }
+
+size_t prefill_tc_image_stride() { return kImgStride; }
 
 cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool prep_only) {
   static_assert(kDK == 256 && kDV == 256, "image layouts assume 256 x 256 heads");
@@ -893,66 +1131,57 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
   if (!make_token_map(&tq, a.q, T_total, a.H) || !make_token_map(&tk, a.k, T_total, a.H) ||
       !make_token_map(&tv, a.v, T_total, a.H) || !make_token_map_blocked(&tkb, a.k, T_total, a.H))
     return cudaErrorInvalidValue;
+  DeviceFacts* f = device_facts();
+  if (!f) return cudaErrorUnknown;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kPrepSmem)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kStateSmem)) != cudaSuccess)
-    return e;
   uint8_t* scr = (uint8_t*)a.scratch;
-  uint64_t* prep_trace = g_trace ? g_trace + kPrepTraceOffset : nullptr;
-  uint64_t* wave_trace = g_trace ? g_trace + kWaveTraceOffset : nullptr;
-  const int waves = prep_only ? 1 : wave_count(a);
-  if (waves == 1) {
-    if (a.max_chunks > 0) {
-      tc_prep_kernel<<<dim3((unsigned)a.max_chunks, (unsigned)a.H), kPrepThreads, kPrepSmem,
-                       stream>>>(tq, tk, tv, a.alpha, a.beta, a.map, a.H, scr, a.status,
-                                 prep_trace, 0, 0, wave_trace, 0);
+  const int64_t items = a.max_chunks * a.H;
+  uint32_t* ready = (uint32_t*)(scr + (size_t)items * kImgStride);
+  const int64_t n_state = (int64_t)a.map.N * a.H * 2;
+
+  if (!prep_only && a.allow_overlap && f->fused_ok && items > 0 &&
+      n_state + kMinPrepWorkers <= f->sms) {
+    if ((e = cudaMemsetAsync(ready, 0, (size_t)items * sizeof(uint32_t), stream)) != cudaSuccess)
+      return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)f->sms);
+    cfg.blockDim = dim3(kStateThreads);
+    cfg.dynamicSmemBytes = kFusedSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, tc_fused_kernel, tq, tk, tv, tkb, a.alpha, a.beta, a.S0,
+                           (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr, ready, a.status,
+                           g_trace, g_trace_chunks, (int32_t)n_state);
+    if (e == cudaSuccess) {
       count_launches(1);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      g_last_tc_form = 1;
+      return cudaSuccess;
     }
-    if (prep_only) return cudaSuccess;
-    tc_state_kernel<<<dim3((unsigned)a.map.N, (unsigned)a.H, 2), kStateThreads, kStateSmem,
-                      stream>>>(tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr,
-                                a.status, g_trace, g_trace_chunks, 0, 0, wave_trace, 0);
-    count_launches(1);
-    return cudaGetLastError();
+    // not all CTAs can be resident right now (e.g. SMs held by another
+    // context): clear the launch error and take the split form
+    if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+    (void)cudaGetLastError();
   }
-  // Waves: the prep of every wave is queued on a low-priority helper stream
-  // and overlaps the state pass of the earlier waves on a high-priority one
-  // (state wave w waits only for prep wave w); the state carries between
-  // waves in scratch, and the caller's stream waits for the last state wave.
-  WaveStreams* ws = wave_streams();
-  if (!ws) return cudaErrorUnknown;
-  float* carry = (float*)(scr + prefill_tc_scratch_bytes(a.max_chunks, a.H));
-  const int64_t cps = a.map.chunks_per_seq;
-  if ((e = cudaEventRecord(ws->start, stream)) != cudaSuccess) return e;
-  if ((e = cudaStreamWaitEvent(ws->prep, ws->start, 0)) != cudaSuccess) return e;
-  if ((e = cudaStreamWaitEvent(ws->state, ws->start, 0)) != cudaSuccess) return e;
-  for (int w = 0; w < waves; ++w) {
-    const int32_t p0 = (int32_t)(cps * w / waves), np = (int32_t)(cps * (w + 1) / waves) - p0;
-    tc_prep_kernel<<<dim3((unsigned)(a.map.N * np), (unsigned)a.H), kPrepThreads, kPrepSmem,
-                     ws->prep>>>(tq, tk, tv, a.alpha, a.beta, a.map, a.H, scr, a.status,
-                                 w == 0 ? prep_trace : nullptr, p0, np, wave_trace, w);
-    count_launches(1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = cudaEventRecord(ws->prep_done[w], ws->prep)) != cudaSuccess) return e;
-  }
-  for (int w = 0; w < waves; ++w) {
-    const int32_t p0 = (int32_t)(cps * w / waves), np = (int32_t)(cps * (w + 1) / waves) - p0;
-    if ((e = cudaStreamWaitEvent(ws->state, ws->prep_done[w], 0)) != cudaSuccess) return e;
-    const float* s_in = w == 0 ? a.S0 : carry;
-    float* s_out = w == waves - 1 ? a.S_final : carry;
-    tc_state_kernel<<<dim3((unsigned)a.map.N, (unsigned)a.H, 2), kStateThreads, kStateSmem,
-                      ws->state>>>(tkb, s_in, (__nv_bfloat16*)a.out, s_out, a.map, a.H, scr,
-                                   a.status, g_trace, g_trace_chunks, p0, np, wave_trace, w);
+
+  if (items > 0) {
+    const int64_t slots = 2 * (int64_t)f->sms;
+    const unsigned grid = (unsigned)(items < slots ? items : slots);
+    tc_prep_kernel<<<grid, kPrepThreads, kPrepSmemSplit, stream>>>(
+        tq, tk, tv, a.alpha, a.beta, a.map, a.H, scr, a.status, g_trace, items);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if ((e = cudaEventRecord(ws->done, ws->state)) != cudaSuccess) return e;
-  if ((e = cudaStreamWaitEvent(stream, ws->done, 0)) != cudaSuccess) return e;
-  return cudaSuccess;
+  if (prep_only) return cudaSuccess;
+  g_last_tc_form = 0;
+  tc_state_kernel<<<dim3((unsigned)a.map.N, (unsigned)a.H, 2), kStateThreads, kStateSmem,
+                    stream>>>(tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr,
+                              a.status, g_trace, g_trace_chunks);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 }  // namespace gdn

@@ -81,26 +81,36 @@ size_t gdn_testing_prefill_image_stride(void);
 
 /*
  * gdn_testing_set_trace -- phase timeline of the bf16 state pass.  While set,
- * every later gdn_prefill with bf16 I/O makes thread 0 of its first state-pass
- * CTA (sequence 0, head 0, first row half) write its SM cycle counter
- * (clock64) at 12 points of each of its first max_chunks (at most 256)
- * chunks into device_buf (uint64 [max_chunks][12]): loop top, MMA-1 issued, U epilogue done, after
- * the following barrier, MMA-2 issued, MMA-2 complete, state epilogue done,
- * after the closing barrier, then (8) U accumulator loaded, (9) state
- * accumulator folded into the master state, (10) bf16 state operand stored,
- * (11) output accumulator loaded.  Thread 0 of the per-chunk kernel's first
- * CTA (chunk 0, head 0) stamps 9 points of its life at device_buf[4096 +
- * 0..8] (start, prologue done, before the Gram MMA wait, Gram done, A and P^
- * written, T solved, T_w / T_u ready, W / U~ MMAs done, images written).
- * At device_buf[3072 ..] the launches of one call leave a timeline on the GPU
- * global timer (ns): [2w], [2w+1] = start and end of state-pass wave w (its
- * first CTA); [100+2w] = start of per-chunk wave w (first CTA) and [101+2w]
- * its end (last CTA to finish, found with the counter at [200+w], which must
- * start at zero).  So device_buf must hold at least 4105 entries, zeroed.
- * Pass NULL to switch it off.
+ * every later gdn_prefill with bf16 I/O makes thread 0 of the state unit
+ * (sequence 0, head 0, first row half) write its SM cycle counter (clock64)
+ * at 12 points of each of its first max_chunks (at most 256) chunks into
+ * device_buf (uint64 [max_chunks][12]): loop top, MMA-1 issued, U epilogue
+ * done, after the following barrier, MMA-2 issued, MMA-2 complete, state
+ * epilogue done, after the closing barrier, then (8) U accumulator loaded,
+ * (9) state accumulator folded into the master state, (10) bf16 state
+ * operand stored, (11) output accumulator loaded.  Thread 0 of the first
+ * per-chunk worker stamps 9 points of its first (chunk, head) item at
+ * device_buf[4096 + 0..8] (start, prologue done, Q^ in registers, Gram MMA
+ * done, Q^ staged and A and P^ written, T solved, T_w / T_u ready, W / U~
+ * MMAs done, images staged and their stores issued).  On the GPU global
+ * timer (ns) the call also leaves: for state unit u = (sequence * heads +
+ * head) * 2 + half < 128, its start, the top of its first chunk and its end
+ * at device_buf[3072 + 3u + 0..2]; for per-chunk worker w < 200 (CTA w of
+ * the split form's per-chunk kernel, or of the fused form's workers) its
+ * start and end at device_buf[3456 + 2w + 0..1]; the start of each of the
+ * first 240 items of worker 0 at device_buf[3856 + i].  So device_buf must
+ * hold at least 4105 entries, zeroed.  Pass NULL to switch it off.
  * Not thread-safe; for profiling only.
  */
 void gdn_testing_set_trace(uint64_t* device_buf, int32_t max_chunks);
+
+/*
+ * gdn_testing_last_prefill_form -- how the last bf16 prefill of this process
+ * (gdn_prefill or gdn_prefill_noalloc) was launched: 1 fused (one cooperative launch in which per-chunk
+ * workers publish each chunk's operands to the state pass through ready
+ * flags), 0 split (per-chunk kernel, then state-pass kernel), -1 none yet.
+ */
+int32_t gdn_testing_last_prefill_form(void);
 
 #ifdef __cplusplus
 }

@@ -207,28 +207,65 @@ def test_decode_equals_single_token_prefill(gdn_lib):
     assert rel(S.cpu().numpy(), s_p.cpu().numpy()) <= 1e-5
 
 
-def test_prefill_chunk_waves_against_oracle(gdn_lib):
-    """65 chunks per sequence: the tensor-core prefill splits the sequence
-    into chunk-position waves (uneven split), carrying the state between
-    them; the result still matches the oracle."""
-    check_case(gdn_lib, PrefillCase("waves", [4160], H=2, io_dtype=torch.bfloat16, seed=61))
-
-
-def test_prefill_chunk_waves_are_bitwise_neutral(gdn_lib):
-    """The state carried between waves is the fp32 master state itself, so a
-    run split into waves equals the single-wave run bit for bit (the
-    no-allocation entry point always runs one wave)."""
+def _last_form(gdn_lib):
     import ctypes
-    case = PrefillCase("waves bitwise", [4160], H=2, io_dtype=torch.bfloat16, seed=62)
-    x = to_dev(gdn_inputs.make_prefill(case, device="cpu"))
-    out, Sf = run_gpu(gdn_lib, x)
+    f = gdn_lib.load().gdn_testing_last_prefill_form
+    f.restype = ctypes.c_int32
+    return int(f())
+
+
+def _prefill_noalloc(gdn_lib, x, N, seqlen, H):
+    import ctypes
     f = gdn_lib.load().gdn_prefill_noalloc
     vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     f.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, vp]
-    out1 = torch.empty_like(out)
-    Sf1 = torch.empty_like(Sf)
+    T_tot = x["q"].shape[0] * x["q"].shape[1]
+    out = torch.empty(T_tot, H, 256, dtype=torch.bfloat16, device=DEV)
+    Sf = torch.empty(N, H, 256, 256, dtype=torch.float32, device=DEV)
+    cu = x["cu_seqlens"]
     rc = f(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), x["alpha"].data_ptr(),
-           x["beta"].data_ptr(), x["S0"].data_ptr(), None, out1.data_ptr(), Sf1.data_ptr(), 1,
-           4160, 2, 256, 256, 1, torch.cuda.current_stream().cuda_stream)
+           x["beta"].data_ptr(), x["S0"].data_ptr() if x["S0"] is not None else None,
+           cu.data_ptr() if cu is not None else None,
+           out.data_ptr(), Sf.data_ptr(), N, seqlen, H, 256, 256, 1,
+           torch.cuda.current_stream().cuda_stream)
     assert rc == 0 and gdn_lib.device_status() == 0
-    assert torch.equal(out, out1) and torch.equal(Sf, Sf1)
+    return out, Sf
+
+
+@pytest.mark.parametrize("lens,varlen", [([4160], False), ([700, 64, 1, 2000], True)])
+def test_prefill_fused_against_oracle(gdn_lib, lens, varlen):
+    """Few sequences x heads: the tensor-core prefill runs as one cooperative
+    launch in which per-chunk workers hand each chunk's operands to the state
+    pass through ready flags (chunk positions in order, sequences of unequal
+    length included); the result matches the oracle."""
+    check_case(gdn_lib, PrefillCase("fused", lens, H=2, io_dtype=torch.bfloat16, seed=61,
+                                    varlen=varlen))
+    assert _last_form(gdn_lib) == 1
+
+
+@pytest.mark.parametrize("lens,varlen", [([4160], False), ([700, 64, 1, 2000], True)])
+def test_prefill_fused_matches_split_bitwise(gdn_lib, lens, varlen):
+    """The fused launch and the split one (per-chunk kernel, then state-pass
+    kernel; the no-allocation entry point always takes it) do the same
+    arithmetic in the same order, so they agree bit for bit."""
+    H = 2
+    case = PrefillCase("fused vs split", lens, H=H, io_dtype=torch.bfloat16, seed=62, varlen=varlen)
+    x = to_dev(gdn_inputs.make_prefill(case, device="cpu"))
+    out, Sf = run_gpu(gdn_lib, x)
+    assert _last_form(gdn_lib) == 1
+    N = len(lens)
+    seqlen = sum(lens) if varlen else lens[0]
+    out1, Sf1 = _prefill_noalloc(gdn_lib, x, N, seqlen, H)
+    assert _last_form(gdn_lib) == 0
+    assert torch.equal(out.reshape(out1.shape), out1) and torch.equal(Sf, Sf1)
+
+
+def test_prefill_many_units_split_form(gdn_lib):
+    """70 sequences x 1 head leave too few SMs for the fused form's workers:
+    the split form runs (persistent per-chunk kernel over every item), and
+    matches the oracle."""
+    rng = np.random.default_rng(5)
+    lens = [int(t) for t in rng.integers(1, 200, size=70)]
+    check_case(gdn_lib, PrefillCase("split", lens, H=1, io_dtype=torch.bfloat16, seed=63,
+                                    varlen=True))
+    assert _last_form(gdn_lib) == 0
