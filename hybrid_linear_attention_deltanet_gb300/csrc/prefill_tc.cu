@@ -56,9 +56,11 @@ namespace {
 using namespace sm100;
 
 // ---- scratch image per (chunk, head)
-constexpr size_t kImgW = 0;           // W   : MN-major B image, 256 K-rows (c) x 64 (r)
-constexpr size_t kImgQ = 32768;       // Q^  : MN-major B image, 256 K-rows (c) x 64 (r), right
-                                      //       after W so that [W | Q^] is one N = 128 operand
+// [W | Q^] as one N = 128 MN-major B operand of 256 K-rows (c): 64-row
+// blocks interleaved, W_0 Q^_0 W_1 Q^_1 W_2 Q^_2 W_3 Q^_3 (8 KB each), where
+// W_b / Q^_b hold the 128-byte rows c in [64b, 64b + 64) = W[0..63][c] /
+// Q^[0..63][c] (the layout of the per-chunk kernel's K/Q tile buffer)
+constexpr size_t kImgWQ = 0;
 constexpr size_t kImgP = 65536;       // P^  : K-major B image, 64 rows x 64
 // per 128-row half h of S: U~^T rows [128h, 128h+128) (128-byte swizzled,
 // 16 KB) followed by the chunk's decay block (512 B: d_r = gamma_L / gamma_r
@@ -113,14 +115,21 @@ static_assert(kItemTimes + kMaxTracedItems <= kPrepTraceOffset, "trace layout");
 constexpr int kPrepIO = 64;              // thread that issues the prep's bulk copies
 
 // Shared-memory layout of the prep (offsets from the 1024-aligned base).
-// kBufs K/Q buffers of 64 KB; K-block b at b*16K holds rows 0-63 of K, then
-// rows 64-127 of Q.  Within a buffer's life the Q slots hold Q, then the Q^
-// rows on their way out, then V; after the W / U~ MMAs the K slots hold the
-// W rows and the V slots the U~^T rows on their way out.
-template <int kBufs>
+// K/Q buffers of 64 KB (two in the fused form); K-block b at b*16K holds
+// rows 0-63 of K, then rows 64-127 of Q.  Within a buffer's life the Q slots
+// hold Q, then the Q^ rows; after the W / U~ MMAs the K slots hold the W
+// rows, so that the buffer is the [W | Q^] image.  Split form: Q^ leaves
+// early, V lands in the Q slots and the U~^T rows go there after the MMAs.
+// Fused form: V (four 64-column blocks of 8 KB) has a buffer of its own,
+// which afterwards holds the two halves of U~^T with their decay blocks in
+// image layout, and P^ is staged too: an item leaves in three bulk stores.
+template <bool kFused>
 struct PrepSmem {
   static constexpr uint32_t KQ = 0;
-  static constexpr uint32_t A = 65536u * kBufs;      // fp32 [64][65]; then T_w, T_u
+  static constexpr uint32_t V = 65536u * (kFused ? 2 : 1);
+  static_assert(!kFused || 2 * kImgHalf <= 34816, "U~^T halves fit the V buffer");
+  static constexpr uint32_t PS = V + (kFused ? 34816u : 0u);   // V: 2 x 16896 rounded to 1 KB
+  static constexpr uint32_t A = PS + (kFused ? 8192u : 0u);   // fp32 [64][65]; then T_w, T_u
   static constexpr uint32_t TW = A;                  //   (bf16 K-major 64 x 64, 8 KB each)
   static constexpr uint32_t TU = A + 8192;
   static constexpr uint32_t T = A + 64 * kLd * 4;    // fp32 [64][65]
@@ -178,7 +187,7 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
                                           uint64_t* __restrict__ timeline, int64_t n_items,
                                           int64_t worker, int64_t n_workers) {
   constexpr int kBufs = kFused ? 2 : 1;
-  using Lay = PrepSmem<kBufs>;
+  using Lay = PrepSmem<kFused>;
   float* sA = (float*)(sm + Lay::A);
   float* sT = (float*)(sm + Lay::T);
   float* sY1 = (float*)(sm + Lay::Y1);
@@ -195,10 +204,15 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
   const int quarter = warp & 3, hv = warp >> 2;
   const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
   // optional phase timeline (test hook): thread 0 of worker 0 stamps its SM
-  // cycle counter at 9 points of its first item
-  bool tracing = trace && tid == 0 && worker == 0;
+  // cycle counter at 9 points of its item kTracedItem, and the bulk-copy
+  // thread at 8 points around its copy issues
+  constexpr int kTracedItem = 4;
+  bool tracing = false;
   auto stamp = [&](int k) {
-    if (tracing) trace[k] = clock64();
+    if (tracing && tid == 0) trace[k] = clock64();
+  };
+  auto io_stamp = [&](int k) {
+    if (tracing && tid == kPrepIO) trace[9 + k] = clock64();
   };
   const bool timed = timeline && tid == 0 && worker < kMaxTracedWorkers;
   if (timed) timeline[kWorkerTimes + 2 * worker] = globaltimer_ns();
@@ -234,12 +248,16 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
     }
     ++n_kq[b];
   };
+  auto issue_v = [&](const PrepItem& it, uint8_t* dst, uint32_t block_stride) {
+    mbar_arrive_expect_tx(&bar_v, 32768);
+    for (int b = 0; b < 4; ++b)
+      tma_load_3d(dst + b * block_stride, tm_v, b * 64, it.h, (int32_t)it.t0, &bar_v);
+    ++n_v;
+  };
   auto img_of = [&](const PrepItem& it) {
     return scratch + (size_t)(it.ci * H + it.h) * kImgStride;
   };
-  // (kPrepIO) the item's bulk stores have landed: raise its ready flag.  The
-  // P^ rows, written by other threads with plain stores, were fenced by
-  // their writers before the barriers that precede this.
+  // (kPrepIO) the item's bulk stores have landed: raise its ready flag
   auto publish = [&](const PrepItem& it) {
     bulk_wait_all();
     fence_proxy_async_global();
@@ -254,7 +272,10 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
   int buf = 0;
   float a_cur = 1.f, b_cur = 0.f;   // this item's gates (threads < C)
   if (kFused && j < n_items) {
-    if (tid == kPrepIO) issue_kq(cur, 0);
+    if (tid == kPrepIO) {
+      issue_kq(cur, 0);
+      issue_v(cur, sm + Lay::V, 8192);
+    }
     if (tid < kC && tid < cur.L) {
       a_cur = alpha[(cur.t0 + tid) * H + cur.h];
       b_cur = beta[(cur.t0 + tid) * H + cur.h];
@@ -266,6 +287,7 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
     const int L = cur.L;
     uint8_t* const img = img_of(cur);
     uint8_t* const kq = sm + Lay::KQ + buf * 65536;
+    tracing = trace && worker == 0 && n_done == kTracedItem;
     stamp(0);
     if (timed && worker == 0 && n_done < kMaxTracedItems) timeline[kItemTimes + n_done] = globaltimer_ns();
     ++n_done;
@@ -345,11 +367,15 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
     }
     kq_ph[buf] ^= 1u;
     stamp(2);
-    // two buffers: the other one is free once the previous item's stores
-    // have read it; publish that item and start the next item's tiles there
+    // fused: once the previous item's stores have read the other K/Q buffer
+    // and the V buffer, the next item's K/Q tiles and this item's V go there
     if (kFused && tid == kPrepIO) {
-      if (have_prev) publish(prev);
+      io_stamp(0);
+      bulk_wait_read_all();
+      io_stamp(1);
       if (jn < n_items) issue_kq(nxt, buf ^ 1);
+      if (have_prev) issue_v(cur, sm + Lay::V, 8192);
+      io_stamp(2);
     }
     __syncthreads();
     if (s_abort) goto teardown;
@@ -391,29 +417,36 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
             const float p1 = (j1 <= r && r < L) ? kScale * __expf(Gr - sG[j1]) * __uint_as_float(g[8 * cq + 2 * e + 1]) : 0.f;
             w[e] = pack_bf16(p0, p1);
           }
-          *reinterpret_cast<uint4*>(img + kImgP + sw_chunk(r, 4 * hv + cq)) =
+          uint8_t* pdst = kFused ? sm + Lay::PS : img + kImgP;
+          *reinterpret_cast<uint4*>(pdst + sw_chunk(r, 4 * hv + cq)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
-        if (kFused) __threadfence();   // P^ is visible before the item's ready flag
       }
     }
-    // Q^ out of the Q slots, then V into them
+    // fused: P^ out; split: Q^ out, then V into the Q slots
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     if (tid == kPrepIO) {
-      for (int b = 0; b < 4; ++b) tma_store_1d(img + kImgQ + b * 8192, kq + b * 16384 + 8192, 8192);
-      bulk_commit();
-      bulk_wait_read_all();
-      mbar_arrive_expect_tx(&bar_v, 32768);
-      for (int b = 0; b < 4; ++b)
-        tma_load_3d(kq + b * 16384 + 8192, tm_v, b * 64, cur.h, (int32_t)cur.t0, &bar_v);
-      ++n_v;
+      io_stamp(3);
+      if (kFused) {
+        tma_store_1d(img + kImgP, sm + Lay::PS, 8192);
+        bulk_commit();
+      } else {
+        for (int b = 0; b < 4; ++b)
+          tma_store_1d(img + kImgWQ + b * 16384 + 8192, kq + b * 16384 + 8192, 8192);
+        bulk_commit();
+        bulk_wait_read_all();
+        issue_v(cur, kq + 8192, 16384);
+      }
+      io_stamp(4);
     }
 
     stamp(4);
     // ---- T = (I + A)^{-1}: 16 x 16 diagonal inverses, then two levels of
     //      [[T1, 0], [X, T2]] with X = -T2 A21 T1
+    // (forward substitution per column c of block b; four partial sums keep
+    // the dependent chain from x[r-1] to x[r] at one FMA and two adds)
     if (tid < 64) {
       const int b = tid >> 4, c = tid & 15, o = 16 * b;
       float x[16];
@@ -421,13 +454,22 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
       for (int r = 0; r < 16; ++r) x[r] = r == c ? 1.f : 0.f;
 #pragma unroll
       for (int r = 1; r < 16; ++r) {
-        float acc = 0.f;
+        const float* arow = sA + (o + r) * kLd + o;
+        float p[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int jc = 0; jc < r; ++jc) acc = fmaf(sA[(o + r) * kLd + o + jc], x[jc], acc);
-        if (r > c) x[r] = -acc;
+        for (int jc = 0; jc < r; ++jc) p[jc & 3] = fmaf(arow[jc], x[jc], p[jc & 3]);
+        if (r > c) x[r] = -((p[0] + p[1]) + (p[2] + p[3]));
       }
 #pragma unroll
       for (int r = 0; r < 16; ++r) sT[(o + r) * kLd + o + c] = x[r];
+    } else if (kFused && tid == kPrepIO && have_prev) {
+      // meanwhile: every store of the previous item (all groups but this
+      // item's P^) has landed, so it can be published
+      io_stamp(5);
+      bulk_wait_all_but_newest();
+      fence_proxy_async_global();
+      st_release_gpu(ready + prev.ci * H + prev.h, 1u);
+      io_stamp(6);
     }
     __syncthreads();
     {  // level 1, blocks p = 0, 1: Y = A[16(2p+1):, 16(2p):] T_{2p};  T_off = -T_{2p+1} Y
@@ -510,6 +552,9 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
         tc_fence_after();
         const uint32_t idesc = idesc_bf16(128, 64, 1, 0);
         const uint32_t kqa = smem_u32(kq);
+        // V's 64-column blocks: own buffer (fused) or the Q slots (split)
+        const uint32_t va = kFused ? smem_u32(sm + Lay::V) : kqa + 8192;
+        const uint32_t vblk = kFused ? 8192 : 16384;
         const uint32_t tw = smem_u32(sm + Lay::TW), tu = smem_u32(sm + Lay::TU);
         for (int hh = 0; hh < 2; ++hh) {
           for (int s = 0; s < 4; ++s)
@@ -517,7 +562,7 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
                      smem_desc(tw + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
           for (int s = 0; s < 4; ++s)
             mma_bf16(tmem + 128 + hh * 64,
-                     smem_desc(kqa + 8192 + hh * 32768 + s * 2048, 16384, 1024, kSwizzle128B),
+                     smem_desc(va + hh * 2 * vblk + s * 2048, vblk, 1024, kSwizzle128B),
                      smem_desc(tu + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
         }
         mma_commit(&bar_bc);
@@ -530,44 +575,69 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
     if (s_abort) goto teardown;
     stamp(7);
     tc_fence_after();
-    // W rows c over the K slots, U~^T rows over the V slots (both consumed)
+    // W rows c over the K slots (K consumed); U~^T rows over V (consumed):
+    // fused, the V buffer in image layout, split, the Q slots
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const uint32_t c = 128 * hh + 32 * quarter + lane;   // d_k row of W^T / d_v row of U~^T
-      uint8_t* rowblk = kq + (c >> 6) * 16384;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {               // 0: W, 1: U~^T
         uint32_t g[32];
         tmem_ld32(tmem + lane_off + part * 128 + hh * 64 + 32 * hv, g);
         tmem_ld_wait();
-        uint8_t* dst = rowblk + part * 8192;
+        uint8_t* base;    // 128-byte rows from here, swizzled by row
+        uint32_t row;
+        if (part == 0) {
+          base = kq + (c >> 6) * 16384;
+          row = c & 63;
+        } else if (kFused) {
+          base = sm + Lay::V + hh * kImgHalf;
+          row = c & 127;
+        } else {
+          base = kq + (c >> 6) * 16384 + 8192;
+          row = c & 63;
+        }
 #pragma unroll
         for (int cq = 0; cq < 4; ++cq) {
           const uint32_t w0 = pack_bf16(__uint_as_float(g[8 * cq]), __uint_as_float(g[8 * cq + 1]));
           const uint32_t w1 = pack_bf16(__uint_as_float(g[8 * cq + 2]), __uint_as_float(g[8 * cq + 3]));
           const uint32_t w2 = pack_bf16(__uint_as_float(g[8 * cq + 4]), __uint_as_float(g[8 * cq + 5]));
           const uint32_t w3 = pack_bf16(__uint_as_float(g[8 * cq + 6]), __uint_as_float(g[8 * cq + 7]));
-          *reinterpret_cast<uint4*>(dst + sw_chunk(c & 63, 4 * hv + cq)) = make_uint4(w0, w1, w2, w3);
+          *reinterpret_cast<uint4*>(base + sw_chunk(row, 4 * hv + cq)) = make_uint4(w0, w1, w2, w3);
         }
       }
     }
     if (tid < kC) {
-      sDecay[tid] = tid < L ? __expf(sG[L - 1] - sG[tid]) : 0.f;
-      sDecay[64 + tid] = sG[tid];
+      const float d = tid < L ? __expf(sG[L - 1] - sG[tid]) : 0.f;
+      if (kFused) {
+        for (int hh = 0; hh < 2; ++hh) {
+          float* blk = reinterpret_cast<float*>(sm + Lay::V + hh * kImgHalf + kImgDecay);
+          blk[tid] = d;
+          blk[64 + tid] = sG[tid];
+        }
+      } else {
+        sDecay[tid] = d;
+        sDecay[64 + tid] = sG[tid];
+      }
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     if (tid == kPrepIO) {
-      for (int b = 0; b < 4; ++b) {
-        tma_store_1d(img + kImgW + b * 8192, kq + b * 16384, 8192);
-        tma_store_1d(img + kImgU0 + (b >> 1) * kImgHalf + (b & 1) * 8192, kq + b * 16384 + 8192, 8192);
+      if (kFused) {
+        tma_store_1d(img + kImgWQ, kq, 65536);
+        tma_store_1d(img + kImgU0, sm + Lay::V, (uint32_t)(2 * kImgHalf));
+      } else {
+        for (int b = 0; b < 4; ++b) {
+          tma_store_1d(img + kImgWQ + b * 16384, kq + b * 16384, 8192);
+          tma_store_1d(img + kImgU0 + (b >> 1) * kImgHalf + (b & 1) * 8192, kq + b * 16384 + 8192, 8192);
+        }
+        for (int hh = 0; hh < 2; ++hh) tma_store_1d(img + kImgU0 + hh * kImgHalf + kImgDecay, sDecay, 512);
       }
-      for (int hh = 0; hh < 2; ++hh) tma_store_1d(img + kImgU0 + hh * kImgHalf + kImgDecay, sDecay, 512);
       bulk_commit();
+      io_stamp(7);
     }
     stamp(8);
-    tracing = false;
     prev = cur;
     have_prev = true;
     cur = nxt;
@@ -695,7 +765,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   auto flag_of = [&](int64_t ci) { return ready + ci * H + h; };
   auto issue_wq = [&](int64_t ci, int buf) {   // W and Q^ are adjacent in the image
     mbar_arrive_expect_tx(&bar_wq[buf], 65536);
-    tma_load_1d(sm + kS_WQ + buf * 65536, img_of(ci) + kImgW, 65536, &bar_wq[buf]);
+    tma_load_1d(sm + kS_WQ + buf * 65536, img_of(ci) + kImgWQ, 65536, &bar_wq[buf]);
   };
   auto issue_kp = [&](int64_t ci, int buf) {
     uint8_t* dst = sm + kS_KP + buf * 40960;
@@ -787,13 +857,15 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
         s_abort = 1;
       } else {
         tc_fence_after();
-        // [D_U | D_O] = S [W | Q^]^T : one N = 128 operand (MN-major, the two
-        // 64-element MN blocks 32 KB apart)
+        // [D_U | D_O] = S [W | Q^]^T : one N = 128 operand (MN-major; for the
+        // 16 K-rows of step s, block s / 4 of W at 16 KB strides and the
+        // matching Q^ block 8 KB after it)
         const uint32_t id1 = idesc_bf16(128, 128, 0, 1);
         const uint32_t sW = smem_u32(sm + kS_WQ + buf * 65536);
         for (int s = 0; s < 16; ++s)
           mma_bf16_ts(tmem + kT_U, tmem + kT_SA + 8 * s,
-                      smem_desc(sW + s * 2048, 32768, 1024, kSwizzle128B), id1, s > 0);
+                      smem_desc(sW + (s >> 2) * 16384 + (s & 3) * 2048, 8192, 1024, kSwizzle128B),
+                      id1, s > 0);
         mma_commit(&bar_m1);
         mma_commit(&bar_m1b);
       }
@@ -886,23 +958,28 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
       stamp(it, 5);
       tc_fence_after();
       // MMA-1 has finished reading the bf16 state operand (it precedes
-      // MMA-2), so each folded group can replace its columns right away
+      // MMA-2), so each folded group can replace its columns right away.
+      // Groups of 16 columns; the load of group q + 1 is in flight while
+      // group q is folded.
       if (!mbar_wait(&bar_m1b, par)) s_abort = 1;
+      const uint32_t tS = tmem + lane_off + kT_S + 128 * colhalf;
+      const uint32_t tA = tmem + lane_off + kT_SA + 64 * colhalf;
+      uint32_t g[2][16];
+      tmem_ld16(tS, g[0]);
 #pragma unroll
-      for (int g4 = 0; g4 < 4; ++g4) {
-        uint32_t g[32];
-        tmem_ld32(tmem + lane_off + kT_S + 128 * colhalf + 32 * g4, g);
-        tmem_ld_wait();
-        uint32_t pk[16];
+      for (int q = 0; q < 8; ++q) {
+        tmem_ld_wait_regs(g[q & 1]);
+        if (q + 1 < 8) tmem_ld16(tS + 16 * (q + 1), g[(q + 1) & 1]);
+        uint32_t pk[8];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float s0 = fmaf(gC, S[32 * g4 + j], __uint_as_float(g[j]));
-          const float s1 = fmaf(gC, S[32 * g4 + j + 1], __uint_as_float(g[j + 1]));
-          S[32 * g4 + j] = s0;
-          S[32 * g4 + j + 1] = s1;
+        for (int j = 0; j < 16; j += 2) {
+          const float s0 = fmaf(gC, S[16 * q + j], __uint_as_float(g[q & 1][j]));
+          const float s1 = fmaf(gC, S[16 * q + j + 1], __uint_as_float(g[q & 1][j + 1]));
+          S[16 * q + j] = s0;
+          S[16 * q + j + 1] = s1;
           pk[j >> 1] = pack_bf16(s0, s1);
         }
-        tmem_st16(tmem + lane_off + kT_SA + 64 * colhalf + 16 * g4, pk);
+        tmem_st8(tA + 8 * q, pk);
       }
       tmem_st_wait();
       stamp(it, 9);
@@ -1018,8 +1095,9 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
 }
 
-constexpr uint32_t kPrepSmemSplit = PrepSmem<1>::BYTES;
-constexpr uint32_t kFusedSmem = kStateSmem > PrepSmem<2>::BYTES ? kStateSmem : PrepSmem<2>::BYTES;
+constexpr uint32_t kPrepSmemSplit = PrepSmem<false>::BYTES;
+constexpr uint32_t kFusedSmem = kStateSmem > PrepSmem<true>::BYTES ? kStateSmem : PrepSmem<true>::BYTES;
+static_assert(PrepSmem<false>::A == 65536 && PrepSmem<true>::A % 1024 == 0, "prep layout");
 // the fused form runs only if this many SMs are left for prep workers
 constexpr int kMinPrepWorkers = 32;
 

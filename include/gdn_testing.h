@@ -60,9 +60,10 @@ int gdn_testing_umma_timing(int32_t N, int32_t K, int32_t a_from_tmem, int32_t b
  * for a dense batch and (T_total + 63 * N) / 64 for a packed one).  Chunk
  * ci (global index over all sequences), head h lives at byte offset
  * (ci * heads + h) * stride and holds, for the chunked WY form:
- *   +0       W      (64 x 256): 256 rows of 128 B; row c = W[0..63][c]
- *   +32768   Q^     (64 x 256): 256 rows of 128 B; row c = Q^[0..63][c]
- *                               (Q^ = gamma Q / sqrt(dk))
+ *   +0       W and Q^ (64 x 256 each), 128-byte rows, row c = W[0..63][c]
+ *            or Q^[0..63][c] (Q^ = gamma Q / sqrt(dk)), in blocks of 64 rows
+ *            interleaved W_0 Q^_0 W_1 Q^_1 W_2 Q^_2 W_3 Q^_3: block b of W
+ *            (rows 64b .. 64b+63) at +16384 b, of Q^ at +16384 b + 8192
  *   +65536   P^     (64 x 64) : 64 rows of 128 B (lower(Gam Q K^T) / sqrt(dk))
  *   +73728   U~^T rows 0-127   : row i = U~[0..63][i]
  *   +90112   decay block       : fp32 d[64] (d_r = gamma_L / gamma_r for r < L,
@@ -89,17 +90,22 @@ size_t gdn_testing_prefill_image_stride(void);
  * epilogue done, after the closing barrier, then (8) U accumulator loaded,
  * (9) state accumulator folded into the master state, (10) bf16 state
  * operand stored, (11) output accumulator loaded.  Thread 0 of the first
- * per-chunk worker stamps 9 points of its first (chunk, head) item at
+ * per-chunk worker stamps 9 points of its fifth (chunk, head) item at
  * device_buf[4096 + 0..8] (start, prologue done, Q^ in registers, Gram MMA
  * done, Q^ staged and A and P^ written, T solved, T_w / T_u ready, W / U~
- * MMAs done, images staged and their stores issued).  On the GPU global
+ * MMAs done, images staged and their stores issued), and the worker's
+ * bulk-copy thread 8 points around its copy issues at device_buf[4105 +
+ * 0..7] (fused form: before and after publishing the previous item, after
+ * issuing the next K / Q tiles; both forms: before and after issuing the
+ * Q^ stores; fused: before and after waiting for those stores to read shared
+ * memory; after issuing the W / U~ stores and the next V tile).  On the GPU global
  * timer (ns) the call also leaves: for state unit u = (sequence * heads +
  * head) * 2 + half < 128, its start, the top of its first chunk and its end
  * at device_buf[3072 + 3u + 0..2]; for per-chunk worker w < 200 (CTA w of
  * the split form's per-chunk kernel, or of the fused form's workers) its
  * start and end at device_buf[3456 + 2w + 0..1]; the start of each of the
  * first 240 items of worker 0 at device_buf[3856 + i].  So device_buf must
- * hold at least 4105 entries, zeroed.  Pass NULL to switch it off.
+ * hold at least 4113 entries, zeroed.  Pass NULL to switch it off.
  * Not thread-safe; for profiling only.
  */
 void gdn_testing_set_trace(uint64_t* device_buf, int32_t max_chunks);

@@ -40,9 +40,16 @@ def _blocks(img, off):
                            for b in range(4)], axis=1)    # [64][256]
 
 
+def _wq(img, off):
+    """W (off 0) or Q^ (off 8192) from the interleaved [W_0 Q^_0 W_1 Q^_1 ...]
+    blocks of 64 rows c each -> [256 c][64 r]."""
+    return np.concatenate([_rows(img[b * 16384 + off:b * 16384 + off + 8192], 64)
+                           for b in range(4)])
+
+
 def _decode(img):
-    W = _rows(img[0:32768], 256).T                        # [64 r][256 c]
-    Q = _rows(img[32768:65536], 256).T                    # [64 r][256 c]
+    W = _wq(img, 0).T                                     # [64 r][256 c]
+    Q = _wq(img, 8192).T                                  # [64 r][256 c]
     P = _rows(img[65536:65536 + 8192], 64)                # [64][64]
     half = 16896                                          # U~^T rows of one half + decay block
     Ut = np.concatenate([_rows(img[73728 + h * half:73728 + h * half + 16384], 128)
