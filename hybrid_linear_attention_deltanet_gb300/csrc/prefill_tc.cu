@@ -77,33 +77,28 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// exp(x) = 2^(x log2 e) on the special-function unit; results below the
+// smallest normal float flush to zero (they only scale terms that are
+// already negligible)
+__device__ __forceinline__ float exp_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+  return y;
+}
+
 // byte offset of 16-byte chunk `ch` (0..7) of row `row` in a 128-byte-swizzled image
 __device__ __forceinline__ uint32_t sw_chunk(uint32_t row, uint32_t ch) {
   return row * 128u + ((ch ^ (row & 7u)) << 4);
 }
 
-// Bounded spin on a ready flag (fused form): false after one second.
+// Bounded wait for a ready flag (fused form): give up after one second.
 constexpr uint64_t kReadyWaitNs = 1000000000ull;
-__device__ __forceinline__ bool ready_wait(const uint32_t* f) {
-  if (!ld_acquire_gpu(f)) {
-    const uint64_t t_start = globaltimer_ns();
-    while (!ld_acquire_gpu(f)) {
-      if (globaltimer_ns() - t_start > kReadyWaitNs) return false;
-      __nanosleep(64);
-    }
-  }
-  fence_proxy_async_global();
-  return true;
-}
-__device__ __forceinline__ bool ready_now(const uint32_t* f) {
-  if (!ld_acquire_gpu(f)) return false;
-  fence_proxy_async_global();
-  return true;
-}
 
 // ============================================================ prep
 constexpr int kPrepThreads = 256;
-constexpr int kLd = 65;                  // row stride of the fp32 64 x 64 tiles
+// row stride (floats) of the fp32 64 x 64 tiles: rows stay 16-byte aligned,
+// so the block inverse reads four consecutive elements of a row at once
+constexpr int kLd = 68;
 constexpr int kPrepTraceOffset = 4096;   // uint64 slots before the prep timeline
 // global-timer timeline of one call (test hook): per state unit u < 128 its
 // start, first chunk top and end; per prep worker w < 200 its start and end;
@@ -129,10 +124,10 @@ struct PrepSmem {
   static constexpr uint32_t V = 65536u * (kFused ? 2 : 1);
   static_assert(!kFused || 2 * kImgHalf <= 34816, "U~^T halves fit the V buffer");
   static constexpr uint32_t PS = V + (kFused ? 34816u : 0u);   // V: 2 x 16896 rounded to 1 KB
-  static constexpr uint32_t A = PS + (kFused ? 8192u : 0u);   // fp32 [64][65]; then T_w, T_u
+  static constexpr uint32_t A = PS + (kFused ? 8192u : 0u);   // fp32 [64][kLd]; then T_w, T_u
   static constexpr uint32_t TW = A;                  //   (bf16 K-major 64 x 64, 8 KB each)
   static constexpr uint32_t TU = A + 8192;
-  static constexpr uint32_t T = A + 64 * kLd * 4;    // fp32 [64][65]
+  static constexpr uint32_t T = A + 64 * kLd * 4;    // fp32 [64][kLd]
   static constexpr uint32_t Y1 = T + 64 * kLd * 4;   // fp32 [2][16][16]; decay block at the end
   static constexpr uint32_t Y2 = Y1 + 2 * 256 * 4;   // fp32 [32][33]
   static constexpr uint32_t G = Y2 + 32 * 33 * 4;    // fp32 [64]
@@ -146,6 +141,7 @@ struct PrepItem {
   int64_t ci = 0, t0 = 0;   // global chunk index, first token
   int h = 0, L = 0;         // head, valid rows
 };
+
 
 // Item j of the prep.  kOrdered: chunk positions in order (position p of
 // every sequence and head before position p + 1), so that the next chunk of
@@ -322,7 +318,7 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
     for (int e = tid; e < 64 * kLd; e += kPrepThreads) sT[e] = 0.f;
     __syncthreads();
     if (tid >= 32 && tid < kC) sG[tid] = g_scan + sG[31];
-    if (tid < kC) sGam[tid] = __expf(tid < 32 ? g_scan : g_scan + sG[31]);
+    if (tid < kC) sGam[tid] = exp_fast(tid < 32 ? g_scan : g_scan + sG[31]);
     __syncthreads();
     stamp(1);
 
@@ -369,12 +365,16 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
     stamp(2);
     // fused: once the previous item's stores have read the other K/Q buffer
     // and the V buffer, the next item's K/Q tiles and this item's V go there
+    // The state pass waits for the first chunk positions: a worker's first
+    // item is published here, later ones during the block inverse below.
+    const bool publish_now = n_done == 2;
     if (kFused && tid == kPrepIO) {
       io_stamp(0);
       bulk_wait_read_all();
       io_stamp(1);
       if (jn < n_items) issue_kq(nxt, buf ^ 1);
       if (have_prev) issue_v(cur, sm + Lay::V, 8192);
+      if (publish_now) publish(prev);
       io_stamp(2);
     }
     __syncthreads();
@@ -402,7 +402,7 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int jc = 32 * hv + jj;
-          sA[row * kLd + jc] = jc < row ? br * __expf(Gr - sG[jc]) * __uint_as_float(g[jj]) : 0.f;
+          sA[row * kLd + jc] = jc < row ? br * exp_fast(Gr - sG[jc]) * __uint_as_float(g[jj]) : 0.f;
         }
       } else {          // P^ = lower(Gam_rj q_r.k_j) / sqrt(dk), chunks 4hv .. 4hv+3 of row r
         const int r = row - kC;
@@ -413,8 +413,8 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j0 = 32 * hv + 8 * cq + 2 * e, j1 = j0 + 1;
-            const float p0 = (j0 <= r && r < L) ? kScale * __expf(Gr - sG[j0]) * __uint_as_float(g[8 * cq + 2 * e]) : 0.f;
-            const float p1 = (j1 <= r && r < L) ? kScale * __expf(Gr - sG[j1]) * __uint_as_float(g[8 * cq + 2 * e + 1]) : 0.f;
+            const float p0 = (j0 <= r && r < L) ? kScale * exp_fast(Gr - sG[j0]) * __uint_as_float(g[8 * cq + 2 * e]) : 0.f;
+            const float p1 = (j1 <= r && r < L) ? kScale * exp_fast(Gr - sG[j1]) * __uint_as_float(g[8 * cq + 2 * e + 1]) : 0.f;
             w[e] = pack_bf16(p0, p1);
           }
           uint8_t* pdst = kFused ? sm + Lay::PS : img + kImgP;
@@ -462,7 +462,7 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
       }
 #pragma unroll
       for (int r = 0; r < 16; ++r) sT[(o + r) * kLd + o + c] = x[r];
-    } else if (kFused && tid == kPrepIO && have_prev) {
+    } else if (kFused && tid == kPrepIO && have_prev && !publish_now) {
       // meanwhile: every store of the previous item (all groups but this
       // item's P^) has landed, so it can be published
       io_stamp(5);
@@ -477,20 +477,26 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
       const int ro = 16 * (2 * p + 1), co = 16 * (2 * p);
       float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float t = sT[(co + k) * kLd + co + c];
-        y0 = fmaf(sA[(ro + r0) * kLd + co + k], t, y0);
-        y1 = fmaf(sA[(ro + r0 + 8) * kLd + co + k], t, y1);
+      for (int k4 = 0; k4 < 16; k4 += 4) {
+        const float4 a0 = *reinterpret_cast<const float4*>(sA + (ro + r0) * kLd + co + k4);
+        const float4 a1 = *reinterpret_cast<const float4*>(sA + (ro + r0 + 8) * kLd + co + k4);
+        const float t0 = sT[(co + k4) * kLd + co + c], t1 = sT[(co + k4 + 1) * kLd + co + c];
+        const float t2 = sT[(co + k4 + 2) * kLd + co + c], t3 = sT[(co + k4 + 3) * kLd + co + c];
+        y0 = fmaf(a0.x, t0, fmaf(a0.y, t1, fmaf(a0.z, t2, fmaf(a0.w, t3, y0))));
+        y1 = fmaf(a1.x, t0, fmaf(a1.y, t1, fmaf(a1.z, t2, fmaf(a1.w, t3, y1))));
       }
       sY1[p * 256 + r0 * 16 + c] = y0;
       sY1[p * 256 + (r0 + 8) * 16 + c] = y1;
       __syncthreads();
       float z0 = 0.f, z1 = 0.f;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float y = sY1[p * 256 + k * 16 + c];
-        z0 = fmaf(sT[(ro + r0) * kLd + ro + k], y, z0);
-        z1 = fmaf(sT[(ro + r0 + 8) * kLd + ro + k], y, z1);
+      for (int k4 = 0; k4 < 16; k4 += 4) {
+        const float4 b0 = *reinterpret_cast<const float4*>(sT + (ro + r0) * kLd + ro + k4);
+        const float4 b1 = *reinterpret_cast<const float4*>(sT + (ro + r0 + 8) * kLd + ro + k4);
+        const float u0 = sY1[p * 256 + k4 * 16 + c], u1 = sY1[p * 256 + (k4 + 1) * 16 + c];
+        const float u2 = sY1[p * 256 + (k4 + 2) * 16 + c], u3 = sY1[p * 256 + (k4 + 3) * 16 + c];
+        z0 = fmaf(b0.x, u0, fmaf(b0.y, u1, fmaf(b0.z, u2, fmaf(b0.w, u3, z0))));
+        z1 = fmaf(b1.x, u0, fmaf(b1.y, u1, fmaf(b1.z, u2, fmaf(b1.w, u3, z1))));
       }
       sT[(ro + r0) * kLd + co + c] = -z0;
       sT[(ro + r0 + 8) * kLd + co + c] = -z1;
@@ -499,21 +505,29 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
     {  // level 2: Y = A[32:, :32] T[:32, :32];  T[32:, :32] = -T[32:, 32:] Y
       const int c = tid & 31, r0 = tid >> 5;
       float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-      for (int k = 0; k < 32; ++k) {
-        const float t = sT[k * kLd + c];
+#pragma unroll 2
+      for (int k4 = 0; k4 < 32; k4 += 4) {
+        const float t0 = sT[k4 * kLd + c], t1 = sT[(k4 + 1) * kLd + c];
+        const float t2 = sT[(k4 + 2) * kLd + c], t3 = sT[(k4 + 3) * kLd + c];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) y[m] = fmaf(sA[(32 + r0 + 8 * m) * kLd + k], t, y[m]);
+        for (int m = 0; m < 4; ++m) {
+          const float4 a = *reinterpret_cast<const float4*>(sA + (32 + r0 + 8 * m) * kLd + k4);
+          y[m] = fmaf(a.x, t0, fmaf(a.y, t1, fmaf(a.z, t2, fmaf(a.w, t3, y[m]))));
+        }
       }
 #pragma unroll
       for (int m = 0; m < 4; ++m) sY2[(r0 + 8 * m) * 33 + c] = y[m];
       __syncthreads();
       float z[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-      for (int k = 0; k < 32; ++k) {
-        const float yy = sY2[k * 33 + c];
+#pragma unroll 2
+      for (int k4 = 0; k4 < 32; k4 += 4) {
+        const float u0 = sY2[k4 * 33 + c], u1 = sY2[(k4 + 1) * 33 + c];
+        const float u2 = sY2[(k4 + 2) * 33 + c], u3 = sY2[(k4 + 3) * 33 + c];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) z[m] = fmaf(sT[(32 + r0 + 8 * m) * kLd + 32 + k], yy, z[m]);
+        for (int m = 0; m < 4; ++m) {
+          const float4 b = *reinterpret_cast<const float4*>(sT + (32 + r0 + 8 * m) * kLd + 32 + k4);
+          z[m] = fmaf(b.x, u0, fmaf(b.y, u1, fmaf(b.z, u2, fmaf(b.w, u3, z[m]))));
+        }
       }
 #pragma unroll
       for (int m = 0; m < 4; ++m) sT[(32 + r0 + 8 * m) * kLd + c] = -z[m];
@@ -608,7 +622,7 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
       }
     }
     if (tid < kC) {
-      const float d = tid < L ? __expf(sG[L - 1] - sG[tid]) : 0.f;
+      const float d = tid < L ? exp_fast(sG[L - 1] - sG[tid]) : 0.f;
       if (kFused) {
         for (int hh = 0; hh < 2; ++hh) {
           float* blk = reinterpret_cast<float*>(sm + Lay::V + hh * kImgHalf + kImgDecay);
@@ -696,7 +710,11 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   const bool timed = trace && threadIdx.x == 0 && unit < kMaxTracedUnits;
   if (timed) trace[kUnitTimes + 3 * unit] = globaltimer_ns();
   const float* sD = reinterpret_cast<const float*>(sm + kS_UT + kImgDecay);   // d_r, then G_r
-  __shared__ uint64_t bar_wq[2], bar_kp[2], bar_u, bar_m1, bar_m1b, bar_m2, bar_mo;
+  __shared__ uint64_t bar_wq[2], bar_kp[2], bar_p[2], bar_u, bar_m1, bar_m1b, bar_m2, bar_mo;
+  // (fused) chunks [cb, s_ready_hi) of this unit are known to be published;
+  // written only by warp 1 at the top of a chunk, read by the loaders after
+  // the chunk's first barrier
+  __shared__ long long s_ready_hi;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
 
@@ -717,6 +735,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar_wq[b], 1);
       mbar_init(&bar_kp[b], 1);
+      mbar_init(&bar_p[b], 1);
     }
     mbar_init(&bar_u, 1);
     mbar_init(&bar_m1, 1);
@@ -725,6 +744,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     mbar_init(&bar_mo, 1);
     fence_barrier_init();
     s_abort = 0;
+    s_ready_hi = cb;
     prefetch_tensormap(tm_k);
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
@@ -767,29 +787,81 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     mbar_arrive_expect_tx(&bar_wq[buf], 65536);
     tma_load_1d(sm + kS_WQ + buf * 65536, img_of(ci) + kImgWQ, 65536, &bar_wq[buf]);
   };
-  auto issue_kp = [&](int64_t ci, int buf) {
-    uint8_t* dst = sm + kS_KP + buf * 40960;
-    mbar_arrive_expect_tx(&bar_kp[buf], 40960);
-    tma_load_4d(dst, tm_k, 0, t0_of(ci), 0, h, &bar_kp[buf]);
-    tma_load_1d(dst + 32768, img_of(ci) + kImgP, 8192, &bar_kp[buf]);
+  auto issue_k = [&](int64_t ci, int buf) {   // K tile of the chunk, straight from the input
+    mbar_arrive_expect_tx(&bar_kp[buf], 32768);
+    tma_load_4d(sm + kS_KP + buf * 40960, tm_k, 0, t0_of(ci), 0, h, &bar_kp[buf]);
+  };
+  auto issue_p = [&](int64_t ci, int buf) {
+    mbar_arrive_expect_tx(&bar_p[buf], 8192);
+    tma_load_1d(sm + kS_KP + buf * 40960 + 32768, img_of(ci) + kImgP, 8192, &bar_p[buf]);
   };
   auto issue_u = [&](int64_t ci) {    // this half's U~^T rows and the decay block
     mbar_arrive_expect_tx(&bar_u, (uint32_t)kImgHalf);
     tma_load_1d(sm + kS_UT, img_of(ci) + kImgU0 + half * kImgHalf, (uint32_t)kImgHalf, &bar_u);
   };
-  auto warm_l2 = [&](int64_t ci) {    // the whole image of a later chunk
+  auto warm_l2 = [&](int64_t ci) {    // the whole image of a later chunk (split form)
     prefetch_l2(img_of(ci), (uint32_t)kImgStride);
   };
-  // Loads are issued by single threads of warps 1 and 2 (thread 0 issues the
-  // MMAs), so the kinds of issue overlap.  Each counts the phases it started
-  // on its load barriers, for a clean exit after a timeout.
-  constexpr int kLoaderA = 32;   // K / P^ and U~^T, one chunk ahead
+  // Loads are issued by single threads of warps 1, 2 and 3 (thread 0 issues
+  // the MMAs), so that each one's issue work fits in the time MMA-2 takes.
+  // Each counts the phases it started on its load barriers, for a clean exit
+  // after a timeout.
+  constexpr int kLoaderA = 32;   // K, one chunk ahead; polls the ready flags
   constexpr int kLoaderB = 64;   // W / Q^, two chunks ahead, and the L2 warm-up
-  uint32_t n_wq[2] = {0, 0}, n_kp[2] = {0, 0}, n_u = 0;
+  constexpr int kLoaderC = 96;   // P^, U~^T and the decay block, one chunk ahead
+  uint32_t n_wq[2] = {0, 0}, n_kp[2] = {0, 0}, n_p[2] = {0, 0}, n_u = 0;
   int64_t wq_next = cb;          // (kLoaderB) first chunk whose W / Q^ is not issued yet
-  auto load_kp_u = [&](int64_t ci, int buf) -> bool {   // (kLoaderA)
-    if (kFused && !ready_wait(flag_of(ci))) return false;
-    issue_kp(ci, buf); ++n_kp[buf];
+  // Ready flags (fused form).  A poll reads the flags of eight chunks from
+  // `from` with relaxed loads (one round trip) and, when the first few are
+  // set, makes what they published visible with one acquire fence; it
+  // returns the new bound of known-published chunks.  Warp 1 polls 32 chunks
+  // at a time at the top of a chunk, while MMA-1 runs and warps 1-3 have
+  // nothing else to do, and shares the bound; the loaders' own checks then
+  // cost nothing unless the per-chunk work has fallen behind.
+  auto poll_from = [&](int64_t from) -> int64_t {
+    uint32_t v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = from + k < ce ? ld_relaxed_gpu(flag_of(from + k)) : 0u;
+    int k = 0;
+    bool run = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      run = run && v[i] != 0;
+      k += run;
+    }
+    if (k > 0) {
+      fence_acq_rel_gpu();
+      fence_proxy_async_global();
+    }
+    return from + k;
+  };
+  int64_t my_hi = cb;   // this thread's own bound
+  auto is_ready = [&](int64_t ci, bool wait) -> bool {
+    if (!kFused || ci < my_hi) return true;
+    const int64_t sh = (int64_t)*reinterpret_cast<volatile long long*>(&s_ready_hi);
+    if (ci < sh) {   // published as seen by the first loader before the last barrier
+      my_hi = sh;
+      fence_proxy_async_global();
+      return true;
+    }
+    my_hi = poll_from(my_hi > sh ? my_hi : sh);
+    if (ci < my_hi || !wait) return ci < my_hi;
+    const uint64_t t_start = globaltimer_ns();
+    do {
+      __nanosleep(64);
+      my_hi = poll_from(my_hi);
+      if (ci < my_hi) return true;
+    } while (globaltimer_ns() - t_start < kReadyWaitNs);
+    return false;
+  };
+  auto load_k = [&](int64_t ci, int buf) -> bool {   // (kLoaderA)
+    if (!is_ready(ci, true)) return false;
+    issue_k(ci, buf); ++n_kp[buf];
+    return true;
+  };
+  auto load_pu = [&](int64_t ci, int buf) -> bool {   // (kLoaderC)
+    if (!is_ready(ci, true)) return false;
+    issue_p(ci, buf); ++n_p[buf];
     issue_u(ci); ++n_u;
     return true;
   };
@@ -799,9 +871,8 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   auto load_wq = [&](int64_t must, bool m1_done) -> bool {
     while (wq_next < ce && wq_next <= must + 1) {
       if (wq_next == must + 1) {
-        if (!m1_done) break;
-        if (kFused && !ready_now(flag_of(wq_next))) break;
-      } else if (kFused && !ready_wait(flag_of(wq_next))) {
+        if (!m1_done || !is_ready(wq_next, false)) break;
+      } else if (!is_ready(wq_next, true)) {
         return false;
       }
       const int b = (int)((wq_next - cb) & 1);
@@ -810,7 +881,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     }
     return true;
   };
-  if (tid == kLoaderA && cb < ce && !load_kp_u(cb, 0)) {
+  if (cb < ce && ((tid == kLoaderA && !load_k(cb, 0)) || (tid == kLoaderC && !load_pu(cb, 0)))) {
     flag_status(status, GDN_ERR_TIMEOUT);
     s_abort = 1;
   }
@@ -827,17 +898,18 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   int prev_L = 0;
   int64_t prev_t0 = 0;
   // rows of out for the previous chunk, staged in its (consumed) K / P^ buffer
-  // (warps 1-7 only: warp 0 is busy issuing MMA-1 at that point)
+  // as [r][128] bf16 (256 B per row, this unit's half of the row of out);
+  // consecutive threads of warps 4-7 move consecutive 16-byte pieces, so each
+  // warp store covers two whole 256-byte row segments.  (Warp 0 is issuing
+  // MMA-1 then; warps 1-3 hold the loader threads, whose acquire fences
+  // would otherwise wait for these stores to drain.)
   auto copy_out_prev = [&](int prev_buf) {
-    for (int w = tid - 32; w < 256; w += kStateThreads - 32) {
-      if (w < 0) break;
-      const int r = w >> 2, seg = w & 3;
-      if (r < prev_L) {
-        const uint4* src = reinterpret_cast<const uint4*>(sm + kS_KP + prev_buf * 40960 + r * 256 + seg * 64);
-        uint4* dst = reinterpret_cast<uint4*>(out + ((prev_t0 + r) * H + h) * kDV + 128 * half + 32 * seg);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = src[q];
-      }
+    const uint8_t* stage = sm + kS_KP + prev_buf * 40960;
+    for (int p = tid - 128; p < 16 * prev_L; p += kStateThreads - 128) {
+      if (p < 0) break;
+      const int r = p >> 4, c16 = p & 15;
+      const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 256 + c16 * 16);
+      *reinterpret_cast<uint4*>(out + ((prev_t0 + r) * H + h) * kDV + 128 * half + 8 * c16) = v;
     }
   };
 
@@ -851,6 +923,23 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
 
     // 1. [D_U | D_O] = S [W | Q^]^T (commit m1 and m1b); A = S from TMEM
     stamp(it, 0);
+    // (fused) warp 1 refreshes the shared bound when fewer than eight chunks
+    // ahead are known: one flag per lane, the run of published chunks from
+    // the bound by ballot, one acquire fence for all of them
+    if (kFused && warp == 1) {
+      const int64_t hi = *reinterpret_cast<volatile long long*>(&s_ready_hi);
+      if (hi < (ci + 8 < ce ? ci + 8 : ce)) {
+        const uint32_t f = hi + lane < ce ? ld_relaxed_gpu(flag_of(hi + lane)) : 0u;
+        const unsigned set = __ballot_sync(0xffffffffu, f != 0);
+        const int k = set == 0xffffffffu ? 32 : __ffs(~set) - 1;
+        if (k > 0) {
+          fence_acq_rel_gpu();
+          fence_proxy_async_global();
+        }
+        __syncwarp();
+        if (lane == 0) s_ready_hi = hi + k;
+      }
+    }
     if (timed && it == 0) trace[kUnitTimes + 3 * unit + 1] = globaltimer_ns();
     if (tid == 0) {
       if (!mbar_wait(&bar_wq[buf], bpar)) {
@@ -884,7 +973,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
       tmem_ld32(tmem + lane_off + kT_U + 32 * colhalf, g);
       tmem_ld_wait();
       stamp(it, 8);
-      gC = __expf(sD[64 + L - 1]);
+      gC = exp_fast(sD[64 + L - 1]);
       uint32_t ua[16], ud[16];
 #pragma unroll
       for (int cq = 0; cq < 4; ++cq) {
@@ -912,7 +1001,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
 
     // 3. D_S = (dU)^T K (commit m2) ; D_O += U^T P^^T (commit mo)
     if (tid == 0) {
-      if (!mbar_wait(&bar_kp[buf], bpar)) {
+      if (!mbar_wait(&bar_kp[buf], bpar) || !mbar_wait(&bar_p[buf], bpar)) {
         s_abort = 1;
       } else {
         tc_fence_after();
@@ -933,7 +1022,8 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     // with the U~^T buffer), W / Q^ of the next chunk if not yet in flight
     // and of the chunk after it once MMA-1 finished reading this buffer, and
     // (split form) L2 warm-up of a later chunk's image
-    if (tid == kLoaderA && ci + 1 < ce && !load_kp_u(ci + 1, buf ^ 1)) {
+    if (ci + 1 < ce && ((tid == kLoaderA && !load_k(ci + 1, buf ^ 1)) ||
+                        (tid == kLoaderC && !load_pu(ci + 1, buf ^ 1)))) {
       flag_status(status, GDN_ERR_TIMEOUT);
       s_abort = 1;
     }
@@ -1021,12 +1111,13 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
 #pragma unroll
     for (int j = 0; j < 32; ++j) p[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
   }
-  if ((tid == kLoaderA || tid == kLoaderB) && s_abort) {   // let copies in flight land
+  if ((tid == kLoaderA || tid == kLoaderB || tid == kLoaderC) && s_abort) {   // let copies in flight land
     flag_status(status, GDN_ERR_TIMEOUT);
     const uint64_t lim = 100000000ull;
     for (int b = 0; b < 2; ++b) {
       if (n_wq[b]) mbar_wait(&bar_wq[b], (n_wq[b] - 1) & 1, lim);
       if (n_kp[b]) mbar_wait(&bar_kp[b], (n_kp[b] - 1) & 1, lim);
+      if (n_p[b]) mbar_wait(&bar_p[b], (n_p[b] - 1) & 1, lim);
     }
     if (n_u) mbar_wait(&bar_u, (n_u - 1) & 1, lim);
   }
@@ -1064,7 +1155,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
 
 // fused form: cooperative, one CTA per SM; CTAs [0, n_state) are the state
 // units (unit u = (sequence u / 2H, head (u / 2) % H, half u % 2)), the rest
-// prep workers over all chunk positions in order
+// prep workers over all chunk positions in order; ready[] holds a flag per
+// (chunk, head)
 __global__ void __launch_bounds__(kStateThreads, 1)
 tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kb,
@@ -1078,8 +1170,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint8_t* sm = align_smem_1024(smem_raw);
   if ((int32_t)blockIdx.x < n_state) {
     const int u = blockIdx.x;
-    state_role<true>(sm, &tm_kb, S0, out, S_final, map, H, scratch, ready, status, trace,
-                     trace_chunks, u / (2 * H), (u >> 1) % H, u & 1);
+    state_role<true>(sm, &tm_kb, S0, out, S_final, map, H, scratch, ready, status, trace, trace_chunks, u / (2 * H), (u >> 1) % H, u & 1);
   } else {
     int64_t positions = map.chunks_per_seq;
     if (map.cu_seqlens) {
