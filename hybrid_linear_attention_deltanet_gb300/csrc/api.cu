@@ -20,6 +20,35 @@ constexpr int kMaxDevices = 64;
 unsigned* g_status_ptr[kMaxDevices] = {};
 std::mutex g_status_mu;
 
+// Per-device stream-ordered pool for the prefill scratch.  Its release
+// threshold keeps freed scratch mapped for later calls: the default pool
+// hands memory back to the system at every synchronisation, and mapping a
+// few hundred MB again costs about as much as the prefill itself.  The pool
+// holds the largest scratch any call needed until the process exits.
+cudaMemPool_t g_scratch_pool[kMaxDevices] = {};
+std::mutex g_pool_mu;
+
+cudaMemPool_t scratch_pool() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  if (!g_scratch_pool[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = ~0ull;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return nullptr;
+    }
+    g_scratch_pool[dev] = pool;
+  }
+  return g_scratch_pool[dev];
+}
+
 }  // namespace
 
 // Address of this device's status word, looked up once per device with that
@@ -163,7 +192,9 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
                                : prefill_simt_scratch_bytes(a.max_chunks, heads);
   void* scratch = nullptr;
   if (off_bytes + work_bytes > 0 &&
-      cudaMallocAsync(&scratch, off_bytes + work_bytes, stream) != cudaSuccess)
+      (!scratch_pool() ||
+       cudaMallocFromPoolAsync(&scratch, off_bytes + work_bytes, scratch_pool(), stream) !=
+           cudaSuccess))
     return GDN_ERR_CUDA;
   a.scratch = (char*)scratch + off_bytes;
   cudaError_t e = cudaSuccess;

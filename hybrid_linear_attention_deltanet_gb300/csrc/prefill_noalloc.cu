@@ -2,7 +2,7 @@
 // memory during a call.
 //
 // gdn_prefill obtains its scratch (per-chunk operand images and, for packed
-// batches, the chunk offsets) with stream-ordered cudaMallocAsync.  Some
+// batches, the chunk offsets) stream-ordered from a memory pool.  Some
 // callers cannot allow that: serving loops that fix their memory footprint
 // at start-up so that no request can fail on an allocation or fragment the
 // pool mid-flight, hosts whose device memory is owned by another allocator
