@@ -154,7 +154,7 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
   // token tensors may be empty (and then null) only when there are no tokens
   if (T_total > 0 && (!q || !k || !v || !alpha || !beta || !out)) return GDN_ERR_INVALID_ARG;
   if (io_dtype != GDN_F32 && io_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
-  if (dk != kDK || dv != kDV) return GDN_ERR_UNSUPPORTED;
+  if (dk != kDK || !supported_dv(dv)) return GDN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(alpha) || !aligned4(beta) ||
       !aligned16(out) || !aligned16(S0) || !aligned16(S_final) || !aligned4(cu_seqlens))
     return GDN_ERR_ALIGNMENT;
@@ -186,10 +186,13 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
   a.max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
 
   const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
-  const bool tc = io_dtype == GDN_BF16;
+  // bf16 I/O at dv = 256 runs on the tensor cores; fp32 I/O, and bf16 at
+  // dv = 512, on the CUDA cores
+  const bool tc = io_dtype == GDN_BF16 && dv == kDV;
+  a.dv = dv;
   a.allow_overlap = true;
   const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads)
-                               : prefill_simt_scratch_bytes(a.max_chunks, heads);
+                               : prefill_simt_scratch_bytes(a.max_chunks, heads, dv);
   void* scratch = nullptr;
   if (off_bytes + work_bytes > 0 &&
       (!scratch_pool() ||
@@ -215,7 +218,7 @@ int gdn_decode_step(const void* q, const void* k, const void* v, const float* al
   if (!q || !k || !v || !alpha || !beta || !S_inout || !out) return GDN_ERR_INVALID_ARG;
   if (batch < 1 || heads < 1) return GDN_ERR_INVALID_ARG;
   if (io_dtype != GDN_F32 && io_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
-  if (dk != kDK || dv != kDV) return GDN_ERR_UNSUPPORTED;
+  if (dk != kDK || !supported_dv(dv)) return GDN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(alpha) || !aligned4(beta) ||
       !aligned16(S_inout) || !aligned16(out))
     return GDN_ERR_ALIGNMENT;
@@ -230,7 +233,7 @@ int gdn_decode_step(const void* q, const void* k, const void* v, const float* al
   for (int i = 0; i < 5; ++i)
     if (overlaps(others[i], others[5])) return GDN_ERR_INVALID_ARG;
   const cudaError_t e =
-      launch_decode_step(q, k, v, alpha, beta, S_inout, out, batch, heads, io_dtype, stream);
+      launch_decode_step(q, k, v, alpha, beta, S_inout, out, batch, heads, dv, io_dtype, stream);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -244,7 +247,7 @@ int gdn_testing_prefill_prep(const void* q, const void* k, const void* v, const 
   const bool varlen = cu_seqlens != nullptr;
   const int64_t T_total = varlen ? seqlen : (int64_t)batch * seqlen;
   PrefillLaunch a{};
-  a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.H = heads;
+  a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.H = heads; a.dv = kDV;
   a.status = status_ptr();
   if (!a.status) return GDN_ERR_CUDA;
   a.map.cu_seqlens = cu_seqlens;

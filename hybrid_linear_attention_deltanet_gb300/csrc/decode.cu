@@ -10,8 +10,9 @@
 // i.e. Eq. 16-18 for one column of the paper's S, and Eq. 19 read from the
 // updated row without a second pass over it.
 //
-// Roofline: HBM.  Per (sequence, head) the 256 x 256 fp32 state is read once
-// and written once (512 KiB), against ~3 KiB of q, k, v, out, alpha, beta.
+// Roofline: HBM.  Per (sequence, head) the dv x 256 fp32 state is read once
+// and written once (512 KiB at dv = 256), against ~3 KiB of q, k, v, out,
+// alpha, beta.
 // Each warp streams whole 1 KiB rows with two 16-byte loads per lane (a fully
 // coalesced 512 B per instruction), keeps 8 of them in flight, and reduces
 // the two dot products with warp shuffles; the state never touches shared
@@ -22,7 +23,7 @@
 namespace gdn {
 namespace {
 
-constexpr int kRowsPerCta = 64;                 // a quarter of one head's state
+constexpr int kRowsPerCta = 64;                 // a quarter of one head's state at dv = 256
 constexpr int kWarps = 8;
 constexpr int kRowsPerWarp = kRowsPerCta / kWarps;  // 8
 constexpr int kBatch = 4;                       // rows in flight per warp
@@ -47,10 +48,11 @@ template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                    const float* __restrict__ alpha, const float* __restrict__ beta,
-                   float* __restrict__ S, T* __restrict__ out) {
-  static_assert(kDK == 256 && kDV == 256, "row layout assumes 256 x 256 states");
-  const int64_t unit = blockIdx.x >> 2;    // n * H + h
-  const int quarter = blockIdx.x & 3;
+                   float* __restrict__ S, T* __restrict__ out, int32_t dv) {
+  static_assert(kDK == 256, "row layout assumes rows of 256 fp32");
+  const int blocks_per_unit = dv / kRowsPerCta;
+  const int64_t unit = blockIdx.x / blocks_per_unit;    // n * H + h
+  const int quarter = (int)(blockIdx.x % blocks_per_unit);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   float kr[8], qr[8];
@@ -63,8 +65,8 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
   const float a = alpha[unit], b = beta[unit];
 
   const int row0 = quarter * kRowsPerCta + warp * kRowsPerWarp;
-  float* Srow0 = S + (unit * kDV + row0) * kDK;
-  const float vj = lane < kRowsPerWarp ? ld_in(v + unit * kDV + row0 + lane) : 0.f;
+  float* Srow0 = S + (unit * dv + row0) * kDK;
+  const float vj = lane < kRowsPerWarp ? ld_in(v + unit * dv + row0 + lane) : 0.f;
   float o_mine = 0.f;
 
 #pragma unroll
@@ -100,25 +102,26 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
       if (lane == rb + r) o_mine = o;
     }
   }
-  if (lane < kRowsPerWarp) st_out(out + unit * kDV + row0 + lane, o_mine);
+  if (lane < kRowsPerWarp) st_out(out + unit * dv + row0 + lane, o_mine);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, const float* alpha,
                                const float* beta, float* S, void* out, int32_t N, int32_t H,
-                               int io_dtype, cudaStream_t stream) {
+                               int32_t dv, int io_dtype, cudaStream_t stream) {
+  if (!supported_dv(dv)) return cudaErrorInvalidValue;
   const int64_t units = (int64_t)N * H;
-  const int64_t blocks = units * (kDV / kRowsPerCta);
+  const int64_t blocks = units * (dv / kRowsPerCta);
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (blocks == 0) return cudaSuccess;
   if (io_dtype == GDN_BF16) {
     decode_step_kernel<__nv_bfloat16><<<(unsigned)blocks, kWarps * 32, 0, stream>>>(
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, alpha, beta,
-        S, (__nv_bfloat16*)out);
+        S, (__nv_bfloat16*)out, dv);
   } else {
     decode_step_kernel<float><<<(unsigned)blocks, kWarps * 32, 0, stream>>>(
-        (const float*)q, (const float*)k, (const float*)v, alpha, beta, S, (float*)out);
+        (const float*)q, (const float*)k, (const float*)v, alpha, beta, S, (float*)out, dv);
   }
   count_launches(1);
   return cudaGetLastError();

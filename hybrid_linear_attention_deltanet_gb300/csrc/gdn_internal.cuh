@@ -11,9 +11,14 @@
 
 namespace gdn {
 
-// Head geometry implemented by the kernels (Table 8: head dim 256).
+// Head geometry implemented by the kernels (Table 8: head dim 256).  The
+// value dimension dv is 256 (the configurations) or 512 (Table 8's value
+// expansion dv = 2 dk); kDV is the 256 case, which the tensor-core prefill
+// implements.
 constexpr int kDK = 256;
 constexpr int kDV = 256;
+constexpr int kDVMax = 512;
+inline bool supported_dv(int32_t dv) { return dv == 256 || dv == 512; }
 // Chunk length of the chunkwise-parallel form (Appendix A.3: C = 64).
 constexpr int kC = 64;
 // 1/sqrt(dk) for dk = 256: a power of two, so the scaling is exact.
@@ -100,6 +105,7 @@ struct PrefillLaunch {
   void* out; float* S_final;
   SeqMap map;
   int32_t H;
+  int32_t dv;           // 256 or 512
   int64_t max_chunks;   // grid bound for per-chunk kernels
   unsigned* status;
   void* scratch;        // device scratch of the size the path's *_scratch_bytes asks for
@@ -110,7 +116,7 @@ cudaError_t launch_chunk_offsets(const int32_t* cu_seqlens, int32_t N, int64_t T
                                  int32_t* chunk_off, unsigned* status, cudaStream_t stream);
 
 // CUDA-core (fp32 FFMA) chunkwise path: used for fp32 I/O.
-size_t prefill_simt_scratch_bytes(int64_t max_chunks, int32_t H);
+size_t prefill_simt_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv);
 cudaError_t launch_prefill_simt(const PrefillLaunch& a, int io_dtype, cudaStream_t stream);
 
 // Tensor-core (tcgen05) chunkwise path: used for bf16 I/O.
@@ -125,6 +131,6 @@ extern int32_t g_last_tc_form;
 
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, const float* alpha,
                                const float* beta, float* S, void* out, int32_t N, int32_t H,
-                               int io_dtype, cudaStream_t stream);
+                               int32_t dv, int io_dtype, cudaStream_t stream);
 
 }  // namespace gdn

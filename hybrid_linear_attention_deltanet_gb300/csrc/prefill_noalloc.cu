@@ -65,7 +65,7 @@ extern "C" int gdn_prefill_noalloc(const void* q, const void* k, const void* v,
   const int64_t T_total = varlen ? seqlen : (int64_t)batch * seqlen;
   if (T_total > 0 && (!q || !k || !v || !alpha || !beta || !out)) return GDN_ERR_INVALID_ARG;
   if (io_dtype != GDN_F32 && io_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
-  if (dk != kDK || dv != kDV) return GDN_ERR_UNSUPPORTED;
+  if (dk != kDK || !supported_dv(dv)) return GDN_ERR_UNSUPPORTED;
   if (!is_aligned(q, 16) || !is_aligned(k, 16) || !is_aligned(v, 16) || !is_aligned(out, 16) ||
       !is_aligned(S0, 16) || !is_aligned(S_final, 16) || !is_aligned(alpha, 4) ||
       !is_aligned(beta, 4) || !is_aligned(cu_seqlens, 4))
@@ -91,10 +91,13 @@ extern "C" int gdn_prefill_noalloc(const void* q, const void* k, const void* v,
   a.map.T = varlen ? T_total : seqlen;
   a.map.chunks_per_seq = varlen ? 0 : (seqlen + kC - 1) / kC;
   a.max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
-  const bool tc = io_dtype == GDN_BF16;
+  // bf16 I/O at dv = 256 runs on the tensor cores; fp32 I/O, and bf16 at
+  // dv = 512, on the CUDA cores
+  const bool tc = io_dtype == GDN_BF16 && dv == kDV;
+  a.dv = dv;
   const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
   const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads)
-                               : prefill_simt_scratch_bytes(a.max_chunks, heads);
+                               : prefill_simt_scratch_bytes(a.max_chunks, heads, dv);
   if (off_bytes + work_bytes > kNoAllocScratchBytes) return GDN_ERR_SCRATCH_LIMIT;
 
   a.status = status_ptr();

@@ -37,18 +37,20 @@ constexpr int kNS = 32;          // rows of S per state-pass CTA
 // scratch per (chunk, head): W [C][dk], U~ [C][dv], P [C][C], G [C]
 struct SimtScratch {
   float* W; float* Ut; float* P; float* G;
+  int32_t dv;
   __host__ __device__ static size_t stride_W() { return (size_t)kC * kDK; }
-  __host__ __device__ static size_t stride_U() { return (size_t)kC * kDV; }
+  __host__ __device__ size_t stride_U() const { return (size_t)kC * dv; }
   __host__ __device__ static size_t stride_P() { return (size_t)kC * kC; }
   __host__ __device__ static size_t stride_G() { return (size_t)kC; }
 };
 
-inline SimtScratch carve(void* base, int64_t max_chunks, int32_t H) {
+inline SimtScratch carve(void* base, int64_t max_chunks, int32_t H, int32_t dv) {
   const size_t units = (size_t)max_chunks * H;
   char* p = (char*)base;
   SimtScratch s;
+  s.dv = dv;
   s.W = (float*)p;  p += align_up(units * SimtScratch::stride_W() * 4, 256);
-  s.Ut = (float*)p; p += align_up(units * SimtScratch::stride_U() * 4, 256);
+  s.Ut = (float*)p; p += align_up(units * s.stride_U() * 4, 256);
   s.P = (float*)p;  p += align_up(units * SimtScratch::stride_P() * 4, 256);
   s.G = (float*)p;
   return s;
@@ -125,11 +127,15 @@ chunk_prep_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
   }
   __syncthreads();
 
-  // V replaces Q
-  for (int e = tid; e < kC * kDV; e += kThreads) {
-    const int r = e / kDV, c = e % kDV;
-    QVs[r * kPad + c] = r < L ? ld_in(v + ((t0 + r) * H + h) * kDV + c) : 0.f;
-  }
+  // V block 0 (columns 0 .. 255) replaces Q
+  const int dv = scr.dv;
+  auto load_v = [&](int vb) {
+    for (int e = tid; e < kC * kDK; e += kThreads) {
+      const int r = e / kDK, c = e % kDK;
+      QVs[r * kPad + c] = r < L ? ld_in(v + ((t0 + r) * H + h) * dv + kDK * vb + c) : 0.f;
+    }
+  };
+  load_v(0);
   // T = (I + A)^{-1} by forward substitution, one column per thread
   if (tid < kC) {
     const int c = tid;
@@ -147,11 +153,12 @@ chunk_prep_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
   }
   __syncthreads();
 
-  // W = T diag(beta gamma) K ; U~ = T diag(beta) V ; one output column per thread
+  // W = T diag(beta gamma) K ; U~ = T diag(beta) V ; one output column per
+  // thread, V in blocks of 256 columns
   {
     const int c = tid;
     float* Wg = scr.W + (size_t)(ci * H + h) * SimtScratch::stride_W();
-    float* Ug = scr.Ut + (size_t)(ci * H + h) * SimtScratch::stride_U();
+    float* Ug = scr.Ut + (size_t)(ci * H + h) * scr.stride_U();
     for (int r = 0; r < kC; ++r) {
       float w = 0.f, u = 0.f;
       for (int j = 0; j <= r; ++j) {
@@ -160,7 +167,17 @@ chunk_prep_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
         u = fmaf(t * bs[j], QVs[j * kPad + c], u);
       }
       Wg[r * kDK + c] = w;
-      Ug[r * kDV + c] = u;
+      Ug[r * dv + c] = u;
+    }
+    for (int vb = 1; vb * kDK < dv; ++vb) {
+      __syncthreads();
+      load_v(vb);
+      __syncthreads();
+      for (int r = 0; r < kC; ++r) {
+        float u = 0.f;
+        for (int j = 0; j <= r; ++j) u = fmaf(Ts[r * kCP + j] * bs[j], QVs[j * kPad + c], u);
+        Ug[r * dv + kDK * vb + c] = u;
+      }
     }
   }
   if (tid < kC) scr.G[(size_t)(ci * H + h) * SimtScratch::stride_G() + tid] = Gs[tid];
@@ -182,7 +199,8 @@ state_pass_kernel(const T* __restrict__ q, const T* __restrict__ k,
 
   const int n = blockIdx.x, h = blockIdx.y, slice = blockIdx.z;
   const int tid = threadIdx.x, i = tid & 31, rg = tid >> 5;
-  const int64_t state_base = ((int64_t)n * H + h) * kDV * kDK + (int64_t)slice * kNS * kDK;
+  const int dv = scr.dv;
+  const int64_t state_base = ((int64_t)n * H + h) * dv * kDK + (int64_t)slice * kNS * kDK;
 
   for (int e = tid; e < kNS * kDK; e += kThreads) {
     const int r = e / kDK, c = e % kDK;
@@ -228,11 +246,11 @@ state_pass_kernel(const T* __restrict__ q, const T* __restrict__ k,
         }
       }
     }
-    const float* Ug = scr.Ut + u * SimtScratch::stride_U();
+    const float* Ug = scr.Ut + u * scr.stride_U();
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       const int r = rg * 8 + m;
-      Us[r * 33 + i] = Ug[r * kDV + slice * kNS + i] - accU[m];
+      Us[r * 33 + i] = Ug[r * dv + slice * kNS + i] - accU[m];
     }
     __syncthreads();
 
@@ -244,7 +262,7 @@ state_pass_kernel(const T* __restrict__ q, const T* __restrict__ k,
       if (r < L) {
         float o = gam[r] * accQ[m];
         for (int j = 0; j <= r; ++j) o = fmaf(Pg[r * kC + j], Us[j * 33 + i], o);
-        st_out(out + ((t0 + r) * H + h) * kDV + slice * kNS + i, o);
+        st_out(out + ((t0 + r) * H + h) * dv + slice * kNS + i, o);
       }
     }
 
@@ -274,7 +292,7 @@ constexpr size_t kStateSmem = sizeof(float) * (kNS * kPad + 3 * kC * 33 + 2 * kC
 
 template <typename T>
 cudaError_t launch_typed(const PrefillLaunch& a, cudaStream_t stream) {
-  SimtScratch scr = carve(a.scratch, a.max_chunks, a.H);
+  SimtScratch scr = carve(a.scratch, a.max_chunks, a.H, a.dv);
   cudaError_t e;
   e = cudaFuncSetAttribute(chunk_prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kPrepSmem);
@@ -289,7 +307,7 @@ cudaError_t launch_typed(const PrefillLaunch& a, cudaStream_t stream) {
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  dim3 g2((unsigned)a.map.N, (unsigned)a.H, kDV / kNS);
+  dim3 g2((unsigned)a.map.N, (unsigned)a.H, (unsigned)(a.dv / kNS));
   state_pass_kernel<T><<<g2, kThreads, kStateSmem, stream>>>(
       (const T*)a.q, (const T*)a.k, a.S0, (T*)a.out, a.S_final, a.map, a.H, scr);
   count_launches(1);
@@ -298,10 +316,10 @@ cudaError_t launch_typed(const PrefillLaunch& a, cudaStream_t stream) {
 
 }  // namespace
 
-size_t prefill_simt_scratch_bytes(int64_t max_chunks, int32_t H) {
+size_t prefill_simt_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv) {
   const size_t units = (size_t)max_chunks * H;
   return align_up(units * SimtScratch::stride_W() * 4, 256) +
-         align_up(units * SimtScratch::stride_U() * 4, 256) +
+         align_up(units * (size_t)kC * dv * 4, 256) +
          align_up(units * SimtScratch::stride_P() * 4, 256) +
          align_up(units * SimtScratch::stride_G() * 4, 256);
 }

@@ -24,8 +24,9 @@
  *  - io_dtype selects the element type of q, k, v and out: GDN_F32 (float) or
  *    GDN_BF16 (bfloat16 stored as uint16).  alpha, beta and every state are
  *    always fp32; accumulation is always fp32.
- *  - Supported head geometry: dk = dv = 256 (6 heads of 256 in the pages'
- *    GDN layers; any heads >= 1 is accepted).  Others: GDN_ERR_UNSUPPORTED.
+ *  - Supported head geometry: dk = 256 and dv = 256 (6 heads of 256 in the
+ *    pages' GDN layers) or dv = 512 (the value expansion dv = 2 dk of their
+ *    Table 8); any heads >= 1.  Others: GDN_ERR_UNSUPPORTED.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream) and never synchronise the host.  Host-side argument
  *    errors are returned before any launch; a failed launch or allocation
@@ -168,8 +169,9 @@ uint64_t gdn_kernel_launches(void);
 
 /*
  * gdn_prefill_path -- name of the kernel path gdn_prefill takes for an
- * io_dtype ("simt-f32": CUDA-core fp32 FFMA; "tcgen05-bf16": tensor-core
- * MMAs with bf16 operands and fp32 accumulation).  NULL for an unknown dtype.
+ * io_dtype at dv = 256 ("simt-f32": CUDA-core fp32 FFMA; "tcgen05-bf16":
+ * tensor-core MMAs with bf16 operands and fp32 accumulation).  At dv = 512
+ * both dtypes take the CUDA-core path.  NULL for an unknown dtype.
  */
 const char* gdn_prefill_path(int32_t io_dtype);
 

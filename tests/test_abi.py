@@ -65,7 +65,8 @@ def test_prefill_rejects_bad_host_arguments(lib):
     assert _prefill(lib, H=0) == 1
     assert _prefill(lib, T=-1) == 1
     assert _prefill(lib, dk=128) == 2
-    assert _prefill(lib, dv=512) == 2
+    assert _prefill(lib, dv=384) == 2
+    assert _prefill(lib, dv=128) == 2
     assert _prefill(lib, io=7) == 2
     assert _prefill(lib, q=MIS) == 3
     assert _prefill(lib, S_final=MIS) == 3
@@ -84,5 +85,7 @@ def test_decode_rejects_bad_host_arguments(lib):
     assert f(S=None) == 1
     assert f(N=0) == 1
     assert f(dk=64) == 2
+    assert lib.gdn_decode_step(A16, A16, A16, A16, A16, P(0x800000), P(0x900000), 4, 6, 256, 384,
+                               1, None) == 2
     assert f(q=MIS) == 3
     assert f(out=P(0x800000 + 1024)) == 1      # out inside the state
