@@ -46,19 +46,19 @@ def prefill_flops(lengths, H=H, dk=DK, dv=DV):
     return f_chunk * chunks * H
 
 
-def prefill_bytes(lengths, io_bytes=2, H=H, s0=True, s_final=True):
+def prefill_bytes(lengths, io_bytes=2, H=H, s0=True, s_final=True, dv=DV):
     """Algorithmic bytes: q, k, v in, out written (io dtype), alpha and beta
     (fp32) per token-head, plus S0 read and S_final written per sequence."""
     tok = sum(lengths)
-    per_tok = H * ((2 * DK + 2 * DV) * io_bytes + 8)
-    state = len(lengths) * H * DV * DK * 4
+    per_tok = H * ((2 * DK + 2 * dv) * io_bytes + 8)
+    state = len(lengths) * H * dv * DK * 4
     return tok * per_tok + state * (int(s0) + int(s_final))
 
 
-def decode_bytes(N, io_bytes=2):
+def decode_bytes(N, io_bytes=2, dv=DV):
     """Per step: the fp32 state read and written once, q, k, v, out and
     alpha, beta once."""
-    return N * H * (2 * DV * DK * 4 + (2 * DK + 2 * DV) * io_bytes + 8)
+    return N * H * (2 * dv * DK * 4 + (2 * DK + 2 * dv) * io_bytes + 8)
 
 
 def load_peaks():
@@ -315,6 +315,42 @@ def run_ours(args, rank, world, local_rank, dist):
     dbytes = decode_bytes(dcase.N)
     d_gbs_local = dbytes / (d_ms_local * 1e-3) / 1e9
 
+    # ---- dv = 512 (the value expansion dv = 2 dk of Table 8): decode over the
+    # same 256 sequences and the 8K prefill, each timed on its own
+    dcase5 = gdn_inputs.decode_256_dv512()
+    d5 = gdn_inputs.make_decode(dcase5, device=dev)
+    S5 = d5["S"]
+    dout5 = torch.empty(d5["v"].shape[1:], dtype=d5["v"].dtype, device=dev)
+    for t in range(3):
+        gdn.decode_step(d5["q"][t], d5["k"][t], d5["v"][t], d5["alpha"][t], d5["beta"][t], S5,
+                        out=dout5)
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for t in range(dcase5.steps):
+        gdn.decode_step(d5["q"][t], d5["k"][t], d5["v"][t], d5["alpha"][t], d5["beta"][t], S5,
+                        out=dout5)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    d5_ms = max_over_ranks(ev0.elapsed_time(ev1) / dcase5.steps)
+    del d5, S5, dout5
+    pcase5 = gdn_inputs.prefill_8k_dv512()
+    x5 = gdn_inputs.make_prefill(pcase5, device=dev)
+    out5, sf5 = torch.empty_like(x5["v"]), torch.empty_like(x5["S0"])
+    step5 = lambda: gdn.prefill(x5["q"], x5["k"], x5["v"], x5["alpha"], x5["beta"], x5["S0"],
+                                out=out5, S_final=sf5)
+    for _ in range(2):
+        step5()
+    torch.cuda.synchronize(dev)
+    p5_steps = 5
+    ev0.record(stream)
+    for _ in range(p5_steps):
+        step5()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    assert gdn.device_status() == 0
+    p5_ms = max_over_ranks(ev0.elapsed_time(ev1) / p5_steps)
+    del x5, out5, sf5
+
     res = None
     if rank == 0:
         clocks = sampler.summary()
@@ -358,6 +394,20 @@ def run_ours(args, rank, world, local_rank, dist):
                     "pipeline": "two buffer sets; H2D of step i+1 and D2H of step i-1 "
                                 "overlap step i on separate streams"},
             "gpu_launches": int(n1 - n0),
+            "dv512": {
+                "decode": {"workload": dcase5.name,
+                           "value": round(throughput(decode_bytes(dcase5.N, dv=512) * world,
+                                                     d5_ms) / 1e9, 2),
+                           "unit": "GB/s", "ms_per_step": round(d5_ms, 4),
+                           "frac_of_hbm": round(decode_bytes(dcase5.N, dv=512) / (d5_ms * 1e-3)
+                                                / 1e9 / peaks["hbm_gbs"], 4)},
+                "prefill": {"workload": pcase5.name,
+                            "value": round(throughput(pcase5.total_tokens * world, p5_ms) / 1e6, 4),
+                            "unit": "Mtok/s/layer", "ms_per_step": round(p5_ms, 4),
+                            "path": "CUDA-core (fp32 FFMA) chunked form",
+                            "counted_tflops": round(prefill_flops(pcase5.lengths, dv=512)
+                                                    / (p5_ms * 1e-3) / 1e12, 3)},
+            },
             "clocks": clocks,
             "decode": {
                 "workload": dcase.name,

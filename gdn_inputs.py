@@ -154,6 +154,15 @@ def decode_256x1000() -> DecodeCase:
     return DecodeCase("decode N=256 H=6 d=256 bf16 x1000 steps", N=256, steps=1000, seed=2)
 
 
+def prefill_8k_dv512() -> PrefillCase:
+    return PrefillCase("prefill B=4 T=8192 H=6 dk=256 dv=512 bf16", [8192] * 4, dv=512, seed=5)
+
+
+def decode_256_dv512() -> DecodeCase:
+    return DecodeCase("decode N=256 H=6 dk=256 dv=512 bf16 x200 steps", N=256, steps=200, dv=512,
+                      seed=6)
+
+
 def prefill_64k() -> PrefillCase:
     return PrefillCase("prefill B=1 T=65536 H=6 d=256 bf16 S0=0", [65536], s0_std=None, seed=3)
 
