@@ -404,7 +404,7 @@ def run_ours(args, rank, world, local_rank, dist):
                 "prefill": {"workload": pcase5.name,
                             "value": round(throughput(pcase5.total_tokens * world, p5_ms) / 1e6, 4),
                             "unit": "Mtok/s/layer", "ms_per_step": round(p5_ms, 4),
-                            "path": "CUDA-core (fp32 FFMA) chunked form",
+                            "path": gdn.prefill_path(pcase5.io_dtype),
                             "counted_tflops": round(prefill_flops(pcase5.lengths, dv=512)
                                                     / (p5_ms * 1e-3) / 1e12, 3)},
             },

@@ -186,12 +186,11 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
   a.max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
 
   const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
-  // bf16 I/O at dv = 256 runs on the tensor cores; fp32 I/O, and bf16 at
-  // dv = 512, on the CUDA cores
-  const bool tc = io_dtype == GDN_BF16 && dv == kDV;
+  // bf16 I/O runs on the tensor cores, fp32 I/O on the CUDA cores
+  const bool tc = io_dtype == GDN_BF16;
   a.dv = dv;
   a.allow_overlap = true;
-  const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads)
+  const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads, dv)
                                : prefill_simt_scratch_bytes(a.max_chunks, heads, dv);
   void* scratch = nullptr;
   if (off_bytes + work_bytes > 0 &&

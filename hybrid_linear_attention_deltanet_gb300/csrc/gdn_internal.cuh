@@ -13,8 +13,7 @@ namespace gdn {
 
 // Head geometry implemented by the kernels (Table 8: head dim 256).  The
 // value dimension dv is 256 (the configurations) or 512 (Table 8's value
-// expansion dv = 2 dk); kDV is the 256 case, which the tensor-core prefill
-// implements.
+// expansion dv = 2 dk); kDV is the 256 case.
 constexpr int kDK = 256;
 constexpr int kDV = 256;
 constexpr int kDVMax = 512;
@@ -120,7 +119,7 @@ size_t prefill_simt_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv);
 cudaError_t launch_prefill_simt(const PrefillLaunch& a, int io_dtype, cudaStream_t stream);
 
 // Tensor-core (tcgen05) chunkwise path: used for bf16 I/O.
-size_t prefill_tc_scratch_bytes(int64_t max_chunks, int32_t H);
+size_t prefill_tc_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv);
 cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool prep_only = false);
 size_t prefill_tc_image_stride();
 // phase-timeline buffer of the tensor-core state pass (test hook)

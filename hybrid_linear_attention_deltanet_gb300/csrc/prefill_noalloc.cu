@@ -91,12 +91,11 @@ extern "C" int gdn_prefill_noalloc(const void* q, const void* k, const void* v,
   a.map.T = varlen ? T_total : seqlen;
   a.map.chunks_per_seq = varlen ? 0 : (seqlen + kC - 1) / kC;
   a.max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
-  // bf16 I/O at dv = 256 runs on the tensor cores; fp32 I/O, and bf16 at
-  // dv = 512, on the CUDA cores
-  const bool tc = io_dtype == GDN_BF16 && dv == kDV;
+  // bf16 I/O runs on the tensor cores, fp32 I/O on the CUDA cores
+  const bool tc = io_dtype == GDN_BF16;
   a.dv = dv;
   const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
-  const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads)
+  const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads, dv)
                                : prefill_simt_scratch_bytes(a.max_chunks, heads, dv);
   if (off_bytes + work_bytes > kNoAllocScratchBytes) return GDN_ERR_SCRATCH_LIMIT;
 

@@ -68,7 +68,13 @@ constexpr size_t kImgP = 65536;       // P^  : K-major B image, 64 rows x 64
 constexpr size_t kImgU0 = 73728;
 constexpr size_t kImgHalf = 16896;    // 16384 + 512
 constexpr size_t kImgDecay = 16384;   // offset of the decay block inside a half
-constexpr size_t kImgStride = 107520; // kImgU0 + 2 * kImgHalf, rounded to 1 KB
+constexpr size_t kImgStride = 107520; // kImgU0 + 2 * kImgHalf (dv = 256), a multiple of 1 KB
+// At dv = 512 the image carries four 128-row slices of U~^T, each with its
+// decay block: kImgU0 + 4 * kImgHalf = 141312 bytes (also a multiple of 1 KB).
+__host__ __device__ constexpr size_t img_stride(int dv) {
+  return kImgU0 + (size_t)(dv / 128) * kImgHalf;
+}
+static_assert(img_stride(256) == kImgStride && img_stride(512) % 1024 == 0, "image strides");
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
@@ -178,7 +184,7 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
                                           const float* __restrict__ alpha,
                                           const float* __restrict__ beta, const SeqMap& map,
                                           int32_t H, uint8_t* __restrict__ scratch,
-                                          uint32_t* ready, unsigned* status,
+                                          uint32_t* ready, unsigned* status, int32_t dv,
                                           uint64_t* __restrict__ trace,
                                           uint64_t* __restrict__ timeline, int64_t n_items,
                                           int64_t worker, int64_t n_workers) {
@@ -244,14 +250,15 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
     }
     ++n_kq[b];
   };
-  auto issue_v = [&](const PrepItem& it, uint8_t* dst, uint32_t block_stride) {
+  // V columns [256 vh, 256 vh + 256) of the item
+  auto issue_v = [&](const PrepItem& it, int vh, uint8_t* dst, uint32_t block_stride) {
     mbar_arrive_expect_tx(&bar_v, 32768);
     for (int b = 0; b < 4; ++b)
-      tma_load_3d(dst + b * block_stride, tm_v, b * 64, it.h, (int32_t)it.t0, &bar_v);
+      tma_load_3d(dst + b * block_stride, tm_v, kDK * vh + b * 64, it.h, (int32_t)it.t0, &bar_v);
     ++n_v;
   };
   auto img_of = [&](const PrepItem& it) {
-    return scratch + (size_t)(it.ci * H + it.h) * kImgStride;
+    return scratch + (size_t)(it.ci * H + it.h) * img_stride(dv);
   };
   // (kPrepIO) the item's bulk stores have landed: raise its ready flag
   auto publish = [&](const PrepItem& it) {
@@ -264,13 +271,14 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
   bool have_prev = false;
   int64_t j = next_valid(worker, cur);
   uint32_t kq_ph[kBufs] = {};   // parity of each K/Q buffer's next phase
-  uint32_t ph = 0;              // parity of bar_v / bar_a / bar_bc for this item
+  uint32_t ph = 0;              // parity of bar_a for this item
+  uint32_t vph = 0, bcph = 0;   // parities of bar_v / bar_bc (dv / 256 uses per item)
   int buf = 0;
   float a_cur = 1.f, b_cur = 0.f;   // this item's gates (threads < C)
   if (kFused && j < n_items) {
     if (tid == kPrepIO) {
       issue_kq(cur, 0);
-      issue_v(cur, sm + Lay::V, 8192);
+      issue_v(cur, 0, sm + Lay::V, 8192);
     }
     if (tid < kC && tid < cur.L) {
       a_cur = alpha[(cur.t0 + tid) * H + cur.h];
@@ -373,7 +381,7 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
       bulk_wait_read_all();
       io_stamp(1);
       if (jn < n_items) issue_kq(nxt, buf ^ 1);
-      if (have_prev) issue_v(cur, sm + Lay::V, 8192);
+      if (have_prev) issue_v(cur, 0, sm + Lay::V, 8192);
       if (publish_now) publish(prev);
       io_stamp(2);
     }
@@ -437,7 +445,7 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
           tma_store_1d(img + kImgWQ + b * 16384 + 8192, kq + b * 16384 + 8192, 8192);
         bulk_commit();
         bulk_wait_read_all();
-        issue_v(cur, kq + 8192, 16384);
+        issue_v(cur, 0, kq + 8192, 16384);
       }
       io_stamp(4);
     }
@@ -558,98 +566,112 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
     __syncthreads();
 
     stamp(6);
-    // ---- W^T = K^T T_w^T and U~^T = V^T T_u^T, two 128-row halves each
-    if (tid == 0) {
-      if (!mbar_wait(&bar_v, ph)) {
-        s_abort = 1;
-      } else {
-        tc_fence_after();
-        const uint32_t idesc = idesc_bf16(128, 64, 1, 0);
-        const uint32_t kqa = smem_u32(kq);
-        // V's 64-column blocks: own buffer (fused) or the Q slots (split)
-        const uint32_t va = kFused ? smem_u32(sm + Lay::V) : kqa + 8192;
-        const uint32_t vblk = kFused ? 8192 : 16384;
-        const uint32_t tw = smem_u32(sm + Lay::TW), tu = smem_u32(sm + Lay::TU);
-        for (int hh = 0; hh < 2; ++hh) {
-          for (int s = 0; s < 4; ++s)
-            mma_bf16(tmem + hh * 64, smem_desc(kqa + hh * 32768 + s * 2048, 16384, 1024, kSwizzle128B),
-                     smem_desc(tw + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
-          for (int s = 0; s < 4; ++s)
-            mma_bf16(tmem + 128 + hh * 64,
-                     smem_desc(va + hh * 2 * vblk + s * 2048, vblk, 1024, kSwizzle128B),
-                     smem_desc(tu + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
-        }
-        mma_commit(&bar_bc);
+    // ---- W^T = K^T T_w^T and U~^T = V^T T_u^T: two 128-row halves of W^T
+    //      and of each 256-column block vh of V (dv = 512: a second pass
+    //      over the second block, once the first block's U~^T has left)
+    for (int vh = 0; vh * kDK < dv; ++vh) {
+      if (vh > 0 && tid == kPrepIO) {
+        bulk_wait_read_all();
+        issue_v(cur, vh, kFused ? sm + Lay::V : kq + 8192, kFused ? 8192 : 16384);
       }
-    }
-    __syncthreads();
-    if (s_abort) goto teardown;
-    if (!mbar_wait(&bar_bc, ph)) { flag_status(status, GDN_ERR_TIMEOUT); s_abort = 1; }
-    __syncthreads();
-    if (s_abort) goto teardown;
-    stamp(7);
-    tc_fence_after();
-    // W rows c over the K slots (K consumed); U~^T rows over V (consumed):
-    // fused, the V buffer in image layout, split, the Q slots
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const uint32_t c = 128 * hh + 32 * quarter + lane;   // d_k row of W^T / d_v row of U~^T
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {               // 0: W, 1: U~^T
-        uint32_t g[32];
-        tmem_ld32(tmem + lane_off + part * 128 + hh * 64 + 32 * hv, g);
-        tmem_ld_wait();
-        uint8_t* base;    // 128-byte rows from here, swizzled by row
-        uint32_t row;
-        if (part == 0) {
-          base = kq + (c >> 6) * 16384;
-          row = c & 63;
-        } else if (kFused) {
-          base = sm + Lay::V + hh * kImgHalf;
-          row = c & 127;
+      if (tid == 0) {
+        if (!mbar_wait(&bar_v, vph)) {
+          s_abort = 1;
         } else {
-          base = kq + (c >> 6) * 16384 + 8192;
-          row = c & 63;
+          tc_fence_after();
+          const uint32_t idesc = idesc_bf16(128, 64, 1, 0);
+          const uint32_t kqa = smem_u32(kq);
+          // V's 64-column blocks: own buffer (fused) or the Q slots (split)
+          const uint32_t va = kFused ? smem_u32(sm + Lay::V) : kqa + 8192;
+          const uint32_t vblk = kFused ? 8192 : 16384;
+          const uint32_t tw = smem_u32(sm + Lay::TW), tu = smem_u32(sm + Lay::TU);
+          for (int hh = 0; hh < 2; ++hh) {
+            if (vh == 0)
+              for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem + hh * 64, smem_desc(kqa + hh * 32768 + s * 2048, 16384, 1024, kSwizzle128B),
+                         smem_desc(tw + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
+            for (int s = 0; s < 4; ++s)
+              mma_bf16(tmem + 128 + hh * 64,
+                       smem_desc(va + hh * 2 * vblk + s * 2048, vblk, 1024, kSwizzle128B),
+                       smem_desc(tu + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
+          }
+          mma_commit(&bar_bc);
         }
+      }
+      vph ^= 1u;
+      __syncthreads();
+      if (s_abort) goto teardown;
+      if (!mbar_wait(&bar_bc, bcph)) { flag_status(status, GDN_ERR_TIMEOUT); s_abort = 1; }
+      bcph ^= 1u;
+      __syncthreads();
+      if (s_abort) goto teardown;
+      if (vh == 0) stamp(7);
+      tc_fence_after();
+      // W rows c over the K slots (K consumed); U~^T rows over V (consumed):
+      // fused, the V buffer in image layout, split, the Q slots
 #pragma unroll
-        for (int cq = 0; cq < 4; ++cq) {
-          const uint32_t w0 = pack_bf16(__uint_as_float(g[8 * cq]), __uint_as_float(g[8 * cq + 1]));
-          const uint32_t w1 = pack_bf16(__uint_as_float(g[8 * cq + 2]), __uint_as_float(g[8 * cq + 3]));
-          const uint32_t w2 = pack_bf16(__uint_as_float(g[8 * cq + 4]), __uint_as_float(g[8 * cq + 5]));
-          const uint32_t w3 = pack_bf16(__uint_as_float(g[8 * cq + 6]), __uint_as_float(g[8 * cq + 7]));
-          *reinterpret_cast<uint4*>(base + sw_chunk(row, 4 * hv + cq)) = make_uint4(w0, w1, w2, w3);
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t c = 128 * hh + 32 * quarter + lane;   // d_k row of W^T / d_v row of U~^T
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {               // 0: W, 1: U~^T
+          if (part == 0 && vh > 0) continue;
+          uint32_t g[32];
+          tmem_ld32(tmem + lane_off + part * 128 + hh * 64 + 32 * hv, g);
+          tmem_ld_wait();
+          uint8_t* base;    // 128-byte rows from here, swizzled by row
+          uint32_t row;
+          if (part == 0) {
+            base = kq + (c >> 6) * 16384;
+            row = c & 63;
+          } else if (kFused) {
+            base = sm + Lay::V + hh * kImgHalf;
+            row = c & 127;
+          } else {
+            base = kq + (c >> 6) * 16384 + 8192;
+            row = c & 63;
+          }
+#pragma unroll
+          for (int cq = 0; cq < 4; ++cq) {
+            const uint32_t w0 = pack_bf16(__uint_as_float(g[8 * cq]), __uint_as_float(g[8 * cq + 1]));
+            const uint32_t w1 = pack_bf16(__uint_as_float(g[8 * cq + 2]), __uint_as_float(g[8 * cq + 3]));
+            const uint32_t w2 = pack_bf16(__uint_as_float(g[8 * cq + 4]), __uint_as_float(g[8 * cq + 5]));
+            const uint32_t w3 = pack_bf16(__uint_as_float(g[8 * cq + 6]), __uint_as_float(g[8 * cq + 7]));
+            *reinterpret_cast<uint4*>(base + sw_chunk(row, 4 * hv + cq)) = make_uint4(w0, w1, w2, w3);
+          }
         }
       }
-    }
-    if (tid < kC) {
-      const float d = tid < L ? exp_fast(sG[L - 1] - sG[tid]) : 0.f;
-      if (kFused) {
-        for (int hh = 0; hh < 2; ++hh) {
-          float* blk = reinterpret_cast<float*>(sm + Lay::V + hh * kImgHalf + kImgDecay);
-          blk[tid] = d;
-          blk[64 + tid] = sG[tid];
+      if (tid < kC) {
+        const float d = tid < L ? exp_fast(sG[L - 1] - sG[tid]) : 0.f;
+        if (kFused) {
+          for (int hh = 0; hh < 2; ++hh) {
+            float* blk = reinterpret_cast<float*>(sm + Lay::V + hh * kImgHalf + kImgDecay);
+            blk[tid] = d;
+            blk[64 + tid] = sG[tid];
+          }
+        } else if (vh == 0) {
+          sDecay[tid] = d;
+          sDecay[64 + tid] = sG[tid];
         }
-      } else {
-        sDecay[tid] = d;
-        sDecay[64 + tid] = sG[tid];
       }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == kPrepIO) {
-      if (kFused) {
-        tma_store_1d(img + kImgWQ, kq, 65536);
-        tma_store_1d(img + kImgU0, sm + Lay::V, (uint32_t)(2 * kImgHalf));
-      } else {
-        for (int b = 0; b < 4; ++b) {
-          tma_store_1d(img + kImgWQ + b * 16384, kq + b * 16384, 8192);
-          tma_store_1d(img + kImgU0 + (b >> 1) * kImgHalf + (b & 1) * 8192, kq + b * 16384 + 8192, 8192);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      if (tid == kPrepIO) {
+        // U~^T slices 2 vh and 2 vh + 1 of the image
+        uint8_t* uimg = img + kImgU0 + 2 * vh * kImgHalf;
+        if (kFused) {
+          if (vh == 0) tma_store_1d(img + kImgWQ, kq, 65536);
+          tma_store_1d(uimg, sm + Lay::V, (uint32_t)(2 * kImgHalf));
+        } else {
+          for (int b = 0; b < 4; ++b) {
+            if (vh == 0) tma_store_1d(img + kImgWQ + b * 16384, kq + b * 16384, 8192);
+            tma_store_1d(uimg + (b >> 1) * kImgHalf + (b & 1) * 8192, kq + b * 16384 + 8192, 8192);
+          }
+          for (int hh = 0; hh < 2; ++hh) tma_store_1d(uimg + hh * kImgHalf + kImgDecay, sDecay, 512);
         }
-        for (int hh = 0; hh < 2; ++hh) tma_store_1d(img + kImgU0 + hh * kImgHalf + kImgDecay, sDecay, 512);
+        bulk_commit();
+        io_stamp(7);
       }
-      bulk_commit();
-      io_stamp(7);
     }
     stamp(8);
     prev = cur;
@@ -705,8 +727,8 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
                                            int32_t H, const uint8_t* __restrict__ scratch,
                                            const uint32_t* ready, unsigned* status,
                                            uint64_t* __restrict__ trace, int32_t trace_chunks,
-                                           int n, int h, int half) {
-  const int unit = (n * H + h) * 2 + half;
+                                           int32_t dv, int n, int h, int slice) {
+  const int unit = (n * H + h) * (dv / 128) + slice;
   const bool timed = trace && threadIdx.x == 0 && unit < kMaxTracedUnits;
   if (timed) trace[kUnitTimes + 3 * unit] = globaltimer_ns();
   const float* sD = reinterpret_cast<const float*>(sm + kS_UT + kImgDecay);   // d_r, then G_r
@@ -726,7 +748,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   const int64_t s_begin = map.seq_begin(n), s_end = map.seq_end(n);
   // optional phase timeline (test hook): thread 0 of unit (0, 0, 0) stamps
   // its SM cycle counter at 12 points of each of its first trace_chunks chunks
-  const bool tracing = trace && tid == 0 && n == 0 && h == 0 && half == 0;
+  const bool tracing = trace && tid == 0 && n == 0 && h == 0 && slice == 0;
   auto stamp = [&](int64_t it, int k) {
     if (tracing && it < trace_chunks) trace[it * 12 + k] = clock64();
   };
@@ -751,7 +773,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
 
   // master state: this thread's 128 columns of row iloc (fp32, registers)
   float S[128];
-  const size_t srow = (((size_t)n * H + h) * kDV + 128 * half + iloc) * kDK + 128 * colhalf;
+  const size_t srow = (((size_t)n * H + h) * dv + 128 * slice + iloc) * kDK + 128 * colhalf;
   if (S0) {
     const float4* p = reinterpret_cast<const float4*>(S0 + srow);
 #pragma unroll
@@ -780,7 +802,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   };
   store_S_operand();
 
-  auto img_of = [&](int64_t ci) { return scratch + (size_t)(ci * H + h) * kImgStride; };
+  auto img_of = [&](int64_t ci) { return scratch + (size_t)(ci * H + h) * img_stride(dv); };
   auto t0_of = [&](int64_t ci) { return (int32_t)(s_begin + (ci - cb) * kC); };
   auto flag_of = [&](int64_t ci) { return ready + ci * H + h; };
   auto issue_wq = [&](int64_t ci, int buf) {   // W and Q^ are adjacent in the image
@@ -797,10 +819,10 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   };
   auto issue_u = [&](int64_t ci) {    // this half's U~^T rows and the decay block
     mbar_arrive_expect_tx(&bar_u, (uint32_t)kImgHalf);
-    tma_load_1d(sm + kS_UT, img_of(ci) + kImgU0 + half * kImgHalf, (uint32_t)kImgHalf, &bar_u);
+    tma_load_1d(sm + kS_UT, img_of(ci) + kImgU0 + slice * kImgHalf, (uint32_t)kImgHalf, &bar_u);
   };
   auto warm_l2 = [&](int64_t ci) {    // the whole image of a later chunk (split form)
-    prefetch_l2(img_of(ci), (uint32_t)kImgStride);
+    prefetch_l2(img_of(ci), (uint32_t)img_stride(dv));
   };
   // Loads are issued by single threads of warps 1, 2 and 3 (thread 0 issues
   // the MMAs), so that each one's issue work fits in the time MMA-2 takes.
@@ -909,7 +931,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
       if (p < 0) break;
       const int r = p >> 4, c16 = p & 15;
       const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 256 + c16 * 16);
-      *reinterpret_cast<uint4*>(out + ((prev_t0 + r) * H + h) * kDV + 128 * half + 8 * c16) = v;
+      *reinterpret_cast<uint4*>(out + ((prev_t0 + r) * H + h) * dv + 128 * slice + 8 * c16) = v;
     }
   };
 
@@ -1135,26 +1157,28 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ alpha,
                const float* __restrict__ beta, SeqMap map, int32_t H,
                uint8_t* __restrict__ scratch, unsigned* status, uint64_t* __restrict__ trace,
-               int64_t n_items) {
+               int64_t n_items, int32_t dv) {
   extern __shared__ uint8_t smem_raw[];
   prep_role<false>(align_smem_1024(smem_raw), &tm_q, &tm_k, &tm_v, alpha, beta, map, H, scratch,
-                   nullptr, status, trace ? trace + kPrepTraceOffset : nullptr, trace, n_items,
+                   nullptr, status, dv, trace ? trace + kPrepTraceOffset : nullptr, trace, n_items,
                    blockIdx.x, gridDim.x);
 }
 
-// split form, kernel 2: one CTA per unit (blockIdx = sequence, head, half)
+// split form, kernel 2: one CTA per unit (blockIdx = sequence, head, 128-row
+// slice of S)
 __global__ void __launch_bounds__(kStateThreads, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restrict__ S0,
                 __nv_bfloat16* __restrict__ out, float* __restrict__ S_final, SeqMap map,
                 int32_t H, const uint8_t* __restrict__ scratch, unsigned* status,
-                uint64_t* __restrict__ trace, int32_t trace_chunks) {
+                uint64_t* __restrict__ trace, int32_t trace_chunks, int32_t dv) {
   extern __shared__ uint8_t smem_raw[];
   state_role<false>(align_smem_1024(smem_raw), &tm_k, S0, out, S_final, map, H, scratch, nullptr,
-                    status, trace, trace_chunks, blockIdx.x, blockIdx.y, blockIdx.z);
+                    status, trace, trace_chunks, dv, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
 // fused form: cooperative, one CTA per SM; CTAs [0, n_state) are the state
-// units (unit u = (sequence u / 2H, head (u / 2) % H, half u % 2)), the rest
+// units (with ns = dv / 128 slices of S per head, unit u = (sequence
+// u / (ns H), head (u / ns) % H, slice u % ns)), the rest
 // prep workers over all chunk positions in order; ready[] holds a flag per
 // (chunk, head)
 __global__ void __launch_bounds__(kStateThreads, 1)
@@ -1164,13 +1188,15 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const float* __restrict__ S0, __nv_bfloat16* __restrict__ out,
                 float* __restrict__ S_final, SeqMap map, int32_t H, uint8_t* __restrict__ scratch,
                 uint32_t* ready, unsigned* status, uint64_t* __restrict__ trace,
-                int32_t trace_chunks, int32_t n_state) {
+                int32_t trace_chunks, int32_t n_state, int32_t dv) {
   static_assert(kPrepThreads == kStateThreads, "one block shape for both roles");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align_smem_1024(smem_raw);
   if ((int32_t)blockIdx.x < n_state) {
     const int u = blockIdx.x;
-    state_role<true>(sm, &tm_kb, S0, out, S_final, map, H, scratch, ready, status, trace, trace_chunks, u / (2 * H), (u >> 1) % H, u & 1);
+    const int ns = dv / 128;
+    state_role<true>(sm, &tm_kb, S0, out, S_final, map, H, scratch, ready, status, trace,
+                     trace_chunks, dv, u / (ns * H), (u / ns) % H, u % ns);
   } else {
     int64_t positions = map.chunks_per_seq;
     if (map.cu_seqlens) {
@@ -1180,7 +1206,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         positions = c > positions ? c : positions;
       }
     }
-    prep_role<true>(sm, &tm_q, &tm_k, &tm_v, alpha, beta, map, H, scratch, ready, status,
+    prep_role<true>(sm, &tm_q, &tm_k, &tm_v, alpha, beta, map, H, scratch, ready, status, dv,
                     trace ? trace + kPrepTraceOffset : nullptr, trace, positions * map.N * H,
                     blockIdx.x - n_state, gridDim.x - n_state);
   }
@@ -1210,14 +1236,14 @@ EncodeFn encoder() {
   return fn;
 }
 
-// [T_total][H][256] bf16 viewed as (feature, head, token); box 64 x 1 x 64,
+// [T_total][H][D] bf16 viewed as (feature, head, token); box 64 x 1 x 64,
 // 128-byte swizzle; token rows past the end of the tensor read as zero.
-bool make_token_map(CUtensorMap* m, const void* base, int64_t T_total, int32_t H) {
+bool make_token_map(CUtensorMap* m, const void* base, int64_t T_total, int32_t H, int32_t D = kDK) {
   EncodeFn enc = encoder();
   if (!enc) return false;
   memset(m, 0, sizeof *m);
-  cuuint64_t dims[3] = {(cuuint64_t)kDK, (cuuint64_t)H, (cuuint64_t)(T_total > 0 ? T_total : 1)};
-  cuuint64_t strides[2] = {(cuuint64_t)kDK * 2, (cuuint64_t)H * kDK * 2};
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(T_total > 0 ? T_total : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
   cuuint32_t box[3] = {64, 1, 64};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
@@ -1286,27 +1312,29 @@ int32_t g_trace_chunks = 0;
 int32_t g_last_tc_form = -1;
 
 // operand images, then one ready flag per (chunk, head) for the fused form
-size_t prefill_tc_scratch_bytes(int64_t max_chunks, int32_t H) {
+size_t prefill_tc_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv) {
   const size_t items = (size_t)max_chunks * H;
-  return items * kImgStride + align_up(items * sizeof(uint32_t), 256);
+  return items * img_stride(dv) + align_up(items * sizeof(uint32_t), 256);
 }
 
 size_t prefill_tc_image_stride() { return kImgStride; }
 
 cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool prep_only) {
-  static_assert(kDK == 256 && kDV == 256, "image layouts assume 256 x 256 heads");
+  static_assert(kDK == 256, "image layouts assume dk = 256");
+  const int32_t dv = a.dv;
+  if (!supported_dv(dv)) return cudaErrorInvalidValue;
   const int64_t T_total = a.map.cu_seqlens ? a.map.T : (int64_t)a.map.N * a.map.T;
   CUtensorMap tq, tk, tv, tkb;
   if (!make_token_map(&tq, a.q, T_total, a.H) || !make_token_map(&tk, a.k, T_total, a.H) ||
-      !make_token_map(&tv, a.v, T_total, a.H) || !make_token_map_blocked(&tkb, a.k, T_total, a.H))
+      !make_token_map(&tv, a.v, T_total, a.H, dv) || !make_token_map_blocked(&tkb, a.k, T_total, a.H))
     return cudaErrorInvalidValue;
   DeviceFacts* f = device_facts();
   if (!f) return cudaErrorUnknown;
   cudaError_t e;
   uint8_t* scr = (uint8_t*)a.scratch;
   const int64_t items = a.max_chunks * a.H;
-  uint32_t* ready = (uint32_t*)(scr + (size_t)items * kImgStride);
-  const int64_t n_state = (int64_t)a.map.N * a.H * 2;
+  uint32_t* ready = (uint32_t*)(scr + (size_t)items * img_stride(dv));
+  const int64_t n_state = (int64_t)a.map.N * a.H * (dv / 128);
 
   if (!prep_only && a.allow_overlap && f->fused_ok && items > 0 &&
       n_state + kMinPrepWorkers <= f->sms) {
@@ -1324,7 +1352,7 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, tc_fused_kernel, tq, tk, tv, tkb, a.alpha, a.beta, a.S0,
                            (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr, ready, a.status,
-                           g_trace, g_trace_chunks, (int32_t)n_state);
+                           g_trace, g_trace_chunks, (int32_t)n_state, dv);
     if (e == cudaSuccess) {
       count_launches(1);
       g_last_tc_form = 1;
@@ -1340,15 +1368,15 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
     const int64_t slots = 2 * (int64_t)f->sms;
     const unsigned grid = (unsigned)(items < slots ? items : slots);
     tc_prep_kernel<<<grid, kPrepThreads, kPrepSmemSplit, stream>>>(
-        tq, tk, tv, a.alpha, a.beta, a.map, a.H, scr, a.status, g_trace, items);
+        tq, tk, tv, a.alpha, a.beta, a.map, a.H, scr, a.status, g_trace, items, dv);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (prep_only) return cudaSuccess;
   g_last_tc_form = 0;
-  tc_state_kernel<<<dim3((unsigned)a.map.N, (unsigned)a.H, 2), kStateThreads, kStateSmem,
-                    stream>>>(tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr,
-                              a.status, g_trace, g_trace_chunks);
+  tc_state_kernel<<<dim3((unsigned)a.map.N, (unsigned)a.H, (unsigned)(dv / 128)), kStateThreads,
+                    kStateSmem, stream>>>(tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map,
+                                          a.H, scr, a.status, g_trace, g_trace_chunks, dv);
   count_launches(1);
   return cudaGetLastError();
 }

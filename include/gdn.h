@@ -169,9 +169,9 @@ uint64_t gdn_kernel_launches(void);
 
 /*
  * gdn_prefill_path -- name of the kernel path gdn_prefill takes for an
- * io_dtype at dv = 256 ("simt-f32": CUDA-core fp32 FFMA; "tcgen05-bf16":
- * tensor-core MMAs with bf16 operands and fp32 accumulation).  At dv = 512
- * both dtypes take the CUDA-core path.  NULL for an unknown dtype.
+ * io_dtype ("simt-f32": CUDA-core fp32 FFMA; "tcgen05-bf16": tensor-core
+ * MMAs with bf16 operands and fp32 accumulation), at either dv.  NULL for an
+ * unknown dtype.
  */
 const char* gdn_prefill_path(int32_t io_dtype);
 

@@ -71,3 +71,44 @@ def test_decode_dv512_equals_single_token_prefill(gdn_lib):
     o_d = gdn_lib.decode_step(a["q"], a["k"], a["v"], a["alpha"], a["beta"], S)
     assert rel(o_d.cpu().numpy(), o_p[:, 0].cpu().numpy()) <= 1e-5
     assert rel(S.cpu().numpy(), s_p.cpu().numpy()) <= 1e-5
+
+
+def _last_form(gdn_lib):
+    import ctypes
+    f = gdn_lib.load().gdn_testing_last_prefill_form
+    f.restype = ctypes.c_int32
+    return int(f())
+
+
+def test_prefill_dv512_split_form(gdn_lib):
+    """40 sequences x 1 head x 4 slices of S leave too few SMs for the fused
+    form: the split form runs at dv = 512 and matches the oracle."""
+    rng = np.random.default_rng(75)
+    lens = [int(t) for t in rng.integers(1, 150, size=40)]
+    check_case(gdn_lib, PrefillCase("dv512 split", lens, H=1, dv=512, io_dtype=torch.bfloat16,
+                                    seed=75, varlen=True))
+    assert _last_form(gdn_lib) == 0
+
+
+def test_prefill_dv512_fused_matches_split_bitwise(gdn_lib):
+    """At dv = 512 the fused launch and the split one (which the no-allocation
+    entry point always takes) agree bit for bit."""
+    import ctypes
+    lens = [700, 64, 1, 900]
+    H, dv = 2, 512
+    case = PrefillCase("dv512 fused vs split", lens, H=H, dv=dv, io_dtype=torch.bfloat16, seed=76,
+                       varlen=True)
+    x = to_dev(gdn_inputs.make_prefill(case, device="cpu"))
+    out, Sf = run_gpu(gdn_lib, x)
+    assert _last_form(gdn_lib) == 1
+    f = gdn_lib.load().gdn_prefill_noalloc
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    f.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, vp]
+    out1, Sf1 = torch.empty_like(out), torch.empty_like(Sf)
+    rc = f(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), x["alpha"].data_ptr(),
+           x["beta"].data_ptr(), x["S0"].data_ptr(), x["cu_seqlens"].data_ptr(), out1.data_ptr(),
+           Sf1.data_ptr(), len(lens), sum(lens), H, 256, dv, 1,
+           torch.cuda.current_stream().cuda_stream)
+    assert rc == 0 and gdn_lib.device_status() == 0
+    assert _last_form(gdn_lib) == 0
+    assert torch.equal(out, out1) and torch.equal(Sf, Sf1)
