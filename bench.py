@@ -61,6 +61,20 @@ def decode_bytes(N, io_bytes=2, dv=DV):
     return N * H * (2 * dv * DK * 4 + (2 * DK + 2 * dv) * io_bytes + 8)
 
 
+def prepare_bytes(T_total, N, H=H, dk=DK, dv=DV, io_bytes=2, state=True):
+    """gdn_prepare: read the packed q|k|v projection and the two gate inputs,
+    write q, k, v, alpha, beta; carried convolution state in and out; conv
+    weights and per-head parameters once."""
+    C = H * (2 * dk + dv)
+    per_tok = 2 * C * io_bytes + 4 * H * 4
+    return T_total * per_tok + (2 * N * 3 * C * io_bytes if state else 0) + C * 16 + 2 * H * 4
+
+
+def norm_gate_bytes(rows, dv=DV, io_bytes=2):
+    """gdn_output_norm_gate: read o and g, write y, per (token, head) row."""
+    return rows * dv * io_bytes * 3 + dv * 4
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -351,6 +365,79 @@ def run_ours(args, rank, world, local_rank, dist):
     p5_ms = max_over_ranks(ev0.elapsed_time(ev1) / p5_steps)
     del x5, out5, sf5
 
+    # ---- the layer steps around the recurrence on the 8K workload
+    # (gdn_prepare: conv + SiLU, q/k L2 norm, gates; gdn_output_norm_gate:
+    # Eq. 20's gated RMSNorm) and one decode step's gdn_prepare_decode_step
+    lcase = gdn_inputs.layer_8k()
+    lx = gdn_inputs.make_layer(lcase, device=dev)
+    lstate = torch.empty_like(lx["conv_state"])
+    lstep = lambda: gdn.prepare(lx["qkv"], lx["conv_w"], lx["a_raw"], lx["b_raw"], lx["A_log"],
+                                lx["dt_bias"], lcase.H, conv_state_in=lx["conv_state"],
+                                conv_state_out=lstate)
+    lo = torch.randn(lx["g"].shape, device=dev).to(lx["g"].dtype)
+    ly = torch.empty_like(lo)
+    gstep = lambda: gdn.output_norm_gate(lo, lx["g"], lx["norm_w"], 1e-5, "silu", y=ly)
+
+    def time_it(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        c0 = gdn.kernel_launches()
+        ev0.record(stream)
+        for _ in range(n):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        return ev0.elapsed_time(ev1) / n, int(gdn.kernel_launches() - c0) // n
+
+    prep_ms, prep_launch = time_it(lstep, 10)
+    ng_ms, ng_launch = time_it(gstep, 10)
+    assert gdn.device_status() == 0
+    prep_b = prepare_bytes(lcase.total_tokens, len(lcase.lengths))
+    ng_b = norm_gate_bytes(lcase.total_tokens * lcase.H)
+    del lx, lstate, lo, ly
+    dl = gdn_inputs.layer_decode_256()
+    dl_steps = 200
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(dl.seed)
+    dqkv = torch.randn((dl_steps, len(dl.lengths), dl.channels), generator=gen,
+                       device=dev).to(dl.io_dtype)
+    dlx = gdn_inputs.make_layer(dl, device=dev)
+    dl_out = gdn.prepare_decode_step(dlx["qkv"], dlx["conv_w"], dlx["a_raw"], dlx["b_raw"],
+                                     dlx["A_log"], dlx["dt_bias"], dlx["conv_state"], dl.H)
+    dl_i = [0]
+
+    def dstep():
+        gdn.prepare_decode_step(dqkv[dl_i[0] % dl_steps], dlx["conv_w"], dlx["a_raw"],
+                                dlx["b_raw"], dlx["A_log"], dlx["dt_bias"], dlx["conv_state"],
+                                dl.H, out=dl_out)
+        dl_i[0] += 1
+
+    # a step this small is bound by the host's call rate, so the 200 steps are
+    # replayed from a CUDA graph, as a serving loop would run them
+    for _ in range(3):
+        dstep()
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            for _ in range(dl_steps):
+                dstep()
+    stream.wait_stream(cap)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    graph.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    pd_ms = ev0.elapsed_time(ev1) / dl_steps
+    assert gdn.device_status() == 0
+    del graph
+    pd_b = prepare_bytes(len(dl.lengths), len(dl.lengths))
+    del dqkv, dlx, dl_out
+
     res = None
     if rank == 0:
         clocks = sampler.summary()
@@ -408,6 +495,27 @@ def run_ours(args, rank, world, local_rank, dist):
                             "counted_tflops": round(prefill_flops(pcase5.lengths, dv=512)
                                                     / (p5_ms * 1e-3) / 1e12, 3)},
             },
+            "layer_steps": {
+                "prepare": {"workload": lcase.name + " (gdn_prepare)",
+                            "ms_per_step": round(prep_ms, 4),
+                            "value": round(prep_b / (prep_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                            "algorithmic_bytes_per_launch": prep_b,
+                            "frac_of_hbm": round(prep_b / (prep_ms * 1e-3) / 1e9
+                                                 / peaks["hbm_gbs"], 4),
+                            "mtok_per_s": round(lcase.total_tokens / (prep_ms * 1e-3) / 1e6, 2),
+                            "launches_per_step": prep_launch},
+                "output_norm_gate": {"workload": lcase.name + " (gdn_output_norm_gate)",
+                                     "ms_per_step": round(ng_ms, 4),
+                                     "value": round(ng_b / (ng_ms * 1e-3) / 1e9, 2),
+                                     "unit": "GB/s", "algorithmic_bytes_per_launch": ng_b,
+                                     "frac_of_hbm": round(ng_b / (ng_ms * 1e-3) / 1e9
+                                                          / peaks["hbm_gbs"], 4),
+                                     "launches_per_step": ng_launch},
+                "prepare_decode_step": {"workload": dl.name + f" x{dl_steps} steps (CUDA graph)",
+                                        "ms_per_step": round(pd_ms, 5),
+                                        "value": round(pd_b / (pd_ms * 1e-3) / 1e9, 2),
+                                        "unit": "GB/s", "algorithmic_bytes_per_launch": pd_b},
+            },
             "clocks": clocks,
             "decode": {
                 "workload": dcase.name,
@@ -446,7 +554,8 @@ def cpu_baseline(args, sample_tokens=2048):
 
 def run_profile(args):
     """Only the library's kernels of one family, for a profiler: W warm-up
-    then K steps of the 8K prefill workload, or of the 256-sequence decode."""
+    then K steps of the 8K prefill workload, of the 256-sequence decode, or
+    of the 8K layer steps around the recurrence."""
     import torch
 
     import gdn_inputs
@@ -459,6 +568,16 @@ def run_profile(args):
         for _ in range(args.warmup + args.steps):
             gdn.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"], out=out,
                         S_final=sf)
+    elif args.profile == "layer":
+        # gdn_prepare then gdn_output_norm_gate on the 8K layer inputs, per step
+        lc = gdn_inputs.layer_8k()
+        lx = gdn_inputs.make_layer(lc, device=dev)
+        st = torch.empty_like(lx["conv_state"])
+        o = torch.randn(lx["g"].shape, device=dev).to(lx["g"].dtype)
+        for _ in range(args.warmup + args.steps):
+            gdn.prepare(lx["qkv"], lx["conv_w"], lx["a_raw"], lx["b_raw"], lx["A_log"],
+                        lx["dt_bias"], lc.H, conv_state_in=lx["conv_state"], conv_state_out=st)
+            gdn.output_norm_gate(o, lx["g"], lx["norm_w"], 1e-5, "silu")
     else:
         case = gdn_inputs.decode_256x1000()
         d = gdn_inputs.make_decode(case, device=dev, steps=args.warmup + args.steps)
@@ -513,7 +632,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "layer"], default=None,
                     help="run only W + K steps of one kernel family (for ncu captures); "
                          "prints no benchmark line")
     args = ap.parse_args()

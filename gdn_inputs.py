@@ -171,3 +171,80 @@ def prefill_varlen16() -> PrefillCase:
     lengths = varlen_lengths(16, 1024, 65536, seed=4)
     return PrefillCase("varlen prefill N=16 len~U[1024,65536] H=6 d=256 bf16", lengths,
                        seed=4, varlen=True)
+
+
+# ---------------------------------------------------------------------------
+# Inputs of the layer steps around the recurrence (Appendix A.3: short
+# convolution + SiLU, gates, Eq. 20's gated read-out).  Parameters are drawn
+# like a fresh initialisation of the layer (no trained weights exist here):
+#   qkv (the packed q|k|v projection) ~ N(0, 1)       [.., C], C = H (2 dk + dv)
+#   conv_w ~ U(-0.5, 0.5) (1/sqrt(fan-in 4))          [C, 4]
+#   a_raw, b_raw ~ N(0, 1)                            [.., H]
+#   A_log = log U(1, 16)                              [H]
+#   dt_bias ~ U(-5, -2)                               [H]
+#   conv_state_in ~ N(0, 1) or omitted                [N, 3, C]
+#   g (the W_G projection) ~ N(0, 1)                  [.., H, dv]
+#   norm_w = 1 + 0.1 N(0, 1)                          [dv]
+# drawn in that order from one CPU generator seeded with ``seed``, then qkv,
+# the states and g are cast to the I/O dtype.  Varlen lengths are the
+# caller's.
+
+
+@dataclass
+class LayerCase:
+    name: str
+    lengths: list
+    H: int = H_PAGES
+    dk: int = D_PAGES
+    dv: int = D_PAGES
+    io_dtype: torch.dtype = torch.bfloat16
+    seed: int = 0
+    varlen: bool = False
+    carry_state: bool = True      # conv_state_in given (else zero history)
+
+    @property
+    def total_tokens(self) -> int:
+        return int(sum(self.lengths))
+
+    @property
+    def channels(self) -> int:
+        return self.H * (2 * self.dk + self.dv)
+
+
+def make_layer(case: LayerCase, device="cpu") -> dict:
+    g = _gen("cpu", case.seed)
+    N, H, dv, C = len(case.lengths), case.H, case.dv, case.channels
+    if case.varlen:
+        lead = (case.total_tokens,)
+    else:
+        assert len(set(case.lengths)) == 1, "dense batches share one length"
+        lead = (N, case.lengths[0])
+    qkv = _randn(lead + (C,), g, "cpu")
+    conv_w = torch.rand((C, 4), generator=g) - 0.5
+    a_raw = _randn(lead + (H,), g, "cpu")
+    b_raw = _randn(lead + (H,), g, "cpu")
+    A_log = torch.log(1.0 + 15.0 * torch.rand((H,), generator=g))
+    dt_bias = -5.0 + 3.0 * torch.rand((H,), generator=g)
+    state = _randn((N, 3, C), g, "cpu") if case.carry_state else None
+    gate = _randn(lead + (H, dv), g, "cpu")
+    norm_w = 1.0 + 0.1 * _randn((dv,), g, "cpu")
+    io = case.io_dtype
+    out = dict(qkv=qkv.to(io), conv_w=conv_w, a_raw=a_raw, b_raw=b_raw, A_log=A_log,
+               dt_bias=dt_bias, conv_state=None if state is None else state.to(io),
+               g=gate.to(io), norm_w=norm_w, cu_seqlens=None)
+    if case.varlen:
+        cu = [0]
+        for L in case.lengths:
+            cu.append(cu[-1] + L)
+        out["cu_seqlens"] = torch.tensor(cu, dtype=torch.int32)
+    return {k: (v.to(device).contiguous() if isinstance(v, torch.Tensor) else v)
+            for k, v in out.items()}
+
+
+def layer_8k() -> LayerCase:
+    return LayerCase("layer steps B=4 T=8192 H=6 d=256 bf16", [8192] * 4, seed=7)
+
+
+def layer_decode_256() -> LayerCase:
+    """One decode step's layer inputs for 256 sequences (as 256 one-token sequences)."""
+    return LayerCase("layer steps decode N=256 H=6 d=256 bf16", [1] * 256, seed=8, varlen=True)

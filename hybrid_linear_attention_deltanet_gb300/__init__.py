@@ -8,6 +8,8 @@ raise when the compiled library is missing.
 
     out, S_final = prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None)
     out = decode_step(q, k, v, alpha, beta, S)          # S updated in place
+    x = prepare(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, heads)   # -> q, k, v, alpha, beta
+    y = output_norm_gate(out, g, w)                     # Eq. 20 read-out
 
 Recurrence (Appendix A.3, Eq. 16-19 of "Long-Context Aware Upcycling"):
 S_t = alpha_t S_{t-1}(I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
@@ -63,6 +65,13 @@ def load():
     lib.gdn_kernel_launches.restype = ctypes.c_uint64
     lib.gdn_prefill_path.argtypes = [ctypes.c_int32]
     lib.gdn_prefill_path.restype = ctypes.c_char_p
+    lib.gdn_prepare.argtypes = [vp] * 14 + [i32, i64, i32, i32, i32, i32, vp]
+    lib.gdn_prepare.restype = ctypes.c_int
+    lib.gdn_prepare_decode_step.argtypes = [vp] * 12 + [i32, i32, i32, i32, i32, vp]
+    lib.gdn_prepare_decode_step.restype = ctypes.c_int
+    lib.gdn_output_norm_gate.argtypes = [vp, vp, vp, ctypes.c_float, i32, vp, i64, i32, i32, i32,
+                                         vp]
+    lib.gdn_output_norm_gate.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -188,6 +197,132 @@ def decode_step(q, k, v, alpha, beta, S, out=None, stream=None):
     if rc != 0:
         raise GDNError("gdn_decode_step", rc)
     return out
+
+
+GATE_ACT = {"silu": 0, "sigmoid": 1}
+
+
+def prepare(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, heads, dk=256, dv=256, cu_seqlens=None,
+            conv_state_in=None, conv_state_out=None, stream=None):
+    """Pre-recurrence steps (``gdn_prepare``): short conv + SiLU on the packed
+    q|k|v projection, q/k L2 normalisation, decay and write strength.
+
+    qkv [B, T, C] or [T, C] (C = H*(2*dk + dv)); conv_w [C, 4] fp32;
+    a_raw, b_raw [B, T, H] / [T, H] fp32; A_log, dt_bias [H] fp32;
+    conv_state_in / conv_state_out [N, 3, C] in qkv's dtype (or None).
+    Returns dict q, k [.., H, dk], v [.., H, dv], alpha, beta [.., H] ready
+    for :func:`prefill`.
+    """
+    lib = load()
+    dev, io = qkv.device, qkv.dtype
+    _io_code(io)
+    H = heads
+    C = H * (2 * dk + dv)
+    _check(qkv, "qkv", io, dev)
+    if qkv.shape[-1] != C or qkv.dim() not in (2, 3):
+        raise ValueError(f"qkv must be [B, T, {C}] or [T, {C}]")
+    lead = tuple(qkv.shape[:-1])
+    for name, t in (("a_raw", a_raw), ("b_raw", b_raw)):
+        _check(t, name, torch.float32, dev)
+        if tuple(t.shape) != lead + (H,):
+            raise ValueError(f"{name} must be {list(lead + (H,))}")
+    _check(conv_w, "conv_w", torch.float32, dev)
+    if tuple(conv_w.shape) != (C, 4):
+        raise ValueError(f"conv_w must be [{C}, 4]")
+    for name, t in (("A_log", A_log), ("dt_bias", dt_bias)):
+        _check(t, name, torch.float32, dev)
+        if tuple(t.shape) != (H,):
+            raise ValueError(f"{name} must be [{H}]")
+    if cu_seqlens is None:
+        B, T = (qkv.shape[0], qkv.shape[1]) if qkv.dim() == 3 else (1, qkv.shape[0])
+        N, seqlen = B, T
+    else:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        if qkv.dim() == 3 and qkv.shape[0] != 1:
+            raise ValueError("varlen input must have batch axis 1")
+        N, seqlen = cu_seqlens.numel() - 1, qkv.shape[-2]
+    for name, t in (("conv_state_in", conv_state_in), ("conv_state_out", conv_state_out)):
+        if t is not None:
+            _check(t, name, io, dev)
+            if tuple(t.shape) != (N, 3, C):
+                raise ValueError(f"{name} must be [{N}, 3, {C}]")
+    out = dict(q=torch.empty(lead + (H, dk), dtype=io, device=dev),
+               k=torch.empty(lead + (H, dk), dtype=io, device=dev),
+               v=torch.empty(lead + (H, dv), dtype=io, device=dev),
+               alpha=torch.empty(lead + (H,), dtype=torch.float32, device=dev),
+               beta=torch.empty(lead + (H,), dtype=torch.float32, device=dev))
+    with torch.cuda.device(dev):
+        rc = lib.gdn_prepare(_ptr(qkv), _ptr(conv_w), _ptr(a_raw), _ptr(b_raw), _ptr(A_log),
+                             _ptr(dt_bias), _ptr(cu_seqlens), _ptr(conv_state_in),
+                             _ptr(conv_state_out), _ptr(out["q"]), _ptr(out["k"]),
+                             _ptr(out["v"]), _ptr(out["alpha"]), _ptr(out["beta"]), N, seqlen,
+                             H, dk, dv, _io_code(io), _stream_handle(stream))
+    if rc != 0:
+        raise GDNError("gdn_prepare", rc)
+    return out
+
+
+def prepare_decode_step(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, conv_state, heads, dk=256,
+                        dv=256, out=None, stream=None):
+    """``gdn_prepare_decode_step``: one token per sequence, qkv [N, C],
+    a_raw / b_raw [N, H], conv_state [N, 3, C] updated in place.  Returns
+    dict q, k [N, H, dk], v [N, H, dv], alpha, beta [N, H] (or fills ``out``)."""
+    lib = load()
+    dev, io = qkv.device, qkv.dtype
+    _io_code(io)
+    H = heads
+    C = H * (2 * dk + dv)
+    _check(qkv, "qkv", io, dev)
+    if qkv.dim() != 2 or qkv.shape[1] != C:
+        raise ValueError(f"qkv must be [N, {C}]")
+    N = qkv.shape[0]
+    _check(conv_state, "conv_state", io, dev)
+    _check(conv_w, "conv_w", torch.float32, dev)
+    for name, t in (("a_raw", a_raw), ("b_raw", b_raw)):
+        _check(t, name, torch.float32, dev)
+    if (tuple(conv_state.shape) != (N, 3, C) or tuple(conv_w.shape) != (C, 4)
+            or tuple(a_raw.shape) != (N, H) or tuple(b_raw.shape) != (N, H)):
+        raise ValueError("shape mismatch in prepare_decode_step arguments")
+    if out is None:
+        out = dict(q=torch.empty((N, H, dk), dtype=io, device=dev),
+                   k=torch.empty((N, H, dk), dtype=io, device=dev),
+                   v=torch.empty((N, H, dv), dtype=io, device=dev),
+                   alpha=torch.empty((N, H), dtype=torch.float32, device=dev),
+                   beta=torch.empty((N, H), dtype=torch.float32, device=dev))
+    with torch.cuda.device(dev):
+        rc = lib.gdn_prepare_decode_step(
+            _ptr(qkv), _ptr(conv_w), _ptr(a_raw), _ptr(b_raw), _ptr(A_log), _ptr(dt_bias),
+            _ptr(conv_state), _ptr(out["q"]), _ptr(out["k"]), _ptr(out["v"]), _ptr(out["alpha"]),
+            _ptr(out["beta"]), N, H, dk, dv, _io_code(io), _stream_handle(stream))
+    if rc != 0:
+        raise GDNError("gdn_prepare_decode_step", rc)
+    return out
+
+
+def output_norm_gate(o, g, w, eps=1e-5, act="silu", y=None, stream=None):
+    """Eq. 20 read-out (``gdn_output_norm_gate``): o / rms(o) * w * act(g)
+    per (token, head) over dv.  o, g [.., H, dv] (same dtype); w [dv] fp32.
+    ``y`` defaults to a new tensor; pass ``y=o`` to normalise in place."""
+    lib = load()
+    dev, io = o.device, o.dtype
+    _io_code(io)
+    _check(o, "o", io, dev)
+    _check(g, "g", io, dev)
+    _check(w, "w", torch.float32, dev)
+    if g.shape != o.shape or o.dim() < 2 or tuple(w.shape) != (o.shape[-1],):
+        raise ValueError("o and g must share [.., H, dv]; w must be [dv]")
+    H, dv = o.shape[-2], o.shape[-1]
+    tokens = o.numel() // (H * dv)
+    if y is None:
+        y = torch.empty_like(o)
+    else:
+        _check(y, "y", io, dev)
+    with torch.cuda.device(dev):
+        rc = lib.gdn_output_norm_gate(_ptr(o), _ptr(g), _ptr(w), float(eps), GATE_ACT[act], _ptr(y),
+                                      tokens, H, dv, _io_code(io), _stream_handle(stream))
+    if rc != 0:
+        raise GDNError("gdn_output_norm_gate", rc)
+    return y
 
 
 def device_status(stream=None) -> int:

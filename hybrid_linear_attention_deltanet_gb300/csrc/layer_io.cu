@@ -1,0 +1,597 @@
+// The steps of a Gated DeltaNet layer on either side of the recurrence
+// ("Long-Context Aware Upcycling", Appendix A.3):
+//
+//  * before it (the paragraph after Table 8 and the text under Eq. 16-21):
+//    a short causal depthwise convolution of width 4 + SiLU on q, k and v,
+//    L2 normalisation of q and k per head, the decay
+//    alpha = exp(-exp(A_log) * softplus(W_alpha x + Delta_bias)) (Eq. 16's
+//    e^{g_t}) and the write strength beta = sigmoid(W_beta x);
+//  * after it (Eq. 20): the read-out o_t RMS-normalised per head, times a
+//    learned weight and an activated gate computed from W_G x_t.
+//
+// The projections themselves (W_Q, W_K, W_V, W_alpha, W_beta, W_G, W_O) are
+// plain GEMMs and stay outside.  Every kernel here is an HBM stream: one warp
+// owns 256 channels of one token row (8 per lane, one 16-byte vector at bf16)
+// so that each global access is a fully coalesced 512 B (bf16) or 1 KiB
+// (fp32) row piece, and the per-head reductions are warp shuffles.
+//
+// Layouts and argument contracts are those of include/gdn.h.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kTaps = 4;            // short convolution width (Table 8's paragraph)
+constexpr int kHist = kTaps - 1;    // inputs carried across calls per channel
+constexpr int kSeg = 256;           // channels per warp unit (one q/k head)
+constexpr int kTile = 64;           // tokens one warp walks in the prefill form
+// tokens whose loads one lane keeps in flight together (16 B each at bf16)
+template <typename T> __host__ __device__ constexpr int group_of() { return sizeof(T) == 2 ? 4 : 2; }
+constexpr int kWarpsPerCta = 8;
+constexpr float kL2Eps = 1e-6f;
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// 8 consecutive elements <-> 8 floats.  bf16 widens exactly (a shift); the
+// narrowing rounds to nearest even.
+struct Raw8 {
+  uint4 a, b;  // bf16 uses a only
+};
+
+__device__ __forceinline__ Raw8 load8(const __nv_bfloat16* p) {
+  Raw8 r;
+  r.a = __ldcs(reinterpret_cast<const uint4*>(p));
+  r.b = make_uint4(0, 0, 0, 0);
+  return r;
+}
+__device__ __forceinline__ Raw8 load8(const float* p) {
+  Raw8 r;
+  r.a = __ldcs(reinterpret_cast<const uint4*>(p));
+  r.b = __ldcs(reinterpret_cast<const uint4*>(p) + 1);
+  return r;
+}
+__device__ __forceinline__ Raw8 load8_cached(const __nv_bfloat16* p) {
+  Raw8 r;
+  r.a = __ldg(reinterpret_cast<const uint4*>(p));
+  r.b = make_uint4(0, 0, 0, 0);
+  return r;
+}
+__device__ __forceinline__ Raw8 load8_cached(const float* p) {
+  Raw8 r;
+  r.a = __ldg(reinterpret_cast<const uint4*>(p));
+  r.b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <typename T>
+__device__ __forceinline__ void widen8(const Raw8& r, float (&f)[8]);
+template <>
+__device__ __forceinline__ void widen8<__nv_bfloat16>(const Raw8& r, float (&f)[8]) {
+  const uint32_t w[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = bf16_lo(w[i]);
+    f[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+template <>
+__device__ __forceinline__ void widen8<float>(const Raw8& r, float (&f)[8]) {
+  const uint32_t w[8] = {r.a.x, r.a.y, r.a.z, r.a.w, r.b.x, r.b.y, r.b.z, r.b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(w[i]);
+}
+
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+// Elementwise activations of the streams use the fast exponential and divide
+// intrinsics (a few ulp, far inside the fp32 output tolerance); at e^-x = inf
+// the quotient is 0, the correct limit.  The per-head gates use expf/log1pf.
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
+// log(1 + e^x); above 20 the correction e^-x is below fp32 resolution
+__device__ __forceinline__ float softplusf_(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+
+// Conv taps of 8 channels, tap-major in registers: w[j][i] for channel c0 + i.
+__device__ __forceinline__ void load_taps(const float* __restrict__ conv_w, int64_t c0,
+                                          float (&w)[kTaps][8]) {
+  const float4* p = reinterpret_cast<const float4*>(conv_w + c0 * kTaps);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 t = __ldg(p + i);  // channel c0 + i: taps 0..3
+    w[0][i] = t.x; w[1][i] = t.y; w[2][i] = t.z; w[3][i] = t.w;
+  }
+}
+
+// The three inputs before a sequence's first token: its carried state, or
+// zeros.  kNC: the state is read-only for the whole launch (it may then take
+// the non-coherent path); the in-place decode form reads it coherently.
+template <typename T, bool kNC>
+__device__ __forceinline__ void history(const T* state_in, int64_t n, int64_t C, int64_t c0,
+                                        float (&win)[kHist][8]) {
+#pragma unroll
+  for (int j = 0; j < kHist; ++j) {
+    if (state_in) {
+      const T* p = state_in + (n * kHist + j) * C + c0;
+      widen8<T>(kNC ? load8_cached(p) : load8(p), win[j]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) win[j][i] = 0.f;
+    }
+  }
+}
+
+// One token of one 256-channel segment: conv + SiLU (+ L2 norm over the
+// segment when it is a q or k head), then the window shifts in x.
+__device__ __forceinline__ void conv_token(const float (&w)[kTaps][8], float (&win)[kHist][8],
+                                           const float (&x)[8], bool l2, float (&y)[8]) {
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float acc = w[0][i] * win[0][i];
+    acc = fmaf(w[1][i], win[1][i], acc);
+    acc = fmaf(w[2][i], win[2][i], acc);
+    acc = fmaf(w[3][i], x[i], acc);
+    y[i] = silu_fast(acc);
+    ss = fmaf(y[i], y[i], ss);
+    win[0][i] = win[1][i];
+    win[1][i] = win[2][i];
+    win[2][i] = x[i];
+  }
+  if (l2) {  // warp-uniform branch: the segment is one q or k head
+    const float r = rsqrtf(warp_sum(ss) + kL2Eps);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] *= r;
+  }
+}
+
+struct PrepareArgs {
+  const void* qkv;          // [T_total, C] io dtype
+  const float* conv_w;      // [C, 4]
+  const float* a_raw;       // [T_total, H]
+  const float* b_raw;       // [T_total, H]
+  const float* A_log;       // [H]
+  const float* dt_bias;     // [H]
+  const void* state_in;     // [N, 3, C] io dtype or null
+  void* state_out;          // [N, 3, C] io dtype or null
+  void* q; void* k; void* v;
+  float* alpha; float* beta;
+  const int32_t* cu;        // [N + 1] or null (dense)
+  int32_t N;
+  int64_t T;                // dense: tokens per sequence; varlen: T_total
+  int64_t T_total;
+  int32_t H, dk, dv;
+  int64_t n_tiles;
+  int32_t n_seg;            // C / 256
+  unsigned* status;         // device status word (malformed cu_seqlens)
+};
+
+struct Seqs {
+  const int32_t* cu;
+  int64_t T;
+  __device__ __forceinline__ int64_t begin(int64_t n) const { return cu ? (int64_t)cu[n] : n * T; }
+  __device__ __forceinline__ int64_t end(int64_t n) const {
+    return cu ? (int64_t)cu[n + 1] : (n + 1) * T;
+  }
+  // sequence holding token t (the last n with begin(n) <= t, skipping empties)
+  __device__ __forceinline__ int64_t find(int64_t t, int32_t N) const {
+    if (!cu) return t / T;
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((int64_t)cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  }
+};
+
+__device__ __forceinline__ void gates_one(const PrepareArgs& a, int64_t idx) {
+  const int h = (int)(idx % a.H);
+  const float decay_rate = expf(__ldg(a.A_log + h));
+  const float g = -decay_rate * softplusf_(__ldcs(a.a_raw + idx) + __ldg(a.dt_bias + h));
+  a.alpha[idx] = expf(g);
+  a.beta[idx] = sigmoidf_(__ldcs(a.b_raw + idx));
+}
+
+// Warp units: for each tile of kTile tokens, n_seg channel segments and one
+// gate unit; then one unit per sequence that copies the carried state of an
+// empty sequence through.
+// At most 128 registers a thread, so that two CTAs (16 warps, each with a
+// group of tokens in flight while it computes the previous one) share an SM.
+template <typename T>
+__global__ void __launch_bounds__(kWarpsPerCta * 32, 2)
+prepare_kernel(PrepareArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t unit = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t C = (int64_t)a.H * (2 * a.dk + a.dv);
+  const int64_t per_tile = a.n_seg + 1;
+  const Seqs seqs{a.cu, a.T};
+  const T* state_in = static_cast<const T*>(a.state_in);
+  T* state_out = static_cast<T*>(a.state_out);
+
+  if (unit >= a.n_tiles * per_tile) {  // per-sequence units
+    const int64_t n = unit - a.n_tiles * per_tile;
+    if (n >= a.N) return;
+    if (a.cu && lane == 0 &&
+        (a.cu[n + 1] < a.cu[n] || (n == 0 && a.cu[0] != 0) ||
+         (n == a.N - 1 && (int64_t)a.cu[a.N] != a.T_total)))
+      flag_status(a.status, GDN_ERR_BAD_SEQLENS);
+    if (!state_out || seqs.end(n) > seqs.begin(n)) return;   // only empty sequences copy
+    for (int64_t e = lane * 8; e < kHist * C; e += 32 * 8) {
+      float f[8];
+      if (state_in) widen8<T>(load8_cached(state_in + n * kHist * C + e), f);
+      else for (int i = 0; i < 8; ++i) f[i] = 0.f;
+      store8(state_out + n * kHist * C + e, f);
+    }
+    return;
+  }
+  const int64_t tile = unit / per_tile;
+  const int seg = (int)(unit % per_tile);
+  const int64_t t0 = tile * kTile;
+  const int64_t t1 = min(t0 + (int64_t)kTile, a.T_total);
+
+  if (seg == a.n_seg) {  // decay and write strength of the tile's tokens
+    for (int64_t idx = t0 * a.H + lane; idx < t1 * a.H; idx += 32) gates_one(a, idx);
+    return;
+  }
+
+  const int64_t c0 = (int64_t)seg * kSeg + lane * 8;
+  const bool l2 = seg < 2 * a.H * a.dk / kSeg;   // q and k heads
+  T* dst;
+  int64_t dst_stride, dst_c;
+  if (c0 < (int64_t)a.H * a.dk) {
+    dst = static_cast<T*>(a.q); dst_stride = (int64_t)a.H * a.dk; dst_c = c0;
+  } else if (c0 < 2 * (int64_t)a.H * a.dk) {
+    dst = static_cast<T*>(a.k); dst_stride = (int64_t)a.H * a.dk; dst_c = c0 - (int64_t)a.H * a.dk;
+  } else {
+    dst = static_cast<T*>(a.v); dst_stride = (int64_t)a.H * a.dv;
+    dst_c = c0 - 2 * (int64_t)a.H * a.dk;
+  }
+  float w[kTaps][8];
+  load_taps(a.conv_w, c0, w);
+  const T* x = static_cast<const T*>(a.qkv);
+
+  // window before t0: inputs of the same sequence, or the slots of its
+  // carried history that precede the sequence start (slot p - sb + 3)
+  int64_t n = seqs.find(t0, a.N);
+  int64_t sb = seqs.begin(n), se = seqs.end(n);
+  float win[kHist][8];
+#pragma unroll
+  for (int j = 0; j < kHist; ++j) {
+    const int64_t p = t0 - kHist + j;
+    if (p >= sb) {
+      widen8<T>(load8_cached(x + p * C + c0), win[j]);
+    } else if (state_in) {
+      widen8<T>(load8_cached(state_in + (n * kHist + (p - sb + kHist)) * C + c0), win[j]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) win[j][i] = 0.f;
+    }
+  }
+
+  // Ping-pong over groups of kGroup tokens: the next group's loads are in
+  // flight while the current group computes.
+  constexpr int kGroup = group_of<T>();
+  Raw8 ga[kGroup], gb[kGroup];
+  auto load_group = [&](Raw8 (&r)[kGroup], int64_t tg) {
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i)
+      if (tg + i < t1) r[i] = load8(x + (tg + i) * C + c0);
+  };
+  auto run_group = [&](const Raw8 (&r)[kGroup], int64_t tg) {
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) {
+      const int64_t t = tg + i;
+      if (t >= t1) break;
+      if (t >= se && n + 1 < a.N) {  // a new sequence starts here (skipping empty ones)
+        do { ++n; } while (n + 1 < a.N && seqs.end(n) <= t);
+        sb = seqs.begin(n);
+        se = seqs.end(n);
+        history<T, true>(state_in, n, C, c0, win);
+      }
+      float xf[8], y[8];
+      widen8<T>(r[i], xf);
+      conv_token(w, win, xf, l2, y);
+      store8(dst + t * dst_stride + dst_c, y);
+      if (t == se - 1 && state_out) {
+#pragma unroll
+        for (int j = 0; j < kHist; ++j) store8(state_out + (n * kHist + j) * C + c0, win[j]);
+      }
+    }
+  };
+  load_group(ga, t0);
+  for (int64_t tg = t0; tg < t1; tg += 2 * kGroup) {
+    load_group(gb, tg + kGroup);
+    run_group(ga, tg);
+    load_group(ga, tg + 2 * kGroup);
+    run_group(gb, tg + kGroup);
+  }
+}
+
+// One token per sequence against the carried convolution state, which is
+// updated in place (each lane reads its channels' history before writing it).
+template <typename T>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+prepare_decode_kernel(PrepareArgs a, T* __restrict__ state) {
+  const int lane = threadIdx.x & 31;
+  const int64_t unit = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t per_seq = a.n_seg + 1;
+  if (unit >= (int64_t)a.N * per_seq) return;
+  const int64_t n = unit / per_seq;
+  const int seg = (int)(unit % per_seq);
+  const int64_t C = (int64_t)a.H * (2 * a.dk + a.dv);
+  if (seg == a.n_seg) {
+    for (int64_t idx = n * a.H + lane; idx < (n + 1) * a.H; idx += 32) gates_one(a, idx);
+    return;
+  }
+  const int64_t c0 = (int64_t)seg * kSeg + lane * 8;
+  const bool l2 = seg < 2 * a.H * a.dk / kSeg;
+  float w[kTaps][8], win[kHist][8], xf[8], y[8];
+  load_taps(a.conv_w, c0, w);
+  history<T, false>(state, n, C, c0, win);
+  widen8<T>(load8(static_cast<const T*>(a.qkv) + n * C + c0), xf);
+  conv_token(w, win, xf, l2, y);
+  if (c0 < (int64_t)a.H * a.dk) {
+    store8(static_cast<T*>(a.q) + n * a.H * a.dk + c0, y);
+  } else if (c0 < 2 * (int64_t)a.H * a.dk) {
+    store8(static_cast<T*>(a.k) + n * a.H * a.dk + (c0 - (int64_t)a.H * a.dk), y);
+  } else {
+    store8(static_cast<T*>(a.v) + n * a.H * a.dv + (c0 - 2 * (int64_t)a.H * a.dk), y);
+  }
+#pragma unroll
+  for (int j = 0; j < kHist; ++j) store8(state + (n * kHist + j) * C + c0, win[j]);
+}
+
+// Eq. 20 read-out: y = o / sqrt(mean(o^2) + eps) * w * act(g) over the dv
+// values of one (token, head) row; one warp per row, NV groups of 8 per lane.
+template <typename T, int NV, bool kSilu>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+norm_gate_kernel(const T* o, const T* __restrict__ g, const float* __restrict__ w, float eps,
+                 T* y, int64_t rows) {   // y may be o itself
+  constexpr int dv = NV * kSeg;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * kWarpsPerCta;
+  float wr[NV][8];
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wr[v][i] = __ldg(w + v * kSeg + lane * 8 + i);
+  // two rows per iteration: both rows' loads are in flight before either is used
+  for (int64_t r0 = ((int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)) * 2; r0 < rows;
+       r0 += 2 * warps) {
+    Raw8 ro[2][NV], rg[2][NV];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (r0 + u < rows) {
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          ro[u][v] = load8(o + (r0 + u) * dv + v * kSeg + lane * 8);
+          rg[u][v] = load8(g + (r0 + u) * dv + v * kSeg + lane * 8);
+        }
+      }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int64_t r = r0 + u;
+      if (r >= rows) break;
+      float of[NV][8], ss = 0.f;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        widen8<T>(ro[u][v], of[v]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(of[v][i], of[v][i], ss);
+      }
+      const float rs = rsqrtf(warp_sum(ss) * (1.f / dv) + eps);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        float gf[8], out[8];
+        widen8<T>(rg[u][v], gf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float act = kSilu ? silu_fast(gf[i]) : sigmoid_fast(gf[i]);
+          out[i] = of[v][i] * rs * wr[v][i] * act;
+        }
+        store8(y + r * dv + v * kSeg + lane * 8, out);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+struct Span {
+  uintptr_t lo, hi;
+};
+Span span_of(const void* p, size_t bytes) { return {(uintptr_t)p, (uintptr_t)p + (p ? bytes : 0)}; }
+bool intersect(Span a, Span b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 148;
+  return n;
+}
+
+bool geometry_ok(int32_t dk, int32_t dv, int32_t io_dtype) {
+  return dk == kDK && supported_dv(dv) && (io_dtype == GDN_F32 || io_dtype == GDN_BF16);
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+int gdn_prepare(const void* qkv, const float* conv_w, const float* a_raw, const float* b_raw,
+                const float* A_log, const float* dt_bias, const int32_t* cu_seqlens,
+                const void* conv_state_in, void* conv_state_out, void* q, void* k, void* v,
+                float* alpha, float* beta, int32_t batch, int64_t seqlen, int32_t heads,
+                int32_t dk, int32_t dv, int32_t io_dtype, gdn_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (batch < 1 || seqlen < 0 || heads < 1) return GDN_ERR_INVALID_ARG;
+  if (!geometry_ok(dk, dv, io_dtype)) return GDN_ERR_UNSUPPORTED;
+  const bool varlen = cu_seqlens != nullptr;
+  const int64_t T_total = varlen ? seqlen : (int64_t)batch * seqlen;
+  if (!conv_w || !A_log || !dt_bias) return GDN_ERR_INVALID_ARG;
+  if (T_total > 0 && (!qkv || !a_raw || !b_raw || !q || !k || !v || !alpha || !beta))
+    return GDN_ERR_INVALID_ARG;
+  if (varlen && T_total > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+  const void* v16[] = {qkv, conv_w, conv_state_in, conv_state_out, q, k, v};
+  for (const void* p : v16)
+    if (!aligned(p, 16)) return GDN_ERR_ALIGNMENT;
+  const void* v4[] = {a_raw, b_raw, A_log, dt_bias, cu_seqlens, alpha, beta};
+  for (const void* p : v4)
+    if (!aligned(p, 4)) return GDN_ERR_ALIGNMENT;
+  const size_t es = io_dtype == GDN_BF16 ? 2 : 4;
+  const int64_t C = (int64_t)heads * (2 * dk + dv);
+  const size_t nt = (size_t)T_total, nh = nt * heads;
+  const size_t state_bytes = (size_t)batch * kHist * C * es;
+  const Span ins[] = {span_of(qkv, nt * C * es), span_of(conv_w, (size_t)C * kTaps * 4),
+                      span_of(a_raw, nh * 4), span_of(b_raw, nh * 4),
+                      span_of(A_log, heads * 4), span_of(dt_bias, heads * 4),
+                      span_of(cu_seqlens, varlen ? ((size_t)batch + 1) * 4 : 0),
+                      span_of(conv_state_in, state_bytes)};
+  const Span outs[] = {span_of(q, nh * dk * es), span_of(k, nh * dk * es),
+                       span_of(v, nh * dv * es), span_of(alpha, nh * 4), span_of(beta, nh * 4),
+                       span_of(conv_state_out, state_bytes)};
+  for (const Span& o : outs) {
+    for (const Span& i : ins)
+      if (intersect(i, o)) return GDN_ERR_INVALID_ARG;   // includes state_in == state_out
+    for (const Span& o2 : outs)
+      if (&o2 != &o && intersect(o, o2)) return GDN_ERR_INVALID_ARG;
+  }
+
+  PrepareArgs a{};
+  a.qkv = qkv; a.conv_w = conv_w; a.a_raw = a_raw; a.b_raw = b_raw; a.A_log = A_log;
+  a.dt_bias = dt_bias; a.state_in = conv_state_in; a.state_out = conv_state_out;
+  a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta;
+  a.cu = cu_seqlens; a.N = batch; a.T = varlen ? T_total : seqlen; a.T_total = T_total;
+  a.H = heads; a.dk = dk; a.dv = dv;
+  a.n_tiles = (T_total + kTile - 1) / kTile;
+  a.n_seg = (int32_t)(C / kSeg);
+  a.status = status_ptr();
+  if (!a.status) return GDN_ERR_CUDA;
+  const int64_t units = a.n_tiles * (a.n_seg + 1) + batch;
+  const int64_t blocks = (units + kWarpsPerCta - 1) / kWarpsPerCta;
+  if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+  if (blocks == 0) return GDN_OK;
+  if (io_dtype == GDN_BF16)
+    prepare_kernel<__nv_bfloat16><<<(unsigned)blocks, kWarpsPerCta * 32, 0, stream>>>(a);
+  else
+    prepare_kernel<float><<<(unsigned)blocks, kWarpsPerCta * 32, 0, stream>>>(a);
+  count_launches(1);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_prepare_decode_step(const void* qkv, const float* conv_w, const float* a_raw,
+                            const float* b_raw, const float* A_log, const float* dt_bias,
+                            void* conv_state, void* q, void* k, void* v, float* alpha,
+                            float* beta, int32_t batch, int32_t heads, int32_t dk, int32_t dv,
+                            int32_t io_dtype, gdn_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (batch < 1 || heads < 1) return GDN_ERR_INVALID_ARG;
+  if (!geometry_ok(dk, dv, io_dtype)) return GDN_ERR_UNSUPPORTED;
+  if (!qkv || !conv_w || !a_raw || !b_raw || !A_log || !dt_bias || !conv_state || !q || !k ||
+      !v || !alpha || !beta)
+    return GDN_ERR_INVALID_ARG;
+  const void* v16[] = {qkv, conv_w, conv_state, q, k, v};
+  for (const void* p : v16)
+    if (!aligned(p, 16)) return GDN_ERR_ALIGNMENT;
+  const void* v4[] = {a_raw, b_raw, A_log, dt_bias, alpha, beta};
+  for (const void* p : v4)
+    if (!aligned(p, 4)) return GDN_ERR_ALIGNMENT;
+  const size_t es = io_dtype == GDN_BF16 ? 2 : 4;
+  const int64_t C = (int64_t)heads * (2 * dk + dv);
+  const size_t nh = (size_t)batch * heads;
+  const Span ins[] = {span_of(qkv, (size_t)batch * C * es), span_of(conv_w, (size_t)C * kTaps * 4),
+                      span_of(a_raw, nh * 4), span_of(b_raw, nh * 4),
+                      span_of(A_log, heads * 4), span_of(dt_bias, heads * 4)};
+  const Span outs[] = {span_of(q, nh * dk * es), span_of(k, nh * dk * es),
+                       span_of(v, nh * dv * es), span_of(alpha, nh * 4), span_of(beta, nh * 4),
+                       span_of(conv_state, (size_t)batch * kHist * C * es)};
+  for (const Span& o : outs) {
+    for (const Span& i : ins)
+      if (intersect(i, o)) return GDN_ERR_INVALID_ARG;
+    for (const Span& o2 : outs)
+      if (&o2 != &o && intersect(o, o2)) return GDN_ERR_INVALID_ARG;
+  }
+  PrepareArgs a{};
+  a.qkv = qkv; a.conv_w = conv_w; a.a_raw = a_raw; a.b_raw = b_raw; a.A_log = A_log;
+  a.dt_bias = dt_bias; a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta;
+  a.N = batch; a.H = heads; a.dk = dk; a.dv = dv;
+  a.n_seg = (int32_t)(C / kSeg);
+  const int64_t units = (int64_t)batch * (a.n_seg + 1);
+  const int64_t blocks = (units + kWarpsPerCta - 1) / kWarpsPerCta;
+  if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+  if (io_dtype == GDN_BF16)
+    prepare_decode_kernel<__nv_bfloat16><<<(unsigned)blocks, kWarpsPerCta * 32, 0, stream>>>(
+        a, static_cast<__nv_bfloat16*>(conv_state));
+  else
+    prepare_decode_kernel<float><<<(unsigned)blocks, kWarpsPerCta * 32, 0, stream>>>(
+        a, static_cast<float*>(conv_state));
+  count_launches(1);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_output_norm_gate(const void* o, const void* g, const float* w, float eps, int32_t act,
+                         void* y, int64_t tokens, int32_t heads, int32_t dv, int32_t io_dtype,
+                         gdn_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (tokens < 0 || heads < 1 || !(eps >= 0.f)) return GDN_ERR_INVALID_ARG;
+  if (!supported_dv(dv) || (io_dtype != GDN_F32 && io_dtype != GDN_BF16) ||
+      (act != GDN_GATE_SILU && act != GDN_GATE_SIGMOID))
+    return GDN_ERR_UNSUPPORTED;
+  if (tokens == 0) return GDN_OK;
+  if (!o || !g || !w || !y) return GDN_ERR_INVALID_ARG;
+  if (!aligned(o, 16) || !aligned(g, 16) || !aligned(y, 16) || !aligned(w, 4))
+    return GDN_ERR_ALIGNMENT;
+  const size_t es = io_dtype == GDN_BF16 ? 2 : 4;
+  const size_t bytes = (size_t)tokens * heads * dv * es;
+  const Span so = span_of(o, bytes), sg = span_of(g, bytes), sy = span_of(y, bytes),
+             sw = span_of(w, (size_t)dv * 4);
+  // y may be o itself (in place) but may not overlap it partially, nor g or w
+  if ((y != o && intersect(sy, so)) || intersect(sy, sg) || intersect(sy, sw))
+    return GDN_ERR_INVALID_ARG;
+  const int64_t rows = tokens * heads;
+  const int64_t want = ((rows + 1) / 2 + kWarpsPerCta - 1) / kWarpsPerCta;
+  const int64_t cap = (int64_t)sm_count() * 8;   // grid-stride beyond 8 CTAs per SM
+  const unsigned blocks = (unsigned)(want < cap ? want : cap);
+  const bool silu = act == GDN_GATE_SILU;
+#define GDN_NG(T, NV, S)                                                              \
+  norm_gate_kernel<T, NV, S><<<blocks, kWarpsPerCta * 32, 0, stream>>>(              \
+      (const T*)o, (const T*)g, w, eps, (T*)y, rows)
+  if (io_dtype == GDN_BF16) {
+    if (dv == 256) { if (silu) GDN_NG(__nv_bfloat16, 1, true); else GDN_NG(__nv_bfloat16, 1, false); }
+    else           { if (silu) GDN_NG(__nv_bfloat16, 2, true); else GDN_NG(__nv_bfloat16, 2, false); }
+  } else {
+    if (dv == 256) { if (silu) GDN_NG(float, 1, true); else GDN_NG(float, 1, false); }
+    else           { if (silu) GDN_NG(float, 2, true); else GDN_NG(float, 2, false); }
+  }
+#undef GDN_NG
+  count_launches(1);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // extern "C"

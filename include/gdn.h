@@ -153,6 +153,86 @@ int gdn_decode_step(const void* q, const void* k, const void* v, const float* al
                     gdn_stream_t stream);
 
 /*
+ * ---------------------------------------------------------------------------
+ * The layer's steps on either side of the recurrence (Appendix A.3: the
+ * paragraph after Table 8, the text under Eq. 16-21, and Eq. 20).  The
+ * projections W_Q, W_K, W_V, W_alpha, W_beta, W_G and W_O are plain GEMMs and
+ * stay with the caller; these calls take their outputs.
+ *
+ * Channel layout of the packed q|k|v projection: C = H * (2 dk + dv)
+ * channels per token, q heads first (channel h*dk + i), then k heads, then v
+ * heads (2*H*dk + h*dv + j).
+ * ---------------------------------------------------------------------------
+ */
+
+enum gdn_gate_act { GDN_GATE_SILU = 0, GDN_GATE_SIGMOID = 1 };
+
+/*
+ * gdn_prepare -- the pre-recurrence steps for a dense or packed batch,
+ * producing exactly the q, k, v, alpha, beta that gdn_prefill consumes:
+ *
+ *   u      = SiLU(causal depthwise conv of width 4 over qkv)     per channel
+ *            u[t, c] = SiLU(sum_{j=0..3} conv_w[c, j] * qkv[t - 3 + j, c])
+ *   q, k   = u's q and k heads, each divided by sqrt(|.|^2 + 1e-6)
+ *   v      = u's v heads
+ *   alpha  = exp(-exp(A_log[h]) * softplus(a_raw[t, h] + dt_bias[h]))
+ *   beta   = sigmoid(b_raw[t, h])
+ *
+ * Inputs before a sequence's first token are its carried convolution state
+ * (conv_state_in[n, j, c] = the input 3 - j tokens before the start, i.e.
+ * oldest first) or zero when conv_state_in is NULL; each sequence of a packed
+ * batch starts over.  conv_state_out (NULL to skip) receives the three last
+ * inputs of each sequence's (history, tokens), oldest first -- the state a
+ * following gdn_prepare_decode_step continues from.  It may not alias
+ * conv_state_in.
+ *
+ *   qkv                    [B, T, C] or [T_total, C]          io dtype
+ *   conv_w                 [C, 4] fp32 (tap 3 multiplies the current token)
+ *   a_raw, b_raw           [B, T, H] or [T_total, H] fp32     (W_alpha x, W_beta x)
+ *   A_log, dt_bias         [H] fp32
+ *   conv_state_in / _out   [N, 3, C] io dtype, or NULL
+ *   q, k [.., H, dk]; v [.., H, dv] io dtype; alpha, beta [.., H] fp32 (outputs)
+ * batch / seqlen / cu_seqlens as in gdn_prefill (device cu_seqlens checked on
+ * the device: GDN_ERR_BAD_SEQLENS).  Outputs may not overlap inputs or each
+ * other (GDN_ERR_INVALID_ARG).  Tensors 16-byte aligned except the fp32
+ * [.., H] and [H] arrays (4 bytes).  dk = 256, dv = 256 or 512.
+ */
+int gdn_prepare(const void* qkv, const float* conv_w, const float* a_raw, const float* b_raw,
+                const float* A_log, const float* dt_bias, const int32_t* cu_seqlens,
+                const void* conv_state_in, void* conv_state_out, void* q, void* k, void* v,
+                float* alpha, float* beta, int32_t batch, int64_t seqlen, int32_t heads,
+                int32_t dk, int32_t dv, int32_t io_dtype, gdn_stream_t stream);
+
+/*
+ * gdn_prepare_decode_step -- gdn_prepare for one new token of each of `batch`
+ * sequences: qkv [N, C], a_raw / b_raw [N, H], outputs [N, H, .], and the
+ * convolution state conv_state [N, 3, C] (io dtype) read and updated in place.
+ * Equal to gdn_prepare on N one-token sequences with
+ * conv_state_in = old state, conv_state_out = new state.
+ */
+int gdn_prepare_decode_step(const void* qkv, const float* conv_w, const float* a_raw,
+                            const float* b_raw, const float* A_log, const float* dt_bias,
+                            void* conv_state, void* q, void* k, void* v, float* alpha,
+                            float* beta, int32_t batch, int32_t heads, int32_t dk, int32_t dv,
+                            int32_t io_dtype, gdn_stream_t stream);
+
+/*
+ * gdn_output_norm_gate -- Eq. 20's read-out for every (token, head) row:
+ *
+ *   y = o / sqrt(mean_j o_j^2 + eps) * w * act(g)        over the dv values
+ *
+ * with act = SiLU (GDN_GATE_SILU) or the logistic sigmoid (GDN_GATE_SIGMOID).
+ *   o, g, y   [tokens, H, dv] io dtype (o: gdn_prefill's / gdn_decode_step's
+ *             out; g: the W_G x projection).  y may be o itself (in place) but
+ *             no other overlap is allowed.
+ *   w         [dv] fp32, shared by the heads.
+ * eps >= 0.  dv = 256 or 512.
+ */
+int gdn_output_norm_gate(const void* o, const void* g, const float* w, float eps, int32_t act,
+                         void* y, int64_t tokens, int32_t heads, int32_t dv, int32_t io_dtype,
+                         gdn_stream_t stream);
+
+/*
  * gdn_get_device_status -- synchronises `stream`, then returns and clears the
  * device status word of the current device (GDN_OK when no kernel flagged a
  * problem since the last call; GDN_ERR_CUDA if the synchronisation failed).

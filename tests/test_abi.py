@@ -89,3 +89,50 @@ def test_decode_rejects_bad_host_arguments(lib):
                                1, None) == 2
     assert f(q=MIS) == 3
     assert f(out=P(0x800000 + 1024)) == 1      # out inside the state
+
+
+def _prepare(lib, qkv=A16, conv_w=A16, a_raw=A16, b_raw=A16, cu=None, sin=None, sout=None,
+             q=P(0x100000), k=P(0x200000), v=P(0x300000), alpha=P(0x400000), beta=P(0x500000),
+             batch=1, T=64, H=6, dk=256, dv=256, io=1):
+    return lib.gdn_prepare(qkv, conv_w, a_raw, b_raw, A16, A16, cu, sin, sout, q, k, v, alpha, beta,
+                           batch, T, H, dk, dv, io, None)
+
+
+def test_prepare_rejects_bad_host_arguments(lib):
+    assert _prepare(lib, batch=0) == 1
+    assert _prepare(lib, T=-1) == 1
+    assert _prepare(lib, conv_w=None) == 1
+    assert _prepare(lib, q=None) == 1
+    assert _prepare(lib, dk=128) == 2
+    assert _prepare(lib, dv=384) == 2
+    assert _prepare(lib, io=7) == 2
+    assert _prepare(lib, qkv=MIS) == 3
+    assert _prepare(lib, sout=P(0x600008)) == 3
+    assert _prepare(lib, a_raw=P(0x40001)) == 3
+    assert _prepare(lib, q=P(0x10000 + 4096)) == 1                  # q inside qkv
+    assert _prepare(lib, sin=P(0x700000), sout=P(0x700000)) == 1    # state in place: not here
+    assert _prepare(lib, k=P(0x100000 + 1024)) == 1                 # two outputs overlap
+
+
+def test_prepare_decode_rejects_bad_host_arguments(lib):
+    f = lambda st=P(0x700000), q=P(0x100000), H=6, dv=256, io=1: lib.gdn_prepare_decode_step(
+        A16, A16, A16, A16, A16, A16, st, q, P(0x200000), P(0x300000), P(0x400000), P(0x500000),
+        4, H, 256, dv, io, None)
+    assert f(st=None) == 1
+    assert f(H=0) == 1
+    assert f(dv=128) == 2
+    assert f(st=P(0x700004)) == 3
+    assert f(q=P(0x700000 + 2048)) == 1                                # q inside the state
+
+
+def test_output_norm_gate_rejects_bad_host_arguments(lib):
+    f = lambda o=A16, g=P(0x200000), w=P(0x300000), eps=1e-5, act=0, y=P(0x400000), dv=256, io=1: \
+        lib.gdn_output_norm_gate(o, g, w, ctypes.c_float(eps), act, y, 64, 6, dv, io, None)
+    assert f(act=5) == 2
+    assert f(dv=128) == 2
+    assert f(io=3) == 2
+    assert f(eps=-1.0) == 1
+    assert f(g=None) == 1
+    assert f(y=MIS) == 3
+    assert f(y=P(0x200000)) == 1                                      # y over g
+    assert f(y=P(0x10000 + 1024)) == 1                                # y partly over o
