@@ -8,6 +8,7 @@ raise when the compiled library is missing.
 
     out, S_final = prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None)
     out = decode_step(q, k, v, alpha, beta, S)          # S updated in place
+    grads = prefill_backward(q, k, v, alpha, beta, dout, S0, dS_final)   # training
     x = prepare(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, heads)   # -> q, k, v, alpha, beta
     y = output_norm_gate(out, g, w)                     # Eq. 20 read-out
 
@@ -65,6 +66,8 @@ def load():
     lib.gdn_kernel_launches.restype = ctypes.c_uint64
     lib.gdn_prefill_path.argtypes = [ctypes.c_int32]
     lib.gdn_prefill_path.restype = ctypes.c_char_p
+    lib.gdn_prefill_backward.argtypes = [vp] * 15 + [i32, i64, i32, i32, i32, i32, vp]
+    lib.gdn_prefill_backward.restype = ctypes.c_int
     lib.gdn_prepare.argtypes = [vp] * 14 + [i32, i64, i32, i32, i32, i32, vp]
     lib.gdn_prepare.restype = ctypes.c_int
     lib.gdn_prepare_decode_step.argtypes = [vp] * 12 + [i32, i32, i32, i32, i32, vp]
@@ -168,6 +171,51 @@ def prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=No
     if rc != 0:
         raise GDNError("gdn_prefill", rc)
     return out, S_final
+
+
+def prefill_backward(q, k, v, alpha, beta, dout, S0=None, dS_final=None, cu_seqlens=None,
+                     want_dS0: bool = True, stream=None):
+    """Gradients of the prefill (``gdn_prefill_backward``) for
+    L = <dout, out> + <dS_final, S_final>: returns dict dq, dk, dv (dtype of
+    q), dalpha, dbeta (fp32) and dS0 ([N, H, dv, dk] fp32, or None when
+    ``want_dS0`` is False).  Arguments as in :func:`prefill`; dout like out."""
+    lib = load()
+    dev, io = q.device, q.dtype
+    _io_code(io)
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+        _check(t, name, io, dev)
+    _check(alpha, "alpha", torch.float32, dev)
+    _check(beta, "beta", torch.float32, dev)
+    if q.dim() not in (3, 4) or k.shape != q.shape or dout.shape != v.shape:
+        raise ValueError("q, k must be [B, T, H, dk] (or [T, H, dk]); dout shaped like v")
+    H, dk, dv = q.shape[-2], q.shape[-1], v.shape[-1]
+    if v.shape[:-1] != q.shape[:-1] or alpha.shape != q.shape[:-1] or beta.shape != q.shape[:-1]:
+        raise ValueError("v, alpha, beta must match q's leading [.., T, H] axes")
+    if cu_seqlens is None:
+        B, T = (q.shape[0], q.shape[1]) if q.dim() == 4 else (1, q.shape[0])
+        N, seqlen = B, T
+    else:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        if q.dim() == 4 and q.shape[0] != 1:
+            raise ValueError("varlen input must have batch axis 1")
+        N, seqlen = cu_seqlens.numel() - 1, q.shape[-3]
+    for name, t in (("S0", S0), ("dS_final", dS_final)):
+        if t is not None:
+            _check(t, name, torch.float32, dev)
+            if tuple(t.shape) != (N, H, dv, dk):
+                raise ValueError(f"{name} must be [{N}, {H}, {dv}, {dk}]")
+    g = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+             dalpha=torch.empty_like(alpha), dbeta=torch.empty_like(beta),
+             dS0=torch.empty((N, H, dv, dk), dtype=torch.float32, device=dev) if want_dS0 else None)
+    with torch.cuda.device(dev):
+        rc = lib.gdn_prefill_backward(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
+            _ptr(dout), _ptr(dS_final), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+            _ptr(g["dalpha"]), _ptr(g["dbeta"]), _ptr(g["dS0"]), N, seqlen, H, dk, dv,
+            _io_code(io), _stream_handle(stream))
+    if rc != 0:
+        raise GDNError("gdn_prefill_backward", rc)
+    return g
 
 
 def decode_step(q, k, v, alpha, beta, S, out=None, stream=None):

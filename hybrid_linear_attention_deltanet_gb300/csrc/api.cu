@@ -3,6 +3,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "backward.cuh"
 #include "gdn_internal.cuh"
 #include "../../include/gdn_testing.h"
 
@@ -206,6 +207,74 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
   }
   if (e == cudaSuccess) e = tc ? launch_prefill_tc(a, stream) : launch_prefill_simt(a, io_dtype, stream);
   const cudaError_t ef = scratch ? cudaFreeAsync(scratch, stream) : cudaSuccess;
+  return (e == cudaSuccess && ef == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_prefill_backward(const void* q, const void* k, const void* v, const float* alpha,
+                         const float* beta, const float* S0, const int32_t* cu_seqlens,
+                         const void* dout, const float* dS_final, void* dq, void* dk, void* dv_,
+                         float* dalpha, float* dbeta, float* dS0, int32_t batch, int64_t seqlen,
+                         int32_t heads, int32_t dk_, int32_t dv, int32_t io_dtype,
+                         gdn_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (batch < 1 || seqlen < 0 || heads < 1) return GDN_ERR_INVALID_ARG;
+  const bool varlen = cu_seqlens != nullptr;
+  const int64_t T_total = varlen ? seqlen : (int64_t)batch * seqlen;
+  if (T_total > 0 && (!q || !k || !v || !alpha || !beta || !dout || !dq || !dk || !dv_ ||
+                      !dalpha || !dbeta))
+    return GDN_ERR_INVALID_ARG;
+  if (io_dtype != GDN_F32 && io_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  if (dk_ != kDK || !supported_dv(dv)) return GDN_ERR_UNSUPPORTED;
+  const void* a16[] = {q, k, v, dout, dq, dk, dv_, S0, dS_final, dS0};
+  for (const void* p : a16)
+    if (!aligned16(p)) return GDN_ERR_ALIGNMENT;
+  if (!aligned4(alpha) || !aligned4(beta) || !aligned4(dalpha) || !aligned4(dbeta) ||
+      !aligned4(cu_seqlens))
+    return GDN_ERR_ALIGNMENT;
+  if (varlen && T_total > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+  const size_t es = io_dtype == GDN_BF16 ? 2 : 4;
+  const size_t nth = (size_t)T_total * heads;
+  const size_t state_bytes = (size_t)batch * heads * dv * dk_ * sizeof(float);
+  const Range in[] = {span(q, nth * dk_ * es), span(k, nth * dk_ * es), span(v, nth * dv * es),
+                      span(alpha, nth * 4), span(beta, nth * 4), span(S0, S0 ? state_bytes : 0),
+                      span(cu_seqlens, varlen ? ((size_t)batch + 1) * 4 : 0),
+                      span(dout, nth * dv * es), span(dS_final, dS_final ? state_bytes : 0)};
+  const Range outs[] = {span(dq, nth * dk_ * es), span(dk, nth * dk_ * es),
+                        span(dv_, nth * dv * es), span(dalpha, nth * 4), span(dbeta, nth * 4),
+                        span(dS0, dS0 ? state_bytes : 0)};
+  for (const Range& o : outs) {
+    for (const Range& r : in)
+      if (overlaps(r, o)) return GDN_ERR_INVALID_ARG;
+    for (const Range& o2 : outs)
+      if (&o2 != &o && overlaps(o, o2)) return GDN_ERR_INVALID_ARG;
+  }
+  unsigned* status = status_ptr();
+  if (!status) return GDN_ERR_CUDA;
+  PrefillLaunch a{};
+  a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.S0 = S0; a.H = heads;
+  a.status = status; a.dv = dv;
+  a.map.cu_seqlens = cu_seqlens;
+  a.map.N = batch;
+  a.map.T = varlen ? T_total : seqlen;
+  a.map.chunks_per_seq = varlen ? 0 : (seqlen + kC - 1) / kC;
+  a.max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
+  const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
+  const size_t work_bytes = prefill_backward_scratch_bytes(a.max_chunks, heads, dv);
+  void* scratch = nullptr;
+  if (!scratch_pool() ||
+      cudaMallocFromPoolAsync(&scratch, off_bytes + work_bytes, scratch_pool(), stream) !=
+          cudaSuccess)
+    return GDN_ERR_CUDA;
+  a.scratch = (char*)scratch + off_bytes;
+  cudaError_t e = cudaSuccess;
+  if (varlen) {
+    a.map.chunk_off = (int32_t*)scratch;
+    e = launch_chunk_offsets(cu_seqlens, batch, T_total, (int32_t*)scratch, status, stream);
+  }
+  if (e == cudaSuccess)
+    e = launch_prefill_backward(a, dout, dS_final, dq, dk, dv_, dalpha, dbeta, dS0, io_dtype,
+                                stream);
+  const cudaError_t ef = cudaFreeAsync(scratch, stream);
   return (e == cudaSuccess && ef == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -1,0 +1,654 @@
+// Backward pass of the chunked gated delta rule on the CUDA cores (fp32).
+//
+// The training kernel of "Long-Context Aware Upcycling" (Appendix A.3, last
+// paragraph) splits sequences into chunks of C = 64 tokens, batches the delta
+// corrections of a chunk through the WY representation and carries the state
+// across chunks sequentially.  This file differentiates that chunked form.
+// Per chunk (rows r, j), with start state S (dv x dk), G = cumsum(log alpha),
+// gamma = e^G, Gam_rj = e^{G_r - G_j}, d_r = e^{G_L - G_r}, s = 1/sqrt(dk):
+//   A = strict_lower(beta_r Gam KK^T), T = (I + A)^-1,
+//   W = T diag(beta gamma) K, U~ = T diag(beta) V, U = U~ - W S^T,
+//   Qh = s diag(gamma) Q, Ph = s lower(Gam QK^T),
+//   O = Qh S^T + Ph U,  S' = gamma_L S + U^T diag(d) K.
+// Given dO and the gradient dS' of the chunk's end state:
+//   dU  = Ph^T dO + diag(d) K dS'^T
+//   dS  = gamma_L dS' + dO^T Qh - dU^T W             (carried to the chunk before)
+//   dQh = dO S, dPh = lower(dO U^T), dW = -dU S, dK += diag(d) U dS',
+//   dd_r = u_r . (dS' k_r), dgamma_L = <dS', S>,
+// then through W and U~ (dT = dW Bw^T + dU Bu^T with Bw = diag(beta gamma) K,
+// Bu = diag(beta) V), T (dA = -T^T dT T^T, strictly lower), A, Ph, Qh and the
+// decays down to log alpha (a reverse cumulative sum inside the chunk).
+//
+// Structure (every intermediate per (chunk, head) unit in fp32 scratch):
+//   gather      q, k, v, dO of each chunk -> zero-padded 64-row fp32 tiles;
+//               G (padding rows add log alpha = 0) and beta (0 on padding).
+//               Padding rows then contribute exactly nothing anywhere.
+//   prep        KK^T, QK^T (batched GEMM), T by forward substitution, Ph,
+//               W and U~ (batched GEMM).
+//   fwd_states  per (sequence, head, 32-row slice of S): the forward state
+//               pass, storing every chunk's start state.
+//   rev_states  per (sequence, head, 32-row slice): the reverse pass over
+//               chunks for dS; stores dS' and dU per chunk, dS0 at the end.
+//               Rows of dS are independent exactly as rows of S are.
+//   then batched 64-row GEMMs and three per-chunk elementwise kernels for the
+//   local gradients, and a final scatter into the token layout.
+#include "backward.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kNS = 32;              // rows of S (or dS) per state-pass CTA
+constexpr int kPad = kDK + 1;
+constexpr int kCC = kC * kC;
+
+// ------------------------------------------------------------------ scratch
+struct Bwd {
+  int64_t units;   // max_chunks * H
+  int32_t dv;
+  float *Q, *K, *V, *dO;          // [64][256] [64][256] [64][dv] [64][dv]
+  float *G, *B, *BG;              // [64]: cumsum log alpha, beta, beta*gamma
+  float *KK, *QK, *Tm, *TmB, *TmU, *Ph;   // [64][64]
+  float *W, *Ut;                  // [64][256] [64][dv]
+  float *Sst, *dSp;               // [dv][256]
+  float *dU, *U, *KdS, *TdU;      // [64][dv]
+  float *dQh, *dW, *dK1, *TdW, *dKa, *dQa;   // [64][256]
+  float *dPh, *dTm, *X, *dA, *Ms, *FG;       // [64][64]
+  float *dGc, *dBc;               // [64]
+  float *dgLp;                    // [dv / 32]
+  __host__ __device__ size_t sD() const { return (size_t)kC * kDK; }
+  __host__ __device__ size_t sV() const { return (size_t)kC * dv; }
+  __host__ __device__ size_t sS() const { return (size_t)dv * kDK; }
+};
+
+size_t bwd_bytes_per_unit(int32_t dv) {
+  const size_t D = (size_t)kC * kDK, V = (size_t)kC * dv, S = (size_t)dv * kDK;
+  return 4 * (2 * D + 2 * V + 3 * kC + 6 * kCC + D + V + 2 * S + 4 * V + 6 * D + 6 * kCC +
+              2 * kC + dv / kNS);
+}
+
+Bwd carve(void* base, int64_t units, int32_t dv) {
+  Bwd s{};
+  s.units = units;
+  s.dv = dv;
+  char* p = (char*)base;
+  auto take = [&](size_t per_unit) {
+    float* r = (float*)p;
+    p += align_up((size_t)units * per_unit * 4, 256);
+    return r;
+  };
+  const size_t D = (size_t)kC * kDK, V = (size_t)kC * dv, S = (size_t)dv * kDK;
+  s.Q = take(D); s.K = take(D); s.V = take(V); s.dO = take(V);
+  s.G = take(kC); s.B = take(kC); s.BG = take(kC);
+  s.KK = take(kCC); s.QK = take(kCC); s.Tm = take(kCC); s.TmB = take(kCC); s.TmU = take(kCC);
+  s.Ph = take(kCC);
+  s.W = take(D); s.Ut = take(V);
+  s.Sst = take(S); s.dSp = take(S);
+  s.dU = take(V); s.U = take(V); s.KdS = take(V); s.TdU = take(V);
+  s.dQh = take(D); s.dW = take(D); s.dK1 = take(D); s.TdW = take(D); s.dKa = take(D);
+  s.dQa = take(D);
+  s.dPh = take(kCC); s.dTm = take(kCC); s.X = take(kCC); s.dA = take(kCC); s.Ms = take(kCC);
+  s.FG = take(kCC);
+  s.dGc = take(kC); s.dBc = take(kC);
+  s.dgLp = take(dv / kNS);
+  return s;
+}
+
+size_t bwd_scratch_bytes(int64_t units, int32_t dv) {
+  // every array is padded to 256 B: bound by the per-unit sum plus 40 paddings
+  return (size_t)units * bwd_bytes_per_unit(dv) + 40 * 256;
+}
+
+// ------------------------------------------------------------------ gather
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+gather_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+              const T* __restrict__ dout, const float* __restrict__ alpha,
+              const float* __restrict__ beta, SeqMap map, int32_t H, Bwd s) {
+  const int64_t ci = blockIdx.x;
+  const int h = blockIdx.y, tid = threadIdx.x;
+  const int64_t u = ci * H + h;
+  int n = 0, L = 0;
+  int64_t t0 = 0;
+  if (!map.locate(ci, n, t0, L)) L = 0;   // units past the last chunk stay all-zero
+  const int dv = s.dv;
+  for (int e = tid; e < kC * kDK; e += kThreads) {
+    const int r = e / kDK, c = e % kDK;
+    const int64_t g = ((t0 + r) * H + h) * kDK + c;
+    s.Q[u * s.sD() + e] = r < L ? ld_in(q + g) : 0.f;
+    s.K[u * s.sD() + e] = r < L ? ld_in(k + g) : 0.f;
+  }
+  for (int e = tid; e < kC * dv; e += kThreads) {
+    const int r = e / dv, c = e % dv;
+    const int64_t g = ((t0 + r) * H + h) * dv + c;
+    s.V[u * s.sV() + e] = r < L ? ld_in(v + g) : 0.f;
+    s.dO[u * s.sV() + e] = r < L ? ld_in(dout + g) : 0.f;
+  }
+  if (tid < 32) {   // G = cumsum(log alpha) by warp scan over two halves
+    float carry = 0.f;
+    for (int half = 0; half < 2; ++half) {
+      const int r = half * 32 + tid;
+      float x = r < L ? logf(alpha[(t0 + r) * H + h]) : 0.f;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (tid >= o) x += y;
+      }
+      x += carry;
+      s.G[u * kC + r] = x;
+      s.B[u * kC + r] = r < L ? beta[(t0 + r) * H + h] : 0.f;
+      carry = __shfl_sync(0xffffffffu, x, 31);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ batched GEMM
+// C = alpha * colscale[n] * (A' B')[m][n] + beta * Cin[m][n], m < 64, per unit b.
+// A' = A [64][K] (row stride lda) or, kTA, A stored [K][64];
+// B' = B [K][N] or, kTB, B stored [N][K].  mask 1: keep n <= m; 2: keep n < m.
+struct BG {
+  const float* A; size_t sA; int lda;
+  const float* B; size_t sB; int ldb;
+  const float* Cin; float* C; size_t sC; int ldc;
+  const float* col; size_t sCol;
+  int N, K;
+  float alpha, beta;
+  int mask;
+  int64_t batch;
+};
+
+template <bool kTA, bool kTB>
+__global__ void __launch_bounds__(kThreads) bgemm_kernel(BG g) {
+  __shared__ __align__(16) float As[16][kC + 4];
+  __shared__ __align__(16) float Bs[16][kC + 4];
+  const int tid = threadIdx.x, tm = tid >> 4, tn = tid & 15;
+  const int n0 = blockIdx.x * kC;
+  for (int64_t b = blockIdx.y; b < g.batch; b += gridDim.y) {
+    const float* A = g.A + b * g.sA;
+    const float* B = g.B + b * g.sB;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int k0 = 0; k0 < g.K; k0 += 16) {
+      __syncthreads();
+      for (int e = tid; e < 16 * kC; e += kThreads) {
+        if (!kTA) { const int m = e >> 4, kk = e & 15; As[kk][m] = A[(size_t)m * g.lda + k0 + kk]; }
+        else      { const int kk = e >> 6, m = e & 63; As[kk][m] = A[(size_t)(k0 + kk) * g.lda + m]; }
+        if (!kTB) { const int kk = e >> 6, nn = e & 63; Bs[kk][nn] = B[(size_t)(k0 + kk) * g.ldb + n0 + nn]; }
+        else      { const int nn = e >> 4, kk = e & 15; Bs[kk][nn] = B[(size_t)(n0 + nn) * g.ldb + k0 + kk]; }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        const float4 a = *reinterpret_cast<const float4*>(&As[kk][tm * 4]);
+        const float4 bb = *reinterpret_cast<const float4*>(&Bs[kk][tn * 4]);
+        const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int m = tm * 4 + i;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int nn = n0 + tn * 4 + j;
+        float val = g.alpha * acc[i][j];
+        if (g.col) val *= g.col[b * g.sCol + nn];
+        if (g.Cin) val = fmaf(g.beta, g.Cin[b * g.sC + (size_t)m * g.ldc + nn], val);
+        if ((g.mask == 1 && nn > m) || (g.mask == 2 && nn >= m)) val = 0.f;
+        g.C[b * g.sC + (size_t)m * g.ldc + nn] = val;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ prep: T, Ph
+__global__ void __launch_bounds__(kThreads) tprep_kernel(Bwd s) {
+  __shared__ float As[kC][kC + 1];
+  __shared__ float Ts[kC][kC + 1];
+  __shared__ float Gs[kC], Bs[kC];
+  const int64_t u = blockIdx.x;
+  const int tid = threadIdx.x;
+  if (tid < kC) { Gs[tid] = s.G[u * kC + tid]; Bs[tid] = s.B[u * kC + tid]; }
+  __syncthreads();
+  for (int e = tid; e < kCC; e += kThreads) {
+    const int r = e >> 6, j = e & 63;
+    const float gam = j <= r ? expf(Gs[r] - Gs[j]) : 0.f;
+    As[r][j] = j < r ? Bs[r] * gam * s.KK[u * kCC + e] : 0.f;
+    s.Ph[u * kCC + e] = j <= r ? kScale * gam * s.QK[u * kCC + e] : 0.f;
+  }
+  __syncthreads();
+  if (tid < kC) {   // (I + A)^-1 by forward substitution, one column per thread
+    const int c = tid;
+    for (int r = 0; r < kC; ++r) Ts[r][c] = r == c ? 1.f : 0.f;
+    for (int r = 1; r < kC; ++r) {
+      float acc = 0.f;
+      for (int j = c; j < r; ++j) acc = fmaf(As[r][j], Ts[j][c], acc);
+      if (r > c) Ts[r][c] = -acc;
+    }
+    s.BG[u * kC + c] = Bs[c] * expf(Gs[c]);
+  }
+  __syncthreads();
+  for (int e = tid; e < kCC; e += kThreads) {
+    const int r = e >> 6, j = e & 63;
+    const float t = Ts[r][j];
+    s.Tm[u * kCC + e] = t;
+    s.TmB[u * kCC + e] = t * Bs[j] * expf(Gs[j]);
+    s.TmU[u * kCC + e] = t * Bs[j];
+  }
+}
+
+// ------------------------------------------------------------------ forward states
+__global__ void __launch_bounds__(kThreads)
+fwd_states_kernel(const float* __restrict__ S0, SeqMap map, int32_t H, Bwd s) {
+  extern __shared__ float sm[];
+  float* Ss = sm;                   // [kNS][kPad]
+  float* Wt = Ss + kNS * kPad;      // [C][33]
+  float* Us = Wt + kC * 33;         // [C][33]
+  float* dec = Us + kC * 33;        // [C]
+  const int n = blockIdx.x, h = blockIdx.y, slice = blockIdx.z;
+  const int tid = threadIdx.x, i = tid & 31, rg = tid >> 5;
+  const int dv = s.dv;
+  const int64_t sbase = ((int64_t)n * H + h) * dv * kDK + (int64_t)slice * kNS * kDK;
+  for (int e = tid; e < kNS * kDK; e += kThreads)
+    Ss[(e / kDK) * kPad + e % kDK] = S0 ? S0[sbase + e] : 0.f;
+  const int64_t cb = map.chunk_begin(n), ce = map.chunk_end(n);
+  for (int64_t ci = cb; ci < ce; ++ci) {
+    const int64_t u = ci * H + h;
+    __syncthreads();
+    float* dst = s.Sst + u * s.sS() + (size_t)slice * kNS * kDK;
+    for (int e = tid; e < kNS * kDK; e += kThreads) dst[e] = Ss[(e / kDK) * kPad + e % kDK];
+    const float* G = s.G + u * kC;
+    const float GL = G[kC - 1];
+    if (tid < kC) dec[tid] = expf(GL - G[tid]);
+    const float gL = expf(GL);
+    // U = U~ - W S^T for rows rg*8 .. rg*8+7, column i of the slice
+    float acc[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+    const float* Wg = s.W + u * s.sD();
+    for (int c0 = 0; c0 < kDK; c0 += 32) {
+      __syncthreads();
+      for (int e = tid; e < kC * 32; e += kThreads) Wt[(e >> 5) * 33 + (e & 31)] = Wg[(e >> 5) * kDK + c0 + (e & 31)];
+      __syncthreads();
+#pragma unroll 4
+      for (int cc = 0; cc < 32; ++cc) {
+        const float sv = Ss[i * kPad + c0 + cc];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[m] = fmaf(Wt[(rg * 8 + m) * 33 + cc], sv, acc[m]);
+      }
+    }
+    const float* Ug = s.Ut + u * s.sV();
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int r = rg * 8 + m;
+      Us[r * 33 + i] = Ug[r * dv + slice * kNS + i] - acc[m];
+    }
+    __syncthreads();
+    // S' = gamma_L S + U^T diag(d) K, column c = tid
+    {
+      const int c = tid;
+      const float* Kg = s.K + u * s.sD();
+      float a2[kNS];
+#pragma unroll
+      for (int m = 0; m < kNS; ++m) a2[m] = 0.f;
+      for (int r = 0; r < kC; ++r) {
+        const float kd = dec[r] * Kg[r * kDK + c];
+#pragma unroll
+        for (int m = 0; m < kNS; ++m) a2[m] = fmaf(Us[r * 33 + m], kd, a2[m]);
+      }
+#pragma unroll
+      for (int m = 0; m < kNS; ++m) Ss[m * kPad + c] = fmaf(gL, Ss[m * kPad + c], a2[m]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ reverse states
+__global__ void __launch_bounds__(kThreads)
+rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, SeqMap map,
+                  int32_t H, Bwd s) {
+  extern __shared__ float sm[];
+  float* Ds = sm;                   // [kNS][kPad]  this CTA's rows of dS
+  float* Kt = Ds + kNS * kPad;      // [C][33]
+  float* Os = Kt + kC * 33;         // [C][33]  dO columns of the slice
+  float* Us = Os + kC * 33;         // [C][33]  dU columns of the slice
+  float* Pt = Us + kC * 33;         // [C][C + 1]
+  float* dec = Pt + kC * (kC + 1);  // [C]
+  float* gq = dec + kC;             // [C]  s * gamma_r
+  float* red = gq + kC;             // [8]
+  const int n = blockIdx.x, h = blockIdx.y, slice = blockIdx.z;
+  const int tid = threadIdx.x, i = tid & 31, rg = tid >> 5;
+  const int dv = s.dv;
+  const int64_t sbase = ((int64_t)n * H + h) * dv * kDK + (int64_t)slice * kNS * kDK;
+  for (int e = tid; e < kNS * kDK; e += kThreads)
+    Ds[(e / kDK) * kPad + e % kDK] = dS_final ? dS_final[sbase + e] : 0.f;
+  const int64_t cb = map.chunk_begin(n), ce = map.chunk_end(n);
+  for (int64_t ci = ce - 1; ci >= cb; --ci) {
+    const int64_t u = ci * H + h;
+    __syncthreads();
+    // dS' of this chunk, and its part of <dS', S_start>
+    float* dst = s.dSp + u * s.sS() + (size_t)slice * kNS * kDK;
+    const float* Sg = s.Sst + u * s.sS() + (size_t)slice * kNS * kDK;
+    float part = 0.f;
+    for (int e = tid; e < kNS * kDK; e += kThreads) {
+      const float d = Ds[(e / kDK) * kPad + e % kDK];
+      dst[e] = d;
+      part = fmaf(d, Sg[e], part);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (i == 0) red[rg] = part;
+    const float* G = s.G + u * kC;
+    const float GL = G[kC - 1];
+    if (tid < kC) {
+      dec[tid] = expf(GL - G[tid]);
+      gq[tid] = kScale * expf(G[tid]);
+    }
+    const float gL = expf(GL);
+    const float* Og = s.dO + u * s.sV();
+    for (int e = tid; e < kC * 32; e += kThreads) Os[(e >> 5) * 33 + (e & 31)] = Og[(e >> 5) * dv + slice * kNS + (e & 31)];
+    const float* Pg = s.Ph + u * kCC;
+    for (int e = tid; e < kCC; e += kThreads) Pt[(e >> 6) * (kC + 1) + (e & 63)] = Pg[e];
+    // K dS^T for rows rg*8 .. +7, column i
+    float acc[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+    const float* Kg = s.K + u * s.sD();
+    for (int c0 = 0; c0 < kDK; c0 += 32) {
+      __syncthreads();
+      for (int e = tid; e < kC * 32; e += kThreads) Kt[(e >> 5) * 33 + (e & 31)] = Kg[(e >> 5) * kDK + c0 + (e & 31)];
+      __syncthreads();
+#pragma unroll 4
+      for (int cc = 0; cc < 32; ++cc) {
+        const float dsv = Ds[i * kPad + c0 + cc];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[m] = fmaf(Kt[(rg * 8 + m) * 33 + cc], dsv, acc[m]);
+      }
+    }
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < kThreads / 32; ++w) t += red[w];
+      s.dgLp[u * (dv / kNS) + slice] = t;
+    }
+    // dU = Ph^T dO + diag(d) K dS^T
+    float* dUg = s.dU + u * s.sV();
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int r = rg * 8 + m;
+      float x = dec[r] * acc[m];
+      for (int j = r; j < kC; ++j) x = fmaf(Pt[j * (kC + 1) + r], Os[j * 33 + i], x);
+      Us[r * 33 + i] = x;
+      dUg[r * dv + slice * kNS + i] = x;
+    }
+    __syncthreads();
+    // dS = gamma_L dS' + dO^T Qh - dU^T W, column c = tid
+    {
+      const int c = tid;
+      const float* Qg = s.Q + u * s.sD();
+      const float* Wg = s.W + u * s.sD();
+      float a2[kNS];
+#pragma unroll
+      for (int m = 0; m < kNS; ++m) a2[m] = 0.f;
+      for (int r = 0; r < kC; ++r) {
+        const float qh = gq[r] * Qg[r * kDK + c], w = Wg[r * kDK + c];
+#pragma unroll
+        for (int m = 0; m < kNS; ++m) a2[m] = fmaf(Os[r * 33 + m], qh, fmaf(-Us[r * 33 + m], w, a2[m]));
+      }
+#pragma unroll
+      for (int m = 0; m < kNS; ++m) Ds[m * kPad + c] = fmaf(gL, Ds[m * kPad + c], a2[m]);
+    }
+  }
+  __syncthreads();
+  if (dS0)
+    for (int e = tid; e < kNS * kDK; e += kThreads) dS0[sbase + e] = Ds[(e / kDK) * kPad + e % kDK];
+}
+
+// ------------------------------------------------------------------ C x C terms
+// Ms = M + M^T with M = dA o Gam o beta_r;  FG = s dPh o Gam;
+// dGc_r = rowsum_r(X) - colsum_r(X) with X = (dA beta_r KK + s dPh QK) o Gam;
+// dBc_r = sum_j dA_rj Gam_rj KK_rj.
+__global__ void __launch_bounds__(kThreads) cc_kernel(Bwd s) {
+  __shared__ float Mt[kC][kC + 1];
+  __shared__ float Xt[kC][kC + 1];
+  __shared__ float Gs[kC], Bs[kC];
+  const int64_t u = blockIdx.x;
+  const int tid = threadIdx.x;
+  if (tid < kC) { Gs[tid] = s.G[u * kC + tid]; Bs[tid] = s.B[u * kC + tid]; }
+  __syncthreads();
+  for (int e = tid; e < kCC; e += kThreads) {
+    const int r = e >> 6, j = e & 63;
+    const float gam = j <= r ? expf(Gs[r] - Gs[j]) : 0.f;
+    const float dA = s.dA[u * kCC + e], dP = s.dPh[u * kCC + e];
+    const float kk = s.KK[u * kCC + e], qk = s.QK[u * kCC + e];
+    Mt[r][j] = dA * gam * Bs[r];
+    Xt[r][j] = (dA * Bs[r] * kk + kScale * dP * qk) * gam;
+    s.FG[u * kCC + e] = kScale * dP * gam;
+  }
+  __syncthreads();
+  for (int e = tid; e < kCC; e += kThreads) {
+    const int r = e >> 6, j = e & 63;
+    s.Ms[u * kCC + e] = Mt[r][j] + Mt[j][r];
+  }
+  if (tid < kC) {
+    const int r = tid;
+    float rs = 0.f, cs = 0.f, db = 0.f;
+    for (int j = 0; j < kC; ++j) {
+      rs += Xt[r][j];
+      cs += Xt[j][r];
+    }
+    for (int j = 0; j < r; ++j)   // dA is strictly lower
+      db = fmaf(s.dA[u * kCC + r * kC + j] * expf(Gs[r] - Gs[j]), s.KK[u * kCC + r * kC + j], db);
+    s.dGc[u * kC + r] = rs - cs;
+    s.dBc[u * kC + r] = db;
+  }
+}
+
+// ------------------------------------------------------------------ assemble
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+assemble_kernel(const float* __restrict__ alpha, T* __restrict__ dq, T* __restrict__ dk,
+                T* __restrict__ dv_out, float* __restrict__ dalpha, float* __restrict__ dbeta,
+                SeqMap map, int32_t H, Bwd s) {
+  __shared__ float dG[kC], dB[kC], dsum[kC];
+  const int64_t ci = blockIdx.x;
+  const int h = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int n, L;
+  int64_t t0;
+  if (!map.locate(ci, n, t0, L)) return;
+  const int64_t u = ci * H + h;
+  const int dv = s.dv;
+  const float* G = s.G + u * kC;
+  const float GL = G[kC - 1];
+  for (int rr = 0; rr < kC / 8; ++rr) {
+    const int r = warp * (kC / 8) + rr;
+    const float gam = expf(G[r]), d = expf(GL - G[r]);
+    const float be = s.B[u * kC + r], bg = s.BG[u * kC + r];
+    float kTdW = 0.f, qdQh = 0.f, vTdU = 0.f, dd = 0.f;
+    for (int c = lane; c < kDK; c += 32) {
+      const size_t o = u * s.sD() + (size_t)r * kDK + c;
+      const float tdw = s.TdW[o], dqh = s.dQh[o];
+      kTdW = fmaf(s.K[o], tdw, kTdW);
+      qdQh = fmaf(s.Q[o], dqh, qdQh);
+      if (r < L) {
+        const size_t g = ((t0 + r) * H + h) * kDK + c;
+        st_out(dq + g, fmaf(kScale * gam, dqh, s.dQa[o]));
+        st_out(dk + g, fmaf(bg, tdw, fmaf(d, s.dK1[o], s.dKa[o])));
+      }
+    }
+    for (int c = lane; c < dv; c += 32) {
+      const size_t o = u * s.sV() + (size_t)r * dv + c;
+      const float tdu = s.TdU[o];
+      vTdU = fmaf(s.V[o], tdu, vTdU);
+      dd = fmaf(s.U[o], s.KdS[o], dd);
+      if (r < L) st_out(dv_out + ((t0 + r) * H + h) * dv + c, be * tdu);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      kTdW += __shfl_xor_sync(0xffffffffu, kTdW, o);
+      qdQh += __shfl_xor_sync(0xffffffffu, qdQh, o);
+      vTdU += __shfl_xor_sync(0xffffffffu, vTdU, o);
+      dd += __shfl_xor_sync(0xffffffffu, dd, o);
+    }
+    if (lane == 0) {
+      const float dgam = be * kTdW + kScale * qdQh;
+      dG[r] = gam * dgam + s.dGc[u * kC + r] - d * dd;
+      dB[r] = gam * kTdW + vTdU + s.dBc[u * kC + r];
+      dsum[r] = d * dd;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float extra = 0.f;
+    for (int r = 0; r < kC; ++r) extra += dsum[r];
+    float dgl = 0.f;
+    for (int sl = 0; sl < dv / kNS; ++sl) dgl += s.dgLp[u * (dv / kNS) + sl];
+    dG[kC - 1] += extra + expf(GL) * dgl;
+    float acc = 0.f;   // d log alpha_i = sum_{r >= i} dG_r
+    for (int r = kC - 1; r >= 0; --r) {
+      acc += dG[r];
+      dG[r] = acc;
+    }
+  }
+  __syncthreads();
+  if (tid < L) {
+    const int64_t g = (t0 + tid) * H + h;
+    dalpha[g] = dG[tid] / alpha[g];
+    dbeta[g] = dB[tid];
+  }
+}
+
+// ------------------------------------------------------------------ host helpers
+struct Mat {
+  const float* p; size_t stride; int ld;
+};
+
+cudaError_t gemm(cudaStream_t st, bool tA, bool tB, Mat A, Mat B, float* C, size_t sC, int ldc,
+                 int N, int K, float alpha, const float* Cin, float beta, int mask,
+                 const float* col, size_t sCol, int64_t batch) {
+  BG g{A.p, A.stride, A.ld, B.p, B.stride, B.ld, Cin, C, sC, ldc, col, sCol, N, K, alpha,
+       beta, mask, batch};
+  dim3 grid((unsigned)(N / kC), (unsigned)(batch < 65535 ? batch : 65535));
+  if (!tA && !tB) bgemm_kernel<false, false><<<grid, kThreads, 0, st>>>(g);
+  else if (!tA && tB) bgemm_kernel<false, true><<<grid, kThreads, 0, st>>>(g);
+  else if (tA && !tB) bgemm_kernel<true, false><<<grid, kThreads, 0, st>>>(g);
+  else bgemm_kernel<true, true><<<grid, kThreads, 0, st>>>(g);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+constexpr size_t kFwdSmem = sizeof(float) * (kNS * kPad + 2 * kC * 33 + kC);
+constexpr size_t kRevSmem = sizeof(float) * (kNS * kPad + 3 * kC * 33 + kC * (kC + 1) + 2 * kC + 8);
+
+}  // namespace
+
+size_t prefill_backward_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv) {
+  return bwd_scratch_bytes(max_chunks * H, dv);
+}
+
+cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
+                                    const float* dS_final, void* dq, void* dk, void* dv_out,
+                                    float* dalpha, float* dbeta, float* dS0, int io_dtype,
+                                    cudaStream_t st) {
+  const int64_t units = a.max_chunks * a.H;
+  const int dv = a.dv;
+  Bwd s = carve(a.scratch, units, dv);
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(fwd_states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kFwdSmem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(rev_states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kRevSmem)) != cudaSuccess)
+    return e;
+  const dim3 gu((unsigned)a.max_chunks, (unsigned)a.H);
+  if (units > 0) {
+    if (io_dtype == GDN_BF16)
+      gather_kernel<__nv_bfloat16><<<gu, kThreads, 0, st>>>(
+          (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
+          (const __nv_bfloat16*)dout, a.alpha, a.beta, a.map, a.H, s);
+    else
+      gather_kernel<float><<<gu, kThreads, 0, st>>>((const float*)a.q, (const float*)a.k,
+                                                     (const float*)a.v, (const float*)dout,
+                                                     a.alpha, a.beta, a.map, a.H, s);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t D = s.sD(), V = s.sV(), CC = kCC;
+    // KK^T and QK^T
+    if ((e = gemm(st, false, true, {s.K, D, kDK}, {s.K, D, kDK}, s.KK, CC, kC, kC, kDK, 1.f,
+                  nullptr, 0.f, 0, nullptr, 0, units)) != cudaSuccess) return e;
+    if ((e = gemm(st, false, true, {s.Q, D, kDK}, {s.K, D, kDK}, s.QK, CC, kC, kC, kDK, 1.f,
+                  nullptr, 0.f, 0, nullptr, 0, units)) != cudaSuccess) return e;
+    tprep_kernel<<<(unsigned)units, kThreads, 0, st>>>(s);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // W = T diag(beta gamma) K, U~ = T diag(beta) V
+    if ((e = gemm(st, false, false, {s.TmB, CC, kC}, {s.K, D, kDK}, s.W, D, kDK, kDK, kC, 1.f,
+                  nullptr, 0.f, 0, nullptr, 0, units)) != cudaSuccess) return e;
+    if ((e = gemm(st, false, false, {s.TmU, CC, kC}, {s.V, V, dv}, s.Ut, V, dv, dv, kC, 1.f,
+                  nullptr, 0.f, 0, nullptr, 0, units)) != cudaSuccess) return e;
+  }
+  const dim3 gs((unsigned)a.map.N, (unsigned)a.H, (unsigned)(dv / kNS));
+  fwd_states_kernel<<<gs, kThreads, kFwdSmem, st>>>(a.S0, a.map, a.H, s);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  rev_states_kernel<<<gs, kThreads, kRevSmem, st>>>(dS_final, dS0, a.map, a.H, s);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (units == 0) return cudaSuccess;
+  const size_t D = s.sD(), V = s.sV(), S = s.sS(), CC = kCC;
+  struct G {
+    bool tA, tB; Mat A, B; float* C; size_t sC; int ldc, N, K; float alpha;
+    const float* Cin; float beta; int mask; const float* col;
+  };
+  const G list[] = {
+      // U = U~ - W S^T
+      {false, true, {s.W, D, kDK}, {s.Sst, S, kDK}, s.U, V, dv, dv, kDK, -1.f, s.Ut, 1.f, 0, nullptr},
+      // dQh = dO S ; dW = -dU S ; dK1 = U dS' ; K dS'^T
+      {false, false, {s.dO, V, dv}, {s.Sst, S, kDK}, s.dQh, D, kDK, kDK, dv, 1.f, nullptr, 0.f, 0, nullptr},
+      {false, false, {s.dU, V, dv}, {s.Sst, S, kDK}, s.dW, D, kDK, kDK, dv, -1.f, nullptr, 0.f, 0, nullptr},
+      {false, false, {s.U, V, dv}, {s.dSp, S, kDK}, s.dK1, D, kDK, kDK, dv, 1.f, nullptr, 0.f, 0, nullptr},
+      {false, true, {s.K, D, kDK}, {s.dSp, S, kDK}, s.KdS, V, dv, dv, kDK, 1.f, nullptr, 0.f, 0, nullptr},
+      // dPh = lower(dO U^T)
+      {false, true, {s.dO, V, dv}, {s.U, V, dv}, s.dPh, CC, kC, kC, dv, 1.f, nullptr, 0.f, 1, nullptr},
+      // dT = (dW K^T) diag(beta gamma) + (dU V^T) diag(beta)
+      {false, true, {s.dW, D, kDK}, {s.K, D, kDK}, s.dTm, CC, kC, kC, kDK, 1.f, nullptr, 0.f, 0, s.BG},
+      {false, true, {s.dU, V, dv}, {s.V, V, dv}, s.dTm, CC, kC, kC, dv, 1.f, s.dTm, 1.f, 0, s.B},
+      // T^T dW, T^T dU, dA = -(T^T dT) T^T strictly lower
+      {true, false, {s.Tm, CC, kC}, {s.dW, D, kDK}, s.TdW, D, kDK, kDK, kC, 1.f, nullptr, 0.f, 0, nullptr},
+      {true, false, {s.Tm, CC, kC}, {s.dU, V, dv}, s.TdU, V, dv, dv, kC, 1.f, nullptr, 0.f, 0, nullptr},
+      {true, false, {s.Tm, CC, kC}, {s.dTm, CC, kC}, s.X, CC, kC, kC, kC, 1.f, nullptr, 0.f, 0, nullptr},
+      {false, true, {s.X, CC, kC}, {s.Tm, CC, kC}, s.dA, CC, kC, kC, kC, -1.f, nullptr, 0.f, 2, nullptr},
+  };
+  for (const G& g : list)
+    if ((e = gemm(st, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc, g.N, g.K, g.alpha, g.Cin, g.beta,
+                  g.mask, g.col, kC, units)) != cudaSuccess)
+      return e;
+  cc_kernel<<<(unsigned)units, kThreads, 0, st>>>(s);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const G list2[] = {
+      // dK: (M + M^T) K + FG^T Q ; dQ: FG K
+      {false, false, {s.Ms, CC, kC}, {s.K, D, kDK}, s.dKa, D, kDK, kDK, kC, 1.f, nullptr, 0.f, 0, nullptr},
+      {true, false, {s.FG, CC, kC}, {s.Q, D, kDK}, s.dKa, D, kDK, kDK, kC, 1.f, s.dKa, 1.f, 0, nullptr},
+      {false, false, {s.FG, CC, kC}, {s.K, D, kDK}, s.dQa, D, kDK, kDK, kC, 1.f, nullptr, 0.f, 0, nullptr},
+  };
+  for (const G& g : list2)
+    if ((e = gemm(st, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc, g.N, g.K, g.alpha, g.Cin, g.beta,
+                  g.mask, g.col, kC, units)) != cudaSuccess)
+      return e;
+  if (io_dtype == GDN_BF16)
+    assemble_kernel<__nv_bfloat16><<<gu, kThreads, 0, st>>>(
+        a.alpha, (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv_out, dalpha, dbeta,
+        a.map, a.H, s);
+  else
+    assemble_kernel<float><<<gu, kThreads, 0, st>>>(a.alpha, (float*)dq, (float*)dk,
+                                                     (float*)dv_out, dalpha, dbeta, a.map, a.H, s);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,19 @@
+// Launcher of the chunked backward pass (backward.cu).  Arguments and layouts
+// are those of gdn_prefill_backward in include/gdn.h.
+#pragma once
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+// Device scratch the backward of a call with this many chunks needs.
+size_t prefill_backward_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv);
+
+// a: the forward's arguments (q, k, v, alpha, beta, S0, map, H, dv,
+// max_chunks, scratch of prefill_backward_scratch_bytes); out and S_final unused.
+cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
+                                    const float* dS_final, void* dq, void* dk, void* dv,
+                                    float* dalpha, float* dbeta, float* dS0, int io_dtype,
+                                    cudaStream_t stream);
+
+}  // namespace gdn

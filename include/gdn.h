@@ -105,6 +105,32 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
                 int32_t dv, int32_t io_dtype, gdn_stream_t stream);
 
 /*
+ * gdn_prefill_backward -- gradients of the prefill, for training with the
+ * chunked kernel (Appendix A.3, last paragraph: the pages train with it).
+ *
+ * With L = <dout, out> + <dS_final, S_final> for the out and S_final that
+ * gdn_prefill computes from the same q, k, v, alpha, beta, S0 and
+ * cu_seqlens, it writes dL/dq, dL/dk, dL/dv (io dtype), dL/dalpha and
+ * dL/dbeta (fp32, [.., H]) and, when dS0 is not NULL, dL/dS0 (fp32
+ * [N, H, dv, dk]).  dS_final == NULL means a zero gradient on the final
+ * state; S0 == NULL a zero initial state.  The forward is recomputed inside
+ * (nothing has to be kept from gdn_prefill).  Layouts, batch / seqlen /
+ * cu_seqlens and alignment as in gdn_prefill; dout has the layout and dtype of
+ * out.  No output may overlap an input or another output.  Arithmetic is fp32
+ * on the CUDA cores for both io dtypes.
+ *
+ * Scratch: stream-ordered from the library's pool, about 1.7 MiB per
+ * (chunk of 64 tokens, head) at dv = 256 (5.4 GB for 32K tokens of a 6-head
+ * layer).
+ */
+int gdn_prefill_backward(const void* q, const void* k, const void* v, const float* alpha,
+                         const float* beta, const float* S0, const int32_t* cu_seqlens,
+                         const void* dout, const float* dS_final, void* dq, void* dk, void* dv,
+                         float* dalpha, float* dbeta, float* dS0, int32_t batch, int64_t seqlen,
+                         int32_t heads, int32_t dk_dim, int32_t dv_dim, int32_t io_dtype,
+                         gdn_stream_t stream);
+
+/*
  * gdn_prefill_noalloc -- gdn_prefill for callers that cannot allocate.
  *
  * The pages have no counterpart: this is a deployment variant of the same
