@@ -70,9 +70,31 @@ def prepare_bytes(T_total, N, H=H, dk=DK, dv=DV, io_bytes=2, state=True):
     return T_total * per_tok + (2 * N * 3 * C * io_bytes if state else 0) + C * 16 + 2 * H * 4
 
 
+def backward_flops(lengths, H=H, dk=DK, dv=DV):
+    """FLOPs the chunked backward executes per call (C = 64 rows a chunk,
+    padded chunks counted whole): the forward re-run for the chunk-start
+    states (KK^T, QK^T, W, U~, U and S' per chunk) plus the reverse state pass
+    (K dS'^T, Ph^T dO, dO^T Qh, dU^T W) and the per-chunk gradient products
+    (U, dO S, dU S, U dS', K dS'^T at C x d x d; dPh, dT, T^T dW, T^T dU, T^T dT,
+    dA, (M + M^T) K, FG^T Q, FG K at C x C x d)."""
+    chunks = sum((L + C - 1) // C for L in lengths) * H
+    big = 2 * C * dk * dv                      # one C x d x d product
+    small_k, small_v = 2 * C * C * dk, 2 * C * C * dv
+    fwd = 2 * small_k + small_k + small_v + 2 * big
+    rev = big + small_v + 2 * big
+    local = 5 * big + small_v + small_k + small_v + small_k + small_v + 4 * C * C * C \
+        + 3 * small_k
+    return chunks * (fwd + rev + local)
+
+
 def norm_gate_bytes(rows, dv=DV, io_bytes=2):
     """gdn_output_norm_gate: read o and g, write y, per (token, head) row."""
     return rows * dv * io_bytes * 3 + dv * 4
+
+
+# fp32 FMA peak of the CUDA cores, from the unit counts and the maximum SM
+# clock (152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz)
+FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def load_peaks():
@@ -365,6 +387,31 @@ def run_ours(args, rank, world, local_rank, dist):
     p5_ms = max_over_ranks(ev0.elapsed_time(ev1) / p5_steps)
     del x5, out5, sf5
 
+    # ---- backward of the 8K prefill (gdn_prefill_backward), dout and dS_final
+    # drawn once; each call recomputes the forward internally
+    bx = x
+    gen_b = torch.Generator(device=dev)
+    gen_b.manual_seed(11)
+    b_dout = torch.randn(bx["v"].shape, generator=gen_b, device=dev).to(bx["v"].dtype)
+    b_dsf = torch.randn(bx["S0"].shape, generator=gen_b, device=dev) * 0.1
+    bstep = lambda: gdn.prefill_backward(bx["q"], bx["k"], bx["v"], bx["alpha"], bx["beta"],
+                                         b_dout, bx["S0"], b_dsf)
+    for _ in range(2):
+        bstep()
+    torch.cuda.synchronize(dev)
+    bn0 = gdn.kernel_launches()
+    ev0.record(stream)
+    b_steps = 3
+    for _ in range(b_steps):
+        bstep()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    assert gdn.device_status() == 0
+    bw_ms = max_over_ranks(ev0.elapsed_time(ev1) / b_steps)
+    bw_launches = int(gdn.kernel_launches() - bn0) // b_steps
+    bw_flops = backward_flops(case.lengths)
+    del b_dout, b_dsf
+
     # ---- the layer steps around the recurrence on the 8K workload
     # (gdn_prepare: conv + SiLU, q/k L2 norm, gates; gdn_output_norm_gate:
     # Eq. 20's gated RMSNorm) and one decode step's gdn_prepare_decode_step
@@ -495,6 +542,21 @@ def run_ours(args, rank, world, local_rank, dist):
                             "counted_tflops": round(prefill_flops(pcase5.lengths, dv=512)
                                                     / (p5_ms * 1e-3) / 1e12, 3)},
             },
+            "backward": {
+                "workload": case.name + " (gdn_prefill_backward, dout and dS_final given)",
+                "ms_per_step": round(bw_ms, 3),
+                "value": round(throughput(tokens * world, bw_ms) / 1e6, 3),
+                "unit": "Mtok/s/layer",
+                "launches_per_step": bw_launches,
+                "roofline": {"bound": "alu", "unit": "TFLOP/s",
+                             "achieved": round(bw_flops / (bw_ms * 1e-3) / 1e12, 3),
+                             "peak": round(FP32_FMA_TFLOPS, 1),
+                             "frac": round(bw_flops / (bw_ms * 1e-3) / 1e12 / FP32_FMA_TFLOPS, 4),
+                             "executed_flops_per_launch": bw_flops,
+                             "peak_source": "fp32 FMA of the CUDA cores: 152 SMs x 128 lanes "
+                                            "x 2 FLOP x 2.07 GHz"},
+                "path": "CUDA-core fp32 (chunked form; forward re-run inside)",
+            },
             "layer_steps": {
                 "prepare": {"workload": lcase.name + " (gdn_prepare)",
                             "ms_per_step": round(prep_ms, 4),
@@ -554,8 +616,8 @@ def cpu_baseline(args, sample_tokens=2048):
 
 def run_profile(args):
     """Only the library's kernels of one family, for a profiler: W warm-up
-    then K steps of the 8K prefill workload, of the 256-sequence decode, or
-    of the 8K layer steps around the recurrence."""
+    then K steps of the 8K prefill workload, of the 256-sequence decode, of
+    the 8K layer steps around the recurrence, or of the 8K backward."""
     import torch
 
     import gdn_inputs
@@ -568,6 +630,13 @@ def run_profile(args):
         for _ in range(args.warmup + args.steps):
             gdn.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"], out=out,
                         S_final=sf)
+    elif args.profile == "backward":
+        x = gdn_inputs.make_prefill(gdn_inputs.prefill_8k(), device=dev)
+        dout = torch.randn(x["v"].shape, device=dev).to(x["v"].dtype)
+        dsf = torch.randn(x["S0"].shape, device=dev) * 0.1
+        for _ in range(args.warmup + args.steps):
+            gdn.prefill_backward(x["q"], x["k"], x["v"], x["alpha"], x["beta"], dout, x["S0"],
+                                 dsf)
     elif args.profile == "layer":
         # gdn_prepare then gdn_output_norm_gate on the 8K layer inputs, per step
         lc = gdn_inputs.layer_8k()
@@ -632,7 +701,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--profile", choices=["prefill", "decode", "layer"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "layer", "backward"], default=None,
                     help="run only W + K steps of one kernel family (for ncu captures); "
                          "prints no benchmark line")
     args = ap.parse_args()

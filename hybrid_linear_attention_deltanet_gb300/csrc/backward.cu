@@ -41,6 +41,7 @@ constexpr int kThreads = 256;
 constexpr int kNS = 32;              // rows of S (or dS) per state-pass CTA
 constexpr int kPad = kDK + 1;
 constexpr int kCC = kC * kC;
+constexpr int kSlab = 16;            // rows of a 64 x 256 operand staged at a time
 
 // ------------------------------------------------------------------ scratch
 struct Bwd {
@@ -250,7 +251,8 @@ fwd_states_kernel(const float* __restrict__ S0, SeqMap map, int32_t H, Bwd s) {
   float* Ss = sm;                   // [kNS][kPad]
   float* Wt = Ss + kNS * kPad;      // [C][33]
   float* Us = Wt + kC * 33;         // [C][33]
-  float* dec = Us + kC * 33;        // [C]
+  float* Ks = Us + kC * 33;         // [kSlab][256], 16-byte aligned
+  float* dec = Ks + kSlab * kDK;    // [C]
   const int n = blockIdx.x, h = blockIdx.y, slice = blockIdx.z;
   const int tid = threadIdx.x, i = tid & 31, rg = tid >> 5;
   const int dv = s.dv;
@@ -290,17 +292,24 @@ fwd_states_kernel(const float* __restrict__ S0, SeqMap map, int32_t H, Bwd s) {
       Us[r * 33 + i] = Ug[r * dv + slice * kNS + i] - acc[m];
     }
     __syncthreads();
-    // S' = gamma_L S + U^T diag(d) K, column c = tid
+    // S' = gamma_L S + U^T diag(d) K, column c = tid; K staged 16 rows at a time
     {
       const int c = tid;
-      const float* Kg = s.K + u * s.sD();
+      const float4* Kg = reinterpret_cast<const float4*>(s.K + u * s.sD());
       float a2[kNS];
 #pragma unroll
       for (int m = 0; m < kNS; ++m) a2[m] = 0.f;
-      for (int r = 0; r < kC; ++r) {
-        const float kd = dec[r] * Kg[r * kDK + c];
+      for (int r0 = 0; r0 < kC; r0 += kSlab) {
+        __syncthreads();
+        for (int e = tid; e < kSlab * kDK / 4; e += kThreads)
+          reinterpret_cast<float4*>(Ks)[e] = Kg[r0 * kDK / 4 + e];
+        __syncthreads();
+#pragma unroll 4
+        for (int r = 0; r < kSlab; ++r) {
+          const float kd = dec[r0 + r] * Ks[r * kDK + c];
 #pragma unroll
-        for (int m = 0; m < kNS; ++m) a2[m] = fmaf(Us[r * 33 + m], kd, a2[m]);
+          for (int m = 0; m < kNS; ++m) a2[m] = fmaf(Us[(r0 + r) * 33 + m], kd, a2[m]);
+        }
       }
 #pragma unroll
       for (int m = 0; m < kNS; ++m) Ss[m * kPad + c] = fmaf(gL, Ss[m * kPad + c], a2[m]);
@@ -317,7 +326,9 @@ rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, S
   float* Kt = Ds + kNS * kPad;      // [C][33]
   float* Os = Kt + kC * 33;         // [C][33]  dO columns of the slice
   float* Us = Os + kC * 33;         // [C][33]  dU columns of the slice
-  float* Pt = Us + kC * 33;         // [C][C + 1]
+  float* Qs = Us + kC * 33;         // [kSlab][256]
+  float* Ws = Qs + kSlab * kDK;     // [kSlab][256]
+  float* Pt = Ws + kSlab * kDK;     // [C][C + 1]
   float* dec = Pt + kC * (kC + 1);  // [C]
   float* gq = dec + kC;             // [C]  s * gamma_r
   float* red = gq + kC;             // [8]
@@ -386,18 +397,28 @@ rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, S
       dUg[r * dv + slice * kNS + i] = x;
     }
     __syncthreads();
-    // dS = gamma_L dS' + dO^T Qh - dU^T W, column c = tid
+    // dS = gamma_L dS' + dO^T Qh - dU^T W, column c = tid; Q and W staged 16 rows at a time
     {
       const int c = tid;
-      const float* Qg = s.Q + u * s.sD();
-      const float* Wg = s.W + u * s.sD();
+      const float4* Qg = reinterpret_cast<const float4*>(s.Q + u * s.sD());
+      const float4* Wg = reinterpret_cast<const float4*>(s.W + u * s.sD());
       float a2[kNS];
 #pragma unroll
       for (int m = 0; m < kNS; ++m) a2[m] = 0.f;
-      for (int r = 0; r < kC; ++r) {
-        const float qh = gq[r] * Qg[r * kDK + c], w = Wg[r * kDK + c];
+      for (int r0 = 0; r0 < kC; r0 += kSlab) {
+        __syncthreads();
+        for (int e = tid; e < kSlab * kDK / 4; e += kThreads) {
+          reinterpret_cast<float4*>(Qs)[e] = Qg[r0 * kDK / 4 + e];
+          reinterpret_cast<float4*>(Ws)[e] = Wg[r0 * kDK / 4 + e];
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int r = 0; r < kSlab; ++r) {
+          const float qh = gq[r0 + r] * Qs[r * kDK + c], w = Ws[r * kDK + c];
 #pragma unroll
-        for (int m = 0; m < kNS; ++m) a2[m] = fmaf(Os[r * 33 + m], qh, fmaf(-Us[r * 33 + m], w, a2[m]));
+          for (int m = 0; m < kNS; ++m)
+            a2[m] = fmaf(Os[(r0 + r) * 33 + m], qh, fmaf(-Us[(r0 + r) * 33 + m], w, a2[m]));
+        }
       }
 #pragma unroll
       for (int m = 0; m < kNS; ++m) Ds[m * kPad + c] = fmaf(gL, Ds[m * kPad + c], a2[m]);
@@ -541,8 +562,9 @@ cudaError_t gemm(cudaStream_t st, bool tA, bool tB, Mat A, Mat B, float* C, size
   return cudaGetLastError();
 }
 
-constexpr size_t kFwdSmem = sizeof(float) * (kNS * kPad + 2 * kC * 33 + kC);
-constexpr size_t kRevSmem = sizeof(float) * (kNS * kPad + 3 * kC * 33 + kC * (kC + 1) + 2 * kC + 8);
+constexpr size_t kFwdSmem = sizeof(float) * (kNS * kPad + 2 * kC * 33 + kSlab * kDK + kC);
+constexpr size_t kRevSmem =
+    sizeof(float) * (kNS * kPad + 3 * kC * 33 + 2 * kSlab * kDK + kC * (kC + 1) + 2 * kC + 8);
 
 }  // namespace
 

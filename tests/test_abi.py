@@ -136,3 +136,18 @@ def test_output_norm_gate_rejects_bad_host_arguments(lib):
     assert f(y=MIS) == 3
     assert f(y=P(0x200000)) == 1                                      # y over g
     assert f(y=P(0x10000 + 1024)) == 1                                # y partly over o
+
+
+def test_prefill_backward_rejects_bad_host_arguments(lib):
+    f = lambda q=A16, dout=P(0x600000), dq=P(0x100000), dS0=None, dv=256, io=1, batch=1, T=64: \
+        lib.gdn_prefill_backward(q, A16b, A16b, A16b, A16b, None, None, dout, None, dq,
+                                 P(0x200000), P(0x300000), P(0x400000), P(0x500000), dS0, batch,
+                                 T, 6, 256, dv, io, None)
+    assert f(batch=0) == 1
+    assert f(dout=None) == 1
+    assert f(dv=384) == 2
+    assert f(io=5) == 2
+    assert f(q=MIS) == 3
+    assert f(dS0=P(0x700008)) == 3
+    assert f(dq=P(0x600000 + 1024)) == 1                              # dq over dout
+    assert f(dq=P(0x200000 + 1024)) == 1                              # dq over dk
