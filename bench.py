@@ -483,7 +483,41 @@ def run_ours(args, rank, world, local_rank, dist):
     assert gdn.device_status() == 0
     del graph
     pd_b = prepare_bytes(len(dl.lengths), len(dl.lengths))
-    del dqkv, dlx, dl_out
+    # the whole mixer core of a decode step: fused (one cluster launch) and as
+    # three calls (prepare, recurrence, gated RMSNorm), 200 consecutive steps
+    # over 256 sequences with fresh projections each step
+    S_l = torch.randn((len(dl.lengths), dl.H, dl.dv, dl.dk), generator=gen, device=dev) * 0.02
+    dgate = torch.randn((dl_steps, len(dl.lengths), dl.H, dl.dv), generator=gen,
+                        device=dev).to(dl.io_dtype)
+    y_l = torch.empty_like(dgate[0])
+    o_l = torch.empty_like(dgate[0])
+    fl_i = [0]
+
+    def fused_step():
+        i = fl_i[0] % dl_steps
+        gdn.decode_layer_step(dqkv[i], dlx["conv_w"], dlx["a_raw"], dlx["b_raw"], dlx["A_log"],
+                              dlx["dt_bias"], dlx["conv_state"], S_l, dgate[i], dlx["norm_w"],
+                              1e-5, "silu", y=y_l)
+        fl_i[0] += 1
+
+    def three_calls():
+        i = fl_i[0] % dl_steps
+        p = gdn.prepare_decode_step(dqkv[i], dlx["conv_w"], dlx["a_raw"], dlx["b_raw"],
+                                    dlx["A_log"], dlx["dt_bias"], dlx["conv_state"], dl.H,
+                                    out=dl_out)
+        gdn.decode_step(p["q"], p["k"], p["v"], p["alpha"], p["beta"], S_l, out=o_l)
+        gdn.output_norm_gate(o_l, dgate[i], dlx["norm_w"], 1e-5, "silu", y=y_l)
+        fl_i[0] += 1
+
+    fused_ms, fused_launch = time_it(fused_step, dl_steps)
+    three_ms, three_launch = time_it(three_calls, dl_steps)
+    assert gdn.device_status() == 0
+    C_l = dl.channels
+    nl = len(dl.lengths)
+    fused_b = (decode_bytes(nl) - nl * dl.H * (3 * 512 + 8)      # state, out -> y, gates
+               + nl * (C_l * 2 + 2 * 3 * C_l * 2 + dl.H * 8) + nl * dl.H * dl.dv * 2
+               + C_l * 16 + dl.dv * 4)
+    del dqkv, dlx, dl_out, S_l, dgate, y_l, o_l
 
     res = None
     if rank == 0:
@@ -577,6 +611,16 @@ def run_ours(args, rank, world, local_rank, dist):
                                         "ms_per_step": round(pd_ms, 5),
                                         "value": round(pd_b / (pd_ms * 1e-3) / 1e9, 2),
                                         "unit": "GB/s", "algorithmic_bytes_per_launch": pd_b},
+                "decode_layer_step": {
+                    "workload": "fused decode step of the mixer core, 256 sequences x 6 heads, "
+                                f"bf16, x{dl_steps} steps (gdn_decode_layer_step)",
+                    "ms_per_step": round(fused_ms, 5),
+                    "value": round(fused_b / (fused_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "frac_of_hbm": round(fused_b / (fused_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                    "algorithmic_bytes_per_launch": fused_b,
+                    "launches_per_step": fused_launch,
+                    "three_calls_ms_per_step": round(three_ms, 5),
+                    "three_calls_launches_per_step": three_launch},
             },
             "clocks": clocks,
             "decode": {
@@ -637,6 +681,14 @@ def run_profile(args):
         for _ in range(args.warmup + args.steps):
             gdn.prefill_backward(x["q"], x["k"], x["v"], x["alpha"], x["beta"], dout, x["S0"],
                                  dsf)
+    elif args.profile == "decode_layer":
+        lc = gdn_inputs.layer_decode_256()
+        lx = gdn_inputs.make_layer(lc, device=dev)
+        S = torch.randn((len(lc.lengths), lc.H, lc.dv, lc.dk), device=dev) * 0.02
+        for _ in range(args.warmup + args.steps):
+            gdn.decode_layer_step(lx["qkv"], lx["conv_w"], lx["a_raw"], lx["b_raw"], lx["A_log"],
+                                  lx["dt_bias"], lx["conv_state"], S,
+                                  lx["g"].reshape(len(lc.lengths), lc.H, lc.dv), lx["norm_w"])
     elif args.profile == "layer":
         # gdn_prepare then gdn_output_norm_gate on the 8K layer inputs, per step
         lc = gdn_inputs.layer_8k()
@@ -701,7 +753,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--profile", choices=["prefill", "decode", "layer", "backward"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "layer", "backward", "decode_layer"],
+                    default=None,
                     help="run only W + K steps of one kernel family (for ncu captures); "
                          "prints no benchmark line")
     args = ap.parse_args()

@@ -11,6 +11,7 @@ raise when the compiled library is missing.
     grads = prefill_backward(q, k, v, alpha, beta, dout, S0, dS_final)   # training
     x = prepare(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, heads)   # -> q, k, v, alpha, beta
     y = output_norm_gate(out, g, w)                     # Eq. 20 read-out
+    y = decode_layer_step(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, conv_state, S, g, w)
 
 Recurrence (Appendix A.3, Eq. 16-19 of "Long-Context Aware Upcycling"):
 S_t = alpha_t S_{t-1}(I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
@@ -74,6 +75,9 @@ def load():
     lib.gdn_prepare_decode_step.restype = ctypes.c_int
     lib.gdn_output_norm_gate.argtypes = [vp, vp, vp, ctypes.c_float, i32, vp, i64, i32, i32, i32,
                                          vp]
+    lib.gdn_decode_layer_step.argtypes = [vp] * 10 + [ctypes.c_float, i32, vp, i32, i32, i32,
+                                                      i32, i32, vp]
+    lib.gdn_decode_layer_step.restype = ctypes.c_int
     lib.gdn_output_norm_gate.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -370,6 +374,43 @@ def output_norm_gate(o, g, w, eps=1e-5, act="silu", y=None, stream=None):
                                       tokens, H, dv, _io_code(io), _stream_handle(stream))
     if rc != 0:
         raise GDNError("gdn_output_norm_gate", rc)
+    return y
+
+
+def decode_layer_step(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, conv_state, S, gate, norm_w,
+                      eps=1e-5, act="silu", y=None, stream=None):
+    """One fused decode step of the mixer core (``gdn_decode_layer_step``):
+    conv + SiLU + L2 norm + gates, the state update, and Eq. 20's gated
+    RMSNorm.  qkv [N, C]; conv_state [N, 3, C] and S [N, H, dv, dk] updated in
+    place; gate [N, H, dv]; norm_w [dv].  Returns y [N, H, dv]."""
+    lib = load()
+    dev, io = qkv.device, qkv.dtype
+    _io_code(io)
+    N, H, dv, dk = S.shape
+    C = H * (2 * dk + dv)
+    _check(qkv, "qkv", io, dev)
+    _check(conv_state, "conv_state", io, dev)
+    _check(gate, "gate", io, dev)
+    _check(S, "S", torch.float32, dev)
+    for name, t in (("conv_w", conv_w), ("a_raw", a_raw), ("b_raw", b_raw), ("A_log", A_log),
+                    ("dt_bias", dt_bias), ("norm_w", norm_w)):
+        _check(t, name, torch.float32, dev)
+    if (tuple(qkv.shape) != (N, C) or tuple(conv_state.shape) != (N, 3, C)
+            or tuple(conv_w.shape) != (C, 4) or tuple(a_raw.shape) != (N, H)
+            or tuple(b_raw.shape) != (N, H) or tuple(gate.shape) != (N, H, dv)
+            or tuple(norm_w.shape) != (dv,)):
+        raise ValueError("shape mismatch in decode_layer_step arguments")
+    if y is None:
+        y = torch.empty_like(gate)
+    else:
+        _check(y, "y", io, dev)
+    with torch.cuda.device(dev):
+        rc = lib.gdn_decode_layer_step(
+            _ptr(qkv), _ptr(conv_w), _ptr(a_raw), _ptr(b_raw), _ptr(A_log), _ptr(dt_bias),
+            _ptr(conv_state), _ptr(S), _ptr(gate), _ptr(norm_w), float(eps), GATE_ACT[act],
+            _ptr(y), N, H, dk, dv, _io_code(io), _stream_handle(stream))
+    if rc != 0:
+        raise GDNError("gdn_decode_layer_step", rc)
     return y
 
 

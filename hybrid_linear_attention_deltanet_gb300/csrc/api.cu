@@ -52,6 +52,16 @@ cudaMemPool_t scratch_pool() {
 
 }  // namespace
 
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t stream) {
+  cudaMemPool_t pool = scratch_pool();
+  if (!pool) return cudaErrorMemoryAllocation;
+  return cudaMallocFromPoolAsync(p, bytes, pool, stream);
+}
+
+cudaError_t scratch_free(void* p, cudaStream_t stream) {
+  return p ? cudaFreeAsync(p, stream) : cudaSuccess;
+}
+
 // Address of this device's status word, looked up once per device with that
 // device current.
 unsigned* status_ptr() {

@@ -259,6 +259,29 @@ int gdn_output_norm_gate(const void* o, const void* g, const float* w, float eps
                          gdn_stream_t stream);
 
 /*
+ * gdn_decode_layer_step -- one decode step of the whole mixer core:
+ * gdn_prepare_decode_step, gdn_decode_step and gdn_output_norm_gate fused
+ * into two launches (the convolution, gates and state update in one; Eq. 20
+ * and the q / k history shift in the other), for the serving loop.
+ *
+ *   qkv, conv_w, a_raw, b_raw, A_log, dt_bias, conv_state   as in gdn_prepare_decode_step
+ *   S        [N, H, dv, dk] fp32 states, updated in place
+ *   gate     [N, H, dv] io dtype (the W_G x projection); norm_w [dv] fp32; eps >= 0; act
+ *   y        [N, H, dv] io dtype: o / sqrt(mean(o^2) + eps) * norm_w * act(gate), where o
+ *            is the step's read-out S_t q_t / sqrt(dk) (o itself is not written)
+ * q, k and v stay fp32 between the convolution and the recurrence (the three
+ * separate calls round them to the io dtype in between), so results agree with
+ * the three calls to within that rounding.  The read-outs between the two
+ * launches live in stream-ordered scratch from the library's pool
+ * (N * H * dv * 4 bytes).  No output may overlap an input or another output.
+ */
+int gdn_decode_layer_step(const void* qkv, const float* conv_w, const float* a_raw,
+                          const float* b_raw, const float* A_log, const float* dt_bias,
+                          void* conv_state, float* S, const void* gate, const float* norm_w,
+                          float eps, int32_t act, void* y, int32_t batch, int32_t heads,
+                          int32_t dk, int32_t dv, int32_t io_dtype, gdn_stream_t stream);
+
+/*
  * gdn_get_device_status -- synchronises `stream`, then returns and clears the
  * device status word of the current device (GDN_OK when no kernel flagged a
  * problem since the last call; GDN_ERR_CUDA if the synchronisation failed).

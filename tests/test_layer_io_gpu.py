@@ -229,3 +229,46 @@ def test_layer_steps_at_full_size(gdn_lib):
     assert gdn_lib.device_status() == 0
     yr = lio.output_norm_gate(o, x["g"], x["norm_w"], 1e-5, "silu")
     assert rel(_f64(y), yr) <= 3e-3
+
+
+@pytest.mark.parametrize("io", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dv,act", [(256, "silu"), (512, "sigmoid")])
+def test_decode_layer_step_matches_oracle_composition(gdn_lib, io, dv, act):
+    """The fused decode step (one cluster launch) against the oracle's prepare,
+    token recurrence and gated RMSNorm, over four steps with the convolution
+    and recurrent states carried in place."""
+    H, N, steps = 2, 5, 4
+    case = LayerCase("fused decode", [1] * (N * steps), H=H, dv=dv, io_dtype=io, seed=97,
+                     varlen=True)
+    x = gdn_inputs.make_layer(case, device="cpu")
+    C = case.channels
+    qkv = x["qkv"].reshape(steps, N, C)
+    a = x["a_raw"].reshape(steps, N, H)
+    b = x["b_raw"].reshape(steps, N, H)
+    gate = x["g"].reshape(steps, N, H, dv)
+    gen = torch.Generator().manual_seed(98)
+    S0 = torch.randn((N, H, dv, 256), generator=gen) * 0.02
+    st_gpu, S_gpu = x["conv_state"][:N].clone().to(DEV), S0.clone().to(DEV)
+    st_ref, S_ref = lio.widen(x["conv_state"][:N]).copy(), S0.double().numpy().copy()
+    tol = 1e-4 if io == torch.float32 else 2e-2
+    dev = {k: x[k].to(DEV) for k in ("conv_w", "A_log", "dt_bias", "norm_w")}
+    for t in range(steps):
+        y = gdn_lib.decode_layer_step(qkv[t].to(DEV), dev["conv_w"], a[t].to(DEV), b[t].to(DEV),
+                                      dev["A_log"], dev["dt_bias"], st_gpu, S_gpu,
+                                      gate[t].to(DEV), dev["norm_w"], 1e-5, act)
+        p = lio.prepare_decode_step(qkv[t], x["conv_w"], a[t], b[t], x["A_log"], x["dt_bias"],
+                                    st_ref, H, 256, dv)
+        f32 = lambda z: np.ascontiguousarray(z, np.float32)
+        o = oracle.decode_step(f32(p["q"]), f32(p["k"]), f32(p["v"]), f32(p["alpha"]),
+                               f32(p["beta"]), S_ref)
+        y_ref = lio.output_norm_gate(o, gate[t], x["norm_w"], 1e-5, act)
+        got = _f64(y)
+        for n in range(N):
+            for h in range(H):
+                assert rel(got[n, h], y_ref[n, h]) <= tol, (t, n, h)
+        assert np.array_equal(_f64(st_gpu), st_ref)
+    assert gdn_lib.device_status() == 0
+    Sg = S_gpu.cpu().numpy()
+    for n in range(N):
+        for h in range(H):
+            assert rel(Sg[n, h], S_ref[n, h]) <= 1e-4
