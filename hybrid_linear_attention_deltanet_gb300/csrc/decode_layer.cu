@@ -183,34 +183,48 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_layer_kernel(LayerArgs 
   if (lane < kRowsPerWarp) a.o_buf[unit * a.dv + row0 + lane] = o_mine;
 }
 
-// Launch 2: Eq. 20 for every (sequence, head) row of read-outs, one warp per
-// row, and the in-place shift of the head's q and k convolution history (the
-// first launch has finished reading it).
+// Launch 2: Eq. 20 for every (sequence, head), one CTA of 256 threads each
+// (one or two read-outs a thread, a block reduction for the mean square), and
+// the in-place shift of the head's q and k convolution history (two channels
+// a thread; the first launch has finished reading it).
 template <typename T, bool kSilu>
-__global__ void __launch_bounds__(kWarps * 32) finish_kernel(LayerArgs a, int64_t units) {
-  const int lane = threadIdx.x & 31;
-  const int64_t unit = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-  if (unit >= units) return;
+__global__ void __launch_bounds__(kWarps * 32) finish_kernel(LayerArgs a) {
+  const int64_t unit = blockIdx.x;
   const int64_t n = unit / a.H;
   const int h = (int)(unit % a.H);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ float part[kWarps];
   const float* o = a.o_buf + unit * a.dv;
-  float ss = 0.f;
-  for (int r = lane; r < a.dv; r += 32) ss = fmaf(o[r], o[r], ss);
-  const float rs = rsqrtf(warp_sum(ss) / a.dv + a.eps);
-  for (int r = lane; r < a.dv; r += 32) {
-    const float g = ld_in(static_cast<const T*>(a.gate) + unit * a.dv + r);
-    const float act = kSilu ? silu_fast(g) : __fdividef(1.f, 1.f + __expf(-g));
-    st_out(static_cast<T*>(a.y) + unit * a.dv + r, o[r] * rs * a.norm_w[r] * act);
+  float ov[2] = {0.f, 0.f}, ss = 0.f;
+  for (int i = 0; i * kWarps * 32 < a.dv; ++i) {
+    ov[i] = o[i * kWarps * 32 + tid];
+    ss = fmaf(ov[i], ov[i], ss);
   }
+  ss = warp_sum(ss);
+  if (lane == 0) part[warp] = ss;
+  // the q / k history shift does not depend on the norm: issue it meanwhile
   const int64_t C = (int64_t)a.H * (2 * kDK + a.dv);
   const T* x = static_cast<const T*>(a.qkv) + n * C;
   T* st = static_cast<T*>(a.conv_state) + n * 3 * C;
-  for (int e = lane; e < 2 * kDK; e += 32) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int e = i * kWarps * 32 + tid;               // 0 .. 511 over q | k
     const int64_t c = (e < kDK ? 0 : (int64_t)a.H * kDK - kDK) + (int64_t)h * kDK + e;
     const float h1 = ld_in(st + C + c), h2 = ld_in(st + 2 * C + c), xc = ld_in(x + c);
     st_out(st + c, h1);
     st_out(st + C + c, h2);
     st_out(st + 2 * C + c, xc);
+  }
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) tot += part[w];
+  const float rs = rsqrtf(tot / a.dv + a.eps);
+  for (int i = 0; i * kWarps * 32 < a.dv; ++i) {
+    const int r = i * kWarps * 32 + tid;
+    const float g = ld_in(static_cast<const T*>(a.gate) + unit * a.dv + r);
+    const float act = kSilu ? silu_fast(g) : __fdividef(1.f, 1.f + __expf(-g));
+    st_out(static_cast<T*>(a.y) + unit * a.dv + r, ov[i] * rs * a.norm_w[r] * act);
   }
 }
 
@@ -226,8 +240,7 @@ cudaError_t launch(const LayerArgs& a, int64_t units, cudaStream_t stream) {
   decode_layer_kernel<T><<<(unsigned)(units * (a.dv / kRows)), kWarps * 32, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  finish_kernel<T, kSilu><<<(unsigned)((units + kWarps - 1) / kWarps), kWarps * 32, 0, stream>>>(
-      a, units);
+  finish_kernel<T, kSilu><<<(unsigned)units, kWarps * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
