@@ -118,6 +118,20 @@ void gdn_testing_set_trace(uint64_t* device_buf, int32_t max_chunks);
  */
 int32_t gdn_testing_last_prefill_form(void);
 
+/*
+ * gdn_testing_bounded_wait -- fault test of the library's bounded waits.
+ * One thread waits on something that never completes: which = 0, an
+ * mbarrier that expects one arrival and gets none (the try-wait every
+ * tensor-core kernel uses for its copies and MMAs); which = 1, a ready flag in
+ * global memory that nothing sets (the relaxed-load poll the fused prefill's
+ * state pass uses for the per-chunk workers' results).  After limit_ns
+ * nanoseconds of GPU global time (0 .. 2e9) the wait gives up, records
+ * GDN_ERR_TIMEOUT in the device status word (read back with
+ * gdn_get_device_status) and the kernel returns; nothing traps or hangs.
+ * Returns GDN_ERR_INVALID_ARG for other arguments.
+ */
+int gdn_testing_bounded_wait(int32_t which, int64_t limit_ns, gdn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

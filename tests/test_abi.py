@@ -151,3 +151,11 @@ def test_prefill_backward_rejects_bad_host_arguments(lib):
     assert f(dS0=P(0x700008)) == 3
     assert f(dq=P(0x600000 + 1024)) == 1                              # dq over dout
     assert f(dq=P(0x200000 + 1024)) == 1                              # dq over dk
+
+
+def test_fault_hook_rejects_bad_arguments(lib):
+    f = lib.gdn_testing_bounded_wait
+    f.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p]
+    assert f(2, 1000, None) == 1
+    assert f(0, -1, None) == 1
+    assert f(1, 3_000_000_000, None) == 1
