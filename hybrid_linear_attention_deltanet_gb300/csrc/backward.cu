@@ -25,9 +25,9 @@
 //               Padding rows then contribute exactly nothing anywhere.
 //   prep        KK^T, QK^T (batched GEMM), T by forward substitution, Ph,
 //               W and U~ (batched GEMM).
-//   fwd_states  per (sequence, head, 32-row slice of S): the forward state
+//   fwd_states  per (sequence, head, 16-row slice of S): the forward state
 //               pass, storing every chunk's start state.
-//   rev_states  per (sequence, head, 32-row slice): the reverse pass over
+//   rev_states  per (sequence, head, 16-row slice): the reverse pass over
 //               chunks for dS; stores dS' and dU per chunk, dS0 at the end.
 //               Rows of dS are independent exactly as rows of S are.
 //   then batched 64-row GEMMs and three per-chunk elementwise kernels for the
@@ -38,10 +38,16 @@ namespace gdn {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kNS = 32;              // rows of S (or dS) per state-pass CTA
+constexpr int kNS = 16;              // rows of S (or dS) per state-pass CTA
+constexpr int kUS = kNS + 1;         // row stride of the C x kNS slice tiles
+constexpr int kCS = 64;              // dk columns of W / K staged at a time
+constexpr int kCSP = kCS + 1;        // their row stride
+constexpr int kRG = 256 / kNS;       // row groups of the C x kNS products (256 threads)
+constexpr int kRPT = kC / kRG;       // rows a thread owns in them
 constexpr int kPad = kDK + 1;
 constexpr int kCC = kC * kC;
-constexpr int kSlab = 16;            // rows of a 64 x 256 operand staged at a time
+constexpr int kSlabF = 32;           // rows of a 64 x 256 operand staged at a time (forward)
+constexpr int kSlabR = 8;            // ... (reverse, which stages two operands)
 
 // ------------------------------------------------------------------ scratch
 struct Bwd {
@@ -249,12 +255,12 @@ __global__ void __launch_bounds__(kThreads)
 fwd_states_kernel(const float* __restrict__ S0, SeqMap map, int32_t H, Bwd s) {
   extern __shared__ float sm[];
   float* Ss = sm;                   // [kNS][kPad]
-  float* Wt = Ss + kNS * kPad;      // [C][33]
-  float* Us = Wt + kC * 33;         // [C][33]
-  float* Ks = Us + kC * 33;         // [kSlab][256], 16-byte aligned
-  float* dec = Ks + kSlab * kDK;    // [C]
+  float* Wt = Ss + kNS * kPad;      // [C][kCSP]
+  float* Us = Wt + kC * kCSP;       // [C][kUS]
+  float* Ks = Us + kC * kUS;        // [kSlabF][256], 16-byte aligned
+  float* dec = Ks + kSlabF * kDK;   // [C]
   const int n = blockIdx.x, h = blockIdx.y, slice = blockIdx.z;
-  const int tid = threadIdx.x, i = tid & 31, rg = tid >> 5;
+  const int tid = threadIdx.x, i = tid % kNS, rg = tid / kNS;
   const int dv = s.dv;
   const int64_t sbase = ((int64_t)n * H + h) * dv * kDK + (int64_t)slice * kNS * kDK;
   for (int e = tid; e < kNS * kDK; e += kThreads)
@@ -270,26 +276,27 @@ fwd_states_kernel(const float* __restrict__ S0, SeqMap map, int32_t H, Bwd s) {
     if (tid < kC) dec[tid] = expf(GL - G[tid]);
     const float gL = expf(GL);
     // U = U~ - W S^T for rows rg*8 .. rg*8+7, column i of the slice
-    float acc[8];
+    float acc[kRPT];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+    for (int m = 0; m < kRPT; ++m) acc[m] = 0.f;
     const float* Wg = s.W + u * s.sD();
-    for (int c0 = 0; c0 < kDK; c0 += 32) {
+    for (int c0 = 0; c0 < kDK; c0 += kCS) {
       __syncthreads();
-      for (int e = tid; e < kC * 32; e += kThreads) Wt[(e >> 5) * 33 + (e & 31)] = Wg[(e >> 5) * kDK + c0 + (e & 31)];
+      for (int e = tid; e < kC * kCS; e += kThreads)
+        Wt[(e / kCS) * kCSP + e % kCS] = Wg[(e / kCS) * kDK + c0 + e % kCS];
       __syncthreads();
 #pragma unroll 4
-      for (int cc = 0; cc < 32; ++cc) {
+      for (int cc = 0; cc < kCS; ++cc) {
         const float sv = Ss[i * kPad + c0 + cc];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) acc[m] = fmaf(Wt[(rg * 8 + m) * 33 + cc], sv, acc[m]);
+        for (int m = 0; m < kRPT; ++m) acc[m] = fmaf(Wt[(rg * kRPT + m) * kCSP + cc], sv, acc[m]);
       }
     }
     const float* Ug = s.Ut + u * s.sV();
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int r = rg * 8 + m;
-      Us[r * 33 + i] = Ug[r * dv + slice * kNS + i] - acc[m];
+    for (int m = 0; m < kRPT; ++m) {
+      const int r = rg * kRPT + m;
+      Us[r * kUS + i] = Ug[r * dv + slice * kNS + i] - acc[m];
     }
     __syncthreads();
     // S' = gamma_L S + U^T diag(d) K, column c = tid; K staged 16 rows at a time
@@ -299,16 +306,16 @@ fwd_states_kernel(const float* __restrict__ S0, SeqMap map, int32_t H, Bwd s) {
       float a2[kNS];
 #pragma unroll
       for (int m = 0; m < kNS; ++m) a2[m] = 0.f;
-      for (int r0 = 0; r0 < kC; r0 += kSlab) {
+      for (int r0 = 0; r0 < kC; r0 += kSlabF) {
         __syncthreads();
-        for (int e = tid; e < kSlab * kDK / 4; e += kThreads)
+        for (int e = tid; e < kSlabF * kDK / 4; e += kThreads)
           reinterpret_cast<float4*>(Ks)[e] = Kg[r0 * kDK / 4 + e];
         __syncthreads();
 #pragma unroll 4
-        for (int r = 0; r < kSlab; ++r) {
+        for (int r = 0; r < kSlabF; ++r) {
           const float kd = dec[r0 + r] * Ks[r * kDK + c];
 #pragma unroll
-          for (int m = 0; m < kNS; ++m) a2[m] = fmaf(Us[(r0 + r) * 33 + m], kd, a2[m]);
+          for (int m = 0; m < kNS; ++m) a2[m] = fmaf(Us[(r0 + r) * kUS + m], kd, a2[m]);
         }
       }
 #pragma unroll
@@ -323,17 +330,17 @@ rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, S
                   int32_t H, Bwd s) {
   extern __shared__ float sm[];
   float* Ds = sm;                   // [kNS][kPad]  this CTA's rows of dS
-  float* Kt = Ds + kNS * kPad;      // [C][33]
-  float* Os = Kt + kC * 33;         // [C][33]  dO columns of the slice
-  float* Us = Os + kC * 33;         // [C][33]  dU columns of the slice
-  float* Qs = Us + kC * 33;         // [kSlab][256]
-  float* Ws = Qs + kSlab * kDK;     // [kSlab][256]
-  float* Pt = Ws + kSlab * kDK;     // [C][C + 1]
+  float* Kt = Ds + kNS * kPad;      // [C][kCSP]
+  float* Os = Kt + kC * kCSP;       // [C][kUS]  dO columns of the slice
+  float* Us = Os + kC * kUS;        // [C][kUS]  dU columns of the slice
+  float* Qs = Us + kC * kUS;        // [kSlabR][256], 16-byte aligned
+  float* Ws = Qs + kSlabR * kDK;    // [kSlabR][256]
+  float* Pt = Ws + kSlabR * kDK;    // [C][C + 1]
   float* dec = Pt + kC * (kC + 1);  // [C]
   float* gq = dec + kC;             // [C]  s * gamma_r
   float* red = gq + kC;             // [8]
   const int n = blockIdx.x, h = blockIdx.y, slice = blockIdx.z;
-  const int tid = threadIdx.x, i = tid & 31, rg = tid >> 5;
+  const int tid = threadIdx.x, i = tid % kNS, rg = tid / kNS;
   const int dv = s.dv;
   const int64_t sbase = ((int64_t)n * H + h) * dv * kDK + (int64_t)slice * kNS * kDK;
   for (int e = tid; e < kNS * kDK; e += kThreads)
@@ -353,7 +360,7 @@ rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, S
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    if (i == 0) red[rg] = part;
+    if ((tid & 31) == 0) red[tid >> 5] = part;
     const float* G = s.G + u * kC;
     const float GL = G[kC - 1];
     if (tid < kC) {
@@ -362,23 +369,25 @@ rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, S
     }
     const float gL = expf(GL);
     const float* Og = s.dO + u * s.sV();
-    for (int e = tid; e < kC * 32; e += kThreads) Os[(e >> 5) * 33 + (e & 31)] = Og[(e >> 5) * dv + slice * kNS + (e & 31)];
+    for (int e = tid; e < kC * kNS; e += kThreads)
+      Os[(e / kNS) * kUS + e % kNS] = Og[(e / kNS) * dv + slice * kNS + e % kNS];
     const float* Pg = s.Ph + u * kCC;
     for (int e = tid; e < kCC; e += kThreads) Pt[(e >> 6) * (kC + 1) + (e & 63)] = Pg[e];
     // K dS^T for rows rg*8 .. +7, column i
-    float acc[8];
+    float acc[kRPT];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+    for (int m = 0; m < kRPT; ++m) acc[m] = 0.f;
     const float* Kg = s.K + u * s.sD();
-    for (int c0 = 0; c0 < kDK; c0 += 32) {
+    for (int c0 = 0; c0 < kDK; c0 += kCS) {
       __syncthreads();
-      for (int e = tid; e < kC * 32; e += kThreads) Kt[(e >> 5) * 33 + (e & 31)] = Kg[(e >> 5) * kDK + c0 + (e & 31)];
+      for (int e = tid; e < kC * kCS; e += kThreads)
+        Kt[(e / kCS) * kCSP + e % kCS] = Kg[(e / kCS) * kDK + c0 + e % kCS];
       __syncthreads();
 #pragma unroll 4
-      for (int cc = 0; cc < 32; ++cc) {
+      for (int cc = 0; cc < kCS; ++cc) {
         const float dsv = Ds[i * kPad + c0 + cc];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) acc[m] = fmaf(Kt[(rg * 8 + m) * 33 + cc], dsv, acc[m]);
+        for (int m = 0; m < kRPT; ++m) acc[m] = fmaf(Kt[(rg * kRPT + m) * kCSP + cc], dsv, acc[m]);
       }
     }
     if (tid == 0) {
@@ -389,11 +398,11 @@ rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, S
     // dU = Ph^T dO + diag(d) K dS^T
     float* dUg = s.dU + u * s.sV();
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int r = rg * 8 + m;
+    for (int m = 0; m < kRPT; ++m) {
+      const int r = rg * kRPT + m;
       float x = dec[r] * acc[m];
-      for (int j = r; j < kC; ++j) x = fmaf(Pt[j * (kC + 1) + r], Os[j * 33 + i], x);
-      Us[r * 33 + i] = x;
+      for (int j = r; j < kC; ++j) x = fmaf(Pt[j * (kC + 1) + r], Os[j * kUS + i], x);
+      Us[r * kUS + i] = x;
       dUg[r * dv + slice * kNS + i] = x;
     }
     __syncthreads();
@@ -405,19 +414,19 @@ rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, S
       float a2[kNS];
 #pragma unroll
       for (int m = 0; m < kNS; ++m) a2[m] = 0.f;
-      for (int r0 = 0; r0 < kC; r0 += kSlab) {
+      for (int r0 = 0; r0 < kC; r0 += kSlabR) {
         __syncthreads();
-        for (int e = tid; e < kSlab * kDK / 4; e += kThreads) {
+        for (int e = tid; e < kSlabR * kDK / 4; e += kThreads) {
           reinterpret_cast<float4*>(Qs)[e] = Qg[r0 * kDK / 4 + e];
           reinterpret_cast<float4*>(Ws)[e] = Wg[r0 * kDK / 4 + e];
         }
         __syncthreads();
 #pragma unroll 4
-        for (int r = 0; r < kSlab; ++r) {
+        for (int r = 0; r < kSlabR; ++r) {
           const float qh = gq[r0 + r] * Qs[r * kDK + c], w = Ws[r * kDK + c];
 #pragma unroll
           for (int m = 0; m < kNS; ++m)
-            a2[m] = fmaf(Os[(r0 + r) * 33 + m], qh, fmaf(-Us[(r0 + r) * 33 + m], w, a2[m]));
+            a2[m] = fmaf(Os[(r0 + r) * kUS + m], qh, fmaf(-Us[(r0 + r) * kUS + m], w, a2[m]));
         }
       }
 #pragma unroll
@@ -562,9 +571,13 @@ cudaError_t gemm(cudaStream_t st, bool tA, bool tB, Mat A, Mat B, float* C, size
   return cudaGetLastError();
 }
 
-constexpr size_t kFwdSmem = sizeof(float) * (kNS * kPad + 2 * kC * 33 + kSlab * kDK + kC);
-constexpr size_t kRevSmem =
-    sizeof(float) * (kNS * kPad + 3 * kC * 33 + 2 * kSlab * kDK + kC * (kC + 1) + 2 * kC + 8);
+constexpr size_t kFwdSmem = sizeof(float) * (kNS * kPad + kC * kCSP + kC * kUS + kSlabF * kDK + kC);
+constexpr size_t kRevSmem = sizeof(float) * (kNS * kPad + kC * kCSP + 2 * kC * kUS +
+                                             2 * kSlabR * kDK + kC * (kC + 1) + 2 * kC + 8);
+static_assert((kNS * kPad + kC * kCSP + kC * kUS) % 4 == 0, "16-byte aligned slabs");
+static_assert((kNS * kPad + kC * kCSP + 2 * kC * kUS) % 4 == 0, "16-byte aligned slabs");
+static_assert(3 * (kRevSmem + 1024) <= 228 * 1024, "three reverse CTAs a SM");
+static_assert(kC * kNS % 256 == 0 && kRPT * kRG == kC, "thread mapping");
 
 }  // namespace
 
