@@ -150,7 +150,8 @@ gather_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
 }
 
 // ------------------------------------------------------------------ batched GEMM
-// C = alpha * colscale[n] * (A' B')[m][n] + beta * Cin[m][n], m < 64, per unit b.
+// C = alpha * colscale[n] * (A' B')[m][n] + beta * Cin[m][n], m < 64, per unit b;
+// K a multiple of 32, N of 64.
 // A' = A [64][K] (row stride lda) or, kTA, A stored [K][64];
 // B' = B [K][N] or, kTB, B stored [N][K].  mask 1: keep n <= m; 2: keep n < m.
 struct BG {
@@ -164,43 +165,99 @@ struct BG {
   int64_t batch;
 };
 
-template <bool kTA, bool kTB>
+// 64 x TN output tiles (TN = 128: 8 x 4 outputs a thread; TN = 64: 4 x 4), K
+// in slabs of 32 staged through shared memory, the next slab's global loads
+// (16-byte vectors along the contiguous axis) in registers while the current
+// slab computes.
+template <bool kTA, bool kTB, int TN>
 __global__ void __launch_bounds__(kThreads) bgemm_kernel(BG g) {
-  __shared__ __align__(16) float As[16][kC + 4];
-  __shared__ __align__(16) float Bs[16][kC + 4];
-  const int tid = threadIdx.x, tm = tid >> 4, tn = tid & 15;
-  const int n0 = blockIdx.x * kC;
+  constexpr int KS = 32;
+  constexpr int RM = TN == 128 ? 8 : 4;              // rows a thread
+  constexpr int TNG = TN / 4;                         // column groups of 4
+  constexpr int NA = KS * kC / 4 / kThreads;          // float4 loads of A a thread (2)
+  constexpr int NB = KS * TN / 4 / kThreads;          // ... of B (4 or 2)
+  __shared__ __align__(16) float As[KS][kC + 4];
+  __shared__ __align__(16) float Bs[KS][TN + 4];
+  const int tid = threadIdx.x, tm = tid / TNG, tn = tid % TNG;
+  const int n0 = blockIdx.x * TN;
   for (int64_t b = blockIdx.y; b < g.batch; b += gridDim.y) {
     const float* A = g.A + b * g.sA;
     const float* B = g.B + b * g.sB;
-    float acc[4][4];
+    float4 ra[NA], rb[NB];
+    auto load = [&](int k0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+      for (int j = 0; j < NA; ++j) {
+        const int idx = tid + j * kThreads;
+        ra[j] = !kTA ? *reinterpret_cast<const float4*>(A + (size_t)(idx >> 3) * g.lda + k0 + 4 * (idx & 7))
+                     : *reinterpret_cast<const float4*>(A + (size_t)(k0 + (idx >> 4)) * g.lda + 4 * (idx & 15));
+      }
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        const int idx = tid + j * kThreads;
+        rb[j] = !kTB ? *reinterpret_cast<const float4*>(B + (size_t)(k0 + idx / TNG) * g.ldb + n0 + 4 * (idx % TNG))
+                     : *reinterpret_cast<const float4*>(B + (size_t)(n0 + (idx >> 3)) * g.ldb + k0 + 4 * (idx & 7));
+      }
+    };
+    auto stage = [&]() {
+#pragma unroll
+      for (int j = 0; j < NA; ++j) {
+        const int idx = tid + j * kThreads;
+        if (!kTA) {
+          const int m = idx >> 3, q = idx & 7;
+          As[4 * q][m] = ra[j].x; As[4 * q + 1][m] = ra[j].y;
+          As[4 * q + 2][m] = ra[j].z; As[4 * q + 3][m] = ra[j].w;
+        } else {
+          *reinterpret_cast<float4*>(&As[idx >> 4][4 * (idx & 15)]) = ra[j];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        const int idx = tid + j * kThreads;
+        if (!kTB) {
+          *reinterpret_cast<float4*>(&Bs[idx / TNG][4 * (idx % TNG)]) = rb[j];
+        } else {
+          const int nn = idx >> 3, q = idx & 7;
+          Bs[4 * q][nn] = rb[j].x; Bs[4 * q + 1][nn] = rb[j].y;
+          Bs[4 * q + 2][nn] = rb[j].z; Bs[4 * q + 3][nn] = rb[j].w;
+        }
+      }
+    };
+    float acc[RM][4];
+#pragma unroll
+    for (int i = 0; i < RM; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-    for (int k0 = 0; k0 < g.K; k0 += 16) {
-      __syncthreads();
-      for (int e = tid; e < 16 * kC; e += kThreads) {
-        if (!kTA) { const int m = e >> 4, kk = e & 15; As[kk][m] = A[(size_t)m * g.lda + k0 + kk]; }
-        else      { const int kk = e >> 6, m = e & 63; As[kk][m] = A[(size_t)(k0 + kk) * g.lda + m]; }
-        if (!kTB) { const int kk = e >> 6, nn = e & 63; Bs[kk][nn] = B[(size_t)(k0 + kk) * g.ldb + n0 + nn]; }
-        else      { const int nn = e >> 4, kk = e & 15; Bs[kk][nn] = B[(size_t)(n0 + nn) * g.ldb + k0 + kk]; }
-      }
-      __syncthreads();
+    __syncthreads();                     // the previous unit's last slab is consumed
+    load(0);
+    stage();
+    __syncthreads();
+    for (int k0 = 0; k0 < g.K; k0 += KS) {
+      const bool more = k0 + KS < g.K;
+      if (more) load(k0 + KS);
 #pragma unroll
-      for (int kk = 0; kk < 16; ++kk) {
-        const float4 a = *reinterpret_cast<const float4*>(&As[kk][tm * 4]);
-        const float4 bb = *reinterpret_cast<const float4*>(&Bs[kk][tn * 4]);
-        const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {bb.x, bb.y, bb.z, bb.w};
+      for (int kk = 0; kk < KS; ++kk) {
+        float av[RM];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < RM; i += 4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(&As[kk][tm * RM + i]);
+          av[i] = a4.x; av[i + 1] = a4.y; av[i + 2] = a4.z; av[i + 3] = a4.w;
+        }
+        const float4 b4 = *reinterpret_cast<const float4*>(&Bs[kk][tn * 4]);
+        const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+        for (int i = 0; i < RM; ++i)
 #pragma unroll
           for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
       }
+      if (more) {
+        __syncthreads();
+        stage();
+        __syncthreads();
+      }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int m = tm * 4 + i;
+    for (int i = 0; i < RM; ++i) {
+      const int m = tm * RM + i;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int nn = n0 + tn * 4 + j;
@@ -562,11 +619,20 @@ cudaError_t gemm(cudaStream_t st, bool tA, bool tB, Mat A, Mat B, float* C, size
                  const float* col, size_t sCol, int64_t batch) {
   BG g{A.p, A.stride, A.ld, B.p, B.stride, B.ld, Cin, C, sC, ldc, col, sCol, N, K, alpha,
        beta, mask, batch};
-  dim3 grid((unsigned)(N / kC), (unsigned)(batch < 65535 ? batch : 65535));
-  if (!tA && !tB) bgemm_kernel<false, false><<<grid, kThreads, 0, st>>>(g);
-  else if (!tA && tB) bgemm_kernel<false, true><<<grid, kThreads, 0, st>>>(g);
-  else if (tA && !tB) bgemm_kernel<true, false><<<grid, kThreads, 0, st>>>(g);
-  else bgemm_kernel<true, true><<<grid, kThreads, 0, st>>>(g);
+  const unsigned by = (unsigned)(batch < 65535 ? batch : 65535);
+  if (N % 128 == 0) {
+    const dim3 grid((unsigned)(N / 128), by);
+    if (!tA && !tB) bgemm_kernel<false, false, 128><<<grid, kThreads, 0, st>>>(g);
+    else if (!tA && tB) bgemm_kernel<false, true, 128><<<grid, kThreads, 0, st>>>(g);
+    else if (tA && !tB) bgemm_kernel<true, false, 128><<<grid, kThreads, 0, st>>>(g);
+    else bgemm_kernel<true, true, 128><<<grid, kThreads, 0, st>>>(g);
+  } else {
+    const dim3 grid((unsigned)(N / 64), by);
+    if (!tA && !tB) bgemm_kernel<false, false, 64><<<grid, kThreads, 0, st>>>(g);
+    else if (!tA && tB) bgemm_kernel<false, true, 64><<<grid, kThreads, 0, st>>>(g);
+    else if (tA && !tB) bgemm_kernel<true, false, 64><<<grid, kThreads, 0, st>>>(g);
+    else bgemm_kernel<true, true, 64><<<grid, kThreads, 0, st>>>(g);
+  }
   count_launches(1);
   return cudaGetLastError();
 }
