@@ -39,12 +39,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kNS = 16;              // rows of S (or dS) per state-pass CTA
-constexpr int kUS = kNS + 1;         // row stride of the C x kNS slice tiles
-constexpr int kCS = 64;              // dk columns of W / K staged at a time
-constexpr int kCSP = kCS + 1;        // their row stride
 constexpr int kRG = 256 / kNS;       // row groups of the C x kNS products (256 threads)
 constexpr int kRPT = kC / kRG;       // rows a thread owns in them
-constexpr int kPad = kDK + 1;
 constexpr int kCC = kC * kC;
 constexpr int kSlabF = 32;           // rows of a 64 x 256 operand staged at a time (forward)
 constexpr int kSlabR = 8;            // ... (reverse, which stages two operands)
@@ -308,75 +304,91 @@ __global__ void __launch_bounds__(kThreads) tprep_kernel(Bwd s) {
 }
 
 // ------------------------------------------------------------------ forward states
+// Shared-memory rows are 16-byte multiples so that the inner products read
+// four values a load: ~5 loads per 16 FMAs.
+constexpr int kSP = kDK + 4;         // row stride of the S / dS slice
+constexpr int kWS = 68;              // row stride of a 64-column W slab (forward)
+constexpr int kKS = 32;              // dk columns of a K slab (reverse)
+constexpr int kKSP = kKS + 4;        // its row stride
+constexpr int kUP = kNS + 4;         // row stride of the C x kNS tiles
+constexpr int kPP = kC + 4;          // row stride of the staged Ph
+
 __global__ void __launch_bounds__(kThreads)
 fwd_states_kernel(const float* __restrict__ S0, SeqMap map, int32_t H, Bwd s) {
-  extern __shared__ float sm[];
-  float* Ss = sm;                   // [kNS][kPad]
-  float* Wt = Ss + kNS * kPad;      // [C][kCSP]
-  float* Us = Wt + kC * kCSP;       // [C][kUS]
-  float* Ks = Us + kC * kUS;        // [kSlabF][256], 16-byte aligned
+  extern __shared__ __align__(16) float sm[];
+  float* Ss = sm;                   // [kNS][kSP]
+  float* Wt = Ss + kNS * kSP;       // [C][kWS]  64 columns of W
+  float* Us = Wt + kC * kWS;        // [C][kUP]
+  float* Ks = Us + kC * kUP;        // [kSlabF][256]
   float* dec = Ks + kSlabF * kDK;   // [C]
   const int n = blockIdx.x, h = blockIdx.y, slice = blockIdx.z;
-  const int tid = threadIdx.x, i = tid % kNS, rg = tid / kNS;
+  const int tid = threadIdx.x, i = tid % kNS, r4 = (tid / kNS) * kRPT;
   const int dv = s.dv;
   const int64_t sbase = ((int64_t)n * H + h) * dv * kDK + (int64_t)slice * kNS * kDK;
   for (int e = tid; e < kNS * kDK; e += kThreads)
-    Ss[(e / kDK) * kPad + e % kDK] = S0 ? S0[sbase + e] : 0.f;
+    Ss[(e / kDK) * kSP + e % kDK] = S0 ? S0[sbase + e] : 0.f;
   const int64_t cb = map.chunk_begin(n), ce = map.chunk_end(n);
   for (int64_t ci = cb; ci < ce; ++ci) {
     const int64_t u = ci * H + h;
     __syncthreads();
     float* dst = s.Sst + u * s.sS() + (size_t)slice * kNS * kDK;
-    for (int e = tid; e < kNS * kDK; e += kThreads) dst[e] = Ss[(e / kDK) * kPad + e % kDK];
+    for (int e = tid; e < kNS * kDK; e += kThreads) dst[e] = Ss[(e / kDK) * kSP + e % kDK];
     const float* G = s.G + u * kC;
     const float GL = G[kC - 1];
     if (tid < kC) dec[tid] = expf(GL - G[tid]);
     const float gL = expf(GL);
-    // U = U~ - W S^T for rows rg*8 .. rg*8+7, column i of the slice
+    // U = U~ - W S^T: rows r4 .. r4+3, column i; 4 columns of dk a step
     float acc[kRPT];
 #pragma unroll
     for (int m = 0; m < kRPT; ++m) acc[m] = 0.f;
     const float* Wg = s.W + u * s.sD();
-    for (int c0 = 0; c0 < kDK; c0 += kCS) {
+    for (int c0 = 0; c0 < kDK; c0 += 64) {
       __syncthreads();
-      for (int e = tid; e < kC * kCS; e += kThreads)
-        Wt[(e / kCS) * kCSP + e % kCS] = Wg[(e / kCS) * kDK + c0 + e % kCS];
+      for (int e = tid; e < kC * 16; e += kThreads)
+        *reinterpret_cast<float4*>(&Wt[(e >> 4) * kWS + 4 * (e & 15)]) =
+            *reinterpret_cast<const float4*>(Wg + (e >> 4) * kDK + c0 + 4 * (e & 15));
       __syncthreads();
 #pragma unroll 4
-      for (int cc = 0; cc < kCS; ++cc) {
-        const float sv = Ss[i * kPad + c0 + cc];
+      for (int cc = 0; cc < 64; cc += 4) {
+        const float4 sv = *reinterpret_cast<const float4*>(&Ss[i * kSP + c0 + cc]);
 #pragma unroll
-        for (int m = 0; m < kRPT; ++m) acc[m] = fmaf(Wt[(rg * kRPT + m) * kCSP + cc], sv, acc[m]);
+        for (int m = 0; m < kRPT; ++m) {
+          const float4 w = *reinterpret_cast<const float4*>(&Wt[(r4 + m) * kWS + cc]);
+          acc[m] = fmaf(w.x, sv.x, fmaf(w.y, sv.y, fmaf(w.z, sv.z, fmaf(w.w, sv.w, acc[m]))));
+        }
       }
     }
     const float* Ug = s.Ut + u * s.sV();
 #pragma unroll
-    for (int m = 0; m < kRPT; ++m) {
-      const int r = rg * kRPT + m;
-      Us[r * kUS + i] = Ug[r * dv + slice * kNS + i] - acc[m];
-    }
-    __syncthreads();
-    // S' = gamma_L S + U^T diag(d) K, column c = tid; K staged 16 rows at a time
+    for (int m = 0; m < kRPT; ++m) Us[(r4 + m) * kUP + i] = Ug[(r4 + m) * dv + slice * kNS + i] - acc[m];
+    // S' = gamma_L S + U^T diag(d) K: column c = tid, the slice's kNS rows
     {
       const int c = tid;
       const float4* Kg = reinterpret_cast<const float4*>(s.K + u * s.sD());
       float a2[kNS];
 #pragma unroll
       for (int m = 0; m < kNS; ++m) a2[m] = 0.f;
-      for (int r0 = 0; r0 < kC; r0 += kSlabF) {
+      for (int q0 = 0; q0 < kC; q0 += kSlabF) {
         __syncthreads();
         for (int e = tid; e < kSlabF * kDK / 4; e += kThreads)
-          reinterpret_cast<float4*>(Ks)[e] = Kg[r0 * kDK / 4 + e];
+          reinterpret_cast<float4*>(Ks)[e] = Kg[q0 * kDK / 4 + e];
         __syncthreads();
-#pragma unroll 4
+#pragma unroll 2
         for (int r = 0; r < kSlabF; ++r) {
-          const float kd = dec[r0 + r] * Ks[r * kDK + c];
+          const float kd = dec[q0 + r] * Ks[r * kDK + c];
+          const float4* ur = reinterpret_cast<const float4*>(&Us[(q0 + r) * kUP]);
 #pragma unroll
-          for (int m = 0; m < kNS; ++m) a2[m] = fmaf(Us[(r0 + r) * kUS + m], kd, a2[m]);
+          for (int m4 = 0; m4 < kNS / 4; ++m4) {
+            const float4 u4 = ur[m4];
+            a2[4 * m4] = fmaf(u4.x, kd, a2[4 * m4]);
+            a2[4 * m4 + 1] = fmaf(u4.y, kd, a2[4 * m4 + 1]);
+            a2[4 * m4 + 2] = fmaf(u4.z, kd, a2[4 * m4 + 2]);
+            a2[4 * m4 + 3] = fmaf(u4.w, kd, a2[4 * m4 + 3]);
+          }
         }
       }
 #pragma unroll
-      for (int m = 0; m < kNS; ++m) Ss[m * kPad + c] = fmaf(gL, Ss[m * kPad + c], a2[m]);
+      for (int m = 0; m < kNS; ++m) Ss[m * kSP + c] = fmaf(gL, Ss[m * kSP + c], a2[m]);
     }
   }
 }
@@ -385,23 +397,23 @@ fwd_states_kernel(const float* __restrict__ S0, SeqMap map, int32_t H, Bwd s) {
 __global__ void __launch_bounds__(kThreads)
 rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, SeqMap map,
                   int32_t H, Bwd s) {
-  extern __shared__ float sm[];
-  float* Ds = sm;                   // [kNS][kPad]  this CTA's rows of dS
-  float* Kt = Ds + kNS * kPad;      // [C][kCSP]
-  float* Os = Kt + kC * kCSP;       // [C][kUS]  dO columns of the slice
-  float* Us = Os + kC * kUS;        // [C][kUS]  dU columns of the slice
-  float* Qs = Us + kC * kUS;        // [kSlabR][256], 16-byte aligned
+  extern __shared__ __align__(16) float sm[];
+  float* Ds = sm;                   // [kNS][kSP]  this CTA's rows of dS
+  float* Kt = Ds + kNS * kSP;       // [C][kKSP]   32 columns of K
+  float* Os = Kt + kC * kKSP;       // [C][kUP]    dO columns of the slice
+  float* Us = Os + kC * kUP;        // [C][kUP]    dU columns of the slice
+  float* Qs = Us + kC * kUP;        // [kSlabR][256]
   float* Ws = Qs + kSlabR * kDK;    // [kSlabR][256]
-  float* Pt = Ws + kSlabR * kDK;    // [C][C + 1]
-  float* dec = Pt + kC * (kC + 1);  // [C]
+  float* Pt = Ws + kSlabR * kDK;    // [C][kPP]
+  float* dec = Pt + kC * kPP;       // [C]
   float* gq = dec + kC;             // [C]  s * gamma_r
   float* red = gq + kC;             // [8]
   const int n = blockIdx.x, h = blockIdx.y, slice = blockIdx.z;
-  const int tid = threadIdx.x, i = tid % kNS, rg = tid / kNS;
+  const int tid = threadIdx.x, i = tid % kNS, r4 = (tid / kNS) * kRPT;
   const int dv = s.dv;
   const int64_t sbase = ((int64_t)n * H + h) * dv * kDK + (int64_t)slice * kNS * kDK;
   for (int e = tid; e < kNS * kDK; e += kThreads)
-    Ds[(e / kDK) * kPad + e % kDK] = dS_final ? dS_final[sbase + e] : 0.f;
+    Ds[(e / kDK) * kSP + e % kDK] = dS_final ? dS_final[sbase + e] : 0.f;
   const int64_t cb = map.chunk_begin(n), ce = map.chunk_end(n);
   for (int64_t ci = ce - 1; ci >= cb; --ci) {
     const int64_t u = ci * H + h;
@@ -411,7 +423,7 @@ rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, S
     const float* Sg = s.Sst + u * s.sS() + (size_t)slice * kNS * kDK;
     float part = 0.f;
     for (int e = tid; e < kNS * kDK; e += kThreads) {
-      const float d = Ds[(e / kDK) * kPad + e % kDK];
+      const float d = Ds[(e / kDK) * kSP + e % kDK];
       dst[e] = d;
       part = fmaf(d, Sg[e], part);
     }
@@ -427,24 +439,30 @@ rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, S
     const float gL = expf(GL);
     const float* Og = s.dO + u * s.sV();
     for (int e = tid; e < kC * kNS; e += kThreads)
-      Os[(e / kNS) * kUS + e % kNS] = Og[(e / kNS) * dv + slice * kNS + e % kNS];
+      Os[(e / kNS) * kUP + e % kNS] = Og[(e / kNS) * dv + slice * kNS + e % kNS];
     const float* Pg = s.Ph + u * kCC;
-    for (int e = tid; e < kCC; e += kThreads) Pt[(e >> 6) * (kC + 1) + (e & 63)] = Pg[e];
-    // K dS^T for rows rg*8 .. +7, column i
+    for (int e = tid; e < kCC / 4; e += kThreads)
+      *reinterpret_cast<float4*>(&Pt[(e >> 4) * kPP + 4 * (e & 15)]) =
+          *reinterpret_cast<const float4*>(Pg + 4 * e);
+    // K dS^T for rows r4 .. r4+3, column i
     float acc[kRPT];
 #pragma unroll
     for (int m = 0; m < kRPT; ++m) acc[m] = 0.f;
     const float* Kg = s.K + u * s.sD();
-    for (int c0 = 0; c0 < kDK; c0 += kCS) {
+    for (int c0 = 0; c0 < kDK; c0 += kKS) {
       __syncthreads();
-      for (int e = tid; e < kC * kCS; e += kThreads)
-        Kt[(e / kCS) * kCSP + e % kCS] = Kg[(e / kCS) * kDK + c0 + e % kCS];
+      for (int e = tid; e < kC * kKS / 4; e += kThreads)
+        *reinterpret_cast<float4*>(&Kt[(e / (kKS / 4)) * kKSP + 4 * (e % (kKS / 4))]) =
+            *reinterpret_cast<const float4*>(Kg + (e / (kKS / 4)) * kDK + c0 + 4 * (e % (kKS / 4)));
       __syncthreads();
-#pragma unroll 4
-      for (int cc = 0; cc < kCS; ++cc) {
-        const float dsv = Ds[i * kPad + c0 + cc];
 #pragma unroll
-        for (int m = 0; m < kRPT; ++m) acc[m] = fmaf(Kt[(rg * kRPT + m) * kCSP + cc], dsv, acc[m]);
+      for (int cc = 0; cc < kKS; cc += 4) {
+        const float4 dsv = *reinterpret_cast<const float4*>(&Ds[i * kSP + c0 + cc]);
+#pragma unroll
+        for (int m = 0; m < kRPT; ++m) {
+          const float4 kk = *reinterpret_cast<const float4*>(&Kt[(r4 + m) * kKSP + cc]);
+          acc[m] = fmaf(kk.x, dsv.x, fmaf(kk.y, dsv.y, fmaf(kk.z, dsv.z, fmaf(kk.w, dsv.w, acc[m]))));
+        }
       }
     }
     if (tid == 0) {
@@ -452,18 +470,28 @@ rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, S
       for (int w = 0; w < kThreads / 32; ++w) t += red[w];
       s.dgLp[u * (dv / kNS) + slice] = t;
     }
-    // dU = Ph^T dO + diag(d) K dS^T
+    // dU = Ph^T dO + diag(d) K dS^T; Ph[j][r] = 0 for j < r
     float* dUg = s.dU + u * s.sV();
+    {
+      float x[kRPT];
 #pragma unroll
-    for (int m = 0; m < kRPT; ++m) {
-      const int r = rg * kRPT + m;
-      float x = dec[r] * acc[m];
-      for (int j = r; j < kC; ++j) x = fmaf(Pt[j * (kC + 1) + r], Os[j * kUS + i], x);
-      Us[r * kUS + i] = x;
-      dUg[r * dv + slice * kNS + i] = x;
+      for (int m = 0; m < kRPT; ++m) x[m] = dec[r4 + m] * acc[m];
+      for (int j = r4; j < kC; ++j) {
+        const float4 p = *reinterpret_cast<const float4*>(&Pt[j * kPP + r4]);
+        const float o = Os[j * kUP + i];
+        x[0] = fmaf(p.x, o, x[0]);
+        x[1] = fmaf(p.y, o, x[1]);
+        x[2] = fmaf(p.z, o, x[2]);
+        x[3] = fmaf(p.w, o, x[3]);
+      }
+#pragma unroll
+      for (int m = 0; m < kRPT; ++m) {
+        Us[(r4 + m) * kUP + i] = x[m];
+        dUg[(r4 + m) * dv + slice * kNS + i] = x[m];
+      }
     }
     __syncthreads();
-    // dS = gamma_L dS' + dO^T Qh - dU^T W, column c = tid; Q and W staged 16 rows at a time
+    // dS = gamma_L dS' + dO^T Qh - dU^T W, column c = tid; Q and W staged kSlabR rows at a time
     {
       const int c = tid;
       const float4* Qg = reinterpret_cast<const float4*>(s.Q + u * s.sD());
@@ -471,28 +499,35 @@ rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, S
       float a2[kNS];
 #pragma unroll
       for (int m = 0; m < kNS; ++m) a2[m] = 0.f;
-      for (int r0 = 0; r0 < kC; r0 += kSlabR) {
+      for (int q0 = 0; q0 < kC; q0 += kSlabR) {
         __syncthreads();
         for (int e = tid; e < kSlabR * kDK / 4; e += kThreads) {
-          reinterpret_cast<float4*>(Qs)[e] = Qg[r0 * kDK / 4 + e];
-          reinterpret_cast<float4*>(Ws)[e] = Wg[r0 * kDK / 4 + e];
+          reinterpret_cast<float4*>(Qs)[e] = Qg[q0 * kDK / 4 + e];
+          reinterpret_cast<float4*>(Ws)[e] = Wg[q0 * kDK / 4 + e];
         }
         __syncthreads();
-#pragma unroll 4
+#pragma unroll 2
         for (int r = 0; r < kSlabR; ++r) {
-          const float qh = gq[r0 + r] * Qs[r * kDK + c], w = Ws[r * kDK + c];
+          const float qh = gq[q0 + r] * Qs[r * kDK + c], w = Ws[r * kDK + c];
+          const float4* orow = reinterpret_cast<const float4*>(&Os[(q0 + r) * kUP]);
+          const float4* urow = reinterpret_cast<const float4*>(&Us[(q0 + r) * kUP]);
 #pragma unroll
-          for (int m = 0; m < kNS; ++m)
-            a2[m] = fmaf(Os[(r0 + r) * kUS + m], qh, fmaf(-Us[(r0 + r) * kUS + m], w, a2[m]));
+          for (int m4 = 0; m4 < kNS / 4; ++m4) {
+            const float4 o4 = orow[m4], u4 = urow[m4];
+            a2[4 * m4] = fmaf(o4.x, qh, fmaf(-u4.x, w, a2[4 * m4]));
+            a2[4 * m4 + 1] = fmaf(o4.y, qh, fmaf(-u4.y, w, a2[4 * m4 + 1]));
+            a2[4 * m4 + 2] = fmaf(o4.z, qh, fmaf(-u4.z, w, a2[4 * m4 + 2]));
+            a2[4 * m4 + 3] = fmaf(o4.w, qh, fmaf(-u4.w, w, a2[4 * m4 + 3]));
+          }
         }
       }
 #pragma unroll
-      for (int m = 0; m < kNS; ++m) Ds[m * kPad + c] = fmaf(gL, Ds[m * kPad + c], a2[m]);
+      for (int m = 0; m < kNS; ++m) Ds[m * kSP + c] = fmaf(gL, Ds[m * kSP + c], a2[m]);
     }
   }
   __syncthreads();
   if (dS0)
-    for (int e = tid; e < kNS * kDK; e += kThreads) dS0[sbase + e] = Ds[(e / kDK) * kPad + e % kDK];
+    for (int e = tid; e < kNS * kDK; e += kThreads) dS0[sbase + e] = Ds[(e / kDK) * kSP + e % kDK];
 }
 
 // ------------------------------------------------------------------ C x C terms
@@ -637,13 +672,16 @@ cudaError_t gemm(cudaStream_t st, bool tA, bool tB, Mat A, Mat B, float* C, size
   return cudaGetLastError();
 }
 
-constexpr size_t kFwdSmem = sizeof(float) * (kNS * kPad + kC * kCSP + kC * kUS + kSlabF * kDK + kC);
-constexpr size_t kRevSmem = sizeof(float) * (kNS * kPad + kC * kCSP + 2 * kC * kUS +
-                                             2 * kSlabR * kDK + kC * (kC + 1) + 2 * kC + 8);
-static_assert((kNS * kPad + kC * kCSP + kC * kUS) % 4 == 0, "16-byte aligned slabs");
-static_assert((kNS * kPad + kC * kCSP + 2 * kC * kUS) % 4 == 0, "16-byte aligned slabs");
-static_assert(3 * (kRevSmem + 1024) <= 228 * 1024, "three reverse CTAs a SM");
-static_assert(kC * kNS % 256 == 0 && kRPT * kRG == kC, "thread mapping");
+constexpr size_t kFwdSmem = sizeof(float) * (kNS * kSP + kC * kWS + kC * kUP + kSlabF * kDK + kC);
+constexpr size_t kRevSmem = sizeof(float) * (kNS * kSP + kC * kKSP + 2 * kC * kUP +
+                                             2 * kSlabR * kDK + kC * kPP + 2 * kC + 8);
+static_assert(kSP % 4 == 0 && kWS % 4 == 0 && kKSP % 4 == 0 && kUP % 4 == 0 && kPP % 4 == 0,
+              "16-byte rows");
+static_assert((kNS * kSP + kC * kWS + kC * kUP) % 4 == 0, "16-byte aligned slab");
+static_assert((kNS * kSP + kC * kKSP + 2 * kC * kUP) % 4 == 0, "16-byte aligned slabs");
+static_assert(kRPT == 4 && kNS % 4 == 0, "thread mapping of the state passes");
+static_assert(3 * (kFwdSmem + 1024) <= 228 * 1024 && 3 * (kRevSmem + 1024) <= 228 * 1024,
+              "three state-pass CTAs a SM");
 
 }  // namespace
 
