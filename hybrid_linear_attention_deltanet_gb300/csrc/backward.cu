@@ -342,12 +342,26 @@ fwd_states_kernel(const float* __restrict__ S0, SeqMap map, int32_t H, Bwd s) {
 #pragma unroll
     for (int m = 0; m < kRPT; ++m) acc[m] = 0.f;
     const float* Wg = s.W + u * s.sD();
+    // the next 64 columns of W are in flight (registers) while a slab computes
+    constexpr int kWL = kC * 16 / kThreads;          // float4 loads a thread a slab
+    float4 wpre[kWL];
+    auto load_w = [&](int c0) {
+#pragma unroll
+      for (int j = 0; j < kWL; ++j) {
+        const int e = tid + j * kThreads;
+        wpre[j] = *reinterpret_cast<const float4*>(Wg + (e >> 4) * kDK + c0 + 4 * (e & 15));
+      }
+    };
+    load_w(0);
     for (int c0 = 0; c0 < kDK; c0 += 64) {
       __syncthreads();
-      for (int e = tid; e < kC * 16; e += kThreads)
-        *reinterpret_cast<float4*>(&Wt[(e >> 4) * kWS + 4 * (e & 15)]) =
-            *reinterpret_cast<const float4*>(Wg + (e >> 4) * kDK + c0 + 4 * (e & 15));
+#pragma unroll
+      for (int j = 0; j < kWL; ++j) {
+        const int e = tid + j * kThreads;
+        *reinterpret_cast<float4*>(&Wt[(e >> 4) * kWS + 4 * (e & 15)]) = wpre[j];
+      }
       __syncthreads();
+      if (c0 + 64 < kDK) load_w(c0 + 64);
 #pragma unroll 4
       for (int cc = 0; cc < 64; cc += 4) {
         const float4 sv = *reinterpret_cast<const float4*>(&Ss[i * kSP + c0 + cc]);
@@ -368,11 +382,19 @@ fwd_states_kernel(const float* __restrict__ S0, SeqMap map, int32_t H, Bwd s) {
       float a2[kNS];
 #pragma unroll
       for (int m = 0; m < kNS; ++m) a2[m] = 0.f;
+      constexpr int kKL = kSlabF * kDK / 4 / kThreads;
+      float4 kpre[kKL];
+      auto load_k = [&](int q0) {
+#pragma unroll
+        for (int j = 0; j < kKL; ++j) kpre[j] = Kg[q0 * kDK / 4 + tid + j * kThreads];
+      };
+      load_k(0);
       for (int q0 = 0; q0 < kC; q0 += kSlabF) {
         __syncthreads();
-        for (int e = tid; e < kSlabF * kDK / 4; e += kThreads)
-          reinterpret_cast<float4*>(Ks)[e] = Kg[q0 * kDK / 4 + e];
+#pragma unroll
+        for (int j = 0; j < kKL; ++j) reinterpret_cast<float4*>(Ks)[tid + j * kThreads] = kpre[j];
         __syncthreads();
+        if (q0 + kSlabF < kC) load_k(q0 + kSlabF);
 #pragma unroll 2
         for (int r = 0; r < kSlabF; ++r) {
           const float kd = dec[q0 + r] * Ks[r * kDK + c];
@@ -449,12 +471,25 @@ rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, S
 #pragma unroll
     for (int m = 0; m < kRPT; ++m) acc[m] = 0.f;
     const float* Kg = s.K + u * s.sD();
+    constexpr int kKL = kC * kKS / 4 / kThreads;     // float4 loads a thread a slab
+    float4 kpre[kKL];
+    auto load_k = [&](int c0) {
+#pragma unroll
+      for (int j = 0; j < kKL; ++j) {
+        const int e = tid + j * kThreads;
+        kpre[j] = *reinterpret_cast<const float4*>(Kg + (e / (kKS / 4)) * kDK + c0 + 4 * (e % (kKS / 4)));
+      }
+    };
+    load_k(0);
     for (int c0 = 0; c0 < kDK; c0 += kKS) {
       __syncthreads();
-      for (int e = tid; e < kC * kKS / 4; e += kThreads)
-        *reinterpret_cast<float4*>(&Kt[(e / (kKS / 4)) * kKSP + 4 * (e % (kKS / 4))]) =
-            *reinterpret_cast<const float4*>(Kg + (e / (kKS / 4)) * kDK + c0 + 4 * (e % (kKS / 4)));
+#pragma unroll
+      for (int j = 0; j < kKL; ++j) {
+        const int e = tid + j * kThreads;
+        *reinterpret_cast<float4*>(&Kt[(e / (kKS / 4)) * kKSP + 4 * (e % (kKS / 4))]) = kpre[j];
+      }
       __syncthreads();
+      if (c0 + kKS < kDK) load_k(c0 + kKS);
 #pragma unroll
       for (int cc = 0; cc < kKS; cc += 4) {
         const float4 dsv = *reinterpret_cast<const float4*>(&Ds[i * kSP + c0 + cc]);
@@ -499,13 +534,25 @@ rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, S
       float a2[kNS];
 #pragma unroll
       for (int m = 0; m < kNS; ++m) a2[m] = 0.f;
+      constexpr int kQL = kSlabR * kDK / 4 / kThreads;
+      float4 qpre[kQL], wpre[kQL];
+      auto load_qw = [&](int q0) {
+#pragma unroll
+        for (int j = 0; j < kQL; ++j) {
+          qpre[j] = Qg[q0 * kDK / 4 + tid + j * kThreads];
+          wpre[j] = Wg[q0 * kDK / 4 + tid + j * kThreads];
+        }
+      };
+      load_qw(0);
       for (int q0 = 0; q0 < kC; q0 += kSlabR) {
         __syncthreads();
-        for (int e = tid; e < kSlabR * kDK / 4; e += kThreads) {
-          reinterpret_cast<float4*>(Qs)[e] = Qg[q0 * kDK / 4 + e];
-          reinterpret_cast<float4*>(Ws)[e] = Wg[q0 * kDK / 4 + e];
+#pragma unroll
+        for (int j = 0; j < kQL; ++j) {
+          reinterpret_cast<float4*>(Qs)[tid + j * kThreads] = qpre[j];
+          reinterpret_cast<float4*>(Ws)[tid + j * kThreads] = wpre[j];
         }
         __syncthreads();
+        if (q0 + kSlabR < kC) load_qw(q0 + kSlabR);
 #pragma unroll 2
         for (int r = 0; r < kSlabR; ++r) {
           const float qh = gq[q0 + r] * Qs[r * kDK + c], w = Ws[r * kDK + c];
@@ -680,6 +727,9 @@ static_assert(kSP % 4 == 0 && kWS % 4 == 0 && kKSP % 4 == 0 && kUP % 4 == 0 && k
 static_assert((kNS * kSP + kC * kWS + kC * kUP) % 4 == 0, "16-byte aligned slab");
 static_assert((kNS * kSP + kC * kKSP + 2 * kC * kUP) % 4 == 0, "16-byte aligned slabs");
 static_assert(kRPT == 4 && kNS % 4 == 0, "thread mapping of the state passes");
+static_assert(kC * 16 % kThreads == 0 && kSlabF * kDK / 4 % kThreads == 0 &&
+              kC * kKS / 4 % kThreads == 0 && kSlabR * kDK / 4 % kThreads == 0,
+              "whole float4 loads a thread for every staged slab");
 static_assert(3 * (kFwdSmem + 1024) <= 228 * 1024 && 3 * (kRevSmem + 1024) <= 228 * 1024,
               "three state-pass CTAs a SM");
 

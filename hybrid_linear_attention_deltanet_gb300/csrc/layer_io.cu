@@ -26,7 +26,7 @@ constexpr int kHist = kTaps - 1;    // inputs carried across calls per channel
 constexpr int kSeg = 256;           // channels per warp unit (one q/k head)
 constexpr int kTile = 64;           // tokens one warp walks in the prefill form
 // tokens whose loads one lane keeps in flight together (16 B each at bf16)
-template <typename T> __host__ __device__ constexpr int group_of() { return sizeof(T) == 2 ? 4 : 2; }
+template <typename T> __host__ __device__ constexpr int group_of() { return 2; }
 constexpr int kWarpsPerCta = 8;
 constexpr float kL2Eps = 1e-6f;
 
