@@ -263,13 +263,16 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   PrefillLaunch a{};
   a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.S0 = S0; a.H = heads;
   a.status = status; a.dv = dv;
+  // the backward's scratch starts 1024-byte aligned (the tensor-core forward
+  // it may run stages images with bulk copies)
   a.map.cu_seqlens = cu_seqlens;
   a.map.N = batch;
   a.map.T = varlen ? T_total : seqlen;
   a.map.chunks_per_seq = varlen ? 0 : (seqlen + kC - 1) / kC;
   a.max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
-  const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
-  const size_t work_bytes = prefill_backward_scratch_bytes(a.max_chunks, heads, dv);
+  const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 1024) : 0;
+  const size_t work_bytes =
+      prefill_backward_scratch_bytes(a.max_chunks, heads, dv, T_total, io_dtype);
   void* scratch = nullptr;
   if (!scratch_pool() ||
       cudaMallocFromPoolAsync(&scratch, off_bytes + work_bytes, scratch_pool(), stream) !=

@@ -26,7 +26,8 @@
 //   prep        KK^T, QK^T (batched GEMM), T by forward substitution, Ph,
 //               W and U~ (batched GEMM).
 //   fwd_states  per (sequence, head, 16-row slice of S): the forward state
-//               pass, storing every chunk's start state.
+//               pass, storing every chunk's start state (fp32 I/O; with bf16
+//               I/O the tensor-core forward of gdn_prefill stores them).
 //   rev_states  per (sequence, head, 16-row slice): the reverse pass over
 //               chunks for dS; stores dS' and dU per chunk, dS0 at the end.
 //               Rows of dS are independent exactly as rows of S are.
@@ -735,8 +736,13 @@ static_assert(3 * (kFwdSmem + 1024) <= 228 * 1024 && 3 * (kRevSmem + 1024) <= 22
 
 }  // namespace
 
-size_t prefill_backward_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv) {
-  return bwd_scratch_bytes(max_chunks * H, dv);
+size_t prefill_backward_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv, int64_t T_total,
+                                      int io_dtype) {
+  size_t b = align_up(bwd_scratch_bytes(max_chunks * H, dv), 1024);
+  if (io_dtype == GDN_BF16)
+    b += align_up(prefill_tc_scratch_bytes(max_chunks, H, dv), 1024) +
+         align_up((size_t)T_total * H * dv * 2, 1024);
+  return b;
 }
 
 cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
@@ -781,9 +787,22 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
                   nullptr, 0.f, 0, nullptr, 0, units)) != cudaSuccess) return e;
   }
   const dim3 gs((unsigned)a.map.N, (unsigned)a.H, (unsigned)(dv / kNS));
-  fwd_states_kernel<<<gs, kThreads, kFwdSmem, st>>>(a.S0, a.map, a.H, s);
-  count_launches(1);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (io_dtype == GDN_BF16) {
+    // chunk-start states from the tensor-core forward (bf16 operands, fp32
+    // state), its output discarded
+    char* extra = (char*)a.scratch + align_up(bwd_scratch_bytes(units, dv), 1024);
+    PrefillLaunch f = a;
+    f.scratch = extra;
+    f.out = extra + align_up(prefill_tc_scratch_bytes(a.max_chunks, a.H, dv), 1024);
+    f.S_final = nullptr;
+    f.allow_overlap = true;
+    f.state_dump = s.Sst;
+    if ((e = launch_prefill_tc(f, st)) != cudaSuccess) return e;
+  } else {
+    fwd_states_kernel<<<gs, kThreads, kFwdSmem, st>>>(a.S0, a.map, a.H, s);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   rev_states_kernel<<<gs, kThreads, kRevSmem, st>>>(dS_final, dS0, a.map, a.H, s);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -6,8 +6,11 @@
 
 namespace gdn {
 
-// Device scratch the backward of a call with this many chunks needs.
-size_t prefill_backward_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv);
+// Device scratch the backward of a call with this many chunks (and T_total
+// tokens) needs.  With bf16 I/O it includes the tensor-core forward's scratch
+// and a throwaway output: that forward re-run stores every chunk's start state.
+size_t prefill_backward_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv, int64_t T_total,
+                                      int io_dtype);
 
 // a: the forward's arguments (q, k, v, alpha, beta, S0, map, H, dv,
 // max_chunks, scratch of prefill_backward_scratch_bytes); out and S_final unused.

@@ -109,6 +109,8 @@ struct PrefillLaunch {
   unsigned* status;
   void* scratch;        // device scratch of the size the path's *_scratch_bytes asks for
   bool allow_overlap;   // tensor-core path may run prep and state pass in one cooperative launch
+  float* state_dump;    // tensor-core path: every chunk's start state, [chunks * H][dv][dk]
+                        // fp32 (the backward's forward re-run), or nullptr
 };
 
 cudaError_t launch_chunk_offsets(const int32_t* cu_seqlens, int32_t N, int64_t T_total,

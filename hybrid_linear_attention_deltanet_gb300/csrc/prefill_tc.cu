@@ -727,7 +727,8 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
                                            int32_t H, const uint8_t* __restrict__ scratch,
                                            const uint32_t* ready, unsigned* status,
                                            uint64_t* __restrict__ trace, int32_t trace_chunks,
-                                           int32_t dv, int n, int h, int slice) {
+                                           int32_t dv, int n, int h, int slice,
+                                           float* __restrict__ sdump) {
   const int unit = (n * H + h) * (dv / 128) + slice;
   const bool timed = trace && threadIdx.x == 0 && unit < kMaxTracedUnits;
   if (timed) trace[kUnitTimes + 3 * unit] = globaltimer_ns();
@@ -984,6 +985,13 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     stamp(it, 1);
     // the previous chunk's output rows go out while MMA-1 runs
     if (it > 0) copy_out_prev(buf ^ 1);
+    // (optional) this chunk's start state, for the backward's forward re-run
+    if (sdump) {
+      float4* p = reinterpret_cast<float4*>(
+          sdump + ((size_t)(ci * H + h) * dv + 128 * slice + iloc) * kDK + 128 * colhalf);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) p[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+    }
     // 2. U = U~ - D_U (columns r = 32 colhalf ..), and d_r U: bf16 A operands in TMEM
     float gC = 0.f;
     if (!mbar_wait(&bar_m1, par) || !mbar_wait(&bar_u, par)) {
@@ -1170,10 +1178,11 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restrict__ S0,
                 __nv_bfloat16* __restrict__ out, float* __restrict__ S_final, SeqMap map,
                 int32_t H, const uint8_t* __restrict__ scratch, unsigned* status,
-                uint64_t* __restrict__ trace, int32_t trace_chunks, int32_t dv) {
+                uint64_t* __restrict__ trace, int32_t trace_chunks, int32_t dv,
+                float* __restrict__ sdump) {
   extern __shared__ uint8_t smem_raw[];
   state_role<false>(align_smem_1024(smem_raw), &tm_k, S0, out, S_final, map, H, scratch, nullptr,
-                    status, trace, trace_chunks, dv, blockIdx.x, blockIdx.y, blockIdx.z);
+                    status, trace, trace_chunks, dv, blockIdx.x, blockIdx.y, blockIdx.z, sdump);
 }
 
 // fused form: cooperative, one CTA per SM; CTAs [0, n_state) are the state
@@ -1188,7 +1197,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const float* __restrict__ S0, __nv_bfloat16* __restrict__ out,
                 float* __restrict__ S_final, SeqMap map, int32_t H, uint8_t* __restrict__ scratch,
                 uint32_t* ready, unsigned* status, uint64_t* __restrict__ trace,
-                int32_t trace_chunks, int32_t n_state, int32_t dv) {
+                int32_t trace_chunks, int32_t n_state, int32_t dv, float* __restrict__ sdump) {
   static_assert(kPrepThreads == kStateThreads, "one block shape for both roles");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align_smem_1024(smem_raw);
@@ -1196,7 +1205,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int u = blockIdx.x;
     const int ns = dv / 128;
     state_role<true>(sm, &tm_kb, S0, out, S_final, map, H, scratch, ready, status, trace,
-                     trace_chunks, dv, u / (ns * H), (u / ns) % H, u % ns);
+                     trace_chunks, dv, u / (ns * H), (u / ns) % H, u % ns, sdump);
   } else {
     int64_t positions = map.chunks_per_seq;
     if (map.cu_seqlens) {
@@ -1352,7 +1361,7 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, tc_fused_kernel, tq, tk, tv, tkb, a.alpha, a.beta, a.S0,
                            (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr, ready, a.status,
-                           g_trace, g_trace_chunks, (int32_t)n_state, dv);
+                           g_trace, g_trace_chunks, (int32_t)n_state, dv, a.state_dump);
     if (e == cudaSuccess) {
       count_launches(1);
       g_last_tc_form = 1;
@@ -1376,7 +1385,8 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
   g_last_tc_form = 0;
   tc_state_kernel<<<dim3((unsigned)a.map.N, (unsigned)a.H, (unsigned)(dv / 128)), kStateThreads,
                     kStateSmem, stream>>>(tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map,
-                                          a.H, scr, a.status, g_trace, g_trace_chunks, dv);
+                                          a.H, scr, a.status, g_trace, g_trace_chunks, dv,
+                                          a.state_dump);
   count_launches(1);
   return cudaGetLastError();
 }
