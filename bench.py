@@ -72,8 +72,10 @@ def prepare_bytes(T_total, N, H=H, dk=DK, dv=DV, io_bytes=2, state=True):
 
 def backward_flops(lengths, H=H, dk=DK, dv=DV):
     """FLOPs the chunked backward executes per call (C = 64 rows a chunk,
-    padded chunks counted whole): the forward re-run for the chunk-start
-    states (KK^T, QK^T, W, U~, U and S' per chunk) plus the reverse state pass
+    padded chunks counted whole), counted as the CUDA-core form runs them: the
+    forward re-run for the chunk-start states (KK^T, QK^T, W, U~, U and S' per
+    chunk; with bf16 I/O the U and S' products run on the tensor cores inside
+    the forward prefill instead) plus the reverse state pass
     (K dS'^T, Ph^T dO, dO^T Qh, dU^T W) and the per-chunk gradient products
     (U, dO S, dU S, U dS', K dS'^T at C x d x d; dPh, dT, T^T dW, T^T dU, T^T dT,
     dA, (M + M^T) K, FG^T Q, FG K at C x C x d)."""
@@ -589,7 +591,9 @@ def run_ours(args, rank, world, local_rank, dist):
                              "executed_flops_per_launch": bw_flops,
                              "peak_source": "fp32 FMA of the CUDA cores: 152 SMs x 128 lanes "
                                             "x 2 FLOP x 2.07 GHz"},
-                "path": "CUDA-core fp32 (chunked form; forward re-run inside)",
+                "path": "chunked form: forward re-run on the tensor cores (bf16 I/O) storing "
+                        "the chunk-start states, reverse state pass and chunk gradients on "
+                        "the CUDA cores in fp32",
             },
             "layer_steps": {
                 "prepare": {"workload": lcase.name + " (gdn_prepare)",
