@@ -270,6 +270,7 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   a.map.T = varlen ? T_total : seqlen;
   a.map.chunks_per_seq = varlen ? 0 : (seqlen + kC - 1) / kC;
   a.max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
+  if (a.max_chunks * heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;   // grid bound
   const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 1024) : 0;
   const size_t work_bytes =
       prefill_backward_scratch_bytes(a.max_chunks, heads, dv, T_total, io_dtype);
