@@ -44,7 +44,9 @@ def _bounds(T_total, cu_seqlens, B=None, T=None):
 
 def prefill_backward(q, k, v, alpha, beta, dout, S0=None, dS_final=None, cu_seqlens=None):
     """Gradients of L = <dout, out> + <dS_final, S_final> with respect to
-    q, k, v, alpha, beta and S0.
+    q, k, v, alpha, beta and S0, for the recurrence of Eq. 16-19 (Appendix
+    A.3), differentiated token by token in reverse order (the lines of this
+    module's header, each the derivative of one term of the forward line).
 
     q, k: [B, T, H, dk] or [T_total, H, dk]; v, dout likewise with dv;
     alpha, beta: [.., H]; S0, dS_final: [N, H, dv, dk] or None (zero).

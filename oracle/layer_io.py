@@ -83,7 +83,9 @@ def _seq_bounds(T, cu_seqlens):
 
 
 def short_conv_silu(x, w, cu_seqlens=None, conv_state=None):
-    """Causal depthwise convolution of width 4, then SiLU, per sequence.
+    """Causal depthwise convolution of width 4, then SiLU, per sequence
+    (Appendix A.3, the paragraph after Table 8: short convolution, kernel
+    size 4, with SiLU, on q, k and v).
 
     x [T, C]; w [C, 4]; conv_state [N, 3, C] or None (zero history).
     Returns (y [T, C] fp64, final_state [N, 3, C] fp64): the final state is
@@ -109,12 +111,16 @@ def short_conv_silu(x, w, cu_seqlens=None, conv_state=None):
 
 
 def l2_normalize(x, eps=L2_EPS):
-    """x / sqrt(sum(x^2) + eps) over the last axis."""
+    """x / sqrt(sum(x^2) + eps) over the last axis: the per-head q / k
+    normalisation the recurrence's inputs assume (a reading: the pages do not
+    state it for GDN)."""
     return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
 
 
 def gates(a_raw, b_raw, A_log, dt_bias):
-    """alpha = exp(-exp(A_log) * softplus(a_raw + dt_bias)), beta = sigmoid(b_raw).
+    """alpha = exp(-exp(A_log) * softplus(a_raw + dt_bias)), beta = sigmoid(b_raw):
+    the forget gate g_t of Eq. 16 (alpha = e^{g_t}) and the write strength of
+    Eq. 18, as the text under Eq. 16-21 defines them.
     a_raw, b_raw [..., H]; A_log, dt_bias [H]."""
     g = -np.exp(widen(A_log)) * softplus(widen(a_raw) + widen(dt_bias))
     return np.exp(g), sigmoid(widen(b_raw))
@@ -122,7 +128,9 @@ def gates(a_raw, b_raw, A_log, dt_bias):
 
 def prepare(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, H, dk, dv, cu_seqlens=None,
             conv_state=None):
-    """The layer's pre-recurrence steps for a packed batch.
+    """The layer's pre-recurrence steps for a packed batch (Appendix A.3:
+    Table 8's paragraph and the text under Eq. 16-21), in order: convolution
+    + SiLU of the packed q|k|v projection, q / k normalisation, gates.
 
     Returns dict of fp64 arrays: q, k [T, H, dk]; v [T, H, dv]; alpha, beta
     [T, H]; conv_state [N, 3, C] (the state after the last token).
@@ -138,8 +146,8 @@ def prepare(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, H, dk, dv, cu_seqlens=Non
 
 
 def prepare_decode_step(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, conv_state, H, dk, dv):
-    """One token per sequence: qkv [N, C], conv_state [N, 3, C] (fp64, updated
-    in place).  Returns q, k [N, H, dk]; v [N, H, dv]; alpha, beta [N, H]."""
+    """One token per sequence, the decode form of `prepare` (the same
+    passages): qkv [N, C], conv_state [N, 3, C] (fp64, updated in place).  Returns q, k [N, H, dk]; v [N, H, dv]; alpha, beta [N, H]."""
     assert isinstance(conv_state, np.ndarray) and conv_state.dtype == np.float64
     N = conv_state.shape[0]
     cu = np.arange(N + 1)
@@ -149,7 +157,8 @@ def prepare_decode_step(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, conv_state, H
 
 
 def output_norm_gate(o, g, w, eps, act="silu"):
-    """Eq. 20 read-out: o / sqrt(mean(o^2) + eps) * w * act(g) per head.
+    """Eq. 20 read-out (Appendix A.3), in this module's reading of the garbled
+    equation: o / sqrt(mean(o^2) + eps) * w * act(g) per head.
     o, g [..., dv]; w [dv]."""
     o = widen(o)
     gv = widen(g)
