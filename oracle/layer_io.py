@@ -147,7 +147,8 @@ def prepare(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, H, dk, dv, cu_seqlens=Non
 
 def prepare_decode_step(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, conv_state, H, dk, dv):
     """One token per sequence, the decode form of `prepare` (the same
-    passages): qkv [N, C], conv_state [N, 3, C] (fp64, updated in place).  Returns q, k [N, H, dk]; v [N, H, dv]; alpha, beta [N, H]."""
+    passages): qkv [N, C], conv_state [N, 3, C] (fp64, updated in place).
+    Returns q, k [N, H, dk]; v [N, H, dv]; alpha, beta [N, H]."""
     assert isinstance(conv_state, np.ndarray) and conv_state.dtype == np.float64
     N = conv_state.shape[0]
     cu = np.arange(N + 1)
