@@ -2,6 +2,7 @@
 and rejects malformed host arguments before touching the GPU.  CPU only: no
 call here reaches a CUDA runtime function."""
 import ctypes
+import glob
 import os
 import re
 
@@ -11,13 +12,17 @@ import hybrid_linear_attention_deltanet_gb300 as gdn
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gdn.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
-def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(gdn_\w+)\s*\(", text,
-                                 flags=re.M)))
+def declared_functions(headers=(HEADER,)):
+    names = set()
+    for h in headers:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(gdn_\w+)\s*\(", text,
+                                flags=re.M))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
@@ -36,7 +41,9 @@ def test_header_declares_the_boundary():
 
 
 def test_every_declared_symbol_is_exported(lib):
-    for fn in declared_functions():
+    names = declared_functions(HEADERS)
+    assert len(HEADERS) >= 2 and "gdn_testing_bounded_wait" in names and "gdn_prepare" in names
+    for fn in names:
         assert hasattr(lib, fn), fn
 
 
