@@ -114,3 +114,17 @@ def test_backward_packing_bitwise(gdn_lib):
         for key in ("dq", "dk", "dv", "dalpha", "dbeta"):
             assert np.array_equal(alone[key][0], packed[key][0, sl]), (n, key)
         assert np.array_equal(alone["dS0"][0], packed["dS0"][n])
+
+
+def test_backward_split_form_forward_rerun(gdn_lib):
+    """70 sequences x 2 heads (140 state units) leave too few SMs for the fused
+    launch, so the backward's tensor-core forward re-run (which stores the
+    chunk-start states) takes the split form; gradients still match."""
+    import ctypes
+    rng = np.random.default_rng(97)
+    lens = [int(t) for t in rng.integers(1, 150, size=70)]
+    check(gdn_lib, PrefillCase("bwd split", lens, H=2, io_dtype=torch.bfloat16, seed=98,
+                               varlen=True), seed=13)
+    f = gdn_lib.load().gdn_testing_last_prefill_form
+    f.restype = ctypes.c_int32
+    assert int(f()) == 0
