@@ -389,6 +389,34 @@ def run_ours(args, rank, world, local_rank, dist):
     p5_ms = max_over_ranks(ev0.elapsed_time(ev1) / p5_steps)
     del x5, out5, sf5
 
+    # ---- the 64K single-sequence prefill: one chain per (head, half) with
+    # gdn_prefill, and the segmented scan (gdn_prefill_scan, 8 segments)
+    c64 = gdn_inputs.prefill_64k()
+    x64 = gdn_inputs.make_prefill(c64, device=dev)
+    o64 = torch.empty_like(x64["v"])
+    s64 = torch.empty((1, H, DV, DK), dtype=torch.float32, device=dev)
+    p64_plain = lambda: gdn.prefill(x64["q"], x64["k"], x64["v"], x64["alpha"], x64["beta"], None,
+                                    out=o64, S_final=s64)
+    p64_scan = lambda: gdn.prefill_scan(x64["q"], x64["k"], x64["v"], x64["alpha"], x64["beta"],
+                                        None, segments=8, out=o64, S_final=s64)
+
+    def time_calls(fn, n=5):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(n):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        return ev0.elapsed_time(ev1) / n
+
+    p64_ms = time_calls(p64_plain)
+    p64s_ms = time_calls(p64_scan)
+    assert gdn.device_status() == 0
+    f64 = prefill_flops(c64.lengths)
+    del x64, o64, s64
+
     # ---- backward of the 8K prefill (gdn_prefill_backward), dout and dS_final
     # drawn once; each call recomputes the forward internally
     bx = x
@@ -577,6 +605,18 @@ def run_ours(args, rank, world, local_rank, dist):
                             "path": gdn.prefill_path(pcase5.io_dtype),
                             "counted_tflops": round(prefill_flops(pcase5.lengths, dv=512)
                                                     / (p5_ms * 1e-3) / 1e12, 3)},
+            },
+            "prefill_64k": {
+                "workload": c64.name,
+                "gdn_prefill": {"ms_per_step": round(p64_ms, 4),
+                                "value": round(c64.total_tokens / (p64_ms * 1e-3) / 1e6, 3),
+                                "unit": "Mtok/s/layer",
+                                "counted_tflops": round(f64 / (p64_ms * 1e-3) / 1e12, 2)},
+                "gdn_prefill_scan_8_segments": {
+                    "ms_per_step": round(p64s_ms, 4),
+                    "value": round(c64.total_tokens / (p64s_ms * 1e-3) / 1e6, 3),
+                    "unit": "Mtok/s/layer",
+                    "counted_tflops": round(f64 / (p64s_ms * 1e-3) / 1e12, 2)},
             },
             "backward": {
                 "workload": case.name + " (gdn_prefill_backward, dout and dS_final given)",

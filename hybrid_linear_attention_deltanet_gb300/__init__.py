@@ -67,6 +67,8 @@ def load():
     lib.gdn_kernel_launches.restype = ctypes.c_uint64
     lib.gdn_prefill_path.argtypes = [ctypes.c_int32]
     lib.gdn_prefill_path.restype = ctypes.c_char_p
+    lib.gdn_prefill_scan.argtypes = [vp] * 8 + [i32, i64, i32, i32, i32, i32, vp]
+    lib.gdn_prefill_scan.restype = ctypes.c_int
     lib.gdn_prefill_backward.argtypes = [vp] * 15 + [i32, i64, i32, i32, i32, i32, vp]
     lib.gdn_prefill_backward.restype = ctypes.c_int
     lib.gdn_prepare.argtypes = [vp] * 14 + [i32, i64, i32, i32, i32, i32, vp]
@@ -174,6 +176,43 @@ def prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=No
                              _io_code(io), _stream_handle(stream))
     if rc != 0:
         raise GDNError("gdn_prefill", rc)
+    return out, S_final
+
+
+def prefill_scan(q, k, v, alpha, beta, S0=None, segments=8, out=None, S_final=None,
+                 return_final: bool = True, stream=None):
+    """``gdn_prefill_scan``: the prefill of a dense bf16 batch [B, T, H, .] run
+    as a scan over ``segments`` pieces of each sequence (for few, long
+    sequences).  Returns (out, S_final) like :func:`prefill`."""
+    lib = load()
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, torch.bfloat16, dev)
+    _check(alpha, "alpha", torch.float32, dev)
+    _check(beta, "beta", torch.float32, dev)
+    if q.dim() != 4 or k.shape != q.shape or v.shape[:-1] != q.shape[:-1] \
+            or alpha.shape != q.shape[:-1] or beta.shape != q.shape[:-1]:
+        raise ValueError("dense inputs: q, k [B, T, H, dk]; v [B, T, H, dv]; alpha, beta [B, T, H]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if S0 is not None:
+        _check(S0, "S0", torch.float32, dev)
+        if tuple(S0.shape) != (B, H, dv, dk):
+            raise ValueError(f"S0 must be [{B}, {H}, {dv}, {dk}]")
+    if out is None:
+        out = torch.empty_like(v)
+    else:
+        _check(out, "out", torch.bfloat16, dev)
+    if S_final is None and return_final:
+        S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    elif S_final is not None:
+        _check(S_final, "S_final", torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = lib.gdn_prefill_scan(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
+                                  _ptr(out), _ptr(S_final), B, T, H, dk, dv, int(segments),
+                                  _stream_handle(stream))
+    if rc != 0:
+        raise GDNError("gdn_prefill_scan", rc)
     return out, S_final
 
 

@@ -111,6 +111,8 @@ struct PrefillLaunch {
   bool allow_overlap;   // tensor-core path may run prep and state pass in one cooperative launch
   float* state_dump;    // tensor-core path: every chunk's start state, [chunks * H][dv][dk]
                         // fp32 (the backward's forward re-run), or nullptr
+  bool state_only;      // tensor-core path: the per-chunk images are already in scratch
+                        // (an earlier call on the same inputs and map); run the state pass only
 };
 
 cudaError_t launch_chunk_offsets(const int32_t* cu_seqlens, int32_t N, int64_t T_total,

@@ -1345,7 +1345,7 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
   uint32_t* ready = (uint32_t*)(scr + (size_t)items * img_stride(dv));
   const int64_t n_state = (int64_t)a.map.N * a.H * (dv / 128);
 
-  if (!prep_only && a.allow_overlap && f->fused_ok && items > 0 &&
+  if (!prep_only && !a.state_only && a.allow_overlap && f->fused_ok && items > 0 &&
       n_state + kMinPrepWorkers <= f->sms) {
     if ((e = cudaMemsetAsync(ready, 0, (size_t)items * sizeof(uint32_t), stream)) != cudaSuccess)
       return e;
@@ -1373,7 +1373,7 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
     (void)cudaGetLastError();
   }
 
-  if (items > 0) {
+  if (items > 0 && !a.state_only) {
     const int64_t slots = 2 * (int64_t)f->sms;
     const unsigned grid = (unsigned)(items < slots ? items : slots);
     tc_prep_kernel<<<grid, kPrepThreads, kPrepSmemSplit, stream>>>(

@@ -105,6 +105,32 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
                 int32_t dv, int32_t io_dtype, gdn_stream_t stream);
 
 /*
+ * gdn_prefill_scan -- gdn_prefill for a dense bf16 batch of long sequences,
+ * run as a scan over segments.
+ *
+ * Over any run of chunks the state pass is affine in its start state,
+ * S_end = S_start A + B (A the product of the per-token transitions
+ * alpha_t (I - beta_t k_t k_t^T), B the end state from a zero start).  Each
+ * sequence is cut into `segments` pieces of whole chunks that run as
+ * independent chains: a pass from the caller's S0 / zero starts gives B, a pass
+ * from identity starts on the same per-chunk factors gives A, a scan composes
+ * the true start of every segment, and a last pass from those starts writes
+ * out and S_final.  Three passes over chains `segments` times shorter replace
+ * one long chain -- faster when the batch has few (sequence, head) units and
+ * long sequences (e.g. one 64K-token sequence of 6 heads: 12 segments).
+ *
+ * Arguments as gdn_prefill with cu_seqlens = NULL and io_dtype = GDN_BF16.
+ * Results equal gdn_prefill's to within the bf16 tolerance, not bit for bit
+ * (the chains are composed in a different order).  segments = 1, or a
+ * sequence too short to cut, runs gdn_prefill itself.  Scratch from the
+ * library's pool: gdn_prefill's plus five per-(segment, head) states.
+ */
+int gdn_prefill_scan(const void* q, const void* k, const void* v, const float* alpha,
+                     const float* beta, const float* S0, void* out, float* S_final, int32_t batch,
+                     int64_t seqlen, int32_t heads, int32_t dk, int32_t dv, int32_t segments,
+                     gdn_stream_t stream);
+
+/*
  * gdn_prefill_backward -- gradients of the prefill, for training with the
  * chunked kernel (Appendix A.3, last paragraph: the pages train with it).
  *

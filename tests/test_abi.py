@@ -166,3 +166,13 @@ def test_fault_hook_rejects_bad_arguments(lib):
     assert f(2, 1000, None) == 1
     assert f(0, -1, None) == 1
     assert f(1, 3_000_000_000, None) == 1
+
+
+def test_prefill_scan_rejects_bad_host_arguments(lib):
+    f = lambda q=A16, out=A16b, batch=1, T=4096, dv=256, seg=4: lib.gdn_prefill_scan(
+        q, A16, A16, A16, A16, None, out, None, batch, T, 6, 256, dv, seg, None)
+    assert f(seg=0) == 1
+    assert f(batch=0) == 1
+    assert f(dv=384) == 2
+    assert f(q=MIS) == 3
+    assert f(out=A16) == 1                                              # out over q
