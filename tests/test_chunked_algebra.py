@@ -49,3 +49,60 @@ def test_chunked_backward_model_matches_backward_oracle():
                              x["dS"], cu, C=C)
         for key in ("dq", "dk", "dv", "dalpha", "dbeta", "dS0"):
             assert np.max(np.abs(o[key] - m[key])) <= 1e-12 * np.max(np.abs(o[key])), (lens, key)
+
+
+@pytest.mark.parametrize("T,P,C,dk,dv", [(300, 4, 16, 8, 8), (257, 5, 16, 8, 12), (96, 6, 16, 6, 6)])
+def test_segment_scan_composes_to_the_full_chain(T, P, C, dk, dv):
+    """The long-sequence prefill as a scan over segments: over a run of tokens
+    the recurrence is affine in its start state, S_end = S_start A + B, with
+    A = prod_t alpha_t (I - beta_t k_t k_t^T) (in token order, acting on the
+    right of S) and B the end state from a zero start.  A pass from the start
+    [I; 0] gives F = A + B on the first dk rows; composing the segments'
+    (A, B) pairs reproduces the single chain's outputs and end state to fp64
+    rounding.  Segments are whole chunks of C tokens, the last one ragged."""
+    rng = np.random.default_rng(T * 7 + P)
+    H = 2
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, dv))
+    alpha = rng.uniform(0.9, 1.0, (T, H)).astype(np.float32)     # long memory: starts matter
+    beta = rng.uniform(0.0, 1.0, (T, H)).astype(np.float32)
+    q, k, v = (x.astype(np.float32) for x in (q, k, v))
+    S0 = rng.standard_normal((1, H, dv, dk))
+    o_ref, s_ref, _ = oracle.prefill(q, k, v, alpha, beta, S0,
+                                     cu_seqlens=np.array([0, T], dtype=np.int64))
+    seg = -(-(-(-T // C)) // P) * C                   # whole chunks per segment
+    cu = np.array(sorted({min(j * seg, T) for j in range(P + 1)}), dtype=np.int64)
+    n = len(cu) - 1
+    assert n >= 2
+    zero = np.zeros((n, H, dv, dk))
+    start_b = zero.copy()
+    start_b[0] = S0[0]
+    ident = zero.copy()
+    ident[:, :, :dk, :] = np.eye(dk)
+    _, B, _ = oracle.prefill(q, k, v, alpha, beta, start_b, cu_seqlens=cu)
+    _, F, _ = oracle.prefill(q, k, v, alpha, beta, ident, cu_seqlens=cu)
+    # [segment, head, dk, dk]; for segment 0, whose B pass starts from S0, this
+    # is (I - S0) A(0) instead, and the scan never uses it
+    A = F[:, :, :dk, :] - B[:, :, :dk, :]
+    # A is the product of the segment's per-token transitions (written out here)
+    for j in range(1, n):
+        for h in range(H):
+            M = np.eye(dk)
+            for t in range(cu[j], cu[j + 1]):
+                kt = k[t, h].astype(np.float64)
+                M = M @ (float(alpha[t, h]) * (np.eye(dk) - float(beta[t, h]) * np.outer(kt, kt)))
+            assert np.abs(A[j, h] - M).max() <= 1e-12
+    # the scan: every segment's true start from its predecessor's (A, B)
+    starts = zero.copy()
+    starts[0] = S0[0]
+    starts[1] = B[0]
+    for j in range(2, n):
+        starts[j] = np.einsum("hij,hjk->hik", starts[j - 1], A[j - 1]) + B[j - 1]
+    o, S_end, _ = oracle.prefill(q, k, v, alpha, beta, starts, cu_seqlens=cu)
+    assert np.abs(o - o_ref).max() <= 1e-11 * np.abs(o_ref).max()
+    assert np.abs(S_end[-1] - s_ref[0]).max() <= 1e-11 * np.abs(s_ref).max()
+    # and the segment starts do matter on this input
+    o_cut, _, _ = oracle.prefill(q, k, v, alpha, beta, start_b, cu_seqlens=cu)
+    assert np.abs(o_cut - o_ref).max() > 1e-3 * np.abs(o_ref).max()
