@@ -25,15 +25,40 @@ constexpr int kTaps = 4;            // short convolution width (Table 8's paragr
 constexpr int kHist = kTaps - 1;    // inputs carried across calls per channel
 constexpr int kSeg = 256;           // channels per warp unit (one q/k head)
 constexpr int kTile = 64;           // tokens one warp walks in the prefill form
-// tokens whose loads one lane keeps in flight together (16 B each at bf16)
-template <typename T> __host__ __device__ constexpr int group_of() { return 2; }
 constexpr int kWarpsPerCta = 8;
+// The prefill form streams its input rows through a per-warp ring in shared
+// memory filled by cp.async: kRing tokens a warp in flight without holding
+// registers (16 warps an SM x 8 tokens x 512 B = 64 KB of loads in flight, about
+// what HBM's bandwidth x latency asks of one SM).  16-byte copies a lane per
+// token: 1 at bf16, 2 at fp32 (4 tokens deep: the same 32 KB a CTA).
+template <typename T> __host__ __device__ constexpr int vecs_of() { return (int)sizeof(T) * 8 / 16; }
+template <typename T> __host__ __device__ constexpr int ring_of() { return 8 / vecs_of<T>(); }
+template <typename T> __host__ __device__ constexpr size_t ring_bytes() {
+  return (size_t)kWarpsPerCta * ring_of<T>() * vecs_of<T>() * 32 * 16;
+}
 constexpr float kL2Eps = 1e-6f;
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
+}
+
+// 16-byte global -> shared copy of this thread, completed by cp_async_wait;
+// each lane later reads back only what it copied itself
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(smem)),
+               "l"((uint64_t)__cvta_generic_to_global(gmem))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// at most N of this thread's most recent groups still pending
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // 8 consecutive elements <-> 8 floats.  bf16 widens exactly (a shift); the
@@ -215,8 +240,8 @@ __device__ __forceinline__ void gates_one(const PrepareArgs& a, int64_t idx) {
 // Warp units: for each tile of kTile tokens, n_seg channel segments and one
 // gate unit; then one unit per sequence that copies the carried state of an
 // empty sequence through.
-// At most 128 registers a thread, so that two CTAs (16 warps, each with a
-// group of tokens in flight while it computes the previous one) share an SM.
+// At most 128 registers a thread and 32 KB of ring a CTA, so that two CTAs
+// (16 warps, each with kRing tokens in flight) share an SM.
 template <typename T>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, 2)
 prepare_kernel(PrepareArgs a) {
@@ -288,43 +313,76 @@ prepare_kernel(PrepareArgs a) {
     }
   }
 
-  // Ping-pong over groups of kGroup tokens: the next group's loads are in
-  // flight while the current group computes.
-  constexpr int kGroup = group_of<T>();
-  Raw8 ga[kGroup], gb[kGroup];
-  auto load_group = [&](Raw8 (&r)[kGroup], int64_t tg) {
+  // The ring: slot i of this warp holds token t0 + i (mod kRing), one
+  // cp.async group per token; groups past the tile's end are empty, so that
+  // "all but the kRing - 1 newest groups complete" always means "token t is in".
+  constexpr int kRing = ring_of<T>(), kVec = vecs_of<T>();
+  extern __shared__ uint4 ring_smem[];
+  uint4* ring = ring_smem + (threadIdx.x >> 5) * (kRing * kVec * 32) + lane;
+  auto issue = [&](int64_t t) {
+    if (t < t1) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + t * C + c0);
+      uint4* slot = ring + (int)((t - t0) & (kRing - 1)) * (kVec * 32);
 #pragma unroll
-    for (int i = 0; i < kGroup; ++i)
-      if (tg + i < t1) r[i] = load8(x + (tg + i) * C + c0);
+      for (int u = 0; u < kVec; ++u) cp_async16(slot + u * 32, src + u);
+    }
+    cp_async_commit();
   };
-  auto run_group = [&](const Raw8 (&r)[kGroup], int64_t tg) {
 #pragma unroll
-    for (int i = 0; i < kGroup; ++i) {
-      const int64_t t = tg + i;
-      if (t >= t1) break;
-      if (t >= se && n + 1 < a.N) {  // a new sequence starts here (skipping empty ones)
-        do { ++n; } while (n + 1 < a.N && seqs.end(n) <= t);
-        sb = seqs.begin(n);
-        se = seqs.end(n);
-        history<T, true>(state_in, n, C, c0, win);
-      }
-      float xf[8], y[8];
-      widen8<T>(r[i], xf);
-      conv_token(w, win, xf, l2, y);
-      store8(dst + t * dst_stride + dst_c, y);
-      if (t == se - 1 && state_out) {
+  for (int d = 0; d < kRing; ++d) issue(t0 + d);
+  auto read = [&](int64_t t) {
+    Raw8 r;
+    const uint4* slot = ring + (int)((t - t0) & (kRing - 1)) * (kVec * 32);
+    r.a = slot[0];
+    r.b = kVec > 1 ? slot[32] : make_uint4(0, 0, 0, 0);
+    return r;
+  };
+  // one token, with the sequence bookkeeping
+  auto one = [&](int64_t t, const Raw8& r) {
+    if (t >= se && n + 1 < a.N) {  // a new sequence starts here (skipping empty ones)
+      do { ++n; } while (n + 1 < a.N && seqs.end(n) <= t);
+      sb = seqs.begin(n);
+      se = seqs.end(n);
+      history<T, true>(state_in, n, C, c0, win);
+    }
+    float xf[8], y[8];
+    widen8<T>(r, xf);
+    conv_token(w, win, xf, l2, y);
+    store8(dst + t * dst_stride + dst_c, y);
+    if (t == se - 1 && state_out) {
+#pragma unroll
+      for (int j = 0; j < kHist; ++j) store8(state_out + (n * kHist + j) * C + c0, win[j]);
+    }
+  };
+  // Two tokens an iteration: when both lie inside the current sequence their
+  // arithmetic has no branch between it, so the two dependent chains (taps,
+  // SiLU, the L2 reduction) interleave.
+  for (int64_t t = t0; t < t1; t += 2) {
+    cp_async_wait<kRing - 2>();   // tokens t and t + 1 are in
+    const Raw8 r0 = read(t);
+    const bool pair = t + 1 < t1;
+    const Raw8 r1 = pair ? read(t + 1) : r0;
+    if (pair && t + 1 < se) {
+      float x0[8], x1[8], y0[8], y1[8];
+      widen8<T>(r0, x0);
+      widen8<T>(r1, x1);
+      conv_token(w, win, x0, l2, y0);
+      conv_token(w, win, x1, l2, y1);
+      store8(dst + t * dst_stride + dst_c, y0);
+      store8(dst + (t + 1) * dst_stride + dst_c, y1);
+      if (t + 1 == se - 1 && state_out) {
 #pragma unroll
         for (int j = 0; j < kHist; ++j) store8(state_out + (n * kHist + j) * C + c0, win[j]);
       }
+    } else {
+      one(t, r0);
+      if (pair) one(t + 1, r1);
     }
-  };
-  load_group(ga, t0);
-  for (int64_t tg = t0; tg < t1; tg += 2 * kGroup) {
-    load_group(gb, tg + kGroup);
-    run_group(ga, tg);
-    load_group(ga, tg + 2 * kGroup);
-    run_group(gb, tg + kGroup);
+    // both slots' values are in registers (consumed above): refill them
+    issue(t + kRing);
+    issue(t + 1 + kRing);
   }
+  cp_async_wait<0>();
 }
 
 // One token per sequence against the carried convolution state, which is
@@ -498,9 +556,10 @@ int gdn_prepare(const void* qkv, const float* conv_w, const float* a_raw, const 
   if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
   if (blocks == 0) return GDN_OK;
   if (io_dtype == GDN_BF16)
-    prepare_kernel<__nv_bfloat16><<<(unsigned)blocks, kWarpsPerCta * 32, 0, stream>>>(a);
+    prepare_kernel<__nv_bfloat16>
+        <<<(unsigned)blocks, kWarpsPerCta * 32, ring_bytes<__nv_bfloat16>(), stream>>>(a);
   else
-    prepare_kernel<float><<<(unsigned)blocks, kWarpsPerCta * 32, 0, stream>>>(a);
+    prepare_kernel<float><<<(unsigned)blocks, kWarpsPerCta * 32, ring_bytes<float>(), stream>>>(a);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
