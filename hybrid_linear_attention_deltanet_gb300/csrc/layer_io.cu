@@ -316,39 +316,53 @@ prepare_kernel(PrepareArgs a) {
   // The ring: slot i of this warp holds token t0 + i (mod kRing), one
   // cp.async group per token; groups past the tile's end are empty, so that
   // "all but the kRing - 1 newest groups complete" always means "token t is in".
+  // Inside the tile tokens are counted from t0 in 32 bits and the row pointers
+  // advance by one row a token (no 64-bit index products on the way).
   constexpr int kRing = ring_of<T>(), kVec = vecs_of<T>();
   extern __shared__ uint4 ring_smem[];
   uint4* ring = ring_smem + (threadIdx.x >> 5) * (kRing * kVec * 32) + lane;
-  auto issue = [&](int64_t t) {
-    if (t < t1) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + t * C + c0);
-      uint4* slot = ring + (int)((t - t0) & (kRing - 1)) * (kVec * 32);
+  const int n_tok = (int)(t1 - t0);
+  const T* src = x + t0 * C + c0;          // row of the next token to fetch
+  int fetched = 0;                          // tokens fetched so far
+  auto issue = [&]() {
+    if (fetched < n_tok) {
+      uint4* slot = ring + (fetched & (kRing - 1)) * (kVec * 32);
+      const uint4* g = reinterpret_cast<const uint4*>(src);
 #pragma unroll
-      for (int u = 0; u < kVec; ++u) cp_async16(slot + u * 32, src + u);
+      for (int u = 0; u < kVec; ++u) cp_async16(slot + u * 32, g + u);
+      src += C;
     }
+    ++fetched;
     cp_async_commit();
   };
 #pragma unroll
-  for (int d = 0; d < kRing; ++d) issue(t0 + d);
-  auto read = [&](int64_t t) {
+  for (int d = 0; d < kRing; ++d) issue();
+  auto read = [&](int i) {
     Raw8 r;
-    const uint4* slot = ring + (int)((t - t0) & (kRing - 1)) * (kVec * 32);
+    const uint4* slot = ring + (i & (kRing - 1)) * (kVec * 32);
     r.a = slot[0];
     r.b = kVec > 1 ? slot[32] : make_uint4(0, 0, 0, 0);
     return r;
   };
+  T* out_row = dst + t0 * dst_stride + dst_c;   // row of token t0 + i: out_row + i rows
+  // the current sequence's end relative to t0, clamped so that it fits 32 bits
+  // and stays above i + 2 for every i of the tile when the sequence runs on
+  auto rel_end = [&]() { return (int)min(se - t0, (int64_t)kTile + 2); };
+  int se_rel = rel_end();
   // one token, with the sequence bookkeeping
-  auto one = [&](int64_t t, const Raw8& r) {
+  auto one = [&](int i, const Raw8& r) {
+    const int64_t t = t0 + i;
     if (t >= se && n + 1 < a.N) {  // a new sequence starts here (skipping empty ones)
       do { ++n; } while (n + 1 < a.N && seqs.end(n) <= t);
       sb = seqs.begin(n);
       se = seqs.end(n);
+      se_rel = rel_end();
       history<T, true>(state_in, n, C, c0, win);
     }
     float xf[8], y[8];
     widen8<T>(r, xf);
     conv_token(w, win, xf, l2, y);
-    store8(dst + t * dst_stride + dst_c, y);
+    store8(out_row + i * dst_stride, y);
     if (t == se - 1 && state_out) {
 #pragma unroll
       for (int j = 0; j < kHist; ++j) store8(state_out + (n * kHist + j) * C + c0, win[j]);
@@ -357,30 +371,31 @@ prepare_kernel(PrepareArgs a) {
   // Two tokens an iteration: when both lie inside the current sequence their
   // arithmetic has no branch between it, so the two dependent chains (taps,
   // SiLU, the L2 reduction) interleave.
-  for (int64_t t = t0; t < t1; t += 2) {
-    cp_async_wait<kRing - 2>();   // tokens t and t + 1 are in
-    const Raw8 r0 = read(t);
-    const bool pair = t + 1 < t1;
-    const Raw8 r1 = pair ? read(t + 1) : r0;
-    if (pair && t + 1 < se) {
+  for (int i = 0; i < n_tok; i += 2) {
+    cp_async_wait<kRing - 2>();   // tokens i and i + 1 are in
+    const Raw8 r0 = read(i);
+    const bool pair = i + 1 < n_tok;
+    const Raw8 r1 = pair ? read(i + 1) : r0;
+    if (pair && i + 1 < se_rel) {
       float x0[8], x1[8], y0[8], y1[8];
       widen8<T>(r0, x0);
       widen8<T>(r1, x1);
       conv_token(w, win, x0, l2, y0);
       conv_token(w, win, x1, l2, y1);
-      store8(dst + t * dst_stride + dst_c, y0);
-      store8(dst + (t + 1) * dst_stride + dst_c, y1);
-      if (t + 1 == se - 1 && state_out) {
+      T* o = out_row + i * dst_stride;
+      store8(o, y0);
+      store8(o + dst_stride, y1);
+      if (i + 2 == se_rel && state_out) {   // token i + 1 ends the sequence
 #pragma unroll
         for (int j = 0; j < kHist; ++j) store8(state_out + (n * kHist + j) * C + c0, win[j]);
       }
     } else {
-      one(t, r0);
-      if (pair) one(t + 1, r1);
+      one(i, r0);
+      if (pair) one(i + 1, r1);
     }
     // both slots' values are in registers (consumed above): refill them
-    issue(t + kRing);
-    issue(t + 1 + kRing);
+    issue();
+    issue();
   }
   cp_async_wait<0>();
 }
