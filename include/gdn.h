@@ -124,6 +124,13 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
  * (the chains are composed in a different order).  segments = 1, or a
  * sequence too short to cut, runs gdn_prefill itself.  Scratch from the
  * library's pool: gdn_prefill's plus five per-(segment, head) states.
+ *
+ * Errors, before any launch: GDN_ERR_INVALID_ARG for segments < 1, a
+ * non-positive batch or heads, a null token tensor or out, or out / S_final
+ * overlapping an input or each other; GDN_ERR_UNSUPPORTED for dk != 256, dv
+ * not 256 or 512, batch > 65535, or more than 2^31 - 1 tokens or
+ * (segment, head) pairs; GDN_ERR_ALIGNMENT as gdn_prefill.  GDN_ERR_CUDA when
+ * the scratch cannot be had or a launch fails.
  */
 int gdn_prefill_scan(const void* q, const void* k, const void* v, const float* alpha,
                      const float* beta, const float* S0, void* out, float* S_final, int32_t batch,
