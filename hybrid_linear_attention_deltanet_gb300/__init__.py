@@ -7,6 +7,7 @@ the library's CUDA kernels; there is no CPU or PyTorch fallback, and calls
 raise when the compiled library is missing.
 
     out, S_final = prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None)
+    out, S_final = prefill(..., workspace=ws)  # caller-owned scratch, nothing allocated
     out = decode_step(q, k, v, alpha, beta, S)          # S updated in place
     grads = prefill_backward(q, k, v, alpha, beta, dout, S0, dS_final)   # training
     x = prepare(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, heads)   # -> q, k, v, alpha, beta
@@ -81,8 +82,76 @@ def load():
                                                       i32, i32, vp]
     lib.gdn_decode_layer_step.restype = ctypes.c_int
     lib.gdn_output_norm_gate.restype = ctypes.c_int
+    sz = ctypes.c_size_t
+    lib.gdn_prefill_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32]
+    lib.gdn_prefill_workspace_size.restype = sz
+    lib.gdn_prefill_ws.argtypes = [vp] * 9 + [i32, i64, i32, i32, i32, i32, vp, sz, vp]
+    lib.gdn_prefill_ws.restype = ctypes.c_int
+    lib.gdn_prefill_scan_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32]
+    lib.gdn_prefill_scan_workspace_size.restype = sz
+    lib.gdn_prefill_scan_ws.argtypes = [vp] * 8 + [i32, i64, i32, i32, i32, i32, vp, sz, vp]
+    lib.gdn_prefill_scan_ws.restype = ctypes.c_int
+    lib.gdn_prefill_backward_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32]
+    lib.gdn_prefill_backward_workspace_size.restype = sz
+    lib.gdn_prefill_backward_ws.argtypes = [vp] * 15 + [i32, i64, i32, i32, i32, i32, vp, sz, vp]
+    lib.gdn_prefill_backward_ws.restype = ctypes.c_int
+    lib.gdn_release_scratch.restype = ctypes.c_int
+    lib.gdn_testing_scratch_reserved.argtypes = [vp]
+    lib.gdn_testing_scratch_reserved.restype = ctypes.c_int
     _lib = lib
     return lib
+
+
+def _ws_args(workspace):
+    """(pointer, bytes) of a caller workspace: a uint8 CUDA tensor."""
+    if not isinstance(workspace, torch.Tensor) or workspace.dtype != torch.uint8 \
+            or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous torch.uint8 tensor")
+    return ctypes.c_void_p(workspace.data_ptr()), workspace.numel()
+
+
+def prefill_workspace_size(batch, seqlen, heads, dk=256, dv=256, io_dtype=torch.bfloat16,
+                           varlen=False) -> int:
+    """Bytes of device workspace ``prefill(..., workspace=...)`` needs
+    (``gdn_prefill_workspace_size``)."""
+    n = load().gdn_prefill_workspace_size(batch, seqlen, heads, dk, dv, _io_code(io_dtype),
+                                          int(bool(varlen)))
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("unsupported prefill arguments")
+    return int(n)
+
+
+def prefill_scan_workspace_size(batch, seqlen, heads, dk=256, dv=256, segments=8) -> int:
+    n = load().gdn_prefill_scan_workspace_size(batch, seqlen, heads, dk, dv, int(segments))
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("unsupported prefill_scan arguments")
+    return int(n)
+
+
+def prefill_backward_workspace_size(batch, seqlen, heads, dk=256, dv=256,
+                                    io_dtype=torch.bfloat16, varlen=False) -> int:
+    n = load().gdn_prefill_backward_workspace_size(batch, seqlen, heads, dk, dv,
+                                                   _io_code(io_dtype), int(bool(varlen)))
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("unsupported prefill_backward arguments")
+    return int(n)
+
+
+def release_scratch() -> None:
+    """Hand the library's scratch pool on the current device back to the system
+    (``gdn_release_scratch``; synchronises the device)."""
+    rc = load().gdn_release_scratch()
+    if rc != 0:
+        raise GDNError("gdn_release_scratch", rc)
+
+
+def scratch_reserved() -> int:
+    """Bytes the library's scratch pool holds mapped on the current device."""
+    v = ctypes.c_uint64(0)
+    rc = load().gdn_testing_scratch_reserved(ctypes.byref(v))
+    if rc != 0:
+        raise GDNError("gdn_testing_scratch_reserved", rc)
+    return int(v.value)
 
 
 def version() -> str:
@@ -128,12 +197,15 @@ def _check(t, name, dtype, device):
 
 
 def prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=None,
-            return_final: bool = True, stream=None):
+            return_final: bool = True, stream=None, workspace=None):
     """Chunkwise prefill (``gdn_prefill``).
 
     Dense: q, k [B, T, H, dk]; v [B, T, H, dv]; alpha, beta [B, T, H] fp32.
     Varlen: the same with B = 1 (or no batch axis) and ``cu_seqlens`` int32
     [N + 1] on the device.  S0 / S_final: [N, H, dv, dk] fp32.
+    ``workspace``: a uint8 CUDA tensor of at least
+    :func:`prefill_workspace_size` bytes (``gdn_prefill_ws``: the call then
+    allocates nothing); None takes scratch from the library's pool.
     Returns (out, S_final); S_final is None when ``return_final`` is False.
     """
     lib = load()
@@ -171,16 +243,19 @@ def prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=No
     elif S_final is not None:
         _check(S_final, "S_final", torch.float32, dev)
     with torch.cuda.device(dev):
-        rc = lib.gdn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
-                             _ptr(cu_seqlens), _ptr(out), _ptr(S_final), N, seqlen, H, dk, dv,
-                             _io_code(io), _stream_handle(stream))
+        args = (_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
+                _ptr(out), _ptr(S_final), N, seqlen, H, dk, dv, _io_code(io))
+        if workspace is None:
+            rc = lib.gdn_prefill(*args, _stream_handle(stream))
+        else:
+            rc = lib.gdn_prefill_ws(*args, *_ws_args(workspace), _stream_handle(stream))
     if rc != 0:
-        raise GDNError("gdn_prefill", rc)
+        raise GDNError("gdn_prefill_ws" if workspace is not None else "gdn_prefill", rc)
     return out, S_final
 
 
 def prefill_scan(q, k, v, alpha, beta, S0=None, segments=8, out=None, S_final=None,
-                 return_final: bool = True, stream=None):
+                 return_final: bool = True, stream=None, workspace=None):
     """``gdn_prefill_scan``: the prefill of a dense bf16 batch [B, T, H, .] run
     as a scan over ``segments`` pieces of each sequence (for few, long
     sequences).  Returns (out, S_final) like :func:`prefill`."""
@@ -208,16 +283,19 @@ def prefill_scan(q, k, v, alpha, beta, S0=None, segments=8, out=None, S_final=No
     elif S_final is not None:
         _check(S_final, "S_final", torch.float32, dev)
     with torch.cuda.device(dev):
-        rc = lib.gdn_prefill_scan(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
-                                  _ptr(out), _ptr(S_final), B, T, H, dk, dv, int(segments),
-                                  _stream_handle(stream))
+        args = (_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(out),
+                _ptr(S_final), B, T, H, dk, dv, int(segments))
+        if workspace is None:
+            rc = lib.gdn_prefill_scan(*args, _stream_handle(stream))
+        else:
+            rc = lib.gdn_prefill_scan_ws(*args, *_ws_args(workspace), _stream_handle(stream))
     if rc != 0:
         raise GDNError("gdn_prefill_scan", rc)
     return out, S_final
 
 
 def prefill_backward(q, k, v, alpha, beta, dout, S0=None, dS_final=None, cu_seqlens=None,
-                     want_dS0: bool = True, stream=None):
+                     want_dS0: bool = True, stream=None, workspace=None):
     """Gradients of the prefill (``gdn_prefill_backward``) for
     L = <dout, out> + <dS_final, S_final>: returns dict dq, dk, dv (dtype of
     q), dalpha, dbeta (fp32) and dS0 ([N, H, dv, dk] fp32, or None when
@@ -251,11 +329,14 @@ def prefill_backward(q, k, v, alpha, beta, dout, S0=None, dS_final=None, cu_seql
              dalpha=torch.empty_like(alpha), dbeta=torch.empty_like(beta),
              dS0=torch.empty((N, H, dv, dk), dtype=torch.float32, device=dev) if want_dS0 else None)
     with torch.cuda.device(dev):
-        rc = lib.gdn_prefill_backward(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
-            _ptr(dout), _ptr(dS_final), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
-            _ptr(g["dalpha"]), _ptr(g["dbeta"]), _ptr(g["dS0"]), N, seqlen, H, dk, dv,
-            _io_code(io), _stream_handle(stream))
+        args = (_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
+                _ptr(dout), _ptr(dS_final), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+                _ptr(g["dalpha"]), _ptr(g["dbeta"]), _ptr(g["dS0"]), N, seqlen, H, dk, dv,
+                _io_code(io))
+        if workspace is None:
+            rc = lib.gdn_prefill_backward(*args, _stream_handle(stream))
+        else:
+            rc = lib.gdn_prefill_backward_ws(*args, *_ws_args(workspace), _stream_handle(stream))
     if rc != 0:
         raise GDNError("gdn_prefill_backward", rc)
     return g

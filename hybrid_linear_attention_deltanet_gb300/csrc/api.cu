@@ -1,6 +1,7 @@
 // C ABI of the library: host-side argument checks, scratch management and
 // dispatch to the kernels.  Declarations and contracts: include/gdn.h.
 #include <atomic>
+#include <cstdint>
 #include <mutex>
 
 #include "backward.cuh"
@@ -47,6 +48,13 @@ cudaMemPool_t scratch_pool() {
     }
     g_scratch_pool[dev] = pool;
   }
+  return g_scratch_pool[dev];
+}
+
+// This device's pool if a call has created it (nullptr otherwise).
+cudaMemPool_t existing_scratch_pool(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_pool_mu);
   return g_scratch_pool[dev];
 }
 
@@ -154,11 +162,44 @@ using namespace gdn;
 
 extern "C" {
 
-int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
-                const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
-                float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
-                int32_t dv, int32_t io_dtype, gdn_stream_t stream_) {
-  cudaStream_t stream = (cudaStream_t)stream_;
+}  // extern "C"
+
+namespace gdn {
+namespace {
+
+// Scratch of one prefill call: the packed batch's chunk offsets, then the
+// path's per-chunk scratch (bf16 I/O: the tensor-core path; fp32: the
+// CUDA-core path).  Zero when the call needs none.
+size_t prefill_scratch_bytes(int32_t batch, int64_t seqlen, int32_t heads, int32_t dv,
+                             int32_t io_dtype, bool varlen) {
+  const int64_t T_total = varlen ? seqlen : (int64_t)batch * seqlen;
+  const int64_t max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
+  const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
+  const size_t work_bytes = io_dtype == GDN_BF16
+                                ? prefill_tc_scratch_bytes(max_chunks, heads, dv)
+                                : prefill_simt_scratch_bytes(max_chunks, heads, dv);
+  return off_bytes + work_bytes;
+}
+
+// A caller's workspace: large enough, 256-byte aligned, overlapping nothing
+// the call reads or writes.
+int check_workspace(const void* ws, size_t ws_bytes, size_t need, const Range* used, int n_used) {
+  if (need == 0) return GDN_OK;
+  if (!ws || ws_bytes < need) return GDN_ERR_INVALID_ARG;
+  if ((uintptr_t)ws & 255u) return GDN_ERR_ALIGNMENT;
+  const Range w = span(ws, need);
+  for (int i = 0; i < n_used; ++i)
+    if (overlaps(w, used[i])) return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
+}
+
+// gdn_prefill and gdn_prefill_ws: scratch from the caller's workspace when
+// ws is not null, else stream-ordered from the library's pool.
+int prefill_common(const void* q, const void* k, const void* v, const float* alpha,
+                   const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
+                   float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                   int32_t dv, int32_t io_dtype, cudaStream_t stream, bool use_ws, void* ws,
+                   size_t ws_bytes) {
   if (batch < 1 || seqlen < 0 || heads < 1) return GDN_ERR_INVALID_ARG;
   const bool varlen = cu_seqlens != nullptr;
   const int64_t T_total = varlen ? seqlen : (int64_t)batch * seqlen;
@@ -169,20 +210,29 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(alpha) || !aligned4(beta) ||
       !aligned16(out) || !aligned16(S0) || !aligned16(S_final) || !aligned4(cu_seqlens))
     return GDN_ERR_ALIGNMENT;
-  if (varlen && T_total > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;   // int32 offsets
+  // 32-bit offsets (packed batches) and token coordinates (tensor-core path)
+  if ((varlen || io_dtype == GDN_BF16) && T_total > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
   const size_t es = io_dtype == GDN_BF16 ? 2 : 4;
   const size_t n_tok_h = (size_t)T_total * heads;
   const size_t state_bytes = (size_t)batch * heads * dv * dk * sizeof(float);
-  const Range in[] = {span(q, n_tok_h * dk * es), span(k, n_tok_h * dk * es),
-                      span(v, n_tok_h * dv * es), span(alpha, n_tok_h * 4),
-                      span(beta, n_tok_h * 4),
-                      span(S0, S0 ? state_bytes : 0),
-                      span(cu_seqlens, varlen ? ((size_t)batch + 1) * 4 : 0)};
-  const Range r_out = span(out, n_tok_h * dv * es);
-  const Range r_sf = span(S_final, S_final ? state_bytes : 0);
-  for (const Range& r : in)
-    if (overlaps(r, r_out) || overlaps(r, r_sf)) return GDN_ERR_INVALID_ARG;
+  const Range used[] = {span(q, n_tok_h * dk * es), span(k, n_tok_h * dk * es),
+                        span(v, n_tok_h * dv * es), span(alpha, n_tok_h * 4),
+                        span(beta, n_tok_h * 4),
+                        span(S0, S0 ? state_bytes : 0),
+                        span(cu_seqlens, varlen ? ((size_t)batch + 1) * 4 : 0),
+                        span(out, n_tok_h * dv * es),
+                        span(S_final, S_final ? state_bytes : 0)};
+  const int n_in = 7;
+  const Range& r_out = used[7];
+  const Range& r_sf = used[8];
+  for (int i = 0; i < n_in; ++i)
+    if (overlaps(used[i], r_out) || overlaps(used[i], r_sf)) return GDN_ERR_INVALID_ARG;
   if (overlaps(r_out, r_sf)) return GDN_ERR_INVALID_ARG;
+  const size_t need = prefill_scratch_bytes(batch, seqlen, heads, dv, io_dtype, varlen);
+  if (use_ws) {
+    const int rc = check_workspace(ws, ws_bytes, need, used, 9);
+    if (rc != GDN_OK) return rc;
+  }
 
   unsigned* status = status_ptr();
   if (!status) return GDN_ERR_CUDA;
@@ -201,13 +251,10 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
   const bool tc = io_dtype == GDN_BF16;
   a.dv = dv;
   a.allow_overlap = true;
-  const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads, dv)
-                               : prefill_simt_scratch_bytes(a.max_chunks, heads, dv);
-  void* scratch = nullptr;
-  if (off_bytes + work_bytes > 0 &&
+  void* scratch = use_ws ? ws : nullptr;
+  if (!use_ws && need > 0 &&
       (!scratch_pool() ||
-       cudaMallocFromPoolAsync(&scratch, off_bytes + work_bytes, scratch_pool(), stream) !=
-           cudaSuccess))
+       cudaMallocFromPoolAsync(&scratch, need, scratch_pool(), stream) != cudaSuccess))
     return GDN_ERR_CUDA;
   a.scratch = (char*)scratch + off_bytes;
   cudaError_t e = cudaSuccess;
@@ -216,17 +263,60 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
     e = launch_chunk_offsets(cu_seqlens, batch, T_total, (int32_t*)scratch, status, stream);
   }
   if (e == cudaSuccess) e = tc ? launch_prefill_tc(a, stream) : launch_prefill_simt(a, io_dtype, stream);
-  const cudaError_t ef = scratch ? cudaFreeAsync(scratch, stream) : cudaSuccess;
+  const cudaError_t ef = (!use_ws && scratch) ? cudaFreeAsync(scratch, stream) : cudaSuccess;
   return (e == cudaSuccess && ef == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
 }
 
-int gdn_prefill_backward(const void* q, const void* k, const void* v, const float* alpha,
-                         const float* beta, const float* S0, const int32_t* cu_seqlens,
-                         const void* dout, const float* dS_final, void* dq, void* dk, void* dv_,
-                         float* dalpha, float* dbeta, float* dS0, int32_t batch, int64_t seqlen,
-                         int32_t heads, int32_t dk_, int32_t dv, int32_t io_dtype,
-                         gdn_stream_t stream_) {
-  cudaStream_t stream = (cudaStream_t)stream_;
+}  // namespace
+}  // namespace gdn
+
+extern "C" {
+
+int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
+                const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
+                float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                int32_t dv, int32_t io_dtype, gdn_stream_t stream) {
+  return prefill_common(q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, batch, seqlen, heads,
+                        dk, dv, io_dtype, (cudaStream_t)stream, false, nullptr, 0);
+}
+
+size_t gdn_prefill_workspace_size(int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                                  int32_t dv, int32_t io_dtype, int32_t varlen) {
+  if (batch < 1 || seqlen < 0 || heads < 1 || dk != kDK || !supported_dv(dv) ||
+      (io_dtype != GDN_F32 && io_dtype != GDN_BF16))
+    return SIZE_MAX;
+  return prefill_scratch_bytes(batch, seqlen, heads, dv, io_dtype, varlen != 0);
+}
+
+int gdn_prefill_ws(const void* q, const void* k, const void* v, const float* alpha,
+                   const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
+                   float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                   int32_t dv, int32_t io_dtype, void* workspace, size_t workspace_bytes,
+                   gdn_stream_t stream) {
+  return prefill_common(q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, batch, seqlen, heads,
+                        dk, dv, io_dtype, (cudaStream_t)stream, true, workspace, workspace_bytes);
+}
+
+}  // extern "C"
+
+namespace gdn {
+namespace {
+
+size_t backward_scratch_bytes(int32_t batch, int64_t seqlen, int32_t heads, int32_t dv,
+                              int32_t io_dtype, bool varlen) {
+  const int64_t T_total = varlen ? seqlen : (int64_t)batch * seqlen;
+  const int64_t max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
+  const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 1024) : 0;
+  return off_bytes + prefill_backward_scratch_bytes(max_chunks, heads, dv, T_total, io_dtype);
+}
+
+// gdn_prefill_backward and gdn_prefill_backward_ws (workspace 1024-byte aligned)
+int backward_common(const void* q, const void* k, const void* v, const float* alpha,
+                    const float* beta, const float* S0, const int32_t* cu_seqlens,
+                    const void* dout, const float* dS_final, void* dq, void* dk, void* dv_,
+                    float* dalpha, float* dbeta, float* dS0, int32_t batch, int64_t seqlen,
+                    int32_t heads, int32_t dk_, int32_t dv, int32_t io_dtype, cudaStream_t stream,
+                    bool use_ws, void* ws, size_t ws_bytes) {
   if (batch < 1 || seqlen < 0 || heads < 1) return GDN_ERR_INVALID_ARG;
   const bool varlen = cu_seqlens != nullptr;
   const int64_t T_total = varlen ? seqlen : (int64_t)batch * seqlen;
@@ -241,22 +331,31 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   if (!aligned4(alpha) || !aligned4(beta) || !aligned4(dalpha) || !aligned4(dbeta) ||
       !aligned4(cu_seqlens))
     return GDN_ERR_ALIGNMENT;
-  if (varlen && T_total > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+  if ((varlen || io_dtype == GDN_BF16) && T_total > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
   const size_t es = io_dtype == GDN_BF16 ? 2 : 4;
   const size_t nth = (size_t)T_total * heads;
   const size_t state_bytes = (size_t)batch * heads * dv * dk_ * sizeof(float);
-  const Range in[] = {span(q, nth * dk_ * es), span(k, nth * dk_ * es), span(v, nth * dv * es),
-                      span(alpha, nth * 4), span(beta, nth * 4), span(S0, S0 ? state_bytes : 0),
-                      span(cu_seqlens, varlen ? ((size_t)batch + 1) * 4 : 0),
-                      span(dout, nth * dv * es), span(dS_final, dS_final ? state_bytes : 0)};
-  const Range outs[] = {span(dq, nth * dk_ * es), span(dk, nth * dk_ * es),
-                        span(dv_, nth * dv * es), span(dalpha, nth * 4), span(dbeta, nth * 4),
-                        span(dS0, dS0 ? state_bytes : 0)};
-  for (const Range& o : outs) {
-    for (const Range& r : in)
-      if (overlaps(r, o)) return GDN_ERR_INVALID_ARG;
-    for (const Range& o2 : outs)
-      if (&o2 != &o && overlaps(o, o2)) return GDN_ERR_INVALID_ARG;
+  const Range all[] = {span(q, nth * dk_ * es), span(k, nth * dk_ * es), span(v, nth * dv * es),
+                       span(alpha, nth * 4), span(beta, nth * 4), span(S0, S0 ? state_bytes : 0),
+                       span(cu_seqlens, varlen ? ((size_t)batch + 1) * 4 : 0),
+                       span(dout, nth * dv * es), span(dS_final, dS_final ? state_bytes : 0),
+                       span(dq, nth * dk_ * es), span(dk, nth * dk_ * es),
+                       span(dv_, nth * dv * es), span(dalpha, nth * 4), span(dbeta, nth * 4),
+                       span(dS0, dS0 ? state_bytes : 0)};
+  const int n_in = 9, n_all = 15;
+  for (int o = n_in; o < n_all; ++o) {
+    for (int r = 0; r < n_in; ++r)
+      if (overlaps(all[r], all[o])) return GDN_ERR_INVALID_ARG;
+    for (int o2 = n_in; o2 < n_all; ++o2)
+      if (o2 != o && overlaps(all[o], all[o2])) return GDN_ERR_INVALID_ARG;
+  }
+  const int64_t max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
+  if (max_chunks * heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;   // grid bound
+  const size_t need = backward_scratch_bytes(batch, seqlen, heads, dv, io_dtype, varlen);
+  if (use_ws) {
+    if (ws && ((uintptr_t)ws & 1023u)) return GDN_ERR_ALIGNMENT;
+    const int rc = check_workspace(ws, ws_bytes, need, all, n_all);
+    if (rc != GDN_OK) return rc;
   }
   unsigned* status = status_ptr();
   if (!status) return GDN_ERR_CUDA;
@@ -269,15 +368,11 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   a.map.N = batch;
   a.map.T = varlen ? T_total : seqlen;
   a.map.chunks_per_seq = varlen ? 0 : (seqlen + kC - 1) / kC;
-  a.max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
-  if (a.max_chunks * heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;   // grid bound
+  a.max_chunks = max_chunks;
   const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 1024) : 0;
-  const size_t work_bytes =
-      prefill_backward_scratch_bytes(a.max_chunks, heads, dv, T_total, io_dtype);
-  void* scratch = nullptr;
-  if (!scratch_pool() ||
-      cudaMallocFromPoolAsync(&scratch, off_bytes + work_bytes, scratch_pool(), stream) !=
-          cudaSuccess)
+  void* scratch = use_ws ? ws : nullptr;
+  if (!use_ws && (!scratch_pool() ||
+                  cudaMallocFromPoolAsync(&scratch, need, scratch_pool(), stream) != cudaSuccess))
     return GDN_ERR_CUDA;
   a.scratch = (char*)scratch + off_bytes;
   cudaError_t e = cudaSuccess;
@@ -288,8 +383,70 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   if (e == cudaSuccess)
     e = launch_prefill_backward(a, dout, dS_final, dq, dk, dv_, dalpha, dbeta, dS0, io_dtype,
                                 stream);
-  const cudaError_t ef = cudaFreeAsync(scratch, stream);
+  const cudaError_t ef = use_ws ? cudaSuccess : cudaFreeAsync(scratch, stream);
   return (e == cudaSuccess && ef == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" {
+
+int gdn_prefill_backward(const void* q, const void* k, const void* v, const float* alpha,
+                         const float* beta, const float* S0, const int32_t* cu_seqlens,
+                         const void* dout, const float* dS_final, void* dq, void* dk, void* dv_,
+                         float* dalpha, float* dbeta, float* dS0, int32_t batch, int64_t seqlen,
+                         int32_t heads, int32_t dk_, int32_t dv, int32_t io_dtype,
+                         gdn_stream_t stream) {
+  return backward_common(q, k, v, alpha, beta, S0, cu_seqlens, dout, dS_final, dq, dk, dv_,
+                         dalpha, dbeta, dS0, batch, seqlen, heads, dk_, dv, io_dtype,
+                         (cudaStream_t)stream, false, nullptr, 0);
+}
+
+size_t gdn_prefill_backward_workspace_size(int32_t batch, int64_t seqlen, int32_t heads,
+                                           int32_t dk, int32_t dv, int32_t io_dtype,
+                                           int32_t varlen) {
+  if (batch < 1 || seqlen < 0 || heads < 1 || dk != kDK || !supported_dv(dv) ||
+      (io_dtype != GDN_F32 && io_dtype != GDN_BF16))
+    return SIZE_MAX;
+  return backward_scratch_bytes(batch, seqlen, heads, dv, io_dtype, varlen != 0);
+}
+
+int gdn_prefill_backward_ws(const void* q, const void* k, const void* v, const float* alpha,
+                            const float* beta, const float* S0, const int32_t* cu_seqlens,
+                            const void* dout, const float* dS_final, void* dq, void* dk,
+                            void* dv_, float* dalpha, float* dbeta, float* dS0, int32_t batch,
+                            int64_t seqlen, int32_t heads, int32_t dk_, int32_t dv,
+                            int32_t io_dtype, void* workspace, size_t workspace_bytes,
+                            gdn_stream_t stream) {
+  return backward_common(q, k, v, alpha, beta, S0, cu_seqlens, dout, dS_final, dq, dk, dv_,
+                         dalpha, dbeta, dS0, batch, seqlen, heads, dk_, dv, io_dtype,
+                         (cudaStream_t)stream, true, workspace, workspace_bytes);
+}
+
+int gdn_release_scratch(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  cudaMemPool_t pool = existing_scratch_pool(dev);
+  if (!pool) return GDN_OK;
+  // the pool only returns memory whose frees have completed: finish every
+  // stream's work on this device first
+  if (cudaDeviceSynchronize() != cudaSuccess) return GDN_ERR_CUDA;
+  return cudaMemPoolTrimTo(pool, 0) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_testing_scratch_reserved(uint64_t* bytes) {
+  if (!bytes) return GDN_ERR_INVALID_ARG;
+  *bytes = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  cudaMemPool_t pool = existing_scratch_pool(dev);
+  if (!pool) return GDN_OK;
+  uint64_t v = 0;
+  if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &v) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  *bytes = v;
+  return GDN_OK;
 }
 
 int gdn_decode_step(const void* q, const void* k, const void* v, const float* alpha,

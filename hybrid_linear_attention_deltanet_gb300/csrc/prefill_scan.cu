@@ -111,21 +111,51 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 using namespace gdn;
 
-extern "C" int gdn_prefill_scan(const void* q, const void* k, const void* v, const float* alpha,
-                                const float* beta, const float* S0, void* out, float* S_final,
-                                int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
-                                int32_t dv, int32_t segments, gdn_stream_t stream_) {
-  cudaStream_t stream = (cudaStream_t)stream_;
-  if (batch < 1 || seqlen < 0 || heads < 1 || segments < 1) return GDN_ERR_INVALID_ARG;
-  if (dk != kDK || !supported_dv(dv)) return GDN_ERR_UNSUPPORTED;
+namespace gdn {
+namespace {
+
+// Segmentation of a dense batch of B sequences of T tokens into P pieces of
+// whole chunks (P = 1: nothing to split).
+struct ScanPlan {
+  int64_t seg_len = 0;   // tokens per segment (a multiple of the chunk)
+  int32_t P = 1;
+  int64_t max_chunks = 0;
+  size_t cu_bytes = 0, tc_bytes = 0, ss = 0;
+  size_t bytes() const { return P > 1 ? 2 * cu_bytes + tc_bytes + 5 * ss : 0; }
+};
+
+ScanPlan plan_scan(int32_t batch, int64_t seqlen, int32_t heads, int32_t dv, int32_t segments) {
+  ScanPlan sp;
   const int64_t chunks = (seqlen + kC - 1) / kC;
   const int64_t seg_chunks = (chunks + segments - 1) / segments;
-  const int64_t seg_len = seg_chunks * kC;
-  const int64_t P64 = seg_len > 0 ? (seqlen + seg_len - 1) / seg_len : 1;
-  if (P64 <= 1)   // nothing to split: the plain prefill
-    return gdn_prefill(q, k, v, alpha, beta, S0, nullptr, out, S_final, batch, seqlen, heads, dk,
-                       dv, GDN_BF16, stream_);
-  const int32_t P = (int32_t)P64;
+  sp.seg_len = seg_chunks * kC;
+  const int64_t P64 = sp.seg_len > 0 ? (seqlen + sp.seg_len - 1) / sp.seg_len : 1;
+  sp.P = P64 > 1 && P64 < 0x7fffffffLL ? (int32_t)P64 : 1;
+  if (sp.P <= 1) return sp;
+  const int64_t n_seg = (int64_t)batch * sp.P;
+  const int64_t T_total = (int64_t)batch * seqlen;
+  sp.max_chunks = max_chunks_bound((int32_t)n_seg, T_total, true, 0);
+  // segmented cu_seqlens and chunk offsets, the per-chunk images, and five
+  // per-(segment, head) states: starts of passes 1 and 2, B, F, ends
+  sp.cu_bytes = align_up((size_t)(n_seg + 1) * 4, 1024);
+  sp.tc_bytes = align_up(prefill_tc_scratch_bytes(sp.max_chunks, heads, dv), 1024);
+  sp.ss = align_up((size_t)n_seg * heads * dv * kDK * 4, 1024);
+  return sp;
+}
+
+int scan_common(const void* q, const void* k, const void* v, const float* alpha,
+                const float* beta, const float* S0, void* out, float* S_final, int32_t batch,
+                int64_t seqlen, int32_t heads, int32_t dk, int32_t dv, int32_t segments,
+                cudaStream_t stream, bool use_ws, void* ws, size_t ws_bytes) {
+  if (batch < 1 || seqlen < 0 || heads < 1 || segments < 1) return GDN_ERR_INVALID_ARG;
+  if (dk != kDK || !supported_dv(dv)) return GDN_ERR_UNSUPPORTED;
+  const ScanPlan sp = plan_scan(batch, seqlen, heads, dv, segments);
+  if (sp.P <= 1)   // nothing to split: the plain prefill
+    return use_ws ? gdn_prefill_ws(q, k, v, alpha, beta, S0, nullptr, out, S_final, batch, seqlen,
+                                   heads, dk, dv, GDN_BF16, ws, ws_bytes, (gdn_stream_t)stream)
+                  : gdn_prefill(q, k, v, alpha, beta, S0, nullptr, out, S_final, batch, seqlen,
+                                heads, dk, dv, GDN_BF16, (gdn_stream_t)stream);
+  const int32_t P = sp.P;
   const int64_t T_total = (int64_t)batch * seqlen;
   const int64_t n_seg = (int64_t)batch * P;
   if (T_total > 0x7fffffffLL || n_seg * heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
@@ -146,6 +176,15 @@ extern "C" int gdn_prefill_scan(const void* q, const void* k, const void* v, con
   for (const R& r : ins)
     if (ov(r, ro) || ov(r, rs)) return GDN_ERR_INVALID_ARG;
   if (ov(ro, rs)) return GDN_ERR_INVALID_ARG;
+  const size_t need = sp.bytes();
+  if (use_ws) {   // the caller's workspace: large enough, 1024-byte aligned, apart from the tensors
+    if (!ws || ws_bytes < need) return GDN_ERR_INVALID_ARG;
+    if ((uintptr_t)ws & 1023u) return GDN_ERR_ALIGNMENT;
+    const R w = span(ws, need);
+    for (const R& r : ins)
+      if (ov(w, r)) return GDN_ERR_INVALID_ARG;
+    if (ov(w, ro) || ov(w, rs)) return GDN_ERR_INVALID_ARG;
+  }
 
   unsigned* status = status_ptr();
   if (!status) return GDN_ERR_CUDA;
@@ -154,33 +193,25 @@ extern "C" int gdn_prefill_scan(const void* q, const void* k, const void* v, con
   a.status = status; a.out = out;
   a.map.N = (int32_t)n_seg;
   a.map.T = T_total;
-  a.max_chunks = max_chunks_bound((int32_t)n_seg, T_total, true, 0);
+  a.max_chunks = sp.max_chunks;
   a.allow_overlap = false;   // prep on every SM first: the state passes need most of them
 
-  // scratch: segmented cu_seqlens and chunk offsets, the per-chunk images, and
-  // five per-(segment, head) states: starts of passes 1 and 2, B, F, ends
-  const size_t cu_bytes = align_up((size_t)(n_seg + 1) * 4, 1024);
-  const size_t tc_bytes = align_up(prefill_tc_scratch_bytes(a.max_chunks, heads, dv), 1024);
-  const size_t seg_state = (size_t)n_seg * heads * dv * dk * 4;
-  const size_t ss = align_up(seg_state, 1024);
-  void* scratch = nullptr;
-  if (scratch_alloc(&scratch, 2 * cu_bytes + tc_bytes + 5 * ss, stream) != cudaSuccess)
-    return GDN_ERR_CUDA;
+  void* scratch = use_ws ? ws : nullptr;
+  if (!use_ws && scratch_alloc(&scratch, need, stream) != cudaSuccess) return GDN_ERR_CUDA;
   char* p = (char*)scratch;
-  int32_t* seg_cu = (int32_t*)p; p += cu_bytes;
-  int32_t* chunk_off = (int32_t*)p; p += cu_bytes;
-  a.scratch = p; p += tc_bytes;
-  float* S0seg = (float*)p; p += ss;
-  float* Iseg = (float*)p; p += ss;
-  float* Bseg = (float*)p; p += ss;
-  float* Fseg = (float*)p; p += ss;
+  int32_t* seg_cu = (int32_t*)p; p += sp.cu_bytes;
+  int32_t* chunk_off = (int32_t*)p; p += sp.cu_bytes;
+  a.scratch = p; p += sp.tc_bytes;
+  float* S0seg = (float*)p; p += sp.ss;
+  float* Iseg = (float*)p; p += sp.ss;
+  float* Bseg = (float*)p; p += sp.ss;
+  float* Fseg = (float*)p; p += sp.ss;
   float* Eseg = (float*)p;
   a.map.cu_seqlens = seg_cu;
   a.map.chunk_off = chunk_off;
-
   cudaError_t e = cudaSuccess;
   seg_cu_kernel<<<(unsigned)((n_seg + 1 + 255) / 256), 256, 0, stream>>>(seg_cu, batch, seqlen,
-                                                                          seg_len, P);
+                                                                          sp.seg_len, P);
   count_launches(1);
   if ((e = cudaGetLastError()) == cudaSuccess)
     e = launch_chunk_offsets(seg_cu, (int32_t)n_seg, T_total, chunk_off, status, stream);
@@ -214,6 +245,35 @@ extern "C" int gdn_prefill_scan(const void* q, const void* k, const void* v, con
       e = cudaMemcpyAsync(S_final + b * one, Eseg + ((size_t)b * P + P - 1) * one, one * 4,
                           cudaMemcpyDeviceToDevice, stream);
   }
-  const cudaError_t ef = scratch_free(scratch, stream);
+  const cudaError_t ef = use_ws ? cudaSuccess : scratch_free(scratch, stream);
   return (e == cudaSuccess && ef == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" int gdn_prefill_scan(const void* q, const void* k, const void* v, const float* alpha,
+                                const float* beta, const float* S0, void* out, float* S_final,
+                                int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                                int32_t dv, int32_t segments, gdn_stream_t stream) {
+  return scan_common(q, k, v, alpha, beta, S0, out, S_final, batch, seqlen, heads, dk, dv,
+                     segments, (cudaStream_t)stream, false, nullptr, 0);
+}
+
+extern "C" size_t gdn_prefill_scan_workspace_size(int32_t batch, int64_t seqlen, int32_t heads,
+                                                  int32_t dk, int32_t dv, int32_t segments) {
+  if (batch < 1 || seqlen < 0 || heads < 1 || segments < 1 || dk != kDK || !supported_dv(dv))
+    return SIZE_MAX;
+  const ScanPlan sp = plan_scan(batch, seqlen, heads, dv, segments);
+  if (sp.P <= 1) return gdn_prefill_workspace_size(batch, seqlen, heads, dk, dv, GDN_BF16, 0);
+  return sp.bytes();
+}
+
+extern "C" int gdn_prefill_scan_ws(const void* q, const void* k, const void* v,
+                                   const float* alpha, const float* beta, const float* S0,
+                                   void* out, float* S_final, int32_t batch, int64_t seqlen,
+                                   int32_t heads, int32_t dk, int32_t dv, int32_t segments,
+                                   void* workspace, size_t workspace_bytes, gdn_stream_t stream) {
+  return scan_common(q, k, v, alpha, beta, S0, out, S_final, batch, seqlen, heads, dk, dv,
+                     segments, (cudaStream_t)stream, true, workspace, workspace_bytes);
 }

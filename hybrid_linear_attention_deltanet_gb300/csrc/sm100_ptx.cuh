@@ -56,6 +56,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of the phase with the given parity (never suspends).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase with the given parity to complete, giving up after
 // `limit_ns` nanoseconds of wall time.  Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
@@ -133,6 +144,24 @@ __device__ __forceinline__ void bulk_wait_all() {
 __device__ __forceinline__ void bulk_wait_all_but_newest() {
   asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");
 }
+// 16-byte asynchronous copy global -> shared by one thread (non-bulk
+// cp.async: many threads reach a far higher per-SM rate than TMA copies);
+// src_bytes < 16 zero-fills the rest (0: the 16 bytes become zero and
+// nothing is read).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes = 16) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+// Arrive on `bar` once every cp.async this thread started so far has
+// completed; the arrival counts against the barrier's expected count.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes).
 // dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes,
@@ -177,6 +206,13 @@ __device__ __forceinline__ void prefetch_l2_3d(const CUtensorMap* map, int32_t x
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                    (uint64_t)map),
                "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_l2_4d(const CUtensorMap* map, int32_t x, int32_t y,
+                                               int32_t z, int32_t w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   (uint64_t)map),
+               "r"(x), "r"(y), "r"(z), "r"(w)
                : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {

@@ -96,13 +96,60 @@ enum gdn_status {
  * Scratch: intermediate per-chunk factors are kept in device memory obtained
  * stream-ordered on `stream` (cudaMallocFromPoolAsync / cudaFreeAsync) from a
  * per-device pool owned by the library.  The pool keeps freed scratch mapped
- * for later calls, so it holds the largest scratch any call needed until the
- * process exits (about 0.33 GB for 32K tokens of a 6-head bf16 layer).
+ * for later calls (mapping it again after every synchronisation costs about
+ * as much as a call), so it holds the largest scratch any call needed until
+ * gdn_release_scratch() or process exit (about 0.33 GB for 32K tokens of a
+ * 6-head bf16 layer).  Callers that manage device memory themselves use
+ * gdn_prefill_ws instead.
  */
 int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
                 const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
                 float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
                 int32_t dv, int32_t io_dtype, gdn_stream_t stream);
+
+/*
+ * gdn_prefill_workspace_size -- bytes of scratch gdn_prefill_ws needs for this
+ * problem: batch, seqlen, heads, dk, dv and io_dtype as for gdn_prefill;
+ * varlen != 0 for a packed batch (cu_seqlens given), 0 for a dense one.
+ * Host-side arithmetic only (no CUDA call).  Layout of the scratch: the
+ * packed batch's per-sequence chunk offsets (4 (batch + 1) bytes rounded up
+ * to 256), then the path's per-chunk scratch over max_chunks = batch *
+ * ceil(seqlen / 64) (dense) or (seqlen + 63 batch) / 64 (packed) chunks:
+ *   bf16 I/O  max_chunks * heads * 107520 bytes of operand images at dv = 256
+ *             (141312 at dv = 512), then one 4-byte flag per (chunk, head)
+ *             rounded up to 256;
+ *   fp32 I/O  the CUDA-core path's four per-(chunk, head) arrays.
+ * 0 when the call needs no scratch; SIZE_MAX for arguments gdn_prefill would
+ * reject as invalid or unsupported.
+ */
+size_t gdn_prefill_workspace_size(int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                                  int32_t dv, int32_t io_dtype, int32_t varlen);
+
+/*
+ * gdn_prefill_ws -- gdn_prefill with its scratch in a caller-owned device
+ * workspace instead of the library's pool: same arguments and results, plus
+ * `workspace` (device, 256-byte aligned) of `workspace_bytes` >=
+ * gdn_prefill_workspace_size(...).  The call allocates nothing.  The
+ * workspace is in use until the work queued on `stream` completes; calls
+ * that overlap on the GPU must not share one.  Errors, before any launch:
+ * GDN_ERR_INVALID_ARG for a null or too small workspace (when the problem
+ * needs one) or one that overlaps a tensor of the call, GDN_ERR_ALIGNMENT for
+ * a misaligned one; otherwise as gdn_prefill.
+ */
+int gdn_prefill_ws(const void* q, const void* k, const void* v, const float* alpha,
+                   const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
+                   float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                   int32_t dv, int32_t io_dtype, void* workspace, size_t workspace_bytes,
+                   gdn_stream_t stream);
+
+/*
+ * gdn_release_scratch -- hand the library's scratch pool on the current device
+ * back to the system: synchronises the device (every stream's work, so that
+ * pending stream-ordered frees complete), then trims the pool to zero bytes.
+ * Later calls map scratch again as they need it.  GDN_OK (also when no call
+ * has created the pool yet) or GDN_ERR_CUDA.
+ */
+int gdn_release_scratch(void);
 
 /*
  * gdn_prefill_scan -- gdn_prefill for a dense bf16 batch of long sequences,
@@ -138,6 +185,22 @@ int gdn_prefill_scan(const void* q, const void* k, const void* v, const float* a
                      gdn_stream_t stream);
 
 /*
+ * gdn_prefill_scan_workspace_size / gdn_prefill_scan_ws -- the same with the
+ * scratch in a caller-owned device workspace (1024-byte aligned) of at least
+ * gdn_prefill_scan_workspace_size(batch, seqlen, heads, dk, dv, segments)
+ * bytes (SIZE_MAX for invalid arguments).  When the sequences are too short to
+ * cut, the size and the call are gdn_prefill_ws's.  Workspace rules and errors
+ * as gdn_prefill_ws.
+ */
+size_t gdn_prefill_scan_workspace_size(int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                                       int32_t dv, int32_t segments);
+int gdn_prefill_scan_ws(const void* q, const void* k, const void* v, const float* alpha,
+                        const float* beta, const float* S0, void* out, float* S_final,
+                        int32_t batch, int64_t seqlen, int32_t heads, int32_t dk, int32_t dv,
+                        int32_t segments, void* workspace, size_t workspace_bytes,
+                        gdn_stream_t stream);
+
+/*
  * gdn_prefill_backward -- gradients of the prefill, for training with the
  * chunked kernel (Appendix A.3, last paragraph: the pages train with it).
  *
@@ -165,6 +228,25 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
                          float* dalpha, float* dbeta, float* dS0, int32_t batch, int64_t seqlen,
                          int32_t heads, int32_t dk_dim, int32_t dv_dim, int32_t io_dtype,
                          gdn_stream_t stream);
+
+/*
+ * gdn_prefill_backward_workspace_size / gdn_prefill_backward_ws -- the
+ * backward with its scratch in a caller-owned device workspace (1024-byte
+ * aligned) of at least gdn_prefill_backward_workspace_size(batch, seqlen,
+ * heads, dk, dv, io_dtype, varlen) bytes (SIZE_MAX for invalid arguments).
+ * Workspace rules and errors as gdn_prefill_ws; results equal
+ * gdn_prefill_backward's bit for bit.
+ */
+size_t gdn_prefill_backward_workspace_size(int32_t batch, int64_t seqlen, int32_t heads,
+                                           int32_t dk_dim, int32_t dv_dim, int32_t io_dtype,
+                                           int32_t varlen);
+int gdn_prefill_backward_ws(const void* q, const void* k, const void* v, const float* alpha,
+                            const float* beta, const float* S0, const int32_t* cu_seqlens,
+                            const void* dout, const float* dS_final, void* dq, void* dk, void* dv,
+                            float* dalpha, float* dbeta, float* dS0, int32_t batch,
+                            int64_t seqlen, int32_t heads, int32_t dk_dim, int32_t dv_dim,
+                            int32_t io_dtype, void* workspace, size_t workspace_bytes,
+                            gdn_stream_t stream);
 
 /*
  * gdn_prefill_noalloc -- gdn_prefill for callers that cannot allocate.

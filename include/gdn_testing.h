@@ -132,6 +132,14 @@ int32_t gdn_testing_last_prefill_form(void);
  */
 int gdn_testing_bounded_wait(int32_t which, int64_t limit_ns, gdn_stream_t stream);
 
+/*
+ * gdn_testing_scratch_reserved -- bytes the library's scratch pool on the
+ * current device holds mapped right now (cudaMemPoolAttrReservedMemCurrent;
+ * 0 when no call has created the pool).  GDN_ERR_INVALID_ARG for a null
+ * pointer, GDN_ERR_CUDA when the attribute cannot be read.
+ */
+int gdn_testing_scratch_reserved(uint64_t* bytes);
+
 #ifdef __cplusplus
 }
 #endif

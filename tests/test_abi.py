@@ -5,7 +5,9 @@ call here reaches a CUDA runtime function.
 The pointers below are fake addresses.  Every call therefore asserts an exact
 host-check code (1-3): a call that got past all host checks would go on to the
 device (code 4 on a machine without one, a launch on fake addresses on a
-machine with one).  The launch-counter fixture fails any test that launches."""
+machine with one).  The launch-counter fixture fails any test that launches,
+and the tests that pass fake addresses do not run at all where a CUDA device
+is visible, so that a missed host check can never reach a GPU."""
 import ctypes
 import glob
 import os
@@ -36,6 +38,20 @@ def lib():
         from hybrid_linear_attention_deltanet_gb300 import _build
         _build.build()
     return gdn.load()
+
+
+def _device_visible() -> bool:
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+# tests that hand the library fake device addresses
+fake_addresses = pytest.mark.skipif(_device_visible(),
+                                    reason="fake device addresses are only passed where no GPU "
+                                           "is visible")
 
 
 @pytest.fixture(autouse=True)
@@ -81,6 +97,7 @@ def _prefill(lib, q=A16, k=A16, v=A16, alpha=A16, beta=A16, S0=None, cu=None, ou
                            None)
 
 
+@fake_addresses
 def test_prefill_rejects_bad_host_arguments(lib):
     assert _prefill(lib, q=None) == 1
     assert _prefill(lib, out=None) == 1
@@ -104,6 +121,7 @@ def test_prefill_rejects_bad_host_arguments(lib):
                     beta=P(0x500000), out=P(0x100000 + 4096)) == 1
 
 
+@fake_addresses
 def test_decode_rejects_bad_host_arguments(lib):
     f = lambda **kw: lib.gdn_decode_step(kw.get("q", A16), A16, A16, A16, A16,
                                          kw.get("S", P(0x800000)), kw.get("out", P(0x900000)),
@@ -124,6 +142,7 @@ def _prepare(lib, qkv=A16, conv_w=A16, a_raw=A16, b_raw=A16, cu=None, sin=None, 
                            batch, T, H, dk, dv, io, None)
 
 
+@fake_addresses
 def test_prepare_rejects_bad_host_arguments(lib):
     assert _prepare(lib, batch=0) == 1
     assert _prepare(lib, T=-1) == 1
@@ -140,6 +159,7 @@ def test_prepare_rejects_bad_host_arguments(lib):
     assert _prepare(lib, k=P(0x100000 + 1024)) == 1                 # two outputs overlap
 
 
+@fake_addresses
 def test_prepare_decode_rejects_bad_host_arguments(lib):
     f = lambda st=P(0x700000), q=P(0x100000), H=6, dv=256, io=1: lib.gdn_prepare_decode_step(
         A16, A16, A16, A16, A16, A16, st, q, P(0x200000), P(0x300000), P(0x400000), P(0x500000),
@@ -151,6 +171,7 @@ def test_prepare_decode_rejects_bad_host_arguments(lib):
     assert f(q=P(0x700000 + 2048)) == 1                                # q inside the state
 
 
+@fake_addresses
 def test_output_norm_gate_rejects_bad_host_arguments(lib):
     f = lambda o=A16, g=P(0x200000), w=P(0x300000), eps=1e-5, act=0, y=P(0x400000), dv=256, io=1: \
         lib.gdn_output_norm_gate(o, g, w, ctypes.c_float(eps), act, y, 64, 6, dv, io, None)
@@ -164,6 +185,7 @@ def test_output_norm_gate_rejects_bad_host_arguments(lib):
     assert f(y=P(0x10000 + 1024)) == 1                                # y partly over o
 
 
+@fake_addresses
 def test_prefill_backward_rejects_bad_host_arguments(lib):
     f = lambda q=A16, dout=P(0x600000), dq=P(0x100000), dS0=None, dv=256, io=1, batch=1, T=64: \
         lib.gdn_prefill_backward(q, A16b, A16b, A16b, A16b, None, None, dout, None, dq,
@@ -187,6 +209,7 @@ def test_fault_hook_rejects_bad_arguments(lib):
     assert f(1, 3_000_000_000, None) == 1
 
 
+@fake_addresses
 def test_prefill_scan_rejects_bad_host_arguments(lib):
     f = lambda q=A16, out=A16b, batch=1, T=4096, dv=256, seg=4: lib.gdn_prefill_scan(
         q, A16, A16, A16, A16, None, out, None, batch, T, 6, 256, dv, seg, None)
@@ -195,3 +218,89 @@ def test_prefill_scan_rejects_bad_host_arguments(lib):
     assert f(dv=384) == 2
     assert f(q=MIS) == 3
     assert f(out=A16) == 1                                              # out over q
+
+
+SIZE_MAX = ctypes.c_size_t(-1).value
+
+
+def _ws_size_fns(lib):
+    sz, i32, i64 = ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64
+    lib.gdn_prefill_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32]
+    lib.gdn_prefill_workspace_size.restype = sz
+    lib.gdn_prefill_scan_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32]
+    lib.gdn_prefill_scan_workspace_size.restype = sz
+    lib.gdn_prefill_backward_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32]
+    lib.gdn_prefill_backward_workspace_size.restype = sz
+    return (lib.gdn_prefill_workspace_size, lib.gdn_prefill_scan_workspace_size,
+            lib.gdn_prefill_backward_workspace_size)
+
+
+def _up(x, a):
+    return (x + a - 1) // a * a
+
+
+def test_workspace_size_follows_the_documented_layout(lib):
+    """gdn.h's layout of the bf16 prefill scratch, restated: chunk offsets of a
+    packed batch (4 (N + 1) bytes rounded to 256), then one operand image per
+    (chunk, head) of 107520 bytes at dv = 256 (141312 at dv = 512) over the
+    chunk bound, then a 4-byte flag per (chunk, head) rounded to 256."""
+    ws, _, _ = _ws_size_fns(lib)
+    for (B, T, H, dv, varlen) in [(4, 8192, 6, 256, 0), (1, 65536, 6, 256, 0), (3, 1000, 6, 256, 1),
+                                  (16, 388611, 6, 256, 1), (1, 100, 2, 512, 0), (2, 0, 6, 256, 1)]:
+        chunks = B * -(-T // 64) if not varlen else (T + 63 * B) // 64
+        items = chunks * H
+        img = 107520 if dv == 256 else 141312
+        want = items * img + _up(items * 4, 256) + (_up(4 * (B + 1), 256) if varlen else 0)
+        assert ws(B, T, H, 256, dv, 1, varlen) == want, (B, T, H, dv, varlen)
+
+
+def test_workspace_size_queries_reject_bad_arguments(lib):
+    ws, ws_scan, ws_bwd = _ws_size_fns(lib)
+    for f in (ws, ws_bwd):
+        assert f(0, 64, 6, 256, 256, 1, 0) == SIZE_MAX
+        assert f(1, 64, 6, 128, 256, 1, 0) == SIZE_MAX
+        assert f(1, 64, 6, 256, 384, 1, 0) == SIZE_MAX
+        assert f(1, 64, 6, 256, 256, 7, 0) == SIZE_MAX
+        assert f(1, -1, 6, 256, 256, 1, 0) == SIZE_MAX
+    assert ws_scan(1, 4096, 6, 256, 256, 0) == SIZE_MAX
+    assert ws_scan(1, 4096, 0, 256, 256, 4) == SIZE_MAX
+
+
+def test_workspace_sizes_scale_with_the_problem(lib):
+    ws, ws_scan, ws_bwd = _ws_size_fns(lib)
+    # fp32 I/O (CUDA-core path): linear in the number of (chunk, head) units
+    a, b = ws(1, 64 * 8, 6, 256, 256, 0, 0), ws(1, 64 * 16, 6, 256, 256, 0, 0)
+    assert 0 < a < b and b - a == a - ws(1, 0, 6, 256, 256, 0, 0)
+    # a sequence too short to cut: the scan's scratch is the plain prefill's
+    assert ws_scan(1, 64, 6, 256, 256, 8) == ws(1, 64, 6, 256, 256, 1, 0)
+    # cut: the per-segment states come on top of the images
+    assert ws_scan(1, 65536, 6, 256, 256, 8) > ws(1, 65536, 6, 256, 256, 1, 0)
+    # the backward holds at least the forward's images (bf16) and grows with T
+    assert ws_bwd(4, 8192, 6, 256, 256, 1, 0) > ws(4, 8192, 6, 256, 256, 1, 0)
+    assert ws_bwd(1, 1024, 6, 256, 256, 0, 0) < ws_bwd(1, 2048, 6, 256, 256, 0, 0)
+
+
+@fake_addresses
+def test_workspace_entry_points_reject_bad_workspaces(lib):
+    sz, i32, i64 = ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64
+    f = lib.gdn_prefill_ws
+    f.argtypes = [P] * 9 + [i32, i64, i32, i32, i32, i32, P, sz, P]
+    need = _ws_size_fns(lib)[0](1, 64, 6, 256, 256, 1, 0)
+    ins = dict(q=P(0x100000), k=P(0x200000), v=P(0x300000), alpha=P(0x400000),
+               beta=P(0x500000), out=P(0x600000))
+    call = lambda ws, n: f(ins["q"], ins["k"], ins["v"], ins["alpha"], ins["beta"], None, None,
+                           ins["out"], None, 1, 64, 6, 256, 256, 1, ws, n, None)
+    assert call(None, need) == 1                      # the problem needs scratch
+    assert call(P(0x10000000), need - 1) == 1          # too small
+    assert call(P(0x10000010), need) == 3             # not 256-byte aligned
+    assert call(P(0x100000), need) == 1                # over q
+    g = lib.gdn_prefill_backward_ws
+    g.argtypes = [P] * 15 + [i32, i64, i32, i32, i32, i32, P, sz, P]
+    needb = _ws_size_fns(lib)[2](1, 64, 6, 256, 256, 1, 0)
+    callb = lambda ws, n: g(P(0x100000), P(0x200000), P(0x300000), P(0x400000), P(0x500000),
+                            None, None, P(0x600000), None, P(0x700000), P(0x800000),
+                            P(0x900000), P(0xa00000), P(0xb00000), None, 1, 64, 6, 256, 256, 1,
+                            ws, n, None)
+    assert callb(None, needb) == 1
+    assert callb(P(0x10000200), needb) == 3           # not 1024-byte aligned
+    assert callb(P(0x10000000), needb - 1) == 1
