@@ -68,7 +68,7 @@ def load():
     lib.gdn_kernel_launches.restype = ctypes.c_uint64
     lib.gdn_prefill_path.argtypes = [ctypes.c_int32]
     lib.gdn_prefill_path.restype = ctypes.c_char_p
-    lib.gdn_prefill_scan.argtypes = [vp] * 8 + [i32, i64, i32, i32, i32, i32, vp]
+    lib.gdn_prefill_scan.argtypes = [vp] * 9 + [i32, i64, i32, i32, i32, i32, i32, vp]
     lib.gdn_prefill_scan.restype = ctypes.c_int
     lib.gdn_prefill_backward.argtypes = [vp] * 15 + [i32, i64, i32, i32, i32, i32, vp]
     lib.gdn_prefill_backward.restype = ctypes.c_int
@@ -87,9 +87,10 @@ def load():
     lib.gdn_prefill_workspace_size.restype = sz
     lib.gdn_prefill_ws.argtypes = [vp] * 9 + [i32, i64, i32, i32, i32, i32, vp, sz, vp]
     lib.gdn_prefill_ws.restype = ctypes.c_int
-    lib.gdn_prefill_scan_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32]
+    lib.gdn_prefill_scan_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32, i32]
     lib.gdn_prefill_scan_workspace_size.restype = sz
-    lib.gdn_prefill_scan_ws.argtypes = [vp] * 8 + [i32, i64, i32, i32, i32, i32, vp, sz, vp]
+    lib.gdn_prefill_scan_ws.argtypes = [vp] * 9 + [i32, i64, i32, i32, i32, i32, i32, vp, sz,
+                                                    vp]
     lib.gdn_prefill_scan_ws.restype = ctypes.c_int
     lib.gdn_prefill_backward_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32]
     lib.gdn_prefill_backward_workspace_size.restype = sz
@@ -121,8 +122,10 @@ def prefill_workspace_size(batch, seqlen, heads, dk=256, dv=256, io_dtype=torch.
     return int(n)
 
 
-def prefill_scan_workspace_size(batch, seqlen, heads, dk=256, dv=256, segments=8) -> int:
-    n = load().gdn_prefill_scan_workspace_size(batch, seqlen, heads, dk, dv, int(segments))
+def prefill_scan_workspace_size(batch, seqlen, heads, dk=256, dv=256, io_dtype=torch.bfloat16,
+                                varlen=False, segments=8) -> int:
+    n = load().gdn_prefill_scan_workspace_size(batch, seqlen, heads, dk, dv, _io_code(io_dtype),
+                                               int(bool(varlen)), int(segments))
     if n == ctypes.c_size_t(-1).value:
         raise ValueError("unsupported prefill_scan arguments")
     return int(n)
@@ -208,6 +211,23 @@ def prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=No
     allocates nothing); None takes scratch from the library's pool.
     Returns (out, S_final); S_final is None when ``return_final`` is False.
     """
+    return _prefill_call(q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, return_final,
+                         stream, workspace, None)
+
+
+def prefill_scan(q, k, v, alpha, beta, S0=None, cu_seqlens=None, segments=8, out=None,
+                 S_final=None, return_final: bool = True, stream=None, workspace=None):
+    """``gdn_prefill_scan``: :func:`prefill` with every sequence cut into
+    ``segments`` pieces of whole chunks, run as a scan over the segments
+    (dense or packed, bf16 or fp32).  Returns (out, S_final)."""
+    if int(segments) < 1:
+        raise ValueError("segments must be >= 1")
+    return _prefill_call(q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, return_final,
+                         stream, workspace, int(segments))
+
+
+def _prefill_call(q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, return_final, stream,
+                  workspace, segments):
     lib = load()
     dev = q.device
     io = q.dtype
@@ -245,52 +265,16 @@ def prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=No
     with torch.cuda.device(dev):
         args = (_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
                 _ptr(out), _ptr(S_final), N, seqlen, H, dk, dv, _io_code(io))
+        if segments is not None:
+            args = args + (segments,)
+        name = "gdn_prefill" if segments is None else "gdn_prefill_scan"
         if workspace is None:
-            rc = lib.gdn_prefill(*args, _stream_handle(stream))
+            rc = getattr(lib, name)(*args, _stream_handle(stream))
         else:
-            rc = lib.gdn_prefill_ws(*args, *_ws_args(workspace), _stream_handle(stream))
+            name += "_ws"
+            rc = getattr(lib, name)(*args, *_ws_args(workspace), _stream_handle(stream))
     if rc != 0:
-        raise GDNError("gdn_prefill_ws" if workspace is not None else "gdn_prefill", rc)
-    return out, S_final
-
-
-def prefill_scan(q, k, v, alpha, beta, S0=None, segments=8, out=None, S_final=None,
-                 return_final: bool = True, stream=None, workspace=None):
-    """``gdn_prefill_scan``: the prefill of a dense bf16 batch [B, T, H, .] run
-    as a scan over ``segments`` pieces of each sequence (for few, long
-    sequences).  Returns (out, S_final) like :func:`prefill`."""
-    lib = load()
-    dev = q.device
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _check(t, name, torch.bfloat16, dev)
-    _check(alpha, "alpha", torch.float32, dev)
-    _check(beta, "beta", torch.float32, dev)
-    if q.dim() != 4 or k.shape != q.shape or v.shape[:-1] != q.shape[:-1] \
-            or alpha.shape != q.shape[:-1] or beta.shape != q.shape[:-1]:
-        raise ValueError("dense inputs: q, k [B, T, H, dk]; v [B, T, H, dv]; alpha, beta [B, T, H]")
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    if S0 is not None:
-        _check(S0, "S0", torch.float32, dev)
-        if tuple(S0.shape) != (B, H, dv, dk):
-            raise ValueError(f"S0 must be [{B}, {H}, {dv}, {dk}]")
-    if out is None:
-        out = torch.empty_like(v)
-    else:
-        _check(out, "out", torch.bfloat16, dev)
-    if S_final is None and return_final:
-        S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
-    elif S_final is not None:
-        _check(S_final, "S_final", torch.float32, dev)
-    with torch.cuda.device(dev):
-        args = (_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(out),
-                _ptr(S_final), B, T, H, dk, dv, int(segments))
-        if workspace is None:
-            rc = lib.gdn_prefill_scan(*args, _stream_handle(stream))
-        else:
-            rc = lib.gdn_prefill_scan_ws(*args, *_ws_args(workspace), _stream_handle(stream))
-    if rc != 0:
-        raise GDNError("gdn_prefill_scan", rc)
+        raise GDNError(name, rc)
     return out, S_final
 
 

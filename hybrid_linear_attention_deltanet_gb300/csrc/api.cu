@@ -167,11 +167,19 @@ extern "C" {
 namespace gdn {
 namespace {
 
-// Scratch of one prefill call: the packed batch's chunk offsets, then the
-// path's per-chunk scratch (bf16 I/O: the tensor-core path; fp32: the
-// CUDA-core path).  Zero when the call needs none.
+// Scratch of one prefill call.  Plain form: the packed batch's chunk
+// offsets, then the path's per-chunk scratch (bf16 I/O: the tensor-core
+// path; fp32: the CUDA-core path); zero when the call needs none.  Segmented
+// form (a sequence may be long, or the caller fixed the segment count): the
+// plan's layout.
+bool takes_long_form(int64_t seqlen, int32_t forced_P) {
+  return forced_P > 0 || long_form_applies(seqlen);
+}
+
 size_t prefill_scratch_bytes(int32_t batch, int64_t seqlen, int32_t heads, int32_t dv,
-                             int32_t io_dtype, bool varlen) {
+                             int32_t io_dtype, bool varlen, int32_t forced_P) {
+  if (takes_long_form(seqlen, forced_P))
+    return plan_long(batch, seqlen, varlen, heads, dv, io_dtype, forced_P).bytes;
   const int64_t T_total = varlen ? seqlen : (int64_t)batch * seqlen;
   const int64_t max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
   const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
@@ -179,6 +187,12 @@ size_t prefill_scratch_bytes(int32_t batch, int64_t seqlen, int32_t heads, int32
                                 ? prefill_tc_scratch_bytes(max_chunks, heads, dv)
                                 : prefill_simt_scratch_bytes(max_chunks, heads, dv);
   return off_bytes + work_bytes;
+}
+
+bool prefill_shape_ok(int32_t batch, int64_t seqlen, int32_t heads, int32_t dk, int32_t dv,
+                      int32_t io_dtype) {
+  return batch >= 1 && seqlen >= 0 && heads >= 1 && dk == kDK && supported_dv(dv) &&
+         (io_dtype == GDN_F32 || io_dtype == GDN_BF16);
 }
 
 // A caller's workspace: large enough, 256-byte aligned, overlapping nothing
@@ -193,14 +207,15 @@ int check_workspace(const void* ws, size_t ws_bytes, size_t need, const Range* u
   return GDN_OK;
 }
 
-// gdn_prefill and gdn_prefill_ws: scratch from the caller's workspace when
-// ws is not null, else stream-ordered from the library's pool.
+// gdn_prefill, gdn_prefill_scan and their _ws forms: scratch from the
+// caller's workspace when use_ws, else stream-ordered from the library's
+// pool; forced_P > 0 fixes the segment count of every sequence.
 int prefill_common(const void* q, const void* k, const void* v, const float* alpha,
                    const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
                    float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
-                   int32_t dv, int32_t io_dtype, cudaStream_t stream, bool use_ws, void* ws,
-                   size_t ws_bytes) {
-  if (batch < 1 || seqlen < 0 || heads < 1) return GDN_ERR_INVALID_ARG;
+                   int32_t dv, int32_t io_dtype, int32_t forced_P, cudaStream_t stream,
+                   bool use_ws, void* ws, size_t ws_bytes) {
+  if (batch < 1 || seqlen < 0 || heads < 1 || forced_P < 0) return GDN_ERR_INVALID_ARG;
   const bool varlen = cu_seqlens != nullptr;
   const int64_t T_total = varlen ? seqlen : (int64_t)batch * seqlen;
   // token tensors may be empty (and then null) only when there are no tokens
@@ -210,8 +225,16 @@ int prefill_common(const void* q, const void* k, const void* v, const float* alp
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(alpha) || !aligned4(beta) ||
       !aligned16(out) || !aligned16(S0) || !aligned16(S_final) || !aligned4(cu_seqlens))
     return GDN_ERR_ALIGNMENT;
-  // 32-bit offsets (packed batches) and token coordinates (tensor-core path)
-  if ((varlen || io_dtype == GDN_BF16) && T_total > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+  const bool long_form = takes_long_form(seqlen, forced_P);
+  // 32-bit offsets (packed batches, the segmented form) and token coordinates
+  // (tensor-core path)
+  if ((varlen || long_form || io_dtype == GDN_BF16) && T_total > 0x7fffffffLL)
+    return GDN_ERR_UNSUPPORTED;
+  LongPlan plan;
+  if (long_form) {
+    plan = plan_long(batch, seqlen, varlen, heads, dv, io_dtype, forced_P);
+    if (plan.n_slots * 2 > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+  }
   const size_t es = io_dtype == GDN_BF16 ? 2 : 4;
   const size_t n_tok_h = (size_t)T_total * heads;
   const size_t state_bytes = (size_t)batch * heads * dv * dk * sizeof(float);
@@ -228,7 +251,9 @@ int prefill_common(const void* q, const void* k, const void* v, const float* alp
   for (int i = 0; i < n_in; ++i)
     if (overlaps(used[i], r_out) || overlaps(used[i], r_sf)) return GDN_ERR_INVALID_ARG;
   if (overlaps(r_out, r_sf)) return GDN_ERR_INVALID_ARG;
-  const size_t need = prefill_scratch_bytes(batch, seqlen, heads, dv, io_dtype, varlen);
+  const size_t need = long_form ? plan.bytes
+                                : prefill_scratch_bytes(batch, seqlen, heads, dv, io_dtype,
+                                                        varlen, 0);
   if (use_ws) {
     const int rc = check_workspace(ws, ws_bytes, need, used, 9);
     if (rc != GDN_OK) return rc;
@@ -246,7 +271,6 @@ int prefill_common(const void* q, const void* k, const void* v, const float* alp
   a.map.chunks_per_seq = varlen ? 0 : (seqlen + kC - 1) / kC;
   a.max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
 
-  const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
   // bf16 I/O runs on the tensor cores, fp32 I/O on the CUDA cores
   const bool tc = io_dtype == GDN_BF16;
   a.dv = dv;
@@ -256,13 +280,20 @@ int prefill_common(const void* q, const void* k, const void* v, const float* alp
       (!scratch_pool() ||
        cudaMallocFromPoolAsync(&scratch, need, scratch_pool(), stream) != cudaSuccess))
     return GDN_ERR_CUDA;
-  a.scratch = (char*)scratch + off_bytes;
   cudaError_t e = cudaSuccess;
-  if (varlen) {
-    a.map.chunk_off = (int32_t*)scratch;
-    e = launch_chunk_offsets(cu_seqlens, batch, T_total, (int32_t*)scratch, status, stream);
+  if (long_form) {
+    a.scratch = scratch;
+    e = launch_prefill_long(a, io_dtype, plan, forced_P, stream);
+  } else {
+    const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
+    a.scratch = (char*)scratch + off_bytes;
+    if (varlen) {
+      a.map.chunk_off = (int32_t*)scratch;
+      e = launch_chunk_offsets(cu_seqlens, batch, T_total, (int32_t*)scratch, status, stream);
+    }
+    if (e == cudaSuccess)
+      e = tc ? launch_prefill_tc(a, stream) : launch_prefill_simt(a, io_dtype, stream);
   }
-  if (e == cudaSuccess) e = tc ? launch_prefill_tc(a, stream) : launch_prefill_simt(a, io_dtype, stream);
   const cudaError_t ef = (!use_ws && scratch) ? cudaFreeAsync(scratch, stream) : cudaSuccess;
   return (e == cudaSuccess && ef == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -277,15 +308,13 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
                 float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
                 int32_t dv, int32_t io_dtype, gdn_stream_t stream) {
   return prefill_common(q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, batch, seqlen, heads,
-                        dk, dv, io_dtype, (cudaStream_t)stream, false, nullptr, 0);
+                        dk, dv, io_dtype, 0, (cudaStream_t)stream, false, nullptr, 0);
 }
 
 size_t gdn_prefill_workspace_size(int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
                                   int32_t dv, int32_t io_dtype, int32_t varlen) {
-  if (batch < 1 || seqlen < 0 || heads < 1 || dk != kDK || !supported_dv(dv) ||
-      (io_dtype != GDN_F32 && io_dtype != GDN_BF16))
-    return SIZE_MAX;
-  return prefill_scratch_bytes(batch, seqlen, heads, dv, io_dtype, varlen != 0);
+  if (!prefill_shape_ok(batch, seqlen, heads, dk, dv, io_dtype)) return SIZE_MAX;
+  return prefill_scratch_bytes(batch, seqlen, heads, dv, io_dtype, varlen != 0, 0);
 }
 
 int gdn_prefill_ws(const void* q, const void* k, const void* v, const float* alpha,
@@ -294,7 +323,35 @@ int gdn_prefill_ws(const void* q, const void* k, const void* v, const float* alp
                    int32_t dv, int32_t io_dtype, void* workspace, size_t workspace_bytes,
                    gdn_stream_t stream) {
   return prefill_common(q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, batch, seqlen, heads,
-                        dk, dv, io_dtype, (cudaStream_t)stream, true, workspace, workspace_bytes);
+                        dk, dv, io_dtype, 0, (cudaStream_t)stream, true, workspace,
+                        workspace_bytes);
+}
+
+int gdn_prefill_scan(const void* q, const void* k, const void* v, const float* alpha,
+                     const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
+                     float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                     int32_t dv, int32_t io_dtype, int32_t segments, gdn_stream_t stream) {
+  if (segments < 1) return GDN_ERR_INVALID_ARG;
+  return prefill_common(q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, batch, seqlen, heads,
+                        dk, dv, io_dtype, segments, (cudaStream_t)stream, false, nullptr, 0);
+}
+
+size_t gdn_prefill_scan_workspace_size(int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                                       int32_t dv, int32_t io_dtype, int32_t varlen,
+                                       int32_t segments) {
+  if (!prefill_shape_ok(batch, seqlen, heads, dk, dv, io_dtype) || segments < 1) return SIZE_MAX;
+  return prefill_scratch_bytes(batch, seqlen, heads, dv, io_dtype, varlen != 0, segments);
+}
+
+int gdn_prefill_scan_ws(const void* q, const void* k, const void* v, const float* alpha,
+                        const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
+                        float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                        int32_t dv, int32_t io_dtype, int32_t segments, void* workspace,
+                        size_t workspace_bytes, gdn_stream_t stream) {
+  if (segments < 1) return GDN_ERR_INVALID_ARG;
+  return prefill_common(q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, batch, seqlen, heads,
+                        dk, dv, io_dtype, segments, (cudaStream_t)stream, true, workspace,
+                        workspace_bytes);
 }
 
 }  // extern "C"

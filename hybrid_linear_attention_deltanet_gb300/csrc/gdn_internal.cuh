@@ -98,6 +98,78 @@ unsigned* status_ptr();
 
 // ---------------------------------------------------------------------------
 // launchers (one translation unit each)
+// Long sequences run as a scan over segments of whole chunks (prefill_long.cu):
+// a sequence of at least kLongChunks chunks is cut into ceil(chunks /
+// kSegChunks) pieces of equal length; shorter ones are one segment.
+constexpr int64_t kLongChunks = 1024;
+constexpr int64_t kSegChunks = 160;
+
+// Role bits of a segment (one byte per segment slot).
+constexpr uint8_t kSegFirst = 1, kSegLast = 2;
+
+// Per-unit routing of the state pass over a segmented packing (the map's
+// sequences are then segment slots).  pass 0: a plain call, every unit runs
+// from S0 into S_final with outputs.  pass 1: the grid holds two units per
+// slot and row block: x < N, a first segment from the caller's start (outputs,
+// end into the caller's S_final when it is also the last segment, else into
+// Bseg) or a middle segment from zero (no outputs, end into Bseg); x >= N, a
+// middle segment from [I; 0] (no outputs, end into Fseg).  pass 2: every
+// segment but the first from its true start S0seg (outputs; end into the
+// caller's S_final for a last segment).  Last segments skip pass 1, first
+// segments pass 2.
+struct SegRoute {
+  int32_t pass = 0;
+  const int32_t* seg_seq = nullptr;   // per slot: its sequence, -1 for an unused slot
+  const uint8_t* role = nullptr;      // per slot: kSegFirst | kSegLast
+  const float* S0 = nullptr;          // the caller's [N][H][dv][dk] starts, or nullptr (zero)
+  float* S_final = nullptr;           // the caller's final states, or nullptr
+  const float* S0seg = nullptr;       // [slots][H][dv][dk]
+  float* Bseg = nullptr;
+  float* Fseg = nullptr;
+};
+
+// Where one unit of the state pass starts and ends; S0 / S_final point at
+// its sequence's (or slot's) [H][dv][dk] block.
+struct UnitRoute {
+  bool run, ident, write_out;
+  const float* S0;
+  float* S_final;
+};
+
+__device__ __forceinline__ UnitRoute route_unit(const SegRoute& r, const float* S0,
+                                                float* S_final, int x, int N, int64_t per_seq) {
+  UnitRoute u{true, false, true, nullptr, nullptr};
+  if (r.pass == 0) {
+    u.S0 = S0 ? S0 + x * per_seq : nullptr;
+    u.S_final = S_final ? S_final + x * per_seq : nullptr;
+    return u;
+  }
+  const bool second = x >= N;
+  const int s = second ? x - N : x;
+  const int n = r.seg_seq[s];
+  const uint8_t ro = r.role[s];
+  const bool first = ro & kSegFirst, last = ro & kSegLast;
+  u.run = n >= 0;
+  if (r.pass == 1 && second) {          // A + B of a middle segment
+    u.run = u.run && !first && !last;
+    u.ident = true;
+    u.write_out = false;
+    u.S_final = r.Fseg + s * per_seq;
+  } else if (r.pass == 1 && first) {    // the sequence's own start
+    u.S0 = r.S0 ? r.S0 + n * per_seq : nullptr;
+    u.S_final = !last ? r.Bseg + s * per_seq : r.S_final ? r.S_final + n * per_seq : nullptr;
+  } else if (r.pass == 1) {             // B of a middle segment
+    u.run = u.run && !last;
+    u.write_out = false;
+    u.S_final = r.Bseg + s * per_seq;
+  } else {                              // the true start of a later segment
+    u.run = u.run && !first;
+    u.S0 = r.S0seg + s * per_seq;
+    u.S_final = last && r.S_final ? r.S_final + n * per_seq : nullptr;
+  }
+  return u;
+}
+
 struct PrefillLaunch {
   const void* q; const void* k; const void* v;
   const float* alpha; const float* beta; const float* S0;
@@ -111,8 +183,9 @@ struct PrefillLaunch {
   bool allow_overlap;   // tensor-core path may run prep and state pass in one cooperative launch
   float* state_dump;    // tensor-core path: every chunk's start state, [chunks * H][dv][dk]
                         // fp32 (the backward's forward re-run), or nullptr
-  bool state_only;      // tensor-core path: the per-chunk images are already in scratch
-                        // (an earlier call on the same inputs and map); run the state pass only
+  bool state_only;      // the per-chunk factors are already in scratch (an earlier call on
+                        // the same inputs and map): run the state pass only
+  SegRoute route;       // see SegRoute (pass != 0 forces the split form)
 };
 
 cudaError_t launch_chunk_offsets(const int32_t* cu_seqlens, int32_t N, int64_t T_total,
@@ -131,6 +204,26 @@ extern uint64_t* g_trace;
 extern int32_t g_trace_chunks;
 // launch form of the last tensor-core prefill on this process: 1 fused, 0 split
 extern int32_t g_last_tc_form;
+
+// Long sequences as a scan over segments (prefill_long.cu).  The segmented
+// form takes over a call when some sequence may have kLongChunks chunks
+// (seqlen: T of a dense batch, T_total of a packed one) or when the caller
+// fixes the segment count (forced_P > 0).  Its scratch: chunk offsets,
+// token starts, sequences and roles of the segment slots, the path's
+// per-chunk scratch over the caller's chunks, then three per-(slot, head)
+// states (true starts, ends from zero, ends from [I; 0]).
+struct LongPlan {
+  int64_t n_slots = 0, max_chunks = 0;
+  size_t off_chunk_off = 0, off_seg_cu = 0, off_seg_seq = 0, off_seq_first = 0, off_role = 0,
+         off_work = 0, off_S0seg = 0, off_Bseg = 0, off_Fseg = 0, bytes = 0;
+};
+bool long_form_applies(int64_t seqlen);
+LongPlan plan_long(int32_t N, int64_t seqlen, bool varlen, int32_t H, int32_t dv, int io_dtype,
+                   int32_t forced_P);
+// base: the caller's problem (map over its own sequences, S0 / S_final / out
+// as given), scratch = the start of plan.bytes of device memory
+cudaError_t launch_prefill_long(const PrefillLaunch& base, int io_dtype, const LongPlan& plan,
+                                int32_t forced_P, cudaStream_t stream);
 
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, const float* alpha,
                                const float* beta, float* S, void* out, int32_t N, int32_t H,

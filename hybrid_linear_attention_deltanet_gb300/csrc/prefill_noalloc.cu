@@ -97,7 +97,11 @@ extern "C" int gdn_prefill_noalloc(const void* q, const void* k, const void* v,
   const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
   const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads, dv)
                                : prefill_simt_scratch_bytes(a.max_chunks, heads, dv);
-  if (off_bytes + work_bytes > kNoAllocScratchBytes) return GDN_ERR_SCRATCH_LIMIT;
+  // a problem that may hold a sequence of kLongChunks chunks takes
+  // gdn_prefill's segmented form, whose per-chunk factors alone (over 100 MB)
+  // never fit here: rejected, so that both entry points always agree
+  if (long_form_applies(seqlen) || off_bytes + work_bytes > kNoAllocScratchBytes)
+    return GDN_ERR_SCRATCH_LIMIT;
 
   a.status = status_ptr();
   void* scratch = noalloc_scratch();

@@ -188,7 +188,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 state_pass_kernel(const T* __restrict__ q, const T* __restrict__ k,
                   const float* __restrict__ S0, T* __restrict__ out,
-                  float* __restrict__ S_final, SeqMap map, int32_t H, SimtScratch scr) {
+                  float* __restrict__ S_final, SeqMap map, int32_t H, SimtScratch scr,
+                  SegRoute route) {
   extern __shared__ float smem[];
   float* Ss = smem;                  // [kNS][kPad]  this CTA's rows of S
   float* Wt = Ss + kNS * kPad;       // [C][33]
@@ -197,14 +198,21 @@ state_pass_kernel(const T* __restrict__ q, const T* __restrict__ k,
   float* gam = Us + kC * 33;         // [C]  gamma_r * scale
   float* dec = gam + kC;             // [C]  gamma_L / gamma_r (0 on pad rows)
 
-  const int n = blockIdx.x, h = blockIdx.y, slice = blockIdx.z;
+  const int x = blockIdx.x, h = blockIdx.y, slice = blockIdx.z;
+  const int n = x >= map.N ? x - map.N : x;
   const int tid = threadIdx.x, i = tid & 31, rg = tid >> 5;
   const int dv = scr.dv;
-  const int64_t state_base = ((int64_t)n * H + h) * dv * kDK + (int64_t)slice * kNS * kDK;
+  const UnitRoute ur = route_unit(route, S0, S_final, x, map.N, (int64_t)H * dv * kDK);
+  // a chain from [I; 0] needs only the first dk rows
+  if (!ur.run || (ur.ident && slice * kNS >= kDK)) return;
+  // this CTA's rows of the unit's [H][dv][dk] start and end blocks
+  const int64_t state_base = (int64_t)h * dv * kDK + (int64_t)slice * kNS * kDK;
 
   for (int e = tid; e < kNS * kDK; e += kThreads) {
     const int r = e / kDK, c = e % kDK;
-    Ss[r * kPad + c] = S0 ? S0[state_base + e] : 0.f;
+    Ss[r * kPad + c] = ur.S0      ? ur.S0[state_base + e]
+                       : ur.ident ? (slice * kNS + r == c ? 1.f : 0.f)
+                                  : 0.f;
   }
   __syncthreads();
 
@@ -258,6 +266,7 @@ state_pass_kernel(const T* __restrict__ q, const T* __restrict__ k,
     const float* Pg = scr.P + u * SimtScratch::stride_P();
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
+      if (!ur.write_out) break;
       const int r = rg * 8 + m;
       if (r < L) {
         float o = gam[r] * accQ[m];
@@ -282,9 +291,9 @@ state_pass_kernel(const T* __restrict__ q, const T* __restrict__ k,
     }
   }
   __syncthreads();
-  if (S_final)
+  if (ur.S_final)
     for (int e = tid; e < kNS * kDK; e += kThreads)
-      S_final[state_base + e] = Ss[(e / kDK) * kPad + (e % kDK)];
+      ur.S_final[state_base + e] = Ss[(e / kDK) * kPad + (e % kDK)];
 }
 
 constexpr size_t kPrepSmem = sizeof(float) * (2 * kC * kPad + 2 * kC * kCP + 3 * kC);
@@ -300,16 +309,17 @@ cudaError_t launch_typed(const PrefillLaunch& a, cudaStream_t stream) {
   e = cudaFuncSetAttribute(state_pass_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kStateSmem);
   if (e != cudaSuccess) return e;
-  if (a.max_chunks > 0) {
+  if (a.max_chunks > 0 && !a.state_only) {
     dim3 g1((unsigned)a.max_chunks, (unsigned)a.H);
     chunk_prep_kernel<T><<<g1, kThreads, kPrepSmem, stream>>>(
         (const T*)a.q, (const T*)a.k, (const T*)a.v, a.alpha, a.beta, a.map, a.H, scr);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  dim3 g2((unsigned)a.map.N, (unsigned)a.H, (unsigned)(a.dv / kNS));
+  dim3 g2((unsigned)a.map.N * (a.route.pass == 1 ? 2u : 1u), (unsigned)a.H,
+          (unsigned)(a.dv / kNS));
   state_pass_kernel<T><<<g2, kThreads, kStateSmem, stream>>>(
-      (const T*)a.q, (const T*)a.k, a.S0, (T*)a.out, a.S_final, a.map, a.H, scr);
+      (const T*)a.q, (const T*)a.k, a.S0, (T*)a.out, a.S_final, a.map, a.H, scr, a.route);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -728,7 +728,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
                                            const uint32_t* ready, unsigned* status,
                                            uint64_t* __restrict__ trace, int32_t trace_chunks,
                                            int32_t dv, int n, int h, int slice,
-                                           float* __restrict__ sdump) {
+                                           float* __restrict__ sdump, bool ident_start = false) {
   const int unit = (n * H + h) * (dv / 128) + slice;
   const bool timed = trace && threadIdx.x == 0 && unit < kMaxTracedUnits;
   if (timed) trace[kUnitTimes + 3 * unit] = globaltimer_ns();
@@ -774,7 +774,8 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
 
   // master state: this thread's 128 columns of row iloc (fp32, registers)
   float S[128];
-  const size_t srow = (((size_t)n * H + h) * dv + 128 * slice + iloc) * kDK + 128 * colhalf;
+  // S0 / S_final point at this unit's [H][dv][dk] block
+  const size_t srow = (((size_t)h) * dv + 128 * slice + iloc) * kDK + 128 * colhalf;
   if (S0) {
     const float4* p = reinterpret_cast<const float4*>(S0 + srow);
 #pragma unroll
@@ -783,8 +784,11 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
       S[4 * j] = t.x; S[4 * j + 1] = t.y; S[4 * j + 2] = t.z; S[4 * j + 3] = t.w;
     }
   } else {
+    // zero, or [I; 0] (identity in the first dk rows: the transition of the
+    // chunks from an identity start)
+    const uint32_t row = 128 * slice + iloc, col0 = 128 * colhalf;
 #pragma unroll
-    for (int j = 0; j < 128; ++j) S[j] = 0.f;
+    for (int j = 0; j < 128; ++j) S[j] = ident_start && row == col0 + j ? 1.f : 0.f;
   }
   tc_fence_before();
   __syncthreads();
@@ -927,6 +931,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   // MMA-1 then; warps 1-3 hold the loader threads, whose acquire fences
   // would otherwise wait for these stores to drain.)
   auto copy_out_prev = [&](int prev_buf) {
+    if (!out) return;   // a unit whose outputs nobody reads
     const uint8_t* stage = sm + kS_KP + prev_buf * 40960;
     for (int p = tid - 128; p < 16 * prev_L; p += kStateThreads - 128) {
       if (p < 0) break;
@@ -1179,10 +1184,16 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
                 __nv_bfloat16* __restrict__ out, float* __restrict__ S_final, SeqMap map,
                 int32_t H, const uint8_t* __restrict__ scratch, unsigned* status,
                 uint64_t* __restrict__ trace, int32_t trace_chunks, int32_t dv,
-                float* __restrict__ sdump) {
+                float* __restrict__ sdump, SegRoute route) {
   extern __shared__ uint8_t smem_raw[];
-  state_role<false>(align_smem_1024(smem_raw), &tm_k, S0, out, S_final, map, H, scratch, nullptr,
-                    status, trace, trace_chunks, dv, blockIdx.x, blockIdx.y, blockIdx.z, sdump);
+  const int x = blockIdx.x;
+  const UnitRoute u = route_unit(route, S0, S_final, x, map.N, (int64_t)H * dv * kDK);
+  // the whole CTA, before any barrier or TMEM allocation; a chain from
+  // [I; 0] needs only the first dk rows
+  if (!u.run || (u.ident && 128 * (int)blockIdx.z >= kDK)) return;
+  state_role<false>(align_smem_1024(smem_raw), &tm_k, u.S0, u.write_out ? out : nullptr,
+                    u.S_final, map, H, scratch, nullptr, status, trace, trace_chunks, dv,
+                    x >= map.N ? x - map.N : x, blockIdx.y, blockIdx.z, sdump, u.ident);
 }
 
 // fused form: cooperative, one CTA per SM; CTAs [0, n_state) are the state
@@ -1203,9 +1214,11 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint8_t* sm = align_smem_1024(smem_raw);
   if ((int32_t)blockIdx.x < n_state) {
     const int u = blockIdx.x;
-    const int ns = dv / 128;
-    state_role<true>(sm, &tm_kb, S0, out, S_final, map, H, scratch, ready, status, trace,
-                     trace_chunks, dv, u / (ns * H), (u / ns) % H, u % ns, sdump);
+    const int ns = dv / 128, n = u / (ns * H);
+    const int64_t per_seq = (int64_t)H * dv * kDK;
+    state_role<true>(sm, &tm_kb, S0 ? S0 + n * per_seq : nullptr, out,
+                     S_final ? S_final + n * per_seq : nullptr, map, H, scratch, ready, status,
+                     trace, trace_chunks, dv, n, (u / ns) % H, u % ns, sdump);
   } else {
     int64_t positions = map.chunks_per_seq;
     if (map.cu_seqlens) {
@@ -1345,7 +1358,7 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
   uint32_t* ready = (uint32_t*)(scr + (size_t)items * img_stride(dv));
   const int64_t n_state = (int64_t)a.map.N * a.H * (dv / 128);
 
-  if (!prep_only && !a.state_only && a.allow_overlap && f->fused_ok && items > 0 &&
+  if (!prep_only && !a.state_only && a.allow_overlap && a.route.pass == 0 && f->fused_ok && items > 0 &&
       n_state + kMinPrepWorkers <= f->sms) {
     if ((e = cudaMemsetAsync(ready, 0, (size_t)items * sizeof(uint32_t), stream)) != cudaSuccess)
       return e;
@@ -1383,10 +1396,10 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
   }
   if (prep_only) return cudaSuccess;
   g_last_tc_form = 0;
-  tc_state_kernel<<<dim3((unsigned)a.map.N, (unsigned)a.H, (unsigned)(dv / 128)), kStateThreads,
-                    kStateSmem, stream>>>(tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map,
-                                          a.H, scr, a.status, g_trace, g_trace_chunks, dv,
-                                          a.state_dump);
+  const unsigned gx = (unsigned)a.map.N * (a.route.pass == 1 ? 2u : 1u);
+  tc_state_kernel<<<dim3(gx, (unsigned)a.H, (unsigned)(dv / 128)), kStateThreads, kStateSmem,
+                    stream>>>(tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr,
+                              a.status, g_trace, g_trace_chunks, dv, a.state_dump, a.route);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -93,6 +93,24 @@ enum gdn_status {
  * byte ranges intersect).  Results do not depend on how sequences are packed:
  * a sequence gives bit-identical out and S_final alone or inside any batch.
  *
+ * Long sequences (segmented form).  The chunks of one sequence form a chain
+ * that runs one chunk after another, so a single long sequence would leave
+ * most of the GPU idle.  A sequence of at least 1024 chunks (65,473 tokens
+ * or more) is therefore cut into ceil(chunks / 160) segments of equal whole-
+ * chunk length: because the state pass is affine in its start state
+ * (S_end = S_start A + B over a segment), the segments run as parallel
+ * chains -- the first from S0, the middle ones from zero and from [I; 0],
+ * giving B and A -- a short scan composes each segment's true start, and a
+ * second pass over the later segments writes their outputs (two segments of
+ * latency instead of the whole sequence, at up to 2.4 times the state-pass
+ * work).  The cut depends only on the sequence's own length, so packing
+ * still never changes a result; a cut sequence matches the oracle within the
+ * same tolerance, though not bit for bit the uncut chain.  Calls whose seqlen
+ * (T, or T_total of a packed batch) reaches 1024 chunks take this form for
+ * the whole batch; sequences shorter than the threshold then run exactly the
+ * plain kernels, with the same bits, and the call is limited to 2^31 - 1
+ * tokens for either I/O type.
+ *
  * Scratch: intermediate per-chunk factors are kept in device memory obtained
  * stream-ordered on `stream` (cudaMallocFromPoolAsync / cudaFreeAsync) from a
  * per-device pool owned by the library.  The pool keeps freed scratch mapped
@@ -119,6 +137,12 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
  *             (141312 at dv = 512), then one 4-byte flag per (chunk, head)
  *             rounded up to 256;
  *   fp32 I/O  the CUDA-core path's four per-(chunk, head) arrays.
+ * When seqlen reaches 1024 chunks (the segmented form) the layout is instead,
+ * each part rounded up to 256 bytes: the segment slots' chunk offsets, token
+ * starts and sequence indices (4 (slots + 1) bytes each), the sequences'
+ * first slots (4 (batch + 1)), one role byte per slot, the per-chunk scratch
+ * above, then three fp32 states of heads * dv * 256 per slot, where slots =
+ * batch + max_chunks / 160 + 1.
  * 0 when the call needs no scratch; SIZE_MAX for arguments gdn_prefill would
  * reject as invalid or unsupported.
  */
@@ -152,53 +176,42 @@ int gdn_prefill_ws(const void* q, const void* k, const void* v, const float* alp
 int gdn_release_scratch(void);
 
 /*
- * gdn_prefill_scan -- gdn_prefill for a dense bf16 batch of long sequences,
- * run as a scan over segments.
+ * gdn_prefill_scan -- gdn_prefill with every sequence cut into a given
+ * number of segments (gdn_prefill's segmented form, with the count fixed by
+ * the caller instead of by the length rule).
  *
- * Over any run of chunks the state pass is affine in its start state,
- * S_end = S_start A + B (A the product of the per-token transitions
- * alpha_t (I - beta_t k_t k_t^T), B the end state from a zero start).  Each
- * sequence is cut into `segments` pieces of whole chunks that run as
- * independent chains: a pass from the caller's S0 / zero starts gives B, a pass
- * from identity starts on the same per-chunk factors gives A, a scan composes
- * the true start of every segment, and a last pass from those starts writes
- * out and S_final.  Three passes over chains `segments` times shorter replace
- * one long chain -- faster when the batch has few (sequence, head) units and
- * long sequences (one 64K-token sequence of 6 heads ran fastest with 8).
+ * Arguments and results as gdn_prefill (dense or packed, bf16 or fp32), plus
+ * segments >= 1: each sequence of c chunks is cut into ceil(c / L) pieces of
+ * L = ceil(c / segments) whole chunks (a sequence of one chunk or none stays
+ * whole).  segments = 1 leaves every sequence whole, also those gdn_prefill
+ * would cut.  Results agree with gdn_prefill's to within the tolerance of the
+ * I/O type, and bit for bit for every sequence left whole (and for every
+ * sequence that gdn_prefill cuts the same way).
  *
- * Arguments as gdn_prefill with cu_seqlens = NULL and io_dtype = GDN_BF16.
- * Results equal gdn_prefill's to within the bf16 tolerance, not bit for bit
- * (the chains are composed in a different order).  segments = 1, or a
- * sequence too short to cut, runs gdn_prefill itself.  Scratch from the
- * library's pool: gdn_prefill's plus five per-(segment, head) states.
- *
- * Errors, before any launch: GDN_ERR_INVALID_ARG for segments < 1, a
- * non-positive batch or heads, a null token tensor or out, or out / S_final
- * overlapping an input or each other; GDN_ERR_UNSUPPORTED for dk != 256, dv
- * not 256 or 512, batch > 65535, or more than 2^31 - 1 tokens or
- * (segment, head) pairs; GDN_ERR_ALIGNMENT as gdn_prefill.  GDN_ERR_CUDA when
- * the scratch cannot be had or a launch fails.
+ * Errors: GDN_ERR_INVALID_ARG for segments < 1; more than 2^30 segments in
+ * all is GDN_ERR_UNSUPPORTED; otherwise as gdn_prefill.
  */
 int gdn_prefill_scan(const void* q, const void* k, const void* v, const float* alpha,
-                     const float* beta, const float* S0, void* out, float* S_final, int32_t batch,
-                     int64_t seqlen, int32_t heads, int32_t dk, int32_t dv, int32_t segments,
-                     gdn_stream_t stream);
+                     const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
+                     float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                     int32_t dv, int32_t io_dtype, int32_t segments, gdn_stream_t stream);
 
 /*
  * gdn_prefill_scan_workspace_size / gdn_prefill_scan_ws -- the same with the
- * scratch in a caller-owned device workspace (1024-byte aligned) of at least
- * gdn_prefill_scan_workspace_size(batch, seqlen, heads, dk, dv, segments)
- * bytes (SIZE_MAX for invalid arguments).  When the sequences are too short to
- * cut, the size and the call are gdn_prefill_ws's.  Workspace rules and errors
- * as gdn_prefill_ws.
+ * scratch in a caller-owned device workspace (256-byte aligned) of at least
+ * gdn_prefill_scan_workspace_size(batch, seqlen, heads, dk, dv, io_dtype,
+ * varlen, segments) bytes (SIZE_MAX for invalid arguments; the layout of
+ * gdn_prefill's segmented form with slots = min(batch * segments, batch +
+ * max_chunks)).  Workspace rules and errors as gdn_prefill_ws.
  */
 size_t gdn_prefill_scan_workspace_size(int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
-                                       int32_t dv, int32_t segments);
+                                       int32_t dv, int32_t io_dtype, int32_t varlen,
+                                       int32_t segments);
 int gdn_prefill_scan_ws(const void* q, const void* k, const void* v, const float* alpha,
-                        const float* beta, const float* S0, void* out, float* S_final,
-                        int32_t batch, int64_t seqlen, int32_t heads, int32_t dk, int32_t dv,
-                        int32_t segments, void* workspace, size_t workspace_bytes,
-                        gdn_stream_t stream);
+                        const float* beta, const float* S0, const int32_t* cu_seqlens, void* out,
+                        float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                        int32_t dv, int32_t io_dtype, int32_t segments, void* workspace,
+                        size_t workspace_bytes, gdn_stream_t stream);
 
 /*
  * gdn_prefill_backward -- gradients of the prefill, for training with the

@@ -211,11 +211,13 @@ def test_fault_hook_rejects_bad_arguments(lib):
 
 @fake_addresses
 def test_prefill_scan_rejects_bad_host_arguments(lib):
-    f = lambda q=A16, out=A16b, batch=1, T=4096, dv=256, seg=4: lib.gdn_prefill_scan(
-        q, A16, A16, A16, A16, None, out, None, batch, T, 6, 256, dv, seg, None)
+    f = lambda q=A16, out=A16b, batch=1, T=4096, dv=256, io=1, seg=4: lib.gdn_prefill_scan(
+        q, A16, A16, A16, A16, None, None, out, None, batch, T, 6, 256, dv, io, seg, None)
     assert f(seg=0) == 1
+    assert f(seg=-3) == 1
     assert f(batch=0) == 1
     assert f(dv=384) == 2
+    assert f(io=7) == 2
     assert f(q=MIS) == 3
     assert f(out=A16) == 1                                              # out over q
 
@@ -227,7 +229,7 @@ def _ws_size_fns(lib):
     sz, i32, i64 = ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64
     lib.gdn_prefill_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32]
     lib.gdn_prefill_workspace_size.restype = sz
-    lib.gdn_prefill_scan_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32]
+    lib.gdn_prefill_scan_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32, i32]
     lib.gdn_prefill_scan_workspace_size.restype = sz
     lib.gdn_prefill_backward_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32]
     lib.gdn_prefill_backward_workspace_size.restype = sz
@@ -239,19 +241,54 @@ def _up(x, a):
     return (x + a - 1) // a * a
 
 
-def test_workspace_size_follows_the_documented_layout(lib):
-    """gdn.h's layout of the bf16 prefill scratch, restated: chunk offsets of a
-    packed batch (4 (N + 1) bytes rounded to 256), then one operand image per
-    (chunk, head) of 107520 bytes at dv = 256 (141312 at dv = 512) over the
+def _plain_bf16_bytes(B, T, H, dv, varlen):
+    """gdn.h's layout of the plain bf16 prefill scratch, restated: chunk offsets
+    of a packed batch (4 (N + 1) bytes rounded to 256), then one operand image
+    per (chunk, head) of 107520 bytes at dv = 256 (141312 at dv = 512) over the
     chunk bound, then a 4-byte flag per (chunk, head) rounded to 256."""
-    ws, _, _ = _ws_size_fns(lib)
-    for (B, T, H, dv, varlen) in [(4, 8192, 6, 256, 0), (1, 65536, 6, 256, 0), (3, 1000, 6, 256, 1),
-                                  (16, 388611, 6, 256, 1), (1, 100, 2, 512, 0), (2, 0, 6, 256, 1)]:
-        chunks = B * -(-T // 64) if not varlen else (T + 63 * B) // 64
-        items = chunks * H
-        img = 107520 if dv == 256 else 141312
-        want = items * img + _up(items * 4, 256) + (_up(4 * (B + 1), 256) if varlen else 0)
+    items = _chunks(B, T, varlen) * H
+    img = 107520 if dv == 256 else 141312
+    return items * img + _up(items * 4, 256) + (_up(4 * (B + 1), 256) if varlen else 0)
+
+
+def _chunks(B, T, varlen):
+    return B * -(-T // 64) if not varlen else (T + 63 * B) // 64
+
+
+def _segmented_bytes(B, T, H, dv, varlen, work, slots):
+    """gdn.h's layout of the segmented form: chunk offsets, token starts and
+    sequences of the slots, the sequences' first slots, a role byte per slot,
+    the per-chunk scratch, three fp32 states per (slot, head)."""
+    ints = _up(4 * (slots + 1), 256)
+    state = _up(slots * H * dv * 256 * 4, 256)
+    return 3 * ints + _up(4 * (B + 1), 256) + _up(slots, 256) + _up(work, 256) + 3 * state
+
+
+def test_workspace_size_follows_the_documented_layout(lib):
+    ws, ws_scan, _ = _ws_size_fns(lib)
+    for (B, T, H, dv, varlen) in [(4, 8192, 6, 256, 0), (3, 1000, 6, 256, 1), (1, 100, 2, 512, 0),
+                                  (2, 0, 6, 256, 1), (1, 65472, 6, 256, 0), (2, 65472, 6, 256, 1)]:
+        assert ws(B, T, H, 256, dv, 1, varlen) == _plain_bf16_bytes(B, T, H, dv, varlen), \
+            (B, T, H, dv, varlen)
+    # from 1024 chunks on (65,473 tokens: T of a dense batch, T_total of a
+    # packed one) the call takes the segmented form
+    for (B, T, H, dv, varlen) in [(1, 65473, 6, 256, 0), (1, 65536, 6, 256, 0),
+                                  (16, 388611, 6, 256, 1), (2, 100000, 3, 512, 1)]:
+        mc = _chunks(B, T, varlen)
+        work = _plain_bf16_bytes(mc, 64, H, dv, 0)       # the images over the same chunks
+        want = _segmented_bytes(B, T, H, dv, varlen, work, B + mc // 160 + 1)
         assert ws(B, T, H, 256, dv, 1, varlen) == want, (B, T, H, dv, varlen)
+        # fp32: the CUDA-core path's arrays take the images' place
+        work32 = ws(mc, 64, H, 256, dv, 0, 0)
+        assert ws(B, T, H, 256, dv, 0, varlen) == \
+            _segmented_bytes(B, T, H, dv, varlen, work32, B + mc // 160 + 1)
+    # gdn_prefill_scan: the segmented layout with min(B * segments, B + chunks) slots
+    for (B, T, H, dv, io, varlen, seg) in [(1, 64, 6, 256, 1, 0, 8), (2, 1000, 2, 256, 1, 0, 3),
+                                           (3, 5000, 2, 512, 0, 1, 4), (1, 65536, 6, 256, 1, 0, 1)]:
+        mc = _chunks(B, T, varlen)
+        work = ws(mc, 64, H, 256, dv, io, 0)
+        assert ws_scan(B, T, H, 256, dv, io, varlen, seg) == \
+            _segmented_bytes(B, T, H, dv, varlen, work, min(B * seg, B + mc)), (B, T, seg)
 
 
 def test_workspace_size_queries_reject_bad_arguments(lib):
@@ -262,8 +299,9 @@ def test_workspace_size_queries_reject_bad_arguments(lib):
         assert f(1, 64, 6, 256, 384, 1, 0) == SIZE_MAX
         assert f(1, 64, 6, 256, 256, 7, 0) == SIZE_MAX
         assert f(1, -1, 6, 256, 256, 1, 0) == SIZE_MAX
-    assert ws_scan(1, 4096, 6, 256, 256, 0) == SIZE_MAX
-    assert ws_scan(1, 4096, 0, 256, 256, 4) == SIZE_MAX
+    assert ws_scan(1, 4096, 6, 256, 256, 1, 0, 0) == SIZE_MAX
+    assert ws_scan(1, 4096, 0, 256, 256, 1, 0, 4) == SIZE_MAX
+    assert ws_scan(1, 4096, 6, 256, 256, 2, 0, 4) == SIZE_MAX
 
 
 def test_workspace_sizes_scale_with_the_problem(lib):
@@ -271,10 +309,9 @@ def test_workspace_sizes_scale_with_the_problem(lib):
     # fp32 I/O (CUDA-core path): linear in the number of (chunk, head) units
     a, b = ws(1, 64 * 8, 6, 256, 256, 0, 0), ws(1, 64 * 16, 6, 256, 256, 0, 0)
     assert 0 < a < b and b - a == a - ws(1, 0, 6, 256, 256, 0, 0)
-    # a sequence too short to cut: the scan's scratch is the plain prefill's
-    assert ws_scan(1, 64, 6, 256, 256, 8) == ws(1, 64, 6, 256, 256, 1, 0)
-    # cut: the per-segment states come on top of the images
-    assert ws_scan(1, 65536, 6, 256, 256, 8) > ws(1, 65536, 6, 256, 256, 1, 0)
+    # the segmented form holds the plain images plus the per-segment states
+    assert ws_scan(1, 8192, 6, 256, 256, 1, 0, 8) > ws(1, 8192, 6, 256, 256, 1, 0)
+    assert ws(1, 65536, 6, 256, 256, 1, 0) > ws(1, 65472, 6, 256, 256, 1, 0) + 3 * 6 * 2**18 * 4
     # the backward holds at least the forward's images (bf16) and grows with T
     assert ws_bwd(4, 8192, 6, 256, 256, 1, 0) > ws(4, 8192, 6, 256, 256, 1, 0)
     assert ws_bwd(1, 1024, 6, 256, 256, 0, 0) < ws_bwd(1, 2048, 6, 256, 256, 0, 0)

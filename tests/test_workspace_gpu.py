@@ -54,6 +54,20 @@ def test_prefill_ws_matches_oracle_and_pool_form(gdn_lib, case):
     assert torch.equal(out, out2) and torch.equal(S_final, S2)
 
 
+def test_prefill_ws_segmented_form_matches_pool_form(gdn_lib):
+    """A 64K-token sequence (cut into segments by gdn_prefill) with its scratch
+    in a caller workspace of gdn_prefill_workspace_size bytes: the same bits
+    as the pool form."""
+    case = PrefillCase("ws long", [65536], H=1, io_dtype=torch.bfloat16, seed=70)
+    xd = to_dev(gdn_inputs.make_prefill(case, device="cpu"))
+    args = (xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["S0"])
+    ws = _workspace(gdn_lib.prefill_workspace_size(1, 65536, 1))
+    a = gdn_lib.prefill(*args, workspace=ws)
+    b = gdn_lib.prefill(*args)
+    assert gdn_lib.device_status() == 0
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
 def test_prefill_ws_rejects_a_small_workspace_without_launching(gdn_lib):
     case = PrefillCase("ws small", [256], H=2, io_dtype=torch.bfloat16, seed=65)
     xd = to_dev(gdn_inputs.make_prefill(case, device="cpu"))
@@ -66,15 +80,16 @@ def test_prefill_ws_rejects_a_small_workspace_without_launching(gdn_lib):
     assert e.value.code == 1 and gdn_lib.kernel_launches() == before
 
 
-def test_scan_ws_matches_scan(gdn_lib):
-    case = PrefillCase("ws scan", [1000, 1000], H=2, io_dtype=torch.bfloat16, seed=66)
+@pytest.mark.parametrize("io", [torch.bfloat16, torch.float32])
+def test_scan_ws_matches_scan(gdn_lib, io):
+    case = PrefillCase("ws scan", [1000, 0, 1000], H=2, io_dtype=io, seed=66, varlen=True)
     xd = to_dev(gdn_inputs.make_prefill(case, device="cpu"))
-    need = gdn_lib.prefill_scan_workspace_size(2, 1000, 2, segments=3)
+    need = gdn_lib.prefill_scan_workspace_size(3, 2000, 2, io_dtype=io, varlen=True, segments=3)
     ws = _workspace(need)
     a = gdn_lib.prefill_scan(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["S0"],
-                             segments=3, workspace=ws)
+                             xd["cu_seqlens"], segments=3, workspace=ws)
     b = gdn_lib.prefill_scan(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["S0"],
-                             segments=3)
+                             xd["cu_seqlens"], segments=3)
     assert gdn_lib.device_status() == 0
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
