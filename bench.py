@@ -418,6 +418,25 @@ def run_ours(args, rank, world, local_rank, dist):
     f64 = prefill_flops(c64.lengths)
     del x64, o64, s64
 
+    # ---- the small fp32 prefill (the 1e-4 parity workload, CUDA-core path)
+    # and the packed varlen prefill of 16 sequences of U[1024, 65536] tokens
+    c0 = gdn_inputs.prefill_small_fp32()
+    x0 = gdn_inputs.make_prefill(c0, device=dev)
+    p0 = lambda: gdn.prefill(x0["q"], x0["k"], x0["v"], x0["alpha"], x0["beta"], x0["S0"])
+    p0_ms = time_calls(p0, n=20)
+    f0 = prefill_flops(c0.lengths)
+    del x0
+    cv = gdn_inputs.prefill_varlen16()
+    xv = gdn_inputs.make_prefill(cv, device=dev)
+    ov = torch.empty_like(xv["v"])
+    sv = torch.empty_like(xv["S0"])
+    pv = lambda: gdn.prefill(xv["q"], xv["k"], xv["v"], xv["alpha"], xv["beta"], xv["S0"],
+                             xv["cu_seqlens"], out=ov, S_final=sv)
+    pv_ms = time_calls(pv, n=5)
+    assert gdn.device_status() == 0
+    fv = prefill_flops(cv.lengths)
+    del xv, ov, sv
+
     # ---- backward of the 8K prefill (gdn_prefill_backward), dout and dS_final
     # drawn once; each call recomputes the forward internally
     bx = x
@@ -607,12 +626,52 @@ def run_ours(args, rank, world, local_rank, dist):
                             "counted_tflops": round(prefill_flops(pcase5.lengths, dv=512)
                                                     / (p5_ms * 1e-3) / 1e12, 3)},
             },
+            "prefill_small_fp32": {
+                "workload": c0.name,
+                "value": round(throughput(c0.total_tokens * world, p0_ms) / 1e6, 4),
+                "unit": "Mtok/s/layer", "ms_per_step": round(p0_ms, 4),
+                "path": gdn.prefill_path(c0.io_dtype),
+                "roofline": {"bound": "alu", "unit": "TFLOP/s",
+                             "achieved": round(f0 / (p0_ms * 1e-3) / 1e12, 3),
+                             "peak": round(FP32_FMA_TFLOPS, 1),
+                             "frac": round(f0 / (p0_ms * 1e-3) / 1e12 / FP32_FMA_TFLOPS, 4),
+                             "traffic": ncu_traffic("prefill_fp32"),
+                             "counted_flops_per_launch": f0,
+                             "peak_source": "fp32 FMA of the CUDA cores: 152 SMs x 128 lanes "
+                                            "x 2 FLOP x 2.07 GHz",
+                             "l2": "inputs (9.4 MB) fit in L2: traffic is near compulsory"},
+            },
+            "prefill_varlen16": {
+                "workload": cv.name,
+                "value": round(throughput(cv.total_tokens * world, pv_ms) / 1e6, 4),
+                "unit": "Mtok/s/layer", "ms_per_step": round(pv_ms, 4),
+                "tokens": cv.total_tokens,
+                "roofline": {"bound": "tensor", "unit": "TFLOP/s",
+                             "achieved": round(fv / (pv_ms * 1e-3) / 1e12, 3),
+                             "peak": peaks["bf16"],
+                             "frac": round(fv / (pv_ms * 1e-3) / 1e12 / peaks["bf16"], 5),
+                             "traffic": ncu_traffic("prefill_varlen16"),
+                             "counted_flops_per_launch": fv,
+                             "kernel": "whole gdn_prefill call (segment plan, chunk prep, "
+                                       "state passes, scan)",
+                             "peak_source": f"{peaks['src']} bf16 dense (burst)"},
+            },
             "prefill_64k": {
                 "workload": c64.name,
                 "gdn_prefill": {"ms_per_step": round(p64_ms, 4),
                                 "value": round(c64.total_tokens / (p64_ms * 1e-3) / 1e6, 3),
                                 "unit": "Mtok/s/layer",
-                                "counted_tflops": round(f64 / (p64_ms * 1e-3) / 1e12, 2)},
+                                "counted_tflops": round(f64 / (p64_ms * 1e-3) / 1e12, 2),
+                                "roofline": {
+                                    "bound": "tensor", "unit": "TFLOP/s",
+                                    "achieved": round(f64 / (p64_ms * 1e-3) / 1e12, 3),
+                                    "peak": peaks["bf16"],
+                                    "frac": round(f64 / (p64_ms * 1e-3) / 1e12 / peaks["bf16"], 5),
+                                    "traffic": ncu_traffic("prefill_64k"),
+                                    "counted_flops_per_launch": f64,
+                                    "kernel": "whole gdn_prefill call (7 segments: chunk prep, "
+                                              "two state passes, scan)",
+                                    "peak_source": f"{peaks['src']} bf16 dense (burst)"}},
                 "uncut_chain": {
                     "ms_per_step": round(p64s_ms, 4),
                     "value": round(c64.total_tokens / (p64s_ms * 1e-3) / 1e6, 3),
@@ -706,7 +765,43 @@ def cpu_baseline(args, min_seconds=10.0):
     return {"value": round(tok / dt / 1e6, 8), "unit": "Mtok/s/layer", "cores": int(used),
             "kind": "oracle", "seconds": round(dt, 3),
             "sample": f"{passes} full pass(es) of the prefill workload (4 sequences x 8192 "
-                      f"tokens x 6 heads, {tok} token-layers), fp64 token recurrence"}
+                      f"tokens x 6 heads, {tok} token-layers), fp64 token recurrence",
+            "nproc": os.cpu_count(), "cpu_model": cpu_model(),
+            "single_core": single_core_oracle()}
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def single_core_oracle():
+    """The oracle on one host thread over the whole small fp32 workload (512
+    tokens x 6 heads), and that per-token-head rate carried over to the other
+    prefill workloads (the recurrence costs the same per token and head at
+    dk = dv = 256)."""
+    import gdn_inputs
+    import oracle
+    c0 = gdn_inputs.prefill_small_fp32()
+    x = gdn_inputs.make_prefill(c0, device="cpu")
+    t = time.perf_counter()
+    oracle.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"], nthreads=1)
+    dt = time.perf_counter() - t
+    rate = c0.total_tokens / dt                      # tokens (x 6 heads) per second
+    ext = {c.name: round(c.total_tokens / rate, 1)
+           for c in (gdn_inputs.prefill_8k(), gdn_inputs.prefill_64k(),
+                     gdn_inputs.prefill_varlen16())}
+    return {"value": round(rate / 1e6, 8), "unit": "Mtok/s/layer", "cores": 1,
+            "seconds": round(dt, 3), "sample": "the small fp32 workload in full "
+                                               f"({c0.total_tokens} tokens x 6 heads)",
+            "extrapolated_seconds": ext}
 
 
 def run_profile(args):
@@ -725,6 +820,18 @@ def run_profile(args):
         for _ in range(args.warmup + args.steps):
             gdn.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"], out=out,
                         S_final=sf)
+    elif args.profile in ("prefill_64k", "prefill_fp32", "prefill_varlen8"):
+        if args.profile == "prefill_64k":
+            c = gdn_inputs.prefill_64k()
+        elif args.profile == "prefill_fp32":
+            c = gdn_inputs.prefill_small_fp32()
+        else:   # the first 8 of the varlen workload's 16 sequences (149K tokens)
+            c = gdn_inputs.PrefillCase("varlen prefill N=8 (the first 8 of the N=16 draw) bf16",
+                                       gdn_inputs.prefill_varlen16().lengths[:8], seed=4,
+                                       varlen=True)
+        x = gdn_inputs.make_prefill(c, device=dev)
+        for _ in range(args.warmup + args.steps):
+            gdn.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"], x["cu_seqlens"])
     elif args.profile == "backward":
         x = gdn_inputs.make_prefill(gdn_inputs.prefill_8k(), device=dev)
         dout = torch.randn(x["v"].shape, device=dev).to(x["v"].dtype)
@@ -804,7 +911,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--profile", choices=["prefill", "decode", "layer", "backward", "decode_layer"],
+    ap.add_argument("--profile", choices=["prefill", "decode", "layer", "backward", "decode_layer",
+                                          "prefill_64k", "prefill_fp32", "prefill_varlen8"],
                     default=None,
                     help="run only W + K steps of one kernel family (for ncu captures); "
                          "prints no benchmark line")

@@ -109,14 +109,17 @@ constexpr uint8_t kSegFirst = 1, kSegLast = 2;
 
 // Per-unit routing of the state pass over a segmented packing (the map's
 // sequences are then segment slots).  pass 0: a plain call, every unit runs
-// from S0 into S_final with outputs.  pass 1: the grid holds two units per
-// slot and row block: x < N, a first segment from the caller's start (outputs,
-// end into the caller's S_final when it is also the last segment, else into
-// Bseg) or a middle segment from zero (no outputs, end into Bseg); x >= N, a
-// middle segment from [I; 0] (no outputs, end into Fseg).  pass 2: every
-// segment but the first from its true start S0seg (outputs; end into the
-// caller's S_final for a last segment).  Last segments skip pass 1, first
-// segments pass 2.
+// from S0 into S_final with outputs.  pass 1 (no outputs, except for a
+// sequence left whole): the grid holds two units per slot and row block;
+// x < N runs a sequence left whole from the caller's start into the caller's
+// S_final with outputs, the first segment of a cut sequence from the
+// caller's start into Bseg, a middle segment from zero into Bseg; x >= N runs
+// the A chain of a middle segment into Aseg.  An A chain starts from the
+// identity and drops U~: it carries the product A of the segment's
+// transitions, S_end = S_start A + B, in its dk rows.  pass 2 (outputs):
+// every segment of a cut sequence from its true start (the caller's S0 for
+// the first, S0seg for the others; the last one's end into the caller's
+// S_final).
 struct SegRoute {
   int32_t pass = 0;
   const int32_t* seg_seq = nullptr;   // per slot: its sequence, -1 for an unused slot
@@ -125,13 +128,13 @@ struct SegRoute {
   float* S_final = nullptr;           // the caller's final states, or nullptr
   const float* S0seg = nullptr;       // [slots][H][dv][dk]
   float* Bseg = nullptr;
-  float* Fseg = nullptr;
+  float* Aseg = nullptr;              // [slots][H][dv][dk], rows 0 .. dk-1 used
 };
 
 // Where one unit of the state pass starts and ends; S0 / S_final point at
 // its sequence's (or slot's) [H][dv][dk] block.
 struct UnitRoute {
-  bool run, ident, write_out;
+  bool run, ident, write_out;   // ident: an A chain
   const float* S0;
   float* S_final;
 };
@@ -150,21 +153,24 @@ __device__ __forceinline__ UnitRoute route_unit(const SegRoute& r, const float* 
   const uint8_t ro = r.role[s];
   const bool first = ro & kSegFirst, last = ro & kSegLast;
   u.run = n >= 0;
-  if (r.pass == 1 && second) {          // A + B of a middle segment
+  if (r.pass == 1 && second) {          // A of a middle segment
     u.run = u.run && !first && !last;
     u.ident = true;
     u.write_out = false;
-    u.S_final = r.Fseg + s * per_seq;
-  } else if (r.pass == 1 && first) {    // the sequence's own start
-    u.S0 = r.S0 ? r.S0 + n * per_seq : nullptr;
-    u.S_final = !last ? r.Bseg + s * per_seq : r.S_final ? r.S_final + n * per_seq : nullptr;
-  } else if (r.pass == 1) {             // B of a middle segment
-    u.run = u.run && !last;
-    u.write_out = false;
-    u.S_final = r.Bseg + s * per_seq;
-  } else {                              // the true start of a later segment
-    u.run = u.run && !first;
-    u.S0 = r.S0seg + s * per_seq;
+    u.S_final = r.Aseg + s * per_seq;
+  } else if (r.pass == 1) {
+    if (first && last) {                // a sequence left whole: the plain chain
+      u.S0 = r.S0 ? r.S0 + n * per_seq : nullptr;
+      u.S_final = r.S_final ? r.S_final + n * per_seq : nullptr;
+    } else {                            // B of a first or middle segment
+      u.run = u.run && !last;
+      u.write_out = false;
+      u.S0 = first && r.S0 ? r.S0 + n * per_seq : nullptr;
+      u.S_final = r.Bseg + s * per_seq;
+    }
+  } else {                              // a segment of a cut sequence, with outputs
+    u.run = u.run && !(first && last);
+    u.S0 = !first ? r.S0seg + s * per_seq : r.S0 ? r.S0 + n * per_seq : nullptr;
     u.S_final = last && r.S_final ? r.S_final + n * per_seq : nullptr;
   }
   return u;
@@ -211,11 +217,11 @@ extern int32_t g_last_tc_form;
 // fixes the segment count (forced_P > 0).  Its scratch: chunk offsets,
 // token starts, sequences and roles of the segment slots, the path's
 // per-chunk scratch over the caller's chunks, then three per-(slot, head)
-// states (true starts, ends from zero, ends from [I; 0]).
+// states (true starts, ends from zero, transition products A).
 struct LongPlan {
   int64_t n_slots = 0, max_chunks = 0;
   size_t off_chunk_off = 0, off_seg_cu = 0, off_seg_seq = 0, off_seq_first = 0, off_role = 0,
-         off_work = 0, off_S0seg = 0, off_Bseg = 0, off_Fseg = 0, bytes = 0;
+         off_work = 0, off_S0seg = 0, off_Bseg = 0, off_Aseg = 0, bytes = 0;
 };
 bool long_form_applies(int64_t seqlen);
 LongPlan plan_long(int32_t N, int64_t seqlen, bool varlen, int32_t H, int32_t dv, int io_dtype,

@@ -10,17 +10,20 @@
 // sequence one after another (Appendix A.3, last paragraph), so one long
 // sequence leaves most of the GPU idle.  Cut into P segments it runs as P
 // chains joined by a short sequential scan over the segments' (A, B) pairs:
-//   pass 1  the first segment from the sequence's own start (its outputs are
-//           final; its end state is B(0)), every middle segment from zero
-//           (-> B) and, in the same launch, from [I; 0] (-> F, and A = F - B
-//           over the first dk rows);
+//   pass 1  every segment but the last, without outputs: the first from the
+//           sequence's own start (-> B(0), its true end state), the middle
+//           ones from zero (-> B) and, in the same launch, their A chains:
+//           the same chunks from the identity with the inhomogeneous term U~
+//           dropped (-> A);
 //   scan    start(1) = B(0); start(j) = start(j-1) A(j-1) + B(j-1);
-//   pass 2  every segment but the first from its true start: outputs, and the
+//   pass 2  every segment from its true start: the outputs, and the
 //           sequence's final state from the last one.
-// The critical path is two segments instead of P; the work is 3 - 4/P times
-// that of the single chain.  Segments start on chunk boundaries of their
-// sequence, so the per-chunk factors are the plain prefill's, computed once
-// over the segmented packing (the same chunks in the same order).
+// The critical path is two segments instead of P, and the chains without
+// outputs load about two thirds of the bytes per chunk (neither Q^ nor P^;
+// an A chain not even U~); the work is 3 - 3/P chains' worth.  Segments
+// start on chunk boundaries of their sequence, so the per-chunk factors are
+// the plain prefill's, computed once over the segmented packing (the same
+// chunks in the same order).
 //
 // Which sequences are cut, and where, depends on nothing but the sequence's
 // own length (or, for gdn_prefill_scan, the caller's segment count), so a
@@ -147,18 +150,22 @@ __global__ void plan_segments_kernel(const int32_t* __restrict__ cu, int32_t N, 
 
 // The scan, one CTA per (16 rows of the state, head) of a sequence: rows of S
 // are independent under right-multiplication by A, so each CTA walks its
-// sequence's segments on its own.  Thread c owns column c of its 16 rows; for
-// each segment it streams column c of A = F - B (coalesced across the CTA)
-// through registers, eight k at a time, against the previous start's rows in
-// shared memory.
+// sequence's segments on its own.  Thread c owns column c of its 16 rows;
+// the previous start's rows sit in shared memory and column c of each A
+// streams through registers in blocks of 32 rows of A, the next block's loads
+// (coalesced across the CTA) in flight while the current one is consumed:
+// no A depends on the scan, so the stream never waits on the arithmetic.
+constexpr int kScanBlk = 32;
+
 __global__ void __launch_bounds__(256) seg_scan_kernel(float* __restrict__ S0seg,
                                                        const float* __restrict__ Bseg,
-                                                       const float* __restrict__ Fseg,
+                                                       const float* __restrict__ Aseg,
                                                        const int32_t* __restrict__ seq_first,
                                                        int32_t N, int32_t H, int32_t dv) {
-  __shared__ float prev[kScanRows][kDK];
+  __shared__ __align__(16) float prev[kScanRows][kDK];
   const int r0 = blockIdx.x * kScanRows, h = blockIdx.y, c = threadIdx.x;
   const int64_t st = (int64_t)dv * kDK;
+  constexpr int kBlocks = kDK / kScanBlk;   // blocks of A rows per step
   for (int n = blockIdx.z; n < N; n += gridDim.z) {
     const int32_t f = seq_first[n], P = seq_first[n + 1] - f;
     if (P < 2) continue;   // the same for the whole CTA
@@ -172,31 +179,46 @@ __global__ void __launch_bounds__(256) seg_scan_kernel(float* __restrict__ S0seg
       prev[r][c] = x;
       start_of(1)[(r0 + r) * kDK + c] = x;
     }
-    for (int j = 2; j < P; ++j) {
-      const float* Bj = at(Bseg, j - 1);
-      const float* Fj = at(Fseg, j - 1);
-      float acc[kScanRows];
+    // block t of the stream: step j = 2 + t / kBlocks, rows kScanBlk (t %
+    // kBlocks) .. of A(j - 1)
+    const int n_blk = (P - 2) * kBlocks;
+    float a_cur[kScanBlk], a_nxt[kScanBlk], acc[kScanRows];
+    auto load_blk = [&](int t, float* dst) {
+      const float* A = at(Aseg, 1 + t / kBlocks) + (int64_t)(kScanBlk * (t % kBlocks)) * kDK + c;
 #pragma unroll
-      for (int r = 0; r < kScanRows; ++r) acc[r] = Bj[(r0 + r) * kDK + c];
-      __syncthreads();   // prev holds start(j - 1)
-      for (int k0 = 0; k0 < kDK; k0 += 8) {
-        float a[8];
+      for (int i = 0; i < kScanBlk; ++i) dst[i] = A[(int64_t)i * kDK];
+    };
+    if (n_blk > 0) load_blk(0, a_cur);
+    for (int t = 0; t < n_blk; ++t) {
+      const int j = 2 + t / kBlocks, kb = t % kBlocks;
+      if (t + 1 < n_blk) load_blk(t + 1, a_nxt);
+      if (kb == 0) {
+        const float* Bj = at(Bseg, j - 1);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {   // A = F - B over the first dk rows
-          const int64_t g = (int64_t)(k0 + kk) * kDK + c;
-          a[kk] = Fj[g] - Bj[g];
+        for (int r = 0; r < kScanRows; ++r) acc[r] = Bj[(r0 + r) * kDK + c];
+        __syncthreads();   // prev holds start(j - 1)
+      }
+#pragma unroll
+      for (int i = 0; i < kScanBlk; i += 4) {
+#pragma unroll
+        for (int r = 0; r < kScanRows; ++r) {
+          const float4 p = *reinterpret_cast<const float4*>(&prev[r][kScanBlk * kb + i]);
+          acc[r] = fmaf(p.x, a_cur[i], acc[r]);
+          acc[r] = fmaf(p.y, a_cur[i + 1], acc[r]);
+          acc[r] = fmaf(p.z, a_cur[i + 2], acc[r]);
+          acc[r] = fmaf(p.w, a_cur[i + 3], acc[r]);
         }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-#pragma unroll
-          for (int r = 0; r < kScanRows; ++r) acc[r] = fmaf(prev[r][k0 + kk], a[kk], acc[r]);
       }
-      __syncthreads();   // every thread is done reading start(j - 1)
+      if (kb == kBlocks - 1) {
+        __syncthreads();   // every thread is done reading start(j - 1)
 #pragma unroll
-      for (int r = 0; r < kScanRows; ++r) {
-        prev[r][c] = acc[r];
-        start_of(j)[(r0 + r) * kDK + c] = acc[r];
+        for (int r = 0; r < kScanRows; ++r) {
+          prev[r][c] = acc[r];
+          start_of(j)[(r0 + r) * kDK + c] = acc[r];
+        }
       }
+#pragma unroll
+      for (int i = 0; i < kScanBlk; ++i) a_cur[i] = a_nxt[i];
     }
   }
 }
@@ -230,7 +252,7 @@ LongPlan plan_long(int32_t N, int64_t seqlen, bool varlen, int32_t H, int32_t dv
   p.off_work = o;      o += align_up(work, 256);
   p.off_S0seg = o;     o += states;
   p.off_Bseg = o;      o += states;
-  p.off_Fseg = o;      o += states;
+  p.off_Aseg = o;      o += states;
   p.bytes = o;
   return p;
 }
@@ -282,7 +304,7 @@ cudaError_t launch_prefill_long(const PrefillLaunch& base, int io_dtype, const L
   a.route.S_final = base.S_final;
   a.route.S0seg = (const float*)(scr + p.off_S0seg);
   a.route.Bseg = (float*)(scr + p.off_Bseg);
-  a.route.Fseg = (float*)(scr + p.off_Fseg);
+  a.route.Aseg = (float*)(scr + p.off_Aseg);
   auto run = [&](bool state_only, int pass) {
     a.state_only = state_only;
     a.route.pass = pass;
@@ -294,7 +316,7 @@ cudaError_t launch_prefill_long(const PrefillLaunch& base, int io_dtype, const L
   // the scan: every later segment's true start
   seg_scan_kernel<<<dim3((unsigned)(dv / kScanRows), (unsigned)H,
                          (unsigned)std::min<int32_t>(N, 65535)),
-                    256, 0, stream>>>((float*)(scr + p.off_S0seg), a.route.Bseg, a.route.Fseg,
+                    256, 0, stream>>>((float*)(scr + p.off_S0seg), a.route.Bseg, a.route.Aseg,
                                       seq_first, N, H, dv);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -203,7 +203,7 @@ state_pass_kernel(const T* __restrict__ q, const T* __restrict__ k,
   const int tid = threadIdx.x, i = tid & 31, rg = tid >> 5;
   const int dv = scr.dv;
   const UnitRoute ur = route_unit(route, S0, S_final, x, map.N, (int64_t)H * dv * kDK);
-  // a chain from [I; 0] needs only the first dk rows
+  // an A chain (identity start, no U~) has dk rows
   if (!ur.run || (ur.ident && slice * kNS >= kDK)) return;
   // this CTA's rows of the unit's [H][dv][dk] start and end blocks
   const int64_t state_base = (int64_t)h * dv * kDK + (int64_t)slice * kNS * kDK;
@@ -258,7 +258,8 @@ state_pass_kernel(const T* __restrict__ q, const T* __restrict__ k,
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       const int r = rg * 8 + m;
-      Us[r * 33 + i] = Ug[r * dv + slice * kNS + i] - accU[m];
+      // an A chain drops U~ (the homogeneous part of the recurrence)
+      Us[r * 33 + i] = (ur.ident ? 0.f : Ug[r * dv + slice * kNS + i]) - accU[m];
     }
     __syncthreads();
 

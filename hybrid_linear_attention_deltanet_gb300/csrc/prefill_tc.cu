@@ -728,7 +728,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
                                            const uint32_t* ready, unsigned* status,
                                            uint64_t* __restrict__ trace, int32_t trace_chunks,
                                            int32_t dv, int n, int h, int slice,
-                                           float* __restrict__ sdump, bool ident_start = false) {
+                                           float* __restrict__ sdump, bool a_chain = false) {
   const int unit = (n * H + h) * (dv / 128) + slice;
   const bool timed = trace && threadIdx.x == 0 && unit < kMaxTracedUnits;
   if (timed) trace[kUnitTimes + 3 * unit] = globaltimer_ns();
@@ -784,11 +784,11 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
       S[4 * j] = t.x; S[4 * j + 1] = t.y; S[4 * j + 2] = t.z; S[4 * j + 3] = t.w;
     }
   } else {
-    // zero, or [I; 0] (identity in the first dk rows: the transition of the
-    // chunks from an identity start)
+    // zero, or the identity (an A chain: the product of the chunks'
+    // transitions, rows 0 .. dk-1)
     const uint32_t row = 128 * slice + iloc, col0 = 128 * colhalf;
 #pragma unroll
-    for (int j = 0; j < 128; ++j) S[j] = ident_start && row == col0 + j ? 1.f : 0.f;
+    for (int j = 0; j < 128; ++j) S[j] = a_chain && row == col0 + j ? 1.f : 0.f;
   }
   tc_fence_before();
   __syncthreads();
@@ -807,10 +807,23 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   };
   store_S_operand();
 
+  // A unit whose outputs nobody reads (the long-sequence form's B and A
+  // chains) needs neither Q^ nor P^: its MMA-1 is N = 64 over W alone, it
+  // skips MMA-O and the output epilogue, and an A chain also skips U~ (it
+  // reads only the decay block), so its chunk loads 80.5 KB (64.5 KB)
+  // instead of 120.5 KB.
+  const bool nout = out == nullptr;
   auto img_of = [&](int64_t ci) { return scratch + (size_t)(ci * H + h) * img_stride(dv); };
   auto t0_of = [&](int64_t ci) { return (int32_t)(s_begin + (ci - cb) * kC); };
   auto flag_of = [&](int64_t ci) { return ready + ci * H + h; };
   auto issue_wq = [&](int64_t ci, int buf) {   // W and Q^ are adjacent in the image
+    if (nout) {   // the four 8 KB blocks of W, each followed by Q^'s in the image
+      mbar_arrive_expect_tx(&bar_wq[buf], 32768);
+      for (int b = 0; b < 4; ++b)
+        tma_load_1d(sm + kS_WQ + buf * 65536 + b * 16384, img_of(ci) + kImgWQ + b * 16384, 8192,
+                    &bar_wq[buf]);
+      return;
+    }
     mbar_arrive_expect_tx(&bar_wq[buf], 65536);
     tma_load_1d(sm + kS_WQ + buf * 65536, img_of(ci) + kImgWQ, 65536, &bar_wq[buf]);
   };
@@ -823,6 +836,12 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     tma_load_1d(sm + kS_KP + buf * 40960 + 32768, img_of(ci) + kImgP, 8192, &bar_p[buf]);
   };
   auto issue_u = [&](int64_t ci) {    // this half's U~^T rows and the decay block
+    if (a_chain) {                    // the decay block alone
+      mbar_arrive_expect_tx(&bar_u, (uint32_t)(kImgHalf - kImgDecay));
+      tma_load_1d(sm + kS_UT + kImgDecay, img_of(ci) + kImgU0 + slice * kImgHalf + kImgDecay,
+                  (uint32_t)(kImgHalf - kImgDecay), &bar_u);
+      return;
+    }
     mbar_arrive_expect_tx(&bar_u, (uint32_t)kImgHalf);
     tma_load_1d(sm + kS_UT, img_of(ci) + kImgU0 + slice * kImgHalf, (uint32_t)kImgHalf, &bar_u);
   };
@@ -888,7 +907,9 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   };
   auto load_pu = [&](int64_t ci, int buf) -> bool {   // (kLoaderC)
     if (!is_ready(ci, true)) return false;
-    issue_p(ci, buf); ++n_p[buf];
+    if (!nout) {
+      issue_p(ci, buf); ++n_p[buf];
+    }
     issue_u(ci); ++n_u;
     return true;
   };
@@ -977,7 +998,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
         // [D_U | D_O] = S [W | Q^]^T : one N = 128 operand (MN-major; for the
         // 16 K-rows of step s, block s / 4 of W at 16 KB strides and the
         // matching Q^ block 8 KB after it)
-        const uint32_t id1 = idesc_bf16(128, 128, 0, 1);
+        const uint32_t id1 = idesc_bf16(128, nout ? 64 : 128, 0, 1);
         const uint32_t sW = smem_u32(sm + kS_WQ + buf * 65536);
         for (int s = 0; s < 16; ++s)
           mma_bf16_ts(tmem + kT_U, tmem + kT_SA + 8 * s,
@@ -1017,8 +1038,9 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = 8 * cq + 2 * e, r = 32 * colhalf + j;
-          const float u0 = bf16_lo(uw[e]) - __uint_as_float(g[j]);
-          const float u1 = bf16_hi(uw[e]) - __uint_as_float(g[j + 1]);
+          // an A chain drops U~ (the homogeneous part of the recurrence)
+          const float u0 = (a_chain ? 0.f : bf16_lo(uw[e])) - __uint_as_float(g[j]);
+          const float u1 = (a_chain ? 0.f : bf16_hi(uw[e])) - __uint_as_float(g[j + 1]);
           const float d0 = sD[r], d1 = sD[r + 1];
           ua[4 * cq + e] = pack_bf16(u0, u1);
           ud[4 * cq + e] = pack_bf16(u0 * d0, u1 * d1);
@@ -1036,7 +1058,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
 
     // 3. D_S = (dU)^T K (commit m2) ; D_O += U^T P^^T (commit mo)
     if (tid == 0) {
-      if (!mbar_wait(&bar_kp[buf], bpar) || !mbar_wait(&bar_p[buf], bpar)) {
+      if (!mbar_wait(&bar_kp[buf], bpar) || (!nout && !mbar_wait(&bar_p[buf], bpar))) {
         s_abort = 1;
       } else {
         tc_fence_after();
@@ -1046,10 +1068,12 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
           mma_bf16_ts(tmem + kT_S, tmem + kT_U + col_dU(s),
                       smem_desc(sK + s * 2048, 8192, 1024, kSwizzle128B), id2, s > 0);
         mma_commit(&bar_m2);
-        for (int s = 0; s < 4; ++s)
-          mma_bf16_ts(tmem + kT_O, tmem + kT_U + col_U(s),
-                      smem_desc(sP + s * 32, 16, 1024, kSwizzle128B), idO, 1);
-        mma_commit(&bar_mo);
+        if (!nout) {
+          for (int s = 0; s < 4; ++s)
+            mma_bf16_ts(tmem + kT_O, tmem + kT_U + col_U(s),
+                        smem_desc(sP + s * 32, 16, 1024, kSwizzle128B), idO, 1);
+          mma_commit(&bar_mo);
+        }
       }
     }
     // ... meanwhile the loaders fetch ahead: K / P^ and U~^T of the next
@@ -1108,7 +1132,8 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
       }
       tmem_st_wait();
       stamp(it, 9);
-      if (!mbar_wait(&bar_mo, par)) {
+      if (nout) {
+      } else if (!mbar_wait(&bar_mo, par)) {
         flag_status(status, GDN_ERR_TIMEOUT);
         s_abort = 1;
       } else {
@@ -1188,8 +1213,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
   extern __shared__ uint8_t smem_raw[];
   const int x = blockIdx.x;
   const UnitRoute u = route_unit(route, S0, S_final, x, map.N, (int64_t)H * dv * kDK);
-  // the whole CTA, before any barrier or TMEM allocation; a chain from
-  // [I; 0] needs only the first dk rows
+  // the whole CTA, before any barrier or TMEM allocation; an A chain has
+  // dk rows
   if (!u.run || (u.ident && 128 * (int)blockIdx.z >= kDK)) return;
   state_role<false>(align_smem_1024(smem_raw), &tm_k, u.S0, u.write_out ? out : nullptr,
                     u.S_final, map, H, scratch, nullptr, status, trace, trace_chunks, dv,
