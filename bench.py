@@ -820,6 +820,16 @@ def run_profile(args):
         for _ in range(args.warmup + args.steps):
             gdn.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"], out=out,
                         S_final=sf)
+    elif args.profile == "layer_fused":
+        # gdn_prefill_layer on the 8K layer inputs, per step
+        lc = gdn_inputs.layer_8k()
+        lx = gdn_inputs.make_layer(lc, device=dev)
+        S0 = torch.randn((len(lc.lengths), lc.H, lc.dv, lc.dk), device=dev) * 0.02
+        st = torch.empty_like(lx["conv_state"])
+        for _ in range(args.warmup + args.steps):
+            gdn.prefill_layer(lx["qkv"], lx["conv_w"], lx["a_raw"], lx["b_raw"], lx["A_log"],
+                              lx["dt_bias"], lx["g"], lx["norm_w"], lc.H, S0=S0,
+                              conv_state_in=lx["conv_state"], conv_state_out=st)
     elif args.profile in ("prefill_64k", "prefill_fp32", "prefill_varlen8"):
         if args.profile == "prefill_64k":
             c = gdn_inputs.prefill_64k()
@@ -912,7 +922,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--profile", choices=["prefill", "decode", "layer", "backward", "decode_layer",
-                                          "prefill_64k", "prefill_fp32", "prefill_varlen8"],
+                                          "prefill_64k", "prefill_fp32", "prefill_varlen8",
+                                          "layer_fused"],
                     default=None,
                     help="run only W + K steps of one kernel family (for ncu captures); "
                          "prints no benchmark line")

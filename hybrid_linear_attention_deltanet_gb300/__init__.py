@@ -96,6 +96,9 @@ def load():
     lib.gdn_prefill_backward_workspace_size.restype = sz
     lib.gdn_prefill_backward_ws.argtypes = [vp] * 15 + [i32, i64, i32, i32, i32, i32, vp, sz, vp]
     lib.gdn_prefill_backward_ws.restype = ctypes.c_int
+    lib.gdn_prefill_layer.argtypes = [vp] * 12 + [ctypes.c_float, i32, vp, vp, i32, i64, i32,
+                                                  i32, i32, i32, vp]
+    lib.gdn_prefill_layer.restype = ctypes.c_int
     lib.gdn_release_scratch.restype = ctypes.c_int
     lib.gdn_testing_scratch_reserved.argtypes = [vp]
     lib.gdn_testing_scratch_reserved.restype = ctypes.c_int
@@ -516,6 +519,72 @@ def decode_layer_step(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, conv_state, S, 
     if rc != 0:
         raise GDNError("gdn_decode_layer_step", rc)
     return y
+
+
+def prefill_layer(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, gate, norm_w, heads, S0=None,
+                  cu_seqlens=None, conv_state_in=None, conv_state_out=None, eps=1e-5, act="silu",
+                  y=None, S_final=None, return_final=True, stream=None):
+    """The mixer core over whole sequences in one pass (``gdn_prefill_layer``):
+    :func:`prepare`, :func:`prefill` and :func:`output_norm_gate` fused into
+    the tensor-core prefill (bf16, dk = dv = 256).  qkv [B, T, C] or [T, C]
+    (packed with ``cu_seqlens``); a_raw, b_raw [.., H]; gate [.., H, dv];
+    S0 / S_final [N, H, dv, dk]; conv states [N, 3, C].  Returns (y, S_final)."""
+    lib = load()
+    dev, io = qkv.device, qkv.dtype
+    if io != torch.bfloat16:
+        raise TypeError("prefill_layer takes bf16 projections")
+    H, dk, dv = heads, 256, 256
+    C = H * (2 * dk + dv)
+    _check(qkv, "qkv", io, dev)
+    if qkv.shape[-1] != C or qkv.dim() not in (2, 3):
+        raise ValueError(f"qkv must be [B, T, {C}] or [T, {C}]")
+    lead = tuple(qkv.shape[:-1])
+    for name, t in (("a_raw", a_raw), ("b_raw", b_raw)):
+        _check(t, name, torch.float32, dev)
+        if tuple(t.shape) != lead + (H,):
+            raise ValueError(f"{name} must be {list(lead + (H,))}")
+    for name, t, shape in (("conv_w", conv_w, (C, 4)), ("A_log", A_log, (H,)),
+                           ("dt_bias", dt_bias, (H,)), ("norm_w", norm_w, (dv,))):
+        _check(t, name, torch.float32, dev)
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be {list(shape)}")
+    _check(gate, "gate", io, dev)
+    if tuple(gate.shape) != lead + (H, dv):
+        raise ValueError(f"gate must be {list(lead + (H, dv))}")
+    if cu_seqlens is None:
+        B, T = (qkv.shape[0], qkv.shape[1]) if qkv.dim() == 3 else (1, qkv.shape[0])
+        N, seqlen = B, T
+    else:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        if qkv.dim() == 3 and qkv.shape[0] != 1:
+            raise ValueError("varlen input must have batch axis 1")
+        N, seqlen = cu_seqlens.numel() - 1, qkv.shape[-2]
+    for name, t in (("conv_state_in", conv_state_in), ("conv_state_out", conv_state_out)):
+        if t is not None:
+            _check(t, name, io, dev)
+            if tuple(t.shape) != (N, 3, C):
+                raise ValueError(f"{name} must be [{N}, 3, {C}]")
+    if S0 is not None:
+        _check(S0, "S0", torch.float32, dev)
+        if tuple(S0.shape) != (N, H, dv, dk):
+            raise ValueError(f"S0 must be [{N}, {H}, {dv}, {dk}]")
+    if y is None:
+        y = torch.empty_like(gate)
+    else:
+        _check(y, "y", io, dev)
+    if S_final is None and return_final:
+        S_final = torch.empty((N, H, dv, dk), dtype=torch.float32, device=dev)
+    elif S_final is not None:
+        _check(S_final, "S_final", torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = lib.gdn_prefill_layer(
+            _ptr(qkv), _ptr(conv_w), _ptr(a_raw), _ptr(b_raw), _ptr(A_log), _ptr(dt_bias),
+            _ptr(conv_state_in), _ptr(conv_state_out), _ptr(S0), _ptr(cu_seqlens), _ptr(gate),
+            _ptr(norm_w), float(eps), GATE_ACT[act], _ptr(y), _ptr(S_final), N, seqlen, H, dk,
+            dv, GDN_BF16, _stream_handle(stream))
+    if rc != 0:
+        raise GDNError("gdn_prefill_layer", rc)
+    return y, S_final
 
 
 def device_status(stream=None) -> int:

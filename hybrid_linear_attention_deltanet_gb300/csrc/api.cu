@@ -165,7 +165,6 @@ extern "C" {
 }  // extern "C"
 
 namespace gdn {
-namespace {
 
 // Scratch of one prefill call.  Plain form: the packed batch's chunk
 // offsets, then the path's per-chunk scratch (bf16 I/O: the tensor-core
@@ -188,6 +187,34 @@ size_t prefill_scratch_bytes(int32_t batch, int64_t seqlen, int32_t heads, int32
                                 : prefill_simt_scratch_bytes(max_chunks, heads, dv);
   return off_bytes + work_bytes;
 }
+
+// The prefill of a validated problem (a: the caller's map, tensors and
+// status word) with `scratch` of prefill_scratch_bytes(...) bytes: the
+// segmented form, or the chunk offsets of a packed batch and the path's
+// kernels.
+cudaError_t launch_prefill_any(PrefillLaunch a, int32_t io_dtype, int64_t seqlen,
+                               int32_t forced_P, void* scratch, cudaStream_t stream) {
+  const bool varlen = a.map.cu_seqlens != nullptr;
+  if (takes_long_form(seqlen, forced_P)) {
+    a.scratch = scratch;
+    return launch_prefill_long(a, io_dtype,
+                               plan_long(a.map.N, seqlen, varlen, a.H, a.dv, io_dtype, forced_P),
+                               forced_P, stream);
+  }
+  const size_t off_bytes = varlen ? align_up(((size_t)a.map.N + 1) * 4, 256) : 0;
+  a.scratch = (char*)scratch + off_bytes;
+  if (varlen) {
+    a.map.chunk_off = (int32_t*)scratch;
+    const int64_t T_total = a.map.T;
+    const cudaError_t e =
+        launch_chunk_offsets(a.map.cu_seqlens, a.map.N, T_total, (int32_t*)scratch, a.status, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return io_dtype == GDN_BF16 ? launch_prefill_tc(a, stream)
+                              : launch_prefill_simt(a, io_dtype, stream);
+}
+
+namespace {
 
 bool prefill_shape_ok(int32_t batch, int64_t seqlen, int32_t heads, int32_t dk, int32_t dv,
                       int32_t io_dtype) {
@@ -280,20 +307,8 @@ int prefill_common(const void* q, const void* k, const void* v, const float* alp
       (!scratch_pool() ||
        cudaMallocFromPoolAsync(&scratch, need, scratch_pool(), stream) != cudaSuccess))
     return GDN_ERR_CUDA;
-  cudaError_t e = cudaSuccess;
-  if (long_form) {
-    a.scratch = scratch;
-    e = launch_prefill_long(a, io_dtype, plan, forced_P, stream);
-  } else {
-    const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
-    a.scratch = (char*)scratch + off_bytes;
-    if (varlen) {
-      a.map.chunk_off = (int32_t*)scratch;
-      e = launch_chunk_offsets(cu_seqlens, batch, T_total, (int32_t*)scratch, status, stream);
-    }
-    if (e == cudaSuccess)
-      e = tc ? launch_prefill_tc(a, stream) : launch_prefill_simt(a, io_dtype, stream);
-  }
+  (void)tc;
+  const cudaError_t e = launch_prefill_any(a, io_dtype, seqlen, forced_P, scratch, stream);
   const cudaError_t ef = (!use_ws && scratch) ? cudaFreeAsync(scratch, stream) : cudaSuccess;
   return (e == cudaSuccess && ef == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -176,6 +176,42 @@ __device__ __forceinline__ UnitRoute route_unit(const SegRoute& r, const float* 
   return u;
 }
 
+// Eq. 20's read-out applied by the tensor-core state pass to its outputs (the
+// layer entry point): y = o / sqrt(mean(o^2) + eps) * w * act(gate) over the
+// dv values of each (token, head), written in place of o.  The two 128-row
+// units of a head run as a 2-CTA cluster and exchange each token's partial
+// sum of squares through distributed shared memory (dv = 256 only).
+struct NormGate {
+  const __nv_bfloat16* gate = nullptr;   // [T_total, H, dv]; nullptr: plain outputs
+  const float* w = nullptr;              // [dv]
+  float eps = 0.f;
+  int32_t act = 0;                       // GDN_GATE_SILU or GDN_GATE_SIGMOID
+};
+
+// The layer entry point's pre-recurrence steps, run by the tensor-core prep
+// on its input tiles (Appendix A.3, the paragraph after Table 8 and the text
+// under Eq. 16-21): the q, k, v tiles of a (chunk, head) come from the packed
+// projection qkv and pass through the causal depthwise convolution of width 4
+// and SiLU in shared memory (q and k then L2-normalised per head); alpha and
+// beta come from a_raw / b_raw.  The processed keys also go to k_out, where
+// the state pass reads its K tiles.  dv = 256 only.
+struct ConvIn {
+  const __nv_bfloat16* qkv = nullptr;        // [T_total, C], C = H (2 dk + dv); nullptr: off
+  const float* conv_w = nullptr;             // [C, 4]
+  const __nv_bfloat16* state_in = nullptr;   // [N, 3, C], or nullptr (zero history)
+  __nv_bfloat16* state_out = nullptr;        // [N, 3, C], or nullptr
+  const float* a_raw = nullptr;              // [T_total, H]
+  const float* b_raw = nullptr;              // [T_total, H]
+  const float* A_log = nullptr;              // [H]
+  const float* dt_bias = nullptr;            // [H]
+  __nv_bfloat16* k_out = nullptr;            // [T_total, H, dk]
+  // over a segmented packing (the long-sequence form): each slot's sequence
+  // and role, so that a segment's first rows continue its sequence's earlier
+  // tokens and only a sequence's last segment writes state_out
+  const int32_t* seg_seq = nullptr;
+  const uint8_t* seg_role = nullptr;
+};
+
 struct PrefillLaunch {
   const void* q; const void* k; const void* v;
   const float* alpha; const float* beta; const float* S0;
@@ -192,6 +228,8 @@ struct PrefillLaunch {
   bool state_only;      // the per-chunk factors are already in scratch (an earlier call on
                         // the same inputs and map): run the state pass only
   SegRoute route;       // see SegRoute (pass != 0 forces the split form)
+  NormGate ng;          // tensor-core path: see NormGate (forces the split form)
+  ConvIn cv;            // tensor-core path: see ConvIn (q, k, v, alpha, beta unused)
 };
 
 cudaError_t launch_chunk_offsets(const int32_t* cu_seqlens, int32_t N, int64_t T_total,
@@ -230,6 +268,18 @@ LongPlan plan_long(int32_t N, int64_t seqlen, bool varlen, int32_t H, int32_t dv
 // as given), scratch = the start of plan.bytes of device memory
 cudaError_t launch_prefill_long(const PrefillLaunch& base, int io_dtype, const LongPlan& plan,
                                 int32_t forced_P, cudaStream_t stream);
+
+// The whole prefill (api.cu): which form a call takes, its scratch bytes,
+// and its launches into scratch of that size (a: the caller's problem, with
+// its status word; the form and layout as gdn_prefill_workspace_size states).
+bool takes_long_form(int64_t seqlen, int32_t forced_P);
+size_t prefill_scratch_bytes(int32_t batch, int64_t seqlen, int32_t heads, int32_t dv,
+                             int32_t io_dtype, bool varlen, int32_t forced_P);
+cudaError_t launch_prefill_any(PrefillLaunch a, int32_t io_dtype, int64_t seqlen,
+                               int32_t forced_P, void* scratch, cudaStream_t stream);
+// stream-ordered scratch from the library's pool
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t stream);
+cudaError_t scratch_free(void* p, cudaStream_t stream);
 
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, const float* alpha,
                                const float* beta, float* S, void* out, int32_t N, int32_t H,

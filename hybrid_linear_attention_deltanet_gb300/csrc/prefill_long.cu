@@ -305,6 +305,10 @@ cudaError_t launch_prefill_long(const PrefillLaunch& base, int io_dtype, const L
   a.route.S0seg = (const float*)(scr + p.off_S0seg);
   a.route.Bseg = (float*)(scr + p.off_Bseg);
   a.route.Aseg = (float*)(scr + p.off_Aseg);
+  if (a.cv.qkv) {
+    a.cv.seg_seq = seg_seq;
+    a.cv.seg_role = role;
+  }
   auto run = [&](bool state_only, int pass) {
     a.state_only = state_only;
     a.route.pass = pass;

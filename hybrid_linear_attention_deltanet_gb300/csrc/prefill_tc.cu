@@ -92,6 +92,13 @@ __device__ __forceinline__ float exp_fast(float x) {
   return y;
 }
 
+// tanh on the special-function unit (absolute error about 2^-11)
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // byte offset of 16-byte chunk `ch` (0..7) of row `row` in a 128-byte-swizzled image
 __device__ __forceinline__ uint32_t sw_chunk(uint32_t row, uint32_t ch) {
   return row * 128u + ((ch ^ (row & 7u)) << 4);
@@ -146,6 +153,7 @@ struct PrepSmem {
 struct PrepItem {
   int64_t ci = 0, t0 = 0;   // global chunk index, first token
   int h = 0, L = 0;         // head, valid rows
+  int n = 0;                // sequence
 };
 
 
@@ -156,15 +164,15 @@ struct PrepItem {
 template <bool kOrdered>
 __device__ __forceinline__ bool prep_item(const SeqMap& map, int32_t H, int64_t j, PrepItem& it) {
   if (!kOrdered) {
-    int n;
     it.ci = j / H;
     it.h = (int)(j % H);
-    return map.locate(it.ci, n, it.t0, it.L);
+    return map.locate(it.ci, it.n, it.t0, it.L);
   }
   const int64_t nh = (int64_t)map.N * H;
   const int64_t p = j / nh;
   const int rem = (int)(j - p * nh);
   const int n = rem / H;
+  it.n = n;
   it.h = rem - n * H;
   const int64_t cb = map.chunk_begin(n);
   if (cb + p >= map.chunk_end(n)) return false;
@@ -185,7 +193,7 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
                                           const float* __restrict__ beta, const SeqMap& map,
                                           int32_t H, uint8_t* __restrict__ scratch,
                                           uint32_t* ready, unsigned* status, int32_t dv,
-                                          uint64_t* __restrict__ trace,
+                                          const ConvIn& cv, uint64_t* __restrict__ trace,
                                           uint64_t* __restrict__ timeline, int64_t n_items,
                                           int64_t worker, int64_t n_workers) {
   constexpr int kBufs = kFused ? 2 : 1;
@@ -241,11 +249,14 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
   };
   // copies issued by kPrepIO, counted per barrier for a clean exit after a timeout
   uint32_t n_kq[kBufs] = {}, n_v = 0;
+  // (conv) q, k and v heads are heads h, H + h and 2H + h of the packed qkv rows
+  const bool conv = cv.qkv != nullptr;
+  const int kh0 = conv ? H : 0, vh0 = conv ? 2 * H : 0;
   auto issue_kq = [&](const PrepItem& it, int b) {
     uint8_t* dst = sm + Lay::KQ + b * 65536;
     mbar_arrive_expect_tx(&bar_kq[b], 65536);
     for (int kb = 0; kb < 4; ++kb) {
-      tma_load_3d(dst + kb * 16384, tm_k, kb * 64, it.h, (int32_t)it.t0, &bar_kq[b]);
+      tma_load_3d(dst + kb * 16384, tm_k, kb * 64, kh0 + it.h, (int32_t)it.t0, &bar_kq[b]);
       tma_load_3d(dst + kb * 16384 + 8192, tm_q, kb * 64, it.h, (int32_t)it.t0, &bar_kq[b]);
     }
     ++n_kq[b];
@@ -254,7 +265,8 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
   auto issue_v = [&](const PrepItem& it, int vh, uint8_t* dst, uint32_t block_stride) {
     mbar_arrive_expect_tx(&bar_v, 32768);
     for (int b = 0; b < 4; ++b)
-      tma_load_3d(dst + b * block_stride, tm_v, kDK * vh + b * 64, it.h, (int32_t)it.t0, &bar_v);
+      tma_load_3d(dst + b * block_stride, tm_v, kDK * vh + b * 64, vh0 + it.h, (int32_t)it.t0,
+                  &bar_v);
     ++n_v;
   };
   auto img_of = [&](const PrepItem& it) {
@@ -266,6 +278,132 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
     fence_proxy_async_global();
     st_release_gpu(ready + it.ci * H + it.h, 1u);
   };
+
+  // alpha and beta of token t0 + tid of an item: read, or (conv) computed
+  // from the gate projections as the separate pre-recurrence pass does
+  auto gates_of = [&](const PrepItem& it, float& a, float& b) {
+    const int64_t idx = (it.t0 + tid) * H + it.h;
+    if (conv) {
+      const float x = __ldg(cv.a_raw + idx) + __ldg(cv.dt_bias + it.h);
+      const float sp = x > 20.f ? x : log1pf(expf(x));
+      a = expf(-expf(__ldg(cv.A_log + it.h)) * sp);
+      b = 1.f / (1.f + expf(-__ldg(cv.b_raw + idx)));
+    } else {
+      a = alpha[idx];
+      b = beta[idx];
+    }
+  };
+  // (conv) the width-4 causal convolution + SiLU (and the L2 norm for q, k)
+  // of one 64 x 256 tile in place: warp w takes rows 8w .. 8w+7, lane l its
+  // 8 channels.  The taps and the inputs before the chunk (the sequence's
+  // earlier tokens, its carried state or zeros) load before the wait for the
+  // tile's copy; then every warp reads its eight rows and the three before
+  // them, all warps meet, and each row's arithmetic (the separate pass's,
+  // value for value) runs independently of the others.  Keys (rows < L) also
+  // go to k_out; the item holding a sequence's last token writes the
+  // sequence's last three inputs to state_out.
+  auto conv_tile = [&](const PrepItem& it, uint8_t* base, uint32_t blk_stride, int64_t ch0,
+                       bool l2, bool keys, uint64_t* bar, uint32_t parity) {
+    const int64_t C = (int64_t)3 * H * kDK;
+    const int r0 = 8 * warp;
+    const int64_t ch = ch0 + 8 * lane;
+    uint8_t* blk = base + (lane >> 3) * blk_stride;
+    const uint32_t cb = lane & 7;
+    auto cell = [&](int r) { return reinterpret_cast<uint4*>(blk + r * 128 + ((cb ^ (r & 7)) << 4)); };
+    // element k of 8 packed bf16 values
+    auto elt = [](const uint4& u, int k) {
+      const uint32_t v = k < 2 ? u.x : k < 4 ? u.y : k < 6 ? u.z : u.w;
+      return (k & 1) ? bf16_hi(v) : bf16_lo(v);
+    };
+    float w[4][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 t = __ldg(reinterpret_cast<const float4*>(cv.conv_w + (ch + i) * 4));
+      w[0][i] = t.x; w[1][i] = t.y; w[2][i] = t.z; w[3][i] = t.w;
+    }
+    const int64_t sb = map.seq_begin(it.n), se = map.seq_end(it.n);
+    int64_t nseq = it.n;
+    bool seq_first = true, seq_last = true;
+    if (cv.seg_seq) {   // it.n is a segment slot
+      nseq = cv.seg_seq[it.n];
+      seq_first = (cv.seg_role[it.n] & kSegFirst) != 0;
+      seq_last = (cv.seg_role[it.n] & kSegLast) != 0;
+    }
+    // the three inputs before row r0 (packed bf16): the chunk's earlier
+    // tokens (warp 0: from global memory, loaded before the copy lands) or
+    // the tile's rows, read before any warp replaces them
+    uint4 hist[3];
+    if (r0 == 0) {
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int64_t t = it.t0 - 3 + j;
+        if (t >= sb || !seq_first)
+          hist[j] = __ldg(reinterpret_cast<const uint4*>(cv.qkv + t * C + ch));
+        else if (cv.state_in)
+          hist[j] = __ldg(reinterpret_cast<const uint4*>(cv.state_in + (nseq * 3 + (t - sb + 3)) * C + ch));
+        else
+          hist[j] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    if (!mbar_wait(bar, parity)) s_abort = 1;
+    if (r0 > 0) {
+#pragma unroll
+      for (int j = 0; j < 3; ++j) hist[j] = *cell(r0 - 3 + j);
+    }
+    __syncthreads();   // every window is in registers before rows are replaced
+    const bool last_chunk = it.t0 + it.L == se && seq_last;
+    // two rows at a time (this warp's own rows, read before it replaces
+    // them): their arithmetic and their reductions interleave
+#pragma unroll 1
+    for (int i = 0; i < 8; i += 2) {
+      const uint4 in[5] = {hist[0], hist[1], hist[2], *cell(r0 + i), *cell(r0 + i + 1)};
+      float y[2][8], ss[2] = {0.f, 0.f};
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          float acc = w[0][k] * elt(in[u], k);
+          acc = fmaf(w[1][k], elt(in[u + 1], k), acc);
+          acc = fmaf(w[2][k], elt(in[u + 2], k), acc);
+          acc = fmaf(w[3][k], elt(in[u + 3], k), acc);
+          y[u][k] = __fdividef(acc, 1.f + __expf(-acc));
+          ss[u] = fmaf(y[u][k], y[u][k], ss[u]);
+        }
+      }
+      if (l2) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          ss[0] += __shfl_xor_sync(0xffffffffu, ss[0], o);
+          ss[1] += __shfl_xor_sync(0xffffffffu, ss[1], o);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float rr = rsqrtf(ss[u] + 1e-6f);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) y[u][k] *= rr;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        uint4 pk;
+        pk.x = pack_bf16(y[u][0], y[u][1]);
+        pk.y = pack_bf16(y[u][2], y[u][3]);
+        pk.z = pack_bf16(y[u][4], y[u][5]);
+        pk.w = pack_bf16(y[u][6], y[u][7]);
+        const int r = r0 + i + u;
+        *cell(r) = pk;
+        if (keys && r < it.L)
+          *reinterpret_cast<uint4*>(cv.k_out + ((it.t0 + r) * H + it.h) * kDK + 8 * lane) = pk;
+        if (cv.state_out && last_chunk && r == it.L - 1) {
+#pragma unroll
+          for (int j = 0; j < 3; ++j)
+            *reinterpret_cast<uint4*>(cv.state_out + (nseq * 3 + j) * C + ch) = in[u + 1 + j];
+        }
+      }
+      hist[0] = in[2];
+      hist[1] = in[3];
+      hist[2] = in[4];
+    }  };
 
   PrepItem cur, nxt, prev;
   bool have_prev = false;
@@ -280,10 +418,7 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
       issue_kq(cur, 0);
       issue_v(cur, 0, sm + Lay::V, 8192);
     }
-    if (tid < kC && tid < cur.L) {
-      a_cur = alpha[(cur.t0 + tid) * H + cur.h];
-      b_cur = beta[(cur.t0 + tid) * H + cur.h];
-    }
+    if (tid < kC && tid < cur.L) gates_of(cur, a_cur, b_cur);
   }
 
   while (j < n_items) {
@@ -302,13 +437,9 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
         bulk_wait_read_all();
         issue_kq(cur, 0);
       }
-      if (tid < kC && tid < L) {
-        a_cur = alpha[(cur.t0 + tid) * H + cur.h];
-        b_cur = beta[(cur.t0 + tid) * H + cur.h];
-      }
+      if (tid < kC && tid < L) gates_of(cur, a_cur, b_cur);
     } else if (jn < n_items && tid < kC && tid < nxt.L) {   // gates of the next item
-      a_nx = alpha[(nxt.t0 + tid) * H + nxt.h];
-      b_nx = beta[(nxt.t0 + tid) * H + nxt.h];
+      gates_of(nxt, a_nx, b_nx);
     }
     // decay prefix G_r = sum_{s <= r} log alpha_s (pad rows: log alpha = 0, beta = 0)
     float g_scan = 0.f;
@@ -330,6 +461,13 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
     __syncthreads();
     stamp(1);
 
+    if (conv) {   // k, q: convolution + SiLU + L2 in place, once the tiles are in
+      conv_tile(cur, kq, 16384, (int64_t)(H + cur.h) * kDK, true, true, &bar_kq[buf], kq_ph[buf]);
+      conv_tile(cur, kq + 8192, 16384, (int64_t)cur.h * kDK, true, false, &bar_kq[buf],
+                kq_ph[buf]);
+      fence_proxy_async_smem();
+      __syncthreads();
+    }
     // ---- [K; Q] K^T  ->  TMEM columns [0, 64): lanes 0-63 K K^T, 64-127 Q K^T
     if (tid == 0) {
       if (!mbar_wait(&bar_kq[buf], kq_ph[buf])) {
@@ -574,6 +712,12 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
         bulk_wait_read_all();
         issue_v(cur, vh, kFused ? sm + Lay::V : kq + 8192, kFused ? 8192 : 16384);
       }
+      if (conv) {   // v: convolution + SiLU in place
+        conv_tile(cur, kFused ? sm + Lay::V : kq + 8192, kFused ? 8192 : 16384,
+                  (int64_t)(2 * H + cur.h) * kDK + kDK * vh, false, false, &bar_v, vph);
+        fence_proxy_async_smem();
+        __syncthreads();
+      }
       if (tid == 0) {
         if (!mbar_wait(&bar_v, vph)) {
           s_abort = 1;
@@ -721,6 +865,7 @@ __device__ __forceinline__ uint32_t col_dU(int s) { return col_U(s) + 16u; }
 // kFused: the images of each chunk are acquired through its ready flag.
 template <bool kFused>
 __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
+                                           const CUtensorMap* tm_g,
                                            const float* __restrict__ S0,
                                            __nv_bfloat16* __restrict__ out,
                                            float* __restrict__ S_final, const SeqMap& map,
@@ -728,7 +873,8 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
                                            const uint32_t* ready, unsigned* status,
                                            uint64_t* __restrict__ trace, int32_t trace_chunks,
                                            int32_t dv, int n, int h, int slice,
-                                           float* __restrict__ sdump, bool a_chain = false) {
+                                           float* __restrict__ sdump, const NormGate& ng,
+                                           bool a_chain = false) {
   const int unit = (n * H + h) * (dv / 128) + slice;
   const bool timed = trace && threadIdx.x == 0 && unit < kMaxTracedUnits;
   if (timed) trace[kUnitTimes + 3 * unit] = globaltimer_ns();
@@ -740,6 +886,11 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   __shared__ long long s_ready_hi;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
+  // (read-out with the gated RMSNorm) the peer unit's partial sums of
+  // squares of the output rows, double-buffered by chunk parity
+  __shared__ float s_ss[2][kC], s_mine[2][kC];
+  __shared__ uint64_t bar_ss[2], bar_g;
+  const bool norm = ng.gate != nullptr;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, colhalf = warp >> 2;
@@ -765,6 +916,12 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     mbar_init(&bar_m1b, 1);
     mbar_init(&bar_m2, 1);
     mbar_init(&bar_mo, 1);
+    if (norm) {
+      mbar_init(&bar_ss[0], 1);
+      mbar_init(&bar_ss[1], 1);
+      mbar_init(&bar_g, 1);
+      prefetch_tensormap(tm_g);
+    }
     fence_barrier_init();
     s_abort = 0;
     s_ready_hi = cb;
@@ -793,6 +950,8 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // (norm) the peer's barriers are initialised before anything lands in them
+  if (norm) cluster_sync_all();
   const uint32_t tmem = tmem_base;
   // bf16 copy of S into TMEM: one packed column holds two state columns
   auto store_S_operand = [&]() {
@@ -855,7 +1014,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   constexpr int kLoaderA = 32;   // K, one chunk ahead; polls the ready flags
   constexpr int kLoaderB = 64;   // W / Q^, two chunks ahead, and the L2 warm-up
   constexpr int kLoaderC = 96;   // P^, U~^T and the decay block, one chunk ahead
-  uint32_t n_wq[2] = {0, 0}, n_kp[2] = {0, 0}, n_p[2] = {0, 0}, n_u = 0;
+  uint32_t n_wq[2] = {0, 0}, n_kp[2] = {0, 0}, n_p[2] = {0, 0}, n_u = 0, n_g = 0;
   int64_t wq_next = cb;          // (kLoaderB) first chunk whose W / Q^ is not issued yet
   // Ready flags (fused form).  A poll reads the flags of eight chunks from
   // `from` with relaxed loads (one round trip) and, when the first few are
@@ -945,6 +1104,95 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   __syncthreads();
   int prev_L = 0;
   int64_t prev_t0 = 0;
+  // (norm) Eq. 20 on the previous chunk's rows, by all eight warps in the two
+  // windows where they wait for the tensor cores: each row of a head's output
+  // is split over the two units of the cluster.  While MMA-1 runs, the 16
+  // threads holding a row's 16-byte pieces sum the squares of their bf16
+  // values (the values a separate pass would read) and one of them keeps the
+  // row's partial sum and sends it to the peer (st.async completing 4 bytes
+  // on the peer's barrier); while MMA-2 runs, once the peer's partials are
+  // in, y = o rsqrt(mean + eps) w act(gate).  The chunk's gate tile (its
+  // rows x this unit's 128 columns) was copied in by TMA beside the staged
+  // rows once MMA-2 had finished reading the K tile there.
+  uint32_t n_copy = 0;
+  const uint32_t peer = norm ? cluster_ctarank() ^ 1u : 0u;
+  const uint32_t peer_ss = norm ? cluster_map_shared(&s_ss[0][0], peer) : 0u;
+  const uint32_t peer_bar = norm ? cluster_map_shared(&bar_ss[0], peer) : 0u;
+  float nw[8];   // the norm weights of this thread's 8 columns
+  if (norm) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) nw[i] = __ldg(ng.w + 128 * slice + 8 * (tid & 15) + i);
+  }
+  // phase A (MMA-1 of the next chunk runs): the partial sums, to this unit's
+  // shared memory and the peer's
+  auto norm_partials = [&](const uint8_t* stage) {
+    const int k = (int)(n_copy & 1u);
+    if (tid == 0) mbar_arrive_expect_tx(&bar_ss[k], (uint32_t)(4 * prev_L));
+    const unsigned half = 0xffffu << (lane & 16);
+    const int c16 = tid & 15;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = (tid >> 4) + 16 * i;
+      if (r < prev_L) {
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 256 + c16 * 16);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        float ssum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = bf16_lo(w4[e]), b = bf16_hi(w4[e]);
+          ssum = fmaf(a, a, ssum);
+          ssum = fmaf(b, b, ssum);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) ssum += __shfl_xor_sync(half, ssum, o);
+        if (c16 == 0) {
+          s_mine[k][r] = ssum;
+          st_async_peer_f32(peer_ss + (uint32_t)((k * kC + r) * 4), ssum,
+                            peer_bar + (uint32_t)(k * 8));
+        }
+      }
+    }
+  };
+  // phase B (MMA-2 runs): once the peer's partials are in, y = o rsqrt(mean
+  // + eps) w act(gate) to out.  The caller then meets all threads before the
+  // staging buffer is reloaded.
+  auto norm_finish = [&](const uint8_t* stage) {
+    const int k = (int)(n_copy & 1u);
+    const uint32_t kph = (n_copy >> 1) & 1u;
+    const uint32_t gph = n_copy & 1u;
+    ++n_copy;
+    const int c16 = tid & 15;
+    if (!mbar_wait_cluster(&bar_ss[k], kph) || !mbar_wait(&bar_g, gph)) {
+      flag_status(status, GDN_ERR_TIMEOUT);
+      s_abort = 1;
+      return;
+    }
+    const float inv_dv = 1.f / (float)dv;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = (tid >> 4) + 16 * i;
+      if (r < prev_L) {
+        const float rs = rsqrtf((s_mine[k][r] + s_ss[k][r]) * inv_dv + ng.eps);
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 256 + c16 * 16);
+        const uint4 gq = *reinterpret_cast<const uint4*>(stage + 16384 + r * 256 + c16 * 16);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w}, g4[4] = {gq.x, gq.y, gq.z, gq.w};
+        uint32_t yo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float g0 = bf16_lo(g4[e]), g1 = bf16_hi(g4[e]);
+          // sigmoid(x) = (1 + tanh(x / 2)) / 2: one special-function op
+          const float s0 = fmaf(0.5f, tanh_fast(0.5f * g0), 0.5f);
+          const float s1 = fmaf(0.5f, tanh_fast(0.5f * g1), 0.5f);
+          const float a0 = ng.act == GDN_GATE_SIGMOID ? s0 : g0 * s0;
+          const float a1 = ng.act == GDN_GATE_SIGMOID ? s1 : g1 * s1;
+          yo[e] = pack_bf16(bf16_lo(w4[e]) * rs * nw[2 * e] * a0,
+                            bf16_hi(w4[e]) * rs * nw[2 * e + 1] * a1);
+        }
+        *reinterpret_cast<uint4*>(out + ((prev_t0 + r) * H + h) * dv + 128 * slice + 8 * c16) =
+            make_uint4(yo[0], yo[1], yo[2], yo[3]);
+      }
+    }
+  };
   // rows of out for the previous chunk, staged in its (consumed) K / P^ buffer
   // as [r][128] bf16 (256 B per row, this unit's half of the row of out);
   // consecutive threads of warps 4-7 move consecutive 16-byte pieces, so each
@@ -954,12 +1202,16 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   auto copy_out_prev = [&](int prev_buf) {
     if (!out) return;   // a unit whose outputs nobody reads
     const uint8_t* stage = sm + kS_KP + prev_buf * 40960;
-    for (int p = tid - 128; p < 16 * prev_L; p += kStateThreads - 128) {
-      if (p < 0) break;
-      const int r = p >> 4, c16 = p & 15;
-      const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 256 + c16 * 16);
-      *reinterpret_cast<uint4*>(out + ((prev_t0 + r) * H + h) * dv + 128 * slice + 8 * c16) = v;
+    if (!norm) {
+      for (int p = tid - 128; p < 16 * prev_L; p += kStateThreads - 128) {
+        if (p < 0) break;
+        const int r = p >> 4, c16 = p & 15;
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 256 + c16 * 16);
+        *reinterpret_cast<uint4*>(out + ((prev_t0 + r) * H + h) * dv + 128 * slice + 8 * c16) = v;
+      }
+      return;
     }
+    norm_partials(stage);   // norm_finish follows while MMA-2 runs
   };
 
   for (int64_t ci = cb; ci < ce && !s_abort; ++ci) {
@@ -1076,6 +1328,13 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
         }
       }
     }
+    // (norm) the previous chunk's read-out, while MMA-2 runs; all threads meet
+    // before its staging buffer is reloaded
+    if (norm && out && it > 0) {
+      norm_finish(sm + kS_KP + (buf ^ 1) * 40960);
+      fence_proxy_async_smem();
+      __syncthreads();
+    }
     // ... meanwhile the loaders fetch ahead: K / P^ and U~^T of the next
     // chunk (the previous chunk's staging was copied out above and E1 is done
     // with the U~^T buffer), W / Q^ of the next chunk if not yet in flight
@@ -1105,6 +1364,12 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
       s_abort = 1;
     } else {
       stamp(it, 5);
+      // (norm) this chunk's gate tile into the consumed half of the K tile
+      if (norm && out && tid == kLoaderA) {
+        mbar_arrive_expect_tx(&bar_g, 16384);
+        tma_load_3d(sm + kS_KP + buf * 40960 + 16384, tm_g, 128 * slice, h, (int32_t)t0, &bar_g);
+        ++n_g;
+      }
       tc_fence_after();
       // MMA-1 has finished reading the bf16 state operand (it precedes
       // MMA-2), so each folded group can replace its columns right away.
@@ -1164,7 +1429,10 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     prev_t0 = t0;
   }
   // the last chunk's output rows
-  if (!s_abort && ce > cb) copy_out_prev((int)((ce - cb - 1) & 1));
+  if (!s_abort && ce > cb) {
+    copy_out_prev((int)((ce - cb - 1) & 1));
+    if (norm && out && !s_abort) norm_finish(sm + kS_KP + ((ce - cb - 1) & 1) * 40960);
+  }
 
   if (!s_abort && S_final) {
     float4* p = reinterpret_cast<float4*>(S_final + srow);
@@ -1180,10 +1448,13 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
       if (n_p[b]) mbar_wait(&bar_p[b], (n_p[b] - 1) & 1, lim);
     }
     if (n_u) mbar_wait(&bar_u, (n_u - 1) & 1, lim);
+    if (n_g) mbar_wait(&bar_g, (n_g - 1) & 1, lim);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
+  // (norm) no unit leaves while its peer may still write into its shared memory
+  if (norm) cluster_sync_all();
   if (timed) trace[kUnitTimes + 3 * unit + 2] = globaltimer_ns();
 }
 
@@ -1195,30 +1466,31 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ alpha,
                const float* __restrict__ beta, SeqMap map, int32_t H,
                uint8_t* __restrict__ scratch, unsigned* status, uint64_t* __restrict__ trace,
-               int64_t n_items, int32_t dv) {
+               int64_t n_items, int32_t dv, ConvIn cv) {
   extern __shared__ uint8_t smem_raw[];
   prep_role<false>(align_smem_1024(smem_raw), &tm_q, &tm_k, &tm_v, alpha, beta, map, H, scratch,
-                   nullptr, status, dv, trace ? trace + kPrepTraceOffset : nullptr, trace, n_items,
-                   blockIdx.x, gridDim.x);
+                   nullptr, status, dv, cv, trace ? trace + kPrepTraceOffset : nullptr, trace,
+                   n_items, blockIdx.x, gridDim.x);
 }
 
 // split form, kernel 2: one CTA per unit (blockIdx = sequence, head, 128-row
 // slice of S)
 __global__ void __launch_bounds__(kStateThreads, 1)
-tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restrict__ S0,
+tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_g,
+                const float* __restrict__ S0,
                 __nv_bfloat16* __restrict__ out, float* __restrict__ S_final, SeqMap map,
                 int32_t H, const uint8_t* __restrict__ scratch, unsigned* status,
                 uint64_t* __restrict__ trace, int32_t trace_chunks, int32_t dv,
-                float* __restrict__ sdump, SegRoute route) {
+                float* __restrict__ sdump, SegRoute route, NormGate ng) {
   extern __shared__ uint8_t smem_raw[];
   const int x = blockIdx.x;
   const UnitRoute u = route_unit(route, S0, S_final, x, map.N, (int64_t)H * dv * kDK);
   // the whole CTA, before any barrier or TMEM allocation; an A chain has
   // dk rows
   if (!u.run || (u.ident && 128 * (int)blockIdx.z >= kDK)) return;
-  state_role<false>(align_smem_1024(smem_raw), &tm_k, u.S0, u.write_out ? out : nullptr,
+  state_role<false>(align_smem_1024(smem_raw), &tm_k, &tm_g, u.S0, u.write_out ? out : nullptr,
                     u.S_final, map, H, scratch, nullptr, status, trace, trace_chunks, dv,
-                    x >= map.N ? x - map.N : x, blockIdx.y, blockIdx.z, sdump, u.ident);
+                    x >= map.N ? x - map.N : x, blockIdx.y, blockIdx.z, sdump, ng, u.ident);
 }
 
 // fused form: cooperative, one CTA per SM; CTAs [0, n_state) are the state
@@ -1233,7 +1505,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const float* __restrict__ S0, __nv_bfloat16* __restrict__ out,
                 float* __restrict__ S_final, SeqMap map, int32_t H, uint8_t* __restrict__ scratch,
                 uint32_t* ready, unsigned* status, uint64_t* __restrict__ trace,
-                int32_t trace_chunks, int32_t n_state, int32_t dv, float* __restrict__ sdump) {
+                int32_t trace_chunks, int32_t n_state, int32_t dv, float* __restrict__ sdump,
+                ConvIn cv) {
   static_assert(kPrepThreads == kStateThreads, "one block shape for both roles");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align_smem_1024(smem_raw);
@@ -1241,9 +1514,10 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int u = blockIdx.x;
     const int ns = dv / 128, n = u / (ns * H);
     const int64_t per_seq = (int64_t)H * dv * kDK;
-    state_role<true>(sm, &tm_kb, S0 ? S0 + n * per_seq : nullptr, out,
+    const NormGate none{};
+    state_role<true>(sm, &tm_kb, &tm_kb, S0 ? S0 + n * per_seq : nullptr, out,
                      S_final ? S_final + n * per_seq : nullptr, map, H, scratch, ready, status,
-                     trace, trace_chunks, dv, n, (u / ns) % H, u % ns, sdump);
+                     trace, trace_chunks, dv, n, (u / ns) % H, u % ns, sdump, none);
   } else {
     int64_t positions = map.chunks_per_seq;
     if (map.cu_seqlens) {
@@ -1253,7 +1527,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         positions = c > positions ? c : positions;
       }
     }
-    prep_role<true>(sm, &tm_q, &tm_k, &tm_v, alpha, beta, map, H, scratch, ready, status, dv,
+    prep_role<true>(sm, &tm_q, &tm_k, &tm_v, alpha, beta, map, H, scratch, ready, status, dv, cv,
                     trace ? trace + kPrepTraceOffset : nullptr, trace, positions * map.N * H,
                     blockIdx.x - n_state, gridDim.x - n_state);
   }
@@ -1315,6 +1589,21 @@ bool make_token_map_blocked(CUtensorMap* m, const void* base, int64_t T_total, i
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The read-out gate [T, H, 256] (bf16) as boxes of 64 tokens x 128 columns of
+// one head, unswizzled: a state unit's share of a chunk's gate rows.
+bool make_gate_map(CUtensorMap* m, const void* base, int64_t T_total, int32_t H) {
+  EncodeFn enc = encoder();
+  if (!enc) return false;
+  memset(m, 0, sizeof *m);
+  cuuint64_t dims[3] = {(cuuint64_t)kDV, (cuuint64_t)H, (cuuint64_t)(T_total > 0 ? T_total : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)kDV * 2, (cuuint64_t)H * kDV * 2};
+  cuuint32_t box[3] = {128, 1, 64};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Per-device launch facts, looked up once: SM count, and whether the fused
 // form can be launched (cooperative launches supported and one fused CTA
 // fits on an SM).
@@ -1372,9 +1661,19 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
   if (!supported_dv(dv)) return cudaErrorInvalidValue;
   const int64_t T_total = a.map.cu_seqlens ? a.map.T : (int64_t)a.map.N * a.map.T;
   CUtensorMap tq, tk, tv, tkb;
-  if (!make_token_map(&tq, a.q, T_total, a.H) || !make_token_map(&tk, a.k, T_total, a.H) ||
-      !make_token_map(&tv, a.v, T_total, a.H, dv) || !make_token_map_blocked(&tkb, a.k, T_total, a.H))
+  if (a.cv.qkv) {
+    // the packed projection as 3H heads of 256 channels a token (q | k | v),
+    // and the state pass's keys from the prep's processed copy
+    if (dv != kDK || !make_token_map(&tq, a.cv.qkv, T_total, 3 * a.H) ||
+        !make_token_map_blocked(&tkb, a.cv.k_out, T_total, a.H))
+      return cudaErrorInvalidValue;
+    tk = tq;
+    tv = tq;
+  } else if (!make_token_map(&tq, a.q, T_total, a.H) || !make_token_map(&tk, a.k, T_total, a.H) ||
+             !make_token_map(&tv, a.v, T_total, a.H, dv) ||
+             !make_token_map_blocked(&tkb, a.k, T_total, a.H)) {
     return cudaErrorInvalidValue;
+  }
   DeviceFacts* f = device_facts();
   if (!f) return cudaErrorUnknown;
   cudaError_t e;
@@ -1383,7 +1682,8 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
   uint32_t* ready = (uint32_t*)(scr + (size_t)items * img_stride(dv));
   const int64_t n_state = (int64_t)a.map.N * a.H * (dv / 128);
 
-  if (!prep_only && !a.state_only && a.allow_overlap && a.route.pass == 0 && f->fused_ok && items > 0 &&
+  if (!prep_only && !a.state_only && a.allow_overlap && a.route.pass == 0 && !a.ng.gate &&
+      f->fused_ok && items > 0 &&
       n_state + kMinPrepWorkers <= f->sms) {
     if ((e = cudaMemsetAsync(ready, 0, (size_t)items * sizeof(uint32_t), stream)) != cudaSuccess)
       return e;
@@ -1399,7 +1699,7 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, tc_fused_kernel, tq, tk, tv, tkb, a.alpha, a.beta, a.S0,
                            (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr, ready, a.status,
-                           g_trace, g_trace_chunks, (int32_t)n_state, dv, a.state_dump);
+                           g_trace, g_trace_chunks, (int32_t)n_state, dv, a.state_dump, a.cv);
     if (e == cudaSuccess) {
       count_launches(1);
       g_last_tc_form = 1;
@@ -1415,16 +1715,40 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
     const int64_t slots = 2 * (int64_t)f->sms;
     const unsigned grid = (unsigned)(items < slots ? items : slots);
     tc_prep_kernel<<<grid, kPrepThreads, kPrepSmemSplit, stream>>>(
-        tq, tk, tv, a.alpha, a.beta, a.map, a.H, scr, a.status, g_trace, items, dv);
+        tq, tk, tv, a.alpha, a.beta, a.map, a.H, scr, a.status, g_trace, items, dv, a.cv);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (prep_only) return cudaSuccess;
   g_last_tc_form = 0;
   const unsigned gx = (unsigned)a.map.N * (a.route.pass == 1 ? 2u : 1u);
-  tc_state_kernel<<<dim3(gx, (unsigned)a.H, (unsigned)(dv / 128)), kStateThreads, kStateSmem,
-                    stream>>>(tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr,
-                              a.status, g_trace, g_trace_chunks, dv, a.state_dump, a.route);
+  const dim3 grid(gx, (unsigned)a.H, (unsigned)(dv / 128));
+  if (a.ng.gate) {
+    // the read-out norm: the two units of a head (grid z) form a cluster
+    if (dv != 256) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kStateThreads);
+    cfg.dynamicSmemBytes = kStateSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 2;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    CUtensorMap tg;
+    if (!make_gate_map(&tg, a.ng.gate, T_total, a.H)) return cudaErrorInvalidValue;
+    e = cudaLaunchKernelEx(&cfg, tc_state_kernel, tkb, tg, a.S0, (__nv_bfloat16*)a.out, a.S_final,
+                           a.map, a.H, (const uint8_t*)scr, a.status, g_trace, g_trace_chunks, dv,
+                           a.state_dump, a.route, a.ng);
+    count_launches(1);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+  tc_state_kernel<<<grid, kStateThreads, kStateSmem, stream>>>(
+      tkb, tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr, a.status, g_trace,
+      g_trace_chunks, dv, a.state_dump, a.route, a.ng);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -413,6 +413,39 @@ int gdn_decode_layer_step(const void* qkv, const float* conv_w, const float* a_r
                           int32_t dk, int32_t dv, int32_t io_dtype, gdn_stream_t stream);
 
 /*
+ * gdn_prefill_layer -- the mixer core of a layer over whole sequences in one
+ * pass over the projections: gdn_prepare, gdn_prefill and
+ * gdn_output_norm_gate fused into the tensor-core prefill's kernels.  The
+ * per-chunk prep reads the q, k, v tiles of each (chunk, head) straight from
+ * qkv and applies the convolution + SiLU (and the q / k L2 norm) in shared
+ * memory before its first MMA, computing alpha and beta from a_raw / b_raw;
+ * the state pass applies Eq. 20's gated RMSNorm to each output row before
+ * it leaves (the two 128-row units of a head run as a 2-CTA cluster and add
+ * their halves of the row's sum of squares through distributed shared
+ * memory).  Neither q, k, v, alpha, beta nor o is written to HBM.
+ *
+ *   qkv, conv_w, a_raw, b_raw, A_log, dt_bias,
+ *   conv_state_in, conv_state_out      as in gdn_prepare
+ *   S0, S_final, cu_seqlens, batch, seqlen   as in gdn_prefill (long
+ *                                      sequences are cut by the same rule)
+ *   gate, norm_w, eps, act             as in gdn_output_norm_gate
+ *   y        [.., H, dv] io dtype: the read-out y of every token and head
+ * Results agree with the three separate calls (gdn_prepare -> gdn_prefill ->
+ * gdn_output_norm_gate) to within bf16 rounding: q, k, v, alpha and beta are
+ * the same values the separate pass writes, and o enters the norm as the
+ * bf16 values gdn_prefill would store.  bf16 I/O and dk = dv = 256 only
+ * (GDN_ERR_UNSUPPORTED otherwise).  Scratch from the library's pool:
+ * gdn_prefill's plus T_total * H * dk * 2 bytes of processed keys.  Errors as
+ * for the three calls; no output may overlap an input or another output.
+ */
+int gdn_prefill_layer(const void* qkv, const float* conv_w, const float* a_raw, const float* b_raw,
+                      const float* A_log, const float* dt_bias, const void* conv_state_in,
+                      void* conv_state_out, const float* S0, const int32_t* cu_seqlens,
+                      const void* gate, const float* norm_w, float eps, int32_t act, void* y,
+                      float* S_final, int32_t batch, int64_t seqlen, int32_t heads, int32_t dk,
+                      int32_t dv, int32_t io_dtype, gdn_stream_t stream);
+
+/*
  * gdn_get_device_status -- synchronises `stream`, then returns and clears the
  * device status word of the current device (GDN_OK when no kernel flagged a
  * problem since the last call; GDN_ERR_CUDA if the synchronisation failed).

@@ -222,6 +222,22 @@ def test_prefill_scan_rejects_bad_host_arguments(lib):
     assert f(out=A16) == 1                                              # out over q
 
 
+@fake_addresses
+def test_prefill_layer_rejects_bad_host_arguments(lib):
+    def f(qkv=A16, y=A16b, io=1, dv=256, act=0, eps=1e-5, batch=1, T=128, S0=None):
+        return lib.gdn_prefill_layer(qkv, P(0x30000), P(0x40000), P(0x50000), P(0x60000),
+                                     P(0x60100), None, None, S0, None, P(0x70000), P(0x80000),
+                                     eps, act, y, None, batch, T, 2, 256, dv, io, None)
+    assert f(io=0) == 2                      # fp32: the fused layer is bf16 only
+    assert f(dv=512) == 2
+    assert f(act=2) == 1
+    assert f(eps=-1.0) == 1
+    assert f(batch=0) == 1
+    assert f(qkv=MIS) == 3
+    assert f(S0=MIS) == 3
+    assert f(y=P(0x10000 + 4096)) == 1       # y over qkv
+
+
 SIZE_MAX = ctypes.c_size_t(-1).value
 
 
