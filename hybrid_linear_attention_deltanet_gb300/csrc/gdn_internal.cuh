@@ -178,14 +178,16 @@ __device__ __forceinline__ UnitRoute route_unit(const SegRoute& r, const float* 
 
 // Eq. 20's read-out applied by the tensor-core state pass to its outputs (the
 // layer entry point): y = o / sqrt(mean(o^2) + eps) * w * act(gate) over the
-// dv values of each (token, head), written in place of o.  The two 128-row
-// units of a head run as a 2-CTA cluster and exchange each token's partial
-// sum of squares through distributed shared memory (dv = 256 only).
+// dv values of each (token, head), written over o.  Each 128-row unit of a
+// head stores the per-row sums of squares of its half of o as it copies the
+// rows out; the two units of a head run as a 2-CTA cluster, meet after their
+// chains and then apply Eq. 20 to their halves (dv = 256 only).
 struct NormGate {
   const __nv_bfloat16* gate = nullptr;   // [T_total, H, dv]; nullptr: plain outputs
   const float* w = nullptr;              // [dv]
   float eps = 0.f;
   int32_t act = 0;                       // GDN_GATE_SILU or GDN_GATE_SIGMOID
+  float* part = nullptr;                 // scratch [T_total, H, 2]: the halves' sums of squares
 };
 
 // The layer entry point's pre-recurrence steps, run by the tensor-core prep

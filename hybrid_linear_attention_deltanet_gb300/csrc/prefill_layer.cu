@@ -3,10 +3,12 @@
 // Upcycling", Appendix A.3): the pre-recurrence steps (short convolution +
 // SiLU, q / k L2 normalisation, the gates; the paragraph after Table 8 and
 // the text under Eq. 16-21) run inside the per-chunk prep on its input
-// tiles, and Eq. 20's gated RMSNorm inside the state pass's output epilogue,
-// so that q, k, v, alpha, beta and o never exist in HBM: the call reads the
-// projections and writes y.  The prep also leaves the processed keys in
-// scratch, where the state pass reads its K tiles.
+// tiles, and Eq. 20's gated RMSNorm inside the state pass (the per-row sums
+// of squares as it copies its output rows out, the normalisation and the gate
+// over its rows once the chain is done), so that q, k, v, alpha and beta
+// never exist in HBM: the call reads the projections and writes y.  The prep
+// also leaves the processed keys in scratch, where the state pass reads its K
+// tiles.
 #include <algorithm>
 
 #include "gdn_internal.cuh"
@@ -95,7 +97,9 @@ extern "C" int gdn_prefill_layer(const void* qkv, const float* conv_w, const flo
   unsigned* status = status_ptr();
   if (!status) return GDN_ERR_CUDA;
   const size_t kb = k_out_bytes(T_total, heads);
-  const size_t need = kb + prefill_scratch_bytes(batch, seqlen, heads, dv, GDN_BF16, varlen, 0);
+  const size_t pb = align_up((size_t)T_total * heads * 8, 1024);   // the norm's partial sums
+  const size_t need =
+      kb + pb + prefill_scratch_bytes(batch, seqlen, heads, dv, GDN_BF16, varlen, 0);
   void* scratch = nullptr;
   if (scratch_alloc(&scratch, need, stream) != cudaSuccess) return GDN_ERR_CUDA;
 
@@ -116,6 +120,7 @@ extern "C" int gdn_prefill_layer(const void* qkv, const float* conv_w, const flo
   a.ng.w = norm_w;
   a.ng.eps = eps;
   a.ng.act = act;
+  a.ng.part = (float*)((char*)scratch + kb);
   a.cv.qkv = (const __nv_bfloat16*)qkv;
   a.cv.conv_w = conv_w;
   a.cv.state_in = (const __nv_bfloat16*)conv_state_in;
@@ -125,7 +130,7 @@ extern "C" int gdn_prefill_layer(const void* qkv, const float* conv_w, const flo
   a.cv.A_log = A_log;
   a.cv.dt_bias = dt_bias;
   a.cv.k_out = (__nv_bfloat16*)scratch;
-  cudaError_t e = launch_prefill_any(a, GDN_BF16, seqlen, 0, (char*)scratch + kb, stream);
+  cudaError_t e = launch_prefill_any(a, GDN_BF16, seqlen, 0, (char*)scratch + kb + pb, stream);
   if (e == cudaSuccess && conv_state_out && (varlen || seqlen == 0)) {
     empty_state_kernel<<<(unsigned)std::min<int64_t>(((int64_t)batch * 3 * C / 8 + 255) / 256, 4096),
                          256, 0, stream>>>(cu_seqlens, batch, C,

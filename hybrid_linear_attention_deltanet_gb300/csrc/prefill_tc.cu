@@ -92,13 +92,6 @@ __device__ __forceinline__ float exp_fast(float x) {
   return y;
 }
 
-// tanh on the special-function unit (absolute error about 2^-11)
-__device__ __forceinline__ float tanh_fast(float x) {
-  float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // byte offset of 16-byte chunk `ch` (0..7) of row `row` in a 128-byte-swizzled image
 __device__ __forceinline__ uint32_t sw_chunk(uint32_t row, uint32_t ch) {
   return row * 128u + ((ch ^ (row & 7u)) << 4);
@@ -865,7 +858,6 @@ __device__ __forceinline__ uint32_t col_dU(int s) { return col_U(s) + 16u; }
 // kFused: the images of each chunk are acquired through its ready flag.
 template <bool kFused>
 __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
-                                           const CUtensorMap* tm_g,
                                            const float* __restrict__ S0,
                                            __nv_bfloat16* __restrict__ out,
                                            float* __restrict__ S_final, const SeqMap& map,
@@ -886,11 +878,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   __shared__ long long s_ready_hi;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
-  // (read-out with the gated RMSNorm) the peer unit's partial sums of
-  // squares of the output rows, double-buffered by chunk parity
-  __shared__ float s_ss[2][kC], s_mine[2][kC];
-  __shared__ uint64_t bar_ss[2], bar_g;
-  const bool norm = ng.gate != nullptr;
+  const bool norm = ng.gate != nullptr;   // the read-out with the gated RMSNorm
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, colhalf = warp >> 2;
@@ -916,12 +904,6 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     mbar_init(&bar_m1b, 1);
     mbar_init(&bar_m2, 1);
     mbar_init(&bar_mo, 1);
-    if (norm) {
-      mbar_init(&bar_ss[0], 1);
-      mbar_init(&bar_ss[1], 1);
-      mbar_init(&bar_g, 1);
-      prefetch_tensormap(tm_g);
-    }
     fence_barrier_init();
     s_abort = 0;
     s_ready_hi = cb;
@@ -950,8 +932,6 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // (norm) the peer's barriers are initialised before anything lands in them
-  if (norm) cluster_sync_all();
   const uint32_t tmem = tmem_base;
   // bf16 copy of S into TMEM: one packed column holds two state columns
   auto store_S_operand = [&]() {
@@ -1014,7 +994,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   constexpr int kLoaderA = 32;   // K, one chunk ahead; polls the ready flags
   constexpr int kLoaderB = 64;   // W / Q^, two chunks ahead, and the L2 warm-up
   constexpr int kLoaderC = 96;   // P^, U~^T and the decay block, one chunk ahead
-  uint32_t n_wq[2] = {0, 0}, n_kp[2] = {0, 0}, n_p[2] = {0, 0}, n_u = 0, n_g = 0;
+  uint32_t n_wq[2] = {0, 0}, n_kp[2] = {0, 0}, n_p[2] = {0, 0}, n_u = 0;
   int64_t wq_next = cb;          // (kLoaderB) first chunk whose W / Q^ is not issued yet
   // Ready flags (fused form).  A poll reads the flags of eight chunks from
   // `from` with relaxed loads (one round trip) and, when the first few are
@@ -1104,37 +1084,25 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   __syncthreads();
   int prev_L = 0;
   int64_t prev_t0 = 0;
-  // (norm) Eq. 20 on the previous chunk's rows, by all eight warps in the two
-  // windows where they wait for the tensor cores: each row of a head's output
-  // is split over the two units of the cluster.  While MMA-1 runs, the 16
-  // threads holding a row's 16-byte pieces sum the squares of their bf16
-  // values (the values a separate pass would read) and one of them keeps the
-  // row's partial sum and sends it to the peer (st.async completing 4 bytes
-  // on the peer's barrier); while MMA-2 runs, once the peer's partials are
-  // in, y = o rsqrt(mean + eps) w act(gate).  The chunk's gate tile (its
-  // rows x this unit's 128 columns) was copied in by TMA beside the staged
-  // rows once MMA-2 had finished reading the K tile there.
-  uint32_t n_copy = 0;
-  const uint32_t peer = norm ? cluster_ctarank() ^ 1u : 0u;
-  const uint32_t peer_ss = norm ? cluster_map_shared(&s_ss[0][0], peer) : 0u;
-  const uint32_t peer_bar = norm ? cluster_map_shared(&bar_ss[0], peer) : 0u;
-  float nw[8];   // the norm weights of this thread's 8 columns
-  if (norm) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) nw[i] = __ldg(ng.w + 128 * slice + 8 * (tid & 15) + i);
-  }
-  // phase A (MMA-1 of the next chunk runs): the partial sums, to this unit's
-  // shared memory and the peer's
-  auto norm_partials = [&](const uint8_t* stage) {
-    const int k = (int)(n_copy & 1u);
-    if (tid == 0) mbar_arrive_expect_tx(&bar_ss[k], (uint32_t)(4 * prev_L));
-    const unsigned half = 0xffffu << (lane & 16);
-    const int c16 = tid & 15;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = (tid >> 4) + 16 * i;
-      if (r < prev_L) {
-        const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 256 + c16 * 16);
+  // rows of out for the previous chunk, staged in its (consumed) K / P^ buffer
+  // as [r][128] bf16 (256 B per row, this unit's half of the row of out);
+  // consecutive threads of warps 4-7 move consecutive 16-byte pieces, so each
+  // warp store covers two whole 256-byte row segments.  (Warp 0 is issuing
+  // MMA-1 then; warps 1-3 hold the loader threads, whose acquire fences
+  // would otherwise wait for these stores to drain.)
+  //
+  // (norm) The 16 threads of a row also sum the squares of its 128 bf16
+  // values (the values a separate pass would read) and one of them stores the
+  // row's partial sum; Eq. 20 itself runs after the chain (norm_tail).
+  auto copy_out_prev = [&](int prev_buf) {
+    if (!out) return;   // a unit whose outputs nobody reads
+    const uint8_t* stage = sm + kS_KP + prev_buf * 40960;
+    for (int p = tid - 128; p < 16 * prev_L; p += kStateThreads - 128) {
+      if (p < 0) break;
+      const int r = p >> 4, c16 = p & 15;
+      const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 256 + c16 * 16);
+      *reinterpret_cast<uint4*>(out + ((prev_t0 + r) * H + h) * dv + 128 * slice + 8 * c16) = v;
+      if (norm) {   // whole 16-lane halves of a warp share a row
         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
         float ssum = 0.f;
 #pragma unroll
@@ -1143,75 +1111,12 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
           ssum = fmaf(a, a, ssum);
           ssum = fmaf(b, b, ssum);
         }
+        const unsigned half = 0xffffu << (lane & 16);
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) ssum += __shfl_xor_sync(half, ssum, o);
-        if (c16 == 0) {
-          s_mine[k][r] = ssum;
-          st_async_peer_f32(peer_ss + (uint32_t)((k * kC + r) * 4), ssum,
-                            peer_bar + (uint32_t)(k * 8));
-        }
+        if (c16 == 0) ng.part[((prev_t0 + r) * H + h) * 2 + slice] = ssum;
       }
     }
-  };
-  // phase B (MMA-2 runs): once the peer's partials are in, y = o rsqrt(mean
-  // + eps) w act(gate) to out.  The caller then meets all threads before the
-  // staging buffer is reloaded.
-  auto norm_finish = [&](const uint8_t* stage) {
-    const int k = (int)(n_copy & 1u);
-    const uint32_t kph = (n_copy >> 1) & 1u;
-    const uint32_t gph = n_copy & 1u;
-    ++n_copy;
-    const int c16 = tid & 15;
-    if (!mbar_wait_cluster(&bar_ss[k], kph) || !mbar_wait(&bar_g, gph)) {
-      flag_status(status, GDN_ERR_TIMEOUT);
-      s_abort = 1;
-      return;
-    }
-    const float inv_dv = 1.f / (float)dv;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = (tid >> 4) + 16 * i;
-      if (r < prev_L) {
-        const float rs = rsqrtf((s_mine[k][r] + s_ss[k][r]) * inv_dv + ng.eps);
-        const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 256 + c16 * 16);
-        const uint4 gq = *reinterpret_cast<const uint4*>(stage + 16384 + r * 256 + c16 * 16);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w}, g4[4] = {gq.x, gq.y, gq.z, gq.w};
-        uint32_t yo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float g0 = bf16_lo(g4[e]), g1 = bf16_hi(g4[e]);
-          // sigmoid(x) = (1 + tanh(x / 2)) / 2: one special-function op
-          const float s0 = fmaf(0.5f, tanh_fast(0.5f * g0), 0.5f);
-          const float s1 = fmaf(0.5f, tanh_fast(0.5f * g1), 0.5f);
-          const float a0 = ng.act == GDN_GATE_SIGMOID ? s0 : g0 * s0;
-          const float a1 = ng.act == GDN_GATE_SIGMOID ? s1 : g1 * s1;
-          yo[e] = pack_bf16(bf16_lo(w4[e]) * rs * nw[2 * e] * a0,
-                            bf16_hi(w4[e]) * rs * nw[2 * e + 1] * a1);
-        }
-        *reinterpret_cast<uint4*>(out + ((prev_t0 + r) * H + h) * dv + 128 * slice + 8 * c16) =
-            make_uint4(yo[0], yo[1], yo[2], yo[3]);
-      }
-    }
-  };
-  // rows of out for the previous chunk, staged in its (consumed) K / P^ buffer
-  // as [r][128] bf16 (256 B per row, this unit's half of the row of out);
-  // consecutive threads of warps 4-7 move consecutive 16-byte pieces, so each
-  // warp store covers two whole 256-byte row segments.  (Warp 0 is issuing
-  // MMA-1 then; warps 1-3 hold the loader threads, whose acquire fences
-  // would otherwise wait for these stores to drain.)
-  auto copy_out_prev = [&](int prev_buf) {
-    if (!out) return;   // a unit whose outputs nobody reads
-    const uint8_t* stage = sm + kS_KP + prev_buf * 40960;
-    if (!norm) {
-      for (int p = tid - 128; p < 16 * prev_L; p += kStateThreads - 128) {
-        if (p < 0) break;
-        const int r = p >> 4, c16 = p & 15;
-        const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 256 + c16 * 16);
-        *reinterpret_cast<uint4*>(out + ((prev_t0 + r) * H + h) * dv + 128 * slice + 8 * c16) = v;
-      }
-      return;
-    }
-    norm_partials(stage);   // norm_finish follows while MMA-2 runs
   };
 
   for (int64_t ci = cb; ci < ce && !s_abort; ++ci) {
@@ -1328,13 +1233,6 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
         }
       }
     }
-    // (norm) the previous chunk's read-out, while MMA-2 runs; all threads meet
-    // before its staging buffer is reloaded
-    if (norm && out && it > 0) {
-      norm_finish(sm + kS_KP + (buf ^ 1) * 40960);
-      fence_proxy_async_smem();
-      __syncthreads();
-    }
     // ... meanwhile the loaders fetch ahead: K / P^ and U~^T of the next
     // chunk (the previous chunk's staging was copied out above and E1 is done
     // with the U~^T buffer), W / Q^ of the next chunk if not yet in flight
@@ -1364,12 +1262,6 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
       s_abort = 1;
     } else {
       stamp(it, 5);
-      // (norm) this chunk's gate tile into the consumed half of the K tile
-      if (norm && out && tid == kLoaderA) {
-        mbar_arrive_expect_tx(&bar_g, 16384);
-        tma_load_3d(sm + kS_KP + buf * 40960 + 16384, tm_g, 128 * slice, h, (int32_t)t0, &bar_g);
-        ++n_g;
-      }
       tc_fence_after();
       // MMA-1 has finished reading the bf16 state operand (it precedes
       // MMA-2), so each folded group can replace its columns right away.
@@ -1429,10 +1321,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     prev_t0 = t0;
   }
   // the last chunk's output rows
-  if (!s_abort && ce > cb) {
-    copy_out_prev((int)((ce - cb - 1) & 1));
-    if (norm && out && !s_abort) norm_finish(sm + kS_KP + ((ce - cb - 1) & 1) * 40960);
-  }
+  if (!s_abort && ce > cb) copy_out_prev((int)((ce - cb - 1) & 1));
 
   if (!s_abort && S_final) {
     float4* p = reinterpret_cast<float4*>(S_final + srow);
@@ -1448,13 +1337,66 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
       if (n_p[b]) mbar_wait(&bar_p[b], (n_p[b] - 1) & 1, lim);
     }
     if (n_u) mbar_wait(&bar_u, (n_u - 1) & 1, lim);
-    if (n_g) mbar_wait(&bar_g, (n_g - 1) & 1, lim);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
-  // (norm) no unit leaves while its peer may still write into its shared memory
-  if (norm) cluster_sync_all();
+  // (norm) Eq. 20 over this unit's rows, once both units of the head (the
+  // cluster) have stored their outputs and partial sums: an HBM stream of
+  // out, gate and out again, off the chain's critical path (units of other
+  // sequences are still walking their chains meanwhile).  Every thread takes
+  // 16-byte pieces of one column group (tid & 15), kTailRows rows at a time,
+  // with all loads of those rows in flight before any is used (the chain's
+  // registers are free by now).
+  constexpr int kTailRows = 8;
+  if (norm) {
+    cluster_sync_all();
+    if (out && !s_abort) {
+      const int c16 = tid & 15;
+      const int col = 128 * slice + 8 * c16;
+      float w8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w8[i] = __ldg(ng.w + col + i);
+      const float inv_dv = 1.f / (float)dv;
+      for (int64_t t = s_begin + (tid >> 4); t < s_end; t += kTailRows * (kStateThreads / 16)) {
+        uint4 ov[kTailRows], gv[kTailRows];
+        float ps[kTailRows];
+#pragma unroll
+        for (int u = 0; u < kTailRows; ++u) {
+          const int64_t tu = t + u * (kStateThreads / 16);
+          if (tu < s_end) {
+            const size_t off = ((size_t)tu * H + h) * dv + col;
+            ov[u] = *reinterpret_cast<const uint4*>(out + off);
+            gv[u] = __ldg(reinterpret_cast<const uint4*>(ng.gate + off));
+            const float2 pp = *reinterpret_cast<const float2*>(ng.part + ((size_t)tu * H + h) * 2);
+            ps[u] = pp.x + pp.y;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kTailRows; ++u) {
+          const int64_t tu = t + u * (kStateThreads / 16);
+          if (tu < s_end) {
+            const float rs = rsqrtf(ps[u] * inv_dv + ng.eps);
+            const uint32_t o4[4] = {ov[u].x, ov[u].y, ov[u].z, ov[u].w};
+            const uint32_t g4[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
+            uint32_t yo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float g0 = bf16_lo(g4[e]), g1 = bf16_hi(g4[e]);
+              const float a0 = ng.act == GDN_GATE_SIGMOID ? __fdividef(1.f, 1.f + __expf(-g0))
+                                                          : __fdividef(g0, 1.f + __expf(-g0));
+              const float a1 = ng.act == GDN_GATE_SIGMOID ? __fdividef(1.f, 1.f + __expf(-g1))
+                                                          : __fdividef(g1, 1.f + __expf(-g1));
+              yo[e] = pack_bf16(bf16_lo(o4[e]) * rs * w8[2 * e] * a0,
+                                bf16_hi(o4[e]) * rs * w8[2 * e + 1] * a1);
+            }
+            *reinterpret_cast<uint4*>(out + ((size_t)tu * H + h) * dv + col) =
+                make_uint4(yo[0], yo[1], yo[2], yo[3]);
+          }
+        }
+      }
+    }
+  }
   if (timed) trace[kUnitTimes + 3 * unit + 2] = globaltimer_ns();
 }
 
@@ -1476,8 +1418,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 // split form, kernel 2: one CTA per unit (blockIdx = sequence, head, 128-row
 // slice of S)
 __global__ void __launch_bounds__(kStateThreads, 1)
-tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_g,
-                const float* __restrict__ S0,
+tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restrict__ S0,
                 __nv_bfloat16* __restrict__ out, float* __restrict__ S_final, SeqMap map,
                 int32_t H, const uint8_t* __restrict__ scratch, unsigned* status,
                 uint64_t* __restrict__ trace, int32_t trace_chunks, int32_t dv,
@@ -1488,7 +1429,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   // the whole CTA, before any barrier or TMEM allocation; an A chain has
   // dk rows
   if (!u.run || (u.ident && 128 * (int)blockIdx.z >= kDK)) return;
-  state_role<false>(align_smem_1024(smem_raw), &tm_k, &tm_g, u.S0, u.write_out ? out : nullptr,
+  state_role<false>(align_smem_1024(smem_raw), &tm_k, u.S0, u.write_out ? out : nullptr,
                     u.S_final, map, H, scratch, nullptr, status, trace, trace_chunks, dv,
                     x >= map.N ? x - map.N : x, blockIdx.y, blockIdx.z, sdump, ng, u.ident);
 }
@@ -1515,7 +1456,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int ns = dv / 128, n = u / (ns * H);
     const int64_t per_seq = (int64_t)H * dv * kDK;
     const NormGate none{};
-    state_role<true>(sm, &tm_kb, &tm_kb, S0 ? S0 + n * per_seq : nullptr, out,
+    state_role<true>(sm, &tm_kb, S0 ? S0 + n * per_seq : nullptr, out,
                      S_final ? S_final + n * per_seq : nullptr, map, H, scratch, ready, status,
                      trace, trace_chunks, dv, n, (u / ns) % H, u % ns, sdump, none);
   } else {
@@ -1586,21 +1527,6 @@ bool make_token_map_blocked(CUtensorMap* m, const void* base, int64_t T_total, i
   cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// The read-out gate [T, H, 256] (bf16) as boxes of 64 tokens x 128 columns of
-// one head, unswizzled: a state unit's share of a chunk's gate rows.
-bool make_gate_map(CUtensorMap* m, const void* base, int64_t T_total, int32_t H) {
-  EncodeFn enc = encoder();
-  if (!enc) return false;
-  memset(m, 0, sizeof *m);
-  cuuint64_t dims[3] = {(cuuint64_t)kDV, (cuuint64_t)H, (cuuint64_t)(T_total > 0 ? T_total : 1)};
-  cuuint64_t strides[2] = {(cuuint64_t)kDV * 2, (cuuint64_t)H * kDV * 2};
-  cuuint32_t box[3] = {128, 1, 64};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1738,16 +1664,14 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
     at[0].val.clusterDim.z = 2;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    CUtensorMap tg;
-    if (!make_gate_map(&tg, a.ng.gate, T_total, a.H)) return cudaErrorInvalidValue;
-    e = cudaLaunchKernelEx(&cfg, tc_state_kernel, tkb, tg, a.S0, (__nv_bfloat16*)a.out, a.S_final,
+    e = cudaLaunchKernelEx(&cfg, tc_state_kernel, tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final,
                            a.map, a.H, (const uint8_t*)scr, a.status, g_trace, g_trace_chunks, dv,
                            a.state_dump, a.route, a.ng);
     count_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   tc_state_kernel<<<grid, kStateThreads, kStateSmem, stream>>>(
-      tkb, tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr, a.status, g_trace,
+      tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr, a.status, g_trace,
       g_trace_chunks, dv, a.state_dump, a.route, a.ng);
   count_launches(1);
   return cudaGetLastError();

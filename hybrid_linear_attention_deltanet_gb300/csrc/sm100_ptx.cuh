@@ -80,56 +80,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 }
 
 // ------------------------------------------------- thread-block clusters
-// This CTA's rank in its cluster.
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// The shared-memory address (shared::cluster window) of the same variable in
-// the CTA of rank `rank` of this cluster.
-__device__ __forceinline__ uint32_t cluster_map_shared(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-// 4 bytes into a peer CTA's shared memory; the write completes 4 bytes of the
-// transaction count of the peer's mbarrier `remote_bar` (same window).
-__device__ __forceinline__ void st_async_peer_f32(uint32_t remote_addr, float v,
-                                                  uint32_t remote_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
-                   remote_addr),
-               "r"(__float_as_uint(v)), "r"(remote_bar)
-               : "memory");
-}
-// Every thread of every CTA of the cluster (all warps, converged).
+// Every thread of every CTA of the cluster (all warps, converged); release /
+// acquire at cluster scope, so each CTA sees what the others stored before.
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
-}
-// mbar_wait for data a peer CTA delivered (acquire at cluster scope).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
-                                                  uint64_t limit_ns = 1000000000ull) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
-  }
-}
-// L2 prefetch of the line holding p.
-__device__ __forceinline__ void prefetch_line_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // ----------------------------------------------------- proxy fences
