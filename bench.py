@@ -492,7 +492,28 @@ def run_ours(args, rank, world, local_rank, dist):
     assert gdn.device_status() == 0
     prep_b = prepare_bytes(lcase.total_tokens, len(lcase.lengths))
     ng_b = norm_gate_bytes(lcase.total_tokens * lcase.H)
-    del lx, lstate, lo, ly
+    # the whole mixer core over the same inputs: gdn_prefill_layer (the
+    # pre-recurrence steps inside the prefill's prep, the gated RMSNorm inside
+    # its state pass) against the three separate calls
+    lS0 = torch.randn((len(lcase.lengths), lcase.H, lcase.dv, lcase.dk), device=dev) * 0.02
+    lsf = torch.empty_like(lS0)
+    lyf = torch.empty_like(lx["g"])
+    fstep = lambda: gdn.prefill_layer(lx["qkv"], lx["conv_w"], lx["a_raw"], lx["b_raw"],
+                                      lx["A_log"], lx["dt_bias"], lx["g"], lx["norm_w"], lcase.H,
+                                      S0=lS0, conv_state_in=lx["conv_state"],
+                                      conv_state_out=lstate, y=lyf, S_final=lsf)
+
+    def three_step():
+        p = gdn.prepare(lx["qkv"], lx["conv_w"], lx["a_raw"], lx["b_raw"], lx["A_log"],
+                        lx["dt_bias"], lcase.H, conv_state_in=lx["conv_state"],
+                        conv_state_out=lstate)
+        o, _ = gdn.prefill(p["q"], p["k"], p["v"], p["alpha"], p["beta"], lS0, S_final=lsf)
+        gdn.output_norm_gate(o, lx["g"], lx["norm_w"], 1e-5, "silu", y=lyf)
+
+    lf_ms, lf_launch = time_it(fstep, 10)
+    l3_ms, l3_launch = time_it(three_step, 10)
+    assert gdn.device_status() == 0
+    del lx, lstate, lo, ly, lS0, lsf, lyf
     dl = gdn_inputs.layer_decode_256()
     dl_steps = 200
     gen = torch.Generator(device=dev)
@@ -695,6 +716,15 @@ def run_ours(args, rank, world, local_rank, dist):
                         "the chunk-start states, reverse state pass and chunk gradients on "
                         "the CUDA cores in fp32",
             },
+            "layer_prefill": {
+                "workload": lcase.name + " (gdn_prefill_layer: projections in, y out)",
+                "ms_per_step": round(lf_ms, 4),
+                "value": round(throughput(lcase.total_tokens * world, lf_ms) / 1e6, 4),
+                "unit": "Mtok/s/layer", "launches_per_step": lf_launch,
+                "three_calls_ms_per_step": round(l3_ms, 4),
+                "three_calls_launches_per_step": l3_launch,
+                "path": "pre-recurrence steps inside the tensor-core prep, gated RMSNorm "
+                        "inside the state pass (split form, 2-CTA clusters)"},
             "layer_steps": {
                 "prepare": {"workload": lcase.name + " (gdn_prepare)",
                             "ms_per_step": round(prep_ms, 4),

@@ -14,7 +14,8 @@
 // and written once (512 KiB at dv = 256), against ~3 KiB of q, k, v, out,
 // alpha, beta.
 // Each warp streams whole 1 KiB rows with two 16-byte loads per lane (a fully
-// coalesced 512 B per instruction), keeps 8 of them in flight, and reduces
+// coalesced 512 B per instruction), keeps kBatch = 4 rows (8 such loads) in
+// flight, and reduces
 // the two dot products with warp shuffles; the state never touches shared
 // memory.  Loads and stores carry the streaming cache hint because a step's
 // state (hundreds of MB) does not fit in L2.
