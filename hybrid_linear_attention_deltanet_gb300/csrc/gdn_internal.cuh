@@ -129,6 +129,9 @@ struct SegRoute {
   const float* S0seg = nullptr;       // [slots][H][dv][dk]
   float* Bseg = nullptr;
   float* Aseg = nullptr;              // [slots][H][dv][dk], rows 0 .. dk-1 used
+  // (tensor-core path) the order in which the grid takes the units' x values
+  // (longest chain first, units that do not run last), or nullptr: x order
+  const int32_t* order = nullptr;
 };
 
 // Where one unit of the state pass starts and ends; S0 / S_final point at
@@ -261,7 +264,7 @@ extern int32_t g_last_tc_form;
 struct LongPlan {
   int64_t n_slots = 0, max_chunks = 0;
   size_t off_chunk_off = 0, off_seg_cu = 0, off_seg_seq = 0, off_seq_first = 0, off_role = 0,
-         off_work = 0, off_S0seg = 0, off_Bseg = 0, off_Aseg = 0, bytes = 0;
+         off_work = 0, off_S0seg = 0, off_Bseg = 0, off_Aseg = 0, off_order = 0, bytes = 0;
 };
 bool long_form_applies(int64_t seqlen);
 LongPlan plan_long(int32_t N, int64_t seqlen, bool varlen, int32_t H, int32_t dv, int io_dtype,

@@ -223,6 +223,31 @@ __global__ void __launch_bounds__(256) seg_scan_kernel(float* __restrict__ S0seg
   }
 }
 
+// The order in which a state pass's grid takes its units' x values: units
+// that run, longest chain (most chunks) first, then those that do not run;
+// ties in x order.  A grid larger than the SMs runs in waves, and a long
+// chain started in a later wave would set the whole pass's length.  One CTA:
+// the keys in shared memory, then each x counts the keys ahead of it.
+constexpr int kMaxOrdered = 2048;
+
+__global__ void __launch_bounds__(1024)
+unit_order_kernel(SegRoute r, const int32_t* __restrict__ chunk_off, int32_t N, int32_t gx,
+                  int32_t* __restrict__ order) {
+  __shared__ int32_t key[kMaxOrdered];
+  for (int x = threadIdx.x; x < gx; x += blockDim.x) {
+    const UnitRoute u = route_unit(r, nullptr, nullptr, x, N, 0);
+    const int s = x >= N ? x - N : x;
+    key[x] = u.run ? chunk_off[s + 1] - chunk_off[s] : -1;
+  }
+  __syncthreads();
+  for (int x = threadIdx.x; x < gx; x += blockDim.x) {
+    const int32_t kx = key[x];
+    int rank = 0;
+    for (int y = 0; y < gx; ++y) rank += (key[y] > kx || (key[y] == kx && y < x)) ? 1 : 0;
+    order[rank] = x;
+  }
+}
+
 }  // namespace
 
 bool long_form_applies(int64_t seqlen) {
@@ -249,6 +274,7 @@ LongPlan plan_long(int32_t N, int64_t seqlen, bool varlen, int32_t H, int32_t dv
   p.off_seg_seq = o;   o += slot_ints;
   p.off_seq_first = o; o += align_up(((size_t)N + 1) * 4, 256);
   p.off_role = o;      o += align_up((size_t)p.n_slots, 256);
+  p.off_order = o;     o += align_up((size_t)p.n_slots * 3 * 4, 256);
   p.off_work = o;      o += align_up(work, 256);
   p.off_S0seg = o;     o += states;
   p.off_Bseg = o;      o += states;
@@ -309,9 +335,20 @@ cudaError_t launch_prefill_long(const PrefillLaunch& base, int io_dtype, const L
     a.cv.seg_seq = seg_seq;
     a.cv.seg_role = role;
   }
+  int32_t* order = (int32_t*)(scr + p.off_order);
   auto run = [&](bool state_only, int pass) {
     a.state_only = state_only;
     a.route.pass = pass;
+    a.route.order = nullptr;
+    const int32_t gx = pass == 1 ? 2 * slots : slots;
+    if (io_dtype == GDN_BF16 && gx <= kMaxOrdered) {
+      int32_t* ord = order + (pass == 1 ? 0 : 2 * slots);
+      unit_order_kernel<<<1, 1024, 0, stream>>>(a.route, chunk_off, slots, gx, ord);
+      count_launches(1);
+      const cudaError_t eo = cudaGetLastError();
+      if (eo != cudaSuccess) return eo;
+      a.route.order = ord;
+    }
     return io_dtype == GDN_BF16 ? launch_prefill_tc(a, stream)
                                 : launch_prefill_simt(a, io_dtype, stream);
   };

@@ -1424,14 +1424,18 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
                 uint64_t* __restrict__ trace, int32_t trace_chunks, int32_t dv,
                 float* __restrict__ sdump, SegRoute route, NormGate ng) {
   extern __shared__ uint8_t smem_raw[];
-  const int x = blockIdx.x;
+  // a 1-D grid: the slice fastest (a head's units are neighbours, and the
+  // pair of a cluster), then the head, then the unit's x in the route's order
+  const int ns = dv / 128;
+  const int lin = blockIdx.x, slice = lin % ns, h = (lin / ns) % H, rank = lin / (ns * H);
+  const int x = route.order ? route.order[rank] : rank;
   const UnitRoute u = route_unit(route, S0, S_final, x, map.N, (int64_t)H * dv * kDK);
   // the whole CTA, before any barrier or TMEM allocation; an A chain has
   // dk rows
-  if (!u.run || (u.ident && 128 * (int)blockIdx.z >= kDK)) return;
+  if (!u.run || (u.ident && 128 * slice >= kDK)) return;
   state_role<false>(align_smem_1024(smem_raw), &tm_k, u.S0, u.write_out ? out : nullptr,
                     u.S_final, map, H, scratch, nullptr, status, trace, trace_chunks, dv,
-                    x >= map.N ? x - map.N : x, blockIdx.y, blockIdx.z, sdump, ng, u.ident);
+                    x >= map.N ? x - map.N : x, h, slice, sdump, ng, u.ident);
 }
 
 // fused form: cooperative, one CTA per SM; CTAs [0, n_state) are the state
@@ -1647,10 +1651,11 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
   }
   if (prep_only) return cudaSuccess;
   g_last_tc_form = 0;
-  const unsigned gx = (unsigned)a.map.N * (a.route.pass == 1 ? 2u : 1u);
-  const dim3 grid(gx, (unsigned)a.H, (unsigned)(dv / 128));
+  const int64_t n_blocks = (int64_t)a.map.N * (a.route.pass == 1 ? 2 : 1) * a.H * (dv / 128);
+  if (n_blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)n_blocks);
   if (a.ng.gate) {
-    // the read-out norm: the two units of a head (grid z) form a cluster
+    // the read-out norm: the two units of a head form a cluster
     if (dv != 256) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -1659,9 +1664,9 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
     cfg.stream = stream;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.x = 2;   // the two slices of a head: neighbours in the grid
     at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 2;
+    at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, tc_state_kernel, tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final,
