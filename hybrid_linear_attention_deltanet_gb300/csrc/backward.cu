@@ -416,6 +416,33 @@ fwd_states_kernel(const float* __restrict__ S0, SeqMap map, int32_t H, Bwd s) {
   }
 }
 
+// ------------------------------------------------------------------ dgamma_L partials
+// <dS', S_start> of each (chunk, head) over 16-row slices of the state, as
+// the CUDA-core reverse pass leaves them (used with the tensor-core one):
+// one CTA per (unit, slice).
+__global__ void __launch_bounds__(kThreads) dgl_kernel(Bwd s) {
+  __shared__ float red[kThreads / 32];
+  const int64_t u = blockIdx.x;
+  const int sl = blockIdx.y, tid = threadIdx.x;
+  const size_t off = u * s.sS() + (size_t)sl * kNS * kDK;
+  const float4* a = reinterpret_cast<const float4*>(s.dSp + off);
+  const float4* b = reinterpret_cast<const float4*>(s.Sst + off);
+  float part = 0.f;
+  for (int e = tid; e < kNS * kDK / 4; e += kThreads) {
+    const float4 x = a[e], y = b[e];
+    part = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, part))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if ((tid & 31) == 0) red[tid >> 5] = part;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    for (int w = 0; w < kThreads / 32; ++w) t += red[w];
+    s.dgLp[u * (s.dv / kNS) + sl] = t;
+  }
+}
+
 // ------------------------------------------------------------------ reverse states
 __global__ void __launch_bounds__(kThreads)
 rev_states_kernel(const float* __restrict__ dS_final, float* __restrict__ dS0, SeqMap map,
@@ -803,9 +830,33 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  rev_states_kernel<<<gs, kThreads, kRevSmem, st>>>(dS_final, dS0, a.map, a.H, s);
-  count_launches(1);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (io_dtype == GDN_BF16) {
+    // the reverse pass on the tensor cores, on the forward re-run's operand
+    // images; then the <dS', S_start> partials in parallel
+    ReverseLaunch r;
+    r.k = a.k;
+    r.dout = dout;
+    r.map = a.map;
+    r.H = a.H;
+    r.dv = dv;
+    r.T_total = a.map.cu_seqlens ? a.map.T : (int64_t)a.map.N * a.map.T;
+    r.images = (const uint8_t*)a.scratch + align_up(bwd_scratch_bytes(units, dv), 1024);
+    r.dS_final = dS_final;
+    r.dS0 = dS0;
+    r.dSp = s.dSp;
+    r.dU = s.dU;
+    r.status = a.status;
+    if ((e = launch_reverse_tc(r, st)) != cudaSuccess) return e;
+    if (units > 0) {
+      dgl_kernel<<<dim3((unsigned)units, (unsigned)(dv / kNS)), kThreads, 0, st>>>(s);
+      count_launches(1);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+  } else {
+    rev_states_kernel<<<gs, kThreads, kRevSmem, st>>>(dS_final, dS0, a.map, a.H, s);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if (units == 0) return cudaSuccess;
   const size_t D = s.sD(), V = s.sV(), S = s.sS(), CC = kCC;
   struct G {

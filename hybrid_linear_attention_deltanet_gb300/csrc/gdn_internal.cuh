@@ -286,6 +286,27 @@ cudaError_t launch_prefill_any(PrefillLaunch a, int32_t io_dtype, int64_t seqlen
 cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t stream);
 cudaError_t scratch_free(void* p, cudaStream_t stream);
 
+// The backward's reverse state pass on the tensor cores (bf16 I/O): per
+// (sequence, head, 128-row slice of dS), over the chunks in reverse, from
+// dS_final (nullptr: zero) to dS0 (nullptr: not written); stores every
+// chunk's end-state gradient dS' ([chunks * H][dv][dk] fp32) and dU ([chunks *
+// H][64][dv] fp32).  images: the forward's per-chunk operand images over the
+// same map; k, dout: the call's bf16 tensors.
+struct ReverseLaunch {
+  const void* k = nullptr;
+  const void* dout = nullptr;
+  SeqMap map{};
+  int32_t H = 0, dv = 0;
+  int64_t T_total = 0;
+  const uint8_t* images = nullptr;
+  const float* dS_final = nullptr;
+  float* dS0 = nullptr;
+  float* dSp = nullptr;
+  float* dU = nullptr;
+  unsigned* status = nullptr;
+};
+cudaError_t launch_reverse_tc(const ReverseLaunch& r, cudaStream_t stream);
+
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, const float* alpha,
                                const float* beta, float* S, void* out, int32_t N, int32_t H,
                                int32_t dv, int io_dtype, cudaStream_t stream);

@@ -152,10 +152,10 @@ __global__ void plan_segments_kernel(const int32_t* __restrict__ cu, int32_t N, 
 // are independent under right-multiplication by A, so each CTA walks its
 // sequence's segments on its own.  Thread c owns column c of its 16 rows;
 // the previous start's rows sit in shared memory and column c of each A
-// streams through registers in blocks of 32 rows of A, the next block's loads
+// streams through registers in blocks of kScanBlk rows of A, the next block's loads
 // (coalesced across the CTA) in flight while the current one is consumed:
 // no A depends on the scan, so the stream never waits on the arithmetic.
-constexpr int kScanBlk = 32;
+constexpr int kScanBlk = 64;
 
 __global__ void __launch_bounds__(256) seg_scan_kernel(float* __restrict__ S0seg,
                                                        const float* __restrict__ Bseg,

@@ -1478,6 +1478,263 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
 }
 
+// ======================================================= reverse state pass
+// The backward's reverse recurrence over the chunks of a sequence, on the
+// tensor cores (bf16 I/O), mirroring the forward state pass.  For a chunk with
+// end-state gradient dS' (dv x dk; this unit holds 128 of its rows):
+//   dU^T = (dO^T P^) + (dS' K^T) diag(d)         [rows of dS x 64 tokens]
+//   dS   = gamma_L dS' + dO^T Q^ - dU^T W          (the gradient carried back)
+// with P^, Q^, W and the decay factors read from the forward's own operand
+// images (the backward's forward re-run leaves them in scratch).  Per chunk:
+// MMA-X  D_X = dS' K^T (A: the bf16 copy of dS' in TMEM, B: the K tile
+//        K-major, N = 64, 16 K-steps over dk);
+// MMA-P  D_P = dO^T P^ (A: the dO tile MN-major, B: P^ read MN-major, N = 64);
+// E1     dU^T = D_P + d D_X -> fp32 dU to scratch, -dU^T as a bf16 A operand
+//        in TMEM over D_X;
+// MMA-S  D_S = dO^T Q^ + (-dU^T) W, as four N = 64 blocks of dk (the image's
+//        64-row blocks of W and Q^ are 16 KB apart), K = 64 tokens;
+// E2     dS = gamma_L dS' + D_S in fp32 registers, bf16 copy back to TMEM.
+// Before E2 the unit stores dS' (fp32) for the chunk gradients.  Tokens past
+// the chunk's end contribute nothing: their d is 0 and their rows and
+// columns of P^ are 0.
+constexpr uint32_t kR_WQ = 0;         // 2 x 64 KB: the [W | Q^] images
+constexpr uint32_t kR_KP = 131072;    // 40 KB: K tile (32 KB) | P^ (8 KB)
+constexpr uint32_t kR_O = 172032;     // 2 x 16 KB: dO tiles (two 64-column blocks)
+constexpr uint32_t kR_D = 204800;     // 2 x 512 B: decay blocks (d_r, then G_r)
+constexpr uint32_t kR_END = 205824;
+constexpr uint32_t kRevSmemTc = kR_END + 1024;
+constexpr uint32_t kR_TX = 0, kR_TP = 64, kR_TSA = 128, kR_TS = 256;   // TMEM columns
+
+__global__ void __launch_bounds__(kStateThreads, 1)
+tc_reverse_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_o,
+                  SeqMap map, int32_t H, int32_t dv, const uint8_t* __restrict__ images,
+                  const float* __restrict__ dS_final, float* __restrict__ dS0,
+                  float* __restrict__ dSp, float* __restrict__ dUo, unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align_smem_1024(smem_raw);
+  const int ns = dv / 128;
+  const int lin = blockIdx.x, slice = lin % ns, h = (lin / ns) % H, n = lin / (ns * H);
+  __shared__ uint64_t bar_wq[2], bar_kp, bar_o[2], bar_m1, bar_m2;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, colhalf = warp >> 2;
+  const uint32_t iloc = 32 * quarter + lane;
+  const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+  const int64_t cb = map.chunk_begin(n), ce = map.chunk_end(n);
+  const int64_t s_begin = map.seq_begin(n), s_end = map.seq_end(n);
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_wq[b], 1);
+      mbar_init(&bar_o[b], 1);
+    }
+    mbar_init(&bar_kp, 1);
+    mbar_init(&bar_m1, 1);
+    mbar_init(&bar_m2, 1);
+    fence_barrier_init();
+    s_abort = 0;
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_o);
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, 512);
+  // this thread's 128 columns of row iloc of dS (fp32), from dS_final
+  float S[128];
+  const size_t srow = (((size_t)n * H + h) * dv + 128 * slice + iloc) * kDK + 128 * colhalf;
+  if (dS_final) {
+    const float4* p = reinterpret_cast<const float4*>(dS_final + srow);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float4 t = p[j];
+      S[4 * j] = t.x; S[4 * j + 1] = t.y; S[4 * j + 2] = t.z; S[4 * j + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 128; ++j) S[j] = 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  auto store_operand = [&]() {   // bf16 copy of this thread's dS columns into TMEM
+#pragma unroll
+    for (int hq = 0; hq < 2; ++hq) {
+      uint32_t r[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = pack_bf16(S[64 * hq + 2 * j], S[64 * hq + 2 * j + 1]);
+      tmem_st32(tmem + lane_off + kR_TSA + 64 * colhalf + 32 * hq, r);
+    }
+    tmem_st_wait();
+  };
+  store_operand();
+  auto img_of = [&](int64_t ci) { return images + (size_t)(ci * H + h) * img_stride(dv); };
+  auto t0_of = [&](int64_t ci) { return (int32_t)(s_begin + (ci - cb) * kC); };
+  // copies by single threads of warps 1-3, counted for a clean exit after a timeout
+  constexpr int kLK = 32, kLW = 64, kLO = 96;
+  uint32_t n_wq[2] = {0, 0}, n_kp = 0, n_o[2] = {0, 0};
+  auto issue_kp = [&](int64_t ci) {   // the K tile and P^
+    mbar_arrive_expect_tx(&bar_kp, 40960);
+    tma_load_4d(sm + kR_KP, &tm_k, 0, t0_of(ci), 0, h, &bar_kp);
+    tma_load_1d(sm + kR_KP + 32768, img_of(ci) + kImgP, 8192, &bar_kp);
+    ++n_kp;
+  };
+  auto issue_o = [&](int64_t ci, int b) {   // this unit's dO columns and the decay block
+    mbar_arrive_expect_tx(&bar_o[b], 16384 + 512);
+    for (int bb = 0; bb < 2; ++bb)
+      tma_load_3d(sm + kR_O + b * 16384 + bb * 8192, &tm_o, 128 * slice + 64 * bb, h, t0_of(ci),
+                  &bar_o[b]);
+    tma_load_1d(sm + kR_D + b * 512, img_of(ci) + kImgU0 + slice * kImgHalf + kImgDecay, 512,
+                &bar_o[b]);
+    ++n_o[b];
+  };
+  auto issue_wq = [&](int64_t ci, int b) {
+    mbar_arrive_expect_tx(&bar_wq[b], 65536);
+    tma_load_1d(sm + kR_WQ + b * 65536, img_of(ci) + kImgWQ, 65536, &bar_wq[b]);
+    ++n_wq[b];
+  };
+  if (ce > cb) {
+    if (tid == kLK) issue_kp(ce - 1);
+    if (tid == kLO) issue_o(ce - 1, 0);
+    if (tid == kLW) {
+      issue_wq(ce - 1, 0);
+      if (ce - 2 >= cb) issue_wq(ce - 2, 1);
+    }
+  }
+  const size_t dsp_row = 128 * slice + iloc;
+  for (int64_t ci = ce - 1; ci >= cb && !s_abort; --ci) {
+    const int64_t it = ce - 1 - ci;
+    const int b = (int)(it & 1);
+    const uint32_t par = (uint32_t)(it & 1), bpar = (uint32_t)((it >> 1) & 1);
+    const int64_t t0 = t0_of(ci);
+    const int L = (int)min((int64_t)kC, s_end - t0);
+    const size_t u = (size_t)(ci * H + h);
+    const float* sD = reinterpret_cast<const float*>(sm + kR_D + b * 512);
+    if (tid == kLO && ci - 1 >= cb) issue_o(ci - 1, b ^ 1);
+    // MMA-X and MMA-P
+    if (tid == 0) {
+      if (!mbar_wait(&bar_kp, par) || !mbar_wait(&bar_o[b], bpar)) {
+        s_abort = 1;
+      } else {
+        tc_fence_after();
+        const uint32_t sK = smem_u32(sm + kR_KP), sP = sK + 32768;
+        const uint32_t sO = smem_u32(sm + kR_O + b * 16384);
+        const uint32_t idx = idesc_bf16(128, 64, 0, 0), idp = idesc_bf16(128, 64, 1, 1);
+        for (int s = 0; s < 16; ++s)
+          mma_bf16_ts(tmem + kR_TX, tmem + kR_TSA + 8 * s,
+                      smem_desc(sK + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024, kSwizzle128B), idx,
+                      s > 0);
+        for (int s = 0; s < 4; ++s)
+          mma_bf16(tmem + kR_TP, smem_desc(sO + s * 2048, 8192, 1024, kSwizzle128B),
+                   smem_desc(sP + s * 2048, 8192, 1024, kSwizzle128B), idp, s > 0);
+        mma_commit(&bar_m1);
+      }
+    }
+    // dS' of this chunk (fp32), for the chunk gradients
+    {
+      float4* p = reinterpret_cast<float4*>(dSp + (u * dv + dsp_row) * kDK + 128 * colhalf);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) p[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+    }
+    // E1: dU^T = D_P + d D_X
+    if (!mbar_wait(&bar_m1, par)) {
+      flag_status(status, GDN_ERR_TIMEOUT);
+      s_abort = 1;
+    } else {
+      tc_fence_after();
+      if (tid == kLK && ci - 1 >= cb) issue_kp(ci - 1);   // K / P^ are read
+      uint32_t gx[32], gp[32];
+      tmem_ld32(tmem + lane_off + kR_TX + 32 * colhalf, gx);
+      tmem_ld32(tmem + lane_off + kR_TP + 32 * colhalf, gp);
+      tmem_ld_wait();
+      uint32_t pk[16];
+      float* du_out = dUo + (u * kC + 32 * colhalf) * dv + dsp_row;
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const int r = 32 * colhalf + j;
+        const float d0 = fmaf(sD[r], __uint_as_float(gx[j]), __uint_as_float(gp[j]));
+        const float d1 = fmaf(sD[r + 1], __uint_as_float(gx[j + 1]), __uint_as_float(gp[j + 1]));
+        du_out[(size_t)j * dv] = d0;
+        du_out[(size_t)(j + 1) * dv] = d1;
+        pk[j >> 1] = pack_bf16(-d0, -d1);
+      }
+      tmem_st16(tmem + lane_off + kR_TX + 32 * colhalf, pk);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (s_abort) break;
+    // MMA-S: D_S = dO^T Q^ + (-dU^T) W over four 64-column blocks of dk
+    if (tid == 0) {
+      if (!mbar_wait(&bar_wq[b], bpar)) {
+        s_abort = 1;
+      } else {
+        tc_fence_after();
+        const uint32_t sW = smem_u32(sm + kR_WQ + b * 65536);
+        const uint32_t sO = smem_u32(sm + kR_O + b * 16384);
+        const uint32_t idq = idesc_bf16(128, 64, 1, 0), idw = idesc_bf16(128, 64, 0, 0);
+        for (int bk = 0; bk < 4; ++bk)
+          for (int s = 0; s < 4; ++s)
+            mma_bf16(tmem + kR_TS + 64 * bk, smem_desc(sO + s * 2048, 8192, 1024, kSwizzle128B),
+                     smem_desc(sW + bk * 16384 + 8192 + s * 32, 16, 1024, kSwizzle128B), idq, s > 0);
+        for (int bk = 0; bk < 4; ++bk)
+          for (int s = 0; s < 4; ++s)
+            mma_bf16_ts(tmem + kR_TS + 64 * bk, tmem + kR_TX + col_U(s),
+                        smem_desc(sW + bk * 16384 + s * 32, 16, 1024, kSwizzle128B), idw, 1);
+        mma_commit(&bar_m2);
+      }
+    }
+    // E2: dS = gamma_L dS' + D_S, and its bf16 copy (MMA-X has read the old one)
+    if (!mbar_wait(&bar_m2, par)) {
+      flag_status(status, GDN_ERR_TIMEOUT);
+      s_abort = 1;
+    } else {
+      tc_fence_after();
+      if (tid == kLW && ci - 2 >= cb) issue_wq(ci - 2, b);   // this chunk's W | Q^ are read
+      const float gC = exp_fast(sD[64 + L - 1]);
+      const uint32_t tS = tmem + lane_off + kR_TS + 128 * colhalf;
+      const uint32_t tA = tmem + lane_off + kR_TSA + 64 * colhalf;
+      uint32_t g[2][16];
+      tmem_ld16(tS, g[0]);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        tmem_ld_wait_regs(g[q & 1]);
+        if (q + 1 < 8) tmem_ld16(tS + 16 * (q + 1), g[(q + 1) & 1]);
+        uint32_t pk[8];
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          const float s0 = fmaf(gC, S[16 * q + j], __uint_as_float(g[q & 1][j]));
+          const float s1 = fmaf(gC, S[16 * q + j + 1], __uint_as_float(g[q & 1][j + 1]));
+          S[16 * q + j] = s0;
+          S[16 * q + j + 1] = s1;
+          pk[j >> 1] = pack_bf16(s0, s1);
+        }
+        tmem_st8(tA + 8 * q, pk);
+      }
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  if (!s_abort && dS0) {
+    float4* p = reinterpret_cast<float4*>(dS0 + srow);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) p[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+  }
+  if (s_abort && (tid == kLK || tid == kLW || tid == kLO)) {   // let copies in flight land
+    flag_status(status, GDN_ERR_TIMEOUT);
+    const uint64_t lim = 100000000ull;
+    for (int b = 0; b < 2; ++b) {
+      if (tid == kLW && n_wq[b]) mbar_wait(&bar_wq[b], (n_wq[b] - 1) & 1, lim);
+      if (tid == kLO && n_o[b]) mbar_wait(&bar_o[b], (n_o[b] - 1) & 1, lim);
+    }
+    if (tid == kLK && n_kp) mbar_wait(&bar_kp, (n_kp - 1) & 1, lim);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
 constexpr uint32_t kPrepSmemSplit = PrepSmem<false>::BYTES;
 constexpr uint32_t kFusedSmem = kStateSmem > PrepSmem<true>::BYTES ? kStateSmem : PrepSmem<true>::BYTES;
 static_assert(PrepSmem<false>::A == 65536 && PrepSmem<true>::A % 1024 == 0, "prep layout");
@@ -1678,6 +1935,25 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
   tc_state_kernel<<<grid, kStateThreads, kStateSmem, stream>>>(
       tkb, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr, a.status, g_trace,
       g_trace_chunks, dv, a.state_dump, a.route, a.ng);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reverse_tc(const ReverseLaunch& r, cudaStream_t stream) {
+  if (!supported_dv(r.dv)) return cudaErrorInvalidValue;
+  const int64_t n_blocks = (int64_t)r.map.N * r.H * (r.dv / 128);
+  if (n_blocks <= 0) return cudaSuccess;
+  if (n_blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  CUtensorMap tk, to;
+  if (!make_token_map_blocked(&tk, r.k, r.T_total, r.H) ||
+      !make_token_map(&to, r.dout, r.T_total, r.H, r.dv))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(tc_reverse_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kRevSmemTc);
+  if (e != cudaSuccess) return e;
+  tc_reverse_kernel<<<(unsigned)n_blocks, kStateThreads, kRevSmemTc, stream>>>(
+      tk, to, r.map, r.H, r.dv, r.images, r.dS_final, r.dS0, r.dSp, r.dU, r.status);
   count_launches(1);
   return cudaGetLastError();
 }
