@@ -845,6 +845,7 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     r.dS0 = dS0;
     r.dSp = s.dSp;
     r.dU = s.dU;
+    r.KdS = s.KdS;
     r.status = a.status;
     if ((e = launch_reverse_tc(r, st)) != cudaSuccess) return e;
     if (units > 0) {
@@ -882,10 +883,14 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
       {true, false, {s.Tm, CC, kC}, {s.dTm, CC, kC}, s.X, CC, kC, kC, kC, 1.f, nullptr, 0.f, 0, nullptr},
       {false, true, {s.X, CC, kC}, {s.Tm, CC, kC}, s.dA, CC, kC, kC, kC, -1.f, nullptr, 0.f, 2, nullptr},
   };
-  for (const G& g : list)
+  for (int i = 0; i < (int)(sizeof list / sizeof list[0]); ++i) {
+    // bf16 I/O: K dS'^T came from the reverse pass
+    if (io_dtype == GDN_BF16 && list[i].C == s.KdS) continue;
+    const G& g = list[i];
     if ((e = gemm(st, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc, g.N, g.K, g.alpha, g.Cin, g.beta,
                   g.mask, g.col, kC, units)) != cudaSuccess)
       return e;
+  }
   cc_kernel<<<(unsigned)units, kThreads, 0, st>>>(s);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -303,6 +303,7 @@ struct ReverseLaunch {
   float* dS0 = nullptr;
   float* dSp = nullptr;
   float* dU = nullptr;
+  float* KdS = nullptr;   // [chunks * H][64][dv]: K dS'^T of every chunk, or nullptr
   unsigned* status = nullptr;
 };
 cudaError_t launch_reverse_tc(const ReverseLaunch& r, cudaStream_t stream);

@@ -1486,8 +1486,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 //   dS   = gamma_L dS' + dO^T Q^ - dU^T W          (the gradient carried back)
 // with P^, Q^, W and the decay factors read from the forward's own operand
 // images (the backward's forward re-run leaves them in scratch).  Per chunk:
-// MMA-X  D_X = dS' K^T (A: the bf16 copy of dS' in TMEM, B: the K tile
-//        K-major, N = 64, 16 K-steps over dk);
+// MMA-X  D_X = dS' K^T, also stored as the chunk gradients' K dS'^T (A: the
+//        bf16 copy of dS' in TMEM, B: the K tile K-major, N = 64, 16 K-steps);
 // MMA-P  D_P = dO^T P^ (A: the dO tile MN-major, B: P^ read MN-major, N = 64);
 // E1     dU^T = D_P + d D_X -> fp32 dU to scratch, -dU^T as a bf16 A operand
 //        in TMEM over D_X;
@@ -1501,7 +1501,8 @@ constexpr uint32_t kR_WQ = 0;         // 2 x 64 KB: the [W | Q^] images
 constexpr uint32_t kR_KP = 131072;    // 40 KB: K tile (32 KB) | P^ (8 KB)
 constexpr uint32_t kR_O = 172032;     // 2 x 16 KB: dO tiles (two 64-column blocks)
 constexpr uint32_t kR_D = 204800;     // 2 x 512 B: decay blocks (d_r, then G_r)
-constexpr uint32_t kR_END = 205824;
+constexpr uint32_t kR_T = 205824;     // 8 x 2560 B: per-warp transpose tiles (32 x 20 floats)
+constexpr uint32_t kR_END = 226304;
 constexpr uint32_t kRevSmemTc = kR_END + 1024;
 constexpr uint32_t kR_TX = 0, kR_TP = 64, kR_TSA = 128, kR_TS = 256;   // TMEM columns
 
@@ -1509,7 +1510,8 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 tc_reverse_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_o,
                   SeqMap map, int32_t H, int32_t dv, const uint8_t* __restrict__ images,
                   const float* __restrict__ dS_final, float* __restrict__ dS0,
-                  float* __restrict__ dSp, float* __restrict__ dUo, unsigned* status) {
+                  float* __restrict__ dSp, float* __restrict__ dUo, float* __restrict__ kds,
+                  unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align_smem_1024(smem_raw);
   const int ns = dv / 128;
@@ -1628,11 +1630,30 @@ tc_reverse_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         mma_commit(&bar_m1);
       }
     }
-    // dS' of this chunk (fp32), for the chunk gradients
+    // dS' of this chunk (fp32), for the chunk gradients.  A warp holds 32
+    // rows; stored as they are, each 16-byte piece would be its own L2
+    // transaction, so 16 columns at a time go through a per-warp tile in
+    // shared memory and leave as four rows of 64 contiguous bytes per store.
     {
-      float4* p = reinterpret_cast<float4*>(dSp + (u * dv + dsp_row) * kDK + 128 * colhalf);
+      float* tile = reinterpret_cast<float*>(sm + kR_T + warp * 2560);
+      float* row0 = dSp + (u * dv + 128 * slice + 32 * quarter) * kDK + 128 * colhalf;
+      const int rr = lane >> 2, c4 = lane & 3;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) p[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+      for (int q = 0; q < 8; ++q) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<float4*>(tile + lane * 20 + 4 * k) =
+              make_float4(S[16 * q + 4 * k], S[16 * q + 4 * k + 1], S[16 * q + 4 * k + 2],
+                          S[16 * q + 4 * k + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 8 * i + rr;
+          *reinterpret_cast<float4*>(row0 + (size_t)r * kDK + 16 * q + 4 * c4) =
+              *reinterpret_cast<const float4*>(tile + r * 20 + 4 * c4);
+        }
+        __syncwarp();
+      }
     }
     // E1: dU^T = D_P + d D_X
     if (!mbar_wait(&bar_m1, par)) {
@@ -1647,6 +1668,7 @@ tc_reverse_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       tmem_ld_wait();
       uint32_t pk[16];
       float* du_out = dUo + (u * kC + 32 * colhalf) * dv + dsp_row;
+      float* kds_out = kds ? kds + (u * kC + 32 * colhalf) * dv + dsp_row : nullptr;
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         const int r = 32 * colhalf + j;
@@ -1654,6 +1676,10 @@ tc_reverse_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         const float d1 = fmaf(sD[r + 1], __uint_as_float(gx[j + 1]), __uint_as_float(gp[j + 1]));
         du_out[(size_t)j * dv] = d0;
         du_out[(size_t)(j + 1) * dv] = d1;
+        if (kds_out) {   // K dS'^T of the chunk, for the chunk gradients
+          kds_out[(size_t)j * dv] = __uint_as_float(gx[j]);
+          kds_out[(size_t)(j + 1) * dv] = __uint_as_float(gx[j + 1]);
+        }
         pk[j >> 1] = pack_bf16(-d0, -d1);
       }
       tmem_st16(tmem + lane_off + kR_TX + 32 * colhalf, pk);
@@ -1953,7 +1979,7 @@ cudaError_t launch_reverse_tc(const ReverseLaunch& r, cudaStream_t stream) {
                                        (int)kRevSmemTc);
   if (e != cudaSuccess) return e;
   tc_reverse_kernel<<<(unsigned)n_blocks, kStateThreads, kRevSmemTc, stream>>>(
-      tk, to, r.map, r.H, r.dv, r.images, r.dS_final, r.dS0, r.dSp, r.dU, r.status);
+      tk, to, r.map, r.H, r.dv, r.images, r.dS_final, r.dS0, r.dSp, r.dU, r.KdS, r.status);
   count_launches(1);
   return cudaGetLastError();
 }
