@@ -1568,6 +1568,10 @@ tc_reverse_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     tmem_st_wait();
   };
   store_operand();
+  // every warp's rows of the operand are in TMEM before the first MMA-X
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   auto img_of = [&](int64_t ci) { return images + (size_t)(ci * H + h) * img_stride(dv); };
   auto t0_of = [&](int64_t ci) { return (int32_t)(s_begin + (ci - cb) * kC); };
   // copies by single threads of warps 1-3, counted for a clean exit after a timeout

@@ -140,9 +140,10 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
  * When seqlen reaches 1024 chunks (the segmented form) the layout is instead,
  * each part rounded up to 256 bytes: the segment slots' chunk offsets, token
  * starts and sequence indices (4 (slots + 1) bytes each), the sequences'
- * first slots (4 (batch + 1)), one role byte per slot, the per-chunk scratch
- * above, then three fp32 states of heads * dv * 256 per slot, where slots =
- * batch + max_chunks / 160 + 1.
+ * first slots (4 (batch + 1)), one role byte per slot, the state passes'
+ * launch order (12 bytes per slot), the per-chunk scratch above, then three
+ * fp32 states of heads * dv * 256 per slot, where slots = batch + max_chunks
+ * / 160 + 1.
  * 0 when the call needs no scratch; SIZE_MAX for arguments gdn_prefill would
  * reject as invalid or unsupported.
  */

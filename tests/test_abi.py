@@ -274,10 +274,12 @@ def _chunks(B, T, varlen):
 def _segmented_bytes(B, T, H, dv, varlen, work, slots):
     """gdn.h's layout of the segmented form: chunk offsets, token starts and
     sequences of the slots, the sequences' first slots, a role byte per slot,
-    the per-chunk scratch, three fp32 states per (slot, head)."""
+    the launch order (12 bytes per slot), the per-chunk scratch, three fp32
+    states per (slot, head)."""
     ints = _up(4 * (slots + 1), 256)
     state = _up(slots * H * dv * 256 * 4, 256)
-    return 3 * ints + _up(4 * (B + 1), 256) + _up(slots, 256) + _up(work, 256) + 3 * state
+    return (3 * ints + _up(4 * (B + 1), 256) + _up(slots, 256) + _up(12 * slots, 256) +
+            _up(work, 256) + 3 * state)
 
 
 def test_workspace_size_follows_the_documented_layout(lib):

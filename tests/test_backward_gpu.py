@@ -87,6 +87,32 @@ def test_backward_varlen_with_empty_sequences(gdn_lib):
                                io_dtype=torch.bfloat16, seed=93, varlen=True), seed=9)
 
 
+def test_backward_repeatable_bitwise(gdn_lib):
+    """Repeated calls on the same inputs give the same bits, whatever the
+    workspace held before (caller workspaces filled with 0x00 and 0xFF
+    bytes in turn).  The packing has chunks of 1 and 64 rows and a sequence
+    of 129 tokens, whose one-row chunk starts the reverse pass: the pass's
+    first MMA must see every warp's rows of the state-gradient operand."""
+    lens = [0, 70, 1, 0, 129, 64]
+    case = PrefillCase("bwd repeat", lens, H=2, io_dtype=torch.bfloat16, seed=93, varlen=True)
+    x = grad_inputs(case, 9)
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    need = gdn_lib.prefill_backward_workspace_size(len(lens), sum(lens), 2, varlen=True)
+    first = None
+    for i in range(8):
+        buf = torch.full((need + 1024,), 0xFF if i % 2 else 0, dtype=torch.uint8, device=DEV)
+        off = (-buf.data_ptr()) % 1024
+        g = gdn_lib.prefill_backward(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["dout"],
+                                     d["S0"], d["dS_final"], d["cu_seqlens"],
+                                     workspace=buf[off:off + need])
+        assert gdn_lib.device_status() == 0
+        g = {k: v.clone() for k, v in g.items()}
+        if first is None:
+            first = g
+        for key in ("dq", "dk", "dv", "dalpha", "dbeta", "dS0"):
+            assert torch.equal(g[key], first[key]), (i, key)
+
+
 def test_backward_dv512(gdn_lib):
     check(gdn_lib, PrefillCase("bwd dv512", [100, 3], H=1, dv=512, io_dtype=torch.float32,
                                seed=94, varlen=True), seed=10)

@@ -94,6 +94,28 @@ def test_scan_ws_matches_scan(gdn_lib, io):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("lens,H,varlen", [([8192], 1, False), ([0, 70, 1, 0, 129, 64], 2, True)])
+def test_prefill_ws_contents_do_not_matter(gdn_lib, lens, H, varlen):
+    """Every byte the call reads from its workspace it wrote first: workspaces
+    filled with 0x00, 0xFF and 0x7F bytes give the same bits (one sequence
+    over 128 chunks in the fused form; a packing with empty sequences and
+    one-row chunks)."""
+    case = PrefillCase("ws fill", lens, H=H, io_dtype=torch.bfloat16, seed=64, varlen=varlen)
+    xd = to_dev(gdn_inputs.make_prefill(case, device="cpu"))
+    need = gdn_lib.prefill_workspace_size(len(lens), sum(lens) if varlen else lens[0], H,
+                                          varlen=varlen)
+    got = []
+    for fill in (0x00, 0xFF, 0x7F):
+        ws = _workspace(need)
+        ws.fill_(fill)
+        out, Sf = gdn_lib.prefill(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["S0"],
+                                  xd["cu_seqlens"], workspace=ws)
+        assert gdn_lib.device_status() == 0
+        got.append((out.clone(), Sf.clone()))
+    for out, Sf in got[1:]:
+        assert torch.equal(out, got[0][0]) and torch.equal(Sf, got[0][1])
+
+
 @pytest.mark.parametrize("io", [torch.bfloat16, torch.float32])
 def test_backward_ws_matches_backward(gdn_lib, io):
     case = PrefillCase("ws bwd", [70, 129], H=2, io_dtype=io, seed=67, varlen=True)
