@@ -747,6 +747,18 @@ cudaError_t gemm(cudaStream_t st, bool tA, bool tB, Mat A, Mat B, float* C, size
   return cudaGetLastError();
 }
 
+// bf16 I/O: the tensor-core GEMM where its shapes allow (dv = 256), else
+// the CUDA-core one
+cudaError_t gemm_io(int io_dtype, unsigned* status, cudaStream_t st, bool tA, bool tB, Mat A,
+                    Mat B, float* C, size_t sC, int ldc, int N, int K, float alpha,
+                    const float* Cin, float beta, int mask, const float* col, size_t sCol,
+                    int64_t batch) {
+  if (io_dtype == GDN_BF16 && tgemm_shape_ok(N, K, A.ld, B.ld, ldc, tA, tB))
+    return launch_tgemm(A.p, A.stride, A.ld, B.p, B.stride, B.ld, Cin, C, sC, ldc, col, sCol, N,
+                        K, alpha, beta, mask, batch, tA, tB, status, st);
+  return gemm(st, tA, tB, A, B, C, sC, ldc, N, K, alpha, Cin, beta, mask, col, sCol, batch);
+}
+
 constexpr size_t kFwdSmem = sizeof(float) * (kNS * kSP + kC * kWS + kC * kUP + kSlabF * kDK + kC);
 constexpr size_t kRevSmem = sizeof(float) * (kNS * kSP + kC * kKSP + 2 * kC * kUP +
                                              2 * kSlabR * kDK + kC * kPP + 2 * kC + 8);
@@ -800,17 +812,17 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t D = s.sD(), V = s.sV(), CC = kCC;
     // KK^T and QK^T
-    if ((e = gemm(st, false, true, {s.K, D, kDK}, {s.K, D, kDK}, s.KK, CC, kC, kC, kDK, 1.f,
+    if ((e = gemm_io(io_dtype, a.status, st, false, true, {s.K, D, kDK}, {s.K, D, kDK}, s.KK, CC, kC, kC, kDK, 1.f,
                   nullptr, 0.f, 0, nullptr, 0, units)) != cudaSuccess) return e;
-    if ((e = gemm(st, false, true, {s.Q, D, kDK}, {s.K, D, kDK}, s.QK, CC, kC, kC, kDK, 1.f,
+    if ((e = gemm_io(io_dtype, a.status, st, false, true, {s.Q, D, kDK}, {s.K, D, kDK}, s.QK, CC, kC, kC, kDK, 1.f,
                   nullptr, 0.f, 0, nullptr, 0, units)) != cudaSuccess) return e;
     tprep_kernel<<<(unsigned)units, kThreads, 0, st>>>(s);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // W = T diag(beta gamma) K, U~ = T diag(beta) V
-    if ((e = gemm(st, false, false, {s.TmB, CC, kC}, {s.K, D, kDK}, s.W, D, kDK, kDK, kC, 1.f,
+    if ((e = gemm_io(io_dtype, a.status, st, false, false, {s.TmB, CC, kC}, {s.K, D, kDK}, s.W, D, kDK, kDK, kC, 1.f,
                   nullptr, 0.f, 0, nullptr, 0, units)) != cudaSuccess) return e;
-    if ((e = gemm(st, false, false, {s.TmU, CC, kC}, {s.V, V, dv}, s.Ut, V, dv, dv, kC, 1.f,
+    if ((e = gemm_io(io_dtype, a.status, st, false, false, {s.TmU, CC, kC}, {s.V, V, dv}, s.Ut, V, dv, dv, kC, 1.f,
                   nullptr, 0.f, 0, nullptr, 0, units)) != cudaSuccess) return e;
   }
   const dim3 gs((unsigned)a.map.N, (unsigned)a.H, (unsigned)(dv / kNS));
@@ -887,7 +899,7 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     // bf16 I/O: K dS'^T came from the reverse pass
     if (io_dtype == GDN_BF16 && list[i].C == s.KdS) continue;
     const G& g = list[i];
-    if ((e = gemm(st, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc, g.N, g.K, g.alpha, g.Cin, g.beta,
+    if ((e = gemm_io(io_dtype, a.status, st, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc, g.N, g.K, g.alpha, g.Cin, g.beta,
                   g.mask, g.col, kC, units)) != cudaSuccess)
       return e;
   }
@@ -901,7 +913,7 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
       {false, false, {s.FG, CC, kC}, {s.K, D, kDK}, s.dQa, D, kDK, kDK, kC, 1.f, nullptr, 0.f, 0, nullptr},
   };
   for (const G& g : list2)
-    if ((e = gemm(st, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc, g.N, g.K, g.alpha, g.Cin, g.beta,
+    if ((e = gemm_io(io_dtype, a.status, st, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc, g.N, g.K, g.alpha, g.Cin, g.beta,
                   g.mask, g.col, kC, units)) != cudaSuccess)
       return e;
   if (io_dtype == GDN_BF16)

@@ -257,6 +257,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::tf32: fp32 operands (their upper
+// 19 bits), fp32 accumulation; one instruction covers K = 8.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16.  A sits in TMEM with row m in
 // lane m and two consecutive K elements packed per 32-bit column (the lower
 // 16 bits hold the even element).
@@ -376,6 +386,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, uint32
          | (1u << 10)         // B format: bf16
          | (neg_a << 13) | (neg_b << 14) | (a_mn << 15) | (b_mn << 16) |
          ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Instruction descriptor of kind::tf32 (fp32 accumulator, both operands
+// tf32 and K-major): the f16 layout with format code 2 for A and B.
+__host__ __device__ constexpr uint32_t idesc_tf32(uint32_t M, uint32_t N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // Byte offset of element (row, col) inside a 128-byte-swizzled image whose

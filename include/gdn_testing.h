@@ -19,6 +19,24 @@ extern "C" {
 #endif
 
 /*
+ * gdn_testing_tgemm -- the backward's batched tensor-core GEMM (kind::tf32,
+ * the chunk gradients' contractions with bf16 I/O) on caller arrays: for
+ * each unit b < batch,
+ *   C[m][n] = alpha * col[n] * sum_k A'[m][k] B'[k][n] + beta * Cin[m][n]
+ * for m < 64, n < N, then zeroed where mask asks (1: n > m, 2: n >= m).
+ * A' is A stored [64][lda] (tA = 0) or [K][lda] (tA = 1); B' is B stored
+ * [K][ldb] (tB = 0) or [N][ldb] (tB = 1); C and Cin are [64][ldc]; unit b's
+ * arrays start sA, sB, sC, sCol floats after unit 0's.  Cin and col may be
+ * null.  N in {64, 256}, K in {64, 256}, lda and ldb multiples of 4 (A and B
+ * 16-byte aligned): GDN_ERR_UNSUPPORTED / GDN_ERR_ALIGNMENT otherwise.
+ * Operands round to tf32 (10 explicit mantissa bits); fp32 accumulation.
+ */
+int gdn_testing_tgemm(const float* A, int64_t sA, int32_t lda, int32_t tA, const float* B,
+                      int64_t sB, int32_t ldb, int32_t tB, const float* Cin, float beta, float* C,
+                      int64_t sC, int32_t ldc, const float* col, int64_t sCol, int32_t N,
+                      int32_t K, float alpha, int32_t mask, int64_t batch, gdn_stream_t stream);
+
+/*
  * gdn_testing_umma_gemm -- D[128][N] (fp32) = A[128][K] * B[N][K]^T with
  * bf16 row-major inputs, on one CTA through tcgen05.mma (M = 128).
  *   a_mn / b_mn : stage the operand MN-major (1) or K-major (0) in a
