@@ -72,10 +72,10 @@ def prepare_bytes(T_total, N, H=H, dk=DK, dv=DV, io_bytes=2, state=True):
 
 def backward_flops(lengths, H=H, dk=DK, dv=DV):
     """FLOPs the chunked backward executes per call (C = 64 rows a chunk,
-    padded chunks counted whole), counted as the CUDA-core form runs them: the
-    forward re-run for the chunk-start states (KK^T, QK^T, W, U~, U and S' per
-    chunk; with bf16 I/O the U and S' products run on the tensor cores inside
-    the forward prefill instead) plus the reverse state pass
+    padded chunks counted whole): the forward re-run for the chunk-start
+    states (KK^T, QK^T, W, U~, U and S' per chunk; with bf16 I/O the U and S'
+    products run inside the tensor-core forward prefill) plus the reverse
+    state pass
     (K dS'^T, Ph^T dO, dO^T Qh, dU^T W) and the per-chunk gradient products
     (U, dO S, dU S, U dS', K dS'^T at C x d x d; dPh, dT, T^T dW, T^T dU, T^T dT,
     dA, (M + M^T) K, FG^T Q, FG K at C x C x d)."""
@@ -97,6 +97,12 @@ def norm_gate_bytes(rows, dv=DV, io_bytes=2):
 # fp32 FMA peak of the CUDA cores, from the unit counts and the maximum SM
 # clock (152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz)
 FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def TF32_TFLOPS(peaks):
+    """Dense tf32 tensor peak: the bf16 figure scaled by the nominal ratio
+    (1.1 PFLOP/s tf32 against 2.25 bf16)."""
+    return peaks["bf16"] * 1.1 / 2.25
 
 
 def load_peaks():
@@ -705,16 +711,17 @@ def run_ours(args, rank, world, local_rank, dist):
                 "value": round(throughput(tokens * world, bw_ms) / 1e6, 3),
                 "unit": "Mtok/s/layer",
                 "launches_per_step": bw_launches,
-                "roofline": {"bound": "alu", "unit": "TFLOP/s",
+                "roofline": {"bound": "tensor", "unit": "TFLOP/s",
                              "achieved": round(bw_flops / (bw_ms * 1e-3) / 1e12, 3),
-                             "peak": round(FP32_FMA_TFLOPS, 1),
-                             "frac": round(bw_flops / (bw_ms * 1e-3) / 1e12 / FP32_FMA_TFLOPS, 4),
-                             "executed_flops_per_launch": bw_flops,
-                             "peak_source": "fp32 FMA of the CUDA cores: 152 SMs x 128 lanes "
-                                            "x 2 FLOP x 2.07 GHz"},
-                "path": "chunked form: forward re-run on the tensor cores (bf16 I/O) storing "
-                        "the chunk-start states, reverse state pass and chunk gradients on "
-                        "the CUDA cores in fp32",
+                             "peak": round(TF32_TFLOPS(peaks), 1),
+                             "frac": round(bw_flops / (bw_ms * 1e-3) / 1e12 / TF32_TFLOPS(peaks), 4),
+                             "executed_flops_per_call": bw_flops,
+                             "peak_source": f"tf32 dense = {peaks['src']} bf16 burst x 1.1 / 2.25 "
+                                            "(nominal tf32 : bf16)"},
+                "path": "chunked form: forward re-run (bf16 tensor cores) storing the "
+                        "chunk-start states, reverse state pass on the bf16 tensor cores, "
+                        "chunk-gradient GEMMs on the tf32 tensor cores, T and the C x C terms "
+                        "on the CUDA cores",
             },
             "layer_prefill": {
                 "workload": lcase.name + " (gdn_prefill_layer: projections in, y out)",
@@ -879,6 +886,23 @@ def run_profile(args):
         for _ in range(args.warmup + args.steps):
             gdn.prefill_backward(x["q"], x["k"], x["v"], x["alpha"], x["beta"], dout, x["S0"],
                                  dsf)
+    elif args.profile == "tgemm":
+        # the backward's tensor-core GEMM in its dO S shape (B' = S stored
+        # [dv][dk], read transposed; K = dv = 256, N = dk = 256) on 1500
+        # units: 384 MB of S, 96 MB each of dO and C
+        import ctypes
+        f = gdn.load().gdn_testing_tgemm
+        vp, i32, i64, fl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        f.argtypes = [vp, i64, i32, i32, vp, i64, i32, i32, vp, fl, vp, i64, i32, vp, i64, i32,
+                      i32, fl, i32, i64, vp]
+        units = 1500
+        A = torch.randn(units, 64, 256, device=dev)
+        B = torch.randn(units, 256, 256, device=dev)
+        C = torch.empty(units, 64, 256, device=dev)
+        st = torch.cuda.current_stream().cuda_stream
+        for _ in range(args.warmup + args.steps):
+            assert f(A.data_ptr(), 64 * 256, 256, 0, B.data_ptr(), 256 * 256, 256, 0, None, 0.0,
+                     C.data_ptr(), 64 * 256, 256, None, 0, 256, 256, 1.0, 0, units, st) == 0
     elif args.profile == "decode_layer":
         lc = gdn_inputs.layer_decode_256()
         lx = gdn_inputs.make_layer(lc, device=dev)
@@ -951,7 +975,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--profile", choices=["prefill", "decode", "layer", "backward", "decode_layer",
+    ap.add_argument("--profile", choices=["prefill", "decode", "layer", "backward", "tgemm",
+                                          "decode_layer",
                                           "prefill_64k", "prefill_fp32", "prefill_varlen8",
                                           "layer_fused"],
                     default=None,

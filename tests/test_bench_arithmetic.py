@@ -71,3 +71,5 @@ def test_backward_executed_flops():
 def test_fp32_fma_peak():
     assert bench.FP32_FMA_TFLOPS == pytest.approx(152 * 128 * 2 * 2.07e-3)
     assert bench.FP32_FMA_TFLOPS == pytest.approx(80.5, abs=0.05)
+    # the dense tf32 tensor peak scales the bf16 one by the nominal 1.1 / 2.25
+    assert bench.TF32_TFLOPS({"bf16": 2250.0}) == pytest.approx(1100.0)
