@@ -748,14 +748,16 @@ cudaError_t gemm(cudaStream_t st, bool tA, bool tB, Mat A, Mat B, float* C, size
 }
 
 // bf16 I/O: the tensor-core GEMM where its shapes allow (dv = 256), else
-// the CUDA-core one
+// the CUDA-core one.  b_tiled > 0: B is a unit of states in the tiled
+// layout, which only the tensor-core GEMM reads.
 cudaError_t gemm_io(int io_dtype, unsigned* status, cudaStream_t st, bool tA, bool tB, Mat A,
                     Mat B, float* C, size_t sC, int ldc, int N, int K, float alpha,
                     const float* Cin, float beta, int mask, const float* col, size_t sCol,
-                    int64_t batch) {
-  if (io_dtype == GDN_BF16 && tgemm_shape_ok(N, K, A.ld, B.ld, ldc, tA, tB))
+                    int64_t batch, int b_tiled = 0) {
+  if (io_dtype == GDN_BF16 && tgemm_shape_ok(N, K, A.ld, B.ld, ldc, tA, tB, b_tiled))
     return launch_tgemm(A.p, A.stride, A.ld, B.p, B.stride, B.ld, Cin, C, sC, ldc, col, sCol, N,
-                        K, alpha, beta, mask, batch, tA, tB, status, st);
+                        K, alpha, beta, mask, batch, tA, tB, b_tiled, status, st);
+  if (b_tiled) return cudaErrorInvalidValue;
   return gemm(st, tA, tB, A, B, C, sC, ldc, N, K, alpha, Cin, beta, mask, col, sCol, batch);
 }
 
@@ -895,12 +897,16 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
       {true, false, {s.Tm, CC, kC}, {s.dTm, CC, kC}, s.X, CC, kC, kC, kC, 1.f, nullptr, 0.f, 0, nullptr},
       {false, true, {s.X, CC, kC}, {s.Tm, CC, kC}, s.dA, CC, kC, kC, kC, -1.f, nullptr, 0.f, 2, nullptr},
   };
+  // bf16 I/O at dv = 256: the forward re-run and the reverse pass left the
+  // chunk states and dS' in the tiled layout
+  const bool tiled = io_dtype == GDN_BF16 && tiled_states(dv);
   for (int i = 0; i < (int)(sizeof list / sizeof list[0]); ++i) {
     // bf16 I/O: K dS'^T came from the reverse pass
     if (io_dtype == GDN_BF16 && list[i].C == s.KdS) continue;
     const G& g = list[i];
+    const int bt = tiled && (g.B.p == s.Sst || g.B.p == s.dSp) ? dv : 0;
     if ((e = gemm_io(io_dtype, a.status, st, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc, g.N, g.K, g.alpha, g.Cin, g.beta,
-                  g.mask, g.col, kC, units)) != cudaSuccess)
+                  g.mask, g.col, kC, units, bt)) != cudaSuccess)
       return e;
   }
   cc_kernel<<<(unsigned)units, kThreads, 0, st>>>(s);

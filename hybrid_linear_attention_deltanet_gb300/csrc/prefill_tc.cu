@@ -1170,10 +1170,19 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     if (it > 0) copy_out_prev(buf ^ 1);
     // (optional) this chunk's start state, for the backward's forward re-run
     if (sdump) {
-      float4* p = reinterpret_cast<float4*>(
-          sdump + ((size_t)(ci * H + h) * dv + 128 * slice + iloc) * kDK + 128 * colhalf);
+      const size_t v = 128 * slice + iloc;
+      float* base = sdump + (size_t)(ci * H + h) * dv * kDK;
+      if (tiled_states(dv)) {   // lanes: consecutive rows, 512 contiguous bytes a store
+        float4* p = reinterpret_cast<float4*>(base) + (size_t)32 * colhalf * dv + v;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) p[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+        for (int j = 0; j < 32; ++j)
+          p[(size_t)j * dv] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+      } else {
+        float4* p = reinterpret_cast<float4*>(base + v * kDK + 128 * colhalf);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          p[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+      }
     }
     // 2. U = U~ - D_U (columns r = 32 colhalf ..), and d_r U: bf16 A operands in TMEM
     float gC = 0.f;
@@ -1635,10 +1644,17 @@ tc_reverse_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       }
     }
     // dS' of this chunk (fp32), for the chunk gradients.  A warp holds 32
-    // rows; stored as they are, each 16-byte piece would be its own L2
+    // rows.  In the tiled layout (dv = 256) a store of the warp covers 512
+    // contiguous bytes; row-major, each 16-byte piece would be its own L2
     // transaction, so 16 columns at a time go through a per-warp tile in
     // shared memory and leave as four rows of 64 contiguous bytes per store.
-    {
+    if (tiled_states(dv)) {   // lanes: consecutive rows, 512 contiguous bytes a store
+      float4* p = reinterpret_cast<float4*>(dSp + u * dv * kDK) + (size_t)32 * colhalf * dv +
+                  dsp_row;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        p[(size_t)j * dv] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+    } else {
       float* tile = reinterpret_cast<float*>(sm + kR_T + warp * 2560);
       float* row0 = dSp + (u * dv + 128 * slice + 32 * quarter) * kDK + 128 * colhalf;
       const int rr = lane >> 2, c4 = lane & 3;

@@ -8,7 +8,10 @@
 //   C[m][n] = alpha * col[n] * sum_k A'[m][k] B'[k][n] + beta * Cin[m][n],
 //   m < 64, n < N (64 or 256), K = 64 or 256,
 // A' = A stored [64][K] or (kTA) [K][64]; B' = B stored [K][N] or (kTB)
-// [N][K]; mask 1 keeps n <= m, 2 keeps n < m.
+// [N][K]; mask 1 keeps n <= m, 2 keeps n < m.  B may instead be a unit in
+// the 4-column tiled layout of the backward's states (b_tiled = its row count
+// R: element (r, c) of the R x 256 matrix at ((c / 4) R + r) 4 + c % 4), with
+// B' = that matrix (kTB: B' = its transpose, R = N; otherwise R = K).
 //
 // The MMA computes the transpose D = C^T: its M rows are the n (blocks of 128;
 // N = 64 runs one block whose upper 64 rows are unused), its 64 columns the m,
@@ -41,6 +44,7 @@ struct TgArgs {
   int mask;
   int64_t batch;
   unsigned* status;
+  int b_tiled;   // 0: B as ldb says; R > 0: the tiled layout with R rows
 };
 
 template <int kNB>
@@ -102,12 +106,17 @@ __global__ void __launch_bounds__(kTgThreads, 2) tgemm_kernel(TgArgs g) {
     }
 #pragma unroll
     for (int j = 0; j < kXL; ++j) {
-      if (kTB) {    // row n of B, 16-byte piece q
-        const int e = tid + j * kTgThreads, n = e >> 3, q = e & 7;
-        rx[j] = __ldg(reinterpret_cast<const float4*>(B + (size_t)n * g.ldb + k0 + 4 * q));
+      if (kTB) {    // row n of B, 16-byte piece q (tiled: n fastest, 512 B a warp)
+        const int e = tid + j * kTgThreads;
+        const int n = g.b_tiled ? e % kNr : e >> 3, q = g.b_tiled ? e / kNr : e & 7;
+        const size_t o = g.b_tiled ? ((size_t)(k0 / 4 + q) * g.b_tiled + n) * 4
+                                   : (size_t)n * g.ldb + k0 + 4 * q;
+        rx[j] = __ldg(reinterpret_cast<const float4*>(B + o));
       } else {      // row k0 + lane of B, n = 4 (warp + 8 j) .. + 3
         const int n0 = 4 * (warp + 8 * j);
-        rx[j] = __ldg(reinterpret_cast<const float4*>(B + (size_t)(k0 + lane) * g.ldb + n0));
+        const size_t o = g.b_tiled ? ((size_t)(n0 / 4) * g.b_tiled + k0 + lane) * 4
+                                   : (size_t)(k0 + lane) * g.ldb + n0;
+        rx[j] = __ldg(reinterpret_cast<const float4*>(B + o));
       }
     }
   };
@@ -130,7 +139,8 @@ __global__ void __launch_bounds__(kTgThreads, 2) tgemm_kernel(TgArgs g) {
 #pragma unroll
     for (int j = 0; j < kXL; ++j) {
       if (kTB) {
-        const int e = tid + j * kTgThreads, n = e >> 3, q = e & 7;
+        const int e = tid + j * kTgThreads;
+        const int n = g.b_tiled ? e % kNr : e >> 3, q = g.b_tiled ? e / kNr : e & 7;
         *reinterpret_cast<float4*>(X + piece(n, q)) = rx[j];
       } else {
         const int n0 = 4 * (warp + 8 * j);
@@ -244,11 +254,15 @@ cudaError_t launch_nb(const TgArgs& g, bool tA, bool tB, cudaStream_t st) {
 
 }  // namespace
 
-bool tgemm_shape_ok(int N, int K, int lda, int ldb, int ldc, bool tA, bool tB) {
+bool tgemm_shape_ok(int N, int K, int lda, int ldb, int ldc, bool tA, bool tB, int b_tiled) {
   // 16-byte loads: leading dimensions and K multiples of 4
   if ((N != 64 && N != 256) || (K != 64 && K != 256)) return false;
-  if (lda % 4 || ldb % 4 || ldc < N) return false;
+  if (lda % 4 || ldc < N) return false;
   if (!tA ? lda < K : lda < 64) return false;
+  if (b_tiled) {   // an R x 256 tiled matrix: 256 columns, R = N (kTB) or K
+    return b_tiled == (tB ? N : K) && (tB ? K : N) == 256;
+  }
+  if (ldb % 4) return false;
   if (!tB ? ldb < N : ldb < K) return false;
   return true;
 }
@@ -256,11 +270,12 @@ bool tgemm_shape_ok(int N, int K, int lda, int ldb, int ldc, bool tA, bool tB) {
 cudaError_t launch_tgemm(const float* A, size_t sA, int lda, const float* B, size_t sB, int ldb,
                          const float* Cin, float* C, size_t sC, int ldc, const float* col,
                          size_t sCol, int N, int K, float alpha, float beta, int mask,
-                         int64_t batch, bool tA, bool tB, unsigned* status, cudaStream_t st) {
+                         int64_t batch, bool tA, bool tB, int b_tiled, unsigned* status,
+                         cudaStream_t st) {
   if (batch <= 0) return cudaSuccess;
-  if (!tgemm_shape_ok(N, K, lda, ldb, ldc, tA, tB)) return cudaErrorInvalidValue;
+  if (!tgemm_shape_ok(N, K, lda, ldb, ldc, tA, tB, b_tiled)) return cudaErrorInvalidValue;
   TgArgs g{A, sA, lda, B, sB, ldb, Cin, C, sC, ldc, col, sCol, N, K, alpha, beta, mask, batch,
-           status};
+           status, b_tiled};
   const cudaError_t e = N == 256 ? launch_nb<2>(g, tA, tB, st) : launch_nb<1>(g, tA, tB, st);
   count_launches(1);
   return e;
@@ -274,18 +289,20 @@ extern "C" int gdn_testing_tgemm(const float* A, int64_t sA, int32_t lda, int32_
                                  const float* B, int64_t sB, int32_t ldb, int32_t tB,
                                  const float* Cin, float beta, float* C, int64_t sC, int32_t ldc,
                                  const float* col, int64_t sCol, int32_t N, int32_t K,
-                                 float alpha, int32_t mask, int64_t batch, gdn_stream_t stream) {
+                                 float alpha, int32_t mask, int64_t batch, int32_t b_tiled,
+                                 gdn_stream_t stream) {
   if (!A || !B || !C || batch < 0 || sA < 0 || sB < 0 || sC < 0 || sCol < 0 || mask < 0 ||
       mask > 2)
     return GDN_ERR_INVALID_ARG;
-  if (!tgemm_shape_ok(N, K, lda, ldb, ldc, tA != 0, tB != 0)) return GDN_ERR_UNSUPPORTED;
+  if (b_tiled < 0 || !tgemm_shape_ok(N, K, lda, ldb, ldc, tA != 0, tB != 0, b_tiled))
+    return GDN_ERR_UNSUPPORTED;
   const uintptr_t al = (uintptr_t)A | (uintptr_t)B;
   if ((al & 15) || (sA % 4) || (sB % 4)) return GDN_ERR_ALIGNMENT;
   unsigned* status = status_ptr();
   if (!status) return GDN_ERR_CUDA;
   return launch_tgemm(A, (size_t)sA, lda, B, (size_t)sB, ldb, Cin, C, (size_t)sC, ldc, col,
-                      (size_t)sCol, N, K, alpha, beta, mask, batch, tA != 0, tB != 0, status,
-                      (cudaStream_t)stream) == cudaSuccess
+                      (size_t)sCol, N, K, alpha, beta, mask, batch, tA != 0, tB != 0, b_tiled,
+                      status, (cudaStream_t)stream) == cudaSuccess
              ? GDN_OK
              : GDN_ERR_CUDA;
 }

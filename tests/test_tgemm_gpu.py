@@ -20,19 +20,26 @@ def _fn(gdn_lib):
     f = gdn_lib.load().gdn_testing_tgemm
     vp, i32, i64, fl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
     f.argtypes = [vp, i64, i32, i32, vp, i64, i32, i32, vp, fl, vp, i64, i32, vp, i64, i32, i32,
-                  fl, i32, i64, vp]
+                  fl, i32, i64, i32, vp]
     f.restype = ctypes.c_int
     return f
 
 
+def _tile(M):
+    """[units][R][256] -> the tiled state layout: (r, c) at ((c / 4) R + r) 4 + c % 4."""
+    u, R, W = M.shape
+    return M.reshape(u, R, W // 4, 4).permute(0, 2, 1, 3).contiguous()
+
+
 def _run(gdn_lib, tA, tB, N, K, batch, alpha=1.0, beta=0.0, with_cin=False, with_col=False,
-         mask=0, seed=0):
+         mask=0, seed=0, tiled=False):
     g = torch.Generator().manual_seed(seed)
     A = torch.randn((batch, K, 64) if tA else (batch, 64, K), generator=g)
     B = torch.randn((batch, N, K) if tB else (batch, K, N), generator=g)
+    Bstore = _tile(B) if tiled else B
     Cin = torch.randn((batch, 64, N), generator=g) if with_cin else None
     col = torch.rand((batch, N), generator=g) + 0.5 if with_col else None
-    Ad, Bd = A.to(DEV), B.to(DEV)
+    Ad, Bd = A.to(DEV), Bstore.to(DEV)
     Cind = Cin.to(DEV) if Cin is not None else None
     cold = col.to(DEV) if col is not None else None
     C = torch.full((batch, 64, N), float("nan"), device=DEV)
@@ -40,7 +47,8 @@ def _run(gdn_lib, tA, tB, N, K, batch, alpha=1.0, beta=0.0, with_cin=False, with
                       B[0].numel(), B.shape[2], int(tB),
                       Cind.data_ptr() if Cind is not None else None, beta, C.data_ptr(),
                       64 * N, N, cold.data_ptr() if cold is not None else None, N, N, K, alpha,
-                      mask, batch, torch.cuda.current_stream().cuda_stream)
+                      mask, batch, B.shape[1] if tiled else 0,
+                      torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert rc == 0 and gdn_lib.device_status() == 0
     Ap = A.double().transpose(1, 2) if tA else A.double()
@@ -71,6 +79,19 @@ def test_tgemm_transpositions_and_shapes(gdn_lib, tA, tB, N, K):
     assert _run(gdn_lib, tA, tB, N, K, batch=37, seed=N + K + 2 * tA + tB) <= 2e-3
 
 
+@pytest.mark.parametrize("tB", [0, 1])
+def test_tgemm_tiled_state_operand(gdn_lib, tB):
+    """B in the backward's tiled state layout (the chunk states and dS' at
+    dv = 256): B' = the 256 x 256 matrix (dO S, -dU S, U dS') or its transpose
+    (U~ - W S^T, with alpha = -1 and Cin)."""
+    if tB:
+        err = _run(gdn_lib, 0, 1, 256, 256, batch=333, alpha=-1.0, beta=1.0, with_cin=True,
+                   seed=21, tiled=True)
+    else:
+        err = _run(gdn_lib, 0, 0, 256, 256, batch=333, seed=22, tiled=True)
+    assert err <= 2e-3
+
+
 def test_tgemm_many_units_epilogue_terms(gdn_lib):
     """700 units over at most 2 CTAs a SM: alpha, the column scale and
     beta * Cin (C = Cin in place is how the backward accumulates)."""
@@ -93,7 +114,7 @@ def test_tgemm_in_place_accumulate(gdn_lib):
     C0 = torch.randn((batch, 64, N), generator=g)
     Ad, Bd, Cd = A.to(DEV), B.to(DEV), C0.to(DEV)
     rc = _fn(gdn_lib)(Ad.data_ptr(), 64 * K, K, 0, Bd.data_ptr(), N * K, K, 1, Cd.data_ptr(), 1.0,
-                      Cd.data_ptr(), 64 * N, N, None, 0, N, K, 1.0, 0, batch,
+                      Cd.data_ptr(), 64 * N, N, None, 0, N, K, 1.0, 0, batch, 0,
                       torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert rc == 0 and gdn_lib.device_status() == 0
@@ -107,6 +128,8 @@ def test_tgemm_rejects_unsupported_shapes(gdn_lib):
     buf = torch.zeros(64 * 256, device=DEV)
     p = buf.data_ptr()
     s = torch.cuda.current_stream().cuda_stream
-    assert f(p, 0, 256, 0, p, 0, 128, 0, None, 0.0, p, 0, 128, None, 0, 128, 256, 1.0, 0, 1, s) != 0
-    assert f(p, 0, 130, 0, p, 0, 256, 0, None, 0.0, p, 0, 256, None, 0, 256, 128, 1.0, 0, 1, s) != 0
-    assert f(p, 0, 256, 0, p, 0, 256, 0, None, 0.0, p, 0, 256, None, 0, 256, 256, 1.0, 3, 1, s) != 0
+    assert f(p, 0, 256, 0, p, 0, 128, 0, None, 0.0, p, 0, 128, None, 0, 128, 256, 1.0, 0, 1, 0, s) != 0
+    assert f(p, 0, 130, 0, p, 0, 256, 0, None, 0.0, p, 0, 256, None, 0, 256, 128, 1.0, 0, 1, 0, s) != 0
+    assert f(p, 0, 256, 0, p, 0, 256, 0, None, 0.0, p, 0, 256, None, 0, 256, 256, 1.0, 3, 1, 0, s) != 0
+    # a tiled B must be 256 columns wide with R = K (or N when transposed)
+    assert f(p, 0, 64, 0, p, 0, 64, 0, None, 0.0, p, 0, 64, None, 0, 64, 64, 1.0, 0, 1, 64, s) != 0
