@@ -646,6 +646,18 @@ __global__ void __launch_bounds__(kThreads) cc_kernel(Bwd s) {
 }
 
 // ------------------------------------------------------------------ assemble
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+__device__ __forceinline__ void st4_out(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st4_out(__nv_bfloat16* p, float4 v) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 w;
+  w.x = *reinterpret_cast<const uint32_t*>(&lo);
+  w.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = w;
+}
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 assemble_kernel(const float* __restrict__ alpha, T* __restrict__ dq, T* __restrict__ dk,
@@ -666,23 +678,32 @@ assemble_kernel(const float* __restrict__ alpha, T* __restrict__ dq, T* __restri
     const float gam = expf(G[r]), d = expf(GL - G[r]);
     const float be = s.B[u * kC + r], bg = s.BG[u * kC + r];
     float kTdW = 0.f, qdQh = 0.f, vTdU = 0.f, dd = 0.f;
-    for (int c = lane; c < kDK; c += 32) {
+    // four consecutive columns a lane: 16-byte loads, 4-element stores
+    for (int c = 4 * lane; c < kDK; c += 128) {
       const size_t o = u * s.sD() + (size_t)r * kDK + c;
-      const float tdw = s.TdW[o], dqh = s.dQh[o];
-      kTdW = fmaf(s.K[o], tdw, kTdW);
-      qdQh = fmaf(s.Q[o], dqh, qdQh);
+      const float4 tdw = ld4(s.TdW + o), dqh = ld4(s.dQh + o);
+      kTdW += dot4(ld4(s.K + o), tdw);
+      qdQh += dot4(ld4(s.Q + o), dqh);
       if (r < L) {
         const size_t g = ((t0 + r) * H + h) * kDK + c;
-        st_out(dq + g, fmaf(kScale * gam, dqh, s.dQa[o]));
-        st_out(dk + g, fmaf(bg, tdw, fmaf(d, s.dK1[o], s.dKa[o])));
+        const float4 dqa = ld4(s.dQa + o), dk1 = ld4(s.dK1 + o), dka = ld4(s.dKa + o);
+        const float sg = kScale * gam;
+        st4_out(dq + g, make_float4(fmaf(sg, dqh.x, dqa.x), fmaf(sg, dqh.y, dqa.y),
+                                    fmaf(sg, dqh.z, dqa.z), fmaf(sg, dqh.w, dqa.w)));
+        st4_out(dk + g, make_float4(fmaf(bg, tdw.x, fmaf(d, dk1.x, dka.x)),
+                                    fmaf(bg, tdw.y, fmaf(d, dk1.y, dka.y)),
+                                    fmaf(bg, tdw.z, fmaf(d, dk1.z, dka.z)),
+                                    fmaf(bg, tdw.w, fmaf(d, dk1.w, dka.w))));
       }
     }
-    for (int c = lane; c < dv; c += 32) {
+    for (int c = 4 * lane; c < dv; c += 128) {
       const size_t o = u * s.sV() + (size_t)r * dv + c;
-      const float tdu = s.TdU[o];
-      vTdU = fmaf(s.V[o], tdu, vTdU);
-      dd = fmaf(s.U[o], s.KdS[o], dd);
-      if (r < L) st_out(dv_out + ((t0 + r) * H + h) * dv + c, be * tdu);
+      const float4 tdu = ld4(s.TdU + o);
+      vTdU += dot4(ld4(s.V + o), tdu);
+      dd += dot4(ld4(s.U + o), ld4(s.KdS + o));
+      if (r < L)
+        st4_out(dv_out + ((t0 + r) * H + h) * dv + c,
+                make_float4(be * tdu.x, be * tdu.y, be * tdu.z, be * tdu.w));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
