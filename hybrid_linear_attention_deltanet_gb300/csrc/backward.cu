@@ -104,6 +104,16 @@ size_t bwd_scratch_bytes(int64_t units, int32_t dv) {
 }
 
 // ------------------------------------------------------------------ gather
+// four consecutive input elements (8- or 16-byte aligned) as fp32
+__device__ __forceinline__ float4 ld4_in(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+__device__ __forceinline__ float4 ld4_in(const __nv_bfloat16* p) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 gather_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
@@ -116,17 +126,20 @@ gather_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
   int64_t t0 = 0;
   if (!map.locate(ci, n, t0, L)) L = 0;   // units past the last chunk stay all-zero
   const int dv = s.dv;
-  for (int e = tid; e < kC * kDK; e += kThreads) {
+  // four consecutive elements a thread (16-byte fp32 stores)
+  for (int e = 4 * tid; e < kC * kDK; e += 4 * kThreads) {
     const int r = e / kDK, c = e % kDK;
     const int64_t g = ((t0 + r) * H + h) * kDK + c;
-    s.Q[u * s.sD() + e] = r < L ? ld_in(q + g) : 0.f;
-    s.K[u * s.sD() + e] = r < L ? ld_in(k + g) : 0.f;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(s.Q + u * s.sD() + e) = r < L ? ld4_in(q + g) : z;
+    *reinterpret_cast<float4*>(s.K + u * s.sD() + e) = r < L ? ld4_in(k + g) : z;
   }
-  for (int e = tid; e < kC * dv; e += kThreads) {
+  for (int e = 4 * tid; e < kC * dv; e += 4 * kThreads) {
     const int r = e / dv, c = e % dv;
     const int64_t g = ((t0 + r) * H + h) * dv + c;
-    s.V[u * s.sV() + e] = r < L ? ld_in(v + g) : 0.f;
-    s.dO[u * s.sV() + e] = r < L ? ld_in(dout + g) : 0.f;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(s.V + u * s.sV() + e) = r < L ? ld4_in(v + g) : z;
+    *reinterpret_cast<float4*>(s.dO + u * s.sV() + e) = r < L ? ld4_in(dout + g) : z;
   }
   if (tid < 32) {   // G = cumsum(log alpha) by warp scan over two halves
     float carry = 0.f;
