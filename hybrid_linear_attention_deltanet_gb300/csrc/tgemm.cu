@@ -203,13 +203,24 @@ __global__ void __launch_bounds__(kTgThreads, 2) tgemm_kernel(TgArgs g) {
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) + col0, r);
         tmem_ld_wait();
+        // 16 rows at a time: Cin (which may be C itself) is read for all of
+        // them before any is written, so the loads are in flight together
+        // instead of each waiting behind the previous row's store
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int m = m0 + i;
-          float v = g.alpha * cs * __uint_as_float(r[i]);
-          if (cin) v = fmaf(g.beta, cin[(size_t)m * g.ldc], v);
-          if ((g.mask == 1 && n > m) || (g.mask == 2 && n >= m)) v = 0.f;
-          cout[(size_t)m * g.ldc] = v;
+        for (int i0 = 0; i0 < 32; i0 += 16) {
+          float cv[16];
+          if (cin) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) cv[i] = cin[(size_t)(m0 + i0 + i) * g.ldc];
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int m = m0 + i0 + i;
+            float v = g.alpha * cs * __uint_as_float(r[i0 + i]);
+            if (cin) v = fmaf(g.beta, cv[i], v);
+            if ((g.mask == 1 && n > m) || (g.mask == 2 && n >= m)) v = 0.f;
+            cout[(size_t)m * g.ldc] = v;
+          }
         }
       }
     }
