@@ -55,7 +55,7 @@ struct Bwd {
   float *KK, *QK, *Tm, *TmB, *TmU, *Ph;   // [64][64]
   float *W, *Ut;                  // [64][256] [64][dv]
   float *Sst, *dSp;               // [dv][256]
-  float *dU, *U, *KdS, *TdU;      // [64][dv]
+  float *dU, *U, *TdU;            // [64][dv]
   float *dQh, *dW, *dK1, *TdW, *dKa, *dQa;   // [64][256]
   float *dPh, *dTm, *X, *dA, *Ms, *FG;       // [64][64]
   float *dGc, *dBc;               // [64]
@@ -67,7 +67,7 @@ struct Bwd {
 
 size_t bwd_bytes_per_unit(int32_t dv) {
   const size_t D = (size_t)kC * kDK, V = (size_t)kC * dv, S = (size_t)dv * kDK;
-  return 4 * (2 * D + 2 * V + 3 * kC + 6 * kCC + D + V + 2 * S + 4 * V + 6 * D + 6 * kCC +
+  return 4 * (2 * D + 2 * V + 3 * kC + 6 * kCC + D + V + 2 * S + 3 * V + 6 * D + 6 * kCC +
               2 * kC + dv / kNS);
 }
 
@@ -88,7 +88,7 @@ Bwd carve(void* base, int64_t units, int32_t dv) {
   s.Ph = take(kCC);
   s.W = take(D); s.Ut = take(V);
   s.Sst = take(S); s.dSp = take(S);
-  s.dU = take(V); s.U = take(V); s.KdS = take(V); s.TdU = take(V);
+  s.dU = take(V); s.U = take(V); s.TdU = take(V);
   s.dQh = take(D); s.dW = take(D); s.dK1 = take(D); s.TdW = take(D); s.dKa = take(D);
   s.dQa = take(D);
   s.dPh = take(kCC); s.dTm = take(kCC); s.X = take(kCC); s.dA = take(kCC); s.Ms = take(kCC);
@@ -694,12 +694,14 @@ assemble_kernel(const float* __restrict__ alpha, T* __restrict__ dq, T* __restri
     // four consecutive columns a lane: 16-byte loads, 4-element stores
     for (int c = 4 * lane; c < kDK; c += 128) {
       const size_t o = u * s.sD() + (size_t)r * kDK + c;
-      const float4 tdw = ld4(s.TdW + o), dqh = ld4(s.dQh + o);
-      kTdW += dot4(ld4(s.K + o), tdw);
+      const float4 tdw = ld4(s.TdW + o), dqh = ld4(s.dQh + o), kk = ld4(s.K + o);
+      const float4 dk1 = ld4(s.dK1 + o);
+      kTdW += dot4(kk, tdw);
       qdQh += dot4(ld4(s.Q + o), dqh);
+      dd += dot4(kk, dk1);   // u_r . (dS' k_r) = k_r . (U dS')_r
       if (r < L) {
         const size_t g = ((t0 + r) * H + h) * kDK + c;
-        const float4 dqa = ld4(s.dQa + o), dk1 = ld4(s.dK1 + o), dka = ld4(s.dKa + o);
+        const float4 dqa = ld4(s.dQa + o), dka = ld4(s.dKa + o);
         const float sg = kScale * gam;
         st4_out(dq + g, make_float4(fmaf(sg, dqh.x, dqa.x), fmaf(sg, dqh.y, dqa.y),
                                     fmaf(sg, dqh.z, dqa.z), fmaf(sg, dqh.w, dqa.w)));
@@ -713,7 +715,6 @@ assemble_kernel(const float* __restrict__ alpha, T* __restrict__ dq, T* __restri
       const size_t o = u * s.sV() + (size_t)r * dv + c;
       const float4 tdu = ld4(s.TdU + o);
       vTdU += dot4(ld4(s.V + o), tdu);
-      dd += dot4(ld4(s.U + o), ld4(s.KdS + o));
       if (r < L)
         st4_out(dv_out + ((t0 + r) * H + h) * dv + c,
                 make_float4(be * tdu.x, be * tdu.y, be * tdu.z, be * tdu.w));
@@ -893,7 +894,6 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     r.dS0 = dS0;
     r.dSp = s.dSp;
     r.dU = s.dU;
-    r.KdS = s.KdS;
     r.status = a.status;
     if ((e = launch_reverse_tc(r, st)) != cudaSuccess) return e;
     if (units > 0) {
@@ -915,11 +915,11 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
   const G list[] = {
       // U = U~ - W S^T
       {false, true, {s.W, D, kDK}, {s.Sst, S, kDK}, s.U, V, dv, dv, kDK, -1.f, s.Ut, 1.f, 0, nullptr},
-      // dQh = dO S ; dW = -dU S ; dK1 = U dS' ; K dS'^T
+      // dQh = dO S ; dW = -dU S ; dK1 = U dS' (its rows dotted with k_r also
+      // give dd_r = u_r . (dS' k_r) in assemble)
       {false, false, {s.dO, V, dv}, {s.Sst, S, kDK}, s.dQh, D, kDK, kDK, dv, 1.f, nullptr, 0.f, 0, nullptr},
       {false, false, {s.dU, V, dv}, {s.Sst, S, kDK}, s.dW, D, kDK, kDK, dv, -1.f, nullptr, 0.f, 0, nullptr},
       {false, false, {s.U, V, dv}, {s.dSp, S, kDK}, s.dK1, D, kDK, kDK, dv, 1.f, nullptr, 0.f, 0, nullptr},
-      {false, true, {s.K, D, kDK}, {s.dSp, S, kDK}, s.KdS, V, dv, dv, kDK, 1.f, nullptr, 0.f, 0, nullptr},
       // dPh = lower(dO U^T)
       {false, true, {s.dO, V, dv}, {s.U, V, dv}, s.dPh, CC, kC, kC, dv, 1.f, nullptr, 0.f, 1, nullptr},
       // dT = (dW K^T) diag(beta gamma) + (dU V^T) diag(beta)
@@ -935,8 +935,6 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
   // chunk states and dS' in the tiled layout
   const bool tiled = io_dtype == GDN_BF16 && tiled_states(dv);
   for (int i = 0; i < (int)(sizeof list / sizeof list[0]); ++i) {
-    // bf16 I/O: K dS'^T came from the reverse pass
-    if (io_dtype == GDN_BF16 && list[i].C == s.KdS) continue;
     const G& g = list[i];
     const int bt = tiled && (g.B.p == s.Sst || g.B.p == s.dSp) ? dv : 0;
     if ((e = gemm_io(io_dtype, a.status, st, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc, g.N, g.K, g.alpha, g.Cin, g.beta,

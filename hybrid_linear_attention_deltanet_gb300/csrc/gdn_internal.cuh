@@ -298,8 +298,8 @@ cudaError_t scratch_free(void* p, cudaStream_t stream);
 // The backward's reverse state pass on the tensor cores (bf16 I/O): per
 // (sequence, head, 128-row slice of dS), over the chunks in reverse, from
 // dS_final (nullptr: zero) to dS0 (nullptr: not written); stores every
-// chunk's end-state gradient dS' ([chunks * H][dv][dk] fp32) and dU ([chunks *
-// H][64][dv] fp32).  images: the forward's per-chunk operand images over the
+// chunk's end-state gradient dS' ([chunks * H] units of dv x dk fp32, in the
+// tiled_states layout at dv = 256) and dU ([chunks * H][64][dv] fp32).  images: the forward's per-chunk operand images over the
 // same map; k, dout: the call's bf16 tensors.
 struct ReverseLaunch {
   const void* k = nullptr;
@@ -312,7 +312,6 @@ struct ReverseLaunch {
   float* dS0 = nullptr;
   float* dSp = nullptr;
   float* dU = nullptr;
-  float* KdS = nullptr;   // [chunks * H][64][dv]: K dS'^T of every chunk, or nullptr
   unsigned* status = nullptr;
 };
 cudaError_t launch_reverse_tc(const ReverseLaunch& r, cudaStream_t stream);

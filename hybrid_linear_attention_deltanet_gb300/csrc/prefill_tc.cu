@@ -1495,8 +1495,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 //   dS   = gamma_L dS' + dO^T Q^ - dU^T W          (the gradient carried back)
 // with P^, Q^, W and the decay factors read from the forward's own operand
 // images (the backward's forward re-run leaves them in scratch).  Per chunk:
-// MMA-X  D_X = dS' K^T, also stored as the chunk gradients' K dS'^T (A: the
-//        bf16 copy of dS' in TMEM, B: the K tile K-major, N = 64, 16 K-steps);
+// MMA-X  D_X = dS' K^T (A: the bf16 copy of dS' in TMEM, B: the K tile
+//        K-major, N = 64, 16 K-steps);
 // MMA-P  D_P = dO^T P^ (A: the dO tile MN-major, B: P^ read MN-major, N = 64);
 // E1     dU^T = D_P + d D_X -> fp32 dU to scratch, -dU^T as a bf16 A operand
 //        in TMEM over D_X;
@@ -1519,8 +1519,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 tc_reverse_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_o,
                   SeqMap map, int32_t H, int32_t dv, const uint8_t* __restrict__ images,
                   const float* __restrict__ dS_final, float* __restrict__ dS0,
-                  float* __restrict__ dSp, float* __restrict__ dUo, float* __restrict__ kds,
-                  unsigned* status) {
+                  float* __restrict__ dSp, float* __restrict__ dUo, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align_smem_1024(smem_raw);
   const int ns = dv / 128;
@@ -1688,7 +1687,6 @@ tc_reverse_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       tmem_ld_wait();
       uint32_t pk[16];
       float* du_out = dUo + (u * kC + 32 * colhalf) * dv + dsp_row;
-      float* kds_out = kds ? kds + (u * kC + 32 * colhalf) * dv + dsp_row : nullptr;
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         const int r = 32 * colhalf + j;
@@ -1696,10 +1694,6 @@ tc_reverse_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         const float d1 = fmaf(sD[r + 1], __uint_as_float(gx[j + 1]), __uint_as_float(gp[j + 1]));
         du_out[(size_t)j * dv] = d0;
         du_out[(size_t)(j + 1) * dv] = d1;
-        if (kds_out) {   // K dS'^T of the chunk, for the chunk gradients
-          kds_out[(size_t)j * dv] = __uint_as_float(gx[j]);
-          kds_out[(size_t)(j + 1) * dv] = __uint_as_float(gx[j + 1]);
-        }
         pk[j >> 1] = pack_bf16(-d0, -d1);
       }
       tmem_st16(tmem + lane_off + kR_TX + 32 * colhalf, pk);
@@ -1999,7 +1993,7 @@ cudaError_t launch_reverse_tc(const ReverseLaunch& r, cudaStream_t stream) {
                                        (int)kRevSmemTc);
   if (e != cudaSuccess) return e;
   tc_reverse_kernel<<<(unsigned)n_blocks, kStateThreads, kRevSmemTc, stream>>>(
-      tk, to, r.map, r.H, r.dv, r.images, r.dS_final, r.dS0, r.dSp, r.dU, r.KdS, r.status);
+      tk, to, r.map, r.H, r.dv, r.images, r.dS_final, r.dS0, r.dSp, r.dU, r.status);
   count_launches(1);
   return cudaGetLastError();
 }

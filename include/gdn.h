@@ -233,7 +233,7 @@ int gdn_prefill_scan_ws(const void* q, const void* k, const void* v, const float
  *
  * Scratch: stream-ordered from the library's pool, about 1.7 MiB per
  * (chunk of 64 tokens, head) at dv = 256, plus with bf16 I/O the forward's own
- * scratch and a throwaway output (about 5.9 GB in all for 32K tokens of a
+ * scratch and a throwaway output (about 5.7 GB in all for 32K tokens of a
  * 6-head layer).
  */
 int gdn_prefill_backward(const void* q, const void* k, const void* v, const float* alpha,
