@@ -815,9 +815,8 @@ static_assert(3 * (kFwdSmem + 1024) <= 228 * 1024 && 3 * (kRevSmem + 1024) <= 22
 size_t prefill_backward_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv, int64_t T_total,
                                       int io_dtype) {
   size_t b = align_up(bwd_scratch_bytes(max_chunks * H, dv), 1024);
-  if (io_dtype == GDN_BF16)
-    b += align_up(prefill_tc_scratch_bytes(max_chunks, H, dv), 1024) +
-         align_up((size_t)T_total * H * dv * 2, 1024);
+  (void)T_total;
+  if (io_dtype == GDN_BF16) b += align_up(prefill_tc_scratch_bytes(max_chunks, H, dv), 1024);
   return b;
 }
 
@@ -865,11 +864,12 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
   const dim3 gs((unsigned)a.map.N, (unsigned)a.H, (unsigned)(dv / kNS));
   if (io_dtype == GDN_BF16) {
     // chunk-start states from the tensor-core forward (bf16 operands, fp32
-    // state), its output discarded
+    // state), without outputs: its state units then load W alone (no Q^ or
+    // P^) and skip the output products
     char* extra = (char*)a.scratch + align_up(bwd_scratch_bytes(units, dv), 1024);
     PrefillLaunch f = a;
     f.scratch = extra;
-    f.out = extra + align_up(prefill_tc_scratch_bytes(a.max_chunks, a.H, dv), 1024);
+    f.out = nullptr;
     f.S_final = nullptr;
     f.allow_overlap = true;
     f.state_dump = s.Sst;

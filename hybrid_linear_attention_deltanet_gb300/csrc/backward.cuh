@@ -6,9 +6,10 @@
 
 namespace gdn {
 
-// Device scratch the backward of a call with this many chunks (and T_total
-// tokens) needs.  With bf16 I/O it includes the tensor-core forward's scratch
-// and a throwaway output: that forward re-run stores every chunk's start state.
+// Device scratch the backward of a call with this many chunks needs (T_total
+// is unused).  With bf16 I/O it includes the tensor-core forward's scratch:
+// that forward re-run stores every chunk's start state and leaves the
+// per-chunk operand images the reverse pass reads.
 size_t prefill_backward_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv, int64_t T_total,
                                       int io_dtype);
 

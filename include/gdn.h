@@ -228,13 +228,15 @@ int gdn_prefill_scan_ws(const void* q, const void* k, const void* v, const float
  * cu_seqlens and alignment as in gdn_prefill; dout has the layout and dtype of
  * out.  No output may overlap an input or another output.  Arithmetic: with
  * bf16 I/O the chunk-start states come from the tensor-core forward of
- * gdn_prefill (bf16 operands, fp32 accumulation and state); with fp32 I/O from
- * an fp32 CUDA-core pass; everything else is fp32 on the CUDA cores.
+ * gdn_prefill (bf16 operands, fp32 accumulation and state), the reverse state
+ * pass runs on the tensor cores in the same way (bf16 operands, fp32
+ * accumulation and state gradient) and the chunk-gradient products as tf32
+ * tensor-core GEMMs on fp32 operands (fp32 accumulation); with fp32 I/O
+ * everything runs in fp32 on the CUDA cores.
  *
- * Scratch: stream-ordered from the library's pool, about 1.7 MiB per
+ * Scratch: stream-ordered from the library's pool, about 1.6 MiB per
  * (chunk of 64 tokens, head) at dv = 256, plus with bf16 I/O the forward's own
- * scratch and a throwaway output (about 5.7 GB in all for 32K tokens of a
- * 6-head layer).
+ * scratch (about 5.6 GB in all for 32K tokens of a 6-head layer).
  */
 int gdn_prefill_backward(const void* q, const void* k, const void* v, const float* alpha,
                          const float* beta, const float* S0, const int32_t* cu_seqlens,
