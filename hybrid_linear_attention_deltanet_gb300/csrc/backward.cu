@@ -33,6 +33,8 @@
 //               Rows of dS are independent exactly as rows of S are.
 //   then batched 64-row GEMMs and three per-chunk elementwise kernels for the
 //   local gradients, and a final scatter into the token layout.
+#include <mutex>
+
 #include "backward.cuh"
 
 namespace gdn {
@@ -820,6 +822,30 @@ size_t prefill_backward_scratch_bytes(int64_t max_chunks, int32_t H, int32_t dv,
   return b;
 }
 
+// A stream of the greatest priority per device for the reverse state pass,
+// created on first use (nullptr if that fails: the call then stays on the
+// caller's stream).  Its 48-odd CTAs each take a whole SM; the priority puts
+// them on their SMs before the concurrent chunk-gradient work fills the rest.
+cudaStream_t reverse_stream() {
+  static cudaStream_t streams[64] = {};
+  static bool tried[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!tried[dev]) {
+    tried[dev] = true;
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&streams[dev], cudaStreamNonBlocking, greatest) !=
+            cudaSuccess) {
+      streams[dev] = nullptr;
+      (void)cudaGetLastError();
+    }
+  }
+  return streams[dev];
+}
+
 cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
                                     const float* dS_final, void* dq, void* dk, void* dv_out,
                                     float* dalpha, float* dbeta, float* dS0, int io_dtype,
@@ -835,33 +861,78 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
                                 (int)kRevSmem)) != cudaSuccess)
     return e;
   const dim3 gu((unsigned)a.max_chunks, (unsigned)a.H);
-  if (units > 0) {
+  const dim3 gs((unsigned)a.map.N, (unsigned)a.H, (unsigned)(dv / kNS));
+  const size_t D = s.sD(), V = s.sV(), S = s.sS(), CC = kCC;
+  struct G {
+    bool tA, tB; Mat A, B; float* C; size_t sC; int ldc, N, K; float alpha;
+    const float* Cin; float beta; int mask; const float* col;
+  };
+  // bf16 I/O at dv = 256: the forward re-run and the reverse pass leave the
+  // chunk states and dS' in the tiled layout
+  const bool tiled = io_dtype == GDN_BF16 && tiled_states(dv);
+  auto run = [&](const G* list, int n, cudaStream_t q) -> cudaError_t {
+    for (int i = 0; i < n; ++i) {
+      const G& g = list[i];
+      const int bt = tiled && (g.B.p == s.Sst || g.B.p == s.dSp) ? dv : 0;
+      const cudaError_t r = gemm_io(io_dtype, a.status, q, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc,
+                                    g.N, g.K, g.alpha, g.Cin, g.beta, g.mask, g.col, kC, units, bt);
+      if (r != cudaSuccess) return r;
+    }
+    return cudaSuccess;
+  };
+  // the per-chunk factors: q, k, v, dO tiles, KK^T, QK^T, T, P^, W, U~
+  auto local_factors = [&](cudaStream_t q) -> cudaError_t {
     if (io_dtype == GDN_BF16)
-      gather_kernel<__nv_bfloat16><<<gu, kThreads, 0, st>>>(
+      gather_kernel<__nv_bfloat16><<<gu, kThreads, 0, q>>>(
           (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
           (const __nv_bfloat16*)dout, a.alpha, a.beta, a.map, a.H, s);
     else
-      gather_kernel<float><<<gu, kThreads, 0, st>>>((const float*)a.q, (const float*)a.k,
-                                                     (const float*)a.v, (const float*)dout,
-                                                     a.alpha, a.beta, a.map, a.H, s);
+      gather_kernel<float><<<gu, kThreads, 0, q>>>((const float*)a.q, (const float*)a.k,
+                                                    (const float*)a.v, (const float*)dout,
+                                                    a.alpha, a.beta, a.map, a.H, s);
     count_launches(1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t D = s.sD(), V = s.sV(), CC = kCC;
-    // KK^T and QK^T
-    if ((e = gemm_io(io_dtype, a.status, st, false, true, {s.K, D, kDK}, {s.K, D, kDK}, s.KK, CC, kC, kC, kDK, 1.f,
-                  nullptr, 0.f, 0, nullptr, 0, units)) != cudaSuccess) return e;
-    if ((e = gemm_io(io_dtype, a.status, st, false, true, {s.Q, D, kDK}, {s.K, D, kDK}, s.QK, CC, kC, kC, kDK, 1.f,
-                  nullptr, 0.f, 0, nullptr, 0, units)) != cudaSuccess) return e;
-    tprep_kernel<<<(unsigned)units, kThreads, 0, st>>>(s);
+    cudaError_t r = cudaGetLastError();
+    if (r != cudaSuccess) return r;
+    const G f1[] = {
+        {false, true, {s.K, D, kDK}, {s.K, D, kDK}, s.KK, CC, kC, kC, kDK, 1.f, nullptr, 0.f, 0, nullptr},
+        {false, true, {s.Q, D, kDK}, {s.K, D, kDK}, s.QK, CC, kC, kC, kDK, 1.f, nullptr, 0.f, 0, nullptr},
+    };
+    if ((r = run(f1, 2, q)) != cudaSuccess) return r;
+    tprep_kernel<<<(unsigned)units, kThreads, 0, q>>>(s);
     count_launches(1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((r = cudaGetLastError()) != cudaSuccess) return r;
     // W = T diag(beta gamma) K, U~ = T diag(beta) V
-    if ((e = gemm_io(io_dtype, a.status, st, false, false, {s.TmB, CC, kC}, {s.K, D, kDK}, s.W, D, kDK, kDK, kC, 1.f,
-                  nullptr, 0.f, 0, nullptr, 0, units)) != cudaSuccess) return e;
-    if ((e = gemm_io(io_dtype, a.status, st, false, false, {s.TmU, CC, kC}, {s.V, V, dv}, s.Ut, V, dv, dv, kC, 1.f,
-                  nullptr, 0.f, 0, nullptr, 0, units)) != cudaSuccess) return e;
-  }
-  const dim3 gs((unsigned)a.map.N, (unsigned)a.H, (unsigned)(dv / kNS));
+    const G f2[] = {
+        {false, false, {s.TmB, CC, kC}, {s.K, D, kDK}, s.W, D, kDK, kDK, kC, 1.f, nullptr, 0.f, 0, nullptr},
+        {false, false, {s.TmU, CC, kC}, {s.V, V, dv}, s.Ut, V, dv, dv, kC, 1.f, nullptr, 0.f, 0, nullptr},
+    };
+    return run(f2, 2, q);
+  };
+  // the chunk products that need no reverse-pass output ...
+  const G pre[] = {
+      // U = U~ - W S^T
+      {false, true, {s.W, D, kDK}, {s.Sst, S, kDK}, s.U, V, dv, dv, kDK, -1.f, s.Ut, 1.f, 0, nullptr},
+      // dQh = dO S ; dPh = lower(dO U^T)
+      {false, false, {s.dO, V, dv}, {s.Sst, S, kDK}, s.dQh, D, kDK, kDK, dv, 1.f, nullptr, 0.f, 0, nullptr},
+      {false, true, {s.dO, V, dv}, {s.U, V, dv}, s.dPh, CC, kC, kC, dv, 1.f, nullptr, 0.f, 1, nullptr},
+  };
+  // ... and those that do
+  const G post[] = {
+      // dW = -dU S ; dK1 = U dS' (its rows dotted with k_r also give
+      // dd_r = u_r . (dS' k_r) in assemble)
+      {false, false, {s.dU, V, dv}, {s.Sst, S, kDK}, s.dW, D, kDK, kDK, dv, -1.f, nullptr, 0.f, 0, nullptr},
+      {false, false, {s.U, V, dv}, {s.dSp, S, kDK}, s.dK1, D, kDK, kDK, dv, 1.f, nullptr, 0.f, 0, nullptr},
+      // dT = (dW K^T) diag(beta gamma) + (dU V^T) diag(beta)
+      {false, true, {s.dW, D, kDK}, {s.K, D, kDK}, s.dTm, CC, kC, kC, kDK, 1.f, nullptr, 0.f, 0, s.BG},
+      {false, true, {s.dU, V, dv}, {s.V, V, dv}, s.dTm, CC, kC, kC, dv, 1.f, s.dTm, 1.f, 0, s.B},
+      // T^T dW, T^T dU, dA = -(T^T dT) T^T strictly lower
+      {true, false, {s.Tm, CC, kC}, {s.dW, D, kDK}, s.TdW, D, kDK, kDK, kC, 1.f, nullptr, 0.f, 0, nullptr},
+      {true, false, {s.Tm, CC, kC}, {s.dU, V, dv}, s.TdU, V, dv, dv, kC, 1.f, nullptr, 0.f, 0, nullptr},
+      {true, false, {s.Tm, CC, kC}, {s.dTm, CC, kC}, s.X, CC, kC, kC, kC, 1.f, nullptr, 0.f, 0, nullptr},
+      {false, true, {s.X, CC, kC}, {s.Tm, CC, kC}, s.dA, CC, kC, kC, kC, -1.f, nullptr, 0.f, 2, nullptr},
+  };
+  constexpr int kPre = sizeof pre / sizeof pre[0], kPost = sizeof post / sizeof post[0];
+
   if (io_dtype == GDN_BF16) {
     // chunk-start states from the tensor-core forward (bf16 operands, fp32
     // state), without outputs: its state units then load W alone (no Q^ or
@@ -874,14 +945,10 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     f.allow_overlap = true;
     f.state_dump = s.Sst;
     if ((e = launch_prefill_tc(f, st)) != cudaSuccess) return e;
-  } else {
-    fwd_states_kernel<<<gs, kThreads, kFwdSmem, st>>>(a.S0, a.map, a.H, s);
-    count_launches(1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  if (io_dtype == GDN_BF16) {
     // the reverse pass on the tensor cores, on the forward re-run's operand
-    // images; then the <dS', S_start> partials in parallel
+    // images, on the high-priority stream; meanwhile, on the caller's
+    // stream, the per-chunk factors and the products that need no reverse
+    // output use the SMs the reverse pass leaves free
     ReverseLaunch r;
     r.k = a.k;
     r.dout = dout;
@@ -889,58 +956,55 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     r.H = a.H;
     r.dv = dv;
     r.T_total = a.map.cu_seqlens ? a.map.T : (int64_t)a.map.N * a.map.T;
-    r.images = (const uint8_t*)a.scratch + align_up(bwd_scratch_bytes(units, dv), 1024);
+    r.images = (const uint8_t*)extra;
     r.dS_final = dS_final;
     r.dS0 = dS0;
     r.dSp = s.dSp;
     r.dU = s.dU;
     r.status = a.status;
-    if ((e = launch_reverse_tc(r, st)) != cudaSuccess) return e;
-    if (units > 0) {
-      dgl_kernel<<<dim3((unsigned)units, (unsigned)(dv / kNS)), kThreads, 0, st>>>(s);
-      count_launches(1);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cudaStream_t rs = units > 0 ? reverse_stream() : nullptr;
+    cudaEvent_t ev_fwd = nullptr, ev_rev = nullptr;
+    if (rs && (cudaEventCreateWithFlags(&ev_fwd, cudaEventDisableTiming) != cudaSuccess ||
+               cudaEventCreateWithFlags(&ev_rev, cudaEventDisableTiming) != cudaSuccess)) {
+      if (ev_fwd) cudaEventDestroy(ev_fwd);
+      ev_fwd = nullptr;
+      rs = nullptr;
+      (void)cudaGetLastError();
     }
+    if (!rs) {   // one stream, in dependency order
+      if ((e = launch_reverse_tc(r, st)) != cudaSuccess) return e;
+      if (units == 0) return cudaSuccess;
+      if ((e = local_factors(st)) != cudaSuccess) return e;
+      if ((e = run(pre, kPre, st)) != cudaSuccess) return e;
+    } else {
+      e = cudaEventRecord(ev_fwd, st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(rs, ev_fwd, 0);
+      if (e == cudaSuccess) e = launch_reverse_tc(r, rs);
+      if (e == cudaSuccess) e = cudaEventRecord(ev_rev, rs);
+      if (e == cudaSuccess) e = local_factors(st);
+      if (e == cudaSuccess) e = run(pre, kPre, st);
+      const cudaError_t ew = cudaStreamWaitEvent(st, ev_rev, 0);   // join
+      cudaEventDestroy(ev_fwd);
+      cudaEventDestroy(ev_rev);
+      if (e == cudaSuccess) e = ew;
+      if (e != cudaSuccess) return e;
+    }
+    // <dS', S_start> partials
+    dgl_kernel<<<dim3((unsigned)units, (unsigned)(dv / kNS)), kThreads, 0, st>>>(s);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   } else {
+    if (units > 0 && (e = local_factors(st)) != cudaSuccess) return e;
+    fwd_states_kernel<<<gs, kThreads, kFwdSmem, st>>>(a.S0, a.map, a.H, s);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     rev_states_kernel<<<gs, kThreads, kRevSmem, st>>>(dS_final, dS0, a.map, a.H, s);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (units == 0) return cudaSuccess;
+    if ((e = run(pre, kPre, st)) != cudaSuccess) return e;
   }
-  if (units == 0) return cudaSuccess;
-  const size_t D = s.sD(), V = s.sV(), S = s.sS(), CC = kCC;
-  struct G {
-    bool tA, tB; Mat A, B; float* C; size_t sC; int ldc, N, K; float alpha;
-    const float* Cin; float beta; int mask; const float* col;
-  };
-  const G list[] = {
-      // U = U~ - W S^T
-      {false, true, {s.W, D, kDK}, {s.Sst, S, kDK}, s.U, V, dv, dv, kDK, -1.f, s.Ut, 1.f, 0, nullptr},
-      // dQh = dO S ; dW = -dU S ; dK1 = U dS' (its rows dotted with k_r also
-      // give dd_r = u_r . (dS' k_r) in assemble)
-      {false, false, {s.dO, V, dv}, {s.Sst, S, kDK}, s.dQh, D, kDK, kDK, dv, 1.f, nullptr, 0.f, 0, nullptr},
-      {false, false, {s.dU, V, dv}, {s.Sst, S, kDK}, s.dW, D, kDK, kDK, dv, -1.f, nullptr, 0.f, 0, nullptr},
-      {false, false, {s.U, V, dv}, {s.dSp, S, kDK}, s.dK1, D, kDK, kDK, dv, 1.f, nullptr, 0.f, 0, nullptr},
-      // dPh = lower(dO U^T)
-      {false, true, {s.dO, V, dv}, {s.U, V, dv}, s.dPh, CC, kC, kC, dv, 1.f, nullptr, 0.f, 1, nullptr},
-      // dT = (dW K^T) diag(beta gamma) + (dU V^T) diag(beta)
-      {false, true, {s.dW, D, kDK}, {s.K, D, kDK}, s.dTm, CC, kC, kC, kDK, 1.f, nullptr, 0.f, 0, s.BG},
-      {false, true, {s.dU, V, dv}, {s.V, V, dv}, s.dTm, CC, kC, kC, dv, 1.f, s.dTm, 1.f, 0, s.B},
-      // T^T dW, T^T dU, dA = -(T^T dT) T^T strictly lower
-      {true, false, {s.Tm, CC, kC}, {s.dW, D, kDK}, s.TdW, D, kDK, kDK, kC, 1.f, nullptr, 0.f, 0, nullptr},
-      {true, false, {s.Tm, CC, kC}, {s.dU, V, dv}, s.TdU, V, dv, dv, kC, 1.f, nullptr, 0.f, 0, nullptr},
-      {true, false, {s.Tm, CC, kC}, {s.dTm, CC, kC}, s.X, CC, kC, kC, kC, 1.f, nullptr, 0.f, 0, nullptr},
-      {false, true, {s.X, CC, kC}, {s.Tm, CC, kC}, s.dA, CC, kC, kC, kC, -1.f, nullptr, 0.f, 2, nullptr},
-  };
-  // bf16 I/O at dv = 256: the forward re-run and the reverse pass left the
-  // chunk states and dS' in the tiled layout
-  const bool tiled = io_dtype == GDN_BF16 && tiled_states(dv);
-  for (int i = 0; i < (int)(sizeof list / sizeof list[0]); ++i) {
-    const G& g = list[i];
-    const int bt = tiled && (g.B.p == s.Sst || g.B.p == s.dSp) ? dv : 0;
-    if ((e = gemm_io(io_dtype, a.status, st, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc, g.N, g.K, g.alpha, g.Cin, g.beta,
-                  g.mask, g.col, kC, units, bt)) != cudaSuccess)
-      return e;
-  }
+  if ((e = run(post, kPost, st)) != cudaSuccess) return e;
   cc_kernel<<<(unsigned)units, kThreads, 0, st>>>(s);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -950,10 +1014,7 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
       {true, false, {s.FG, CC, kC}, {s.Q, D, kDK}, s.dKa, D, kDK, kDK, kC, 1.f, s.dKa, 1.f, 0, nullptr},
       {false, false, {s.FG, CC, kC}, {s.K, D, kDK}, s.dQa, D, kDK, kDK, kC, 1.f, nullptr, 0.f, 0, nullptr},
   };
-  for (const G& g : list2)
-    if ((e = gemm_io(io_dtype, a.status, st, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc, g.N, g.K, g.alpha, g.Cin, g.beta,
-                  g.mask, g.col, kC, units)) != cudaSuccess)
-      return e;
+  if ((e = run(list2, 3, st)) != cudaSuccess) return e;
   if (io_dtype == GDN_BF16)
     assemble_kernel<__nv_bfloat16><<<gu, kThreads, 0, st>>>(
         a.alpha, (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv_out, dalpha, dbeta,
