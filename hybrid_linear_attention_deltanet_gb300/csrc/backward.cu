@@ -285,12 +285,16 @@ __global__ void __launch_bounds__(kThreads) bgemm_kernel(BG g) {
 
 // ------------------------------------------------------------------ prep: T, Ph
 __global__ void __launch_bounds__(kThreads) tprep_kernel(Bwd s) {
-  __shared__ float As[kC][kC + 1];
+  __shared__ __align__(16) float As[kC][kC + 4];   // 16-byte rows: read 4 at a time
   __shared__ float Ts[kC][kC + 1];
-  __shared__ float Gs[kC], Bs[kC];
+  __shared__ float Gs[kC], Bs[kC], BGs[kC];
   const int64_t u = blockIdx.x;
   const int tid = threadIdx.x;
-  if (tid < kC) { Gs[tid] = s.G[u * kC + tid]; Bs[tid] = s.B[u * kC + tid]; }
+  if (tid < kC) {
+    Gs[tid] = s.G[u * kC + tid];
+    Bs[tid] = s.B[u * kC + tid];
+    BGs[tid] = Bs[tid] * expf(Gs[tid]);   // beta_j gamma_j
+  }
   __syncthreads();
   for (int e = tid; e < kCC; e += kThreads) {
     const int r = e >> 6, j = e & 63;
@@ -300,21 +304,35 @@ __global__ void __launch_bounds__(kThreads) tprep_kernel(Bwd s) {
   }
   __syncthreads();
   if (tid < kC) {   // (I + A)^-1 by forward substitution, one column per thread
+    // column c in registers; row r's sum over j < r in four partial sums
+    // (A is strictly lower, so the terms j >= r a float4 rounds up to are 0)
     const int c = tid;
-    for (int r = 0; r < kC; ++r) Ts[r][c] = r == c ? 1.f : 0.f;
+    float x[kC];
+#pragma unroll
+    for (int r = 0; r < kC; ++r) x[r] = r == c ? 1.f : 0.f;
+#pragma unroll
     for (int r = 1; r < kC; ++r) {
-      float acc = 0.f;
-      for (int j = c; j < r; ++j) acc = fmaf(As[r][j], Ts[j][c], acc);
-      if (r > c) Ts[r][c] = -acc;
+      float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+      for (int j4 = 0; j4 < r; j4 += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(&As[r][j4]);
+        p0 = fmaf(a.x, x[j4], p0);
+        p1 = fmaf(a.y, x[j4 + 1], p1);
+        p2 = fmaf(a.z, x[j4 + 2], p2);
+        p3 = fmaf(a.w, x[j4 + 3], p3);
+      }
+      if (r > c) x[r] = -((p0 + p1) + (p2 + p3));
     }
-    s.BG[u * kC + c] = Bs[c] * expf(Gs[c]);
+#pragma unroll
+    for (int r = 0; r < kC; ++r) Ts[r][c] = x[r];
+    s.BG[u * kC + c] = BGs[c];
   }
   __syncthreads();
   for (int e = tid; e < kCC; e += kThreads) {
     const int r = e >> 6, j = e & 63;
     const float t = Ts[r][j];
     s.Tm[u * kCC + e] = t;
-    s.TmB[u * kCC + e] = t * Bs[j] * expf(Gs[j]);
+    s.TmB[u * kCC + e] = t * BGs[j];
     s.TmU[u * kCC + e] = t * Bs[j];
   }
 }
