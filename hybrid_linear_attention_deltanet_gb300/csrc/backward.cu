@@ -962,11 +962,12 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     f.S_final = nullptr;
     f.allow_overlap = true;
     f.state_dump = s.Sst;
-    if ((e = launch_prefill_tc(f, st)) != cudaSuccess) return e;
-    // the reverse pass on the tensor cores, on the forward re-run's operand
-    // images, on the high-priority stream; meanwhile, on the caller's
-    // stream, the per-chunk factors and the products that need no reverse
-    // output use the SMs the reverse pass leaves free
+    // the forward re-run and then the reverse pass on the tensor cores (on
+    // the re-run's operand images) go to the high-priority stream; on the
+    // caller's stream meanwhile, the per-chunk factors take the SMs the
+    // re-run's per-chunk workers release once done, then (after the re-run)
+    // the products that need no reverse output take those the reverse pass
+    // leaves free
     ReverseLaunch r;
     r.k = a.k;
     r.dout = dout;
@@ -981,29 +982,34 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     r.dU = s.dU;
     r.status = a.status;
     cudaStream_t rs = units > 0 ? reverse_stream() : nullptr;
-    cudaEvent_t ev_fwd = nullptr, ev_rev = nullptr;
-    if (rs && (cudaEventCreateWithFlags(&ev_fwd, cudaEventDisableTiming) != cudaSuccess ||
-               cudaEventCreateWithFlags(&ev_rev, cudaEventDisableTiming) != cudaSuccess)) {
-      if (ev_fwd) cudaEventDestroy(ev_fwd);
-      ev_fwd = nullptr;
-      rs = nullptr;
-      (void)cudaGetLastError();
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};   // inputs ready, re-run done, reverse done
+    for (int i = 0; rs && i < 3; ++i) {
+      if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
+        for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+        rs = nullptr;
+        (void)cudaGetLastError();
+      }
     }
     if (!rs) {   // one stream, in dependency order
+      if ((e = launch_prefill_tc(f, st)) != cudaSuccess) return e;
       if ((e = launch_reverse_tc(r, st)) != cudaSuccess) return e;
       if (units == 0) return cudaSuccess;
       if ((e = local_factors(st)) != cudaSuccess) return e;
       if ((e = run(pre, kPre, st)) != cudaSuccess) return e;
     } else {
-      e = cudaEventRecord(ev_fwd, st);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(rs, ev_fwd, 0);
+      e = cudaEventRecord(ev[0], st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(rs, ev[0], 0);
+      if (e == cudaSuccess) e = launch_prefill_tc(f, rs);
+      if (e == cudaSuccess) e = cudaEventRecord(ev[1], rs);
       if (e == cudaSuccess) e = launch_reverse_tc(r, rs);
-      if (e == cudaSuccess) e = cudaEventRecord(ev_rev, rs);
+      if (e == cudaSuccess) e = cudaEventRecord(ev[2], rs);
       if (e == cudaSuccess) e = local_factors(st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[1], 0);
       if (e == cudaSuccess) e = run(pre, kPre, st);
-      const cudaError_t ew = cudaStreamWaitEvent(st, ev_rev, 0);   // join
-      cudaEventDestroy(ev_fwd);
-      cudaEventDestroy(ev_rev);
+      // join (also on an error above, so that nothing of this call is left
+      // running on the internal stream unordered with the caller's)
+      const cudaError_t ew = cudaStreamWaitEvent(st, ev[2], 0);
+      for (int i = 0; i < 3; ++i) cudaEventDestroy(ev[i]);
       if (e == cudaSuccess) e = ew;
       if (e != cudaSuccess) return e;
     }
