@@ -191,6 +191,15 @@ struct NormGate {
   float eps = 0.f;
   int32_t act = 0;                       // GDN_GATE_SILU or GDN_GATE_SIGMOID
   float* part = nullptr;                 // scratch [T_total, H, 2]: the halves' sums of squares
+                                         // (the split form's read-out)
+  // fused form: one progress count per state unit (N * H * dv / 128, zeroed
+  // by the caller): how many of the unit's chunks have their output rows
+  // out, raised every few chunks; the per-chunk workers apply Eq. 20 to a
+  // chunk's rows (sums of squares included) once both units of its head
+  // have passed it.  nullptr: the two units of a head sum their halves as
+  // they copy the rows out and finish the rows themselves after their
+  // chains, as a 2-CTA cluster (the split form).
+  uint32_t* flags = nullptr;
 };
 
 // The layer entry point's pre-recurrence steps, run by the tensor-core prep

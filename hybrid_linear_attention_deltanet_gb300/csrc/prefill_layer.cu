@@ -1,14 +1,21 @@
 // gdn_prefill_layer -- the mixer core of a Gated DeltaNet layer over whole
-// sequences in the tensor-core prefill's kernels ("Long-Context Aware
-// Upcycling", Appendix A.3): the pre-recurrence steps (short convolution +
-// SiLU, q / k L2 normalisation, the gates; the paragraph after Table 8 and
-// the text under Eq. 16-21) run inside the per-chunk prep on its input
-// tiles, and Eq. 20's gated RMSNorm inside the state pass (the per-row sums
-// of squares as it copies its output rows out, the normalisation and the gate
-// over its rows once the chain is done), so that q, k, v, alpha and beta
-// never exist in HBM: the call reads the projections and writes y.  The prep
-// also leaves the processed keys in scratch, where the state pass reads its K
-// tiles.
+// sequences ("Long-Context Aware Upcycling", Appendix A.3): the
+// pre-recurrence steps (short convolution + SiLU, q / k L2 normalisation, the
+// gates; the paragraph after Table 8 and the text under Eq. 16-21), the
+// chunked recurrence and Eq. 20's gated RMSNorm in one call.
+//
+// Up to the long-sequence length the pre-recurrence steps run as their own
+// pass into scratch (gdn_prepare), then the tensor-core prefill with the
+// read-out inside: in the fused form the per-chunk workers, once their
+// chunks' operands are out, apply Eq. 20 to each chunk's output rows behind
+// the state chains (o exists only in y's memory in between); in the split
+// form the two 128-row units of a head finish their rows as a 2-CTA cluster.
+// Measured alternative: the convolution inside the per-chunk prep on its
+// input tiles (q, k, v, alpha and beta never in HBM) more than doubled each
+// prep item, which the chains then waited for.  For sequences that take the
+// segmented form that is still the path taken: there the prep runs over all
+// items before the state passes anyway, and the keys the prep processes are
+// left in scratch for the state passes' K tiles.
 #include <algorithm>
 
 #include "gdn_internal.cuh"
@@ -96,6 +103,71 @@ extern "C" int gdn_prefill_layer(const void* qkv, const float* conv_w, const flo
 
   unsigned* status = status_ptr();
   if (!status) return GDN_ERR_CUDA;
+
+  if (!takes_long_form(seqlen, 0)) {
+    // The pre-recurrence steps as their own pass (gdn_prepare, into scratch),
+    // then the prefill with the read-out inside: in the fused form its
+    // per-chunk workers, once their chunks' operands are out, apply Eq. 20
+    // to each chunk's rows behind the state chains; in the split form the
+    // two units of a head finish their rows as a cluster.  (Keeping the
+    // convolution inside the per-chunk prep instead measured slower: it
+    // more than doubles each prep item, which the chains then wait for.)
+    const size_t nth = (size_t)T_total * heads;
+    const size_t qb = align_up(nth * kDK * 2, 1024), gb = align_up(nth * 4, 1024);
+    const size_t pb = align_up(nth * 8, 1024);
+    const int64_t max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
+    const size_t fb = align_up((size_t)batch * heads * (dv / 128) * 4, 1024);
+    const size_t need =
+        3 * qb + 2 * gb + pb + fb + prefill_scratch_bytes(batch, seqlen, heads, dv, GDN_BF16,
+                                                          varlen, 0);
+    void* scratch = nullptr;
+    if (scratch_alloc(&scratch, need, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    char* p = (char*)scratch;
+    void* q = p;
+    void* k = p + qb;
+    void* v = p + 2 * qb;
+    float* alpha = (float*)(p + 3 * qb);
+    float* beta = (float*)(p + 3 * qb + gb);
+    float* part = (float*)(p + 3 * qb + 2 * gb);
+    uint32_t* flags = (uint32_t*)(p + 3 * qb + 2 * gb + pb);
+    char* pre = p + 3 * qb + 2 * gb + pb + fb;
+    int rc = gdn_prepare(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, cu_seqlens, conv_state_in,
+                         conv_state_out, q, k, v, alpha, beta, batch, seqlen, heads, kDK, dv,
+                         GDN_BF16, stream_);
+    cudaError_t e = cudaSuccess;
+    if (rc == GDN_OK && fb) e = cudaMemsetAsync(flags, 0, fb, stream);
+    if (rc == GDN_OK && e == cudaSuccess) {
+      PrefillLaunch a{};
+      a.q = q;
+      a.k = k;
+      a.v = v;
+      a.alpha = alpha;
+      a.beta = beta;
+      a.S0 = S0;
+      a.out = y;
+      a.S_final = S_final;
+      a.H = heads;
+      a.dv = dv;
+      a.status = status;
+      a.map.cu_seqlens = cu_seqlens;
+      a.map.N = batch;
+      a.map.T = varlen ? T_total : seqlen;
+      a.map.chunks_per_seq = varlen ? 0 : (seqlen + kC - 1) / kC;
+      a.max_chunks = max_chunks;
+      a.allow_overlap = true;
+      a.ng.gate = (const __nv_bfloat16*)gate;
+      a.ng.w = norm_w;
+      a.ng.eps = eps;
+      a.ng.act = act;
+      a.ng.part = part;
+      a.ng.flags = flags;
+      e = launch_prefill_any(a, GDN_BF16, seqlen, 0, pre, stream);
+    }
+    const cudaError_t ef = scratch_free(scratch, stream);
+    if (rc != GDN_OK) return rc;
+    return (e == cudaSuccess && ef == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
+  }
+
   const size_t kb = k_out_bytes(T_total, heads);
   const size_t pb = align_up((size_t)T_total * heads * 8, 1024);   // the norm's partial sums
   const size_t need =

@@ -99,6 +99,9 @@ __device__ __forceinline__ uint32_t sw_chunk(uint32_t row, uint32_t ch) {
 
 // Bounded wait for a ready flag (fused form): give up after one second.
 constexpr uint64_t kReadyWaitNs = 1000000000ull;
+// (fused form with the read-out) a state unit reports its output progress
+// every kReadoutStep chunks
+constexpr int kReadoutStep = 16;
 
 // ============================================================ prep
 constexpr int kPrepThreads = 256;
@@ -145,6 +148,7 @@ struct PrepSmem {
 
 struct PrepItem {
   int64_t ci = 0, t0 = 0;   // global chunk index, first token
+  int64_t pos = 0;          // chunk position within the sequence (ordered items)
   int h = 0, L = 0;         // head, valid rows
   int n = 0;                // sequence
 };
@@ -170,6 +174,7 @@ __device__ __forceinline__ bool prep_item(const SeqMap& map, int32_t H, int64_t 
   const int64_t cb = map.chunk_begin(n);
   if (cb + p >= map.chunk_end(n)) return false;
   it.ci = cb + p;
+  it.pos = p;
   it.t0 = map.seq_begin(n) + p * kC;
   const int64_t left = map.seq_end(n) - it.t0;
   it.L = left < kC ? (int)left : kC;
@@ -1102,7 +1107,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
       const int r = p >> 4, c16 = p & 15;
       const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 256 + c16 * 16);
       *reinterpret_cast<uint4*>(out + ((prev_t0 + r) * H + h) * dv + 128 * slice + 8 * c16) = v;
-      if (norm) {   // whole 16-lane halves of a warp share a row
+      if (norm && !(kFused && ng.flags)) {   // whole 16-lane halves of a warp share a row
         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
         float ssum = 0.f;
 #pragma unroll
@@ -1221,6 +1226,11 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     __syncthreads();
     if (s_abort) break;
     stamp(it, 3);
+    // (fused read-out) every kReadoutStep chunks: the rows of chunks
+    // [cb, ci) are out (copied before the barrier).  A release waits for the
+    // CTA's stores to drain, so it is not made every chunk.
+    if (kFused && norm && ng.flags && it > 0 && it % kReadoutStep == 0 && tid == 128)
+      st_release_gpu(ng.flags + unit, (uint32_t)it);
 
     // 3. D_S = (dU)^T K (commit m2) ; D_O += U^T P^^T (commit mo)
     if (tid == 0) {
@@ -1331,6 +1341,10 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   }
   // the last chunk's output rows
   if (!s_abort && ce > cb) copy_out_prev((int)((ce - cb - 1) & 1));
+  if (kFused && norm && ng.flags && ce > cb) {   // and finally all of them
+    __syncthreads();
+    if (!s_abort && tid == 128) st_release_gpu(ng.flags + unit, (uint32_t)(ce - cb));
+  }
 
   if (!s_abort && S_final) {
     float4* p = reinterpret_cast<float4*>(S_final + srow);
@@ -1358,7 +1372,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   // with all loads of those rows in flight before any is used (the chain's
   // registers are free by now).
   constexpr int kTailRows = 8;
-  if (norm) {
+  if (norm && !(kFused && ng.flags)) {
     cluster_sync_all();
     if (out && !s_abort) {
       const int c16 = tid & 15;
@@ -1447,6 +1461,95 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restric
                     x >= map.N ? x - map.N : x, h, slice, sdump, ng, u.ident);
 }
 
+// (fused form with the read-out, after a worker's prep items) Eq. 20 over
+// the chunks' rows.  Each warp of each worker takes its own items in the
+// prep's chunk-position order (item j = (worker * 8 + warp) + k * n_workers
+// * 8), so that eight items per worker are in flight and no item waits
+// behind another's flags: lane 0 waits (bounded) until both 128-row units of
+// the item's head report the chunk's output rows out; then a lane takes
+// the 16-byte column group `lane` of every row, eight rows at a time with
+// all their loads in flight, the row's sum of squares (of the bf16 values
+// stored) by a warp reduction, then the split form's arithmetic.  The state
+// units thus add nothing to their chains.  dv = 256.
+__device__ __forceinline__ void readout_role(const SeqMap& map, int32_t H, int32_t dv,
+                                             const NormGate& ng, __nv_bfloat16* __restrict__ out,
+                                             unsigned* status, int64_t n_items, int64_t worker,
+                                             int64_t n_workers) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ns = dv / 128;
+  float w8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w8[i] = __ldg(ng.w + 8 * lane + i);
+  const float inv_dv = 1.f / (float)dv;
+  const int64_t stride = n_workers * (kPrepThreads / 32);
+  for (int64_t j = worker * (kPrepThreads / 32) + warp; j < n_items; j += stride) {
+    PrepItem it;
+    if (!prep_item<true>(map, H, j, it)) continue;
+    int ok = 1;
+    if (lane == 0) {
+      const uint32_t* f = ng.flags + ((size_t)it.n * H + it.h) * ns;
+      const uint32_t need = (uint32_t)(it.pos + 1);
+      const uint64_t t_start = globaltimer_ns();
+      for (int k = 0; k < ns && ok; ++k) {
+        // a chunk of the chain takes a few microseconds: poll at about that
+        // pace, so that hundreds of waiting warps do not crowd the L2 the
+        // chains' loads go through
+        while (ld_relaxed_gpu(f + k) < need) {
+          if (globaltimer_ns() - t_start >= kReadyWaitNs) {
+            ok = 0;
+            break;
+          }
+          __nanosleep(2000);
+        }
+      }
+      if (ok) fence_acq_rel_gpu();
+      else flag_status(status, GDN_ERR_TIMEOUT);
+    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    for (int r0 = 0; r0 < it.L; r0 += 8) {
+      uint4 ov[8], gv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (r0 + u < it.L) {
+          const size_t row = (size_t)(it.t0 + r0 + u) * H + it.h;
+          ov[u] = *reinterpret_cast<const uint4*>(out + row * dv + 8 * lane);
+          gv[u] = __ldg(reinterpret_cast<const uint4*>(ng.gate + row * dv + 8 * lane));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (r0 + u < it.L) {   // uniform across the warp
+          const uint32_t o4[4] = {ov[u].x, ov[u].y, ov[u].z, ov[u].w};
+          const uint32_t g4[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
+          float ssum = 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = bf16_lo(o4[e]), b = bf16_hi(o4[e]);
+            ssum = fmaf(a, a, ssum);
+            ssum = fmaf(b, b, ssum);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+          const float rs = rsqrtf(ssum * inv_dv + ng.eps);
+          uint32_t yo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float g0 = bf16_lo(g4[e]), g1 = bf16_hi(g4[e]);
+            const float a0 = ng.act == GDN_GATE_SIGMOID ? __fdividef(1.f, 1.f + __expf(-g0))
+                                                        : __fdividef(g0, 1.f + __expf(-g0));
+            const float a1 = ng.act == GDN_GATE_SIGMOID ? __fdividef(1.f, 1.f + __expf(-g1))
+                                                        : __fdividef(g1, 1.f + __expf(-g1));
+            yo[e] = pack_bf16(bf16_lo(o4[e]) * rs * w8[2 * e] * a0,
+                              bf16_hi(o4[e]) * rs * w8[2 * e + 1] * a1);
+          }
+          const size_t row = (size_t)(it.t0 + r0 + u) * H + it.h;
+          *reinterpret_cast<uint4*>(out + row * dv + 8 * lane) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+        }
+      }
+    }
+  }
+}
+
 // fused form: cooperative, one CTA per SM; CTAs [0, n_state) are the state
 // units (with ns = dv / 128 slices of S per head, unit u = (sequence
 // u / (ns H), head (u / ns) % H, slice u % ns)), the rest
@@ -1460,7 +1563,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 float* __restrict__ S_final, SeqMap map, int32_t H, uint8_t* __restrict__ scratch,
                 uint32_t* ready, unsigned* status, uint64_t* __restrict__ trace,
                 int32_t trace_chunks, int32_t n_state, int32_t dv, float* __restrict__ sdump,
-                ConvIn cv) {
+                ConvIn cv, NormGate ng) {
   static_assert(kPrepThreads == kStateThreads, "one block shape for both roles");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align_smem_1024(smem_raw);
@@ -1468,10 +1571,9 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int u = blockIdx.x;
     const int ns = dv / 128, n = u / (ns * H);
     const int64_t per_seq = (int64_t)H * dv * kDK;
-    const NormGate none{};
     state_role<true>(sm, &tm_kb, S0 ? S0 + n * per_seq : nullptr, out,
                      S_final ? S_final + n * per_seq : nullptr, map, H, scratch, ready, status,
-                     trace, trace_chunks, dv, n, (u / ns) % H, u % ns, sdump, none);
+                     trace, trace_chunks, dv, n, (u / ns) % H, u % ns, sdump, ng);
   } else {
     int64_t positions = map.chunks_per_seq;
     if (map.cu_seqlens) {
@@ -1484,6 +1586,9 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     prep_role<true>(sm, &tm_q, &tm_k, &tm_v, alpha, beta, map, H, scratch, ready, status, dv, cv,
                     trace ? trace + kPrepTraceOffset : nullptr, trace, positions * map.N * H,
                     blockIdx.x - n_state, gridDim.x - n_state);
+    if (ng.gate && ng.flags)   // the read-out norm of the chunks, behind the chains
+      readout_role(map, H, dv, ng, out, status, positions * map.N * H, blockIdx.x - n_state,
+                   gridDim.x - n_state);
   }
 }
 
@@ -1909,7 +2014,8 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
   uint32_t* ready = (uint32_t*)(scr + (size_t)items * img_stride(dv));
   const int64_t n_state = (int64_t)a.map.N * a.H * (dv / 128);
 
-  if (!prep_only && !a.state_only && a.allow_overlap && a.route.pass == 0 && !a.ng.gate &&
+  if (!prep_only && !a.state_only && a.allow_overlap && a.route.pass == 0 &&
+      (!a.ng.gate || (a.ng.flags && dv == 256)) &&
       f->fused_ok && items > 0 &&
       n_state + kMinPrepWorkers <= f->sms) {
     if ((e = cudaMemsetAsync(ready, 0, (size_t)items * sizeof(uint32_t), stream)) != cudaSuccess)
@@ -1926,7 +2032,8 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, tc_fused_kernel, tq, tk, tv, tkb, a.alpha, a.beta, a.S0,
                            (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr, ready, a.status,
-                           g_trace, g_trace_chunks, (int32_t)n_state, dv, a.state_dump, a.cv);
+                           g_trace, g_trace_chunks, (int32_t)n_state, dv, a.state_dump, a.cv,
+                           a.ng);
     if (e == cudaSuccess) {
       count_launches(1);
       g_last_tc_form = 1;

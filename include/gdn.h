@@ -417,16 +417,15 @@ int gdn_decode_layer_step(const void* qkv, const float* conv_w, const float* a_r
 
 /*
  * gdn_prefill_layer -- the mixer core of a layer over whole sequences in one
- * pass over the projections: gdn_prepare, gdn_prefill and
- * gdn_output_norm_gate fused into the tensor-core prefill's kernels.  The
- * per-chunk prep reads the q, k, v tiles of each (chunk, head) straight from
- * qkv and applies the convolution + SiLU (and the q / k L2 norm) in shared
- * memory before its first MMA, computing alpha and beta from a_raw / b_raw;
- * the state pass sums the squares of each output row's half as it copies
- * the rows out, and once a head's two 128-row units (a 2-CTA cluster) have
- * finished their chains it applies Eq. 20's gated RMSNorm over their rows in
- * place.  Neither q, k, v, alpha nor beta is written to HBM; o exists only
- * in y's memory between the chain and the read-out.
+ * call: gdn_prepare, gdn_prefill and gdn_output_norm_gate with the read-out
+ * inside the tensor-core prefill.  The pre-recurrence steps write q, k, v,
+ * alpha and beta to scratch; in the prefill's fused form its per-chunk
+ * workers then apply Eq. 20's gated RMSNorm to each chunk's output rows as
+ * the state chains pass it (o exists only in y's memory in between; in the
+ * split form a head's two 128-row units, as a 2-CTA cluster, finish their
+ * rows after their chains).  Sequences long enough for gdn_prefill's
+ * segmented form take it with the convolution inside the per-chunk prep
+ * instead (q, k, v, alpha and beta never in HBM) and the cluster read-out.
  *
  *   qkv, conv_w, a_raw, b_raw, A_log, dt_bias,
  *   conv_state_in, conv_state_out      as in gdn_prepare
@@ -439,8 +438,9 @@ int gdn_decode_layer_step(const void* qkv, const float* conv_w, const float* a_r
  * the same values the separate pass writes, and o enters the norm as the
  * bf16 values gdn_prefill would store.  bf16 I/O and dk = dv = 256 only
  * (GDN_ERR_UNSUPPORTED otherwise).  Scratch from the library's pool:
- * gdn_prefill's plus T_total * H * dk * 2 bytes of processed keys and
- * T_total * H * 8 bytes of partial sums.  Errors as
+ * gdn_prefill's plus q, k, v, alpha, beta (segmented form: T_total * H * dk
+ * * 2 bytes of processed keys) and T_total * H * 8 bytes of partial sums.
+ * Errors as
  * for the three calls; no output may overlap an input or another output.
  */
 int gdn_prefill_layer(const void* qkv, const float* conv_w, const float* a_raw, const float* b_raw,
