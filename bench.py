@@ -730,8 +730,8 @@ def run_ours(args, rank, world, local_rank, dist):
                 "unit": "Mtok/s/layer", "launches_per_step": lf_launch,
                 "three_calls_ms_per_step": round(l3_ms, 4),
                 "three_calls_launches_per_step": l3_launch,
-                "path": "pre-recurrence steps inside the tensor-core prep, gated RMSNorm "
-                        "inside the state pass (split form, 2-CTA clusters)"},
+                "path": "pre-recurrence steps as their own pass, then the fused prefill "
+                        "whose per-chunk workers apply the gated RMSNorm behind the chains"},
             "layer_steps": {
                 "prepare": {"workload": lcase.name + " (gdn_prepare)",
                             "ms_per_step": round(prep_ms, 4),
