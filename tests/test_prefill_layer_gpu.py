@@ -1,5 +1,7 @@
-"""gdn_prefill_layer (the pre-recurrence steps fused into the prefill's
-per-chunk prep, Eq. 20's gated RMSNorm into its state pass) through the C ABI:
+"""gdn_prefill_layer (the pre-recurrence steps as their own pass, Eq. 20's
+gated RMSNorm inside the prefill: its per-chunk workers in the fused form, its
+state units as 2-CTA clusters in the split form; for sequences in the
+segmented form the convolution inside the per-chunk prep) through the C ABI:
 
 * against the fp64 oracle's composition layer_io.prepare -> oracle.prefill ->
   layer_io.output_norm_gate, within the bf16 tolerance 2e-2 per (sequence,
@@ -9,6 +11,7 @@ per-chunk prep, Eq. 20's gated RMSNorm into its state pass) through the C ABI:
   gdn_output_norm_gate): q, k, v, alpha and beta are the same values, so
   S_final and the convolution state are equal bit for bit, and y differs only
   in the order of the norm's sum of squares (a bf16 rounding step at most);
+* in both launch forms of the prefill;
 * packing never changes a sequence's result, also for a 64K-token sequence
   that the length rule cuts into segments.
 """
@@ -157,6 +160,30 @@ def test_layer_at_full_size_8k(gdn_lib):
     xo = dict(x)
     xo["qkv"] = x["qkv"].reshape(-1, case.channels)
     _check_oracle(y.reshape(-1, case.H, case.dv), sf, so, xo, case, [(0, 0), (3, 5)])
+
+
+def _last_form(gdn_lib):
+    import ctypes
+    f = gdn_lib.load().gdn_testing_last_prefill_form
+    f.restype = ctypes.c_int32
+    return int(f())
+
+
+@pytest.mark.parametrize("n_seq,form", [(3, 1), (61, 0)])
+def test_layer_readout_in_both_launch_forms(gdn_lib, n_seq, form):
+    """Few heads: the prefill's fused form, whose per-chunk workers apply
+    Eq. 20 behind the chains.  61 sequences x 1 head (122 state units) leave
+    too few SMs for the workers: the split form, whose units finish their
+    rows as 2-CTA clusters.  Both against the three separate calls."""
+    rng = np.random.default_rng(140 + n_seq)
+    lens = [int(t) for t in rng.integers(1, 400, size=n_seq)]
+    case = LayerCase("layer form", lens, H=1 if n_seq > 3 else 2, seed=141, varlen=True)
+    xd = _inputs(case, 142, DEV)
+    y, sf, so = _layer(gdn_lib, xd, case)
+    assert _last_form(gdn_lib) == form
+    y3, sf3, so3 = _three_calls(gdn_lib, xd, case)
+    assert torch.equal(sf, sf3) and torch.equal(so, so3)
+    assert rel(y.float().cpu().numpy(), y3.float().cpu().numpy()) <= 4e-3
 
 
 def test_layer_long_sequence(gdn_lib):
