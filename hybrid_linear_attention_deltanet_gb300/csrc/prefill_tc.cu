@@ -148,7 +148,6 @@ struct PrepSmem {
 
 struct PrepItem {
   int64_t ci = 0, t0 = 0;   // global chunk index, first token
-  int64_t pos = 0;          // chunk position within the sequence (ordered items)
   int h = 0, L = 0;         // head, valid rows
   int n = 0;                // sequence
 };
@@ -174,7 +173,6 @@ __device__ __forceinline__ bool prep_item(const SeqMap& map, int32_t H, int64_t 
   const int64_t cb = map.chunk_begin(n);
   if (cb + p >= map.chunk_end(n)) return false;
   it.ci = cb + p;
-  it.pos = p;
   it.t0 = map.seq_begin(n) + p * kC;
   const int64_t left = map.seq_end(n) - it.t0;
   it.L = left < kC ? (int)left : kC;
@@ -1488,7 +1486,7 @@ __device__ __forceinline__ void readout_role(const SeqMap& map, int32_t H, int32
     int ok = 1;
     if (lane == 0) {
       const uint32_t* f = ng.flags + ((size_t)it.n * H + it.h) * ns;
-      const uint32_t need = (uint32_t)(it.pos + 1);
+      const uint32_t need = (uint32_t)(it.ci - map.chunk_begin(it.n) + 1);
       const uint64_t t_start = globaltimer_ns();
       for (int k = 0; k < ns && ok; ++k) {
         // a chunk of the chain takes a few microseconds: poll at about that
@@ -1554,7 +1552,10 @@ __device__ __forceinline__ void readout_role(const SeqMap& map, int32_t H, int32
 // units (with ns = dv / 128 slices of S per head, unit u = (sequence
 // u / (ns H), head (u / ns) % H, slice u % ns)), the rest
 // prep workers over all chunk positions in order; ready[] holds a flag per
-// (chunk, head)
+// (chunk, head).  kNorm: the layer's read-out (Eq. 20) by the workers after
+// their prep items; without it the state units get a NormGate known to be
+// empty at compile time, so that no read-out code stays in their chains.
+template <bool kNorm>
 __global__ void __launch_bounds__(kStateThreads, 1)
 tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kb,
@@ -1571,9 +1572,10 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int u = blockIdx.x;
     const int ns = dv / 128, n = u / (ns * H);
     const int64_t per_seq = (int64_t)H * dv * kDK;
+    const NormGate none{};
     state_role<true>(sm, &tm_kb, S0 ? S0 + n * per_seq : nullptr, out,
                      S_final ? S_final + n * per_seq : nullptr, map, H, scratch, ready, status,
-                     trace, trace_chunks, dv, n, (u / ns) % H, u % ns, sdump, ng);
+                     trace, trace_chunks, dv, n, (u / ns) % H, u % ns, sdump, kNorm ? ng : none);
   } else {
     int64_t positions = map.chunks_per_seq;
     if (map.cu_seqlens) {
@@ -1586,7 +1588,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     prep_role<true>(sm, &tm_q, &tm_k, &tm_v, alpha, beta, map, H, scratch, ready, status, dv, cv,
                     trace ? trace + kPrepTraceOffset : nullptr, trace, positions * map.N * H,
                     blockIdx.x - n_state, gridDim.x - n_state);
-    if (ng.gate && ng.flags)   // the read-out norm of the chunks, behind the chains
+    if (kNorm)   // the read-out norm of the chunks, behind the chains
       readout_role(map, H, dv, ng, out, status, positions * map.N * H, blockIdx.x - n_state,
                    gridDim.x - n_state);
   }
@@ -1953,19 +1955,23 @@ DeviceFacts* device_facts() {
   std::lock_guard<std::mutex> lock(mu);
   DeviceFacts& f = facts[dev];
   if (!f.ready) {
-    int coop = 0, per_sm = 0;
+    int coop = 0, per_sm = 0, per_sm_norm = 0;
     if (cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
         cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kPrepSmemSplit) != cudaSuccess ||
         cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kStateSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(tc_fused_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kFusedSmem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_fused_kernel, kStateThreads,
-                                                      kFusedSmem) != cudaSuccess)
+        cudaFuncSetAttribute(tc_fused_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kFusedSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_fused_kernel<false>,
+                                                      kStateThreads, kFusedSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_norm, tc_fused_kernel<true>,
+                                                      kStateThreads, kFusedSmem) != cudaSuccess)
       return nullptr;
-    f.fused_ok = coop != 0 && per_sm >= 1;
+    f.fused_ok = coop != 0 && per_sm >= 1 && per_sm_norm >= 1;
     f.ready = true;
   }
   return &f;
@@ -2030,10 +2036,10 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, tc_fused_kernel, tq, tk, tv, tkb, a.alpha, a.beta, a.S0,
-                           (__nv_bfloat16*)a.out, a.S_final, a.map, a.H, scr, ready, a.status,
-                           g_trace, g_trace_chunks, (int32_t)n_state, dv, a.state_dump, a.cv,
-                           a.ng);
+    e = cudaLaunchKernelEx(&cfg, a.ng.gate ? tc_fused_kernel<true> : tc_fused_kernel<false>,
+                           tq, tk, tv, tkb, a.alpha, a.beta, a.S0, (__nv_bfloat16*)a.out,
+                           a.S_final, a.map, a.H, scr, ready, a.status, g_trace, g_trace_chunks,
+                           (int32_t)n_state, dv, a.state_dump, a.cv, a.ng);
     if (e == cudaSuccess) {
       count_launches(1);
       g_last_tc_form = 1;
