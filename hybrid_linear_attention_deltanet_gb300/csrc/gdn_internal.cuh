@@ -36,6 +36,91 @@ __device__ __forceinline__ void flag_status(unsigned* status, unsigned code) {
 }
 
 // ---------------------------------------------------------------------------
+// Arithmetic of the pre-recurrence steps ("Long-Context Aware Upcycling",
+// Appendix A.3: the short convolution's SiLU and the q/k L2 norm), shared by
+// gdn_prepare and by the tensor-core prep that runs the same steps on its
+// tiles, so that the two give the same bits.
+//
+// F2: two fp32 values in one 64-bit register pair.  The .f32x2 forms of mul,
+// add and fma (sm_100 onwards) round each half exactly as the scalar
+// instruction does, at one issue for the pair.
+struct F2 {
+  uint64_t v;
+};
+__device__ __forceinline__ F2 f2(float lo, float hi) {
+  F2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(F2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  return lo;
+}
+__device__ __forceinline__ float f2_hi(F2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  return hi;
+}
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
+  F2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  F2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
+  F2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return r;
+}
+
+// The special-function unit's base-2 exponential and reciprocal (a few ulp
+// each; subnormal results flush to zero).
+__device__ __forceinline__ float ex2_sfu(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_sfu(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kNegLog2e = -1.44269504088896341f;
+// SiLU x / (1 + e^-x), with e^-x = 2^(-x log2 e).  Far below zero e^-x
+// overflows to inf and the reciprocal gives 0 (the limit); far above, it
+// flushes to 0 and the result is x.  silu_pair gives the same bits per half.
+__device__ __forceinline__ float silu_sfu(float x) {
+  return __fmul_rn(x, rcp_sfu(__fadd_rn(ex2_sfu(__fmul_rn(x, kNegLog2e)), 1.f)));
+}
+__device__ __forceinline__ F2 silu_pair(F2 x) {
+  const F2 t = f2_mul(x, f2(kNegLog2e, kNegLog2e));
+  const F2 d = f2_add(f2(ex2_sfu(f2_lo(t)), ex2_sfu(f2_hi(t))), f2(1.f, 1.f));
+  return f2_mul(x, f2(rcp_sfu(f2_lo(d)), rcp_sfu(f2_hi(d))));
+}
+// A lane's part of a row's sum of squares over its 8 values y[0..7]: the
+// even and the odd positions accumulate apart (in order), then add.
+__device__ __forceinline__ float sumsq8(const float (&y)[8]) {
+  float e = __fmul_rn(y[0], y[0]), o = __fmul_rn(y[1], y[1]);
+#pragma unroll
+  for (int k = 2; k < 8; k += 2) {
+    e = fmaf(y[k], y[k], e);
+    o = fmaf(y[k + 1], y[k + 1], o);
+  }
+  return __fadd_rn(e, o);
+}
+__device__ __forceinline__ float sumsq8(const F2 (&y)[4]) {
+  F2 s = f2_mul(y[0], y[0]);
+#pragma unroll
+  for (int k = 1; k < 4; ++k) s = f2_fma(y[k], y[k], s);
+  return __fadd_rn(f2_lo(s), f2_hi(s));
+}
+
+// ---------------------------------------------------------------------------
 // Chunk map.  Sequences are cut into chunks of kC tokens that restart at
 // every sequence start; the last chunk of a sequence may be partial.  A dense
 // batch is the packed case with cu[n] = n * T.

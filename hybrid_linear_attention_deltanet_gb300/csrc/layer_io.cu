@@ -126,24 +126,56 @@ __device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
   reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
   reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
+// The same 8 elements as four fp32 pairs (element 2i in the low half of
+// pair i), for the packed arithmetic of the convolution.
+template <typename T>
+__device__ __forceinline__ void widen8(const Raw8& r, F2 (&f)[4]);
+template <>
+__device__ __forceinline__ void widen8<__nv_bfloat16>(const Raw8& r, F2 (&f)[4]) {
+  const uint32_t w[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f[i] = f2(bf16_lo(w[i]), bf16_hi(w[i]));
+}
+template <>
+__device__ __forceinline__ void widen8<float>(const Raw8& r, F2 (&f)[4]) {
+  const uint32_t w[8] = {r.a.x, r.a.y, r.a.z, r.a.w, r.b.x, r.b.y, r.b.z, r.b.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f[i] = f2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const F2 (&f)[4]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(f2_lo(f[i]), f2_hi(f[i]));
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ void store8(float* p, const F2 (&f)[4]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(f2_lo(f[0]), f2_hi(f[0]), f2_lo(f[1]), f2_hi(f[1]));
+  reinterpret_cast<float4*>(p)[1] = make_float4(f2_lo(f[2]), f2_hi(f[2]), f2_lo(f[3]), f2_hi(f[3]));
+}
 
-// Elementwise activations of the streams use the fast exponential and divide
-// intrinsics (a few ulp, far inside the fp32 output tolerance); at e^-x = inf
-// the quotient is 0, the correct limit.  The per-head gates use expf/log1pf.
+// Elementwise activations of the streams are approximate to a few ulp (far
+// inside the fp32 output tolerance): the convolution's SiLU is silu_pair
+// (gdn_internal.cuh), the read-out gate's uses the fast exponential and
+// divide intrinsics; at e^-x = inf either gives 0, the correct limit.  The
+// per-head gates use expf/log1pf.
 __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
 // log(1 + e^x); above 20 the correction e^-x is below fp32 resolution
 __device__ __forceinline__ float softplusf_(float x) { return x > 20.f ? x : log1pf(expf(x)); }
 
-// Conv taps of 8 channels, tap-major in registers: w[j][i] for channel c0 + i.
+// Conv taps of 8 channels, tap-major in registers as pairs: w[j][i] holds
+// tap j of channels c0 + 2i and c0 + 2i + 1.
 __device__ __forceinline__ void load_taps(const float* __restrict__ conv_w, int64_t c0,
-                                          float (&w)[kTaps][8]) {
+                                          F2 (&w)[kTaps][4]) {
   const float4* p = reinterpret_cast<const float4*>(conv_w + c0 * kTaps);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 t = __ldg(p + i);  // channel c0 + i: taps 0..3
-    w[0][i] = t.x; w[1][i] = t.y; w[2][i] = t.z; w[3][i] = t.w;
+  for (int i = 0; i < 4; ++i) {
+    const float4 a = __ldg(p + 2 * i), b = __ldg(p + 2 * i + 1);  // taps 0..3 of two channels
+    w[0][i] = f2(a.x, b.x); w[1][i] = f2(a.y, b.y); w[2][i] = f2(a.z, b.z); w[3][i] = f2(a.w, b.w);
   }
 }
 
@@ -152,7 +184,7 @@ __device__ __forceinline__ void load_taps(const float* __restrict__ conv_w, int6
 // the non-coherent path); the in-place decode form reads it coherently.
 template <typename T, bool kNC>
 __device__ __forceinline__ void history(const T* state_in, int64_t n, int64_t C, int64_t c0,
-                                        float (&win)[kHist][8]) {
+                                        F2 (&win)[kHist][4]) {
 #pragma unroll
   for (int j = 0; j < kHist; ++j) {
     if (state_in) {
@@ -160,33 +192,62 @@ __device__ __forceinline__ void history(const T* state_in, int64_t n, int64_t C,
       widen8<T>(kNC ? load8_cached(p) : load8(p), win[j]);
     } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) win[j][i] = 0.f;
+      for (int i = 0; i < 4; ++i) win[j][i] = f2(0.f, 0.f);
     }
   }
 }
 
 // One token of one 256-channel segment: conv + SiLU (+ L2 norm over the
-// segment when it is a q or k head), then the window shifts in x.
-__device__ __forceinline__ void conv_token(const float (&w)[kTaps][8], float (&win)[kHist][8],
-                                           const float (&x)[8], bool l2, float (&y)[8]) {
-  float ss = 0.f;
+// segment when it is a q or k head).  The taps run as fp32 pairs (the same
+// roundings as one channel at a time).  The window is kept in rotation:
+// slot R holds the oldest input, R + 1 (mod 3) the next, R + 2 the newest; x
+// replaces the oldest, so the next token takes rotation R + 1, and three
+// tokens bring the slots back to their order with no register moves.
+template <int R>
+__device__ __forceinline__ void conv_rot(const F2 (&w)[kTaps][4], F2 (&win)[kHist][4],
+                                         const F2 (&x)[4], bool l2, F2 (&y)[4]) {
+  constexpr int a = R % 3, b = (R + 1) % 3, c = (R + 2) % 3;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float acc = w[0][i] * win[0][i];
-    acc = fmaf(w[1][i], win[1][i], acc);
-    acc = fmaf(w[2][i], win[2][i], acc);
-    acc = fmaf(w[3][i], x[i], acc);
-    y[i] = silu_fast(acc);
-    ss = fmaf(y[i], y[i], ss);
-    win[0][i] = win[1][i];
-    win[1][i] = win[2][i];
-    win[2][i] = x[i];
+  for (int i = 0; i < 4; ++i) {
+    F2 acc = f2_mul(w[0][i], win[a][i]);
+    acc = f2_fma(w[1][i], win[b][i], acc);
+    acc = f2_fma(w[2][i], win[c][i], acc);
+    acc = f2_fma(w[3][i], x[i], acc);
+    y[i] = silu_pair(acc);
+    win[a][i] = x[i];
   }
   if (l2) {  // warp-uniform branch: the segment is one q or k head
-    const float r = rsqrtf(warp_sum(ss) + kL2Eps);
+    const float r = rsqrtf(warp_sum(sumsq8(y)) + kL2Eps);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] *= r;
+    for (int i = 0; i < 4; ++i) y[i] = f2_mul(y[i], f2(r, r));
   }
+}
+// The same with the window in order (slot 0 the oldest) before and after.
+__device__ __forceinline__ void conv_token(const F2 (&w)[kTaps][4], F2 (&win)[kHist][4],
+                                           const F2 (&x)[4], bool l2, F2 (&y)[4]) {
+  conv_rot<0>(w, win, x, l2, y);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const F2 t = win[0][i];
+    win[0][i] = win[1][i];
+    win[1][i] = win[2][i];
+    win[2][i] = t;
+  }
+}
+// Two consecutive tokens of one sequence with the window at rotation R:
+// their arithmetic has no branch between it, so the two dependent chains
+// (taps, SiLU, the L2 reduction) interleave.  o: the first token's output row.
+template <typename T, int R>
+__device__ __forceinline__ void pair_rot(const F2 (&w)[kTaps][4], F2 (&win)[kHist][4],
+                                         const Raw8& r0, const Raw8& r1, bool l2, T* o,
+                                         int64_t stride) {
+  F2 x0[4], x1[4], y0[4], y1[4];
+  widen8<T>(r0, x0);
+  widen8<T>(r1, x1);
+  conv_rot<R>(w, win, x0, l2, y0);
+  conv_rot<(R + 1) % 3>(w, win, x1, l2, y1);
+  store8(o, y0);
+  store8(o + stride, y1);
 }
 
 struct PrepareArgs {
@@ -291,7 +352,7 @@ prepare_kernel(PrepareArgs a) {
     dst = static_cast<T*>(a.v); dst_stride = (int64_t)a.H * a.dv;
     dst_c = c0 - 2 * (int64_t)a.H * a.dk;
   }
-  float w[kTaps][8];
+  F2 w[kTaps][4];
   load_taps(a.conv_w, c0, w);
   const T* x = static_cast<const T*>(a.qkv);
 
@@ -299,7 +360,7 @@ prepare_kernel(PrepareArgs a) {
   // carried history that precede the sequence start (slot p - sb + 3)
   int64_t n = seqs.find(t0, a.N);
   int64_t sb = seqs.begin(n), se = seqs.end(n);
-  float win[kHist][8];
+  F2 win[kHist][4];
 #pragma unroll
   for (int j = 0; j < kHist; ++j) {
     const int64_t p = t0 - kHist + j;
@@ -309,7 +370,7 @@ prepare_kernel(PrepareArgs a) {
       widen8<T>(load8_cached(state_in + (n * kHist + (p - sb + kHist)) * C + c0), win[j]);
     } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) win[j][i] = 0.f;
+      for (int i = 0; i < 4; ++i) win[j][i] = f2(0.f, 0.f);
     }
   }
 
@@ -359,7 +420,7 @@ prepare_kernel(PrepareArgs a) {
       se_rel = rel_end();
       history<T, true>(state_in, n, C, c0, win);
     }
-    float xf[8], y[8];
+    F2 xf[4], y[4];
     widen8<T>(r, xf);
     conv_token(w, win, xf, l2, y);
     store8(out_row + i * dst_stride, y);
@@ -368,16 +429,39 @@ prepare_kernel(PrepareArgs a) {
       for (int j = 0; j < kHist; ++j) store8(state_out + (n * kHist + j) * C + c0, win[j]);
     }
   };
-  // Two tokens an iteration: when both lie inside the current sequence their
-  // arithmetic has no branch between it, so the two dependent chains (taps,
-  // SiLU, the L2 reduction) interleave.
-  for (int i = 0; i < n_tok; i += 2) {
+  // Six tokens an iteration while they all lie inside the current sequence
+  // (three pairs, the window in rotation: back in order after six), else a
+  // pair, with the sequence bookkeeping where a sequence ends inside it.
+  // Each pair waits for its two tokens, then refills their two slots.
+  int i = 0;
+  while (i < n_tok) {
+    if (i + 6 <= n_tok && i + 6 <= se_rel) {
+      T* o = out_row + i * dst_stride;
+      cp_async_wait<kRing - 2>();
+      pair_rot<T, 0>(w, win, read(i), read(i + 1), l2, o, dst_stride);
+      issue();
+      issue();
+      cp_async_wait<kRing - 2>();
+      pair_rot<T, 2>(w, win, read(i + 2), read(i + 3), l2, o + 2 * dst_stride, dst_stride);
+      issue();
+      issue();
+      cp_async_wait<kRing - 2>();
+      pair_rot<T, 1>(w, win, read(i + 4), read(i + 5), l2, o + 4 * dst_stride, dst_stride);
+      issue();
+      issue();
+      if (i + 6 == se_rel && state_out) {   // token i + 5 ends the sequence
+#pragma unroll
+        for (int j = 0; j < kHist; ++j) store8(state_out + (n * kHist + j) * C + c0, win[j]);
+      }
+      i += 6;
+      continue;
+    }
     cp_async_wait<kRing - 2>();   // tokens i and i + 1 are in
     const Raw8 r0 = read(i);
     const bool pair = i + 1 < n_tok;
     const Raw8 r1 = pair ? read(i + 1) : r0;
     if (pair && i + 1 < se_rel) {
-      float x0[8], x1[8], y0[8], y1[8];
+      F2 x0[4], x1[4], y0[4], y1[4];
       widen8<T>(r0, x0);
       widen8<T>(r1, x1);
       conv_token(w, win, x0, l2, y0);
@@ -396,6 +480,7 @@ prepare_kernel(PrepareArgs a) {
     // both slots' values are in registers (consumed above): refill them
     issue();
     issue();
+    i += 2;
   }
   cp_async_wait<0>();
 }
@@ -418,7 +503,7 @@ prepare_decode_kernel(PrepareArgs a, T* __restrict__ state) {
   }
   const int64_t c0 = (int64_t)seg * kSeg + lane * 8;
   const bool l2 = seg < 2 * a.H * a.dk / kSeg;
-  float w[kTaps][8], win[kHist][8], xf[8], y[8];
+  F2 w[kTaps][4], win[kHist][4], xf[4], y[4];
   load_taps(a.conv_w, c0, w);
   history<T, false>(state, n, C, c0, win);
   widen8<T>(load8(static_cast<const T*>(a.qkv) + n * C + c0), xf);

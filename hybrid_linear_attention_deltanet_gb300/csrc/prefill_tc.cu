@@ -353,18 +353,19 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
 #pragma unroll 1
     for (int i = 0; i < 8; i += 2) {
       const uint4 in[5] = {hist[0], hist[1], hist[2], *cell(r0 + i), *cell(r0 + i + 1)};
-      float y[2][8], ss[2] = {0.f, 0.f};
+      // gdn_prepare's arithmetic, one channel at a time (the same bits)
+      float y[2][8], ss[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          float acc = w[0][k] * elt(in[u], k);
+          float acc = __fmul_rn(w[0][k], elt(in[u], k));
           acc = fmaf(w[1][k], elt(in[u + 1], k), acc);
           acc = fmaf(w[2][k], elt(in[u + 2], k), acc);
           acc = fmaf(w[3][k], elt(in[u + 3], k), acc);
-          y[u][k] = __fdividef(acc, 1.f + __expf(-acc));
-          ss[u] = fmaf(y[u][k], y[u][k], ss[u]);
+          y[u][k] = silu_sfu(acc);
         }
+        ss[u] = sumsq8(y[u]);
       }
       if (l2) {
 #pragma unroll
