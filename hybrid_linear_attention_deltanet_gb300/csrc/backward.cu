@@ -693,9 +693,10 @@ __device__ __forceinline__ void st4_out(__nv_bfloat16* p, float4 v) {
 }
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
-assemble_kernel(const float* __restrict__ alpha, T* __restrict__ dq, T* __restrict__ dk,
-                T* __restrict__ dv_out, float* __restrict__ dalpha, float* __restrict__ dbeta,
-                SeqMap map, int32_t H, Bwd s) {
+assemble_kernel(const float* __restrict__ alpha, const T* __restrict__ q,
+                const T* __restrict__ k, const T* __restrict__ v, T* __restrict__ dq,
+                T* __restrict__ dk, T* __restrict__ dv_out, float* __restrict__ dalpha,
+                float* __restrict__ dbeta, SeqMap map, int32_t H, Bwd s) {
   __shared__ float dG[kC], dB[kC], dsum[kC];
   const int64_t ci = blockIdx.x;
   const int h = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -711,16 +712,20 @@ assemble_kernel(const float* __restrict__ alpha, T* __restrict__ dq, T* __restri
     const float gam = expf(G[r]), d = expf(GL - G[r]);
     const float be = s.B[u * kC + r], bg = s.BG[u * kC + r];
     float kTdW = 0.f, qdQh = 0.f, vTdU = 0.f, dd = 0.f;
-    // four consecutive columns a lane: 16-byte loads, 4-element stores
+    // four consecutive columns a lane: 16-byte loads, 4-element stores.  q,
+    // k and v come from the caller's arrays (rows past the sequence end are
+    // zero, as in the per-chunk copies the GEMMs read)
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c = 4 * lane; c < kDK; c += 128) {
       const size_t o = u * s.sD() + (size_t)r * kDK + c;
-      const float4 tdw = ld4(s.TdW + o), dqh = ld4(s.dQh + o), kk = ld4(s.K + o);
+      const size_t g = ((t0 + r) * H + h) * kDK + c;
+      const float4 tdw = ld4(s.TdW + o), dqh = ld4(s.dQh + o);
+      const float4 kk = r < L ? ld4_in(k + g) : z, qq = r < L ? ld4_in(q + g) : z;
       const float4 dk1 = ld4(s.dK1 + o);
       kTdW += dot4(kk, tdw);
-      qdQh += dot4(ld4(s.Q + o), dqh);
+      qdQh += dot4(qq, dqh);
       dd += dot4(kk, dk1);   // u_r . (dS' k_r) = k_r . (U dS')_r
       if (r < L) {
-        const size_t g = ((t0 + r) * H + h) * kDK + c;
         const float4 dqa = ld4(s.dQa + o), dka = ld4(s.dKa + o);
         const float sg = kScale * gam;
         st4_out(dq + g, make_float4(fmaf(sg, dqh.x, dqa.x), fmaf(sg, dqh.y, dqa.y),
@@ -733,11 +738,11 @@ assemble_kernel(const float* __restrict__ alpha, T* __restrict__ dq, T* __restri
     }
     for (int c = 4 * lane; c < dv; c += 128) {
       const size_t o = u * s.sV() + (size_t)r * dv + c;
+      const size_t g = ((t0 + r) * H + h) * dv + c;
       const float4 tdu = ld4(s.TdU + o);
-      vTdU += dot4(ld4(s.V + o), tdu);
+      vTdU += dot4(r < L ? ld4_in(v + g) : z, tdu);
       if (r < L)
-        st4_out(dv_out + ((t0 + r) * H + h) * dv + c,
-                make_float4(be * tdu.x, be * tdu.y, be * tdu.z, be * tdu.w));
+        st4_out(dv_out + g, make_float4(be * tdu.x, be * tdu.y, be * tdu.z, be * tdu.w));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -1041,11 +1046,13 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
   if ((e = run(list2, 3, st)) != cudaSuccess) return e;
   if (io_dtype == GDN_BF16)
     assemble_kernel<__nv_bfloat16><<<gu, kThreads, 0, st>>>(
-        a.alpha, (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv_out, dalpha, dbeta,
-        a.map, a.H, s);
+        a.alpha, (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
+        (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv_out, dalpha, dbeta, a.map, a.H,
+        s);
   else
-    assemble_kernel<float><<<gu, kThreads, 0, st>>>(a.alpha, (float*)dq, (float*)dk,
-                                                     (float*)dv_out, dalpha, dbeta, a.map, a.H, s);
+    assemble_kernel<float><<<gu, kThreads, 0, st>>>(
+        a.alpha, (const float*)a.q, (const float*)a.k, (const float*)a.v, (float*)dq, (float*)dk,
+        (float*)dv_out, dalpha, dbeta, a.map, a.H, s);
   count_launches(1);
   return cudaGetLastError();
 }
