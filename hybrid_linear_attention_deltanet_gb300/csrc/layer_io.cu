@@ -179,6 +179,17 @@ __device__ __forceinline__ void load_taps(const float* __restrict__ conv_w, int6
   }
 }
 
+// The same one channel at a time: w[j][i] for channel c0 + i.
+__device__ __forceinline__ void load_taps(const float* __restrict__ conv_w, int64_t c0,
+                                          float (&w)[kTaps][8]) {
+  const float4* p = reinterpret_cast<const float4*>(conv_w + c0 * kTaps);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 t = __ldg(p + i);  // channel c0 + i: taps 0..3
+    w[0][i] = t.x; w[1][i] = t.y; w[2][i] = t.z; w[3][i] = t.w;
+  }
+}
+
 // The three inputs before a sequence's first token: its carried state, or
 // zeros.  kNC: the state is read-only for the whole launch (it may then take
 // the non-coherent path); the in-place decode form reads it coherently.
@@ -194,6 +205,39 @@ __device__ __forceinline__ void history(const T* state_in, int64_t n, int64_t C,
 #pragma unroll
       for (int i = 0; i < 4; ++i) win[j][i] = f2(0.f, 0.f);
     }
+  }
+}
+
+// The decode step's form: the carried state of one sequence, one channel at
+// a time.
+template <typename T>
+__device__ __forceinline__ void history8(const T* state, int64_t n, int64_t C, int64_t c0,
+                                         float (&win)[kHist][8]) {
+#pragma unroll
+  for (int j = 0; j < kHist; ++j) widen8<T>(load8(state + (n * kHist + j) * C + c0), win[j]);
+}
+
+// One token of one 256-channel segment, one channel at a time, with the
+// window shifting in x: the same roundings as conv_rot below, channel by
+// channel (the decode step's single token a warp is bound by the latency of
+// this chain, where the pair form's packing costs more than it saves).
+__device__ __forceinline__ void conv_token(const float (&w)[kTaps][8], float (&win)[kHist][8],
+                                           const float (&x)[8], bool l2, float (&y)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float acc = __fmul_rn(w[0][i], win[0][i]);
+    acc = fmaf(w[1][i], win[1][i], acc);
+    acc = fmaf(w[2][i], win[2][i], acc);
+    acc = fmaf(w[3][i], x[i], acc);
+    y[i] = silu_sfu(acc);
+    win[0][i] = win[1][i];
+    win[1][i] = win[2][i];
+    win[2][i] = x[i];
+  }
+  if (l2) {  // warp-uniform branch: the segment is one q or k head
+    const float r = rsqrtf(warp_sum(sumsq8(y)) + kL2Eps);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(y[i], r);
   }
 }
 
@@ -503,9 +547,9 @@ prepare_decode_kernel(PrepareArgs a, T* __restrict__ state) {
   }
   const int64_t c0 = (int64_t)seg * kSeg + lane * 8;
   const bool l2 = seg < 2 * a.H * a.dk / kSeg;
-  F2 w[kTaps][4], win[kHist][4], xf[4], y[4];
+  float w[kTaps][8], win[kHist][8], xf[8], y[8];
   load_taps(a.conv_w, c0, w);
-  history<T, false>(state, n, C, c0, win);
+  history8<T>(state, n, C, c0, win);
   widen8<T>(load8(static_cast<const T*>(a.qkv) + n * C + c0), xf);
   conv_token(w, win, xf, l2, y);
   if (c0 < (int64_t)a.H * a.dk) {

@@ -91,9 +91,13 @@ extern "C" int gdn_prefill_noalloc(const void* q, const void* k, const void* v,
   a.map.T = varlen ? T_total : seqlen;
   a.map.chunks_per_seq = varlen ? 0 : (seqlen + kC - 1) / kC;
   a.max_chunks = max_chunks_bound(batch, T_total, varlen, seqlen);
-  // bf16 I/O runs on the tensor cores, fp32 I/O on the CUDA cores
+  // bf16 I/O runs on the tensor cores, fp32 I/O on the CUDA cores; the same
+  // launch forms as gdn_prefill (the fused cooperative one where it fits: its
+  // ready flags are cleared before the launch, so the array's leftovers from
+  // an earlier call do not matter)
   const bool tc = io_dtype == GDN_BF16;
   a.dv = dv;
+  a.allow_overlap = true;
   const size_t off_bytes = varlen ? align_up(((size_t)batch + 1) * 4, 256) : 0;
   const size_t work_bytes = tc ? prefill_tc_scratch_bytes(a.max_chunks, heads, dv)
                                : prefill_simt_scratch_bytes(a.max_chunks, heads, dv);

@@ -274,8 +274,9 @@ int gdn_prefill_backward_ws(const void* q, const void* k, const void* v, const f
  * no request can fail on an allocation or fragment the pool, processes whose
  * device memory belongs to another allocator that forbids raw CUDA
  * allocations, runtimes with a static memory budget -- call this instead.
- * It takes the same arguments, runs the same kernels and returns the same
- * results, and calls no allocator: its scratch is one static device array of
+ * It takes the same arguments, runs the same kernels in the same launch
+ * forms (at bf16 the fused cooperative form where it fits) and returns the
+ * same results, and calls no allocator: its scratch is one static device array of
  * 64 MiB (enough for about 6600 tokens of a 6-head bf16 layer, or about 4800
  * with fp32 I/O), which every GPU that loads the library holds until the
  * process exits.

@@ -4,9 +4,10 @@ start-up, processes whose device memory belongs to another allocator, static
 memory budgets).  It keeps its scratch in one static device array instead of
 asking cudaMallocAsync for it.  Here it is called through the C ABI twice in
 a row, on different inputs (the array keeps the previous call's contents),
-and each result is compared with gdn_prefill's on the same inputs within the
-tolerances of the parity tests.  A problem larger than the array is rejected
-before anything runs.
+and each result is compared with gdn_prefill's on the same inputs: the same
+launch form and the same bits at bf16 (the fused cooperative form), within
+the parity tests' tolerance at fp32.  A problem larger than the array is
+rejected before anything runs.
 
 This file is named to be collected last, and it passes both on its own in a
 fresh process and after the rest of the suite."""
@@ -49,6 +50,13 @@ def _call(f, x, out, S_final, io):
              code, torch.cuda.current_stream().cuda_stream)
 
 
+def _last_form(gdn_lib):
+    """The tensor-core prefill's last launch form (1: fused cooperative)."""
+    f = gdn_lib.load().gdn_testing_last_prefill_form
+    f.restype = ctypes.c_int32
+    return int(f())
+
+
 def _rel(a, b):
     a, b = a.double().cpu(), b.double().cpu()
     return float(torch.linalg.norm(a - b) / torch.linalg.norm(b))
@@ -67,9 +75,13 @@ def test_noalloc_matches_prefill_on_two_calls(gdn_lib, io):
         S_final = torch.full((len(case.lengths), case.H, 256, 256), float("nan"), device="cuda")
         assert _call(f, x, out, S_final, io) == 0
         assert gdn_lib.device_status() == 0
+        form = _last_form(gdn_lib)
         ref_out, ref_S = gdn_lib.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"],
                                          x["cu_seqlens"])
         assert gdn_lib.device_status() == 0
+        if io == torch.bfloat16:
+            assert form == 1 and _last_form(gdn_lib) == 1, case.name
+            assert torch.equal(out, ref_out) and torch.equal(S_final, ref_S), case.name
         assert _rel(out.float(), ref_out.float()) <= TOL[io], case.name
         assert _rel(S_final, ref_S) <= TOL[io], case.name
 
