@@ -91,9 +91,8 @@ def test_prefill_dv512_split_form(gdn_lib):
 
 
 def test_prefill_dv512_fused_matches_split_bitwise(gdn_lib):
-    """At dv = 512 the fused launch and the split one (which the no-allocation
-    entry point always takes) agree bit for bit."""
-    import ctypes
+    """At dv = 512 the fused launch and the split one (what gdn_prefill_scan
+    runs with one segment) agree bit for bit."""
     lens = [700, 64, 1, 900]
     H, dv = 2, 512
     case = PrefillCase("dv512 fused vs split", lens, H=H, dv=dv, io_dtype=torch.bfloat16, seed=76,
@@ -101,14 +100,8 @@ def test_prefill_dv512_fused_matches_split_bitwise(gdn_lib):
     x = to_dev(gdn_inputs.make_prefill(case, device="cpu"))
     out, Sf = run_gpu(gdn_lib, x)
     assert _last_form(gdn_lib) == 1
-    f = gdn_lib.load().gdn_prefill_noalloc
-    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-    f.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, vp]
-    out1, Sf1 = torch.empty_like(out), torch.empty_like(Sf)
-    rc = f(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), x["alpha"].data_ptr(),
-           x["beta"].data_ptr(), x["S0"].data_ptr(), x["cu_seqlens"].data_ptr(), out1.data_ptr(),
-           Sf1.data_ptr(), len(lens), sum(lens), H, 256, dv, 1,
-           torch.cuda.current_stream().cuda_stream)
-    assert rc == 0 and gdn_lib.device_status() == 0
+    out1, Sf1 = gdn_lib.prefill_scan(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"],
+                                     x["cu_seqlens"], segments=1)
+    assert gdn_lib.device_status() == 0
     assert _last_form(gdn_lib) == 0
     assert torch.equal(out, out1) and torch.equal(Sf, Sf1)

@@ -214,24 +214,6 @@ def _last_form(gdn_lib):
     return int(f())
 
 
-def _prefill_noalloc(gdn_lib, x, N, seqlen, H):
-    import ctypes
-    f = gdn_lib.load().gdn_prefill_noalloc
-    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-    f.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, vp]
-    T_tot = x["q"].shape[0] * x["q"].shape[1]
-    out = torch.empty(T_tot, H, 256, dtype=torch.bfloat16, device=DEV)
-    Sf = torch.empty(N, H, 256, 256, dtype=torch.float32, device=DEV)
-    cu = x["cu_seqlens"]
-    rc = f(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), x["alpha"].data_ptr(),
-           x["beta"].data_ptr(), x["S0"].data_ptr() if x["S0"] is not None else None,
-           cu.data_ptr() if cu is not None else None,
-           out.data_ptr(), Sf.data_ptr(), N, seqlen, H, 256, 256, 1,
-           torch.cuda.current_stream().cuda_stream)
-    assert rc == 0 and gdn_lib.device_status() == 0
-    return out, Sf
-
-
 @pytest.mark.parametrize("lens,varlen", [([4160], False), ([700, 64, 1, 2000], True)])
 def test_prefill_fused_against_oracle(gdn_lib, lens, varlen):
     """Few sequences x heads: the tensor-core prefill runs as one cooperative
@@ -246,16 +228,17 @@ def test_prefill_fused_against_oracle(gdn_lib, lens, varlen):
 @pytest.mark.parametrize("lens,varlen", [([4160], False), ([700, 64, 1, 2000], True)])
 def test_prefill_fused_matches_split_bitwise(gdn_lib, lens, varlen):
     """The fused launch and the split one (per-chunk kernel, then state-pass
-    kernel; the no-allocation entry point always takes it) do the same
-    arithmetic in the same order, so they agree bit for bit."""
+    kernel: what gdn_prefill_scan runs with one segment, every sequence left
+    whole) do the same arithmetic in the same order, so they agree bit for
+    bit."""
     H = 2
     case = PrefillCase("fused vs split", lens, H=H, io_dtype=torch.bfloat16, seed=62, varlen=varlen)
     x = to_dev(gdn_inputs.make_prefill(case, device="cpu"))
     out, Sf = run_gpu(gdn_lib, x)
     assert _last_form(gdn_lib) == 1
-    N = len(lens)
-    seqlen = sum(lens) if varlen else lens[0]
-    out1, Sf1 = _prefill_noalloc(gdn_lib, x, N, seqlen, H)
+    out1, Sf1 = gdn_lib.prefill_scan(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"],
+                                     x["cu_seqlens"], segments=1)
+    assert gdn_lib.device_status() == 0
     assert _last_form(gdn_lib) == 0
     assert torch.equal(out.reshape(out1.shape), out1) and torch.equal(Sf, Sf1)
 
