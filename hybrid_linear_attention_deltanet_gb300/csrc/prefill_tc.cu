@@ -1228,7 +1228,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     // (fused read-out) every kReadoutStep chunks: the rows of chunks
     // [cb, ci) are out (copied before the barrier).  A release waits for the
     // CTA's stores to drain, so it is not made every chunk.
-    if (kFused && norm && ng.flags && it > 0 && it % kReadoutStep == 0 && tid == 128)
+    if (kFused && ng.flags && it > 0 && it % kReadoutStep == 0 && tid == 128)
       st_release_gpu(ng.flags + unit, (uint32_t)it);
 
     // 3. D_S = (dU)^T K (commit m2) ; D_O += U^T P^^T (commit mo)
@@ -1340,7 +1340,7 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
   }
   // the last chunk's output rows
   if (!s_abort && ce > cb) copy_out_prev((int)((ce - cb - 1) & 1));
-  if (kFused && norm && ng.flags && ce > cb) {   // and finally all of them
+  if (kFused && ng.flags && ce > cb) {   // and finally all of them
     __syncthreads();
     if (!s_abort && tid == 128) st_release_gpu(ng.flags + unit, (uint32_t)(ce - cb));
   }
@@ -1573,10 +1573,13 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int u = blockIdx.x;
     const int ns = dv / 128, n = u / (ns * H);
     const int64_t per_seq = (int64_t)H * dv * kDK;
-    const NormGate none{};
+    // the state units only report their progress to the read-out (gate and
+    // weight stay with the workers), so no read-out arithmetic is in their chains
+    NormGate progress{};
+    if (kNorm) progress.flags = ng.flags;
     state_role<true>(sm, &tm_kb, S0 ? S0 + n * per_seq : nullptr, out,
                      S_final ? S_final + n * per_seq : nullptr, map, H, scratch, ready, status,
-                     trace, trace_chunks, dv, n, (u / ns) % H, u % ns, sdump, kNorm ? ng : none);
+                     trace, trace_chunks, dv, n, (u / ns) % H, u % ns, sdump, progress);
   } else {
     int64_t positions = map.chunks_per_seq;
     if (map.cu_seqlens) {
