@@ -60,6 +60,14 @@ __device__ __forceinline__ uint32_t piece(uint32_t r, uint32_t q) {
   return (r >> 7) * 16384u + (r & 127u) * 128u + ((q ^ (r & 7u)) << 4);
 }
 
+// 32 bytes from global memory (read-only path) as two float4; p 32-byte aligned
+__device__ __forceinline__ void ld32_nc(const float* p, float4& lo, float4& hi) {
+  asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w), "=f"(hi.x), "=f"(hi.y),
+                 "=f"(hi.z), "=f"(hi.w)
+               : "l"(p));
+}
+
 template <bool kTA, bool kTB, int kNB>
 __global__ void __launch_bounds__(kTgThreads, 2) tgemm_kernel(TgArgs g) {
   using Lay = TgLayout<kNB>;
@@ -89,6 +97,13 @@ __global__ void __launch_bounds__(kTgThreads, 2) tgemm_kernel(TgArgs g) {
   const int nslab = g.K / kTgSlab;
 
   float4 rx[kXL], ry[kYL];
+  // The transposed operands are read a row of K a lane: each lane takes two
+  // adjacent 16-byte pieces of its row (all of a 32-byte sector), load j
+  // covering columns ym0(j) / xn0(j) .. + 3.
+  // (one 256-bit load for each pair, on 32-byte aligned rows: launch_tgemm
+  // checks the alignment)
+  auto ym0 = [&](int j) { return 8 * warp + 4 * j; };
+  auto xn0 = [&](int j) { return 8 * (warp + 8 * (j >> 1)) + 4 * (j & 1); };
   // slab s of unit b into registers
   auto load = [&](int64_t b, int s) {
     const float* A = g.A + b * g.sA;
@@ -99,9 +114,8 @@ __global__ void __launch_bounds__(kTgThreads, 2) tgemm_kernel(TgArgs g) {
       if (!kTA) {   // row m of A, 16-byte piece q
         const int e = tid + j * kTgThreads, m = e >> 3, q = e & 7;
         ry[j] = __ldg(reinterpret_cast<const float4*>(A + (size_t)m * g.lda + k0 + 4 * q));
-      } else {      // row k0 + lane of A, m = 4 (warp + 8 j) .. + 3
-        const int m0 = 4 * (warp + 8 * j);
-        ry[j] = __ldg(reinterpret_cast<const float4*>(A + (size_t)(k0 + lane) * g.lda + m0));
+      } else if ((j & 1) == 0) {   // row k0 + lane of A, m = m0 .. m0 + 7: one 32-byte load
+        ld32_nc(A + (size_t)(k0 + lane) * g.lda + ym0(j), ry[j], ry[j + 1]);
       }
     }
 #pragma unroll
@@ -112,11 +126,12 @@ __global__ void __launch_bounds__(kTgThreads, 2) tgemm_kernel(TgArgs g) {
         const size_t o = g.b_tiled ? ((size_t)(k0 / 4 + q) * g.b_tiled + n) * 4
                                    : (size_t)n * g.ldb + k0 + 4 * q;
         rx[j] = __ldg(reinterpret_cast<const float4*>(B + o));
-      } else {      // row k0 + lane of B, n = 4 (warp + 8 j) .. + 3
-        const int n0 = 4 * (warp + 8 * j);
-        const size_t o = g.b_tiled ? ((size_t)(n0 / 4) * g.b_tiled + k0 + lane) * 4
-                                   : (size_t)(k0 + lane) * g.ldb + n0;
-        rx[j] = __ldg(reinterpret_cast<const float4*>(B + o));
+      } else if (g.b_tiled) {   // tile n0 / 4, row k0 + lane (16 bytes, 512 B a warp)
+        const int n0 = xn0(j);
+        rx[j] = __ldg(reinterpret_cast<const float4*>(
+            B + ((size_t)(n0 / 4) * g.b_tiled + k0 + lane) * 4));
+      } else if ((j & 1) == 0) {   // row k0 + lane of B, n = n0 .. n0 + 7: one 32-byte load
+        ld32_nc(B + (size_t)(k0 + lane) * g.ldb + xn0(j), rx[j], rx[j + 1]);
       }
     }
   };
@@ -129,7 +144,7 @@ __global__ void __launch_bounds__(kTgThreads, 2) tgemm_kernel(TgArgs g) {
         const int e = tid + j * kTgThreads, m = e >> 3, q = e & 7;
         *reinterpret_cast<float4*>(Y + piece(m, q)) = ry[j];
       } else {
-        const int m0 = 4 * (warp + 8 * j);
+        const int m0 = ym0(j);
         const float v[4] = {ry[j].x, ry[j].y, ry[j].z, ry[j].w};
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -143,7 +158,7 @@ __global__ void __launch_bounds__(kTgThreads, 2) tgemm_kernel(TgArgs g) {
         const int n = g.b_tiled ? e % kNr : e >> 3, q = g.b_tiled ? e / kNr : e & 7;
         *reinterpret_cast<float4*>(X + piece(n, q)) = rx[j];
       } else {
-        const int n0 = 4 * (warp + 8 * j);
+        const int n0 = xn0(j);
         const float v[4] = {rx[j].x, rx[j].y, rx[j].z, rx[j].w};
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -266,15 +281,28 @@ cudaError_t launch_nb(const TgArgs& g, bool tA, bool tB, cudaStream_t st) {
 }  // namespace
 
 bool tgemm_shape_ok(int N, int K, int lda, int ldb, int ldc, bool tA, bool tB, int b_tiled) {
-  // 16-byte loads: leading dimensions and K multiples of 4
+  // 16-byte loads: leading dimensions and K multiples of 4; 32-byte loads of
+  // the transposed A and of a row-major B stored [K][N]: multiples of 8
   if ((N != 64 && N != 256) || (K != 64 && K != 256)) return false;
   if (lda % 4 || ldc < N) return false;
+  if (tA && lda % 8) return false;
   if (!tA ? lda < K : lda < 64) return false;
   if (b_tiled) {   // an R x 256 tiled matrix: 256 columns, R = N (kTB) or K
     return b_tiled == (tB ? N : K) && (tB ? K : N) == 256;
   }
-  if (ldb % 4) return false;
+  if (ldb % 4 || (!tB && ldb % 8)) return false;
   if (!tB ? ldb < N : ldb < K) return false;
+  return true;
+}
+
+// base addresses and unit strides the loads need: 16 bytes throughout, 32
+// for the operands read with 32-byte loads
+bool tgemm_aligned(const float* A, size_t sA, const float* B, size_t sB, bool tA, bool tB,
+                   int b_tiled) {
+  const bool a32 = tA, b32 = !tB && !b_tiled;
+  if ((((uintptr_t)A | (uintptr_t)B) & 15) || sA % 4 || sB % 4) return false;
+  if (a32 && (((uintptr_t)A & 31) || sA % 8)) return false;
+  if (b32 && (((uintptr_t)B & 31) || sB % 8)) return false;
   return true;
 }
 
@@ -285,6 +313,7 @@ cudaError_t launch_tgemm(const float* A, size_t sA, int lda, const float* B, siz
                          cudaStream_t st) {
   if (batch <= 0) return cudaSuccess;
   if (!tgemm_shape_ok(N, K, lda, ldb, ldc, tA, tB, b_tiled)) return cudaErrorInvalidValue;
+  if (!tgemm_aligned(A, sA, B, sB, tA, tB, b_tiled)) return cudaErrorMisalignedAddress;
   TgArgs g{A, sA, lda, B, sB, ldb, Cin, C, sC, ldc, col, sCol, N, K, alpha, beta, mask, batch,
            status, b_tiled};
   const cudaError_t e = N == 256 ? launch_nb<2>(g, tA, tB, st) : launch_nb<1>(g, tA, tB, st);
@@ -307,8 +336,8 @@ extern "C" int gdn_testing_tgemm(const float* A, int64_t sA, int32_t lda, int32_
     return GDN_ERR_INVALID_ARG;
   if (b_tiled < 0 || !tgemm_shape_ok(N, K, lda, ldb, ldc, tA != 0, tB != 0, b_tiled))
     return GDN_ERR_UNSUPPORTED;
-  const uintptr_t al = (uintptr_t)A | (uintptr_t)B;
-  if ((al & 15) || (sA % 4) || (sB % 4)) return GDN_ERR_ALIGNMENT;
+  if (!tgemm_aligned(A, (size_t)sA, B, (size_t)sB, tA != 0, tB != 0, b_tiled))
+    return GDN_ERR_ALIGNMENT;
   unsigned* status = status_ptr();
   if (!status) return GDN_ERR_CUDA;
   return launch_tgemm(A, (size_t)sA, lda, B, (size_t)sB, ldb, Cin, C, (size_t)sC, ldc, col,

@@ -27,8 +27,11 @@ extern "C" {
  * A' is A stored [64][lda] (tA = 0) or [K][lda] (tA = 1); B' is B stored
  * [K][ldb] (tB = 0) or [N][ldb] (tB = 1); C and Cin are [64][ldc]; unit b's
  * arrays start sA, sB, sC, sCol floats after unit 0's.  Cin and col may be
- * null.  N in {64, 256}, K in {64, 256}, lda and ldb multiples of 4 (A and B
- * 16-byte aligned): GDN_ERR_UNSUPPORTED / GDN_ERR_ALIGNMENT otherwise.
+ * null.  N in {64, 256}, K in {64, 256}, lda and ldb multiples of 4, A, B,
+ * sA and sB 16-byte aligned; with tA = 1, lda, sA and A 32-byte aligned (8
+ * floats), and with tB = 0 (not tiled) ldb, sB and B likewise:
+ * GDN_ERR_UNSUPPORTED (shapes, leading dimensions) / GDN_ERR_ALIGNMENT
+ * (addresses, unit strides) otherwise.
  * b_tiled = R > 0: each unit's B is an R x 256 matrix M in the backward's
  * tiled state layout (element (r, c) at ((c / 4) R + r) 4 + c % 4) and B' = M
  * (tB = 0, R = K, N = 256) or M transposed (tB = 1, R = N, K = 256); ldb is

@@ -133,3 +133,16 @@ def test_tgemm_rejects_unsupported_shapes(gdn_lib):
     assert f(p, 0, 256, 0, p, 0, 256, 0, None, 0.0, p, 0, 256, None, 0, 256, 256, 1.0, 3, 1, 0, s) != 0
     # a tiled B must be 256 columns wide with R = K (or N when transposed)
     assert f(p, 0, 64, 0, p, 0, 64, 0, None, 0.0, p, 0, 64, None, 0, 64, 64, 1.0, 0, 1, 64, s) != 0
+    # the transposed A and a row-major B stored [K][N] are read 32 bytes a
+    # lane: lda / ldb multiples of 8 floats, addresses and unit strides 32-byte
+    # aligned (all rejected before any launch)
+    GDN_ERR_ALIGNMENT = 3
+    assert f(p, 0, 68, 1, p, 0, 64, 1, None, 0.0, p, 0, 64, None, 0, 64, 64, 1.0, 0, 1, 0, s) != 0
+    assert f(p, 0, 64, 0, p, 0, 68, 0, None, 0.0, p, 0, 64, None, 0, 64, 64, 1.0, 0, 1, 0, s) != 0
+    q = p + 16   # 16-byte but not 32-byte aligned
+    assert f(q, 0, 64, 1, p, 0, 64, 1, None, 0.0, p, 0, 64, None, 0, 64, 64, 1.0, 0, 1, 0,
+             s) == GDN_ERR_ALIGNMENT
+    assert f(p, 0, 64, 0, q, 0, 64, 0, None, 0.0, p, 0, 64, None, 0, 64, 64, 1.0, 0, 1, 0,
+             s) == GDN_ERR_ALIGNMENT
+    assert f(p, 4, 64, 1, p, 0, 64, 1, None, 0.0, p, 0, 64, None, 0, 64, 64, 1.0, 0, 2, 0,
+             s) == GDN_ERR_ALIGNMENT
