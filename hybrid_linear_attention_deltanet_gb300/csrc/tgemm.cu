@@ -60,9 +60,11 @@ __device__ __forceinline__ uint32_t piece(uint32_t r, uint32_t q) {
   return (r >> 7) * 16384u + (r & 127u) * 128u + ((q ^ (r & 7u)) << 4);
 }
 
-// 32 bytes from global memory (read-only path) as two float4; p 32-byte aligned
+// 32 bytes from global memory (read-only path) as two float4; p 32-byte
+// aligned.  The operands are never written while the kernel runs, so the load
+// may be scheduled freely (not volatile).
 __device__ __forceinline__ void ld32_nc(const float* p, float4& lo, float4& hi) {
-  asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+  asm("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w), "=f"(hi.x), "=f"(hi.y),
                  "=f"(hi.z), "=f"(hi.w)
                : "l"(p));
@@ -118,21 +120,24 @@ __global__ void __launch_bounds__(kTgThreads, 2) tgemm_kernel(TgArgs g) {
         ld32_nc(A + (size_t)(k0 + lane) * g.lda + ym0(j), ry[j], ry[j + 1]);
       }
     }
+    if (kTB) {
 #pragma unroll
-    for (int j = 0; j < kXL; ++j) {
-      if (kTB) {    // row n of B, 16-byte piece q (tiled: n fastest, 512 B a warp)
+      for (int j = 0; j < kXL; ++j) {   // row n of B, 16-byte piece q (tiled: n fastest, 512 B a warp)
         const int e = tid + j * kTgThreads;
         const int n = g.b_tiled ? e % kNr : e >> 3, q = g.b_tiled ? e / kNr : e & 7;
         const size_t o = g.b_tiled ? ((size_t)(k0 / 4 + q) * g.b_tiled + n) * 4
                                    : (size_t)n * g.ldb + k0 + 4 * q;
         rx[j] = __ldg(reinterpret_cast<const float4*>(B + o));
-      } else if (g.b_tiled) {   // tile n0 / 4, row k0 + lane (16 bytes, 512 B a warp)
-        const int n0 = xn0(j);
-        rx[j] = __ldg(reinterpret_cast<const float4*>(
-            B + ((size_t)(n0 / 4) * g.b_tiled + k0 + lane) * 4));
-      } else if ((j & 1) == 0) {   // row k0 + lane of B, n = n0 .. n0 + 7: one 32-byte load
-        ld32_nc(B + (size_t)(k0 + lane) * g.ldb + xn0(j), rx[j], rx[j + 1]);
       }
+    } else if (g.b_tiled) {
+#pragma unroll
+      for (int j = 0; j < kXL; ++j)   // tile n0 / 4, row k0 + lane (16 bytes, 512 B a warp)
+        rx[j] = __ldg(reinterpret_cast<const float4*>(
+            B + ((size_t)(xn0(j) / 4) * g.b_tiled + k0 + lane) * 4));
+    } else {
+#pragma unroll
+      for (int j = 0; j < kXL; j += 2)   // row k0 + lane of B, n = n0 .. n0 + 7: one 32-byte load
+        ld32_nc(B + (size_t)(k0 + lane) * g.ldb + xn0(j), rx[j], rx[j + 1]);
     }
   };
   auto stage = [&](int bf) {
