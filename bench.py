@@ -888,21 +888,22 @@ def run_profile(args):
                                  dsf)
     elif args.profile == "tgemm":
         # the backward's tensor-core GEMM in its dO S shape (B' = S in the
-        # tiled state layout; K = dv = 256, N = dk = 256) on 1500 units:
-        # 384 MB of S, 96 MB each of dO and C
+        # tiled state layout, bf16 as the forward re-run stores it; K = dv =
+        # 256, N = dk = 256) on 1500 units: 197 MB of S, 98 MB each of dO and C
         import ctypes
         f = gdn.load().gdn_testing_tgemm
         vp, i32, i64, fl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
         f.argtypes = [vp, i64, i32, i32, vp, i64, i32, i32, vp, fl, vp, i64, i32, vp, i64, i32,
-                      i32, fl, i32, i64, i32, vp]
+                      i32, fl, i32, i64, i32, i32, vp]
         units = 1500
         A = torch.randn(units, 64, 256, device=dev)
-        B = torch.randn(units, 256, 256, device=dev)
+        B = torch.randn(units, 256, 256, device=dev).to(torch.bfloat16)
         C = torch.empty(units, 64, 256, device=dev)
         st = torch.cuda.current_stream().cuda_stream
         for _ in range(args.warmup + args.steps):
             assert f(A.data_ptr(), 64 * 256, 256, 0, B.data_ptr(), 256 * 256, 256, 0, None, 0.0,
-                     C.data_ptr(), 64 * 256, 256, None, 0, 256, 256, 1.0, 0, units, 256, st) == 0
+                     C.data_ptr(), 64 * 256, 256, None, 0, 256, 256, 1.0, 0, units, 256, 1,
+                     st) == 0
     elif args.profile == "decode_layer":
         lc = gdn_inputs.layer_decode_256()
         lx = gdn_inputs.make_layer(lc, device=dev)

@@ -56,7 +56,8 @@ struct Bwd {
   float *G, *B, *BG;              // [64]: cumsum log alpha, beta, beta*gamma
   float *KK, *QK, *Tm, *TmB, *TmU, *Ph;   // [64][64]
   float *W, *Ut;                  // [64][256] [64][dv]
-  float *Sst, *dSp;               // [dv][256]
+  float *Sst, *dSp;               // [dv][256]; Sst holds bf16 in the tiled layout with bf16 I/O
+                                  // at dv = 256 (the forward re-run's dump), else fp32
   float *dU, *U, *TdU;            // [64][dv]
   float *dQh, *dW, *dK1, *TdW, *dKa, *dQa;   // [64][256]
   float *dPh, *dTm, *X, *dA, *Ms, *FG;       // [64][64]
@@ -453,6 +454,9 @@ fwd_states_kernel(const float* __restrict__ S0, SeqMap map, int32_t H, Bwd s) {
 // <dS', S_start> of each (chunk, head) over 16-row slices of the state, as
 // the CUDA-core reverse pass leaves them (used with the tensor-core one):
 // one CTA per (unit, slice).
+// kBfS: the states are bf16 (the tiled layout at dv = 256, the same element
+// order as dS'), else fp32
+template <bool kBfS>
 __global__ void __launch_bounds__(kThreads) dgl_kernel(Bwd s) {
   __shared__ float red[kThreads / 32];
   const int64_t u = blockIdx.x;
@@ -460,9 +464,18 @@ __global__ void __launch_bounds__(kThreads) dgl_kernel(Bwd s) {
   const size_t off = u * s.sS() + (size_t)sl * kNS * kDK;
   const float4* a = reinterpret_cast<const float4*>(s.dSp + off);
   const float4* b = reinterpret_cast<const float4*>(s.Sst + off);
+  const uint2* bh = reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(s.Sst) + off);
   float part = 0.f;
   for (int e = tid; e < kNS * kDK / 4; e += kThreads) {
-    const float4 x = a[e], y = b[e];
+    const float4 x = a[e];
+    float4 y;
+    if (kBfS) {
+      const uint2 w = bh[e];
+      y = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                      __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+    } else {
+      y = b[e];
+    }
     part = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, part))));
   }
 #pragma unroll
@@ -813,10 +826,10 @@ cudaError_t gemm(cudaStream_t st, bool tA, bool tB, Mat A, Mat B, float* C, size
 cudaError_t gemm_io(int io_dtype, unsigned* status, cudaStream_t st, bool tA, bool tB, Mat A,
                     Mat B, float* C, size_t sC, int ldc, int N, int K, float alpha,
                     const float* Cin, float beta, int mask, const float* col, size_t sCol,
-                    int64_t batch, int b_tiled = 0) {
+                    int64_t batch, int b_tiled = 0, int b_bf16 = 0) {
   if (io_dtype == GDN_BF16 && tgemm_shape_ok(N, K, A.ld, B.ld, ldc, tA, tB, b_tiled))
     return launch_tgemm(A.p, A.stride, A.ld, B.p, B.stride, B.ld, Cin, C, sC, ldc, col, sCol, N,
-                        K, alpha, beta, mask, batch, tA, tB, b_tiled, status, st);
+                        K, alpha, beta, mask, batch, tA, tB, b_tiled, b_bf16, status, st);
   if (b_tiled) return cudaErrorInvalidValue;
   return gemm(st, tA, tB, A, B, C, sC, ldc, N, K, alpha, Cin, beta, mask, col, sCol, batch);
 }
@@ -897,8 +910,10 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     for (int i = 0; i < n; ++i) {
       const G& g = list[i];
       const int bt = tiled && (g.B.p == s.Sst || g.B.p == s.dSp) ? dv : 0;
+      const int bbf = tiled && g.B.p == s.Sst ? 1 : 0;   // the states are bf16 there
       const cudaError_t r = gemm_io(io_dtype, a.status, q, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc,
-                                    g.N, g.K, g.alpha, g.Cin, g.beta, g.mask, g.col, kC, units, bt);
+                                    g.N, g.K, g.alpha, g.Cin, g.beta, g.mask, g.col, kC, units, bt,
+                                    bbf);
       if (r != cudaSuccess) return r;
     }
     return cudaSuccess;
@@ -1019,7 +1034,10 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
       if (e != cudaSuccess) return e;
     }
     // <dS', S_start> partials
-    dgl_kernel<<<dim3((unsigned)units, (unsigned)(dv / kNS)), kThreads, 0, st>>>(s);
+    if (tiled)
+      dgl_kernel<true><<<dim3((unsigned)units, (unsigned)(dv / kNS)), kThreads, 0, st>>>(s);
+    else
+      dgl_kernel<false><<<dim3((unsigned)units, (unsigned)(dv / kNS)), kThreads, 0, st>>>(s);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   } else {

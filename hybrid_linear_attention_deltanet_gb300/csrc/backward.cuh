@@ -24,12 +24,13 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
 // (kind::tf32; tgemm.cu): per unit b, C = alpha * (A' B') diag(col) + beta *
 // Cin, masked (1: keep n <= m, 2: n < m), m < 64.  A' = A [64][K] or (tA)
 // stored [K][64]; B' = B [K][N] or (tB) stored [N][K], or (b_tiled = R > 0)
-// the tiled_states layout of an R x 256 matrix.  N, K in {64, 256}.
+// the tiled_states layout of an R x 256 matrix, fp32 or (b_bf16) bf16.  N, K
+// in {64, 256}.
 bool tgemm_shape_ok(int N, int K, int lda, int ldb, int ldc, bool tA, bool tB, int b_tiled);
 cudaError_t launch_tgemm(const float* A, size_t sA, int lda, const float* B, size_t sB, int ldb,
                          const float* Cin, float* C, size_t sC, int ldc, const float* col,
                          size_t sCol, int N, int K, float alpha, float beta, int mask,
-                         int64_t batch, bool tA, bool tB, int b_tiled, unsigned* status,
-                         cudaStream_t st);
+                         int64_t batch, bool tA, bool tB, int b_tiled, int b_bf16,
+                         unsigned* status, cudaStream_t st);
 
 }  // namespace gdn

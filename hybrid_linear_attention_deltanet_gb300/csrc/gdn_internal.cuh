@@ -311,12 +311,14 @@ struct ConvIn {
   const uint8_t* seg_role = nullptr;
 };
 
-// The backward's fp32 chunk-start states and state gradients dS' at dv = 256
+// The backward's chunk-start states and state gradients dS' at dv = 256
 // (bf16 I/O, where the tensor cores produce and consume them) sit in
 // 4-column tiles: element (v, c) of a unit's [dv][dk] matrix at
 // ((c / 4) * dv + v) * 4 + c % 4.  A warp whose lanes hold consecutive rows
-// then stores 512 contiguous bytes, and a GEMM that reads columns c .. c+3 of
-// consecutive rows reads contiguous memory.  Other dv: row-major.
+// then stores contiguous bytes, and a GEMM that reads columns c .. c+3 of
+// consecutive rows reads contiguous memory.  The states are bf16 there (the
+// forward's MMAs read S as bf16 too; dS' stays fp32).  Other dv: row-major
+// fp32.
 __host__ __device__ constexpr bool tiled_states(int dv) { return dv == 256; }
 
 struct PrefillLaunch {
@@ -331,7 +333,8 @@ struct PrefillLaunch {
   void* scratch;        // device scratch of the size the path's *_scratch_bytes asks for
   bool allow_overlap;   // tensor-core path may run prep and state pass in one cooperative launch
   float* state_dump;    // tensor-core path: every chunk's start state, [chunks * H] units of
-                        // dv x dk fp32 (tiled_states layout at dv = 256), for the
+                        // dv x dk (bf16 in the tiled_states layout at dv = 256, the
+                        // first half of the array; fp32 row-major otherwise), for the
                         // backward's forward re-run, or nullptr
   bool state_only;      // the per-chunk factors are already in scratch (an earlier call on
                         // the same inputs and map): run the state pass only

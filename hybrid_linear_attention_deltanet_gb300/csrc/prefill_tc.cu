@@ -1175,13 +1175,16 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
     // (optional) this chunk's start state, for the backward's forward re-run
     if (sdump) {
       const size_t v = 128 * slice + iloc;
-      float* base = sdump + (size_t)(ci * H + h) * dv * kDK;
-      if (tiled_states(dv)) {   // lanes: consecutive rows, 512 contiguous bytes a store
-        float4* p = reinterpret_cast<float4*>(base) + (size_t)32 * colhalf * dv + v;
+      if (tiled_states(dv)) {   // bf16 tiles; lanes: consecutive rows, 256 contiguous bytes a store
+        uint2* p = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(sdump) +
+                                            (size_t)(ci * H + h) * dv * kDK) +
+                   (size_t)32 * colhalf * dv + v;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          p[(size_t)j * dv] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+          p[(size_t)j * dv] = make_uint2(pack_bf16(S[4 * j], S[4 * j + 1]),
+                                         pack_bf16(S[4 * j + 2], S[4 * j + 3]));
       } else {
+        float* base = sdump + (size_t)(ci * H + h) * dv * kDK;
         float4* p = reinterpret_cast<float4*>(base + v * kDK + 128 * colhalf);
 #pragma unroll
         for (int j = 0; j < 32; ++j)

@@ -45,6 +45,7 @@ struct TgArgs {
   int64_t batch;
   unsigned* status;
   int b_tiled;   // 0: B as ldb says; R > 0: the tiled layout with R rows
+  int b_bf16;    // (tiled B only) its elements are bf16, widened while staging
 };
 
 template <int kNB>
@@ -58,6 +59,13 @@ struct TgLayout {
 // byte offset of 16-byte piece q (K elements 4q .. 4q+3 of the slab) of row r
 __device__ __forceinline__ uint32_t piece(uint32_t r, uint32_t q) {
   return (r >> 7) * 16384u + (r & 127u) * 128u + ((q ^ (r & 7u)) << 4);
+}
+
+// four bf16 (8 bytes, read-only path) widened exactly to fp32
+__device__ __forceinline__ float4 ld4_bf16(const __nv_bfloat16* p) {
+  const uint2 w = __ldg(reinterpret_cast<const uint2*>(p));
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
 }
 
 // 32 bytes from global memory (read-only path) as two float4; p 32-byte
@@ -120,7 +128,14 @@ __global__ void __launch_bounds__(kTgThreads, 2) tgemm_kernel(TgArgs g) {
         ld32_nc(A + (size_t)(k0 + lane) * g.lda + ym0(j), ry[j], ry[j + 1]);
       }
     }
-    if (kTB) {
+    const __nv_bfloat16* Bh = reinterpret_cast<const __nv_bfloat16*>(g.B) + b * g.sB;
+    if (kTB && g.b_bf16) {
+#pragma unroll
+      for (int j = 0; j < kXL; ++j) {   // tiled bf16: row n, 4 columns of piece q (256 B a warp)
+        const int e = tid + j * kTgThreads, n = e % kNr, q = e / kNr;
+        rx[j] = ld4_bf16(Bh + ((size_t)(k0 / 4 + q) * g.b_tiled + n) * 4);
+      }
+    } else if (kTB) {
 #pragma unroll
       for (int j = 0; j < kXL; ++j) {   // row n of B, 16-byte piece q (tiled: n fastest, 512 B a warp)
         const int e = tid + j * kTgThreads;
@@ -129,6 +144,10 @@ __global__ void __launch_bounds__(kTgThreads, 2) tgemm_kernel(TgArgs g) {
                                    : (size_t)n * g.ldb + k0 + 4 * q;
         rx[j] = __ldg(reinterpret_cast<const float4*>(B + o));
       }
+    } else if (g.b_tiled && g.b_bf16) {
+#pragma unroll
+      for (int j = 0; j < kXL; ++j)   // tile n0 / 4, row k0 + lane (8 bytes, 256 B a warp)
+        rx[j] = ld4_bf16(Bh + ((size_t)(xn0(j) / 4) * g.b_tiled + k0 + lane) * 4);
     } else if (g.b_tiled) {
 #pragma unroll
       for (int j = 0; j < kXL; ++j)   // tile n0 / 4, row k0 + lane (16 bytes, 512 B a warp)
@@ -314,13 +333,14 @@ bool tgemm_aligned(const float* A, size_t sA, const float* B, size_t sB, bool tA
 cudaError_t launch_tgemm(const float* A, size_t sA, int lda, const float* B, size_t sB, int ldb,
                          const float* Cin, float* C, size_t sC, int ldc, const float* col,
                          size_t sCol, int N, int K, float alpha, float beta, int mask,
-                         int64_t batch, bool tA, bool tB, int b_tiled, unsigned* status,
-                         cudaStream_t st) {
+                         int64_t batch, bool tA, bool tB, int b_tiled, int b_bf16,
+                         unsigned* status, cudaStream_t st) {
   if (batch <= 0) return cudaSuccess;
   if (!tgemm_shape_ok(N, K, lda, ldb, ldc, tA, tB, b_tiled)) return cudaErrorInvalidValue;
+  if (b_bf16 && !b_tiled) return cudaErrorInvalidValue;
   if (!tgemm_aligned(A, sA, B, sB, tA, tB, b_tiled)) return cudaErrorMisalignedAddress;
   TgArgs g{A, sA, lda, B, sB, ldb, Cin, C, sC, ldc, col, sCol, N, K, alpha, beta, mask, batch,
-           status, b_tiled};
+           status, b_tiled, b_bf16 ? 1 : 0};
   const cudaError_t e = N == 256 ? launch_nb<2>(g, tA, tB, st) : launch_nb<1>(g, tA, tB, st);
   count_launches(1);
   return e;
@@ -335,19 +355,20 @@ extern "C" int gdn_testing_tgemm(const float* A, int64_t sA, int32_t lda, int32_
                                  const float* Cin, float beta, float* C, int64_t sC, int32_t ldc,
                                  const float* col, int64_t sCol, int32_t N, int32_t K,
                                  float alpha, int32_t mask, int64_t batch, int32_t b_tiled,
-                                 gdn_stream_t stream) {
+                                 int32_t b_bf16, gdn_stream_t stream) {
   if (!A || !B || !C || batch < 0 || sA < 0 || sB < 0 || sC < 0 || sCol < 0 || mask < 0 ||
       mask > 2)
     return GDN_ERR_INVALID_ARG;
   if (b_tiled < 0 || !tgemm_shape_ok(N, K, lda, ldb, ldc, tA != 0, tB != 0, b_tiled))
     return GDN_ERR_UNSUPPORTED;
+  if (b_bf16 < 0 || b_bf16 > 1 || (b_bf16 && !b_tiled)) return GDN_ERR_UNSUPPORTED;
   if (!tgemm_aligned(A, (size_t)sA, B, (size_t)sB, tA != 0, tB != 0, b_tiled))
     return GDN_ERR_ALIGNMENT;
   unsigned* status = status_ptr();
   if (!status) return GDN_ERR_CUDA;
   return launch_tgemm(A, (size_t)sA, lda, B, (size_t)sB, ldb, Cin, C, (size_t)sC, ldc, col,
                       (size_t)sCol, N, K, alpha, beta, mask, batch, tA != 0, tB != 0, b_tiled,
-                      status, (cudaStream_t)stream) == cudaSuccess
+                      b_bf16, status, (cudaStream_t)stream) == cudaSuccess
              ? GDN_OK
              : GDN_ERR_CUDA;
 }

@@ -35,14 +35,16 @@ extern "C" {
  * b_tiled = R > 0: each unit's B is an R x 256 matrix M in the backward's
  * tiled state layout (element (r, c) at ((c / 4) R + r) 4 + c % 4) and B' = M
  * (tB = 0, R = K, N = 256) or M transposed (tB = 1, R = N, K = 256); ldb is
- * then unused.  Operands round to tf32 (10 explicit mantissa bits); fp32
- * accumulation.
+ * then unused.  b_bf16 = 1 (tiled B only): M's elements are bf16 (B points at
+ * them, sB counts bf16 elements), widened exactly to fp32 -- the backward's
+ * chunk-start states at bf16 I/O.  Operands round to tf32 (10 explicit
+ * mantissa bits); fp32 accumulation.
  */
 int gdn_testing_tgemm(const float* A, int64_t sA, int32_t lda, int32_t tA, const float* B,
                       int64_t sB, int32_t ldb, int32_t tB, const float* Cin, float beta, float* C,
                       int64_t sC, int32_t ldc, const float* col, int64_t sCol, int32_t N,
                       int32_t K, float alpha, int32_t mask, int64_t batch, int32_t b_tiled,
-                      gdn_stream_t stream);
+                      int32_t b_bf16, gdn_stream_t stream);
 
 /*
  * gdn_testing_umma_gemm -- D[128][N] (fp32) = A[128][K] * B[N][K]^T with
