@@ -524,9 +524,12 @@ def decode_layer_step(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, conv_state, S, 
 def prefill_layer(qkv, conv_w, a_raw, b_raw, A_log, dt_bias, gate, norm_w, heads, S0=None,
                   cu_seqlens=None, conv_state_in=None, conv_state_out=None, eps=1e-5, act="silu",
                   y=None, S_final=None, return_final=True, stream=None):
-    """The mixer core over whole sequences in one pass (``gdn_prefill_layer``):
-    :func:`prepare`, :func:`prefill` and :func:`output_norm_gate` fused into
-    the tensor-core prefill (bf16, dk = dv = 256).  qkv [B, T, C] or [T, C]
+    """The mixer core over whole sequences in one call (``gdn_prefill_layer``):
+    what :func:`prepare`, :func:`prefill` and :func:`output_norm_gate` compute,
+    as the pre-recurrence pass and then the tensor-core prefill with the gated
+    RMSNorm applied inside it (for sequences in the segmented form, the
+    pre-recurrence steps inside the prefill's tile loads too); bf16, dk = dv =
+    256.  qkv [B, T, C] or [T, C]
     (packed with ``cu_seqlens``); a_raw, b_raw [.., H]; gate [.., H, dv];
     S0 / S_final [N, H, dv, dk]; conv states [N, 3, C].  Returns (y, S_final)."""
     lib = load()
