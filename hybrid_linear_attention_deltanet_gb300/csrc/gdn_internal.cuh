@@ -52,15 +52,8 @@ __device__ __forceinline__ F2 f2(float lo, float hi) {
   asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
   return r;
 }
-__device__ __forceinline__ float f2_lo(F2 a) {
-  float lo, hi;
+__device__ __forceinline__ void f2_split(F2 a, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
-  return lo;
-}
-__device__ __forceinline__ float f2_hi(F2 a) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
-  return hi;
 }
 __device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
   F2 r;
@@ -98,9 +91,10 @@ __device__ __forceinline__ float silu_sfu(float x) {
   return __fmul_rn(x, rcp_sfu(__fadd_rn(ex2_sfu(__fmul_rn(x, kNegLog2e)), 1.f)));
 }
 __device__ __forceinline__ F2 silu_pair(F2 x) {
-  const F2 t = f2_mul(x, f2(kNegLog2e, kNegLog2e));
-  const F2 d = f2_add(f2(ex2_sfu(f2_lo(t)), ex2_sfu(f2_hi(t))), f2(1.f, 1.f));
-  return f2_mul(x, f2(rcp_sfu(f2_lo(d)), rcp_sfu(f2_hi(d))));
+  float t0, t1, d0, d1;
+  f2_split(f2_mul(x, f2(kNegLog2e, kNegLog2e)), t0, t1);
+  f2_split(f2_add(f2(ex2_sfu(t0), ex2_sfu(t1)), f2(1.f, 1.f)), d0, d1);
+  return f2_mul(x, f2(rcp_sfu(d0), rcp_sfu(d1)));
 }
 // A lane's part of a row's sum of squares over its 8 values y[0..7]: the
 // even and the odd positions accumulate apart (in order), then add.
@@ -117,7 +111,9 @@ __device__ __forceinline__ float sumsq8(const F2 (&y)[4]) {
   F2 s = f2_mul(y[0], y[0]);
 #pragma unroll
   for (int k = 1; k < 4; ++k) s = f2_fma(y[k], y[k], s);
-  return __fadd_rn(f2_lo(s), f2_hi(s));
+  float e, o;
+  f2_split(s, e, o);
+  return __fadd_rn(e, o);
 }
 
 // ---------------------------------------------------------------------------

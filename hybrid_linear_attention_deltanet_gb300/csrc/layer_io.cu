@@ -146,14 +146,19 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const F2 (&f)[4]) {
   uint32_t w[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(f2_lo(f[i]), f2_hi(f[i]));
+    float lo, hi;
+    f2_split(f[i], lo, hi);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     w[i] = *reinterpret_cast<const uint32_t*>(&h);
   }
   *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 __device__ __forceinline__ void store8(float* p, const F2 (&f)[4]) {
-  reinterpret_cast<float4*>(p)[0] = make_float4(f2_lo(f[0]), f2_hi(f[0]), f2_lo(f[1]), f2_hi(f[1]));
-  reinterpret_cast<float4*>(p)[1] = make_float4(f2_lo(f[2]), f2_hi(f[2]), f2_lo(f[3]), f2_hi(f[3]));
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f2_split(f[i], v[2 * i], v[2 * i + 1]);
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
 // Elementwise activations of the streams are approximate to a few ulp (far

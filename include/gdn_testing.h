@@ -55,7 +55,7 @@ int gdn_testing_tgemm(const float* A, int64_t sA, int32_t lda, int32_t tA, const
  *                 bytes apart and 64-element MN blocks K*128 bytes apart; a
  *                 K-major image keeps 64 K elements per row and K blocks
  *                 R*128 bytes apart (R = 128 for A, N for B).
- *   *_lbo/*_sbo : leading / stride byte offsets written into the matrix
+ *   a_lbo, a_sbo, b_lbo, b_sbo : leading / stride byte offsets written into the matrix
  *                 descriptors (so a test can check the convention).
  *   a_via_tma   : 0: threads stage A in shared memory; 1: a 2-D TMA tensor
  *                 copy loads A (K-major only); 2: A is stored into TMEM
