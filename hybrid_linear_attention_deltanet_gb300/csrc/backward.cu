@@ -56,8 +56,9 @@ struct Bwd {
   float *G, *B, *BG;              // [64]: cumsum log alpha, beta, beta*gamma
   float *KK, *QK, *Tm, *TmB, *TmU, *Ph;   // [64][64]
   float *W, *Ut;                  // [64][256] [64][dv]
-  float *Sst, *dSp;               // [dv][256]; Sst holds bf16 in the tiled layout with bf16 I/O
-                                  // at dv = 256 (the forward re-run's dump), else fp32
+  float *Sst, *dSp;               // [dv][256]; bf16 in the tiled layout with bf16 I/O at
+                                  // dv = 256 (the forward re-run's and the reverse pass's
+                                  // stores), else fp32
   float *dU, *U, *TdU;            // [64][dv]
   float *dQh, *dW, *dK1, *TdW, *dKa, *dQa;   // [64][256]
   float *dPh, *dTm, *X, *dA, *Ms, *FG;       // [64][64]
@@ -454,28 +455,27 @@ fwd_states_kernel(const float* __restrict__ S0, SeqMap map, int32_t H, Bwd s) {
 // <dS', S_start> of each (chunk, head) over 16-row slices of the state, as
 // the CUDA-core reverse pass leaves them (used with the tensor-core one):
 // one CTA per (unit, slice).
-// kBfS: the states are bf16 (the tiled layout at dv = 256, the same element
-// order as dS'), else fp32
-template <bool kBfS>
+// kBf: dS' and the states are bf16 (the tiled layout at dv = 256, both in
+// the same element order), else fp32
+__device__ __forceinline__ float4 widen_bf16x4(uint2 w) {
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+}
+template <bool kBf>
 __global__ void __launch_bounds__(kThreads) dgl_kernel(Bwd s) {
   __shared__ float red[kThreads / 32];
   const int64_t u = blockIdx.x;
   const int sl = blockIdx.y, tid = threadIdx.x;
   const size_t off = u * s.sS() + (size_t)sl * kNS * kDK;
-  const float4* a = reinterpret_cast<const float4*>(s.dSp + off);
-  const float4* b = reinterpret_cast<const float4*>(s.Sst + off);
-  const uint2* bh = reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(s.Sst) + off);
+  auto bf = [&](const float* base) {
+    return reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(base) + off);
+  };
   float part = 0.f;
   for (int e = tid; e < kNS * kDK / 4; e += kThreads) {
-    const float4 x = a[e];
-    float4 y;
-    if (kBfS) {
-      const uint2 w = bh[e];
-      y = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
-                      __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
-    } else {
-      y = b[e];
-    }
+    const float4 x = kBf ? widen_bf16x4(bf(s.dSp)[e])
+                         : reinterpret_cast<const float4*>(s.dSp + off)[e];
+    const float4 y = kBf ? widen_bf16x4(bf(s.Sst)[e])
+                         : reinterpret_cast<const float4*>(s.Sst + off)[e];
     part = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, part))));
   }
 #pragma unroll
@@ -910,7 +910,7 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     for (int i = 0; i < n; ++i) {
       const G& g = list[i];
       const int bt = tiled && (g.B.p == s.Sst || g.B.p == s.dSp) ? dv : 0;
-      const int bbf = tiled && g.B.p == s.Sst ? 1 : 0;   // the states are bf16 there
+      const int bbf = bt ? 1 : 0;   // the states and dS' are bf16 there
       const cudaError_t r = gemm_io(io_dtype, a.status, q, g.tA, g.tB, g.A, g.B, g.C, g.sC, g.ldc,
                                     g.N, g.K, g.alpha, g.Cin, g.beta, g.mask, g.col, kC, units, bt,
                                     bbf);

@@ -312,9 +312,9 @@ struct ConvIn {
 // 4-column tiles: element (v, c) of a unit's [dv][dk] matrix at
 // ((c / 4) * dv + v) * 4 + c % 4.  A warp whose lanes hold consecutive rows
 // then stores contiguous bytes, and a GEMM that reads columns c .. c+3 of
-// consecutive rows reads contiguous memory.  The states are bf16 there (the
-// forward's MMAs read S as bf16 too; dS' stays fp32).  Other dv: row-major
-// fp32.
+// consecutive rows reads contiguous memory.  Both are bf16 there, as the
+// forward's and the reverse pass's own MMAs read S and dS.  Other dv:
+// row-major fp32.
 __host__ __device__ constexpr bool tiled_states(int dv) { return dv == 256; }
 
 struct PrefillLaunch {
@@ -391,8 +391,9 @@ cudaError_t scratch_free(void* p, cudaStream_t stream);
 // The backward's reverse state pass on the tensor cores (bf16 I/O): per
 // (sequence, head, 128-row slice of dS), over the chunks in reverse, from
 // dS_final (nullptr: zero) to dS0 (nullptr: not written); stores every
-// chunk's end-state gradient dS' ([chunks * H] units of dv x dk fp32, in the
-// tiled_states layout at dv = 256) and dU ([chunks * H][64][dv] fp32).  images: the forward's per-chunk operand images over the
+// chunk's end-state gradient dS' ([chunks * H] units of dv x dk: bf16 in the
+// tiled_states layout at dv = 256, fp32 row-major otherwise) and dU
+// ([chunks * H][64][dv] fp32).  images: the forward's per-chunk operand images over the
 // same map; k, dout: the call's bf16 tensors.
 struct ReverseLaunch {
   const void* k = nullptr;

@@ -1756,17 +1756,20 @@ tc_reverse_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         mma_commit(&bar_m1);
       }
     }
-    // dS' of this chunk (fp32), for the chunk gradients.  A warp holds 32
-    // rows.  In the tiled layout (dv = 256) a store of the warp covers 512
-    // contiguous bytes; row-major, each 16-byte piece would be its own L2
-    // transaction, so 16 columns at a time go through a per-warp tile in
-    // shared memory and leave as four rows of 64 contiguous bytes per store.
-    if (tiled_states(dv)) {   // lanes: consecutive rows, 512 contiguous bytes a store
-      float4* p = reinterpret_cast<float4*>(dSp + u * dv * kDK) + (size_t)32 * colhalf * dv +
-                  dsp_row;
+    // dS' of this chunk, for the chunk gradients.  A warp holds 32 rows.  In
+    // the tiled layout (dv = 256) it is stored as bf16, as this pass's own
+    // MMAs read dS, and a store of the warp covers 256 contiguous bytes;
+    // row-major (fp32), each 16-byte piece would be its own L2 transaction, so
+    // 16 columns at a time go through a per-warp tile in shared memory and
+    // leave as four rows of 64 contiguous bytes per store.
+    if (tiled_states(dv)) {   // lanes: consecutive rows
+      uint2* p = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(dSp) +
+                                          u * dv * kDK) +
+                 (size_t)32 * colhalf * dv + dsp_row;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        p[(size_t)j * dv] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+        p[(size_t)j * dv] = make_uint2(pack_bf16(S[4 * j], S[4 * j + 1]),
+                                       pack_bf16(S[4 * j + 2], S[4 * j + 3]));
     } else {
       float* tile = reinterpret_cast<float*>(sm + kR_T + warp * 2560);
       float* row0 = dSp + (u * dv + 128 * slice + 32 * quarter) * kDK + 128 * colhalf;
