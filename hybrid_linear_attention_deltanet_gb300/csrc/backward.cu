@@ -980,14 +980,16 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     f.scratch = extra;
     f.out = nullptr;
     f.S_final = nullptr;
-    f.allow_overlap = true;
+    // the split form: its per-chunk kernel takes every SM briefly, then its
+    // state units hold one SM each and the caller's stream gets the rest (the
+    // fused cooperative form would hold every SM until its workers finish)
+    f.allow_overlap = false;
     f.state_dump = s.Sst;
     // the forward re-run and then the reverse pass on the tensor cores (on
     // the re-run's operand images) go to the high-priority stream; on the
     // caller's stream meanwhile, the per-chunk factors take the SMs the
-    // re-run's per-chunk workers release once done, then (after the re-run)
-    // the products that need no reverse output take those the reverse pass
-    // leaves free
+    // re-run's state units leave, then (after the re-run) the products that
+    // need no reverse output take those the reverse pass leaves free
     ReverseLaunch r;
     r.k = a.k;
     r.dout = dout;
