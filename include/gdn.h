@@ -231,8 +231,10 @@ int gdn_prefill_scan_ws(const void* q, const void* k, const void* v, const float
  * gdn_prefill (bf16 operands, fp32 accumulation and state), the reverse state
  * pass runs on the tensor cores in the same way (bf16 operands, fp32
  * accumulation and state gradient) and the chunk-gradient products as tf32
- * tensor-core GEMMs on fp32 operands (fp32 accumulation); with fp32 I/O
- * everything runs in fp32 on the CUDA cores.
+ * tensor-core GEMMs (fp32 accumulation) on fp32 operands, except the chunk
+ * states and state gradients, which at dv = 256 are kept as the bf16 values
+ * the two state passes' own products use; with fp32 I/O everything runs in
+ * fp32 on the CUDA cores.
  *
  * Scratch: stream-ordered from the library's pool, about 1.6 MiB per
  * (chunk of 64 tokens, head) at dv = 256, plus with bf16 I/O the forward's own
