@@ -35,6 +35,8 @@
 //   local gradients, and a final scatter into the token layout.
 #include <mutex>
 
+#include <functional>
+
 #include "backward.cuh"
 
 namespace gdn {
@@ -156,8 +158,10 @@ gather_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
         if (tid >= o) x += y;
       }
       x += carry;
+      const float b = r < L ? beta[(t0 + r) * H + h] : 0.f;
       s.G[u * kC + r] = x;
-      s.B[u * kC + r] = r < L ? beta[(t0 + r) * H + h] : 0.f;
+      s.B[u * kC + r] = b;
+      s.BG[u * kC + r] = b * expf(x);   // beta_r gamma_r
       carry = __shfl_sync(0xffffffffu, x, 31);
     }
   }
@@ -919,7 +923,13 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     return cudaSuccess;
   };
   // the per-chunk factors: q, k, v, dO tiles, KK^T, QK^T, T, P^, W, U~
-  auto local_factors = [&](cudaStream_t q) -> cudaError_t {
+  // (bf16 I/O) the forward re-run's per-chunk kernel leaves K K^T, Q K^T,
+  // P^, T and its scaled forms in fp32 (PrepSide): the per-chunk factors are
+  // then the gather and, once that kernel is done (wait_prep), the W and U~
+  // products
+  const bool side = io_dtype == GDN_BF16;
+  auto local_factors = [&](cudaStream_t q,
+                           const std::function<cudaError_t()>& wait_prep) -> cudaError_t {
     if (io_dtype == GDN_BF16)
       gather_kernel<__nv_bfloat16><<<gu, kThreads, 0, q>>>(
           (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
@@ -931,14 +941,18 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     count_launches(1);
     cudaError_t r = cudaGetLastError();
     if (r != cudaSuccess) return r;
-    const G f1[] = {
-        {false, true, {s.K, D, kDK}, {s.K, D, kDK}, s.KK, CC, kC, kC, kDK, 1.f, nullptr, 0.f, 0, nullptr},
-        {false, true, {s.Q, D, kDK}, {s.K, D, kDK}, s.QK, CC, kC, kC, kDK, 1.f, nullptr, 0.f, 0, nullptr},
-    };
-    if ((r = run(f1, 2, q)) != cudaSuccess) return r;
-    tprep_kernel<<<(unsigned)units, kThreads, 0, q>>>(s);
-    count_launches(1);
-    if ((r = cudaGetLastError()) != cudaSuccess) return r;
+    if (side) {
+      if ((r = wait_prep()) != cudaSuccess) return r;
+    } else {
+      const G f1[] = {
+          {false, true, {s.K, D, kDK}, {s.K, D, kDK}, s.KK, CC, kC, kC, kDK, 1.f, nullptr, 0.f, 0, nullptr},
+          {false, true, {s.Q, D, kDK}, {s.K, D, kDK}, s.QK, CC, kC, kC, kDK, 1.f, nullptr, 0.f, 0, nullptr},
+      };
+      if ((r = run(f1, 2, q)) != cudaSuccess) return r;
+      tprep_kernel<<<(unsigned)units, kThreads, 0, q>>>(s);
+      count_launches(1);
+      if ((r = cudaGetLastError()) != cudaSuccess) return r;
+    }
     // W = T diag(beta gamma) K, U~ = T diag(beta) V
     const G f2[] = {
         {false, false, {s.TmB, CC, kC}, {s.K, D, kDK}, s.W, D, kDK, kDK, kC, 1.f, nullptr, 0.f, 0, nullptr},
@@ -985,6 +999,9 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     // fused cooperative form would hold every SM until its workers finish)
     f.allow_overlap = false;
     f.state_dump = s.Sst;
+    f.side = PrepSide{s.KK, s.QK, s.Ph, s.Tm, s.TmB, s.TmU};
+    PrefillLaunch f_state = f;   // the re-run's state pass, after its per-chunk kernel
+    f_state.state_only = true;
     // the forward re-run and then the reverse pass on the tensor cores (on
     // the re-run's operand images) go to the high-priority stream; on the
     // caller's stream meanwhile, the per-chunk factors take the SMs the
@@ -1004,8 +1021,9 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     r.dU = s.dU;
     r.status = a.status;
     cudaStream_t rs = units > 0 ? reverse_stream() : nullptr;
-    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};   // inputs ready, re-run done, reverse done
-    for (int i = 0; rs && i < 3; ++i) {
+    // inputs ready, re-run's per-chunk kernel done, re-run done, reverse done
+    cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+    for (int i = 0; rs && i < 4; ++i) {
       if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
         for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
         rs = nullptr;
@@ -1016,22 +1034,25 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
       if ((e = launch_prefill_tc(f, st)) != cudaSuccess) return e;
       if ((e = launch_reverse_tc(r, st)) != cudaSuccess) return e;
       if (units == 0) return cudaSuccess;
-      if ((e = local_factors(st)) != cudaSuccess) return e;
+      if ((e = local_factors(st, [] { return cudaSuccess; })) != cudaSuccess) return e;
       if ((e = run(pre, kPre, st)) != cudaSuccess) return e;
     } else {
       e = cudaEventRecord(ev[0], st);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(rs, ev[0], 0);
-      if (e == cudaSuccess) e = launch_prefill_tc(f, rs);
+      if (e == cudaSuccess) e = launch_prefill_tc(f, rs, /*prep_only=*/true);
       if (e == cudaSuccess) e = cudaEventRecord(ev[1], rs);
-      if (e == cudaSuccess) e = launch_reverse_tc(r, rs);
+      if (e == cudaSuccess) e = launch_prefill_tc(f_state, rs);
       if (e == cudaSuccess) e = cudaEventRecord(ev[2], rs);
-      if (e == cudaSuccess) e = local_factors(st);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[1], 0);
+      if (e == cudaSuccess) e = launch_reverse_tc(r, rs);
+      if (e == cudaSuccess) e = cudaEventRecord(ev[3], rs);
+      if (e == cudaSuccess)
+        e = local_factors(st, [&] { return cudaStreamWaitEvent(st, ev[1], 0); });
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[2], 0);
       if (e == cudaSuccess) e = run(pre, kPre, st);
       // join (also on an error above, so that nothing of this call is left
       // running on the internal stream unordered with the caller's)
-      const cudaError_t ew = cudaStreamWaitEvent(st, ev[2], 0);
-      for (int i = 0; i < 3; ++i) cudaEventDestroy(ev[i]);
+      const cudaError_t ew = cudaStreamWaitEvent(st, ev[3], 0);
+      for (int i = 0; i < 4; ++i) cudaEventDestroy(ev[i]);
       if (e == cudaSuccess) e = ew;
       if (e != cudaSuccess) return e;
     }
@@ -1043,7 +1064,7 @@ cudaError_t launch_prefill_backward(const PrefillLaunch& a, const void* dout,
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   } else {
-    if (units > 0 && (e = local_factors(st)) != cudaSuccess) return e;
+    if (units > 0 && (e = local_factors(st, [] { return cudaSuccess; })) != cudaSuccess) return e;
     fwd_states_kernel<<<gs, kThreads, kFwdSmem, st>>>(a.S0, a.map, a.H, s);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -317,6 +317,20 @@ struct ConvIn {
 // row-major fp32.
 __host__ __device__ constexpr bool tiled_states(int dv) { return dv == 256; }
 
+// (the backward's forward re-run, split form) fp32 copies of per-chunk
+// factors the tensor-core prep computes anyway, each [chunks * H][64][64]
+// row-major with rows and columns past the chunk's valid rows zero: the raw
+// Gram matrices K K^T and Q K^T, P^ = lower(Gam o Q K^T) / sqrt(dk),
+// T = (I + A)^-1, T diag(beta gamma) and T diag(beta).  All null: none.
+struct PrepSide {
+  float* KK = nullptr;
+  float* QK = nullptr;
+  float* Ph = nullptr;
+  float* Tm = nullptr;
+  float* TmB = nullptr;
+  float* TmU = nullptr;
+};
+
 struct PrefillLaunch {
   const void* q; const void* k; const void* v;
   const float* alpha; const float* beta; const float* S0;
@@ -337,6 +351,7 @@ struct PrefillLaunch {
   SegRoute route;       // see SegRoute (pass != 0 forces the split form)
   NormGate ng;          // tensor-core path: see NormGate (forces the split form)
   ConvIn cv;            // tensor-core path: see ConvIn (q, k, v, alpha, beta unused)
+  PrepSide side;        // tensor-core path, split form only: see PrepSide
 };
 
 cudaError_t launch_chunk_offsets(const int32_t* cu_seqlens, int32_t N, int64_t T_total,

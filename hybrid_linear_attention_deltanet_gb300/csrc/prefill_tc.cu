@@ -182,7 +182,8 @@ __device__ __forceinline__ bool prep_item(const SeqMap& map, int32_t H, int64_t 
 // The prep over items worker, worker + n_workers, ... < n_items.
 // kFused: two K/Q buffers (the next item's tiles load during this one),
 // items in chunk-position order, and a ready flag per finished item.
-template <bool kFused>
+// kSide: also the PrepSide copies (split form).
+template <bool kFused, bool kSide = false>
 __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
                                           const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                           const float* __restrict__ alpha,
@@ -191,7 +192,8 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
                                           uint32_t* ready, unsigned* status, int32_t dv,
                                           const ConvIn& cv, uint64_t* __restrict__ trace,
                                           uint64_t* __restrict__ timeline, int64_t n_items,
-                                          int64_t worker, int64_t n_workers) {
+                                          int64_t worker, int64_t n_workers,
+                                          const PrepSide& side = PrepSide{}) {
   constexpr int kBufs = kFused ? 2 : 1;
   using Lay = PrepSmem<kFused>;
   float* sA = (float*)(sm + Lay::A);
@@ -540,6 +542,20 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
       tmem_ld32(tmem + lane_off + 32 * hv, g);
       tmem_ld_wait();
       const int row = 32 * quarter + lane;
+      if (kSide) {   // the raw Gram rows (K K^T, then Q K^T), zero past the valid rows
+        const int r = row & (kC - 1);
+        float* dst = (row < kC ? side.KK : side.QK) + ((size_t)(cur.ci * H + cur.h) * kC + r) * kC +
+                     32 * hv;
+#pragma unroll
+        for (int j4 = 0; j4 < 32; j4 += 4) {
+          float4 o;
+          o.x = (r < L && 32 * hv + j4 < L) ? __uint_as_float(g[j4]) : 0.f;
+          o.y = (r < L && 32 * hv + j4 + 1 < L) ? __uint_as_float(g[j4 + 1]) : 0.f;
+          o.z = (r < L && 32 * hv + j4 + 2 < L) ? __uint_as_float(g[j4 + 2]) : 0.f;
+          o.w = (r < L && 32 * hv + j4 + 3 < L) ? __uint_as_float(g[j4 + 3]) : 0.f;
+          *reinterpret_cast<float4*>(dst + j4) = o;
+        }
+      }
       if (row < kC) {   // A = strict_lower(beta_r Gam_rj k_r.k_j), columns 32hv .. 32hv+31
         const float Gr = sG[row], br = sB[row];
 #pragma unroll
@@ -559,6 +575,9 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
             const float p0 = (j0 <= r && r < L) ? kScale * exp_fast(Gr - sG[j0]) * __uint_as_float(g[8 * cq + 2 * e]) : 0.f;
             const float p1 = (j1 <= r && r < L) ? kScale * exp_fast(Gr - sG[j1]) * __uint_as_float(g[8 * cq + 2 * e + 1]) : 0.f;
             w[e] = pack_bf16(p0, p1);
+            if (kSide)
+              *reinterpret_cast<float2*>(side.Ph + ((size_t)(cur.ci * H + cur.h) * kC + r) * kC + j0) =
+                  make_float2(p0, p1);
           }
           uint8_t* pdst = kFused ? sm + Lay::PS : img + kImgP;
           *reinterpret_cast<uint4*>(pdst + sw_chunk(r, 4 * hv + cq)) =
@@ -692,6 +711,13 @@ __device__ __forceinline__ void prep_role(uint8_t* sm, const CUtensorMap* tm_q,
           const float b0 = sB[j0], b1 = sB[j1];
           ww[e] = pack_bf16(t0v * b0 * sGam[j0], t1v * b1 * sGam[j1]);
           uu[e] = pack_bf16(t0v * b0, t1v * b1);
+          if (kSide) {   // T, T diag(beta gamma), T diag(beta) in fp32
+            const size_t o = ((size_t)(cur.ci * H + cur.h) * kC + r) * kC + j0;
+            *reinterpret_cast<float2*>(side.Tm + o) = make_float2(t0v, t1v);
+            *reinterpret_cast<float2*>(side.TmB + o) =
+                make_float2(t0v * b0 * sGam[j0], t1v * b1 * sGam[j1]);
+            *reinterpret_cast<float2*>(side.TmU + o) = make_float2(t0v * b0, t1v * b1);
+          }
         }
         *reinterpret_cast<uint4*>(sm + Lay::TW + sw_chunk(r, ch)) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
         *reinterpret_cast<uint4*>(sm + Lay::TU + sw_chunk(r, ch)) = make_uint4(uu[0], uu[1], uu[2], uu[3]);
@@ -1428,16 +1454,19 @@ __device__ __forceinline__ void state_role(uint8_t* sm, const CUtensorMap* tm_k,
 // ================================================================ kernels
 // split form, kernel 1: items j = blockIdx.x + k * gridDim.x < n_items,
 // (chunk j / H, head j % H); two CTAs per SM
+// (kSide: also the PrepSide copies)
+template <bool kSide>
 __global__ void __launch_bounds__(kPrepThreads, 2)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ alpha,
                const float* __restrict__ beta, SeqMap map, int32_t H,
                uint8_t* __restrict__ scratch, unsigned* status, uint64_t* __restrict__ trace,
-               int64_t n_items, int32_t dv, ConvIn cv) {
+               int64_t n_items, int32_t dv, ConvIn cv, PrepSide side) {
   extern __shared__ uint8_t smem_raw[];
-  prep_role<false>(align_smem_1024(smem_raw), &tm_q, &tm_k, &tm_v, alpha, beta, map, H, scratch,
-                   nullptr, status, dv, cv, trace ? trace + kPrepTraceOffset : nullptr, trace,
-                   n_items, blockIdx.x, gridDim.x);
+  prep_role<false, kSide>(align_smem_1024(smem_raw), &tm_q, &tm_k, &tm_v, alpha, beta, map, H,
+                          scratch, nullptr, status, dv, cv,
+                          trace ? trace + kPrepTraceOffset : nullptr, trace, n_items, blockIdx.x,
+                          gridDim.x, side);
 }
 
 // split form, kernel 2: one CTA per unit (blockIdx = sequence, head, 128-row
@@ -1968,7 +1997,9 @@ DeviceFacts* device_facts() {
     int coop = 0, per_sm = 0, per_sm_norm = 0;
     if (cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(tc_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kPrepSmemSplit) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kPrepSmemSplit) != cudaSuccess ||
         cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kStateSmem) != cudaSuccess ||
@@ -2064,8 +2095,14 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream, bool 
   if (items > 0 && !a.state_only) {
     const int64_t slots = 2 * (int64_t)f->sms;
     const unsigned grid = (unsigned)(items < slots ? items : slots);
-    tc_prep_kernel<<<grid, kPrepThreads, kPrepSmemSplit, stream>>>(
-        tq, tk, tv, a.alpha, a.beta, a.map, a.H, scr, a.status, g_trace, items, dv, a.cv);
+    if (a.side.KK)
+      tc_prep_kernel<true><<<grid, kPrepThreads, kPrepSmemSplit, stream>>>(
+          tq, tk, tv, a.alpha, a.beta, a.map, a.H, scr, a.status, g_trace, items, dv, a.cv,
+          a.side);
+    else
+      tc_prep_kernel<false><<<grid, kPrepThreads, kPrepSmemSplit, stream>>>(
+          tq, tk, tv, a.alpha, a.beta, a.map, a.H, scr, a.status, g_trace, items, dv, a.cv,
+          a.side);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
