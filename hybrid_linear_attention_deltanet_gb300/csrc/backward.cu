@@ -1,4 +1,5 @@
-// Backward pass of the chunked gated delta rule on the CUDA cores (fp32).
+// Backward pass of the chunked gated delta rule: fp32 I/O on the CUDA cores,
+// bf16 I/O on the tensor cores (see "bf16 I/O" below).
 //
 // The training kernel of "Long-Context Aware Upcycling" (Appendix A.3, last
 // paragraph) splits sequences into chunks of C = 64 tokens, batches the delta
@@ -19,20 +20,26 @@
 // Bu = diag(beta) V), T (dA = -T^T dT T^T, strictly lower), A, Ph, Qh and the
 // decays down to log alpha (a reverse cumulative sum inside the chunk).
 //
-// Structure (every intermediate per (chunk, head) unit in fp32 scratch):
+// Structure (every intermediate per (chunk, head) unit in scratch):
 //   gather      q, k, v, dO of each chunk -> zero-padded 64-row fp32 tiles;
-//               G (padding rows add log alpha = 0) and beta (0 on padding).
-//               Padding rows then contribute exactly nothing anywhere.
+//               G (padding rows add log alpha = 0), beta (0 on padding) and
+//               beta gamma.  Padding rows then contribute nothing anywhere.
 //   prep        KK^T, QK^T (batched GEMM), T by forward substitution, Ph,
 //               W and U~ (batched GEMM).
 //   fwd_states  per (sequence, head, 16-row slice of S): the forward state
-//               pass, storing every chunk's start state (fp32 I/O; with bf16
-//               I/O the tensor-core forward of gdn_prefill stores them).
+//               pass, storing every chunk's start state.
 //   rev_states  per (sequence, head, 16-row slice): the reverse pass over
 //               chunks for dS; stores dS' and dU per chunk, dS0 at the end.
 //               Rows of dS are independent exactly as rows of S are.
 //   then batched 64-row GEMMs and three per-chunk elementwise kernels for the
 //   local gradients, and a final scatter into the token layout.
+// bf16 I/O: the tensor-core forward of gdn_prefill re-runs (split form, no
+// outputs), storing every chunk's start state as bf16 tiles and leaving
+// KK^T, QK^T, Ph and T in fp32 from its per-chunk kernel; the tensor-core
+// reverse pass stores dS' (bf16 tiles) and dU; the GEMMs run as tf32
+// tcgen05 products (tgemm.cu); the re-run and the reverse pass go to an
+// internal high-priority stream while the caller's stream runs the gather,
+// W and U~ and the products that need no reverse output.
 #include <mutex>
 
 #include <functional>
